@@ -1,0 +1,199 @@
+"""fp64 CPU oracle for ManifoldKV-style KV-cache compression (test
+infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline and
+reference legs may import this package. The CUDA library never does: it must
+fail loudly instead of falling back to anything here. The arithmetic lives in
+``mkv_oracle.c`` (plain C, fp64, token-order sums); this module compiles it
+with gcc and marshals numpy arrays into it.
+
+Parity pins: every function here is pinned by the ``-m "not gpu"`` tests in
+``tests/test_oracle_pins.py`` (hand-computed cases, closed forms, invariants,
+library routines and brute force on tiny inputs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mkv_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libmkv_oracle.so")
+
+MODE_L2 = 0
+MODE_COSINE = 1
+_MODES = {"l2": MODE_L2, "cosine": MODE_COSINE, MODE_L2: MODE_L2, MODE_COSINE: MODE_COSINE}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared library with gcc; return its path.
+
+    -ffp-contract=off keeps every multiply and add separately rounded (no
+    fused multiply-add), so the fp64 arithmetic is exactly what the source
+    says on x86 and on Arm alike."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, f64, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+        lib.oracle_bf16_to_double.restype = f64
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_num_keep.restype = i64
+        lib.oracle_num_keep.argtypes = [i64, f64]
+        lib.oracle_window_len.restype = i64
+        lib.oracle_window_len.argtypes = [i64, i64]
+        lib.oracle_num_windows.restype = i64
+        lib.oracle_num_windows.argtypes = [i64, i64]
+        lib.oracle_centroids.restype = None
+        lib.oracle_centroids.argtypes = [vp, i64, i64, i64, vp]
+        lib.oracle_scores.restype = None
+        lib.oracle_scores.argtypes = [vp, i64, i64, i64, i32, vp, vp]
+        lib.oracle_select.restype = i32
+        lib.oracle_select.argtypes = [vp, i64, i64, vp]
+        lib.oracle_gather.restype = None
+        lib.oracle_gather.argtypes = [vp, i64, vp, i64, vp]
+        lib.oracle_compress_head.restype = i64
+        lib.oracle_compress_head.argtypes = [vp, vp, i64, i64, f64, i32, i64, vp, vp, vp, vp, vp]
+        lib.oracle_compress_heads.restype = i32
+        lib.oracle_compress_heads.argtypes = [vp, vp, i64, i64, i64, vp, f64, i32, i64, i64,
+                                              vp, vp, vp, vp]
+        _lib = lib
+        return lib
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 data as a C-contiguous uint16 array of raw bit patterns.
+
+    Accepts a numpy uint16/int16 array or a torch bfloat16 tensor (on the CPU)."""
+    if hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16":
+        import torch
+        x = x.detach().cpu().contiguous().view(torch.int16).numpy()
+    a = np.ascontiguousarray(x)
+    if a.dtype == np.int16:
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected bf16 bits as uint16, got {a.dtype}")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().oracle_bf16_to_double(int(bits) & 0xFFFF)
+
+
+def num_keep(T: int, ratio: float) -> int:
+    """Tokens kept out of T at compression ``ratio`` (the share removed)."""
+    return int(_load().oracle_num_keep(int(T), float(ratio)))
+
+
+def window_len(T: int, window: int) -> int:
+    return int(_load().oracle_window_len(int(T), int(window)))
+
+
+def num_windows(T: int, window: int) -> int:
+    return int(_load().oracle_num_windows(int(T), int(window)))
+
+
+def centroids(K, window: int = 0) -> np.ndarray:
+    """Per-window mean keys of one head: K [T, d] bf16 -> float64 [n_windows, d]."""
+    k = _bits(K)
+    T, d = k.shape
+    C = np.zeros((max(num_windows(T, window), 0), d), dtype=np.float64)
+    _load().oracle_centroids(_ptr(k), T, d, int(window), _ptr(C))
+    return C
+
+
+def scores(K, C: np.ndarray, window: int = 0, mode="l2") -> np.ndarray:
+    """Per-token scores of one head against the centroids C: float64 [T]."""
+    k = _bits(K)
+    T, d = k.shape
+    c = np.ascontiguousarray(C, dtype=np.float64)
+    if c.shape != (num_windows(T, window), d):
+        raise ValueError(f"centroid shape {c.shape} does not match T={T}, window={window}")
+    S = np.zeros(T, dtype=np.float64)
+    _load().oracle_scores(_ptr(k), T, d, int(window), _MODES[mode], _ptr(c), _ptr(S))
+    return S
+
+
+def select(S, n_keep: int) -> np.ndarray:
+    """Indices (ascending, int32) of the n_keep highest scores; ties at the
+    cut go to the lower index."""
+    s = np.ascontiguousarray(S, dtype=np.float64)
+    idx = np.zeros(max(int(n_keep), 0), dtype=np.int32)
+    if _load().oracle_select(_ptr(s), s.shape[0], int(n_keep), _ptr(idx)) != 0:
+        raise ValueError("oracle_select: bad n_keep or NaN score")
+    return idx
+
+
+def gather(X, idx) -> np.ndarray:
+    """Rows X[idx] of a bf16 [T, d] array, as uint16 bits [len(idx), d]."""
+    x = _bits(X)
+    i = np.ascontiguousarray(idx, dtype=np.int32)
+    out = np.zeros((i.shape[0], x.shape[1]), dtype=np.uint16)
+    _load().oracle_gather(_ptr(x), x.shape[1], _ptr(i), i.shape[0], _ptr(out))
+    return out
+
+
+def compress_head(K, V, ratio: float, mode="l2", window: int = 0):
+    """All steps for one head. Returns dict(C, S, idx, K_out, V_out)."""
+    k, v = _bits(K), _bits(V)
+    T, d = k.shape
+    C = np.zeros((max(num_windows(T, window), 1), d), dtype=np.float64)
+    S = np.zeros(max(T, 1), dtype=np.float64)
+    n = num_keep(T, ratio)
+    idx = np.zeros(max(n, 1), dtype=np.int32)
+    ko = np.zeros((max(n, 1), d), dtype=np.uint16)
+    vo = np.zeros((max(n, 1), d), dtype=np.uint16)
+    got = _load().oracle_compress_head(_ptr(k), _ptr(v), T, d, float(ratio), _MODES[mode], int(window),
+                                       _ptr(C), _ptr(S), _ptr(idx), _ptr(ko), _ptr(vo))
+    if got != n:
+        raise ValueError("oracle_compress_head failed")
+    return {"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}
+
+
+def compress_heads(K, V, lens, ratio: float, mode="l2", window: int = 0, keep_stride=None):
+    """All steps for a [n_heads, t_stride, d] cache with per-head lengths.
+
+    Returns (idx int32 [n, keep_stride], kept int32 [n], K_out, V_out uint16
+    [n, keep_stride, d]); entries past a head's kept count are zero."""
+    k, v = _bits(K), _bits(V)
+    n_heads, t_stride, d = k.shape
+    ln = np.ascontiguousarray(lens, dtype=np.int32).reshape(-1)
+    if ln.shape[0] != n_heads:
+        raise ValueError("one length per head is required")
+    if keep_stride is None:
+        keep_stride = num_keep(t_stride, ratio)
+    idx = np.zeros((n_heads, max(keep_stride, 1)), dtype=np.int32)
+    kept = np.zeros(n_heads, dtype=np.int32)
+    ko = np.zeros((n_heads, max(keep_stride, 1), d), dtype=np.uint16)
+    vo = np.zeros_like(ko)
+    rc = _load().oracle_compress_heads(_ptr(k), _ptr(v), n_heads, t_stride, d, _ptr(ln), float(ratio),
+                                       _MODES[mode], int(window), int(max(keep_stride, 1)),
+                                       _ptr(idx), _ptr(kept), _ptr(ko), _ptr(vo))
+    if rc != 0:
+        raise ValueError("oracle_compress_heads failed")
+    return idx[:, :keep_stride], kept, ko[:, :keep_stride], vo[:, :keep_stride]

@@ -1,0 +1,217 @@
+/*
+ * mkv_oracle.c -- the fp64 CPU oracle for ManifoldKV-style KV-cache
+ * compression.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the slow, plain reference that the
+ * CUDA library is checked against. Only the test suite, the smoke check and
+ * the bench's CPU-baseline / reference leg may load it; the library never
+ * does, and it shares no code, header, table or helper with the library.
+ *
+ * What it computes (per head = one (layer, sequence, KV head) triple), from
+ * "ManifoldKV: Training-Free KV Cache Compression via Euclidean Outlier
+ * Detection" (ICML 2026 poster 62526), abstract and lay summary:
+ *   1. the key centroid -- the mean key of the head; the windowed variant
+ *      (WindowedManifoldKV, abstract) uses one mean per non-overlapping
+ *      window of W tokens instead of one global mean;
+ *   2. a score per token: its Euclidean distance to its centroid (the
+ *      ManifoldKV scorer, abstract), or, as the switchable baseline, one
+ *      minus its cosine similarity to the centroid (the KeyDiff-style scorer
+ *      the abstract compares against);
+ *   3. the tokens that sit farthest from the centroid are the ones retained
+ *      (lay summary): keep the n_keep highest scores, where the compression
+ *      percentage is the fraction of tokens removed (abstract: "20%
+ *      compression" at 95.7% accuracy);
+ *   4. the kept key and value rows, in ascending token order, form the
+ *      compacted cache.
+ * Readings where the pages are silent (each one is also listed in the design
+ * notes): ties at the cut go to the lower token index; n_keep =
+ * floor(T*(1-ratio) + 0.5) clamped to [0, T]; the last window holds the
+ * remaining T mod W tokens; a cosine score with a zero key or zero centroid
+ * is 1; the selection is one global top-n_keep per head even when the
+ * centroids are per window.
+ *
+ * Everything is fp64, summed in token order, with no blocking or reordering.
+ * Keys arrive as raw bfloat16 bit patterns (uint16); decoding them to double
+ * is exact. Compile with -ffp-contract=off so every operation rounds once.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_MODE_L2 0
+#define ORACLE_MODE_COSINE 1
+
+/* bfloat16 is the upper half of an IEEE binary32: shifting the 16 bits into
+ * the top of a 32-bit word gives the float exactly; float -> double is exact. */
+double oracle_bf16_to_double(uint16_t bits)
+{
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* Step 3, reading of "% compression": the percentage is the share removed,
+ * so round(T * (1 - ratio)) tokens stay; halves round up. */
+int64_t oracle_num_keep(int64_t T, double ratio)
+{
+    if (T <= 0) return 0;
+    double keep = floor((double)T * (1.0 - ratio) + 0.5);
+    if (keep < 0.0) return 0;
+    if (keep > (double)T) return T;
+    return (int64_t)keep;
+}
+
+/* Window tiling of step 1: window <= 0 or window >= T means one global
+ * window; otherwise non-overlapping windows [jW, min((j+1)W, T)). */
+int64_t oracle_window_len(int64_t T, int64_t window)
+{
+    if (window <= 0 || window >= T) return T;
+    return window;
+}
+
+int64_t oracle_num_windows(int64_t T, int64_t window)
+{
+    if (T <= 0) return 0;
+    int64_t w = oracle_window_len(T, window);
+    return (T + w - 1) / w;
+}
+
+/* Step 1: C[j][i] = (1/|w_j|) * sum_{t in w_j} K[t][i], summed in token order.
+ * K: T x d bf16 bits, row-major. C: num_windows x d doubles. */
+void oracle_centroids(const uint16_t *K, int64_t T, int64_t d, int64_t window, double *C)
+{
+    int64_t wl = oracle_window_len(T, window);
+    int64_t nw = oracle_num_windows(T, window);
+    for (int64_t j = 0; j < nw; ++j) {
+        int64_t a = j * wl;
+        int64_t b = a + wl < T ? a + wl : T;
+        for (int64_t i = 0; i < d; ++i) {
+            double sum = 0.0;
+            for (int64_t t = a; t < b; ++t) sum += oracle_bf16_to_double(K[t * d + i]);
+            C[j * d + i] = sum / (double)(b - a);
+        }
+    }
+}
+
+/* Step 2: each token is scored against the centroid of its own window.
+ *   L2:     s_t = sqrt( sum_i (k_ti - c_i)^2 )
+ *   cosine: s_t = 1 - (k_t . c) / (|k_t| |c|), and 1 when |k_t| |c| = 0. */
+void oracle_scores(const uint16_t *K, int64_t T, int64_t d, int64_t window, int mode,
+                   const double *C, double *S)
+{
+    int64_t wl = oracle_window_len(T, window);
+    for (int64_t t = 0; t < T; ++t) {
+        const double *c = C + (t / wl) * d;
+        if (mode == ORACLE_MODE_L2) {
+            double ss = 0.0;
+            for (int64_t i = 0; i < d; ++i) {
+                double diff = oracle_bf16_to_double(K[t * d + i]) - c[i];
+                ss += diff * diff;
+            }
+            S[t] = sqrt(ss);
+        } else {
+            double dot = 0.0, kk = 0.0, cc = 0.0;
+            for (int64_t i = 0; i < d; ++i) {
+                double k = oracle_bf16_to_double(K[t * d + i]);
+                dot += k * c[i];
+                kk += k * k;
+                cc += c[i] * c[i];
+            }
+            double denom = sqrt(kk) * sqrt(cc);
+            S[t] = denom == 0.0 ? 1.0 : 1.0 - dot / denom;
+        }
+    }
+}
+
+typedef struct {
+    double score;
+    int64_t token;
+} oracle_ranked;
+
+/* Order by score descending, then token index ascending (ties at the cut go
+ * to the lower index). The order is total, so qsort's instability is moot. */
+static int oracle_rank_cmp(const void *pa, const void *pb)
+{
+    const oracle_ranked *a = (const oracle_ranked *)pa, *b = (const oracle_ranked *)pb;
+    if (a->score > b->score) return -1;
+    if (a->score < b->score) return 1;
+    return (a->token > b->token) - (a->token < b->token);
+}
+
+static int oracle_index_cmp(const void *pa, const void *pb)
+{
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a > b) - (a < b);
+}
+
+/* Step 3: full sort of (score desc, index asc); the first n_keep tokens are
+ * retained; their indices are emitted in ascending order (step 4's order).
+ * Returns 0, or -1 if a score is NaN or memory runs out. */
+int oracle_select(const double *S, int64_t T, int64_t n_keep, int32_t *idx)
+{
+    if (n_keep < 0 || n_keep > T) return -1;
+    oracle_ranked *r = (oracle_ranked *)malloc((size_t)(T > 0 ? T : 1) * sizeof *r);
+    if (!r) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        if (isnan(S[t])) { free(r); return -1; }
+        r[t].score = S[t];
+        r[t].token = t;
+    }
+    qsort(r, (size_t)T, sizeof *r, oracle_rank_cmp);
+    for (int64_t j = 0; j < n_keep; ++j) idx[j] = (int32_t)r[j].token;
+    free(r);
+    qsort(idx, (size_t)n_keep, sizeof *idx, oracle_index_cmp);
+    return 0;
+}
+
+/* Step 4: out[j] = X[idx[j]], whole rows of d bf16 values, bit for bit. */
+void oracle_gather(const uint16_t *X, int64_t d, const int32_t *idx, int64_t n, uint16_t *out)
+{
+    for (int64_t j = 0; j < n; ++j)
+        memcpy(out + j * d, X + (int64_t)idx[j] * d, (size_t)d * sizeof *X);
+}
+
+/* Steps 1-4 for one head. C (num_windows x d) and S (T) are caller scratch;
+ * idx, K_out, V_out receive n_keep entries / rows. Returns n_keep or -1. */
+int64_t oracle_compress_head(const uint16_t *K, const uint16_t *V, int64_t T, int64_t d,
+                             double ratio, int mode, int64_t window,
+                             double *C, double *S, int32_t *idx, uint16_t *K_out, uint16_t *V_out)
+{
+    int64_t n_keep = oracle_num_keep(T, ratio);
+    oracle_centroids(K, T, d, window, C);
+    oracle_scores(K, T, d, window, mode, C, S);
+    if (oracle_select(S, T, n_keep, idx) != 0) return -1;
+    if (K_out) oracle_gather(K, d, idx, n_keep, K_out);
+    if (V_out) oracle_gather(V, d, idx, n_keep, V_out);
+    return n_keep;
+}
+
+/* The same for n_heads heads laid out back to back with row stride t_stride
+ * (a [heads, t_stride, d] cache); head h has lens[h] tokens. Outputs use row
+ * stride keep_stride per head. The plain loop over heads is what the bench's
+ * CPU baseline times. Returns 0, or -1 on the first failing head. */
+int oracle_compress_heads(const uint16_t *K, const uint16_t *V, int64_t n_heads, int64_t t_stride,
+                          int64_t d, const int32_t *lens, double ratio, int mode, int64_t window,
+                          int64_t keep_stride, int32_t *idx, int32_t *kept,
+                          uint16_t *K_out, uint16_t *V_out)
+{
+    double *C = (double *)malloc((size_t)(t_stride > 0 ? t_stride : 1) * (size_t)d * sizeof(double));
+    double *S = (double *)malloc((size_t)(t_stride > 0 ? t_stride : 1) * sizeof(double));
+    if (!C || !S) { free(C); free(S); return -1; }
+    int rc = 0;
+    for (int64_t h = 0; h < n_heads && rc == 0; ++h) {
+        int64_t T = lens[h];
+        if (T < 0 || T > t_stride || oracle_num_keep(T, ratio) > keep_stride) { rc = -1; break; }
+        int64_t n = oracle_compress_head(K + h * t_stride * d, V + h * t_stride * d, T, d, ratio,
+                                         mode, window, C, S, idx + h * keep_stride,
+                                         K_out ? K_out + h * keep_stride * d : NULL,
+                                         V_out ? V_out + h * keep_stride * d : NULL);
+        if (n < 0) rc = -1;
+        else kept[h] = (int32_t)n;
+    }
+    free(C);
+    free(S);
+    return rc;
+}

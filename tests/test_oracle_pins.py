@@ -1,0 +1,297 @@
+"""Pins of the fp64 oracle to things other than itself.
+
+Each test ties one oracle function to a hand-worked case, a closed form, an
+invariant of the definitions, a library routine computing the same quantity a
+different way, or brute force on tiny inputs. Together they are chosen so
+that a plausible slip anywhere in the oracle (a dropped term, a wrong sign,
+divisor or window index, an inverted ranking or tie rule, a transposed
+operand, a wrong rounding of the kept count) fails at least one of them.
+
+Definitions followed: "ManifoldKV: Training-Free KV Cache Compression via
+Euclidean Outlier Detection" (ICML 2026 poster 62526), abstract and lay
+summary.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.spatial.distance import cdist
+
+import oracle
+import synthkv
+
+
+def _golden(golden_dir):
+    with open(os.path.join(golden_dir, "hand_cases.json")) as f:
+        return json.load(f)
+
+
+def _bf16(x):
+    return torch.tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _f64(K):
+    return K.to(torch.float64).numpy()
+
+
+# --- decoding ------------------------------------------------------------------
+
+def test_bf16_decode_matches_torch_for_every_finite_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    lib = oracle._load()
+    got = np.array([lib.oracle_bf16_to_double(int(b)) for b in bits])
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+
+
+# --- kept count ----------------------------------------------------------------
+
+def test_num_keep_table(golden_dir):
+    for T, r, want, _why in _golden(golden_dir)["num_keep"]:
+        assert oracle.num_keep(T, r) == want, (T, r)
+
+
+def test_num_keep_is_nearest_integer_and_clamped():
+    rng = np.random.default_rng(1)
+    for _ in range(2000):
+        T = int(rng.integers(0, 200000))
+        r = float(rng.random())
+        x = T * (1.0 - r)
+        k = oracle.num_keep(T, r)
+        assert 0 <= k <= T
+        assert abs(k - x) <= 0.5 + 1e-9
+
+
+# --- hand-worked cases ----------------------------------------------------------
+
+@pytest.mark.parametrize("case_ix", range(5))
+def test_hand_cases(golden_dir, case_ix):
+    case = _golden(golden_dir)["cases"][case_ix]
+    K = _bf16(case["keys"])
+    w, mode = case["window"], case["mode"]
+    C = oracle.centroids(K, w)
+    np.testing.assert_array_equal(C, np.array(case["centroids"], dtype=np.float64))
+    S = oracle.scores(K, C, w, mode)
+    if "scores_squared" in case:
+        np.testing.assert_allclose(S ** 2, case["scores_squared"], rtol=1e-14, atol=0)
+    else:
+        want = [eval(e, {"sqrt": math.sqrt}) for e in case["scores_closed_form"]]
+        np.testing.assert_allclose(S, want, rtol=0, atol=1e-14)
+    for r, idx in case["keep"].items():
+        n = oracle.num_keep(len(case["keys"]), float(r))
+        assert n == len(idx)
+        assert oracle.select(S, n).tolist() == idx, (case["name"], r)
+        full = oracle.compress_head(K, K, float(r), mode, w)
+        assert full["idx"].tolist() == idx
+
+
+# --- centroid -----------------------------------------------------------------
+
+@pytest.mark.parametrize("T,window", [(1000, 0), (1000, 1000), (1000, 128), (1001, 100), (37, 5), (64, 1)])
+def test_centroid_equals_library_mean(T, window):
+    rng = np.random.default_rng(T + window)
+    K = _bf16(rng.normal(size=(T, 64)) * 3 + 0.5)
+    C = oracle.centroids(K, window)
+    k = _f64(K)
+    wl = T if window <= 0 or window >= T else window
+    want = np.stack([k[a:a + wl].mean(axis=0) for a in range(0, T, wl)])
+    assert C.shape == want.shape
+    np.testing.assert_allclose(C, want, rtol=1e-13, atol=1e-13)
+
+
+def test_centroid_closed_form_sum_of_squares():
+    # I9: sum_t |k_t - c|^2 = sum_t |k_t|^2 - T |c|^2, and c minimises it.
+    rng = np.random.default_rng(7)
+    K = _bf16(rng.normal(size=(4096, 128)) * np.exp(0.5 * rng.normal(size=(4096, 1))))
+    C = oracle.centroids(K, 0)
+    S = oracle.scores(K, C, 0, "l2")
+    k = _f64(K)
+    lhs = np.sum(S ** 2)
+    rhs = np.sum(k * k) - k.shape[0] * np.sum(C[0] ** 2)
+    assert abs(lhs - rhs) <= 1e-12 * abs(rhs)
+    for _ in range(4):
+        c2 = C + rng.normal(size=C.shape) * 1e-3
+        assert np.sum(oracle.scores(K, c2, 0, "l2") ** 2) > lhs
+
+
+# --- scores -------------------------------------------------------------------
+
+@pytest.mark.parametrize("window", [0, 256, 100])
+def test_l2_scores_equal_library_distance(window):
+    rng = np.random.default_rng(3)
+    K = _bf16(rng.normal(size=(1000, 128)) * 2 - 1)
+    C = oracle.centroids(K, window)
+    S = oracle.scores(K, C, window, "l2")
+    k = _f64(K)
+    wl = oracle.window_len(1000, window)
+    want = np.array([cdist(k[t:t + 1], C[t // wl][None], "euclidean")[0, 0] for t in range(1000)])
+    np.testing.assert_allclose(S, want, rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("window", [0, 300])
+def test_cosine_scores_equal_library_cosine_distance(window):
+    rng = np.random.default_rng(4)
+    K = _bf16(rng.normal(size=(900, 128)) + 0.3)
+    C = oracle.centroids(K, window)
+    S = oracle.scores(K, C, window, "cosine")
+    k = _f64(K)
+    wl = oracle.window_len(900, window)
+    want = np.array([cdist(k[t:t + 1], C[t // wl][None], "cosine")[0, 0] for t in range(900)])
+    np.testing.assert_allclose(S, want, rtol=0, atol=1e-13)
+    assert S.min() >= -1e-15 and S.max() <= 2 + 1e-15
+
+
+def test_l2_translation_invariance_exact():
+    # I3: integer keys, power-of-two T: every fp64 sum is exact, so shifting all
+    # keys by v leaves the scores bit for bit unchanged.
+    rng = np.random.default_rng(5)
+    base = rng.integers(-20, 20, size=(256, 128)).astype(np.float32)
+    v = rng.integers(-50, 50, size=(1, 128)).astype(np.float32)
+    K1, K2 = _bf16(base), _bf16(base + v)
+    for window in (0, 64):
+        S1 = oracle.scores(K1, oracle.centroids(K1, window), window, "l2")
+        S2 = oracle.scores(K2, oracle.centroids(K2, window), window, "l2")
+        np.testing.assert_array_equal(S1, S2)
+
+
+def test_cosine_scale_invariance():
+    # I4: a global alpha > 0 leaves cosine scores unchanged (exact for powers of
+    # two); a per-token alpha_t against a fixed centroid also does.
+    rng = np.random.default_rng(6)
+    base = rng.normal(size=(512, 128)).astype(np.float32)
+    K1 = _bf16(base)
+    K2 = _bf16(base.astype(np.float64) * 8.0)
+    S1 = oracle.scores(K1, oracle.centroids(K1, 0), 0, "cosine")
+    S2 = oracle.scores(K2, oracle.centroids(K2, 0), 0, "cosine")
+    np.testing.assert_array_equal(S1, S2)
+    alpha = 2.0 ** rng.integers(-3, 4, size=(512, 1))
+    K3 = _bf16(K1.to(torch.float64).numpy() * alpha)
+    C = oracle.centroids(K1, 0)
+    np.testing.assert_allclose(oracle.scores(K3, C, 0, "cosine"), S1, rtol=0, atol=1e-15)
+    # l2 is not scale invariant: the pin above would not pass for it
+    assert not np.allclose(oracle.scores(K2, oracle.centroids(K2, 0), 0, "l2"),
+                           oracle.scores(K1, oracle.centroids(K1, 0), 0, "l2"))
+
+
+@pytest.mark.parametrize("mode", ["l2", "cosine"])
+def test_window_at_least_T_equals_global(mode):
+    # I5
+    rng = np.random.default_rng(8)
+    K = _bf16(rng.normal(size=(300, 128)))
+    ref = oracle.compress_head(K, K, 0.3, mode, 0)
+    for w in (300, 301, 10 ** 6):
+        got = oracle.compress_head(K, K, 0.3, mode, w)
+        np.testing.assert_array_equal(got["S"], ref["S"])
+        np.testing.assert_array_equal(got["idx"], ref["idx"])
+
+
+def test_window_one_gives_zero_scores_and_lowest_indices():
+    # I6: every token is its own centroid, all l2 scores are 0, ties keep the
+    # lowest indices.
+    rng = np.random.default_rng(9)
+    K = _bf16(rng.normal(size=(100, 128)))
+    out = oracle.compress_head(K, K, 0.37, "l2", 1)
+    assert np.all(out["S"] == 0.0)
+    assert out["idx"].tolist() == list(range(oracle.num_keep(100, 0.37)))
+
+
+# --- selection ------------------------------------------------------------------
+
+def test_select_brute_force_tiny():
+    # I2: the kept set is the unique subset of size n in which every kept token
+    # beats every dropped one by (score higher, or equal score and lower index).
+    rng = np.random.default_rng(10)
+    for trial in range(300):
+        T = int(rng.integers(1, 9))
+        S = rng.integers(0, 4, size=T).astype(np.float64) * 0.5
+        n = int(rng.integers(0, T + 1))
+        winners = []
+        for subset in itertools.combinations(range(T), n):
+            kept = set(subset)
+            ok = all((S[i] > S[j]) or (S[i] == S[j] and i < j)
+                     for i in kept for j in range(T) if j not in kept)
+            if ok:
+                winners.append(list(subset))
+        assert len(winners) == 1
+        assert oracle.select(S, n).tolist() == winners[0], (S, n)
+
+
+def test_select_matches_stable_library_sort():
+    rng = np.random.default_rng(11)
+    for T in (1, 17, 1000, 4097):
+        S = rng.integers(0, 50, size=T).astype(np.float64)
+        n = int(rng.integers(0, T + 1))
+        order = np.lexsort((np.arange(T), -S))
+        assert oracle.select(S, n).tolist() == sorted(order[:n].tolist())
+
+
+@pytest.mark.parametrize("T,ratio", [(1, 0.5), (2, 0.5), (513, 0.5), (1000, 0.0), (1000, 1.0), (4096, 0.2)])
+def test_kept_count_exact_including_all_tied(T, ratio):
+    # I8
+    K = _bf16(np.ones((T, 128)))
+    for mode in ("l2", "cosine"):
+        out = oracle.compress_head(K, K, ratio, mode, 0)
+        assert len(out["idx"]) == oracle.num_keep(T, ratio)
+        assert out["idx"].tolist() == list(range(len(out["idx"])))
+
+
+def test_gathered_rows_and_ascending_indices():
+    # I10
+    rng = np.random.default_rng(12)
+    K = _bf16(rng.normal(size=(777, 128)))
+    V = _bf16(rng.normal(size=(777, 128)))
+    out = oracle.compress_head(K, V, 0.45, "l2", 100)
+    idx = out["idx"]
+    assert np.all(np.diff(idx) > 0)
+    kb = K.view(torch.int16).numpy().view(np.uint16)
+    vb = V.view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(out["K_out"], kb[idx])
+    np.testing.assert_array_equal(out["V_out"], vb[idx])
+
+
+def test_planted_outliers_always_retained():
+    # I7, on the single-layer 8-head 4096-token workload (seed 0): the tokens
+    # planted at 4x the median norm sit far from the centroid and are kept, with
+    # a wide margin over the cut.
+    w = synthkv.WORKLOADS["single-layer-h8-t4096"]
+    K, V, lens, planted = synthkv.make_kv(w, seed=0, with_planted=True)
+    Kf = K.reshape(w.n_heads, w.t_max, w.head_dim)
+    mode, window, ratio = w.runs[0]
+    for h in range(w.n_heads):
+        out = oracle.compress_head(Kf[h], Kf[h], ratio, mode, window)
+        kept = set(out["idx"].tolist())
+        assert len(kept) == 3277
+        assert set(planted[h].tolist()) <= kept
+        cut = np.sort(out["S"])[::-1][len(kept) - 1]
+        assert out["S"][planted[h].numpy()].min() > 1.5 * cut
+
+
+def test_compress_heads_matches_per_head_on_ragged_lengths():
+    w = synthkv.WORKLOADS["ragged-b8-llama-kv-t8k-32k"].scaled(
+        "ragged-small", layers=1, batch=3, heads=2, t_max=700, t_min=1, planted=4)
+    K, V, lens = synthkv.make_kv(w, seed=3)
+    Kf = K.reshape(w.n_heads, w.t_max, 128)
+    Vf = V.reshape(w.n_heads, w.t_max, 128)
+    hl = lens.repeat_interleave(w.heads)
+    for mode, window, ratio in (("l2", 0, 0.5), ("cosine", 64, 0.2)):
+        stride = oracle.num_keep(w.t_max, ratio)
+        idx, kept, ko, vo = oracle.compress_heads(Kf, Vf, hl, ratio, mode, window, stride)
+        for h in range(w.n_heads):
+            T = int(hl[h])
+            ref = oracle.compress_head(Kf[h, :T], Vf[h, :T], ratio, mode, window)
+            assert kept[h] == len(ref["idx"])
+            np.testing.assert_array_equal(idx[h, :kept[h]], ref["idx"])
+            np.testing.assert_array_equal(ko[h, :kept[h]], ref["K_out"])
+            np.testing.assert_array_equal(vo[h, :kept[h]], ref["V_out"])
+
+
+def test_empty_head():
+    K = _bf16(np.zeros((0, 128)))
+    out = oracle.compress_head(K, K, 0.5, "l2", 0)
+    assert len(out["idx"]) == 0 and len(out["S"]) == 0
