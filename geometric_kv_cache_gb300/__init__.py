@@ -1,0 +1,252 @@
+"""Python binding of the GB300 ManifoldKV-style KV-cache compressor.
+
+Thin ctypes marshalling over the C ABI in ``include/mkv.h`` (``libmkv.so``,
+built in-tree by ``geometric_kv_cache_gb300.build``). Every step of the path
+runs in the library's CUDA kernels; this module only turns torch tensors into
+pointers and sizes, passes the current CUDA stream, and raises on a non-OK
+status. There is no CPU fallback: without the compiled library, or without a
+CUDA device, the calls raise.
+
+Functions carry the C names (``mkv_centroid``, ``mkv_score``,
+``mkv_select_topk``, ``mkv_compact``, ``mkv_compress``, ...). ``compress`` is
+a convenience wrapper that allocates the outputs and the workspace with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MKV_OK = 0
+MKV_ERR_INVALID_ARG = 1
+MKV_ERR_UNSUPPORTED = 2
+MKV_ERR_WORKSPACE = 3
+MKV_ERR_CUDA = 4
+MKV_ERR_DEVICE = 5
+
+MKV_DEV_BAD_SEQ_LEN = 0x1
+MKV_DEV_BAD_N_KEEP = 0x2
+MKV_DEV_INTERNAL = 0x4
+
+MKV_MODE_L2 = 0
+MKV_MODE_COSINE = 1
+_MODES = {"l2": MKV_MODE_L2, "cosine": MKV_MODE_COSINE, MKV_MODE_L2: MKV_MODE_L2, MKV_MODE_COSINE: MKV_MODE_COSINE}
+
+HEAD_DIM = 128
+
+# Every symbol include/mkv.h declares (checked by the tests).
+EXPORTED = (
+    "mkv_num_keep", "mkv_num_windows", "mkv_workspace_size", "mkv_centroid", "mkv_score",
+    "mkv_select_topk", "mkv_compact", "mkv_compress", "mkv_compress_num_stages",
+    "mkv_compress_profiled", "mkv_compress_host", "mkv_device_status", "mkv_status_string",
+)
+
+
+class MkvShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("t_max", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("seq_lens", ctypes.c_void_p)]
+
+
+class MKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {mkv_status_string(status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Load libmkv.so (building it first if it is missing and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"{path} is missing: run geometric_kv_cache_gb300.build.build_library()")
+            _build.build_library()
+        lib = ctypes.CDLL(path)
+        i32, u32, f64, vp, sz = ctypes.c_int32, ctypes.c_uint32, ctypes.c_double, ctypes.c_void_p, ctypes.c_size_t
+        sig = {
+            "mkv_num_keep": (i32, [i32, f64]),
+            "mkv_num_windows": (i32, [i32, i32]),
+            "mkv_workspace_size": (sz, [MkvShape, i32]),
+            "mkv_centroid": (i32, [vp, MkvShape, i32, vp, vp, sz, vp]),
+            "mkv_score": (i32, [vp, vp, MkvShape, i32, i32, vp, vp, sz, vp]),
+            "mkv_select_topk": (i32, [vp, MkvShape, f64, vp, vp, vp, sz, vp]),
+            "mkv_compact": (i32, [vp, vp, vp, vp, MkvShape, f64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
+            "mkv_compress": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
+            "mkv_compress_num_stages": (i32, []),
+            "mkv_compress_profiled": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp,
+                                            ctypes.POINTER(vp), i32]),
+            "mkv_compress_host": (i32, [vp, vp, vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp,
+                                        vp, vp, vp, vp, vp, sz, vp]),
+            "mkv_device_status": (i32, [vp, vp, ctypes.POINTER(u32)]),
+            "mkv_status_string": (ctypes.c_char_p, [i32]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------------ helpers --
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != MKV_OK:
+        raise MKVError(status, where)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors passed to the CUDA library must live on a CUDA device")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors passed to the CUDA library must be contiguous")
+
+
+def shape_of(K: torch.Tensor, seq_lens: Optional[torch.Tensor] = None) -> MkvShape:
+    """mkv_shape of a [batch, heads, t_max, head_dim] bf16 cache."""
+    if K.dim() != 4 or K.dtype != torch.bfloat16:
+        raise ValueError("K must be a bf16 tensor [batch, heads, t_max, head_dim]")
+    if seq_lens is not None and (seq_lens.dtype != torch.int32 or seq_lens.numel() != K.shape[0]):
+        raise ValueError("seq_lens must be int32 [batch]")
+    b, h, t, d = K.shape
+    return MkvShape(b, h, t, d, None if seq_lens is None else seq_lens.data_ptr())
+
+
+def mkv_status_string(status: int) -> str:
+    return load().mkv_status_string(int(status)).decode()
+
+
+def mkv_num_keep(T: int, ratio: float) -> int:
+    return int(load().mkv_num_keep(int(T), float(ratio)))
+
+
+def mkv_num_windows(t_max: int, window: int) -> int:
+    return int(load().mkv_num_windows(int(t_max), int(window)))
+
+
+def mkv_workspace_size(shape: MkvShape, window: int = 0) -> int:
+    return int(load().mkv_workspace_size(shape, int(window)))
+
+
+def mkv_compress_num_stages() -> int:
+    return int(load().mkv_compress_num_stages())
+
+
+def workspace_for(K: torch.Tensor, window: int = 0, seq_lens=None) -> torch.Tensor:
+    """A zeroed workspace (uint8, 256-byte aligned by the caching allocator)."""
+    n = mkv_workspace_size(shape_of(K, seq_lens), window)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=K.device)
+
+
+# -------------------------------------------------------------- entry points --
+
+def mkv_centroid(K, window, C, workspace, seq_lens=None, stream=None):
+    _need_cuda(K, C, workspace, seq_lens)
+    _check(load().mkv_centroid(_ptr(K), shape_of(K, seq_lens), int(window), _ptr(C), _ptr(workspace),
+                               workspace.numel(), _stream(stream)), "mkv_centroid")
+
+
+def mkv_score(K, C, window, mode, S, workspace, seq_lens=None, stream=None):
+    _need_cuda(K, C, S, workspace, seq_lens)
+    _check(load().mkv_score(_ptr(K), _ptr(C), shape_of(K, seq_lens), int(window), _MODES[mode], _ptr(S),
+                            _ptr(workspace), workspace.numel(), _stream(stream)), "mkv_score")
+
+
+def mkv_select_topk(S, shape: MkvShape, ratio, cut, workspace, n_keep=None, stream=None):
+    _need_cuda(S, cut, workspace, n_keep)
+    _check(load().mkv_select_topk(_ptr(S), shape, float(ratio), _ptr(n_keep), _ptr(cut), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)), "mkv_select_topk")
+
+
+def mkv_compact(S, cut, K, V, shape: MkvShape, ratio, keep_stride, idx, kept, K_out, V_out, workspace,
+                n_keep=None, stream=None):
+    _need_cuda(S, cut, K, V, idx, kept, K_out, V_out, workspace, n_keep)
+    _check(load().mkv_compact(_ptr(S), _ptr(cut), _ptr(K), _ptr(V), shape, float(ratio), _ptr(n_keep),
+                              int(keep_stride), _ptr(idx), _ptr(kept), _ptr(K_out), _ptr(V_out), _ptr(workspace),
+                              workspace.numel(), _stream(stream)), "mkv_compact")
+
+
+def mkv_compress(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, workspace, seq_lens=None,
+                 n_keep=None, stream=None):
+    _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens, n_keep)
+    _check(load().mkv_compress(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _ptr(n_keep), _MODES[mode],
+                               int(window), int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx), _ptr(kept),
+                               _ptr(workspace), workspace.numel(), _stream(stream)), "mkv_compress")
+
+
+def mkv_compress_profiled(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, workspace, events,
+                          seq_lens=None, n_keep=None, stream=None):
+    """mkv_compress with torch.cuda.Event objects recorded around each kernel."""
+    _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens, n_keep)
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(load().mkv_compress_profiled(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _ptr(n_keep),
+                                        _MODES[mode], int(window), int(keep_stride), _ptr(K_out), _ptr(V_out),
+                                        _ptr(idx), _ptr(kept), _ptr(workspace), workspace.numel(), _stream(stream),
+                                        arr, len(events)), "mkv_compress_profiled")
+
+
+def mkv_compress_host(hK, hV, dK, dV, ratio, mode, window, keep_stride, dK_out, dV_out, d_idx, d_kept,
+                      hK_out, hV_out, h_idx, h_kept, workspace, seq_lens=None, stream=None):
+    """Host-resident cache: H2D copies, compress and D2H copies in one call."""
+    _need_cuda(dK, dV, dK_out, dV_out, d_idx, d_kept, workspace, seq_lens)
+    for t in (hK, hV, hK_out, hV_out, h_idx, h_kept):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("host buffers must be contiguous CPU tensors (pinned for asynchrony)")
+    _check(load().mkv_compress_host(_ptr(hK), _ptr(hV), _ptr(dK), _ptr(dV), shape_of(dK, seq_lens), float(ratio),
+                                    _MODES[mode], int(window), int(keep_stride), _ptr(dK_out), _ptr(dV_out),
+                                    _ptr(d_idx), _ptr(d_kept), _ptr(hK_out), _ptr(hV_out), _ptr(h_idx),
+                                    _ptr(h_kept), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mkv_compress_host")
+
+
+def mkv_device_status(workspace, stream=None) -> int:
+    """Synchronise, return the status bits of ``workspace`` and clear them."""
+    bits = ctypes.c_uint32(0)
+    st = load().mkv_device_status(_ptr(workspace), _stream(stream), ctypes.byref(bits))
+    if st not in (MKV_OK, MKV_ERR_DEVICE):
+        raise MKVError(st, "mkv_device_status")
+    return int(bits.value)
+
+
+# ---------------------------------------------------------------- convenience --
+
+def compress(K, V, ratio: float, mode="l2", window: int = 0, seq_lens=None, n_keep=None,
+             keep_stride: Optional[int] = None, workspace=None, stream=None):
+    """Compress a bf16 cache [batch, heads, t_max, 128]; returns
+    (K_out, V_out, idx, kept) with K_out/V_out [batch, heads, keep_stride, 128]."""
+    if keep_stride is None:
+        keep_stride = mkv_num_keep(K.shape[2], ratio) if n_keep is None else int(n_keep.max().item())
+    b, h = K.shape[0], K.shape[1]
+    K_out = torch.empty((b, h, keep_stride, K.shape[3]), dtype=K.dtype, device=K.device)
+    V_out = torch.empty_like(K_out)
+    idx = torch.empty((b, h, keep_stride), dtype=torch.int32, device=K.device)
+    kept = torch.empty((b, h), dtype=torch.int32, device=K.device)
+    ws = workspace if workspace is not None else workspace_for(K, window, seq_lens)
+    mkv_compress(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, ws, seq_lens, n_keep, stream)
+    return K_out, V_out, idx, kept

@@ -1,0 +1,363 @@
+// C ABI of the compression path (declared in include/mkv.h): host-side
+// argument checks, workspace carving and the launch sequence. Nothing here
+// allocates device memory or synchronises, except mkv_device_status.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "mkv_internal.h"
+
+namespace mkv {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// floor(T*(1-ratio) + 0.5) clamped to [0, T]; volatile stops the host
+// compiler from fusing the multiply and add, so this rounds like the kernels.
+int32_t host_num_keep(int32_t T, double ratio)
+{
+    if (T <= 0) return 0;
+    volatile double one_minus = 1.0 - ratio;
+    volatile double prod = (double)T * one_minus;
+    volatile double sum = prod + 0.5;
+    const double x = floor(sum);
+    if (x < 0.0) return 0;
+    if (x > (double)T) return T;
+    return (int32_t)x;
+}
+
+bool ratio_ok(double r) { return r >= 0.0 && r <= 1.0; }  // false for NaN
+
+// Shape checks shared by all entry points. Returns MKV_OK or the error.
+mkv_status check_shape(const mkv_shape &s)
+{
+    if (s.batch < 0 || s.heads < 0 || s.t_max < 0 || s.head_dim <= 0) return MKV_ERR_INVALID_ARG;
+    if (s.head_dim != kHeadDim) return MKV_ERR_UNSUPPORTED;
+    if (s.t_max > (1 << 30)) return MKV_ERR_UNSUPPORTED;
+    if (s.seq_lens && !aligned(s.seq_lens, 4)) return MKV_ERR_INVALID_ARG;
+    return MKV_OK;
+}
+
+bool empty(const mkv_shape &s) { return s.batch == 0 || s.heads == 0 || s.t_max == 0; }
+
+mkv_status check_ws(const Layout &L, void *ws, size_t ws_bytes)
+{
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return MKV_ERR_WORKSPACE;
+    return MKV_OK;
+}
+
+// Workspace needs of the step-wise calls that use no partial sums, centroids
+// or scores of their own: the status word and the compaction offsets. This is
+// never larger than the full layout of the same shape.
+Layout make_step_layout(const Geometry &g)
+{
+    Layout L;
+    L.status = 0;
+    L.chunk = kAlign;
+    L.total = kAlign + round_up((size_t)g.n_heads * g.nch * sizeof(int2), kAlign);
+    return L;
+}
+
+template <typename T>
+T *region(void *ws, size_t off)
+{
+    return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+mkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MKV_OK : MKV_ERR_CUDA; }
+
+// Checks of mkv_compact / mkv_compress outputs.
+mkv_status check_outputs(const mkv_shape &s, double ratio, const int32_t *n_keep, int32_t keep_stride,
+                         const void *K, const void *V, const void *K_out, const void *V_out,
+                         const int32_t *idx, const int32_t *kept, bool need_kv)
+{
+    if (!ratio_ok(ratio) || keep_stride < 0) return MKV_ERR_INVALID_ARG;
+    if (!n_keep && keep_stride < host_num_keep(s.t_max, ratio)) return MKV_ERR_INVALID_ARG;
+    if (n_keep && !aligned(n_keep, 4)) return MKV_ERR_INVALID_ARG;
+    if ((K_out == nullptr) != (V_out == nullptr)) return MKV_ERR_INVALID_ARG;
+    if (need_kv && !K_out) return MKV_ERR_INVALID_ARG;
+    if (K_out && (!K || !V)) return MKV_ERR_INVALID_ARG;
+    if (K && !aligned(K, 16)) return MKV_ERR_INVALID_ARG;
+    if (V && !aligned(V, 16)) return MKV_ERR_INVALID_ARG;
+    if (K_out && (!aligned(K_out, 16) || !aligned(V_out, 16))) return MKV_ERR_INVALID_ARG;
+    if (idx && !aligned(idx, 4)) return MKV_ERR_INVALID_ARG;
+    if (kept && !aligned(kept, 4)) return MKV_ERR_INVALID_ARG;
+    return MKV_OK;
+}
+
+// The fused launch sequence; events (optional) bracket every kernel.
+mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio, const int32_t *n_keep,
+                        mkv_mode mode, int32_t window, int32_t keep_stride, void *K_out, void *V_out,
+                        int32_t *idx, int32_t *kept, void *ws, size_t ws_bytes, cudaStream_t st,
+                        void *const *events)
+{
+    mkv_status rc = check_shape(s);
+    if (rc != MKV_OK) return rc;
+    if (!K || !V || window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE)) return MKV_ERR_INVALID_ARG;
+    rc = check_outputs(s, ratio, n_keep, keep_stride, K, V, K_out, V_out, idx, kept, false);
+    if (rc != MKV_OK) return rc;
+    const Geometry g = make_geometry(s.batch, s.heads, s.t_max, window);
+    const Layout L = make_layout(g);
+    rc = check_ws(L, ws, ws_bytes);
+    if (rc != MKV_OK) return rc;
+    if (empty(s)) return MKV_OK;
+    uint32_t *status = region<uint32_t>(ws, L.status);
+    float *partial = region<float>(ws, L.partial);
+    float *C = region<float>(ws, L.centroid);
+    float *S = region<float>(ws, L.score);
+    mkv_cut *cut = region<mkv_cut>(ws, L.cut);
+    int2 *chunk = region<int2>(ws, L.chunk);
+    int32_t *kept_w = kept ? kept : region<int32_t>(ws, L.kept);
+    auto mark = [&](int i) -> bool {
+        return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+    };
+    cudaError_t e = cudaSuccess;
+    if (!mark(0)) return MKV_ERR_CUDA;
+    if ((e = launch_centroid_partial(g, K, s.seq_lens, partial, status, st)) != cudaSuccess) return cuda_status(e);
+    if (!mark(1)) return MKV_ERR_CUDA;
+    if ((e = launch_centroid_finalize(g, partial, s.seq_lens, C, status, st)) != cudaSuccess) return cuda_status(e);
+    if (!mark(2)) return MKV_ERR_CUDA;
+    if ((e = launch_score(g, K, C, s.seq_lens, (int)mode, S, status, st)) != cudaSuccess) return cuda_status(e);
+    if (!mark(3)) return MKV_ERR_CUDA;
+    if ((e = launch_select(g, S, s.seq_lens, ratio, n_keep, keep_stride, cut, chunk, kept_w, status, st)) != cudaSuccess)
+        return cuda_status(e);
+    if (!mark(4)) return MKV_ERR_CUDA;
+    if ((e = launch_compact_gather(g, S, cut, chunk, s.seq_lens, keep_stride, idx, K, V, K_out, V_out, status, st)) !=
+        cudaSuccess)
+        return cuda_status(e);
+    if (!mark(5)) return MKV_ERR_CUDA;
+    return MKV_OK;
+}
+
+constexpr int32_t kCompressStages = 5;
+
+}  // namespace
+
+Geometry make_geometry(int32_t batch, int32_t heads, int32_t t_max, int32_t window)
+{
+    Geometry g;
+    g.n_heads = (int64_t)batch * heads;
+    g.heads = heads;
+    g.t_max = t_max;
+    g.window = window;
+    g.wl_max = (window <= 0 || window >= t_max) ? t_max : window;
+    g.nwin_max = t_max > 0 ? (t_max + g.wl_max - 1) / g.wl_max : 0;
+    // Pieces of at most kMaxPiece tokens; smaller ones when the problem is
+    // small, so that even a few heads spread over many CTAs.
+    int piece = kMaxPiece;
+    auto pieces = [&](int p) { return g.n_heads * g.nwin_max * (int64_t)((g.wl_max + p - 1) / p); };
+    while (piece > 128 && g.wl_max > 0 && pieces(piece) < 4096) piece /= 2;
+    g.piece = piece;
+    g.ppw = g.wl_max > 0 ? (g.wl_max + piece - 1) / piece : 0;
+    int chunk = kMaxPiece;
+    while (chunk > 256 && t_max > 0 && g.n_heads * (int64_t)((t_max + chunk - 1) / chunk) < 4096) chunk /= 2;
+    g.score_chunk = chunk;
+    g.nch = (t_max + kCompactChunk - 1) / kCompactChunk;
+    return g;
+}
+
+Layout make_layout(const Geometry &g)
+{
+    Layout L;
+    size_t off = 0;
+    L.status = off;
+    off += kAlign;
+    L.partial = off;
+    off += round_up((size_t)g.n_heads * g.nwin_max * g.ppw * kHeadDim * sizeof(float), kAlign);
+    L.centroid = off;
+    off += round_up((size_t)g.n_heads * g.nwin_max * kHeadDim * sizeof(float), kAlign);
+    L.score = off;
+    off += round_up((size_t)g.n_heads * g.t_max * sizeof(float), kAlign);
+    L.cut = off;
+    off += round_up((size_t)g.n_heads * sizeof(mkv_cut), kAlign);
+    L.chunk = off;
+    off += round_up((size_t)g.n_heads * g.nch * sizeof(int2), kAlign);
+    L.kept = off;
+    off += round_up((size_t)g.n_heads * sizeof(int32_t), kAlign);
+    L.total = off;
+    return L;
+}
+
+}  // namespace mkv
+
+using namespace mkv;
+
+extern "C" {
+
+int32_t mkv_num_keep(int32_t T, double ratio)
+{
+    if (T < 0 || !ratio_ok(ratio)) return -1;
+    return host_num_keep(T, ratio);
+}
+
+int32_t mkv_num_windows(int32_t t_max, int32_t window)
+{
+    if (t_max < 0 || window < 0) return -1;
+    return make_geometry(1, 1, t_max, window).nwin_max;
+}
+
+size_t mkv_workspace_size(mkv_shape shape, int32_t window)
+{
+    if (check_shape(shape) != MKV_OK || window < 0) return 0;
+    return make_layout(make_geometry(shape.batch, shape.heads, shape.t_max, window)).total;
+}
+
+mkv_status mkv_centroid(const void *K, mkv_shape shape, int32_t window, float *C, void *workspace,
+                        size_t workspace_bytes, mkv_stream_t stream)
+{
+    mkv_status rc = check_shape(shape);
+    if (rc != MKV_OK) return rc;
+    if (!K || !C || window < 0 || !aligned(K, 16) || !aligned(C, 16)) return MKV_ERR_INVALID_ARG;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window);
+    const Layout L = make_layout(g);
+    if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
+    if (empty(shape)) return MKV_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t *status = region<uint32_t>(workspace, L.status);
+    float *partial = region<float>(workspace, L.partial);
+    cudaError_t e = launch_centroid_partial(g, K, shape.seq_lens, partial, status, st);
+    if (e == cudaSuccess) e = launch_centroid_finalize(g, partial, shape.seq_lens, C, status, st);
+    return cuda_status(e);
+}
+
+mkv_status mkv_score(const void *K, const float *C, mkv_shape shape, int32_t window, mkv_mode mode, float *S,
+                     void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    mkv_status rc = check_shape(shape);
+    if (rc != MKV_OK) return rc;
+    if (!K || !C || !S || window < 0 || !aligned(K, 16) || !aligned(C, 16) || !aligned(S, 4)) return MKV_ERR_INVALID_ARG;
+    if (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE) return MKV_ERR_INVALID_ARG;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window);
+    const Layout L = make_step_layout(g);
+    if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
+    if (empty(shape)) return MKV_OK;
+    return cuda_status(launch_score(g, K, C, shape.seq_lens, (int)mode, S, region<uint32_t>(workspace, L.status),
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mkv_status mkv_select_topk(const float *S, mkv_shape shape, double ratio, const int32_t *n_keep, mkv_cut *cut,
+                           void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    mkv_status rc = check_shape(shape);
+    if (rc != MKV_OK) return rc;
+    if (!S || !cut || !aligned(S, 4) || !aligned(cut, 8) || !ratio_ok(ratio)) return MKV_ERR_INVALID_ARG;
+    if (n_keep && !aligned(n_keep, 4)) return MKV_ERR_INVALID_ARG;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, 0);
+    const Layout L = make_step_layout(g);
+    if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
+    if (empty(shape)) return MKV_OK;
+    return cuda_status(launch_select(g, S, shape.seq_lens, ratio, n_keep, -1, cut, nullptr, nullptr,
+                                     region<uint32_t>(workspace, L.status), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mkv_status mkv_compact(const float *S, const mkv_cut *cut, const void *K, const void *V, mkv_shape shape,
+                       double ratio, const int32_t *n_keep, int32_t keep_stride, int32_t *idx, int32_t *kept,
+                       void *K_out, void *V_out, void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    mkv_status rc = check_shape(shape);
+    if (rc != MKV_OK) return rc;
+    if (!S || !cut || !idx || !kept || !aligned(S, 4) || !aligned(cut, 8)) return MKV_ERR_INVALID_ARG;
+    rc = check_outputs(shape, ratio, n_keep, keep_stride, K, V, K_out, V_out, idx, kept, false);
+    if (rc != MKV_OK) return rc;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, 0);
+    const Layout L = make_step_layout(g);
+    if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
+    if (empty(shape)) return MKV_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t *status = region<uint32_t>(workspace, L.status);
+    int2 *chunk = region<int2>(workspace, L.chunk);
+    cudaError_t e = launch_chunk_offsets(g, S, cut, shape.seq_lens, ratio, n_keep, keep_stride, chunk, kept, status, st);
+    if (e == cudaSuccess)
+        e = launch_compact_gather(g, S, cut, chunk, shape.seq_lens, keep_stride, idx, K, V, K_out, V_out, status, st);
+    return cuda_status(e);
+}
+
+mkv_status mkv_compress(const void *K, const void *V, mkv_shape shape, double ratio, const int32_t *n_keep,
+                        mkv_mode mode, int32_t window, int32_t keep_stride, void *K_out, void *V_out, int32_t *idx,
+                        int32_t *kept, void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    return run_compress(K, V, shape, ratio, n_keep, mode, window, keep_stride, K_out, V_out, idx, kept, workspace,
+                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int32_t mkv_compress_num_stages(void) { return kCompressStages; }
+
+mkv_status mkv_compress_profiled(const void *K, const void *V, mkv_shape shape, double ratio,
+                                 const int32_t *n_keep, mkv_mode mode, int32_t window, int32_t keep_stride,
+                                 void *K_out, void *V_out, int32_t *idx, int32_t *kept, void *workspace,
+                                 size_t workspace_bytes, mkv_stream_t stream, void *const *events,
+                                 int32_t n_events)
+{
+    if (!events || n_events < kCompressStages + 1) return MKV_ERR_INVALID_ARG;
+    for (int i = 0; i <= kCompressStages; ++i)
+        if (!events[i]) return MKV_ERR_INVALID_ARG;
+    return run_compress(K, V, shape, ratio, n_keep, mode, window, keep_stride, K_out, V_out, idx, kept, workspace,
+                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream), events);
+}
+
+mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV, mkv_shape shape, double ratio,
+                             mkv_mode mode, int32_t window, int32_t keep_stride, void *dK_out, void *dV_out,
+                             int32_t *d_idx, int32_t *d_kept, void *hK_out, void *hV_out, int32_t *h_idx,
+                             int32_t *h_kept, void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    mkv_status rc = check_shape(shape);
+    if (rc != MKV_OK) return rc;
+    if (!hK || !hV || !dK || !dV || !dK_out || !dV_out || !d_idx || !d_kept) return MKV_ERR_INVALID_ARG;
+    rc = check_outputs(shape, ratio, nullptr, keep_stride, dK, dV, dK_out, dV_out, d_idx, d_kept, true);
+    if (rc != MKV_OK) return rc;
+    if (window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE)) return MKV_ERR_INVALID_ARG;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window);
+    if ((rc = check_ws(make_layout(g), workspace, workspace_bytes)) != MKV_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t in_bytes = (size_t)g.n_heads * shape.t_max * kRowBytes;
+    const size_t out_rows = (size_t)g.n_heads * keep_stride;
+    if (in_bytes && (cudaMemcpyAsync(dK, hK, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+                     cudaMemcpyAsync(dV, hV, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess))
+        return MKV_ERR_CUDA;
+    rc = run_compress(dK, dV, shape, ratio, nullptr, mode, window, keep_stride, dK_out, dV_out, d_idx, d_kept,
+                      workspace, workspace_bytes, st, nullptr);
+    if (rc != MKV_OK) return rc;
+    if (out_rows && hK_out && cudaMemcpyAsync(hK_out, dK_out, out_rows * kRowBytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MKV_ERR_CUDA;
+    if (out_rows && hV_out && cudaMemcpyAsync(hV_out, dV_out, out_rows * kRowBytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MKV_ERR_CUDA;
+    if (out_rows && h_idx && cudaMemcpyAsync(h_idx, d_idx, out_rows * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MKV_ERR_CUDA;
+    if (g.n_heads && h_kept &&
+        cudaMemcpyAsync(h_kept, d_kept, (size_t)g.n_heads * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MKV_ERR_CUDA;
+    return MKV_OK;
+}
+
+mkv_status mkv_device_status(void *workspace, mkv_stream_t stream, uint32_t *bits)
+{
+    if (!workspace || !aligned(workspace, kAlign)) return MKV_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MKV_ERR_CUDA;
+    if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MKV_ERR_CUDA;
+    if (word && cudaMemset(workspace, 0, sizeof word) != cudaSuccess) return MKV_ERR_CUDA;
+    if (bits) *bits = word;
+    return word ? MKV_ERR_DEVICE : MKV_OK;
+}
+
+const char *mkv_status_string(int32_t status)
+{
+    switch (status) {
+    case MKV_OK: return "MKV_OK";
+    case MKV_ERR_INVALID_ARG: return "MKV_ERR_INVALID_ARG: bad argument (null or misaligned pointer, size, ratio, window or stride)";
+    case MKV_ERR_UNSUPPORTED: return "MKV_ERR_UNSUPPORTED: head_dim must be 128 and t_max at most 2^30";
+    case MKV_ERR_WORKSPACE: return "MKV_ERR_WORKSPACE: workspace missing, misaligned or smaller than mkv_workspace_size";
+    case MKV_ERR_CUDA: return "MKV_ERR_CUDA: a CUDA call or kernel launch failed";
+    case MKV_ERR_DEVICE: return "MKV_ERR_DEVICE: a kernel reported bad device-side input (see the status bits)";
+    default: return "unknown mkv_status";
+    }
+}
+
+}  // extern "C"

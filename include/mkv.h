@@ -1,0 +1,197 @@
+/*
+ * mkv.h -- C ABI of a GB300 (sm_103a) implementation of ManifoldKV-style
+ * KV-cache compression.
+ *
+ * The method ("ManifoldKV: Training-Free KV Cache Compression via Euclidean
+ * Outlier Detection", ICML 2026 poster 62526, abstract and lay summary): for
+ * every head of the key cache, take the key centroid (one global mean, or one
+ * mean per non-overlapping window for WindowedManifoldKV), score every token
+ * by its Euclidean distance to its centroid (or, as the KeyDiff-style
+ * baseline the abstract compares against, by one minus its cosine similarity
+ * to the centroid), keep the highest-scoring tokens -- those far from the
+ * centroid -- and gather the kept key and value rows into a compacted cache.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Cache layout. A cache is bf16 [batch, heads, t_max, head_dim], head_dim
+ *   innermost and contiguous (one 256-byte row per token at head_dim 128).
+ *   "batch" counts (layer, sequence) rows: callers fold layers into it, so a
+ *   "head" is one (layer, sequence, KV head) triple, and every head is
+ *   processed independently. Head h = b*heads + j covers tokens
+ *   [0, T_b) with T_b = seq_lens[b] (or t_max when seq_lens is NULL); rows at
+ *   or past T_b are never read.
+ * Windows. window = 0, or window >= T_b, means one global centroid per head;
+ *   otherwise the windows are [jW, min((j+1)W, T_b)), the last one holding the
+ *   remainder, and every token is scored against its own window's centroid.
+ *   Selection is one top-n_keep per head over all its tokens.
+ * Kept count. n_keep(T, ratio) = floor(T*(1-ratio) + 0.5) clamped to [0, T]
+ *   (ratio is the share removed: 20% compression of 4096 tokens keeps 3277),
+ *   unless a per-head array n_keep[batch*heads] is passed.
+ * Ties. Among equal scores the lower token index is kept. Kept indices are
+ *   emitted in ascending token order.
+ * Memory. Every pointer except the host-pointer arguments of
+ *   mkv_compress_host is a device pointer owned by the caller. The library
+ *   allocates and frees nothing and never synchronises, except
+ *   mkv_device_status (which synchronises the stream). Cache and output row
+ *   pointers must be 16-byte aligned; float / int32 arrays 4-byte aligned; the
+ *   workspace 256-byte aligned.
+ * Streams. All work is enqueued on `stream` (NULL = the legacy default
+ *   stream); results are valid in stream order.
+ * Errors. Arguments are checked on the host before anything is enqueued; a
+ *   bad argument returns a status and enqueues nothing. A failed launch
+ *   returns MKV_ERR_CUDA. Problems only the GPU can see (a seq_lens entry
+ *   outside [0, t_max], an n_keep entry outside [0, min(T_b, keep_stride)])
+ *   set bits in a status word at the start of the workspace; the affected
+ *   head is skipped (nothing written for it). Read and clear the word with
+ *   mkv_device_status. No kernel traps or asserts.
+ * Workspace. mkv_workspace_size() bytes are enough for every entry point on
+ *   that shape and window. The status word must be zero before the first
+ *   call (allocate the workspace zeroed, or call mkv_device_status once).
+ *   Calls that share a workspace must not overlap on the GPU.
+ * Supported. head_dim = 128 only (else MKV_ERR_UNSUPPORTED); t_max <= 2^30.
+ *   Scores must not be NaN (inputs with NaN/Inf are outside the contract).
+ */
+#ifndef MKV_H_
+#define MKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *mkv_stream_t;
+
+typedef enum {
+    MKV_OK = 0,
+    MKV_ERR_INVALID_ARG = 1, /* null / misaligned pointer, negative size, ratio outside [0,1], ... */
+    MKV_ERR_UNSUPPORTED = 2, /* head_dim other than 128, t_max above 2^30 */
+    MKV_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than required */
+    MKV_ERR_CUDA = 4,        /* a CUDA call or launch failed */
+    MKV_ERR_DEVICE = 5       /* mkv_device_status only: the status word is nonzero */
+} mkv_status;
+
+/* Bits of the device status word. */
+#define MKV_DEV_BAD_SEQ_LEN 0x1u  /* a seq_lens entry outside [0, t_max] */
+#define MKV_DEV_BAD_N_KEEP 0x2u   /* an n_keep entry outside [0, min(T_b, keep_stride)] */
+#define MKV_DEV_INTERNAL 0x4u     /* a kept count disagreed with n_keep (a library bug) */
+
+typedef enum {
+    MKV_MODE_L2 = 0,     /* s_t = |k_t - c| (ManifoldKV, abstract) */
+    MKV_MODE_COSINE = 1  /* s_t = 1 - cos(k_t, c); 1 when |k_t||c| = 0 (the cosine baseline, abstract) */
+} mkv_mode;
+
+/* Shape of a cache. seq_lens: device int32 [batch], or NULL for all t_max. */
+typedef struct {
+    int32_t batch;
+    int32_t heads;
+    int32_t t_max;
+    int32_t head_dim;
+    const int32_t *seq_lens;
+} mkv_shape;
+
+/* Result of selection for one head: keep every token whose score key is
+ * above `key`, and the first `ties` tokens (in index order) whose key equals
+ * it. The key is the order-preserving map of the fp32 score bits:
+ * bits ^ 0x80000000 for a nonnegative score, ~bits for a negative one.
+ * n_keep = 0 is encoded as {0xFFFFFFFF, 0}. */
+typedef struct {
+    uint32_t key;
+    int32_t ties;
+} mkv_cut;
+
+/* Kept tokens out of T at compression `ratio` (host helper; same rounding as
+ * the kernels). Returns -1 for T < 0 or ratio outside [0, 1]. */
+int32_t mkv_num_keep(int32_t T, double ratio);
+
+/* Windows per head of t_max tokens (0 if t_max = 0). */
+int32_t mkv_num_windows(int32_t t_max, int32_t window);
+
+/* Bytes of workspace any entry point needs for this shape and window
+ * (0 on a bad shape). */
+size_t mkv_workspace_size(mkv_shape shape, int32_t window);
+
+/* Key centroids (abstract: the key centroid; per-window centroids for
+ * WindowedManifoldKV). K: bf16 cache. C: fp32 [batch, heads, nw, head_dim]
+ * with nw = mkv_num_windows(t_max, window); window j of head h gets the mean
+ * of its keys, accumulated in fp32 in a fixed order (the result does not
+ * depend on the GPU or the grid). Windows a short head does not have are not
+ * written. */
+mkv_status mkv_centroid(const void *K, mkv_shape shape, int32_t window, float *C,
+                        void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
+/* Scores (abstract: Euclidean distance to the key centroid; cosine baseline).
+ * C as written by mkv_centroid. S: fp32 [batch, heads, t_max]; S[h][t] for
+ * t < T_b is the score of token t against its window's centroid (fp32,
+ * correctly rounded sqrt); entries at t >= T_b are not written. */
+mkv_status mkv_score(const void *K, const float *C, mkv_shape shape, int32_t window, mkv_mode mode,
+                     float *S, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
+/* Top-n_keep selection per head (abstract: which past tokens to retain; lay
+ * summary: the far ones). S: fp32 scores as above. n_keep: device int32
+ * [batch*heads] or NULL to use `ratio`. cut: [batch*heads] (see mkv_cut). An
+ * exact radix select over the score keys; ties go to the lower index. */
+mkv_status mkv_select_topk(const float *S, mkv_shape shape, double ratio, const int32_t *n_keep,
+                           mkv_cut *cut, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
+/* Compaction and gather. From S and cut, emit per head the kept token indices
+ * in ascending order into idx [batch*heads, keep_stride] and their count into
+ * kept [batch*heads], and copy the kept rows bit for bit: K_out[h][j] =
+ * K[h][idx[h][j]], V_out likewise, both bf16 [batch, heads, keep_stride,
+ * head_dim]. Slots at or past kept[h] are not written. K_out and V_out may be
+ * NULL together (indices only); then K and V may be NULL too. With n_keep
+ * NULL, keep_stride must be at least mkv_num_keep(t_max, ratio). */
+mkv_status mkv_compact(const float *S, const mkv_cut *cut, const void *K, const void *V,
+                       mkv_shape shape, double ratio, const int32_t *n_keep, int32_t keep_stride,
+                       int32_t *idx, int32_t *kept, void *K_out, void *V_out,
+                       void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
+/* The whole path (centroid -> score -> select -> compact + gather) in one
+ * call, intermediates in the workspace. Outputs as for mkv_compact; idx and
+ * kept may be NULL (not returned). */
+mkv_status mkv_compress(const void *K, const void *V, mkv_shape shape, double ratio,
+                        const int32_t *n_keep, mkv_mode mode, int32_t window, int32_t keep_stride,
+                        void *K_out, void *V_out, int32_t *idx, int32_t *kept,
+                        void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
+/* Number of kernels mkv_compress launches (for mkv_compress_profiled). */
+int32_t mkv_compress_num_stages(void);
+
+/* mkv_compress, recording caller-created CUDA events (cudaEvent_t handles
+ * passed as void*) on `stream`: events[i] right before kernel i and
+ * events[n_stages] after the last, so the caller can time every kernel
+ * inside the real call. n_events must be at least n_stages + 1. */
+mkv_status mkv_compress_profiled(const void *K, const void *V, mkv_shape shape, double ratio,
+                                 const int32_t *n_keep, mkv_mode mode, int32_t window,
+                                 int32_t keep_stride, void *K_out, void *V_out, int32_t *idx,
+                                 int32_t *kept, void *workspace, size_t workspace_bytes,
+                                 mkv_stream_t stream, void *const *events, int32_t n_events);
+
+/* mkv_compress for a cache held in host memory (e.g. offloaded to CPU RAM):
+ * copies hK, hV (host, pinned for asynchrony) into the caller's device
+ * buffers dK, dV, runs mkv_compress, and copies the results back into host
+ * buffers hK_out, hV_out [batch, heads, keep_stride, head_dim] and h_idx,
+ * h_kept [batch*heads(, keep_stride)]; any of the four host outputs may be
+ * NULL. Device output buffers dK_out, dV_out, d_idx, d_kept are required.
+ * Every copy is one cudaMemcpyAsync on `stream`; nothing synchronises. */
+mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV, mkv_shape shape,
+                             double ratio, mkv_mode mode, int32_t window, int32_t keep_stride,
+                             void *dK_out, void *dV_out, int32_t *d_idx, int32_t *d_kept,
+                             void *hK_out, void *hV_out, int32_t *h_idx, int32_t *h_kept,
+                             void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
+/* Synchronise `stream`, read the status word of `workspace` into *bits (may
+ * be NULL) and reset it to zero. MKV_OK if it was zero, MKV_ERR_DEVICE if
+ * not, MKV_ERR_CUDA if the synchronisation or copy failed. */
+mkv_status mkv_device_status(void *workspace, mkv_stream_t stream, uint32_t *bits);
+
+/* Static, human-readable name of a status code. */
+const char *mkv_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MKV_H_ */

@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for
+sm_103a and loads, exports every symbol include/mkv.h declares, and rejects
+bad arguments on the host before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import geometric_kv_cache_gb300 as mkv
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mkv.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = mkv.load()
+    declared = _declared_functions()
+    assert declared, "no functions parsed from the header"
+    assert sorted(mkv.EXPORTED) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_num_keep_matches_the_oracle_rounding():
+    for T in list(range(0, 40)) + [4096, 16384, 32767, 65536, 131072, 8193, 24577]:
+        for r in (0.0, 0.1, 0.2, 0.25, 1 / 3, 0.5, 0.75, 0.9, 1.0, 0.26, 0.24, 0.125):
+            assert mkv.mkv_num_keep(T, r) == oracle.num_keep(T, r), (T, r)
+    assert mkv.mkv_num_keep(4096, 0.2) == 3277
+    assert mkv.mkv_num_keep(10, -0.1) == -1
+    assert mkv.mkv_num_keep(10, 1.5) == -1
+    assert mkv.mkv_num_keep(-1, 0.5) == -1
+    assert mkv.mkv_num_keep(10, float("nan")) == -1
+
+
+def test_num_windows_matches_the_oracle_tiling():
+    for T in (0, 1, 5, 4096, 65536, 65537):
+        for w in (0, 1, 3, 4096, 8192, 10 ** 6):
+            assert mkv.mkv_num_windows(T, w) == oracle.num_windows(T, w), (T, w)
+
+
+def _shape(batch=2, heads=8, t_max=1024, head_dim=128, seq_lens=None):
+    return mkv.MkvShape(batch, heads, t_max, head_dim, seq_lens)
+
+
+def test_workspace_size_grows_with_the_problem():
+    small = mkv.mkv_workspace_size(_shape(t_max=1024))
+    big = mkv.mkv_workspace_size(_shape(t_max=65536))
+    assert 256 < small < big
+    # scores alone need 4 bytes per token
+    assert big >= 2 * 8 * 65536 * 4
+    assert mkv.mkv_workspace_size(_shape(head_dim=64)) == 0
+    assert mkv.mkv_workspace_size(_shape(batch=-1)) == 0
+
+
+# Fake, aligned device addresses: every call below must fail its host checks
+# and so never touch them.
+A = 1 << 20
+
+
+def _compress(shape, ratio=0.5, mode=0, window=0, keep_stride=512, K=A, V=A, Ko=A, Vo=A, idx=A, kept=A,
+              ws=A, ws_bytes=1 << 40, n_keep=None):
+    lib = mkv.load()
+    vp = ctypes.c_void_p
+    return lib.mkv_compress(vp(K), vp(V), shape, ratio, vp(n_keep) if n_keep else None, mode, window, keep_stride,
+                            vp(Ko) if Ko else None, vp(Vo) if Vo else None, vp(idx) if idx else None,
+                            vp(kept) if kept else None, vp(ws) if ws else None, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(shape=_shape(head_dim=64)), mkv.MKV_ERR_UNSUPPORTED),
+    (dict(shape=_shape(t_max=(1 << 30) + 1)), mkv.MKV_ERR_UNSUPPORTED),
+    (dict(shape=_shape(heads=-1)), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), ratio=1.5), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), ratio=-0.1), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), ratio=float("nan")), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), mode=7), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), window=-3), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), keep_stride=511), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), K=0), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), K=A + 8), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), Ko=A + 4), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), Vo=0), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), idx=A + 2), mkv.MKV_ERR_INVALID_ARG),
+    (dict(shape=_shape(), ws=0), mkv.MKV_ERR_WORKSPACE),
+    (dict(shape=_shape(), ws=A + 16), mkv.MKV_ERR_WORKSPACE),
+    (dict(shape=_shape(), ws_bytes=1024), mkv.MKV_ERR_WORKSPACE),
+])
+def test_compress_rejects_bad_arguments_on_the_host(kwargs, status):
+    assert _compress(**kwargs) == status
+
+
+def test_empty_problems_enqueue_nothing_and_succeed():
+    for shp, stride in ((_shape(batch=0), 512), (_shape(heads=0), 512), (_shape(t_max=0), 0)):
+        assert _compress(shp, keep_stride=stride) == mkv.MKV_OK
+
+
+def test_step_calls_reject_bad_arguments():
+    lib = mkv.load()
+    vp = ctypes.c_void_p
+    shp = _shape()
+    big = 1 << 40
+    assert lib.mkv_centroid(vp(A), shp, -1, vp(A), vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_centroid(vp(A), shp, 0, vp(A), vp(A), 16, None) == mkv.MKV_ERR_WORKSPACE
+    assert lib.mkv_score(vp(A), vp(A), shp, 0, 5, vp(A), vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_score(vp(A), None, shp, 0, 0, vp(A), vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_select_topk(vp(A), shp, 2.0, None, vp(A), vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_select_topk(vp(A), shp, 0.5, None, vp(A + 4), vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_compact(vp(A), vp(A), vp(A), vp(A), shp, 0.5, None, 10, vp(A), vp(A), vp(A), vp(A), vp(A), big,
+                           None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_compact(vp(A), vp(A), None, None, shp, 0.5, None, 512, vp(A), vp(A), vp(A), None, vp(A), big,
+                           None) == mkv.MKV_ERR_INVALID_ARG
+    events = (ctypes.c_void_p * 2)(vp(A), vp(A))
+    assert lib.mkv_compress_profiled(vp(A), vp(A), shp, 0.5, None, 0, 0, 512, vp(A), vp(A), None, None, vp(A), big,
+                                     None, events, 2) == mkv.MKV_ERR_INVALID_ARG
+    assert mkv.mkv_compress_num_stages() == 5
+
+
+def test_status_strings():
+    for s in range(6):
+        assert mkv.mkv_status_string(s).startswith("MKV_")
+    assert "unknown" in mkv.mkv_status_string(99)

@@ -1,0 +1,393 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64
+oracle on the same seeded inputs.
+
+Small cases run the oracle on every head; they span several CTA tiles and
+ragged tails. The full-size workloads run in the launch configuration the
+bench times (one mkv_compress over the whole cache) and are checked on
+sampled heads against the oracle and on every head through properties that
+hold at any size (kept count, ascending indices, gathered rows equal to the
+input rows, selection equal to the top-n_keep of the GPU's own scores).
+"""
+import numpy as np
+import pytest
+import torch
+
+import geometric_kv_cache_gb300 as mkv
+import oracle
+import synthkv
+from parity_util import StepBuffers, bits, compare_head, oracle_heads, report
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mkv.load()
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _run_fused(K, V, ratio, mode, window, seq_lens=None, n_keep=None, keep_stride=None):
+    K_out, V_out, idx, kept = None, None, None, None
+    ks = mkv.mkv_num_keep(K.shape[2], ratio) if keep_stride is None else keep_stride
+    B, H, T, D = K.shape
+    K_out = torch.zeros((B, H, max(ks, 1), D), dtype=torch.bfloat16, device=DEV)
+    V_out = torch.zeros_like(K_out)
+    idx = torch.full((B, H, max(ks, 1)), -7, dtype=torch.int32, device=DEV)
+    kept = torch.full((B, H), -7, dtype=torch.int32, device=DEV)
+    ws = mkv.workspace_for(K, window, seq_lens)
+    mkv.mkv_compress(K, V, ratio, mode, window, ks, K_out, V_out, idx, kept, ws, seq_lens, n_keep)
+    status = mkv.mkv_device_status(ws)
+    return K_out, V_out, idx, kept, status
+
+
+def _run_steps(K, V, ratio, mode, window, seq_lens=None):
+    b = StepBuffers(K, window, ratio, seq_lens)
+    mkv.mkv_centroid(K, window, b.C, b.ws, seq_lens)
+    mkv.mkv_score(K, b.C, window, mode, b.S, b.ws, seq_lens)
+    mkv.mkv_select_topk(b.S, b.shape, ratio, b.cut, b.ws)
+    mkv.mkv_compact(b.S, b.cut, K, V, b.shape, ratio, b.keep_stride, b.idx, b.kept, b.K_out, b.V_out, b.ws)
+    status = mkv.mkv_device_status(b.ws)
+    return b, status
+
+
+def _check_all_heads(name, K, V, lens, ratio, mode, window, heads=None, steps=True):
+    """Fused (and step-wise) path against the oracle on the listed heads."""
+    B, H, T, D = K.shape
+    n = B * H
+    heads = list(range(n)) if heads is None else heads
+    lens_cpu = lens.cpu().numpy()
+    seq = lens if lens is not None else None
+    ora = oracle_heads(K, V, lens_cpu, H, heads, ratio, mode, window)
+    Ko, Vo, idx, kept, st = _run_fused(K, V, ratio, mode, window, seq)
+    assert st == 0, f"device status {st:#x}"
+    Kob = bits(Ko).reshape(n, -1, D)
+    Vob = bits(Vo).reshape(n, -1, D)
+    idxc = idx.cpu().numpy().reshape(n, -1)
+    keptc = kept.cpu().numpy().reshape(n)
+    Kf = K.reshape(n, T, D)
+    Vf = V.reshape(n, T, D)
+    sb = None
+    if steps:
+        sb, st2 = _run_steps(K, V, ratio, mode, window, seq)
+        assert st2 == 0, f"device status {st2:#x}"
+        S = sb.S.cpu().numpy().reshape(n, T)
+        C = sb.C.cpu().numpy().reshape(n, sb.nw, D)
+    near_total = 0
+    max_rel = 0.0
+    for h in heads:
+        Th = int(lens_cpu[h // H])
+        res = compare_head(ora[h], Th, S_gpu=S[h] if steps else None, idx_gpu=idxc[h], kept_gpu=keptc[h],
+                           K_head=Kf[h], V_head=Vf[h], Kout_gpu=Kob[h], Vout_gpu=Vob[h],
+                           C_gpu=C[h, :len(ora[h]["C"])] if steps else None,
+                           key_scale=float(Kf[h, :Th].float().abs().mean().item()) if Th else 1.0)
+        near_total += res.get("near_cut_exceptions", 0)
+        max_rel = max(max_rel, res.get("score_max_rel_err", 0.0))
+        if steps:
+            # the step-wise calls give the same result as the fused call
+            assert np.array_equal(sb.idx.cpu().numpy().reshape(n, -1)[h, :keptc[h]], idxc[h, :keptc[h]])
+            assert np.array_equal(bits(sb.K_out).reshape(n, -1, D)[h, :keptc[h]], Kob[h, :keptc[h]])
+    report(name, mode=mode, window=window, ratio=ratio, heads_checked=len(heads), near_cut_exceptions=near_total,
+           score_max_rel_err=max_rel)
+    return near_total
+
+
+# ------------------------------------------------------------- small cases --
+
+def test_single_layer_workload_every_head():
+    w = synthkv.WORKLOADS["single-layer-h8-t4096"]
+    K, V, lens = synthkv.make_kv(w, seed=0, device=DEV)
+    mode, window, ratio = w.runs[0]
+    _check_all_heads(w.name, K, V, lens, ratio, mode, window)
+
+
+SCALED = [
+    # (base workload, changes, runs)
+    ("llama3.1-8b-kv-t16k", dict(layers=2, heads=4), None),
+    ("qwen3-8b-kv-t64k-w4096", dict(layers=1, heads=2, t_max=20000, drift_every=3000), None),
+    ("ragged-b8-llama-kv-t8k-32k", dict(layers=2, batch=3, heads=2, t_max=9001, t_min=1), None),
+    ("phi4-kv-t128k", dict(layers=1, heads=2, t_max=40000, drift_every=5000),
+     (("l2", 3000, 0.5), ("l2", 0, 0.5), ("cosine", 0, 0.5))),
+]
+
+
+@pytest.mark.parametrize("base,changes,runs", SCALED, ids=[s[0] for s in SCALED])
+def test_scaled_workloads_every_head(base, changes, runs):
+    w = synthkv.WORKLOADS[base].scaled(base + "-scaled", **changes)
+    K, V, lens = synthkv.make_kv(w, seed=1, device=DEV)
+    for mode, window, ratio in (runs or w.runs):
+        _check_all_heads(f"{w.name}:{mode}:w{window}:r{ratio}", K, V, lens, ratio, mode, window)
+
+
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 63, 64, 65, 1000, 4095, 4096, 4097, 8193])
+@pytest.mark.parametrize("mode", ["l2", "cosine"])
+def test_ragged_tails(T, mode):
+    g = torch.Generator(device=DEV).manual_seed(T)
+    K = (torch.randn(1, 3, T, 128, generator=g, device=DEV) * 2 + 0.25).to(torch.bfloat16)
+    V = torch.randn(1, 3, T, 128, generator=g, device=DEV).to(torch.bfloat16)
+    lens = torch.tensor([T], dtype=torch.int32, device=DEV)
+    for window in (0, 7, 1000):
+        for ratio in (0.0, 0.5, 0.8, 1.0):
+            _check_all_heads(f"tail-T{T}", K, V, lens, ratio, mode, window)
+
+
+def test_window_one_keeps_lowest_indices_and_window_ge_T_is_global():
+    g = torch.Generator(device=DEV).manual_seed(5)
+    K = torch.randn(2, 2, 777, 128, generator=g, device=DEV).to(torch.bfloat16)
+    V = torch.randn(2, 2, 777, 128, generator=g, device=DEV).to(torch.bfloat16)
+    Ko, Vo, idx, kept, st = _run_fused(K, V, 0.4, "l2", 1)
+    assert st == 0
+    n = mkv.mkv_num_keep(777, 0.4)
+    assert torch.equal(idx[..., :n].cpu(), torch.arange(n, dtype=torch.int32).expand(2, 2, n))
+    b1, _ = _run_steps(K, V, 0.4, "l2", 1)
+    assert torch.all(b1.S == 0)
+    ref = _run_fused(K, V, 0.4, "cosine", 0)
+    for wdw in (777, 778, 1 << 20):
+        got = _run_fused(K, V, 0.4, "cosine", wdw)
+        assert torch.equal(got[2], ref[2]) and torch.equal(got[0], ref[0])
+
+
+def test_all_tied_heads_keep_the_lowest_indices():
+    K = torch.ones(1, 4, 5000, 128, dtype=torch.bfloat16, device=DEV)
+    K[0, 1] = 0  # zero keys: cosine score 1 everywhere
+    V = torch.randn(1, 4, 5000, 128, device=DEV).to(torch.bfloat16)
+    for mode in ("l2", "cosine"):
+        for ratio in (0.2, 0.5, 0.9999):
+            Ko, Vo, idx, kept, st = _run_fused(K, V, ratio, mode, 0)
+            n = mkv.mkv_num_keep(5000, ratio)
+            assert st == 0
+            assert torch.all(kept == n)
+            assert torch.equal(idx[..., :n].cpu(), torch.arange(n, dtype=torch.int32).expand(1, 4, n))
+            assert torch.equal(Vo[..., :n, :], V[..., :n, :])
+
+
+def test_exact_arithmetic_scores_are_bit_equal_to_the_oracle():
+    # Integer keys built so that every 64-row block sums to 64*u (u an integer
+    # offset): every window mean is exactly u, every k - c, square and sum is
+    # an exact fp32 value, so the GPU's l2 scores equal the oracle's rounded
+    # to fp32, bit for bit.
+    g = torch.Generator(device=DEV).manual_seed(11)
+    half = torch.randint(-8, 9, (1, 2, 64, 32, 128), generator=g, device=DEV).float()
+    u = torch.randint(-20, 21, (1, 2, 1, 1, 128), generator=g, device=DEV).float()
+    K = (torch.cat([half, -half], dim=3) + u).reshape(1, 2, 4096, 128).to(torch.bfloat16)
+    V = torch.randn(1, 2, 4096, 128, generator=g, device=DEV).to(torch.bfloat16)
+    for window in (0, 1024, 64):
+        b, st = _run_steps(K, V, 0.5, "l2", window)
+        assert st == 0
+        for h in range(2):
+            ora = oracle.compress_head(K[0, h].cpu(), V[0, h].cpu(), 0.5, "l2", window)
+            np.testing.assert_array_equal(b.S[0, h].cpu().numpy(), ora["S"].astype(np.float32))
+            np.testing.assert_array_equal(b.C[0, h, :len(ora["C"])].cpu().numpy(), ora["C"].astype(np.float32))
+            np.testing.assert_array_equal(b.idx[0, h].cpu().numpy(), ora["idx"])
+
+
+def test_translation_invariance_on_the_gpu():
+    g = torch.Generator(device=DEV).manual_seed(12)
+    base = torch.randint(-8, 9, (1, 1, 2048, 128), generator=g, device=DEV).float()
+    shift = torch.randint(-30, 31, (1, 1, 1, 128), generator=g, device=DEV).float()
+    K1, K2 = base.to(torch.bfloat16), (base + shift).to(torch.bfloat16)
+    V = K1.clone()
+    b1, _ = _run_steps(K1, V, 0.5, "l2", 0)
+    b2, _ = _run_steps(K2, V, 0.5, "l2", 0)
+    assert torch.equal(b1.S, b2.S)
+
+
+def test_cosine_scale_invariance_on_the_gpu():
+    g = torch.Generator(device=DEV).manual_seed(13)
+    base = torch.randn(1, 1, 2048, 128, generator=g, device=DEV).to(torch.bfloat16)
+    scaled = (base.float() * 4.0).to(torch.bfloat16)
+    b1, _ = _run_steps(base, base, 0.5, "cosine", 0)
+    b2, _ = _run_steps(scaled, base, 0.5, "cosine", 0)
+    assert torch.equal(b1.S, b2.S)
+
+
+def test_planted_outliers_are_retained_by_the_gpu():
+    w = synthkv.WORKLOADS["single-layer-h8-t4096"]
+    K, V, lens, planted = synthkv.make_kv(w, seed=0, device=DEV, with_planted=True)
+    Ko, Vo, idx, kept, st = _run_fused(K, V, 0.2, "l2", 0)
+    idxc = idx.cpu().reshape(8, -1)
+    for h in range(8):
+        assert set(planted[h].tolist()) <= set(idxc[h].tolist())
+
+
+def test_selection_alone_on_tied_scores_matches_the_oracle():
+    for levels, tie in ((0, 0.0), (0, 0.3), (7, 0.0), (1, 0.0)):
+        S = synthkv.random_scores(6, 9000, seed=levels + 10, tie_fraction=tie, levels=levels, device=DEV)
+        S = S.reshape(2, 3, 9000).contiguous()
+        K = torch.empty(2, 3, 9000, 128, dtype=torch.bfloat16, device="meta")
+        shape = mkv.shape_of(K)
+        for ratio in (0.0, 0.13, 0.5, 0.77, 1.0):
+            ks = mkv.mkv_num_keep(9000, ratio)
+            cut = torch.zeros(6, 2, dtype=torch.int32, device=DEV)
+            idx = torch.full((2, 3, max(ks, 1)), -7, dtype=torch.int32, device=DEV)
+            kept = torch.zeros(2, 3, dtype=torch.int32, device=DEV)
+            ws = torch.zeros(mkv.mkv_workspace_size(shape, 0), dtype=torch.uint8, device=DEV)
+            mkv.mkv_select_topk(S, shape, ratio, cut, ws)
+            mkv.mkv_compact(S, cut, None, None, shape, ratio, ks, idx, kept, None, None, ws)
+            assert mkv.mkv_device_status(ws) == 0
+            Sc = S.cpu().numpy().reshape(6, 9000)
+            for h in range(6):
+                want = oracle.select(Sc[h].astype(np.float64), ks)
+                assert int(kept.reshape(-1)[h]) == ks
+                assert np.array_equal(idx.cpu().numpy().reshape(6, -1)[h, :ks], want), (levels, tie, ratio, h)
+
+
+def test_per_head_keep_counts_and_wider_stride():
+    g = torch.Generator(device=DEV).manual_seed(14)
+    K = torch.randn(2, 3, 3000, 128, generator=g, device=DEV).to(torch.bfloat16)
+    V = torch.randn(2, 3, 3000, 128, generator=g, device=DEV).to(torch.bfloat16)
+    nk = torch.tensor([0, 1, 1500, 2999, 3000, 17], dtype=torch.int32, device=DEV)
+    Ko, Vo, idx, kept, st = _run_fused(K, V, 0.5, "l2", 0, n_keep=nk, keep_stride=3100)
+    assert st == 0
+    assert torch.equal(kept.reshape(-1), nk)
+    b, _ = _run_steps(K, V, 0.5, "l2", 0)
+    S = b.S.cpu().numpy().reshape(6, 3000)
+    idxc = idx.cpu().numpy().reshape(6, -1)
+    for h in range(6):
+        n = int(nk[h])
+        want = np.sort(np.lexsort((np.arange(3000), -S[h].astype(np.float64)))[:n])
+        assert np.array_equal(idxc[h, :n], want)
+        assert np.all(idxc[h, n:] == -7), "slots past the kept count were written"
+
+
+def test_empty_and_zero_length_heads():
+    g = torch.Generator(device=DEV).manual_seed(15)
+    K = torch.randn(3, 2, 600, 128, generator=g, device=DEV).to(torch.bfloat16)
+    V = torch.randn(3, 2, 600, 128, generator=g, device=DEV).to(torch.bfloat16)
+    lens = torch.tensor([0, 600, 1], dtype=torch.int32, device=DEV)
+    _check_all_heads("zero-length", K, V, lens, 0.5, "l2", 0)
+    _check_all_heads("zero-length-cos", K, V, lens, 0.5, "cosine", 100)
+
+
+def test_bad_device_inputs_set_status_bits_and_skip_the_head():
+    g = torch.Generator(device=DEV).manual_seed(16)
+    K = torch.randn(2, 2, 512, 128, generator=g, device=DEV).to(torch.bfloat16)
+    V = torch.randn(2, 2, 512, 128, generator=g, device=DEV).to(torch.bfloat16)
+    lens = torch.tensor([600, 512], dtype=torch.int32, device=DEV)   # 600 > t_max
+    Ko, Vo, idx, kept, st = _run_fused(K, V, 0.5, "l2", 0, seq_lens=lens)
+    assert st & mkv.MKV_DEV_BAD_SEQ_LEN
+    assert torch.all(kept[0] == 0) and torch.all(kept[1] == 256)
+    nk = torch.tensor([10, 600, 10, 10], dtype=torch.int32, device=DEV)  # 600 > T
+    Ko, Vo, idx, kept, st = _run_fused(K, V, 0.5, "l2", 0, n_keep=nk, keep_stride=512)
+    assert st & mkv.MKV_DEV_BAD_N_KEEP
+    assert kept.reshape(-1).tolist() == [10, 0, 10, 10]
+    assert mkv.mkv_device_status(mkv.workspace_for(K)) == 0
+
+
+def test_deterministic_and_paths_agree():
+    w = synthkv.WORKLOADS["ragged-b8-llama-kv-t8k-32k"].scaled("det", layers=1, batch=2, heads=4, t_max=12000,
+                                                                 t_min=5000)
+    K, V, lens = synthkv.make_kv(w, seed=4, device=DEV)
+    a = _run_fused(K, V, 0.3, "cosine", 2048, lens)
+    b = _run_fused(K, V, 0.3, "cosine", 2048, lens)
+    for x, y in zip(a[:4], b[:4]):
+        assert torch.equal(x, y)
+    # profiled variant
+    ks = mkv.mkv_num_keep(w.t_max, 0.3)
+    Ko = torch.zeros_like(a[0]); Vo = torch.zeros_like(a[1])
+    idx = torch.full_like(a[2], -7); kept = torch.zeros_like(a[3])
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(mkv.mkv_compress_num_stages() + 1)]
+    ws = mkv.workspace_for(K, 2048, lens)
+    mkv.mkv_compress_profiled(K, V, 0.3, "cosine", 2048, ks, Ko, Vo, idx, kept, ws, events, lens)
+    torch.cuda.synchronize()
+    assert all(events[i].elapsed_time(events[i + 1]) >= 0 for i in range(len(events) - 1))
+    assert torch.equal(Ko, a[0]) and torch.equal(idx, a[2])
+    # host-buffer variant
+    hK, hV = K.cpu().pin_memory(), V.cpu().pin_memory()
+    hKo = torch.zeros(a[0].shape, dtype=torch.bfloat16).pin_memory()
+    hVo = torch.zeros_like(hKo).pin_memory()
+    hidx = torch.zeros(a[2].shape, dtype=torch.int32).pin_memory()
+    hkept = torch.zeros(a[3].shape, dtype=torch.int32).pin_memory()
+    dK, dV = torch.empty_like(K), torch.empty_like(V)
+    dKo, dVo = torch.empty_like(a[0]), torch.empty_like(a[1])
+    didx, dkept = torch.empty_like(a[2]), torch.empty_like(a[3])
+    mkv.mkv_compress_host(hK, hV, dK, dV, 0.3, "cosine", 2048, ks, dKo, dVo, didx, dkept, hKo, hVo, hidx, hkept,
+                          ws, lens)
+    torch.cuda.synchronize()
+    kk = a[3].cpu()
+    assert torch.equal(hkept, kk)
+    for h in range(kk.numel()):
+        bb, hh = divmod(h, 4)
+        n = int(kk[bb, hh])
+        assert torch.equal(hidx[bb, hh, :n], a[2][bb, hh, :n].cpu())
+        assert torch.equal(hKo[bb, hh, :n], a[0][bb, hh, :n].cpu())
+        assert torch.equal(hVo[bb, hh, :n], a[1][bb, hh, :n].cpu())
+
+
+# ------------------------------------------------------ full-size workloads --
+
+def _full_size(name, runs=None, sample=4):
+    w = synthkv.WORKLOADS[name]
+    torch.cuda.empty_cache()
+    K, V, lens = synthkv.make_kv(w, seed=0, device=DEV)
+    n, T = w.n_heads, w.t_max
+    rng = np.random.default_rng(0)
+    heads = sorted(set([0, n - 1, n // 2] + rng.integers(0, n, size=sample).tolist()))
+    lens_cpu = lens.cpu().numpy()
+    for mode, window, ratio in (runs or w.runs):
+        ks = mkv.mkv_num_keep(T, ratio)
+        Ko = torch.empty((w.rows, w.heads, ks, 128), dtype=torch.bfloat16, device=DEV)
+        Vo = torch.empty_like(Ko)
+        idx = torch.full((w.rows, w.heads, ks), -1, dtype=torch.int32, device=DEV)
+        kept = torch.zeros((w.rows, w.heads), dtype=torch.int32, device=DEV)
+        ws = mkv.workspace_for(K, window, lens)
+        mkv.mkv_compress(K, V, ratio, mode, window, ks, Ko, Vo, idx, kept, ws, lens)
+        assert mkv.mkv_device_status(ws) == 0
+        # properties on every head, computed on the GPU with torch
+        T_h = lens.repeat_interleave(w.heads).reshape(w.rows, w.heads).long()
+        want_kept = torch.tensor([[mkv.mkv_num_keep(int(t), ratio)] * w.heads for t in lens_cpu],
+                                 dtype=torch.int32, device=DEV)
+        assert torch.equal(kept, want_kept)
+        slot = torch.arange(ks, device=DEV)
+        live = slot[None, None, :] < kept[..., None]
+        ii = idx.long()
+        assert torch.all(ii[live] >= 0) and torch.all((ii < T_h[..., None])[live])
+        asc = (ii[..., 1:] > ii[..., :-1]) | ~live[..., 1:]
+        assert torch.all(asc)
+        for r in range(w.rows):  # gathered rows equal the input rows, row-chunked to bound memory
+            gi = ii[r].clamp(min=0)[..., None].expand(-1, -1, 128)
+            m = live[r][..., None]
+            assert torch.equal(torch.where(m, torch.gather(K[r], 1, gi), 0), torch.where(m, Ko[r], 0))
+            assert torch.equal(torch.where(m, torch.gather(V[r], 1, gi), 0), torch.where(m, Vo[r], 0))
+        # sampled heads against the oracle
+        ora = oracle_heads(K, V, lens_cpu, w.heads, heads, ratio, mode, window)
+        Kf, Vf = K.reshape(n, T, 128), V.reshape(n, T, 128)
+        near = 0
+        for h in heads:
+            b, hh = divmod(h, w.heads)
+            Th = int(lens_cpu[b])
+            nk = int(kept[b, hh])
+            res = compare_head(ora[h], Th, idx_gpu=idx[b, hh].cpu().numpy(), kept_gpu=nk, K_head=Kf[h],
+                               V_head=Vf[h], Kout_gpu=bits(Ko[b, hh, :nk]), Vout_gpu=bits(Vo[b, hh, :nk]))
+            near += res["near_cut_exceptions"]
+        report(f"{name}:{mode}:w{window}:r{ratio}:full", heads_sampled=len(heads), near_cut_exceptions=near,
+               heads_property_checked=n)
+        del Ko, Vo, idx, kept, ws
+        torch.cuda.empty_cache()
+    del K, V
+    torch.cuda.empty_cache()
+
+
+def test_full_size_single_layer():
+    _full_size("single-layer-h8-t4096", sample=8)
+
+
+def test_full_size_llama():
+    _full_size("llama3.1-8b-kv-t16k")
+
+
+def test_full_size_qwen_windowed():
+    _full_size("qwen3-8b-kv-t64k-w4096")
+
+
+def test_full_size_ragged_batch():
+    _full_size("ragged-b8-llama-kv-t8k-32k")
+
+
+def test_full_size_phi4():
+    _full_size("phi4-kv-t128k")
