@@ -1,0 +1,447 @@
+"""Throughput of the ManifoldKV-style compression path on GB300.
+
+One step = one mkv_compress over the whole synthetic cache of the bench
+workload (Llama-3.1-8B-shaped KV: 32 layers x 8 KV heads, d=128, T=16384,
+bf16; global L2 centroid; 50% compression): centroid, score, top-k select,
+compaction and K/V gather for all 256 heads.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). ``value`` is KV token rows (one per layer,
+KV head and position) scored and compacted per second over all ranks, inputs
+resident in HBM. ``e2e`` is the same metric through mkv_compress_host with
+the cache in pinned host memory (H2D of K and V, compress, D2H of the
+compacted cache, indices and counts inside the timed region). ``roofline`` is
+for the kernel with the largest share of the step, timed with CUDA events on
+the launching stream inside the real call. ``cpu_baseline`` is the fp64
+oracle on the host cores on a sample of the same cache.
+
+``--impl reference`` times the oracle (the only reference implementation of
+this path) on the host cores on samples of the same workload and prints the
+same JSON line with ``"impl": "reference"``.
+
+Under torchrun (N > 1) every rank compresses its own cache of the same shape
+(heads are independent; no collective touches the data path); the step time
+is the max over ranks and ``value`` counts all ranks' tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthkv  # noqa: E402
+
+METRIC = "KV tokens scored+compacted/sec and achieved HBM GB/s vs ~8 TB/s peak"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+STAGES = ["centroid_partial", "centroid_finalize", "score", "select", "compact_gather"]
+
+
+# ----------------------------------------------------------------- helpers --
+
+def workload_run(name: str):
+    w = synthkv.WORKLOADS[name]
+    mode, window, ratio = w.runs[0]
+    return w, mode, window, ratio
+
+
+def keep_count(T: int, ratio: float) -> int:
+    """Same rounding as the library's mkv_num_keep (used for byte counts only)."""
+    import geometric_kv_cache_gb300 as mkv
+    return mkv.mkv_num_keep(T, ratio)
+
+
+def path_bytes(lens, heads: int, ratio: float, d: int = 128) -> dict:
+    """Algorithmic bytes of one step: K read twice (centroid, score) plus the
+    kept K and V rows read and written; per kernel as well."""
+    tok = sum(int(t) for t in lens) * heads
+    keep = sum(keep_count(int(t), ratio) for t in lens) * heads
+    k_read = 2 * tok * d
+    return {
+        "tokens": tok,
+        "kept": keep,
+        "path": 2 * k_read + 8 * keep * d,
+        "centroid_partial": k_read,
+        "score": k_read,
+        "compact_gather": 8 * keep * d,
+        "select": 0,
+        "centroid_finalize": 0,
+    }
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank compresses its own cache: seeds differ per rank."""
+    return seed + 1000003 * rank
+
+
+def max_over_ranks(x: float, group=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, group=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+# ----------------------------------------------------------- CPU oracle leg --
+
+def oracle_throughput(K_host, V_host, lens, heads_per_row, ratio, mode, window, budget_s=12.0,
+                      max_heads=None, chunk=8):
+    """Time the oracle (as it stands, single-threaded) on heads of a host cache
+    until ``budget_s`` has passed; returns (tokens/s, heads done, tokens)."""
+    import numpy as np
+
+    import oracle
+    n, T, D = K_host.shape[0] * K_host.shape[1], K_host.shape[2], K_host.shape[3]
+    Kf = K_host.reshape(n, T, D)
+    Vf = V_host.reshape(n, T, D)
+    hl = np.repeat(np.asarray(lens, dtype=np.int32), heads_per_row)
+    stride = keep_count(T, ratio)
+    limit = n if max_heads is None else min(n, max_heads)
+    done, tokens, spent = 0, 0, 0.0
+    while done < limit and spent < budget_s:
+        m = min(chunk, limit - done)
+        t0 = time.perf_counter()
+        oracle.compress_heads(Kf[done:done + m], Vf[done:done + m], hl[done:done + m], ratio, mode, window, stride)
+        spent += time.perf_counter() - t0
+        tokens += int(hl[done:done + m].sum())
+        done += m
+    return tokens / spent, done, tokens, spent
+
+
+# ------------------------------------------------------------------ our arm --
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import geometric_kv_cache_gb300 as mkv
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    mkv.load()
+    w, mode, window, ratio = workload_run(args.workload)
+    K, V, lens = synthkv.make_kv(w, seed=rank_seed(args.seed, rank), device=dev)
+    T = w.t_max
+    ks = mkv.mkv_num_keep(T, ratio)
+    K_out = torch.empty((w.rows, w.heads, ks, w.head_dim), dtype=torch.bfloat16, device=dev)
+    V_out = torch.empty_like(K_out)
+    idx = torch.empty((w.rows, w.heads, ks), dtype=torch.int32, device=dev)
+    kept = torch.empty((w.rows, w.heads), dtype=torch.int32, device=dev)
+    ws = mkv.workspace_for(K, window, lens)
+    stream = torch.cuda.current_stream(dev)
+    lens_list = lens.cpu().tolist()
+    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim)
+
+    def step():
+        mkv.mkv_compress(K, V, ratio, mode, window, ks, K_out, V_out, idx, kept, ws, lens, stream=stream)
+
+    # warm-up, then a correctness guard on the status word
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if mkv.mkv_device_status(ws, stream) != 0:
+        raise RuntimeError("device status nonzero after warm-up")
+
+    # main timed region: exactly K steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ms_local)
+    tokens_all = sum_over_ranks(float(nbytes["tokens"]))
+    value = tokens_all / (ms / 1e3)
+
+    # per-kernel durations inside the real call (events on the launching stream)
+    ns = mkv.mkv_compress_num_stages()
+    prof_steps = max(10, min(args.steps, 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(prof_steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(prof_steps):
+        mkv.mkv_compress_profiled(K, V, ratio, mode, window, ks, K_out, V_out, idx, kept, ws, evs[i], lens,
+                                  stream=stream)
+    torch.cuda.synchronize(dev)
+    stage_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / prof_steps for j in range(ns)]
+    dom = max(range(ns), key=lambda j: stage_ms[j])
+    peaks = measured_peaks()
+    dom_name = STAGES[dom]
+    achieved = nbytes[dom_name] / (stage_ms[dom] / 1e3) / 1e9
+    traffic = args.traffic.get(dom_name) if args.traffic else None
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        hK = K.cpu().pin_memory()
+        hV = V.cpu().pin_memory()
+        hKo = torch.empty(K_out.shape, dtype=torch.bfloat16).pin_memory()
+        hVo = torch.empty_like(hKo).pin_memory()
+        hidx = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
+        hkept = torch.empty(kept.shape, dtype=torch.int32).pin_memory()
+        dK, dV = torch.empty_like(K), torch.empty_like(V)
+
+        def e2e_step():
+            mkv.mkv_compress_host(hK, hV, dK, dV, ratio, mode, window, ks, K_out, V_out, idx, kept, hKo, hVo, hidx,
+                                  hkept, ws, lens, stream=stream)
+        for _ in range(2):
+            e2e_step()
+        e2e_steps = max(3, min(args.steps, args.e2e_steps))
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps)
+        h2d = hK.numel() * 2 + hV.numel() * 2
+        d2h = hKo.numel() * 2 + hVo.numel() * 2 + hidx.numel() * 4 + hkept.numel() * 4
+        e2e = {"value": tokens_all / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
+        if mkv.mkv_device_status(ws, stream) != 0:
+            raise RuntimeError("device status nonzero after the e2e steps")
+
+    # CPU baseline: the oracle on a bounded sample of the same cache (rank 0, N=1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        hKc = hK if e2e is not None else K.cpu()
+        hVc = hV if e2e is not None else V.cpu()
+        tps, done, tok, spent = oracle_throughput(hKc, hVc, lens_list, w.heads, ratio, mode, window,
+                                                  budget_s=args.cpu_budget)
+        cpu = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"first {done} of {w.n_heads} heads ({tok} token rows, {spent:.1f} s), fp64 C oracle, "
+                         f"single thread"}
+
+    hbm_gbs = nbytes["path"] * (world) / (ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "io_dtype": "bf16",
+        "data": "synthetic (seeded; Llama-3.1-8B-shaped KV cache, random keys with outlier channels)",
+        "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "kv_heads": w.heads,
+                   "heads_total": w.n_heads, "t": T, "head_dim": w.head_dim, "mode": mode,
+                   "window": window, "ratio": ratio, "keep_per_head": ks,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "no flush: K+V (%.1f GB) exceed the 129 MB L2" % (2 * K.numel() * 2 / 1e9)},
+        "hbm": {"path_bytes_per_step": nbytes["path"], "achieved_gbs": hbm_gbs,
+                "frac_of_nominal_8000": hbm_gbs / world / NOMINAL_HBM_GBS,
+                "frac_of_measured": hbm_gbs / world / peaks["hbm_gbs"]},
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                     "traffic": traffic, "algorithmic_bytes_per_launch": nbytes[dom_name],
+                     "ms_per_launch": stage_ms[dom]},
+        "stages_ms": dict(zip(STAGES, stage_ms)),
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * ns,
+        "clocks": clocks.summary(),
+    }
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ reference arm --
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    w, mode, window, ratio = workload_run(args.workload)
+    lens = synthkv.seq_lengths(w, args.seed).tolist()
+    oracle.build()
+    # one head to size the per-step sample so the whole run takes about a minute
+    K1, V1, _ = synthkv.make_kv(w, seed=args.seed, heads=[0])
+    t0 = time.perf_counter()
+    oracle.compress_heads(K1, V1, np.array([lens[0]], np.int32), ratio, mode, window)
+    t_head = time.perf_counter() - t0
+    per_step = int(max(1, min(w.n_heads, round(args.ref_budget / max(1, args.steps + args.warmup) / t_head))))
+    ids = list(range(per_step))
+    K, V, _ = synthkv.make_kv(w, seed=args.seed, heads=ids)
+    hl = np.array([lens[h // w.heads] for h in ids], np.int32)
+    for _ in range(args.warmup):
+        oracle.compress_heads(K, V, hl, ratio, mode, window)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.compress_heads(K, V, hl, ratio, mode, window)
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    tok = int(hl.sum())
+    value = tok / sec
+    sample = f"{per_step} of {w.n_heads} heads per step ({tok} token rows), fp64 C oracle, single thread"
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; same generator and workload)",
+        "config": {"workload": w.name, "heads_total": w.n_heads, "t": w.t_max, "head_dim": w.head_dim,
+                   "mode": mode, "window": window, "ratio": ratio, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=synthkv.BENCH_WORKLOAD, choices=sorted(synthkv.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle time for --impl reference")
+    ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
+                    help="per-kernel DRAM bytes per launch from an ncu capture (null when absent)")
+    args = ap.parse_args(argv)
+    args.traffic = None
+    if args.traffic_json and os.path.exists(args.traffic_json):
+        with open(args.traffic_json) as f:
+            t = json.load(f)
+        if t.get("workload") == args.workload:
+            args.traffic = t.get("bytes_per_launch")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -204,6 +204,10 @@ def mkv_compress_profiled(K, V, ratio, mode, window, keep_stride, K_out, V_out, 
                           seq_lens=None, n_keep=None, stream=None):
     """mkv_compress with torch.cuda.Event objects recorded around each kernel."""
     _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens, n_keep)
+    st = torch.cuda.current_stream() if stream is None else stream
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on its first record
+            e.record(st)
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(load().mkv_compress_profiled(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _ptr(n_keep),
                                         _MODES[mode], int(window), int(keep_stride), _ptr(K_out), _ptr(V_out),

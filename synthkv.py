@@ -197,5 +197,5 @@ def random_scores(n_heads: int, t: int, seed: int, tie_fraction: float = 0.0,
         n = max(1, int(math.floor(tie_fraction * t)))
         for h in range(n_heads):
             pos = torch.randperm(t, generator=g, device=device)[:n]
-            s[h, pos] = s[h, pos[0]]
+            s[h, pos] = float(s[h, pos[0]].item())
     return s

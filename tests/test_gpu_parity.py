@@ -85,15 +85,16 @@ def _check_all_heads(name, K, V, lens, ratio, mode, window, heads=None, steps=Tr
         res = compare_head(ora[h], Th, S_gpu=S[h] if steps else None, idx_gpu=idxc[h], kept_gpu=keptc[h],
                            K_head=Kf[h], V_head=Vf[h], Kout_gpu=Kob[h], Vout_gpu=Vob[h],
                            C_gpu=C[h, :len(ora[h]["C"])] if steps else None,
-                           key_scale=float(Kf[h, :Th].float().abs().mean().item()) if Th else 1.0)
+                           key_scale=float(Kf[h, :Th].float().abs().mean().item()) if Th else 1.0,
+                           mode=mode)
         near_total += res.get("near_cut_exceptions", 0)
-        max_rel = max(max_rel, res.get("score_max_rel_err", 0.0))
+        max_rel = max(max_rel, res.get("score_max_err_over_tol", 0.0))
         if steps:
             # the step-wise calls give the same result as the fused call
             assert np.array_equal(sb.idx.cpu().numpy().reshape(n, -1)[h, :keptc[h]], idxc[h, :keptc[h]])
             assert np.array_equal(bits(sb.K_out).reshape(n, -1, D)[h, :keptc[h]], Kob[h, :keptc[h]])
     report(name, mode=mode, window=window, ratio=ratio, heads_checked=len(heads), near_cut_exceptions=near_total,
-           score_max_rel_err=max_rel)
+           score_max_err_over_tol=max_rel)
     return near_total
 
 
@@ -363,7 +364,8 @@ def _full_size(name, runs=None, sample=4):
             Th = int(lens_cpu[b])
             nk = int(kept[b, hh])
             res = compare_head(ora[h], Th, idx_gpu=idx[b, hh].cpu().numpy(), kept_gpu=nk, K_head=Kf[h],
-                               V_head=Vf[h], Kout_gpu=bits(Ko[b, hh, :nk]), Vout_gpu=bits(Vo[b, hh, :nk]))
+                               V_head=Vf[h], Kout_gpu=bits(Ko[b, hh, :nk]), Vout_gpu=bits(Vo[b, hh, :nk]),
+                               mode=mode)
             near += res["near_cut_exceptions"]
         report(f"{name}:{mode}:w{window}:r{ratio}:full", heads_sampled=len(heads), near_cut_exceptions=near,
                heads_property_checked=n)
