@@ -50,8 +50,13 @@ STAGES = ["centroid_partial", "centroid_finalize", "score", "select", "compact_g
 
 # ----------------------------------------------------------------- helpers --
 
-def workload_run(name: str):
+def workload_run(name: str, layers: int = 0):
+    """The workload and its first (mode, window, ratio) run; ``layers`` > 0
+    keeps the shape of each layer but changes the layer count (a smaller
+    case for profiler captures)."""
     w = synthkv.WORKLOADS[name]
+    if layers and layers != w.layers:
+        w = w.scaled(f"{w.name}-{layers}layers", layers=layers)
     mode, window, ratio = w.runs[0]
     return w, mode, window, ratio
 
@@ -233,7 +238,7 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
     mkv.load()
-    w, mode, window, ratio = workload_run(args.workload)
+    w, mode, window, ratio = workload_run(args.workload, args.layers)
     K, V, lens = synthkv.make_kv(w, seed=rank_seed(args.seed, rank), device=dev)
     T = w.t_max
     ks = mkv.mkv_num_keep(T, ratio)
@@ -379,7 +384,7 @@ def run_reference(args):
     import numpy as np
 
     import oracle
-    w, mode, window, ratio = workload_run(args.workload)
+    w, mode, window, ratio = workload_run(args.workload, args.layers)
     lens = synthkv.seq_lengths(w, args.seed).tolist()
     oracle.build()
     # one head to size the per-step sample so the whole run takes about a minute
@@ -422,6 +427,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=synthkv.BENCH_WORKLOAD, choices=sorted(synthkv.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
@@ -435,7 +441,7 @@ def main(argv=None):
     if args.traffic_json and os.path.exists(args.traffic_json):
         with open(args.traffic_json) as f:
             t = json.load(f)
-        if t.get("workload") == args.workload:
+        if t.get("workload") == args.workload and not args.layers:
             args.traffic = t.get("bytes_per_launch")
     if args.impl == "reference":
         run_reference(args)
