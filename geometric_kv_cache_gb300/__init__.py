@@ -44,6 +44,7 @@ EXPORTED = (
     "mkv_num_keep", "mkv_num_windows", "mkv_workspace_size", "mkv_centroid", "mkv_score",
     "mkv_select_topk", "mkv_compact", "mkv_compress", "mkv_compress_num_stages",
     "mkv_compress_profiled", "mkv_compress_host", "mkv_device_status", "mkv_status_string",
+    "mkv_compress_noalloc",
 )
 
 
@@ -94,6 +95,7 @@ def load(build_if_missing: bool = True):
             "mkv_compress_host": (i32, [vp, vp, vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp,
                                         vp, vp, vp, vp, vp, sz, vp]),
             "mkv_device_status": (i32, [vp, vp, ctypes.POINTER(u32)]),
+            "mkv_compress_noalloc": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
             "mkv_status_string": (ctypes.c_char_p, [i32]),
         }
         for name, (res, args) in sig.items():
@@ -227,6 +229,20 @@ def mkv_compress_host(hK, hV, dK, dV, ratio, mode, window, keep_stride, dK_out, 
                                     _ptr(d_idx), _ptr(d_kept), _ptr(hK_out), _ptr(hV_out), _ptr(h_idx),
                                     _ptr(h_kept), _ptr(workspace), workspace.numel(), _stream(stream)),
            "mkv_compress_host")
+
+
+def mkv_compress_noalloc(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, status_out=None,
+                         seq_lens=None, n_keep=None, stream=None):
+    """mkv_compress without a workspace, for callers that cannot allocate
+    device memory: the library uses its own fixed 32 MiB scratch array, so
+    problems needing more scratch than that raise MKV_ERR_UNSUPPORTED, and
+    calls must not overlap on the GPU. ``status_out`` (int32/uint32 [1] on
+    the device, optional) receives the call's device status bits."""
+    _need_cuda(K, V, K_out, V_out, idx, kept, status_out, seq_lens, n_keep)
+    _check(load().mkv_compress_noalloc(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _ptr(n_keep),
+                                       _MODES[mode], int(window), int(keep_stride), _ptr(K_out), _ptr(V_out),
+                                       _ptr(idx), _ptr(kept), _ptr(status_out), _stream(stream)),
+           "mkv_compress_noalloc")
 
 
 def mkv_device_status(workspace, stream=None) -> int:

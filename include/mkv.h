@@ -182,6 +182,39 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
                              void *hK_out, void *hV_out, int32_t *h_idx, int32_t *h_kept,
                              void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
+/* Size of the library-owned scratch array used by mkv_compress_noalloc. */
+#define MKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* mkv_compress for callers that cannot allocate device memory. The paper has
+ * no counterpart: this is an engineering entry point. Some callers get only
+ * input and output pointers and a stream: a custom operator behind an inference
+ * engine's C plugin interface, a server whose memory planner reserves all
+ * device memory up front and forbids allocations while it serves, or a
+ * latency-critical path that cannot afford cudaMalloc's implicit device
+ * synchronisation. This call therefore needs no workspace. It uses a fixed
+ * scratch array of MKV_NOALLOC_SCRATCH_BYTES (32 MiB) in the library's device
+ * image. Every GPU that loads the library holds that array until the process
+ * exits, whether or not this call is used.
+ *   Limits: the problem must fit, i.e. mkv_workspace_size(shape, window) <=
+ *   MKV_NOALLOC_SCRATCH_BYTES (about 7.4M token rows, heads x t_max, per call at window 0).
+ *   Larger problems return MKV_ERR_UNSUPPORTED and enqueue nothing; split
+ *   them into several calls over groups of heads.
+ *   Set-up: the first call on a device, with that device current, looks up the
+ *   array's device address once (cudaGetSymbolAddress). Make that first call
+ *   before any stream capture.
+ *   Sharing: every call uses the same array, and it keeps the last call's
+ *   contents. Calls that can overlap on the GPU (different streams, or
+ *   different host threads, on one device) race on it and corrupt each
+ *   other's results. Serialise them.
+ *   Outputs and arguments: as for mkv_compress. status_out (device, nullable)
+ *   receives the device status word of this call (MKV_DEV_* bits); the call
+ *   then resets the word to zero. After MKV_ERR_CUDA the word may still hold
+ *   that call's bits. The call allocates and frees nothing. */
+mkv_status mkv_compress_noalloc(const void *K, const void *V, mkv_shape shape, double ratio,
+                                const int32_t *n_keep, mkv_mode mode, int32_t window, int32_t keep_stride,
+                                void *K_out, void *V_out, int32_t *idx, int32_t *kept, uint32_t *status_out,
+                                mkv_stream_t stream);
+
 /* Synchronise `stream`, read the status word of `workspace` into *bits (may
  * be NULL) and reset it to zero. MKV_OK if it was zero, MKV_ERR_DEVICE if
  * not, MKV_ERR_CUDA if the synchronisation or copy failed. */
