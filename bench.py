@@ -45,7 +45,7 @@ METRIC = "KV tokens scored+compacted/sec and achieved HBM GB/s vs ~8 TB/s peak"
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-STAGES = ["centroid_partial", "centroid_finalize", "score", "select", "compact_gather"]
+STAGES = ["centroid_score", "select", "compact_gather"]
 
 
 # ----------------------------------------------------------------- helpers --
@@ -67,9 +67,12 @@ def keep_count(T: int, ratio: float) -> int:
     return mkv.mkv_num_keep(T, ratio)
 
 
-def path_bytes(lens, heads: int, ratio: float, d: int = 128) -> dict:
-    """Algorithmic bytes of one step: K read twice (centroid, score) plus the
-    kept K and V rows read and written; per kernel as well."""
+def path_bytes(lens, heads: int, ratio: float, d: int = 128, k_reads: int = 2) -> dict:
+    """Algorithmic bytes of one step as the metric defines them: K read twice
+    (centroid, score) plus the kept K and V rows read and written. Per stage:
+    the bytes each stage must move -- the centroid+score stage reads K
+    ``k_reads`` times (1 for the single-pass kernel) and writes 4 B of score
+    per token; the gather reads and writes the kept K and V rows."""
     tok = sum(int(t) for t in lens) * heads
     keep = sum(keep_count(int(t), ratio) for t in lens) * heads
     k_read = 2 * tok * d
@@ -77,11 +80,9 @@ def path_bytes(lens, heads: int, ratio: float, d: int = 128) -> dict:
         "tokens": tok,
         "kept": keep,
         "path": 2 * k_read + 8 * keep * d,
-        "centroid_partial": k_read,
-        "score": k_read,
-        "compact_gather": 8 * keep * d,
+        "centroid_score": k_reads * k_read + 4 * tok,
         "select": 0,
-        "centroid_finalize": 0,
+        "compact_gather": 8 * keep * d,
     }
 
 
@@ -249,7 +250,8 @@ def run_ours(args):
     ws = mkv.workspace_for(K, window, lens)
     stream = torch.cuda.current_stream(dev)
     lens_list = lens.cpu().tolist()
-    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim)
+    single = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
+    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single == 1 else 2)
 
     def step():
         mkv.mkv_compress(K, V, ratio, mode, window, ks, K_out, V_out, idx, kept, ws, lens, stream=stream)
@@ -354,6 +356,7 @@ def run_ours(args):
         "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "kv_heads": w.heads,
                    "heads_total": w.n_heads, "t": T, "head_dim": w.head_dim, "mode": mode,
                    "window": window, "ratio": ratio, "keep_per_head": ks,
+                   "single_pass_centroid_score": single == 1,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "no flush: K+V (%.1f GB) exceed the 129 MB L2" % (2 * K.numel() * 2 / 1e9)},
         "hbm": {"path_bytes_per_step": nbytes["path"], "achieved_gbs": hbm_gbs,

@@ -32,6 +32,7 @@ MKV_ERR_DEVICE = 5
 MKV_DEV_BAD_SEQ_LEN = 0x1
 MKV_DEV_BAD_N_KEEP = 0x2
 MKV_DEV_INTERNAL = 0x4
+MKV_DEV_TIMEOUT = 0x8
 
 MKV_MODE_L2 = 0
 MKV_MODE_COSINE = 1
@@ -44,7 +45,7 @@ EXPORTED = (
     "mkv_num_keep", "mkv_num_windows", "mkv_workspace_size", "mkv_centroid", "mkv_score",
     "mkv_select_topk", "mkv_compact", "mkv_compress", "mkv_compress_num_stages",
     "mkv_compress_profiled", "mkv_compress_host", "mkv_device_status", "mkv_status_string",
-    "mkv_compress_noalloc",
+    "mkv_compress_noalloc", "mkv_compress_single_pass",
 )
 
 
@@ -90,6 +91,7 @@ def load(build_if_missing: bool = True):
             "mkv_compact": (i32, [vp, vp, vp, vp, MkvShape, f64, vp, i32, vp, vp, vp, vp, vp, sz, vp]),
             "mkv_compress": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
             "mkv_compress_num_stages": (i32, []),
+            "mkv_compress_single_pass": (i32, [MkvShape, i32, i32]),
             "mkv_compress_profiled": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp,
                                             ctypes.POINTER(vp), i32]),
             "mkv_compress_host": (i32, [vp, vp, vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp,
@@ -158,6 +160,11 @@ def mkv_workspace_size(shape: MkvShape, window: int = 0) -> int:
 
 def mkv_compress_num_stages() -> int:
     return int(load().mkv_compress_num_stages())
+
+
+def mkv_compress_single_pass(shape: MkvShape, window: int = 0, mode="l2") -> int:
+    """1 if mkv_compress reads K once for this shape on the current device."""
+    return int(load().mkv_compress_single_pass(shape, int(window), _MODES[mode]))
 
 
 def workspace_for(K: torch.Tensor, window: int = 0, seq_lens=None) -> torch.Tensor:

@@ -119,23 +119,23 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     };
     cudaError_t e = cudaSuccess;
     if (!mark(0)) return MKV_ERR_CUDA;
-    if ((e = launch_centroid_partial(g, K, s.seq_lens, partial, status, st)) != cudaSuccess) return cuda_status(e);
+    // a1 + a2: piece sums, window means, scores
+    e = launch_piece_sums(g.pg, K, s.seq_lens, partial, status, st);
+    if (e == cudaSuccess) e = launch_window_means(g.pg, partial, s.seq_lens, C, status, st);
+    if (e == cudaSuccess) e = launch_piece_scores(g.pg, K, C, s.seq_lens, (int)mode, S, status, st);
+    if (e != cudaSuccess) return cuda_status(e);
     if (!mark(1)) return MKV_ERR_CUDA;
-    if ((e = launch_centroid_finalize(g, partial, s.seq_lens, C, status, st)) != cudaSuccess) return cuda_status(e);
-    if (!mark(2)) return MKV_ERR_CUDA;
-    if ((e = launch_score(g, K, C, s.seq_lens, (int)mode, S, status, st)) != cudaSuccess) return cuda_status(e);
-    if (!mark(3)) return MKV_ERR_CUDA;
     if ((e = launch_select(g, S, s.seq_lens, ratio, n_keep, keep_stride, cut, chunk, kept_w, status, st)) != cudaSuccess)
         return cuda_status(e);
-    if (!mark(4)) return MKV_ERR_CUDA;
+    if (!mark(2)) return MKV_ERR_CUDA;
     if ((e = launch_compact_gather(g, S, cut, chunk, s.seq_lens, keep_stride, idx, K, V, K_out, V_out, status, st)) !=
         cudaSuccess)
         return cuda_status(e);
-    if (!mark(5)) return MKV_ERR_CUDA;
+    if (!mark(3)) return MKV_ERR_CUDA;
     return MKV_OK;
 }
 
-constexpr int32_t kCompressStages = 5;
+constexpr int32_t kCompressStages = 3;
 
 }  // namespace
 
@@ -145,33 +145,41 @@ Geometry make_geometry(int32_t batch, int32_t heads, int32_t t_max, int32_t wind
     g.n_heads = (int64_t)batch * heads;
     g.heads = heads;
     g.t_max = t_max;
-    g.window = window;
-    g.wl_max = (window <= 0 || window >= t_max) ? t_max : window;
-    g.nwin_max = t_max > 0 ? (t_max + g.wl_max - 1) / g.wl_max : 0;
-    // Pieces of at most kMaxPiece tokens; smaller ones when the problem is
-    // small, so that even a few heads spread over many CTAs.
-    int piece = kMaxPiece;
-    auto pieces = [&](int p) { return g.n_heads * g.nwin_max * (int64_t)((g.wl_max + p - 1) / p); };
-    while (piece > 128 && g.wl_max > 0 && pieces(piece) < 4096) piece /= 2;
-    g.piece = piece;
-    g.ppw = g.wl_max > 0 ? (g.wl_max + piece - 1) / piece : 0;
-    int chunk = kMaxPiece;
-    while (chunk > 256 && t_max > 0 && g.n_heads * (int64_t)((t_max + chunk - 1) / chunk) < 4096) chunk /= 2;
-    g.score_chunk = chunk;
     g.nch = (t_max + kCompactChunk - 1) / kCompactChunk;
+    PieceGeometry &p = g.pg;
+    p.n_heads = g.n_heads;
+    p.heads = heads;
+    p.t_max = t_max;
+    p.window = window;
+    const int32_t wl_max = (window <= 0 || window >= t_max) ? t_max : window;
+    p.nwin_max = t_max > 0 ? (int32_t)(((int64_t)t_max + wl_max - 1) / wl_max) : 0;
+    // pieces of 256 * 2^k tokens: the smallest that keep a window within
+    // kMaxPiecesPerWindow pieces (a function of the shape only)
+    int32_t rows = kMinPieceRows;
+    while (wl_max > 0 && (wl_max + rows - 1) / rows > kMaxPiecesPerWindow && rows < (1 << 24)) rows *= 2;
+    p.piece_rows = rows;
+    p.ppw = wl_max > 0 ? (wl_max + rows - 1) / rows : 0;
+    p.ngroups_max = (p.ppw + kGroupPieces - 1) / kGroupPieces;
+    p.n_items = g.n_heads * p.nwin_max * (int64_t)p.ppw;
     return g;
 }
 
 Layout make_layout(const Geometry &g)
 {
+    const PieceGeometry &p = g.pg;
+    const size_t wins = (size_t)g.n_heads * p.nwin_max;
     Layout L;
     size_t off = 0;
     L.status = off;
     off += kAlign;
     L.partial = off;
-    off += round_up((size_t)g.n_heads * g.nwin_max * g.ppw * kHeadDim * sizeof(float), kAlign);
+    off += round_up(wins * p.ppw * kHeadDim * sizeof(float), kAlign);
+    L.gsum = off;
+    off += round_up(wins * p.ngroups_max * kHeadDim * sizeof(float), kAlign);
+    L.counters = off;
+    off += round_up(wins * (p.ngroups_max + 2) * sizeof(uint32_t), kAlign);
     L.centroid = off;
-    off += round_up((size_t)g.n_heads * g.nwin_max * kHeadDim * sizeof(float), kAlign);
+    off += round_up(wins * kHeadDim * sizeof(float), kAlign);
     L.score = off;
     off += round_up((size_t)g.n_heads * g.t_max * sizeof(float), kAlign);
     L.cut = off;
@@ -199,7 +207,7 @@ int32_t mkv_num_keep(int32_t T, double ratio)
 int32_t mkv_num_windows(int32_t t_max, int32_t window)
 {
     if (t_max < 0 || window < 0) return -1;
-    return make_geometry(1, 1, t_max, window).nwin_max;
+    return make_geometry(1, 1, t_max, window).pg.nwin_max;
 }
 
 size_t mkv_workspace_size(mkv_shape shape, int32_t window)
@@ -221,8 +229,8 @@ mkv_status mkv_centroid(const void *K, mkv_shape shape, int32_t window, float *C
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint32_t *status = region<uint32_t>(workspace, L.status);
     float *partial = region<float>(workspace, L.partial);
-    cudaError_t e = launch_centroid_partial(g, K, shape.seq_lens, partial, status, st);
-    if (e == cudaSuccess) e = launch_centroid_finalize(g, partial, shape.seq_lens, C, status, st);
+    cudaError_t e = launch_piece_sums(g.pg, K, shape.seq_lens, partial, status, st);
+    if (e == cudaSuccess) e = launch_window_means(g.pg, partial, shape.seq_lens, C, status, st);
     return cuda_status(e);
 }
 
@@ -237,8 +245,8 @@ mkv_status mkv_score(const void *K, const float *C, mkv_shape shape, int32_t win
     const Layout L = make_step_layout(g);
     if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
     if (empty(shape)) return MKV_OK;
-    return cuda_status(launch_score(g, K, C, shape.seq_lens, (int)mode, S, region<uint32_t>(workspace, L.status),
-                                    reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_piece_scores(g.pg, K, C, shape.seq_lens, (int)mode, S,
+                                           region<uint32_t>(workspace, L.status), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mkv_status mkv_select_topk(const float *S, mkv_shape shape, double ratio, const int32_t *n_keep, mkv_cut *cut,
@@ -287,6 +295,12 @@ mkv_status mkv_compress(const void *K, const void *V, mkv_shape shape, double ra
 }
 
 int32_t mkv_compress_num_stages(void) { return kCompressStages; }
+
+int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
+{
+    if (check_shape(shape) != MKV_OK || window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE)) return -1;
+    return 0;
+}
 
 mkv_status mkv_compress_profiled(const void *K, const void *V, mkv_shape shape, double ratio,
                                  const int32_t *n_keep, mkv_mode mode, int32_t window, int32_t keep_stride,

@@ -1,0 +1,127 @@
+// Device helpers shared by the kernel translation units (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mkv_internal.h"
+
+namespace mkv {
+namespace dev {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v)
+{
+    *reinterpret_cast<uint4 *>(p) = v;
+}
+
+// Eight bf16 values of a 16-byte chunk, widened exactly to fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float f[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// Sum over the 16 lanes of a half-warp (all 32 lanes must call it).
+__device__ __forceinline__ float half_warp_sum(float v)
+{
+    v += __shfl_xor_sync(kFull, v, 8);
+    v += __shfl_xor_sync(kFull, v, 4);
+    v += __shfl_xor_sync(kFull, v, 2);
+    v += __shfl_xor_sync(kFull, v, 1);
+    return v;
+}
+
+// Order-preserving map of fp32 bits to uint32 (larger score -> larger key).
+__device__ __forceinline__ uint32_t score_key(float s)
+{
+    const uint32_t b = __float_as_uint(s);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Tokens of head `head`; a length outside [0, t_max] is reported and the
+// head treated as empty.
+__device__ __forceinline__ int head_len(const int32_t *seq_lens, int64_t head, int heads, int t_max,
+                                        uint32_t *status, bool report)
+{
+    if (!seq_lens) return t_max;
+    const int T = seq_lens[head / heads];
+    if (T < 0 || T > t_max) {
+        if (report) atomicOr(status, MKV_DEV_BAD_SEQ_LEN);
+        return 0;
+    }
+    return T;
+}
+
+__device__ __forceinline__ int window_len(int T, int window)
+{
+    return (window <= 0 || window >= T) ? T : window;
+}
+
+// floor(T*(1-ratio) + 0.5) clamped to [0, T], each operation rounded once
+// (no contraction into an FMA), matching the host helper bit for bit.
+__device__ __forceinline__ int num_keep_dev(int T, double ratio)
+{
+    if (T <= 0) return 0;
+    const double x = floor(__dadd_rn(__dmul_rn((double)T, __dsub_rn(1.0, ratio)), 0.5));
+    if (x < 0.0) return 0;
+    if (x > (double)T) return T;
+    return (int)x;
+}
+
+// Exclusive prefix sum over the CTA in thread order; *total gets the sum.
+// Every thread of the CTA must call it; `scratch` holds one word per warp.
+template <int NT>
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *scratch, uint32_t *total)
+{
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < NW ? scratch[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < NW) scratch[lane] = w;  // inclusive warp totals
+    }
+    __syncthreads();
+    const uint32_t before_warp = warp ? scratch[warp - 1] : 0u;
+    if (total) *total = scratch[NW - 1];
+    __syncthreads();  // scratch may be reused right after
+    return before_warp + x - v;
+}
+
+// Nanoseconds since an arbitrary origin (the GPU's global timer); bounds
+// every wait in the kernels.
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+}  // namespace dev
+}  // namespace mkv

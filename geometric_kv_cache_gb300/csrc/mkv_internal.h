@@ -13,46 +13,56 @@ namespace mkv {
 constexpr int kHeadDim = 128;          // the one supported head_dim
 constexpr int kRowBytes = kHeadDim * 2;  // one bf16 row
 constexpr int kCompactChunk = 4096;    // tokens per compaction CTA (256 threads x 16)
-constexpr int kMaxPiece = 2048;        // tokens per centroid / score CTA item (upper bound)
+constexpr int kStageRows = 64;         // piece lengths are multiples of this
+constexpr int kMinPieceRows = 256;     // pieces are 256 * 2^k tokens (a window shorter than that is one piece) ...
+constexpr int kMaxPiecesPerWindow = 64;  // ... the fewest that keep a window within this many pieces
+constexpr int kGroupPieces = 32;       // pieces per first-level group of a window's sum
 constexpr uint32_t kNoneKey = 0xFFFFFFFFu;  // mkv_cut.key meaning "keep nothing"
 
-// Geometry of one call, derived on the host from the shape and the window.
-// Every choice here depends only on the shape (never on the GPU), so results
-// are the same on every device and grid size.
-struct Geometry {
+// Piece decomposition of the centroid / score work: item = (head, window,
+// piece), head-major. Depends only on the shape and the window (never on
+// the GPU), so results are the same on every device and grid size.
+struct PieceGeometry {
     int64_t n_heads = 0;   // batch * heads
+    int64_t n_items = 0;   // n_heads * nwin_max * ppw
     int32_t heads = 0;
     int32_t t_max = 0;
     int32_t window = 0;    // 0 = global
-    int32_t wl_max = 0;    // window length for a head of t_max tokens
-    int32_t nwin_max = 0;  // windows for a head of t_max tokens
-    int32_t piece = 0;     // tokens per centroid partial-sum piece
+    int32_t nwin_max = 0;  // windows of a head of t_max tokens
+    int32_t piece_rows = 0;  // tokens per piece (256 * 2^k)
     int32_t ppw = 0;       // pieces per window (upper bound)
-    int32_t score_chunk = 0;
+    int32_t ngroups_max = 0;
+};
+
+struct Geometry {
+    PieceGeometry pg;
+    int64_t n_heads = 0;
+    int32_t heads = 0;
+    int32_t t_max = 0;
     int32_t nch = 0;       // compaction chunks per head (upper bound)
 };
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct Layout {
-    size_t status = 0, partial = 0, centroid = 0, score = 0, cut = 0, chunk = 0, kept = 0, total = 0;
+    size_t status = 0, partial = 0, gsum = 0, counters = 0, centroid = 0, score = 0, cut = 0, chunk = 0, kept = 0,
+           total = 0;
 };
 
 Geometry make_geometry(int32_t batch, int32_t heads, int32_t t_max, int32_t window);
 Layout make_layout(const Geometry &g);
 
-struct Launch {
-    int sms = 0;
-};
-Launch device_launch_info();
+// Occupancy helpers (kernels loop over their items, persistent style).
+int resident_grid(const void *fn, int threads, size_t dyn_smem);              // SMs x resident CTAs per SM
+int grid_for_items(const void *fn, int threads, size_t dyn_smem, int64_t items);
 
-// Kernel launchers: each enqueues exactly one kernel on `st` and returns the
+// Kernel launchers: each enqueues its kernel(s) on `st` and returns the
 // launch error (cudaSuccess when fine).
-cudaError_t launch_centroid_partial(const Geometry &g, const void *K, const int32_t *seq_lens,
-                                    float *partial, uint32_t *status, cudaStream_t st);
-cudaError_t launch_centroid_finalize(const Geometry &g, const float *partial, const int32_t *seq_lens,
-                                     float *C, uint32_t *status, cudaStream_t st);
-cudaError_t launch_score(const Geometry &g, const void *K, const float *C, const int32_t *seq_lens,
-                         int mode, float *S, uint32_t *status, cudaStream_t st);
+cudaError_t launch_piece_sums(const PieceGeometry &g, const void *K, const int32_t *seq_lens, float *partial,
+                              uint32_t *status, cudaStream_t st);
+cudaError_t launch_window_means(const PieceGeometry &g, const float *partial, const int32_t *seq_lens, float *C,
+                                uint32_t *status, cudaStream_t st);
+cudaError_t launch_piece_scores(const PieceGeometry &g, const void *K, const float *C, const int32_t *seq_lens,
+                                int mode, float *S, uint32_t *status, cudaStream_t st);
 // Radix select; when chunk_info != nullptr it also computes the per-chunk
 // output offsets and the kept counts (the fused path's fourth pass).
 cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_lens, double ratio,

@@ -77,6 +77,7 @@ typedef enum {
 #define MKV_DEV_BAD_SEQ_LEN 0x1u  /* a seq_lens entry outside [0, t_max] */
 #define MKV_DEV_BAD_N_KEEP 0x2u   /* an n_keep entry outside [0, min(T_b, keep_stride)] */
 #define MKV_DEV_INTERNAL 0x4u     /* a kept count disagreed with n_keep (a library bug) */
+#define MKV_DEV_TIMEOUT 0x8u      /* a bounded wait between CTAs ran out; the scores it guarded are missing */
 
 typedef enum {
     MKV_MODE_L2 = 0,     /* s_t = |k_t - c| (ManifoldKV, abstract) */
@@ -156,12 +157,21 @@ mkv_status mkv_compress(const void *K, const void *V, mkv_shape shape, double ra
                         void *K_out, void *V_out, int32_t *idx, int32_t *kept,
                         void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
-/* Number of kernels mkv_compress launches (for mkv_compress_profiled). */
+/* Number of stages mkv_compress runs (for mkv_compress_profiled): 3 --
+ * centroid + score (a1, a2: one single-pass kernel, or three kernels when a
+ * window has more 128-token pieces than the GPU holds resident CTAs), top-k
+ * select with compaction offsets (a3, a4), compaction + gather (a4, a5). */
 int32_t mkv_compress_num_stages(void);
 
+/* 1 if mkv_compress on the current device reads K once (the single-pass
+ * centroid + score kernel) for this shape, window and mode; 0 if it uses the
+ * three-kernel path (K read twice); -1 on a bad argument or CUDA error.
+ * Both give bit-identical results. */
+int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode);
+
 /* mkv_compress, recording caller-created CUDA events (cudaEvent_t handles
- * passed as void*) on `stream`: events[i] right before kernel i and
- * events[n_stages] after the last, so the caller can time every kernel
+ * passed as void*) on `stream`: events[i] right before stage i and
+ * events[n_stages] after the last, so the caller can time every stage
  * inside the real call. n_events must be at least n_stages + 1. */
 mkv_status mkv_compress_profiled(const void *K, const void *V, mkv_shape shape, double ratio,
                                  const int32_t *n_keep, mkv_mode mode, int32_t window,

@@ -393,3 +393,9 @@ def test_full_size_ragged_batch():
 
 def test_full_size_phi4():
     _full_size("phi4-kv-t128k")
+
+
+def test_single_pass_query():
+    small = mkv.MkvShape(32, 8, 16384, 128, None)
+    assert mkv.mkv_compress_single_pass(small, 0, "l2") in (0, 1)
+    assert mkv.load().mkv_compress_single_pass(small, -1, 0) == -1
