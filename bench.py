@@ -45,7 +45,7 @@ METRIC = "KV tokens scored+compacted/sec and achieved HBM GB/s vs ~8 TB/s peak"
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-STAGES = ["centroid_score", "select", "compact_gather"]
+STAGES = ["centroid_score", "select", "compact", "gather"]
 
 
 # ----------------------------------------------------------------- helpers --
@@ -82,7 +82,8 @@ def path_bytes(lens, heads: int, ratio: float, d: int = 128, k_reads: int = 2) -
         "path": 2 * k_read + 8 * keep * d,
         "centroid_score": k_reads * k_read + 4 * tok,
         "select": 0,
-        "compact_gather": 8 * keep * d,
+        "compact": 0,
+        "gather": 8 * keep * d,
     }
 
 
@@ -369,7 +370,7 @@ def run_ours(args):
         "stages_ms": dict(zip(STAGES, stage_ms)),
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * ns,
+        "gpu_launches": args.steps * (4 if single == 1 else 6),
         "clocks": clocks.summary(),
     }
     if world > 1:

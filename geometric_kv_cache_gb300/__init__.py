@@ -45,7 +45,7 @@ EXPORTED = (
     "mkv_num_keep", "mkv_num_windows", "mkv_workspace_size", "mkv_centroid", "mkv_score",
     "mkv_select_topk", "mkv_compact", "mkv_compress", "mkv_compress_num_stages",
     "mkv_compress_profiled", "mkv_compress_host", "mkv_device_status", "mkv_status_string",
-    "mkv_compress_noalloc", "mkv_compress_single_pass",
+    "mkv_compress_noalloc", "mkv_compress_single_pass", "mkv_set_single_pass",
 )
 
 
@@ -92,6 +92,7 @@ def load(build_if_missing: bool = True):
             "mkv_compress": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
             "mkv_compress_num_stages": (i32, []),
             "mkv_compress_single_pass": (i32, [MkvShape, i32, i32]),
+            "mkv_set_single_pass": (i32, [i32]),
             "mkv_compress_profiled": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp,
                                             ctypes.POINTER(vp), i32]),
             "mkv_compress_host": (i32, [vp, vp, vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp,
@@ -165,6 +166,12 @@ def mkv_compress_num_stages() -> int:
 def mkv_compress_single_pass(shape: MkvShape, window: int = 0, mode="l2") -> int:
     """1 if mkv_compress reads K once for this shape on the current device."""
     return int(load().mkv_compress_single_pass(shape, int(window), _MODES[mode]))
+
+
+def mkv_set_single_pass(enable: bool) -> bool:
+    """Allow or forbid the single-pass centroid + score kernel; returns the
+    previous setting."""
+    return bool(load().mkv_set_single_pass(1 if enable else 0))
 
 
 def workspace_for(K: torch.Tensor, window: int = 0, seq_lens=None) -> torch.Tensor:

@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "mkv_internal.h"
 
 namespace mkv {
@@ -13,6 +15,11 @@ namespace mkv {
 namespace {
 
 constexpr size_t kAlign = 256;
+
+// Whether mkv_compress may use the single-pass centroid + score kernel
+// (mkv_set_single_pass). Off by default: on GB300 the three-kernel path is
+// currently faster for every measured shape.
+std::atomic<int> g_single_pass_enabled{0};
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -119,23 +126,42 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     };
     cudaError_t e = cudaSuccess;
     if (!mark(0)) return MKV_ERR_CUDA;
-    // a1 + a2: piece sums, window means, scores
-    e = launch_piece_sums(g.pg, K, s.seq_lens, partial, status, st);
-    if (e == cudaSuccess) e = launch_window_means(g.pg, partial, s.seq_lens, C, status, st);
-    if (e == cudaSuccess) e = launch_piece_scores(g.pg, K, C, s.seq_lens, (int)mode, S, status, st);
+    // a1 + a2: one pass over K when every window's pieces fit the resident
+    // grid; else piece sums, window means, scores (same arithmetic, same bits)
+    const int grid = g_single_pass_enabled.load(std::memory_order_relaxed) ? single_pass_grid((int)mode) : 0;
+    bool single = grid > 0 && grid >= g.pg.ppw;
+    if (single) {
+        e = launch_single_pass(g.pg, grid, K, s.seq_lens, (int)mode, partial, region<float>(ws, L.gsum),
+                               region<uint32_t>(ws, L.counters), C, S, status, st);
+        if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer CTAs fit right now
+            (void)cudaGetLastError();
+            single = false;
+            e = cudaSuccess;
+        }
+    }
+    if (!single) {
+        e = launch_piece_sums(g.pg, K, s.seq_lens, partial, status, st);
+        if (e == cudaSuccess) e = launch_window_means(g.pg, partial, s.seq_lens, C, status, st);
+        if (e == cudaSuccess) e = launch_piece_scores(g.pg, K, C, s.seq_lens, (int)mode, S, status, st);
+    }
     if (e != cudaSuccess) return cuda_status(e);
     if (!mark(1)) return MKV_ERR_CUDA;
     if ((e = launch_select(g, S, s.seq_lens, ratio, n_keep, keep_stride, cut, chunk, kept_w, status, st)) != cudaSuccess)
         return cuda_status(e);
     if (!mark(2)) return MKV_ERR_CUDA;
-    if ((e = launch_compact_gather(g, S, cut, chunk, s.seq_lens, keep_stride, idx, K, V, K_out, V_out, status, st)) !=
-        cudaSuccess)
+    int32_t *idx_w = idx ? idx : region<int32_t>(ws, L.idx);
+    const int32_t idx_stride = idx ? keep_stride : g.t_max;
+    if ((e = launch_compact(g, S, cut, chunk, s.seq_lens, keep_stride, idx_w, idx_stride, status, st)) != cudaSuccess)
         return cuda_status(e);
     if (!mark(3)) return MKV_ERR_CUDA;
+    if (K_out &&
+        (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st)) != cudaSuccess)
+        return cuda_status(e);
+    if (!mark(4)) return MKV_ERR_CUDA;
     return MKV_OK;
 }
 
-constexpr int32_t kCompressStages = 3;
+constexpr int32_t kCompressStages = 4;
 
 }  // namespace
 
@@ -188,6 +214,8 @@ Layout make_layout(const Geometry &g)
     off += round_up((size_t)g.n_heads * g.nch * sizeof(int2), kAlign);
     L.kept = off;
     off += round_up((size_t)g.n_heads * sizeof(int32_t), kAlign);
+    L.idx = off;  // kept indices when the caller does not ask for them (row stride t_max)
+    off += round_up((size_t)g.n_heads * g.t_max * sizeof(int32_t), kAlign);
     L.total = off;
     return L;
 }
@@ -281,8 +309,9 @@ mkv_status mkv_compact(const float *S, const mkv_cut *cut, const void *K, const 
     uint32_t *status = region<uint32_t>(workspace, L.status);
     int2 *chunk = region<int2>(workspace, L.chunk);
     cudaError_t e = launch_chunk_offsets(g, S, cut, shape.seq_lens, ratio, n_keep, keep_stride, chunk, kept, status, st);
-    if (e == cudaSuccess)
-        e = launch_compact_gather(g, S, cut, chunk, shape.seq_lens, keep_stride, idx, K, V, K_out, V_out, status, st);
+    if (e == cudaSuccess) e = launch_compact(g, S, cut, chunk, shape.seq_lens, keep_stride, idx, keep_stride, status, st);
+    if (e == cudaSuccess && K_out)
+        e = launch_gather(g, idx, keep_stride, kept, keep_stride, K, V, K_out, V_out, status, st);
     return cuda_status(e);
 }
 
@@ -299,7 +328,16 @@ int32_t mkv_compress_num_stages(void) { return kCompressStages; }
 int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
 {
     if (check_shape(shape) != MKV_OK || window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE)) return -1;
-    return 0;
+    if (!g_single_pass_enabled.load(std::memory_order_relaxed)) return 0;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window);
+    const int grid = single_pass_grid((int)mode);
+    if (grid <= 0) return -1;
+    return grid >= g.pg.ppw ? 1 : 0;
+}
+
+int32_t mkv_set_single_pass(int32_t enable)
+{
+    return g_single_pass_enabled.exchange(enable ? 1 : 0);
 }
 
 mkv_status mkv_compress_profiled(const void *K, const void *V, mkv_shape shape, double ratio,

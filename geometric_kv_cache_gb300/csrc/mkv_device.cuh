@@ -25,6 +25,14 @@ __device__ __forceinline__ void st_v4(void *p, uint4 v)
     *reinterpret_cast<uint4 *>(p) = v;
 }
 
+// Streaming 16-byte store (evict-first: the compacted cache is not re-read
+// by this path).
+__device__ __forceinline__ void st_stream(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // Eight bf16 values of a 16-byte chunk, widened exactly to fp32.
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float f[8])
 {

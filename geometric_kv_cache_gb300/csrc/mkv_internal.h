@@ -45,7 +45,7 @@ struct Geometry {
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct Layout {
     size_t status = 0, partial = 0, gsum = 0, counters = 0, centroid = 0, score = 0, cut = 0, chunk = 0, kept = 0,
-           total = 0;
+           idx = 0, total = 0;
 };
 
 Geometry make_geometry(int32_t batch, int32_t heads, int32_t t_max, int32_t window);
@@ -63,6 +63,14 @@ cudaError_t launch_window_means(const PieceGeometry &g, const float *partial, co
                                 uint32_t *status, cudaStream_t st);
 cudaError_t launch_piece_scores(const PieceGeometry &g, const void *K, const float *C, const int32_t *seq_lens,
                                 int mode, float *S, uint32_t *status, cudaStream_t st);
+// CTAs the single-pass centroid + score kernel runs with on the current
+// device (0 on error); it is usable when this is at least g.ppw.
+int single_pass_grid(int mode);
+// Clears the arrival counters, then launches the single-pass kernel
+// cooperatively with `grid` CTAs.
+cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, const int32_t *seq_lens, int mode,
+                               float *partial, float *gsum, uint32_t *cnt, float *C, float *S, uint32_t *status,
+                               cudaStream_t st);
 // Radix select; when chunk_info != nullptr it also computes the per-chunk
 // output offsets and the kept counts (the fused path's fourth pass).
 cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_lens, double ratio,
@@ -72,9 +80,13 @@ cudaError_t launch_chunk_offsets(const Geometry &g, const float *S, const mkv_cu
                                  const int32_t *seq_lens, double ratio, const int32_t *n_keep,
                                  int32_t keep_stride, int2 *chunk_info, int32_t *kept,
                                  uint32_t *status, cudaStream_t st);
-cudaError_t launch_compact_gather(const Geometry &g, const float *S, const mkv_cut *cut,
-                                  const int2 *chunk_info, const int32_t *seq_lens, int32_t keep_stride,
-                                  int32_t *idx, const void *K, const void *V, void *K_out, void *V_out,
-                                  uint32_t *status, cudaStream_t st);
+// Ascending kept indices into idx[head * idx_stride + slot], slot < keep_stride.
+cudaError_t launch_compact(const Geometry &g, const float *S, const mkv_cut *cut, const int2 *chunk_info,
+                           const int32_t *seq_lens, int32_t keep_stride, int32_t *idx, int32_t idx_stride,
+                           uint32_t *status, cudaStream_t st);
+// K_out/V_out rows [head][j] = K/V[head][idx[head * idx_stride + j]] for j < kept[head].
+cudaError_t launch_gather(const Geometry &g, const int32_t *idx, int32_t idx_stride, const int32_t *kept,
+                          int32_t keep_stride, const void *K, const void *V, void *K_out, void *V_out,
+                          uint32_t *status, cudaStream_t st);
 
 }  // namespace mkv

@@ -30,8 +30,8 @@ namespace {
 
 constexpr int kStreamThreads = 256;            // centroid / score / gather CTAs
 constexpr int kSlots = kStreamThreads / 16;    // rows per CTA per load step
-constexpr int kUnroll = 4;                     // load steps in flight per lane
-constexpr int kSelectThreads = 1024;
+constexpr int kSelectThreads = 512;
+constexpr int kSelectSmemScores = 40960;  // heads up to this many tokens are selected from shared memory
 using namespace dev;
 
 // ------------------------------------------------------ a3: radix select --
@@ -80,17 +80,23 @@ __device__ int chunk_offsets_block(const float *srow, int T, mkv_cut cut, int nc
 // One CTA per head (persistent over heads). Three histogram passes over the
 // head's score keys (digits of 11, 11 and 10 bits, most significant first)
 // find the n_keep-th largest key and how many of its ties are kept; with
-// chunk_info it then computes the compaction offsets (fused path).
-__global__ void __launch_bounds__(kSelectThreads, 1)
+// chunk_info it then computes the compaction offsets (fused path). When the
+// launch gives dynamic shared memory for t_max scores (IN_SMEM), the head's
+// scores are copied there once and every pass reads shared memory; otherwise
+// the passes read global memory (L2), four loads in flight per thread.
+template <bool IN_SMEM>
+__global__ void __launch_bounds__(kSelectThreads, 2)
 k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int heads, int t_max,
          double ratio, const int32_t *__restrict__ n_keep, int keep_stride, int64_t n_heads,
          mkv_cut *__restrict__ cut_out, int2 *__restrict__ chunk_info, int nch_max,
          int32_t *__restrict__ kept_out, uint32_t *status)
 {
+    extern __shared__ __align__(16) float s_scores[];
     __shared__ uint32_t hist[2048];
     __shared__ uint32_t s_warp[32];
     __shared__ uint32_t s_digit, s_above;
     const int lane = threadIdx.x & 31;
+    constexpr int kUnroll = 4;
     for (int64_t head = blockIdx.x; head < n_heads; head += gridDim.x) {
         const int T = head_len(seq_lens, head, heads, t_max, status, threadIdx.x == 0);
         const int nk = n_keep ? n_keep[head] : num_keep_dev(T, ratio);
@@ -109,7 +115,20 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
             }
             continue;
         }
-        const float *srow = S + (size_t)head * t_max;
+        const float *grow = S + (size_t)head * t_max;
+        const float *srow = grow;
+        if (IN_SMEM) {
+            if ((t_max & 3) == 0) {  // 16-byte aligned rows
+                const float4 *g4 = reinterpret_cast<const float4 *>(grow);
+                float4 *s4 = reinterpret_cast<float4 *>(s_scores);
+                for (int i = threadIdx.x; i < T / 4; i += kSelectThreads) s4[i] = __ldcg(g4 + i);
+                for (int i = (T & ~3) + threadIdx.x; i < T; i += kSelectThreads) s_scores[i] = __ldcg(grow + i);
+            } else {
+                for (int i = threadIdx.x; i < T; i += kSelectThreads) s_scores[i] = __ldcg(grow + i);
+            }
+            __syncthreads();
+            srow = s_scores;
+        }
         uint32_t prefix = 0, pmask = 0;
         int need = nk;
         if (nk > 0) {
@@ -119,17 +138,21 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
                 const int nb = pass == 2 ? 1024 : 2048;
                 for (int i = threadIdx.x; i < nb; i += kSelectThreads) hist[i] = 0;
                 __syncthreads();
-                for (int base = 0; base < T; base += kSelectThreads) {
-                    const int t = base + threadIdx.x;
-                    bool v = t < T;
-                    uint32_t u = 0;
-                    if (v) {
-                        u = score_key(srow[t]);
-                        v = (u & pmask) == prefix;
+                for (int base = 0; base < T; base += kSelectThreads * kUnroll) {
+                    uint32_t u[kUnroll];
+#pragma unroll
+                    for (int k = 0; k < kUnroll; ++k) {
+                        const int t = base + k * kSelectThreads + threadIdx.x;
+                        u[k] = t < T ? score_key(srow[t]) : 0u;
                     }
-                    const uint32_t dig = v ? ((u >> shift) & (uint32_t)(nb - 1)) : 0xFFFFFFFFu;
-                    const uint32_t peers = __match_any_sync(kFull, dig);
-                    if (v && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], (uint32_t)__popc(peers));
+#pragma unroll
+                    for (int k = 0; k < kUnroll; ++k) {
+                        const int t = base + k * kSelectThreads + threadIdx.x;
+                        const bool v = t < T && (u[k] & pmask) == prefix;
+                        const uint32_t dig = v ? ((u[k] >> shift) & (uint32_t)(nb - 1)) : 0xFFFFFFFFu;
+                        const uint32_t peers = __match_any_sync(kFull, dig);
+                        if (v && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], (uint32_t)__popc(peers));
+                    }
                 }
                 __syncthreads();
                 // Thread i owns bins in descending order: bpt bins from nb-1-i*bpt down.
@@ -167,6 +190,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
                 if (kept_out) kept_out[head] = kept;
             }
         }
+        if (IN_SMEM) __syncthreads();  // s_scores is reused by the next head
     }
 }
 
@@ -200,22 +224,18 @@ k_chunk_offsets(const float *__restrict__ S, const mkv_cut *__restrict__ cuts,
     }
 }
 
-// ------------------------------------------------ a4 + a5: compact, gather --
+// ------------------------------------------------------- a4: compaction --
 
 // Item = (head, chunk of 4096 tokens). Each thread classifies 16 consecutive
-// tokens against the cut; two CTA scans give each kept token its tie rank and
-// its output slot; kept token ids go to shared memory (and idx), then
-// half-warps copy the kept K and V rows, 16 bytes per lane.
+// tokens against the cut; two CTA scans give each kept token its tie rank
+// and its output slot; each thread then writes its kept token ids, in
+// ascending order, to idx[head * idx_stride + slot].
 __global__ void __launch_bounds__(kStreamThreads)
-k_compact_gather(const float *__restrict__ S, const mkv_cut *__restrict__ cuts,
-                 const int2 *__restrict__ chunk_info, const int32_t *__restrict__ seq_lens, int heads,
-                 int t_max, int nch_max, int keep_stride, int64_t n_items, int32_t *__restrict__ idx,
-                 const uint8_t *__restrict__ K, const uint8_t *__restrict__ V, uint8_t *__restrict__ K_out,
-                 uint8_t *__restrict__ V_out, uint32_t *status)
+k_compact(const float *__restrict__ S, const mkv_cut *__restrict__ cuts, const int2 *__restrict__ chunk_info,
+          const int32_t *__restrict__ seq_lens, int heads, int t_max, int nch_max, int keep_stride, int64_t n_items,
+          int32_t *__restrict__ idx, int idx_stride, uint32_t *status)
 {
-    __shared__ int32_t tok[kCompactChunk];
     __shared__ uint32_t s_warp[kStreamThreads / 32];
-    const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int64_t head = item / nch_max;
         const int c = (int)(item - head * nch_max);
@@ -249,48 +269,66 @@ k_compact_gather(const float *__restrict__ S, const mkv_cut *__restrict__ cuts,
             if (rank < (uint32_t)cut.ties) keepm |= m & (~m + 1);
             ++rank;
         }
-        uint32_t n_chunk = 0;
-        const uint32_t kb = block_exclusive_scan<kStreamThreads>(__popc(keepm), s_warp, &n_chunk);
-        int32_t *idx_head = idx ? idx + head * keep_stride : nullptr;
+        const uint32_t kb = block_exclusive_scan<kStreamThreads>(__popc(keepm), s_warp, nullptr);
+        int32_t *idx_head = idx + head * idx_stride;
         uint32_t r = kb;
         for (uint32_t m = keepm; m; m &= m - 1, ++r) {
-            const int t = t0 + __ffs(m) - 1;
-            tok[r] = t;
             const int64_t slot = (int64_t)info.x + r;
-            if (slot >= 0 && slot < keep_stride) {
-                if (idx_head) idx_head[slot] = t;
-            } else {
+            if (slot >= 0 && slot < keep_stride) idx_head[slot] = t0 + __ffs(m) - 1;
+            else atomicOr(status, MKV_DEV_INTERNAL);
+        }
+    }
+}
+
+// ------------------------------------------------------------ a5: gather --
+
+// Item = (head, block of 64 output slots). Half-warps copy rows, 16 bytes per
+// lane: K_out[h][j] = K[h][idx[h][j]], V_out likewise, for j < kept[h]; four
+// rows of K and of V in flight per lane. No CTA barrier anywhere.
+constexpr int kGatherRows = 64;
+
+__global__ void __launch_bounds__(kStreamThreads)
+k_gather_rows(const int32_t *__restrict__ idx, int idx_stride, const int32_t *__restrict__ kept, int t_max,
+              int keep_stride, int blocks_per_head, int64_t n_items, const uint8_t *__restrict__ K,
+              const uint8_t *__restrict__ V, uint8_t *__restrict__ K_out, uint8_t *__restrict__ V_out,
+              uint32_t *status)
+{
+    const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int64_t head = item / blocks_per_head;
+        const int j0 = (int)(item - head * blocks_per_head) * kGatherRows;
+        const int n = min(kGatherRows, min(kept[head], keep_stride) - j0);
+        if (n <= 0) continue;
+        const int32_t *ih = idx + head * idx_stride + j0;
+        const size_t in_head = (size_t)head * t_max * kRowBytes + l16 * 16;
+        const size_t out_head = ((size_t)head * keep_stride + j0) * kRowBytes + l16 * 16;
+        uint4 kv[kGatherRows / kSlots], vv[kGatherRows / kSlots];
+        int src[kGatherRows / kSlots];
+#pragma unroll
+        for (int u = 0; u < kGatherRows / kSlots; ++u) {
+            const int j = u * kSlots + hw;
+            src[u] = j < n ? ih[j] : -1;
+            if (src[u] >= t_max) {
                 atomicOr(status, MKV_DEV_INTERNAL);
+                src[u] = -1;
             }
         }
-        __syncthreads();
-        if (K_out) {
-            const size_t in_head = (size_t)head * t_max * kRowBytes + l16 * 16;
-            const size_t out_head = ((size_t)head * keep_stride + info.x) * kRowBytes + l16 * 16;
-            const int n_rows = (int)min((int64_t)n_chunk, (int64_t)keep_stride - info.x);
-            for (int j0 = 0; j0 < n_rows; j0 += kSlots * kUnroll) {
-                uint4 kv[kUnroll], vv[kUnroll];
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int j = j0 + u * kSlots + hw;
-                    if (j < n_rows) {
-                        const size_t off = in_head + (size_t)tok[j] * kRowBytes;
-                        kv[u] = ld_stream(K + off);
-                        vv[u] = ld_stream(V + off);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int j = j0 + u * kSlots + hw;
-                    if (j < n_rows) {
-                        const size_t off = out_head + (size_t)j * kRowBytes;
-                        st_v4(K_out + off, kv[u]);
-                        st_v4(V_out + off, vv[u]);
-                    }
-                }
+        for (int u = 0; u < kGatherRows / kSlots; ++u) {
+            if (src[u] >= 0) {
+                const size_t off = in_head + (size_t)src[u] * kRowBytes;
+                kv[u] = ld_stream(K + off);
+                vv[u] = ld_stream(V + off);
             }
         }
-        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kGatherRows / kSlots; ++u) {
+            if (src[u] >= 0) {
+                const size_t off = out_head + (size_t)(u * kSlots + hw) * kRowBytes;
+                st_stream(K_out + off, kv[u]);
+                st_stream(V_out + off, vv[u]);
+            }
+        }
     }
 }
 
@@ -368,9 +406,18 @@ cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_
                           int32_t *kept, uint32_t *status, cudaStream_t st)
 {
     if (g.n_heads == 0) return cudaSuccess;
-    const int grid = grid_for(k_select, kSelectThreads, g.n_heads);
-    k_select<<<grid, kSelectThreads, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride,
-                                              g.n_heads, cut, chunk_info, g.nch, kept, status);
+    const size_t smem = (size_t)g.t_max * sizeof(float);
+    if (g.t_max <= kSelectSmemScores) {
+        cudaError_t e = cudaFuncSetAttribute(k_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const int grid = grid_for_items(reinterpret_cast<const void *>(k_select<true>), kSelectThreads, smem, g.n_heads);
+        k_select<true><<<grid, kSelectThreads, smem, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride,
+                                                            g.n_heads, cut, chunk_info, g.nch, kept, status);
+    } else {
+        const int grid = grid_for(k_select<false>, kSelectThreads, g.n_heads);
+        k_select<false><<<grid, kSelectThreads, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride,
+                                                         g.n_heads, cut, chunk_info, g.nch, kept, status);
+    }
     return cudaGetLastError();
 }
 
@@ -387,18 +434,30 @@ cudaError_t launch_chunk_offsets(const Geometry &g, const float *S, const mkv_cu
     return cudaGetLastError();
 }
 
-cudaError_t launch_compact_gather(const Geometry &g, const float *S, const mkv_cut *cut,
-                                  const int2 *chunk_info, const int32_t *seq_lens, int32_t keep_stride,
-                                  int32_t *idx, const void *K, const void *V, void *K_out, void *V_out,
-                                  uint32_t *status, cudaStream_t st)
+cudaError_t launch_compact(const Geometry &g, const float *S, const mkv_cut *cut, const int2 *chunk_info,
+                           const int32_t *seq_lens, int32_t keep_stride, int32_t *idx, int32_t idx_stride,
+                           uint32_t *status, cudaStream_t st)
 {
     const int64_t items = g.n_heads * g.nch;
     if (items == 0) return cudaSuccess;
-    const int grid = grid_for(k_compact_gather, kStreamThreads, items);
-    k_compact_gather<<<grid, kStreamThreads, 0, st>>>(
-        S, cut, chunk_info, seq_lens, g.heads, g.t_max, g.nch, keep_stride, items, idx,
-        static_cast<const uint8_t *>(K), static_cast<const uint8_t *>(V), static_cast<uint8_t *>(K_out),
-        static_cast<uint8_t *>(V_out), status);
+    const int grid = grid_for(k_compact, kStreamThreads, items);
+    k_compact<<<grid, kStreamThreads, 0, st>>>(S, cut, chunk_info, seq_lens, g.heads, g.t_max, g.nch, keep_stride,
+                                               items, idx, idx_stride, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const Geometry &g, const int32_t *idx, int32_t idx_stride, const int32_t *kept,
+                          int32_t keep_stride, const void *K, const void *V, void *K_out, void *V_out,
+                          uint32_t *status, cudaStream_t st)
+{
+    const int bph = (keep_stride + kGatherRows - 1) / kGatherRows;
+    const int64_t items = g.n_heads * bph;
+    if (items == 0) return cudaSuccess;
+    const int grid = grid_for(k_gather_rows, kStreamThreads, items);
+    k_gather_rows<<<grid, kStreamThreads, 0, st>>>(idx, idx_stride, kept, g.t_max, keep_stride, bph, items,
+                                                   static_cast<const uint8_t *>(K), static_cast<const uint8_t *>(V),
+                                                   static_cast<uint8_t *>(K_out), static_cast<uint8_t *>(V_out),
+                                                   status);
     return cudaGetLastError();
 }
 

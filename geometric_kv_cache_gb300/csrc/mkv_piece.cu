@@ -257,16 +257,18 @@ __device__ __forceinline__ void load_centroid(const float *cw, float c[16])
 }
 
 // Sum of n (<= kGroupPieces) consecutive 128-float records, record order,
-// dim d; all loads issued before the adds.
+// dim d; loads issued in batches of 8 ahead of their adds.
 __device__ __forceinline__ float ordered_sum(const float *first, int n, int d)
 {
-    float v[kGroupPieces];
-#pragma unroll
-    for (int j = 0; j < kGroupPieces; ++j) v[j] = j < n ? __ldcg(first + (int64_t)j * kHeadDim + d) : 0.f;
     float s = 0.f;
+    for (int j0 = 0; j0 < n; j0 += 8) {
+        float v[8];
 #pragma unroll
-    for (int j = 0; j < kGroupPieces; ++j)
-        if (j < n) s += v[j];
+        for (int j = 0; j < 8; ++j) v[j] = j0 + j < n ? __ldcg(first + (int64_t)(j0 + j) * kHeadDim + d) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j0 + j < n) s += v[j];
+    }
     return s;
 }
 
@@ -285,6 +287,19 @@ struct Pointers {
 // (this thread's two 16-byte chunks of each), loaded before use.
 constexpr int kBatch = 4;
 
+template <int N>
+__device__ __forceinline__ void load_rows(const uint8_t *base, int len, int i0, uint4 v[2 * N])
+{
+    const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+        const int r = slot + (i0 + u) * kRowSlots;
+        const uint8_t *row = base + (size_t)(r < len ? r : 0) * kRowBytes;
+        v[2 * u] = ld_stream(row + q * 16);
+        v[2 * u + 1] = ld_stream(row + 128 + q * 16);
+    }
+}
+
 __device__ __forceinline__ void load_batch(const uint8_t *base, int len, int i0, uint4 v[2 * kBatch])
 {
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
@@ -300,7 +315,7 @@ __device__ __forceinline__ void load_batch(const uint8_t *base, int len, int i0,
 // a1, first half: piece sums. The first batch of the next piece is loaded
 // before the current piece's CTA reduction, so the loads stay in flight
 // across piece boundaries.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 k_piece_sums(PieceGeometry g, Pointers P)
 {
     __shared__ float red[kWarps * kHeadDim];
@@ -337,16 +352,16 @@ k_piece_sums(PieceGeometry g, Pointers P)
     }
 }
 
-// a1, second half: window means, one warp per (head, window): groups of 32
-// pieces in piece order, then the groups in group order.
-__global__ void __launch_bounds__(256)
+// a1, second half: window means. One 128-thread CTA per (head, window),
+// thread d for dim d: the groups of 32 piece sums in piece order, then the
+// groups in group order, divided by the window's token count (the same order
+// as the single-pass kernel).
+__global__ void __launch_bounds__(kHeadDim)
 k_window_means(PieceGeometry g, Pointers P)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (gw >= g.n_heads * g.nwin_max) return;
-    const int64_t head = gw / g.nwin_max;
-    const int w = (int)(gw - head * g.nwin_max);
+    const int64_t win = blockIdx.x;
+    const int64_t head = win / g.nwin_max;
+    const int w = (int)(win - head * g.nwin_max);
     const int T = head_len(P.seq_lens, head, g.heads, g.t_max, P.status, false);
     if (T == 0) return;
     const int wl = window_len(T, g.window);
@@ -355,18 +370,12 @@ k_window_means(PieceGeometry g, Pointers P)
     const int wlen = (int)min((int64_t)wl, (int64_t)T - wstart);
     const int np = (wlen + g.piece_rows - 1) / g.piece_rows;
     const int ng = (np + kGroupPieces - 1) / kGroupPieces;
-    const float *pw = P.partial + ((head * g.nwin_max + w) * (int64_t)g.ppw) * kHeadDim;
-    float tot[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int gi = 0; gi < ng; ++gi) {
-        const int n = min(kGroupPieces, np - gi * kGroupPieces);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            tot[k] += ordered_sum(pw + (int64_t)gi * kGroupPieces * kHeadDim, n, lane * 4 + k);
-    }
-    float *cw = P.C + (head * g.nwin_max + w) * kHeadDim;
-    const float n = (float)wlen;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) cw[lane * 4 + k] = __fdiv_rn(tot[k], n);
+    const float *pw = P.partial + win * (int64_t)g.ppw * kHeadDim;
+    float tot = 0.f;
+    for (int gi = 0; gi < ng; ++gi)
+        tot += ordered_sum(pw + (int64_t)gi * kGroupPieces * kHeadDim, min(kGroupPieces, np - gi * kGroupPieces),
+                           threadIdx.x);
+    P.C[win * kHeadDim + threadIdx.x] = __fdiv_rn(tot, (float)wlen);
 }
 
 // a2: scores of every piece against its window's mean in C.
@@ -402,6 +411,386 @@ k_piece_scores(PieceGeometry g, Pointers P)
     }
 }
 
+// ------------------------------------------------- single-pass kernel --
+//
+// One read of K from HBM for both a1 and a2, with three warp roles:
+//  * a producer warp streams the CTA's pieces into a ring of kRing 16 KB
+//    shared-memory slots with bulk asynchronous copies (cp.async.bulk,
+//    completion on a "full" mbarrier per slot; the slot is refilled once its
+//    "empty" mbarrier has seen all 8 compute warps), so HBM reads stay in
+//    flight whatever the compute warps are doing;
+//  * 8 compute warps add each piece's rows up from shared memory (phase 1)
+//    and hand the per-warp sums to the sync warp; kLag pieces later they
+//    re-read that older piece's rows with 16-byte loads -- normally L2 hits,
+//    the rows were copied in a few microseconds earlier -- and score them
+//    against the window mean (phase 2);
+//  * a sync warp does all waiting on other CTAs: it publishes each piece sum
+//    (global record, release fence, arrival counter; the last arrival of a
+//    group of 32 pieces adds the group, the last group adds the window,
+//    divides, and raises the window's ready flag) and copies the window mean
+//    of each phase-2 piece into shared memory once that flag is up.
+// Hand-overs between roles go through double-buffered shared memory guarded
+// by mbarriers. The arithmetic is exactly that of k_piece_sums,
+// k_window_means and k_piece_scores, so both paths give the same bits.
+//
+// Progress: the kernel is launched cooperatively (all CTAs resident). A
+// window spans at most kMaxPiecesPerWindow consecutive items and every CTA
+// takes one item per round, so a window's pieces lie in at most two
+// consecutive rounds; the sync warp fetches the mean of round t - kLag
+// before publishing round t (or after, when phase 2 has caught up with the
+// CTA's own latest piece), so every wait depends only on earlier rounds. All
+// waits are still bounded by a timer: running out sets MKV_DEV_TIMEOUT, makes
+// every later wait give up at once, and leaves the affected scores unwritten.
+
+constexpr int kLag = 2;
+constexpr int kBatch2 = 4;  // phase-2 rows per lane in flight (L2 hits)
+constexpr int kRing = 4;
+constexpr uint32_t kStageBytes = kStageRows * kRowBytes;  // 16 KB
+constexpr int kFusedThreads = kThreads + 64;              // + producer warp + sync warp
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ bool timed_out(const uint32_t *status)
+{
+    return (ld_acquire(status) & MKV_DEV_TIMEOUT) != 0u;
+}
+
+// Wait (bounded) for completion `parity` of `bar`. Gives up at once if some
+// wait already timed out; on its own timeout it flags MKV_DEV_TIMEOUT.
+__device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status)
+{
+    const uint32_t b = smem_addr(bar);
+    const uint64_t t0 = global_ns();
+    for (uint32_t spin = 0;; ++spin) {
+        uint32_t done;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(done)
+            : "r"(b), "r"(parity)
+            : "memory");
+        if (done) return;
+        if ((spin & 63u) == 63u) {
+            if (timed_out(status)) return;
+            if (global_ns() - t0 > kWaitNs) {
+                atomicOr(status, MKV_DEV_TIMEOUT);
+                return;
+            }
+        }
+    }
+}
+
+// One thread: expect `bytes` on `bar` and start the copy global -> shared.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Compute warps only (the producer and sync warps never join).
+__device__ __forceinline__ void compute_barrier()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
+
+struct FusedPointers {
+    Pointers P;
+    float *gsum;    // [heads, nwin_max, ngroups_max, 128]
+    uint32_t *cnt;  // [heads, nwin_max, ngroups_max + 2]: group counters, window counter, ready flag
+};
+
+struct FusedShared {
+    uint8_t ring[kRing][kStageBytes];
+    float red[2][kWarps * kHeadDim];
+    float cbuf[2][kHeadDim];
+    uint64_t full[kRing], empty[kRing];
+    uint64_t redfull[2], redempty[2], cfull[2], cempty[2];
+};
+
+// Sum of n (<= kGroupPieces) consecutive 128-float records, record order,
+// for the four dims 4*lane .. 4*lane + 3 (loads in batches of 4).
+__device__ __forceinline__ float4 ordered_sum4(const float *first, int n, int lane)
+{
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < n; j0 += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[j] = j0 + j < n ? __ldcg(reinterpret_cast<const float4 *>(first + (int64_t)(j0 + j) * kHeadDim) + lane)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (j0 + j < n) {
+                s.x += v[j].x;
+                s.y += v[j].y;
+                s.z += v[j].z;
+                s.w += v[j].w;
+            }
+    }
+    return s;
+}
+
+// Sync warp: publish piece `pc` (item `item`) from red[b].
+__device__ __forceinline__ void publish(const Piece &pc, int64_t item, const PieceGeometry &g, const FusedPointers &F,
+                                        FusedShared &sh, int b, uint32_t use)
+{
+    const int lane = threadIdx.x & 31;
+    mbar_wait(&sh.redfull[b], use & 1u, F.P.status);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const float4 r = reinterpret_cast<const float4 *>(sh.red[b] + w * kHeadDim)[lane];
+        s.x += r.x;
+        s.y += r.y;
+        s.z += r.z;
+        s.w += r.w;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.redempty[b]);
+    const int64_t win = pc.head * g.nwin_max + pc.w;
+    float *pw = F.P.partial + win * (int64_t)g.ppw * kHeadDim;
+    reinterpret_cast<float4 *>(F.P.partial + item * kHeadDim)[lane] = s;
+    __threadfence();
+    __syncwarp();
+    uint32_t *cnt = F.cnt + win * (g.ngroups_max + 2);
+    const int ng = (pc.npieces + kGroupPieces - 1) / kGroupPieces;
+    const int gi = pc.p / kGroupPieces;
+    const int gsize = min(kGroupPieces, pc.npieces - gi * kGroupPieces);
+    uint32_t old = 0;
+    if (lane == 0) old = atomicAdd(&cnt[gi], 1u);
+    old = __shfl_sync(kFull, old, 0);
+    if (old != (uint32_t)(gsize - 1)) return;
+    // last piece of its group: the group's sum
+    __threadfence();
+    float *gw = F.gsum + win * (int64_t)g.ngroups_max * kHeadDim;
+    const float4 gs = ordered_sum4(pw + (int64_t)gi * kGroupPieces * kHeadDim, gsize, lane);
+    reinterpret_cast<float4 *>(gw + (int64_t)gi * kHeadDim)[lane] = gs;
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) old = atomicAdd(&cnt[g.ngroups_max], 1u);
+    old = __shfl_sync(kFull, old, 0);
+    if (old != (uint32_t)(ng - 1)) return;
+    // last group of its window: the window mean, then the ready flag
+    __threadfence();
+    const float4 t = ordered_sum4(gw, ng, lane);
+    const float n = (float)pc.wlen;
+    reinterpret_cast<float4 *>(F.P.C + win * kHeadDim)[lane] =
+        make_float4(__fdiv_rn(t.x, n), __fdiv_rn(t.y, n), __fdiv_rn(t.z, n), __fdiv_rn(t.w, n));
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) atomicExch(&cnt[g.ngroups_max + 1], 1u);
+}
+
+// Sync warp: wait for the window of `pc`, copy its mean into cbuf[b].
+__device__ __forceinline__ void fetch_mean(const Piece &pc, const PieceGeometry &g, const FusedPointers &F,
+                                           FusedShared &sh, int b, uint32_t use)
+{
+    const int lane = threadIdx.x & 31;
+    if (use > 0) mbar_wait(&sh.cempty[b], (use - 1) & 1u, F.P.status);
+    const int64_t win = pc.head * g.nwin_max + pc.w;
+    const uint32_t *ready = F.cnt + win * (g.ngroups_max + 2) + g.ngroups_max + 1;
+    if (lane == 0) {
+        const uint64_t t0 = global_ns();
+        while (ld_acquire(ready) == 0u) {
+            if (timed_out(F.P.status)) break;
+            if (global_ns() - t0 > kWaitNs) {
+                atomicOr(F.P.status, MKV_DEV_TIMEOUT);
+                break;
+            }
+            __nanosleep(64);
+        }
+    }
+    __syncwarp();
+    (void)ld_acquire(ready);  // order this lane's reads of the mean after the flag
+    reinterpret_cast<float4 *>(sh.cbuf[b])[lane] = __ldcg(reinterpret_cast<const float4 *>(F.P.C + win * kHeadDim) + lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.cfull[b]);
+}
+
+// Round structure shared by all roles: in round t the compute warps do
+// phase 1 of the CTA's t-th piece (while any is left) and then phase 2 of the
+// (t - kLag)-th (or, once phase 1 is exhausted, of the next pending one).
+template <int MODE>
+__global__ void __launch_bounds__(kFusedThreads, 2)
+k_single_pass(PieceGeometry g, FusedPointers F)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    FusedShared &sh = *reinterpret_cast<FusedShared *>(smem_raw);
+    const Pointers &P = F.P;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], kWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.redfull[b], 1);
+            mbar_init(&sh.redempty[b], 1);
+            mbar_init(&sh.cfull[b], 1);
+            mbar_init(&sh.cempty[b], 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const Steps st = make_steps(g);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == kWarps) {
+        // ---- producer: the phase-1 stages of every piece, in order
+        Cursor c = first_cursor(g, st, P.seq_lens, P.status);
+        uint32_t seq = 0;
+        for (; !c.done; advance(c, st, g, P.seq_lens, P.status)) {
+            for (int r0 = 0; r0 < c.pc.len; r0 += kStageRows, ++seq) {
+                const int s = (int)(seq % kRing);
+                if (seq >= kRing) mbar_wait(&sh.empty[s], ((seq / kRing) - 1) & 1u, P.status);
+                if (lane == 0) {
+                    const int rows = min(kStageRows, c.pc.len - r0);
+                    bulk_load(sh.ring[s], P.K + ((size_t)c.pc.head * g.t_max + c.pc.a + r0) * kRowBytes,
+                              (uint32_t)rows * kRowBytes, &sh.full[s]);
+                }
+                __syncwarp();
+            }
+        }
+        // stay resident until the copies still in flight have landed
+        for (uint32_t k = seq > kRing ? seq - kRing : 0; k < seq; ++k)
+            mbar_wait(&sh.full[k % kRing], (k / kRing) & 1u, P.status);
+        return;
+    }
+
+    Cursor c1 = first_cursor(g, st, P.seq_lens, P.status);  // phase-1 stream
+    Cursor c2 = c1;                                          // phase-2 stream, kLag behind
+    uint32_t u1 = 0, u2 = 0;                                 // pieces through phase 1 / phase 2
+    uint32_t seq = 0;                                        // ring stages consumed
+    const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
+    for (int t = 0; !c1.done || !c2.done; ++t) {
+        const bool do1 = !c1.done;
+        Piece p1;
+        int64_t item1 = 0;
+        if (do1) {
+            p1 = c1.pc;
+            item1 = cursor_item(c1, st);
+            advance(c1, st, g, P.seq_lens, P.status);
+        }
+        const bool do2 = !c2.done && (t >= kLag || c1.done);
+        Piece p2;
+        if (do2) p2 = c2.pc;
+        if (warp == kWarps + 1) {
+            // ---- sync warp. Normally the fetch for the older piece goes
+            // first (its window is complete by now). When phase 2 reaches this
+            // round's own piece, that piece must be published first.
+            if (do1 && do2 && u2 == u1) {
+                publish(p1, item1, g, F, sh, (int)(u1 & 1u), u1 >> 1);
+                fetch_mean(p2, g, F, sh, (int)(u2 & 1u), u2 >> 1);
+            } else {
+                if (do2) fetch_mean(p2, g, F, sh, (int)(u2 & 1u), u2 >> 1);
+                if (do1) publish(p1, item1, g, F, sh, (int)(u1 & 1u), u1 >> 1);
+            }
+        } else {
+            if (do1) {
+                // ---- phase 1: the piece sum from the ring (k_piece_sums order)
+                float acc[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+                for (int r0 = 0; r0 < p1.len; r0 += kStageRows, ++seq) {
+                    const int s = (int)(seq % kRing);
+                    mbar_wait(&sh.full[s], (seq / kRing) & 1u, P.status);
+                    const int rows = min(kStageRows, p1.len - r0);
+#pragma unroll
+                    for (int i = 0; i < kStageRows / kRowSlots; ++i) {
+                        const int r = slot + i * kRowSlots;
+                        if (r < rows) {
+                            const uint8_t *row = sh.ring[s] + r * kRowBytes;
+                            float f[16];
+                            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(row + q * 16), f);
+                            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(row + 128 + q * 16), f + 8);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[j] += f[j];
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.empty[s]);
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    acc[j] += __shfl_xor_sync(kFull, acc[j], 8);
+                    acc[j] += __shfl_xor_sync(kFull, acc[j], 16);
+                }
+                const int b = (int)(u1 & 1u);
+                if (u1 >= 2) mbar_wait(&sh.redempty[b], ((u1 >> 1) - 1) & 1u, P.status);
+                if (lane < 8) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        sh.red[b][warp * kHeadDim + q * 8 + j] = acc[j];
+                        sh.red[b][warp * kHeadDim + 64 + q * 8 + j] = acc[8 + j];
+                    }
+                }
+                compute_barrier();
+                if (threadIdx.x == 0) mbar_arrive(&sh.redfull[b]);
+            }
+            if (do2) {
+                // ---- phase 2: scores of the older piece against its window mean
+                const int b = (int)(u2 & 1u);
+                mbar_wait(&sh.cfull[b], (u2 >> 1) & 1u, P.status);
+                float c[16];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    c[j] = sh.cbuf[b][q * 8 + j];
+                    c[8 + j] = sh.cbuf[b][64 + q * 8 + j];
+                }
+                compute_barrier();
+                if (threadIdx.x == 0) mbar_arrive(&sh.cempty[b]);
+                const float nc = MODE == MKV_MODE_COSINE ? centroid_norm(c) : 0.f;
+                if (!timed_out(P.status)) {
+                    const uint8_t *base = P.K + ((size_t)p2.head * g.t_max + p2.a) * kRowBytes;
+                    float *srow = P.S + (size_t)p2.head * g.t_max + p2.a;
+                    const int nrows = (p2.len + kRowSlots - 1) / kRowSlots;
+                    for (int i0 = 0; i0 < nrows; i0 += kBatch2) {
+                        uint4 v[2 * kBatch2];
+                        load_rows<kBatch2>(base, p2.len, i0, v);
+#pragma unroll
+                        for (int u = 0; u < kBatch2; ++u) {
+                            const int r = slot + (i0 + u) * kRowSlots;
+                            float f[16];
+                            bf16x8_to_f32(v[2 * u], f);
+                            bf16x8_to_f32(v[2 * u + 1], f + 8);
+                            const float sc = score_of<MODE>(f, c, nc);
+                            if (r < p2.len && q == 0) srow[r] = sc;
+                        }
+                    }
+                }
+            }
+        }
+        if (do1) ++u1;
+        if (do2) {
+            ++u2;
+            advance(c2, st, g, P.seq_lens, P.status);
+        }
+    }
+}
+
 Pointers make_pointers(const void *K, const int32_t *seq_lens, float *partial, float *C, float *S, uint32_t *status)
 {
     Pointers P;
@@ -418,6 +807,34 @@ Pointers make_pointers(const void *K, const int32_t *seq_lens, float *partial, f
 
 // ------------------------------------------------------------- launchers --
 
+int single_pass_grid(int mode)
+{
+    const void *fn = mode == MKV_MODE_L2 ? reinterpret_cast<const void *>(k_single_pass<MKV_MODE_L2>)
+                                         : reinterpret_cast<const void *>(k_single_pass<MKV_MODE_COSINE>);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(FusedShared)) != cudaSuccess)
+        return 0;
+    return resident_grid(fn, kFusedThreads, sizeof(FusedShared));
+}
+
+cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, const int32_t *seq_lens, int mode,
+                               float *partial, float *gsum, uint32_t *cnt, float *C, float *S, uint32_t *status,
+                               cudaStream_t st)
+{
+    if (g.n_items == 0) return cudaSuccess;
+    const size_t cnt_bytes = (size_t)g.n_heads * g.nwin_max * (g.ngroups_max + 2) * sizeof(uint32_t);
+    cudaError_t e = cudaMemsetAsync(cnt, 0, cnt_bytes, st);
+    if (e != cudaSuccess) return e;
+    FusedPointers F;
+    F.P = make_pointers(K, seq_lens, partial, C, S, status);
+    F.gsum = gsum;
+    F.cnt = cnt;
+    PieceGeometry gg = g;
+    void *args[] = {&gg, &F};
+    const void *fn = mode == MKV_MODE_L2 ? reinterpret_cast<const void *>(k_single_pass<MKV_MODE_L2>)
+                                         : reinterpret_cast<const void *>(k_single_pass<MKV_MODE_COSINE>);
+    return cudaLaunchCooperativeKernel(fn, dim3((unsigned)grid), dim3(kFusedThreads), args, sizeof(FusedShared), st);
+}
+
 cudaError_t launch_piece_sums(const PieceGeometry &g, const void *K, const int32_t *seq_lens, float *partial,
                               uint32_t *status, cudaStream_t st)
 {
@@ -432,7 +849,7 @@ cudaError_t launch_window_means(const PieceGeometry &g, const float *partial, co
 {
     const int64_t wins = g.n_heads * g.nwin_max;
     if (wins == 0) return cudaSuccess;
-    k_window_means<<<(unsigned)((wins + 7) / 8), 256, 0, st>>>(
+    k_window_means<<<(unsigned)wins, kHeadDim, 0, st>>>(
         g, make_pointers(nullptr, seq_lens, const_cast<float *>(partial), C, nullptr, status));
     return cudaGetLastError();
 }

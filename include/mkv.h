@@ -157,10 +157,10 @@ mkv_status mkv_compress(const void *K, const void *V, mkv_shape shape, double ra
                         void *K_out, void *V_out, int32_t *idx, int32_t *kept,
                         void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
-/* Number of stages mkv_compress runs (for mkv_compress_profiled): 3 --
- * centroid + score (a1, a2: one single-pass kernel, or three kernels when a
- * window has more 128-token pieces than the GPU holds resident CTAs), top-k
- * select with compaction offsets (a3, a4), compaction + gather (a4, a5). */
+/* Number of stages mkv_compress runs (for mkv_compress_profiled): 4 --
+ * centroid + score (a1, a2: three kernels, or one single-pass kernel when
+ * enabled), top-k select with compaction offsets (a3, a4), compaction into
+ * ascending indices (a4), row gather of K and V (a5). */
 int32_t mkv_compress_num_stages(void);
 
 /* 1 if mkv_compress on the current device reads K once (the single-pass
@@ -168,6 +168,13 @@ int32_t mkv_compress_num_stages(void);
  * three-kernel path (K read twice); -1 on a bad argument or CUDA error.
  * Both give bit-identical results. */
 int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode);
+
+/* Allow (1) or forbid (0, the default) the single-pass centroid + score
+ * kernel in mkv_compress, process-wide; returns the previous setting. The
+ * single-pass kernel reads K from HBM once instead of twice but waits on
+ * other CTAs for every window's mean; on GB300 it is currently slower than
+ * the three-kernel path, so it is off unless asked for. */
+int32_t mkv_set_single_pass(int32_t enable);
 
 /* mkv_compress, recording caller-created CUDA events (cudaEvent_t handles
  * passed as void*) on `stream`: events[i] right before stage i and
@@ -206,7 +213,7 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
  * image. Every GPU that loads the library holds that array until the process
  * exits, whether or not this call is used.
  *   Limits: the problem must fit, i.e. mkv_workspace_size(shape, window) <=
- *   MKV_NOALLOC_SCRATCH_BYTES (about 7.4M token rows, heads x t_max, per call at window 0).
+ *   MKV_NOALLOC_SCRATCH_BYTES (about 6.6M token rows, heads x t_max, per call at window 0).
  *   Larger problems return MKV_ERR_UNSUPPORTED and enqueue nothing; split
  *   them into several calls over groups of heads.
  *   Set-up: the first call on a device, with that device current, looks up the

@@ -60,6 +60,6 @@ def test_path_bytes_follow_the_stated_formula():
     heads, T, d, keep = 256, 16384, 128, 8192
     assert nb["tokens"] == heads * T
     assert nb["path"] == heads * (4 * T * d + 8 * keep * d)
-    assert nb["compact_gather"] == heads * 8 * keep * d
+    assert nb["gather"] == heads * 8 * keep * d
     assert nb["centroid_score"] == heads * (2 * 2 * T * d + 4 * T)
     assert bench.path_bytes([16384] * 32, 8, 0.5, k_reads=1)["centroid_score"] == heads * (2 * T * d + 4 * T)

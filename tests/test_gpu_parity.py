@@ -395,7 +395,39 @@ def test_full_size_phi4():
     _full_size("phi4-kv-t128k")
 
 
-def test_single_pass_query():
+def test_single_pass_is_used_for_the_bench_shape_when_enabled():
+    # 256-token pieces, at most 64 per window: the single-pass kernel runs
+    # whenever it is enabled and the resident grid holds that many CTAs.
     small = mkv.MkvShape(32, 8, 16384, 128, None)
-    assert mkv.mkv_compress_single_pass(small, 0, "l2") in (0, 1)
+    prev = mkv.mkv_set_single_pass(True)
+    try:
+        assert mkv.mkv_compress_single_pass(small, 0, "l2") == 1
+        assert mkv.mkv_compress_single_pass(small, 4096, "cosine") == 1
+    finally:
+        mkv.mkv_set_single_pass(prev)
+    assert mkv.mkv_compress_single_pass(small, 0, "l2") == (1 if prev else 0)
     assert mkv.load().mkv_compress_single_pass(small, -1, 0) == -1
+
+
+def test_single_pass_and_three_kernel_paths_give_the_same_bits():
+    # mkv_centroid + mkv_score (three kernels) against mkv_compress (single
+    # pass): same centroids order, same scores, hence same selection.
+    w = synthkv.WORKLOADS["ragged-b8-llama-kv-t8k-32k"].scaled("sp", layers=2, batch=3, heads=4, t_max=20000,
+                                                                 t_min=100)
+    K, V, lens = synthkv.make_kv(w, seed=9, device=DEV)
+    prev = mkv.mkv_set_single_pass(True)
+    try:
+        runs = []
+        for mode, window in (("l2", 0), ("cosine", 0), ("l2", 3000), ("cosine", 777)):
+            assert mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode) == 1
+            runs.append((mode, window, _run_fused(K, V, 0.4, mode, window, lens)))
+    finally:
+        mkv.mkv_set_single_pass(prev)
+    for mode, window, a in runs:
+        b, st = _run_steps(K, V, 0.4, mode, window, lens)
+        assert a[4] == 0 and st == 0
+        assert torch.equal(a[3], b.kept)
+        for h in range(w.n_heads):
+            r, hh = divmod(h, w.heads)
+            n = int(a[3][r, hh])
+            assert torch.equal(a[2][r, hh, :n], b.idx[r, hh, :n])
