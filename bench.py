@@ -45,7 +45,7 @@ METRIC = "KV tokens scored+compacted/sec and achieved HBM GB/s vs ~8 TB/s peak"
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-STAGES = ["centroid_score", "select", "compact", "gather"]
+STAGES = ["piece_sums", "window_means", "piece_scores", "select", "compact", "gather"]
 
 
 # ----------------------------------------------------------------- helpers --
@@ -69,10 +69,11 @@ def keep_count(T: int, ratio: float) -> int:
 
 def path_bytes(lens, heads: int, ratio: float, d: int = 128, k_reads: int = 2) -> dict:
     """Algorithmic bytes of one step as the metric defines them: K read twice
-    (centroid, score) plus the kept K and V rows read and written. Per stage:
-    the bytes each stage must move -- the centroid+score stage reads K
-    ``k_reads`` times (1 for the single-pass kernel) and writes 4 B of score
-    per token; the gather reads and writes the kept K and V rows."""
+    (centroid, score) plus the kept K and V rows read and written. Per kernel:
+    the bytes each must move -- piece sums read K, scores read K and write 4 B
+    per token, the gather reads and writes the kept K and V rows (with
+    k_reads == 1, the single-pass kernel in stage 0 reads K once and writes
+    the scores)."""
     tok = sum(int(t) for t in lens) * heads
     keep = sum(keep_count(int(t), ratio) for t in lens) * heads
     k_read = 2 * tok * d
@@ -80,7 +81,9 @@ def path_bytes(lens, heads: int, ratio: float, d: int = 128, k_reads: int = 2) -
         "tokens": tok,
         "kept": keep,
         "path": 2 * k_read + 8 * keep * d,
-        "centroid_score": k_reads * k_read + 4 * tok,
+        "piece_sums": k_read + (4 * tok if k_reads == 1 else 0),
+        "window_means": 0,
+        "piece_scores": 0 if k_reads == 1 else k_read + 4 * tok,
         "select": 0,
         "compact": 0,
         "gather": 8 * keep * d,
@@ -252,6 +255,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     lens_list = lens.cpu().tolist()
     single = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
+    select_emits = T <= 40960  # select writes the kept indices itself (no compaction kernel)
     nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single == 1 else 2)
 
     def step():
@@ -370,7 +374,7 @@ def run_ours(args):
         "stages_ms": dict(zip(STAGES, stage_ms)),
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (4 if single == 1 else 6),
+        "gpu_launches": args.steps * ((2 if single == 1 else 4) + (0 if select_emits else 1)),
         "clocks": clocks.summary(),
     }
     if world > 1:

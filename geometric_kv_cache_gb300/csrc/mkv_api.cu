@@ -126,8 +126,8 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     };
     cudaError_t e = cudaSuccess;
     if (!mark(0)) return MKV_ERR_CUDA;
-    // a1 + a2: one pass over K when every window's pieces fit the resident
-    // grid; else piece sums, window means, scores (same arithmetic, same bits)
+    // a1 + a2: one pass over K when enabled and every window's pieces fit the
+    // resident grid; else piece sums, window means, scores (same bits)
     const int grid = g_single_pass_enabled.load(std::memory_order_relaxed) ? single_pass_grid((int)mode) : 0;
     bool single = grid > 0 && grid >= g.pg.ppw;
     if (single) {
@@ -138,30 +138,38 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
             single = false;
             e = cudaSuccess;
         }
+        if (e != cudaSuccess) return cuda_status(e);
+        if (!mark(1) || !mark(2) || !mark(3)) return MKV_ERR_CUDA;
     }
     if (!single) {
-        e = launch_piece_sums(g.pg, K, s.seq_lens, partial, status, st);
-        if (e == cudaSuccess) e = launch_window_means(g.pg, partial, s.seq_lens, C, status, st);
-        if (e == cudaSuccess) e = launch_piece_scores(g.pg, K, C, s.seq_lens, (int)mode, S, status, st);
+        if ((e = launch_piece_sums(g.pg, K, s.seq_lens, partial, status, st)) != cudaSuccess) return cuda_status(e);
+        if (!mark(1)) return MKV_ERR_CUDA;
+        if ((e = launch_window_means(g.pg, partial, s.seq_lens, C, status, st)) != cudaSuccess) return cuda_status(e);
+        if (!mark(2)) return MKV_ERR_CUDA;
+        if ((e = launch_piece_scores(g.pg, K, C, s.seq_lens, (int)mode, S, status, st)) != cudaSuccess)
+            return cuda_status(e);
+        if (!mark(3)) return MKV_ERR_CUDA;
     }
-    if (e != cudaSuccess) return cuda_status(e);
-    if (!mark(1)) return MKV_ERR_CUDA;
-    if ((e = launch_select(g, S, s.seq_lens, ratio, n_keep, keep_stride, cut, chunk, kept_w, status, st)) != cudaSuccess)
-        return cuda_status(e);
-    if (!mark(2)) return MKV_ERR_CUDA;
+    // a3 (+ a4 when the head's scores fit shared memory), then a4, a5
     int32_t *idx_w = idx ? idx : region<int32_t>(ws, L.idx);
     const int32_t idx_stride = idx ? keep_stride : g.t_max;
-    if ((e = launch_compact(g, S, cut, chunk, s.seq_lens, keep_stride, idx_w, idx_stride, status, st)) != cudaSuccess)
+    const bool emit = select_emits_indices(g);
+    if ((e = launch_select(g, S, s.seq_lens, ratio, n_keep, keep_stride, cut, emit ? nullptr : chunk, kept_w,
+                           emit ? idx_w : nullptr, idx_stride, status, st)) != cudaSuccess)
         return cuda_status(e);
-    if (!mark(3)) return MKV_ERR_CUDA;
+    if (!mark(4)) return MKV_ERR_CUDA;
+    if (!emit &&
+        (e = launch_compact(g, S, cut, chunk, s.seq_lens, keep_stride, idx_w, idx_stride, status, st)) != cudaSuccess)
+        return cuda_status(e);
+    if (!mark(5)) return MKV_ERR_CUDA;
     if (K_out &&
         (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st)) != cudaSuccess)
         return cuda_status(e);
-    if (!mark(4)) return MKV_ERR_CUDA;
+    if (!mark(6)) return MKV_ERR_CUDA;
     return MKV_OK;
 }
 
-constexpr int32_t kCompressStages = 4;
+constexpr int32_t kCompressStages = 6;
 
 }  // namespace
 
@@ -288,7 +296,7 @@ mkv_status mkv_select_topk(const float *S, mkv_shape shape, double ratio, const 
     const Layout L = make_step_layout(g);
     if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
     if (empty(shape)) return MKV_OK;
-    return cuda_status(launch_select(g, S, shape.seq_lens, ratio, n_keep, -1, cut, nullptr, nullptr,
+    return cuda_status(launch_select(g, S, shape.seq_lens, ratio, n_keep, -1, cut, nullptr, nullptr, nullptr, 0,
                                      region<uint32_t>(workspace, L.status), reinterpret_cast<cudaStream_t>(stream)));
 }
 

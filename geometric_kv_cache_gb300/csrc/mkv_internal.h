@@ -71,11 +71,15 @@ int single_pass_grid(int mode);
 cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, const int32_t *seq_lens, int mode,
                                float *partial, float *gsum, uint32_t *cnt, float *C, float *S, uint32_t *status,
                                cudaStream_t st);
-// Radix select; when chunk_info != nullptr it also computes the per-chunk
-// output offsets and the kept counts (the fused path's fourth pass).
+// Radix select. With idx (only when select_emits_indices(g): the head's
+// scores fit in shared memory) it also writes the ascending kept indices to
+// idx[head * idx_stride + slot] and the kept counts (no compaction kernel
+// needed); else with chunk_info it computes the per-chunk output offsets and
+// the kept counts for k_compact (the fused path's fourth pass).
+bool select_emits_indices(const Geometry &g);
 cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_lens, double ratio,
                           const int32_t *n_keep, int32_t keep_stride, mkv_cut *cut, int2 *chunk_info,
-                          int32_t *kept, uint32_t *status, cudaStream_t st);
+                          int32_t *kept, int32_t *idx, int32_t idx_stride, uint32_t *status, cudaStream_t st);
 cudaError_t launch_chunk_offsets(const Geometry &g, const float *S, const mkv_cut *cut,
                                  const int32_t *seq_lens, double ratio, const int32_t *n_keep,
                                  int32_t keep_stride, int2 *chunk_info, int32_t *kept,

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kSelectThreads, 2)
 k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int heads, int t_max,
          double ratio, const int32_t *__restrict__ n_keep, int keep_stride, int64_t n_heads,
          mkv_cut *__restrict__ cut_out, int2 *__restrict__ chunk_info, int nch_max,
-         int32_t *__restrict__ kept_out, uint32_t *status)
+         int32_t *__restrict__ kept_out, int32_t *__restrict__ idx, int idx_stride, uint32_t *status)
 {
     extern __shared__ __align__(16) float s_scores[];
     __shared__ uint32_t hist[2048];
@@ -183,7 +183,46 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
         cut.key = prefix;
         cut.ties = need;
         if (threadIdx.x == 0) cut_out[head] = cut;
-        if (chunk_info) {
+        if (idx) {
+            // Emit the kept indices in ascending order straight from the
+            // scores in hand: rounds of 16 consecutive tokens per thread, two
+            // CTA scans per round (tie rank, output slot), counts carried
+            // across rounds.
+            uint32_t kept = 0, ties_before = 0;
+            int32_t *idx_head = idx + head * idx_stride;
+            for (int a = 0; a < T && nk > 0; a += kSelectThreads * 16) {
+                const int t0 = a + threadIdx.x * 16;
+                uint32_t gtm = 0, eqm = 0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = t0 + j;
+                    if (t < T) {
+                        const uint32_t u = score_key(srow[t]);
+                        gtm |= (uint32_t)(u > cut.key) << j;
+                        eqm |= (uint32_t)(u == cut.key) << j;
+                    }
+                }
+                uint32_t eq_total = 0;
+                uint32_t rank = ties_before + block_exclusive_scan<kSelectThreads>(__popc(eqm), s_warp, &eq_total);
+                uint32_t keepm = gtm;
+                for (uint32_t m = eqm; m; m &= m - 1) {
+                    if (rank < (uint32_t)cut.ties) keepm |= m & (~m + 1);
+                    ++rank;
+                }
+                uint32_t k_total = 0;
+                uint32_t slot = kept + block_exclusive_scan<kSelectThreads>(__popc(keepm), s_warp, &k_total);
+                for (uint32_t m = keepm; m; m &= m - 1, ++slot) {
+                    if (slot < (uint32_t)keep_stride) idx_head[slot] = t0 + __ffs(m) - 1;
+                    else atomicOr(status, MKV_DEV_INTERNAL);
+                }
+                kept += k_total;
+                ties_before += eq_total;
+            }
+            if (threadIdx.x == 0) {
+                if ((int)kept != nk) atomicOr(status, MKV_DEV_INTERNAL);
+                if (kept_out) kept_out[head] = (int32_t)kept;
+            }
+        } else if (chunk_info) {
             const int kept = nk > 0 ? chunk_offsets_block(srow, T, cut, nch_max, chunk_info + head * nch_max, s_warp) : 0;
             if (threadIdx.x == 0) {
                 if (kept != nk) atomicOr(status, MKV_DEV_INTERNAL);
@@ -401,9 +440,11 @@ int grid_for(Kern kernel, int threads, int64_t items)
 
 // ------------------------------------------------------------- launchers --
 
+bool select_emits_indices(const Geometry &g) { return g.t_max <= kSelectSmemScores; }
+
 cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_lens, double ratio,
                           const int32_t *n_keep, int32_t keep_stride, mkv_cut *cut, int2 *chunk_info,
-                          int32_t *kept, uint32_t *status, cudaStream_t st)
+                          int32_t *kept, int32_t *idx, int32_t idx_stride, uint32_t *status, cudaStream_t st)
 {
     if (g.n_heads == 0) return cudaSuccess;
     const size_t smem = (size_t)g.t_max * sizeof(float);
@@ -412,11 +453,13 @@ cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_
         if (e != cudaSuccess) return e;
         const int grid = grid_for_items(reinterpret_cast<const void *>(k_select<true>), kSelectThreads, smem, g.n_heads);
         k_select<true><<<grid, kSelectThreads, smem, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride,
-                                                            g.n_heads, cut, chunk_info, g.nch, kept, status);
+                                                            g.n_heads, cut, chunk_info, g.nch, kept, idx, idx_stride,
+                                                            status);
     } else {
         const int grid = grid_for(k_select<false>, kSelectThreads, g.n_heads);
         k_select<false><<<grid, kSelectThreads, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride,
-                                                         g.n_heads, cut, chunk_info, g.nch, kept, status);
+                                                         g.n_heads, cut, chunk_info, g.nch, kept, idx, idx_stride,
+                                                         status);
     }
     return cudaGetLastError();
 }

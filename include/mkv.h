@@ -157,10 +157,13 @@ mkv_status mkv_compress(const void *K, const void *V, mkv_shape shape, double ra
                         void *K_out, void *V_out, int32_t *idx, int32_t *kept,
                         void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
-/* Number of stages mkv_compress runs (for mkv_compress_profiled): 4 --
- * centroid + score (a1, a2: three kernels, or one single-pass kernel when
- * enabled), top-k select with compaction offsets (a3, a4), compaction into
- * ascending indices (a4), row gather of K and V (a5). */
+/* Number of stages mkv_compress_profiled brackets with events: 6, one per
+ * kernel -- piece sums (a1), window means (a1), scores (a2), top-k select
+ * (a3; also emits the kept indices when a head's scores fit in shared
+ * memory, t_max <= 40960), compaction into ascending indices (a4; empty when
+ * select emitted them), row gather of K and V (a5). With the single-pass
+ * kernel enabled and in use, stage 0 is that kernel and stages 1-2 are
+ * empty. */
 int32_t mkv_compress_num_stages(void);
 
 /* 1 if mkv_compress on the current device reads K once (the single-pass

@@ -120,7 +120,7 @@ def test_step_calls_reject_bad_arguments():
     events = (ctypes.c_void_p * 2)(vp(A), vp(A))
     assert lib.mkv_compress_profiled(vp(A), vp(A), shp, 0.5, None, 0, 0, 512, vp(A), vp(A), None, None, vp(A), big,
                                      None, events, 2) == mkv.MKV_ERR_INVALID_ARG
-    assert mkv.mkv_compress_num_stages() == 4
+    assert mkv.mkv_compress_num_stages() == 6
 
 
 def test_status_strings():

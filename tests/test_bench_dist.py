@@ -61,5 +61,6 @@ def test_path_bytes_follow_the_stated_formula():
     assert nb["tokens"] == heads * T
     assert nb["path"] == heads * (4 * T * d + 8 * keep * d)
     assert nb["gather"] == heads * 8 * keep * d
-    assert nb["centroid_score"] == heads * (2 * 2 * T * d + 4 * T)
-    assert bench.path_bytes([16384] * 32, 8, 0.5, k_reads=1)["centroid_score"] == heads * (2 * T * d + 4 * T)
+    assert nb["piece_sums"] == heads * 2 * T * d
+    assert nb["piece_scores"] == heads * (2 * T * d + 4 * T)
+    assert bench.path_bytes([16384] * 32, 8, 0.5, k_reads=1)["piece_sums"] == heads * (2 * T * d + 4 * T)
