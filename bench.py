@@ -27,6 +27,7 @@ is the max over ranks and ``value`` counts all ranks' tokens.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -449,7 +450,11 @@ def main(argv=None):
     if args.traffic_json and os.path.exists(args.traffic_json):
         with open(args.traffic_json) as f:
             t = json.load(f)
-        if t.get("workload") == args.workload and not args.layers:
+        # counters only count while the kernels they were taken on are unchanged
+        src = os.path.join(ROOT, "geometric_kv_cache_gb300", "csrc", "mkv_kernels.cu")
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        if t.get("workload") == args.workload and not args.layers and t.get("kernel_source_sha256_16") == sha:
             args.traffic = t.get("bytes_per_launch")
     if args.impl == "reference":
         run_reference(args)

@@ -378,16 +378,20 @@ k_window_means(PieceGeometry g, Pointers P)
     P.C[win * kHeadDim + threadIdx.x] = __fdiv_rn(tot, (float)wlen);
 }
 
-// a2: scores of every piece against its window's mean in C.
+// a2: scores of every piece against its window's mean in C. As in
+// k_piece_sums, the next piece's first batch is loaded as soon as the current
+// piece's last batch is consumed, before the next centroid is read.
 template <int MODE>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 k_piece_scores(PieceGeometry g, Pointers P)
 {
     const Steps st = make_steps(g);
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
     Cursor cur = first_cursor(g, st, P.seq_lens, P.status);
+    uint4 v[2 * kBatch];
+    if (!cur.done) load_batch(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * kRowBytes, cur.pc.len, 0, v);
     while (!cur.done) {
-        const Piece &pc = cur.pc;
+        const Piece pc = cur.pc;
         const uint8_t *base = P.K + ((size_t)pc.head * g.t_max + pc.a) * kRowBytes;
         float *srow = P.S + (size_t)pc.head * g.t_max + pc.a;
         float c[16];
@@ -395,8 +399,6 @@ k_piece_scores(PieceGeometry g, Pointers P)
         const float nc = MODE == MKV_MODE_COSINE ? centroid_norm(c) : 0.f;
         const int nrows = (pc.len + kRowSlots - 1) / kRowSlots;
         for (int i0 = 0; i0 < nrows; i0 += kBatch) {
-            uint4 v[2 * kBatch];
-            load_batch(base, pc.len, i0, v);
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int r = slot + (i0 + u) * kRowSlots;
@@ -406,8 +408,11 @@ k_piece_scores(PieceGeometry g, Pointers P)
                 const float s = score_of<MODE>(f, c, nc);
                 if (r < pc.len && q == 0) srow[r] = s;
             }
+            if (i0 + kBatch < nrows) load_batch(base, pc.len, i0 + kBatch, v);
         }
+        // the next piece's first batch goes out before its centroid is read
         advance(cur, st, g, P.seq_lens, P.status);
+        if (!cur.done) load_batch(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * kRowBytes, cur.pc.len, 0, v);
     }
 }
 
