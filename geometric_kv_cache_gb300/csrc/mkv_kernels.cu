@@ -77,9 +77,10 @@ __device__ int chunk_offsets_block(const float *srow, int T, mkv_cut cut, int nc
     return kept;
 }
 
-// One CTA per head (persistent over heads). Three histogram passes over the
-// head's score keys (digits of 11, 11 and 10 bits, most significant first)
-// find the n_keep-th largest key and how many of its ties are kept; with
+// One CTA per head (persistent over heads). Histogram passes over the head's
+// score keys (digits of up to 11 bits, most significant first, starting at
+// the highest bit where the head's smallest and largest keys differ) find
+// the n_keep-th largest key and how many of its ties are kept; with
 // chunk_info it then computes the compaction offsets (fused path). When the
 // launch gives dynamic shared memory for t_max scores (IN_SMEM), the head's
 // scores are copied there once and every pass reads shared memory; otherwise
@@ -95,6 +96,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
     __shared__ uint32_t hist[2048];
     __shared__ uint32_t s_warp[32];
     __shared__ uint32_t s_digit, s_above;
+    __shared__ uint32_t s_min[kSelectThreads / 32], s_max[kSelectThreads / 32];
     const int lane = threadIdx.x & 31;
     constexpr int kUnroll = 4;
     for (int64_t head = blockIdx.x; head < n_heads; head += gridDim.x) {
@@ -132,48 +134,84 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
         uint32_t prefix = 0, pmask = 0;
         int need = nk;
         if (nk > 0) {
+            // Smallest and largest key of the head: bits above their highest
+            // differing bit are common to every key, so the digits start
+            // there and the first pass spreads over all its bins (no
+            // warp-aggregation needed for the histogram atomics).
+            uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+            for (int t = threadIdx.x; t < T; t += kSelectThreads) {
+                const uint32_t u = score_key(srow[t]);
+                kmin = min(kmin, u);
+                kmax = max(kmax, u);
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+                kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+            }
+            if (lane == 0) {
+                s_min[threadIdx.x >> 5] = kmin;
+                s_max[threadIdx.x >> 5] = kmax;
+            }
+            __syncthreads();
+            kmin = s_min[0];
+            kmax = s_max[0];
+            for (int w = 1; w < kSelectThreads / 32; ++w) {
+                kmin = min(kmin, s_min[w]);
+                kmax = max(kmax, s_max[w]);
+            }
+            __syncthreads();
+            if (kmin == kmax) {  // every key equal: the cut is that key, the first nk tokens are kept
+                prefix = kmin;
+            } else {
+                const int hb = 31 - __clz(kmin ^ kmax);  // highest differing bit
+                pmask = hb == 31 ? 0u : ~((2u << hb) - 1u);
+                prefix = kmin & pmask;
 #pragma unroll 1
-            for (int pass = 0; pass < 3; ++pass) {
-                const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-                const int nb = pass == 2 ? 1024 : 2048;
-                for (int i = threadIdx.x; i < nb; i += kSelectThreads) hist[i] = 0;
-                __syncthreads();
-                for (int base = 0; base < T; base += kSelectThreads * kUnroll) {
-                    uint32_t u[kUnroll];
+                for (int lo = hb + 1; lo > 0;) {
+                    const int width = min(11, lo);
+                    const int shift = lo - width;
+                    const int nb = 1 << width;
+                    for (int i = threadIdx.x; i < nb; i += kSelectThreads) hist[i] = 0;
+                    __syncthreads();
+                    for (int base = 0; base < T; base += kSelectThreads * kUnroll) {
+                        uint32_t u[kUnroll];
 #pragma unroll
-                    for (int k = 0; k < kUnroll; ++k) {
-                        const int t = base + k * kSelectThreads + threadIdx.x;
-                        u[k] = t < T ? score_key(srow[t]) : 0u;
-                    }
+                        for (int k = 0; k < kUnroll; ++k) {
+                            const int t = base + k * kSelectThreads + threadIdx.x;
+                            u[k] = t < T ? score_key(srow[t]) : 0u;
+                        }
 #pragma unroll
-                    for (int k = 0; k < kUnroll; ++k) {
-                        const int t = base + k * kSelectThreads + threadIdx.x;
-                        const bool v = t < T && (u[k] & pmask) == prefix;
-                        const uint32_t dig = v ? ((u[k] >> shift) & (uint32_t)(nb - 1)) : 0xFFFFFFFFu;
-                        const uint32_t peers = __match_any_sync(kFull, dig);
-                        if (v && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], (uint32_t)__popc(peers));
+                        for (int k = 0; k < kUnroll; ++k) {
+                            const int t = base + k * kSelectThreads + threadIdx.x;
+                            if (t < T && (u[k] & pmask) == prefix) atomicAdd(&hist[(u[k] >> shift) & (uint32_t)(nb - 1)], 1u);
+                        }
                     }
-                }
-                __syncthreads();
-                // Thread i owns bins in descending order: bpt bins from nb-1-i*bpt down.
-                const int bpt = nb / kSelectThreads;
-                const int hi = nb - 1 - threadIdx.x * bpt;
-                uint32_t local = 0;
-                for (int j = 0; j < bpt; ++j) local += hist[hi - j];
-                uint32_t above = block_exclusive_scan<kSelectThreads>(local, s_warp, nullptr);
-                for (int j = 0; j < bpt; ++j) {
-                    const uint32_t h = hist[hi - j];
-                    if (above < (uint32_t)need && (uint32_t)need <= above + h) {
-                        s_digit = (uint32_t)(hi - j);
-                        s_above = above;
+                    __syncthreads();
+                    // Thread i owns bpt bins in descending order from nb-1-i*bpt.
+                    const int bpt = nb > kSelectThreads ? nb / kSelectThreads : 1;
+                    const int hi = nb - 1 - (int)threadIdx.x * bpt;
+                    uint32_t local = 0;
+                    if (hi >= 0)
+                        for (int j = 0; j < bpt; ++j) local += hist[hi - j];
+                    uint32_t above = block_exclusive_scan<kSelectThreads>(local, s_warp, nullptr);
+                    if (hi >= 0) {
+                        for (int j = 0; j < bpt; ++j) {
+                            const uint32_t h = hist[hi - j];
+                            if (above < (uint32_t)need && (uint32_t)need <= above + h) {
+                                s_digit = (uint32_t)(hi - j);
+                                s_above = above;
+                            }
+                            above += h;
+                        }
                     }
-                    above += h;
+                    __syncthreads();
+                    prefix |= s_digit << shift;
+                    pmask |= (uint32_t)(nb - 1) << shift;
+                    need -= (int)s_above;
+                    __syncthreads();
+                    lo = shift;
                 }
-                __syncthreads();
-                prefix |= s_digit << shift;
-                pmask |= (uint32_t)(nb - 1) << shift;
-                need -= (int)s_above;
-                __syncthreads();
             }
         } else {
             prefix = kNoneKey;
