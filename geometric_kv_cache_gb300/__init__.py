@@ -45,7 +45,8 @@ EXPORTED = (
     "mkv_num_keep", "mkv_num_windows", "mkv_workspace_size", "mkv_centroid", "mkv_score",
     "mkv_select_topk", "mkv_compact", "mkv_compress", "mkv_compress_num_stages",
     "mkv_compress_profiled", "mkv_compress_host", "mkv_device_status", "mkv_status_string",
-    "mkv_compress_noalloc", "mkv_compress_single_pass", "mkv_set_single_pass",
+    "mkv_compress_noalloc", "mkv_compress_single_pass", "mkv_set_single_pass", "mkv_layer_budgets",
+    "mkv_inject_stalled_windows",
 )
 
 
@@ -93,6 +94,8 @@ def load(build_if_missing: bool = True):
             "mkv_compress_num_stages": (i32, []),
             "mkv_compress_single_pass": (i32, [MkvShape, i32, i32]),
             "mkv_set_single_pass": (i32, [i32]),
+            "mkv_layer_budgets": (i32, [vp, i32, f64, f64, ctypes.c_int64, vp, vp]),
+            "mkv_inject_stalled_windows": (i32, [vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
             "mkv_compress_profiled": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp,
                                             ctypes.POINTER(vp), i32]),
             "mkv_compress_host": (i32, [vp, vp, vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp,
@@ -172,6 +175,23 @@ def mkv_set_single_pass(enable: bool) -> bool:
     """Allow or forbid the single-pass centroid + score kernel; returns the
     previous setting."""
     return bool(load().mkv_set_single_pass(1 if enable else 0))
+
+
+def mkv_layer_budgets(sensitivity, r: float, gamma: float, total: int, cap):
+    """Per-layer kept-token budgets (host helper). Returns (status, budgets)
+    with budgets an int32 list of one entry per layer; status 1 means the caps
+    absorb the whole total."""
+    import array
+    sv = array.array("d", [float(x) for x in sensitivity])
+    cp = array.array("i", [int(x) for x in cap])
+    out = array.array("i", [0] * len(sv))
+    if len(cp) != len(sv):
+        raise ValueError("one cap per layer is required")
+    st = load().mkv_layer_budgets(ctypes.c_void_p(sv.buffer_info()[0]), len(sv), float(r), float(gamma), int(total),
+                                  ctypes.c_void_p(cp.buffer_info()[0]), ctypes.c_void_p(out.buffer_info()[0]))
+    if st < 0:
+        raise MKVError(MKV_ERR_INVALID_ARG, "mkv_layer_budgets")
+    return int(st), list(out)
 
 
 def workspace_for(K: torch.Tensor, window: int = 0, seq_lens=None) -> torch.Tensor:
@@ -257,6 +277,17 @@ def mkv_compress_noalloc(K, V, ratio, mode, window, keep_stride, K_out, V_out, i
                                        _MODES[mode], int(window), int(keep_stride), _ptr(K_out), _ptr(V_out),
                                        _ptr(idx), _ptr(kept), _ptr(status_out), _stream(stream)),
            "mkv_compress_noalloc")
+
+
+def mkv_inject_stalled_windows(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, workspace,
+                               seq_lens=None, stream=None):
+    """Failure injection: the single-pass kernel with no window ever
+    completing; every wait between CTAs must run out (MKV_DEV_TIMEOUT)."""
+    _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens)
+    _check(load().mkv_inject_stalled_windows(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _MODES[mode],
+                                             int(window), int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx),
+                                             _ptr(kept), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mkv_inject_stalled_windows")
 
 
 def mkv_device_status(workspace, stream=None) -> int:

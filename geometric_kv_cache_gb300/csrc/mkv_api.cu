@@ -6,7 +6,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
+#include <vector>
 
 #include "mkv_internal.h"
 
@@ -102,7 +104,7 @@ mkv_status check_outputs(const mkv_shape &s, double ratio, const int32_t *n_keep
 mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio, const int32_t *n_keep,
                         mkv_mode mode, int32_t window, int32_t keep_stride, void *K_out, void *V_out,
                         int32_t *idx, int32_t *kept, void *ws, size_t ws_bytes, cudaStream_t st,
-                        void *const *events)
+                        void *const *events, bool stall_windows = false)
 {
     mkv_status rc = check_shape(s);
     if (rc != MKV_OK) return rc;
@@ -128,11 +130,13 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     if (!mark(0)) return MKV_ERR_CUDA;
     // a1 + a2: one pass over K when enabled and every window's pieces fit the
     // resident grid; else piece sums, window means, scores (same bits)
-    const int grid = g_single_pass_enabled.load(std::memory_order_relaxed) ? single_pass_grid((int)mode) : 0;
+    const int grid =
+        (stall_windows || g_single_pass_enabled.load(std::memory_order_relaxed)) ? single_pass_grid((int)mode) : 0;
     bool single = grid > 0 && grid >= g.pg.ppw;
+    if (stall_windows && !single) return MKV_ERR_UNSUPPORTED;
     if (single) {
         e = launch_single_pass(g.pg, grid, K, s.seq_lens, (int)mode, partial, region<float>(ws, L.gsum),
-                               region<uint32_t>(ws, L.counters), C, S, status, st);
+                               region<uint32_t>(ws, L.counters), C, S, status, st, stall_windows);
         if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer CTAs fit right now
             (void)cudaGetLastError();
             single = false;
@@ -341,6 +345,73 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
     const int grid = single_pass_grid((int)mode);
     if (grid <= 0) return -1;
     return grid >= g.pg.ppw ? 1 : 0;
+}
+
+mkv_status mkv_inject_stalled_windows(const void *K, const void *V, mkv_shape shape, double ratio, mkv_mode mode,
+                                      int32_t window, int32_t keep_stride, void *K_out, void *V_out, int32_t *idx,
+                                      int32_t *kept, void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    return run_compress(K, V, shape, ratio, nullptr, mode, window, keep_stride, K_out, V_out, idx, kept, workspace,
+                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr, true);
+}
+
+int32_t mkv_layer_budgets(const double *sensitivity, int32_t layers, double r, double gamma, int64_t total,
+                          const int32_t *cap, int32_t *budget)
+{
+    if (!sensitivity || !cap || !budget || layers <= 0 || !(r > 0.0) || !(gamma >= 1.0) || total < 0) return -1;
+    double smin = sensitivity[0], smax = sensitivity[0];
+    int64_t capsum = 0;
+    for (int32_t l = 0; l < layers; ++l) {
+        if (sensitivity[l] != sensitivity[l] || cap[l] < 0) return -1;
+        smin = fmin(smin, sensitivity[l]);
+        smax = fmax(smax, sensitivity[l]);
+        capsum += cap[l];
+    }
+    if (total >= capsum) {  // the caps absorb everything
+        for (int32_t l = 0; l < layers; ++l) budget[l] = cap[l];
+        return total == capsum ? 0 : 1;
+    }
+    std::vector<double> w(layers), x(layers);
+    std::vector<char> full(layers, 0);
+    for (int32_t l = 0; l < layers; ++l) {
+        const double sn = smax > smin ? (sensitivity[l] - smin) / (smax - smin) : 0.0;
+        w[l] = fmin(fmax(pow(r, sn), 1.0 / gamma), gamma);
+    }
+    // water-filling: budgets proportional to w, layers that reach their cap
+    // are fixed there and the rest of the total is shared by the others
+    for (;;) {
+        double rest = (double)total, wsum = 0.0;
+        for (int32_t l = 0; l < layers; ++l) {
+            if (full[l]) rest -= cap[l];
+            else wsum += w[l];
+        }
+        const double lambda = rest / wsum;
+        bool grew = false;
+        for (int32_t l = 0; l < layers; ++l)
+            if (!full[l] && lambda * w[l] >= (double)cap[l]) full[l] = 1, grew = true;
+        if (!grew) {
+            for (int32_t l = 0; l < layers; ++l) x[l] = full[l] ? (double)cap[l] : lambda * w[l];
+            break;
+        }
+    }
+    // integers by largest remainder, lower layer first among equal remainders
+    int64_t assigned = 0;
+    for (int32_t l = 0; l < layers; ++l) {
+        budget[l] = (int32_t)floor(x[l]);
+        assigned += budget[l];
+    }
+    std::vector<int32_t> order(layers);
+    for (int32_t l = 0; l < layers; ++l) order[l] = l;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int32_t a, int32_t b) { return x[a] - budget[a] > x[b] - budget[b]; });
+    for (int32_t k = 0; k < layers && assigned < total; ++k) {
+        const int32_t l = order[k];
+        if (budget[l] < cap[l]) {
+            ++budget[l];
+            ++assigned;
+        }
+    }
+    return 0;
 }
 
 int32_t mkv_set_single_pass(int32_t enable)

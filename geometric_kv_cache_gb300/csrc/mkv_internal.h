@@ -68,9 +68,10 @@ cudaError_t launch_piece_scores(const PieceGeometry &g, const void *K, const flo
 int single_pass_grid(int mode);
 // Clears the arrival counters, then launches the single-pass kernel
 // cooperatively with `grid` CTAs.
+// With stall_windows (failure injection) no window ever becomes ready.
 cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, const int32_t *seq_lens, int mode,
                                float *partial, float *gsum, uint32_t *cnt, float *C, float *S, uint32_t *status,
-                               cudaStream_t st);
+                               cudaStream_t st, bool stall_windows = false);
 // Radix select. With idx (only when select_emits_indices(g): the head's
 // scores fit in shared memory) it also writes the ascending kept indices to
 // idx[head * idx_stride + slot] and the kept counts (no compaction kernel

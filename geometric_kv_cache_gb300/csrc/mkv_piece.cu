@@ -452,7 +452,7 @@ constexpr int kBatch2 = 4;  // phase-2 rows per lane in flight (L2 hits)
 constexpr int kRing = 4;
 constexpr uint32_t kStageBytes = kStageRows * kRowBytes;  // 16 KB
 constexpr int kFusedThreads = kThreads + 64;              // + producer warp + sync warp
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s bound on every wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
@@ -481,9 +481,12 @@ __device__ __forceinline__ bool timed_out(const uint32_t *status)
     return (ld_acquire(status) & MKV_DEV_TIMEOUT) != 0u;
 }
 
-// Wait (bounded) for completion `parity` of `bar`. Gives up at once if some
-// wait already timed out; on its own timeout it flags MKV_DEV_TIMEOUT.
-__device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status)
+// Wait (bounded) for completion `parity` of `bar`; on its own timeout it flags
+// MKV_DEV_TIMEOUT. An abortable wait (a hand-over between warps of this CTA)
+// also gives up at once when some other wait already timed out. Waits on the
+// ring's copy barriers are not abortable: a bulk copy always lands, and no
+// slot may be reused or abandoned while its copy is in flight.
+__device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status, bool abortable = true)
 {
     const uint32_t b = smem_addr(bar);
     const uint64_t t0 = global_ns();
@@ -496,7 +499,7 @@ __device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, uint32
             : "memory");
         if (done) return;
         if ((spin & 63u) == 63u) {
-            if (timed_out(status)) return;
+            if (abortable && timed_out(status)) return;
             if (global_ns() - t0 > kWaitNs) {
                 atomicOr(status, MKV_DEV_TIMEOUT);
                 return;
@@ -670,7 +673,7 @@ k_single_pass(PieceGeometry g, FusedPointers F)
         for (; !c.done; advance(c, st, g, P.seq_lens, P.status)) {
             for (int r0 = 0; r0 < c.pc.len; r0 += kStageRows, ++seq) {
                 const int s = (int)(seq % kRing);
-                if (seq >= kRing) mbar_wait(&sh.empty[s], ((seq / kRing) - 1) & 1u, P.status);
+                if (seq >= kRing) mbar_wait(&sh.empty[s], ((seq / kRing) - 1) & 1u, P.status, false);
                 if (lane == 0) {
                     const int rows = min(kStageRows, c.pc.len - r0);
                     bulk_load(sh.ring[s], P.K + ((size_t)c.pc.head * g.t_max + c.pc.a + r0) * kRowBytes,
@@ -681,7 +684,7 @@ k_single_pass(PieceGeometry g, FusedPointers F)
         }
         // stay resident until the copies still in flight have landed
         for (uint32_t k = seq > kRing ? seq - kRing : 0; k < seq; ++k)
-            mbar_wait(&sh.full[k % kRing], (k / kRing) & 1u, P.status);
+            mbar_wait(&sh.full[k % kRing], (k / kRing) & 1u, P.status, false);
         return;
     }
 
@@ -721,7 +724,7 @@ k_single_pass(PieceGeometry g, FusedPointers F)
                 for (int j = 0; j < 16; ++j) acc[j] = 0.f;
                 for (int r0 = 0; r0 < p1.len; r0 += kStageRows, ++seq) {
                     const int s = (int)(seq % kRing);
-                    mbar_wait(&sh.full[s], (seq / kRing) & 1u, P.status);
+                    mbar_wait(&sh.full[s], (seq / kRing) & 1u, P.status, false);
                     const int rows = min(kStageRows, p1.len - r0);
 #pragma unroll
                     for (int i = 0; i < kStageRows / kRowSlots; ++i) {
@@ -823,12 +826,20 @@ int single_pass_grid(int mode)
 
 cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, const int32_t *seq_lens, int mode,
                                float *partial, float *gsum, uint32_t *cnt, float *C, float *S, uint32_t *status,
-                               cudaStream_t st)
+                               cudaStream_t st, bool stall_windows)
 {
     if (g.n_items == 0) return cudaSuccess;
-    const size_t cnt_bytes = (size_t)g.n_heads * g.nwin_max * (g.ngroups_max + 2) * sizeof(uint32_t);
-    cudaError_t e = cudaMemsetAsync(cnt, 0, cnt_bytes, st);
+    const size_t stride = (size_t)(g.ngroups_max + 2) * sizeof(uint32_t);
+    const size_t wins = (size_t)g.n_heads * g.nwin_max;
+    cudaError_t e = cudaMemsetAsync(cnt, 0, wins * stride, st);
     if (e != cudaSuccess) return e;
+    if (stall_windows) {
+        // failure injection: group and window counters start far past any
+        // group size, so no window ever completes and every window wait must
+        // run out; the ready flags stay 0
+        e = cudaMemset2DAsync(cnt, stride, 0x40, (size_t)(g.ngroups_max + 1) * sizeof(uint32_t), wins, st);
+        if (e != cudaSuccess) return e;
+    }
     FusedPointers F;
     F.P = make_pointers(K, seq_lens, partial, C, S, status);
     F.gsum = gsum;

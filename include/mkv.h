@@ -172,6 +172,22 @@ int32_t mkv_compress_num_stages(void);
  * Both give bit-identical results. */
 int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode);
 
+/* Per-layer kept-token budgets for the n_keep array (host helper). The
+ * budget mapping of "RippleKV" (gist.science explainer of arXiv 2608.08684),
+ * Methodology section 2, Sensitivity-Guided Budget Allocation: the layer
+ * sensitivities are normalised to [0, 1] (all equal -> 0), mapped to
+ * multipliers w = r^s, clipped to [1/gamma, gamma], and scaled so that the
+ * budgets add up to `total`. Readings where that text is silent: layer l
+ * cannot keep more than cap[l] tokens (allocation min(cap, lambda * w) with
+ * lambda meeting the total, i.e. water-filling); real budgets become integers
+ * by largest remainder, lower layer first among equal remainders. Writes
+ * budget[layers]; returns 0, 1 when the caps cannot absorb the total (every
+ * layer then gets its cap), -1 on bad input (r <= 0, gamma < 1, NaN,
+ * negative cap or total). The profiling that yields the sensitivities needs
+ * a model and is not part of this library. */
+int32_t mkv_layer_budgets(const double *sensitivity, int32_t layers, double r, double gamma, int64_t total,
+                          const int32_t *cap, int32_t *budget);
+
 /* Allow (1) or forbid (0, the default) the single-pass centroid + score
  * kernel in mkv_compress, process-wide; returns the previous setting. The
  * single-pass kernel reads K from HBM once instead of twice but waits on
@@ -234,6 +250,18 @@ mkv_status mkv_compress_noalloc(const void *K, const void *V, mkv_shape shape, d
                                 const int32_t *n_keep, mkv_mode mode, int32_t window, int32_t keep_stride,
                                 void *K_out, void *V_out, int32_t *idx, int32_t *kept, uint32_t *status_out,
                                 mkv_stream_t stream);
+
+/* Failure injection for tests of the single-pass kernel's bounded waits (no
+ * counterpart in the paper). Runs mkv_compress with the single-pass centroid
+ * + score kernel, but with every window's arrival counters started past any
+ * group size, so no window mean is ever published: each wait between CTAs
+ * runs out after its time bound (about 1 s), MKV_DEV_TIMEOUT is set in the
+ * status word, the remaining waits give up at once, the kernels finish and
+ * the context stays usable. The outputs are not meaningful. Returns
+ * MKV_ERR_UNSUPPORTED when the single-pass kernel cannot run this shape. */
+mkv_status mkv_inject_stalled_windows(const void *K, const void *V, mkv_shape shape, double ratio, mkv_mode mode,
+                                      int32_t window, int32_t keep_stride, void *K_out, void *V_out, int32_t *idx,
+                                      int32_t *kept, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
 /* Synchronise `stream`, read the status word of `workspace` into *bits (may
  * be NULL) and reset it to zero. MKV_OK if it was zero, MKV_ERR_DEVICE if

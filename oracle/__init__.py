@@ -78,6 +78,10 @@ def _load():
         lib.oracle_compress_heads.restype = i32
         lib.oracle_compress_heads.argtypes = [vp, vp, i64, i64, i64, vp, f64, i32, i64, i64,
                                               vp, vp, vp, vp]
+        lib.oracle_layer_budgets.restype = i32
+        lib.oracle_layer_budgets.argtypes = [vp, i32, f64, f64, i64, vp, vp]
+        lib.oracle_compress_head_n.restype = i64
+        lib.oracle_compress_head_n.argtypes = [vp, vp, i64, i64, i64, i32, i64, vp, vp, vp, vp, vp]
         _lib = lib
         return lib
 
@@ -197,3 +201,32 @@ def compress_heads(K, V, lens, ratio: float, mode="l2", window: int = 0, keep_st
     if rc != 0:
         raise ValueError("oracle_compress_heads failed")
     return idx[:, :keep_stride], kept, ko[:, :keep_stride], vo[:, :keep_stride]
+
+
+def layer_budgets(sensitivity, r: float, gamma: float, total: int, cap):
+    """Per-layer kept-token budgets (RippleKV budget mapping). Returns
+    (status, budgets int32 [L]); status 1 means the caps absorb the total."""
+    sv = np.ascontiguousarray(sensitivity, dtype=np.float64)
+    cp = np.ascontiguousarray(cap, dtype=np.int32)
+    out = np.zeros(sv.shape[0], dtype=np.int32)
+    st = _load().oracle_layer_budgets(_ptr(sv), sv.shape[0], float(r), float(gamma), int(total), _ptr(cp), _ptr(out))
+    if st < 0:
+        raise ValueError("oracle_layer_budgets: bad input")
+    return int(st), out
+
+
+def compress_head_n(K, V, n_keep: int, mode="l2", window: int = 0):
+    """All steps for one head keeping exactly n_keep tokens."""
+    k, v = _bits(K), _bits(V)
+    T, d = k.shape
+    C = np.zeros((max(num_windows(T, window), 1), d), dtype=np.float64)
+    S = np.zeros(max(T, 1), dtype=np.float64)
+    n = int(n_keep)
+    idx = np.zeros(max(n, 1), dtype=np.int32)
+    ko = np.zeros((max(n, 1), d), dtype=np.uint16)
+    vo = np.zeros((max(n, 1), d), dtype=np.uint16)
+    got = _load().oracle_compress_head_n(_ptr(k), _ptr(v), T, d, n, _MODES[mode], int(window), _ptr(C), _ptr(S),
+                                         _ptr(idx), _ptr(ko), _ptr(vo))
+    if got != n:
+        raise ValueError("oracle_compress_head_n failed")
+    return {"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}

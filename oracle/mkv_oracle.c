@@ -215,3 +215,96 @@ int oracle_compress_heads(const uint16_t *K, const uint16_t *V, int64_t n_heads,
     free(S);
     return rc;
 }
+
+/* Per-layer kept-token budgets, "RippleKV" (gist.science explainer of arXiv
+ * 2608.08684), Methodology section 2, Sensitivity-Guided Budget Allocation:
+ * layer sensitivities are normalised to [0, 1], mapped to multipliers
+ * w = r^s, clipped to [1/gamma, gamma], and scaled so that the layer budgets
+ * add up to the global budget. Readings where the text is silent: all-equal
+ * sensitivities normalise to 0; a layer's budget cannot exceed its tokens
+ * cap[l] -- the allocation is min(cap, lambda * w) with lambda chosen so the
+ * total is met (found here by bisection); real budgets become integers by
+ * largest remainder (ties to the lower layer). Returns 0, 1 when the caps
+ * cannot absorb the total (every layer gets its cap), -1 on bad input. */
+static double oracle_alloc_sum(const double *w, const int32_t *cap, int32_t L, double lam)
+{
+    double sum = 0.0;
+    for (int32_t l = 0; l < L; ++l) {
+        double x = lam * w[l];
+        sum += x < (double)cap[l] ? x : (double)cap[l];
+    }
+    return sum;
+}
+
+int oracle_layer_budgets(const double *sens, int32_t L, double r, double gamma, int64_t total,
+                         const int32_t *cap, int32_t *budget)
+{
+    if (L <= 0 || !(r > 0.0) || !(gamma >= 1.0) || total < 0) return -1;
+    double smin = sens[0], smax = sens[0];
+    int64_t capsum = 0;
+    for (int32_t l = 0; l < L; ++l) {
+        if (isnan(sens[l]) || cap[l] < 0) return -1;
+        if (sens[l] < smin) smin = sens[l];
+        if (sens[l] > smax) smax = sens[l];
+        capsum += cap[l];
+    }
+    if (total >= capsum) {
+        for (int32_t l = 0; l < L; ++l) budget[l] = cap[l];
+        return total == capsum ? 0 : 1;
+    }
+    double *w = (double *)malloc((size_t)L * sizeof(double));
+    double *x = (double *)malloc((size_t)L * sizeof(double));
+    if (!w || !x) { free(w); free(x); return -1; }
+    for (int32_t l = 0; l < L; ++l) {
+        double s = smax > smin ? (sens[l] - smin) / (smax - smin) : 0.0;
+        double m = pow(r, s);
+        if (m < 1.0 / gamma) m = 1.0 / gamma;
+        if (m > gamma) m = gamma;
+        w[l] = m;
+    }
+    /* lambda by bisection: the allocated sum is nondecreasing in lambda */
+    double lo = 0.0, hi = 1.0;
+    while (oracle_alloc_sum(w, cap, L, hi) < (double)total) hi *= 2.0;
+    for (int it = 0; it < 200; ++it) {
+        double mid = 0.5 * (lo + hi);
+        if (oracle_alloc_sum(w, cap, L, mid) < (double)total) lo = mid; else hi = mid;
+    }
+    int64_t assigned = 0;
+    for (int32_t l = 0; l < L; ++l) {
+        double v = hi * w[l];
+        x[l] = v < (double)cap[l] ? v : (double)cap[l];
+        budget[l] = (int32_t)floor(x[l]);
+        assigned += budget[l];
+    }
+    /* largest remainder: one more token to the layers with the largest
+     * fractional part, lower index first among equals */
+    while (assigned < total) {
+        int32_t best = -1;
+        double bestf = -1.0;
+        for (int32_t l = 0; l < L; ++l) {
+            double f = x[l] - (double)budget[l];
+            if (budget[l] < cap[l] && f > bestf) { bestf = f; best = l; }
+        }
+        if (best < 0) break;
+        budget[best] += 1;
+        x[best] = (double)budget[best];  /* its remainder is used */
+        assigned += 1;
+    }
+    free(w);
+    free(x);
+    return 0;
+}
+
+/* Steps 1-4 for one head with an explicit kept count (per-layer budgets). */
+int64_t oracle_compress_head_n(const uint16_t *K, const uint16_t *V, int64_t T, int64_t d, int64_t n_keep,
+                               int mode, int64_t window, double *C, double *S, int32_t *idx,
+                               uint16_t *K_out, uint16_t *V_out)
+{
+    if (n_keep < 0 || n_keep > T) return -1;
+    oracle_centroids(K, T, d, window, C);
+    oracle_scores(K, T, d, window, mode, C, S);
+    if (oracle_select(S, T, n_keep, idx) != 0) return -1;
+    if (K_out) oracle_gather(K, d, idx, n_keep, K_out);
+    if (V_out) oracle_gather(V, d, idx, n_keep, V_out);
+    return n_keep;
+}

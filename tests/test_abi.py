@@ -127,3 +127,26 @@ def test_status_strings():
     for s in range(6):
         assert mkv.mkv_status_string(s).startswith("MKV_")
     assert "unknown" in mkv.mkv_status_string(99)
+
+
+def test_layer_budgets_match_the_oracle():
+    import json
+    import numpy as np
+    with open(os.path.join(ROOT, "tests", "golden", "budget_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        st, b = mkv.mkv_layer_budgets(c["s"], c["r"], c["gamma"], c["total"], c["cap"])
+        assert (st, b) == (c.get("status", 0), c["budget"]), c
+    rng = np.random.default_rng(23)
+    for _ in range(300):
+        L = int(rng.integers(1, 40))
+        s = rng.normal(size=L)
+        r, gamma = float(np.exp(rng.normal())), float(1 + rng.exponential(3))
+        cap = rng.integers(0, 5000, size=L)
+        total = int(rng.integers(0, max(1, cap.sum()) + 100))
+        st, b = mkv.mkv_layer_budgets(s, r, gamma, total, cap)
+        st_o, b_o = oracle.layer_budgets(s, r, gamma, total, cap)
+        assert st == st_o and b == b_o.tolist()
+    for bad in ((0.0, 2.0), (2.0, 0.5), (float("nan"), 2.0)):
+        with pytest.raises(mkv.MKVError):
+            mkv.mkv_layer_budgets([0, 1], bad[0], bad[1], 10, [10, 10])

@@ -431,3 +431,53 @@ def test_single_pass_and_three_kernel_paths_give_the_same_bits():
             r, hh = divmod(h, w.heads)
             n = int(a[3][r, hh])
             assert torch.equal(a[2][r, hh, :n], b.idx[r, hh, :n])
+
+
+def test_per_layer_budgets_end_to_end():
+    # Per-layer kept counts from the budget mapping, fed as the n_keep array:
+    # every head keeps its layer's budget, selected exactly as the oracle does.
+    w = synthkv.WORKLOADS["llama3.1-8b-kv-t16k"].scaled("budgets", layers=6, heads=2, t_max=5000)
+    K, V, lens = synthkv.make_kv(w, seed=17, device=DEV)
+    sens = [0.1, 0.9, 0.4, 0.0, 0.7, 0.3]
+    st, budget = mkv.mkv_layer_budgets(sens, 4.0, 3.0, 6 * 2500, [5000] * 6)
+    assert st == 0 and sum(budget) == 15000 and len(set(budget)) > 1
+    heads_per_layer = w.batch * w.heads
+    nk = torch.tensor([budget[h // heads_per_layer] for h in range(w.n_heads)], dtype=torch.int32, device=DEV)
+    for mode, window in (("l2", 0), ("cosine", 1000)):
+        Ko, Vo, idx, kept, st = _run_fused(K, V, 0.5, mode, window, lens, n_keep=nk, keep_stride=max(budget))
+        assert st == 0
+        assert torch.equal(kept.reshape(-1), nk)
+        Kf, Vf = K.reshape(w.n_heads, w.t_max, 128), V.reshape(w.n_heads, w.t_max, 128)
+        for h in range(w.n_heads):
+            n = int(nk[h])
+            ora = oracle.compress_head_n(Kf[h].cpu(), Vf[h].cpu(), n, mode, window)
+            b, hh = divmod(h, w.heads)
+            compare_head(ora, w.t_max, idx_gpu=idx[b, hh].cpu().numpy(), kept_gpu=int(kept[b, hh]), K_head=Kf[h],
+                         V_head=Vf[h], Kout_gpu=bits(Ko[b, hh, :n]), Vout_gpu=bits(Vo[b, hh, :n]), mode=mode)
+
+
+def test_stalled_windows_time_out_and_leave_the_context_usable():
+    # Failure detection without a fault: no window of the single-pass kernel
+    # ever completes, so its waits between CTAs run out (about 1 s). The call
+    # must return, the status word must say MKV_DEV_TIMEOUT, and the next
+    # ordinary call must work.
+    w = synthkv.WORKLOADS["llama3.1-8b-kv-t16k"].scaled("stall", layers=2, heads=2, t_max=3000)
+    K, V, lens = synthkv.make_kv(w, seed=19, device=DEV)
+    ks = mkv.mkv_num_keep(w.t_max, 0.5)
+    Ko = torch.zeros((w.rows, w.heads, ks, 128), dtype=torch.bfloat16, device=DEV)
+    Vo = torch.zeros_like(Ko)
+    idx = torch.zeros((w.rows, w.heads, ks), dtype=torch.int32, device=DEV)
+    kept = torch.zeros((w.rows, w.heads), dtype=torch.int32, device=DEV)
+    ws = mkv.workspace_for(K, 0, lens)
+    import time
+    t0 = time.time()
+    mkv.mkv_inject_stalled_windows(K, V, 0.5, "l2", 0, ks, Ko, Vo, idx, kept, ws, lens)
+    bits_ = mkv.mkv_device_status(ws)
+    assert bits_ & mkv.MKV_DEV_TIMEOUT
+    assert time.time() - t0 < 60
+    # the context is still usable: an ordinary call on the same workspace
+    a = _run_fused(K, V, 0.5, "l2", 0, lens)
+    assert a[4] == 0
+    ora = oracle.compress_head(K[0, 0].cpu(), V[0, 0].cpu(), 0.5, "l2", 0)
+    compare_head(ora, w.t_max, idx_gpu=a[2][0, 0].cpu().numpy(), kept_gpu=int(a[3][0, 0]), K_head=K[0, 0],
+                 V_head=V[0, 0], Kout_gpu=bits(a[0][0, 0, :ks]), Vout_gpu=bits(a[1][0, 0, :ks]))

@@ -295,3 +295,54 @@ def test_empty_head():
     K = _bf16(np.zeros((0, 128)))
     out = oracle.compress_head(K, K, 0.5, "l2", 0)
     assert len(out["idx"]) == 0 and len(out["S"]) == 0
+
+
+# --- per-layer budgets ------------------------------------------------------------
+
+def _budget_cases(golden_dir):
+    with open(os.path.join(golden_dir, "budget_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+def test_layer_budgets_hand_cases(golden_dir):
+    for c in _budget_cases(golden_dir):
+        st, b = oracle.layer_budgets(c["s"], c["r"], c["gamma"], c["total"], c["cap"])
+        assert st == c.get("status", 0), c
+        assert b.tolist() == c["budget"], c
+
+
+def test_layer_budgets_invariants():
+    rng = np.random.default_rng(21)
+    for _ in range(300):
+        L = int(rng.integers(1, 40))
+        s = rng.normal(size=L)
+        r = float(np.exp(rng.normal()))
+        gamma = float(1 + rng.exponential(3))
+        cap = rng.integers(0, 5000, size=L)
+        total = int(rng.integers(0, max(1, cap.sum())))
+        st, b = oracle.layer_budgets(s, r, gamma, total, cap)
+        assert st == 0
+        assert int(b.sum()) == total
+        assert np.all(b >= 0) and np.all(b <= cap)
+    # no caps in the way: the allocation follows w within rounding
+    s = rng.normal(size=16)
+    st, b = oracle.layer_budgets(s, 3.0, 2.5, 160000, np.full(16, 10 ** 6))
+    sn = (s - s.min()) / (s.max() - s.min())
+    w = np.clip(3.0 ** sn, 1 / 2.5, 2.5)
+    np.testing.assert_allclose(b, 160000 * w / w.sum(), atol=1.0)
+    assert b.max() / b.min() <= 2.5 ** 2 + 1e-6
+    # r = 1 is uniform; r > 1 gives more to more sensitive layers
+    st, b = oracle.layer_budgets(s, 1.0, 10.0, 1600, np.full(16, 10 ** 6))
+    assert b.max() - b.min() <= 1
+    st, b = oracle.layer_budgets(s, 5.0, 100.0, 160000, np.full(16, 10 ** 6))
+    order = np.argsort(s)
+    assert np.all(np.diff(b[order]) >= -1)
+
+
+def test_compress_head_n_matches_the_ratio_form():
+    rng = np.random.default_rng(22)
+    K = _bf16(rng.normal(size=(500, 128)))
+    for r in (0.0, 0.3, 0.5, 1.0):
+        a = oracle.compress_head(K, K, r, "l2", 0)
+        b = oracle.compress_head_n(K, K, oracle.num_keep(500, r), "l2", 0)
+        np.testing.assert_array_equal(a["idx"], b["idx"])
