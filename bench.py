@@ -451,7 +451,10 @@ def main(argv=None):
         with open(args.traffic_json) as f:
             t = json.load(f)
         # counters only count while the kernels they were taken on are unchanged
-        src = os.path.join(ROOT, "geometric_kv_cache_gb300", "csrc", "mkv_kernels.cu")
+        src = os.path.join(ROOT, t.get("kernel_source", "geometric_kv_cache_gb300/csrc/mkv_gather.cu"))
+        if not os.path.exists(src):
+            t = {}
+            src = os.path.join(ROOT, "bench.py")
         with open(src, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
         if t.get("workload") == args.workload and not args.layers and t.get("kernel_source_sha256_16") == sha:

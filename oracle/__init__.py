@@ -82,6 +82,14 @@ def _load():
         lib.oracle_layer_budgets.argtypes = [vp, i32, f64, f64, i64, vp, vp]
         lib.oracle_compress_head_n.restype = i64
         lib.oracle_compress_head_n.argtypes = [vp, vp, i64, i64, i64, i32, i64, vp, vp, vp, vp, vp]
+        lib.oracle_window_means.restype = None
+        lib.oracle_window_means.argtypes = [vp, i64, i64, i64, vp, vp]
+        lib.oracle_num_keep_quota.restype = i64
+        lib.oracle_num_keep_quota.argtypes = [i64, f64, i64]
+        lib.oracle_select_quota.restype = i64
+        lib.oracle_select_quota.argtypes = [vp, i64, i64, f64, vp]
+        lib.oracle_compress_head_quota.restype = i64
+        lib.oracle_compress_head_quota.argtypes = [vp, vp, i64, i64, f64, i32, i64, vp, vp, vp, vp, vp]
         _lib = lib
         return lib
 
@@ -229,4 +237,50 @@ def compress_head_n(K, V, n_keep: int, mode="l2", window: int = 0):
                                          _ptr(idx), _ptr(ko), _ptr(vo))
     if got != n:
         raise ValueError("oracle_compress_head_n failed")
+    return {"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}
+
+
+def window_means(X, window: int, radius: bool = True):
+    """Cluster summaries of one head's bf16 rows X [T, d] (keys or values):
+    per-window means float64 [n_windows, d] and, when asked, each window's
+    radius max_t |x_t - mean|_2 float64 [n_windows] (else None)."""
+    x = _bits(X)
+    T, d = x.shape
+    nw = max(num_windows(T, window), 0)
+    M = np.zeros((max(nw, 1), d), dtype=np.float64)
+    R = np.zeros(max(nw, 1), dtype=np.float64)
+    _load().oracle_window_means(_ptr(x), T, d, int(window), _ptr(M), _ptr(R) if radius else None)
+    return M[:nw], (R[:nw] if radius else None)
+
+
+def num_keep_quota(T: int, ratio: float, window: int) -> int:
+    """Kept tokens of a T-token head when every window keeps its own share."""
+    return int(_load().oracle_num_keep_quota(int(T), float(ratio), int(window)))
+
+
+def select_quota(S, window: int, ratio: float) -> np.ndarray:
+    """Per-window-quota selection: ascending int32 indices."""
+    s = np.ascontiguousarray(S, dtype=np.float64)
+    n = num_keep_quota(s.shape[0], ratio, window)
+    idx = np.zeros(max(n, 1), dtype=np.int32)
+    got = _load().oracle_select_quota(_ptr(s), s.shape[0], int(window), float(ratio), _ptr(idx))
+    if got != n:
+        raise ValueError("oracle_select_quota: NaN score")
+    return idx[:n]
+
+
+def compress_head_quota(K, V, ratio: float, mode="l2", window: int = 0):
+    """All steps for one head with per-window quotas. Returns dict(C, S, idx, K_out, V_out)."""
+    k, v = _bits(K), _bits(V)
+    T, d = k.shape
+    C = np.zeros((max(num_windows(T, window), 1), d), dtype=np.float64)
+    S = np.zeros(max(T, 1), dtype=np.float64)
+    n = num_keep_quota(T, ratio, window)
+    idx = np.zeros(max(n, 1), dtype=np.int32)
+    ko = np.zeros((max(n, 1), d), dtype=np.uint16)
+    vo = np.zeros((max(n, 1), d), dtype=np.uint16)
+    got = _load().oracle_compress_head_quota(_ptr(k), _ptr(v), T, d, float(ratio), _MODES[mode], int(window),
+                                             _ptr(C), _ptr(S), _ptr(idx), _ptr(ko), _ptr(vo))
+    if got != n:
+        raise ValueError("oracle_compress_head_quota failed")
     return {"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}

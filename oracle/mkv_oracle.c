@@ -308,3 +308,90 @@ int64_t oracle_compress_head_n(const uint16_t *K, const uint16_t *V, int64_t T, 
     if (V_out) oracle_gather(V, d, idx, n_keep, V_out);
     return n_keep;
 }
+
+/* Cluster summaries, "RefineKV: Query-Adaptive KV Cache Compression via
+ * Attention-Error Bounds" (project page), method overview, step 1
+ * (Summarize): the cache is cut into contiguous clusters, and each cluster's
+ * mean key, mean value and some metadata are cached. The clusters here are
+ * the windows of step 1 (W tokens each, the last one holding the rest), and
+ * the mean is the one oracle_centroids computes, applied to whichever tensor
+ * X is passed (keys or values). The metadata taken here (a reading; the page
+ * does not list it) is the cluster's size, implied by the tiling, and
+ * radius[j] = max over t in window j of |X_t - mean_j|_2. That is what a
+ * query-time bound on how far a member's logit can drift from the mean's
+ * needs (|q.k_t - q.mean| <= |q| * radius, Cauchy-Schwarz; Figure 2's
+ * logit-deviation bound). radius may be NULL. */
+void oracle_window_means(const uint16_t *X, int64_t T, int64_t d, int64_t window, double *mean, double *radius)
+{
+    oracle_centroids(X, T, d, window, mean);
+    if (!radius) return;
+    int64_t wl = oracle_window_len(T, window);
+    int64_t nw = oracle_num_windows(T, window);
+    for (int64_t j = 0; j < nw; ++j) {
+        int64_t a = j * wl;
+        int64_t b = a + wl < T ? a + wl : T;
+        double rmax = 0.0;
+        for (int64_t t = a; t < b; ++t) {
+            double ss = 0.0;
+            for (int64_t i = 0; i < d; ++i) {
+                double diff = oracle_bf16_to_double(X[t * d + i]) - mean[j * d + i];
+                ss += diff * diff;
+            }
+            double r = sqrt(ss);
+            if (r > rmax) rmax = r;
+        }
+        radius[j] = rmax;
+    }
+}
+
+/* Per-window quota variant of WindowedManifoldKV (a reading of the abstract,
+ * which replaces the global centroid by per-window centroids and says
+ * nothing more about the selection): every window keeps its own share
+ * oracle_num_keep(|w|, ratio) of its tokens, the highest-scoring ones within
+ * it (ties to the lower index), instead of one top-n over the whole head.
+ * Total kept tokens of a head of T tokens: */
+int64_t oracle_num_keep_quota(int64_t T, double ratio, int64_t window)
+{
+    int64_t wl = oracle_window_len(T, window);
+    int64_t nw = oracle_num_windows(T, window);
+    int64_t total = 0;
+    for (int64_t j = 0; j < nw; ++j) {
+        int64_t a = j * wl;
+        int64_t b = a + wl < T ? a + wl : T;
+        total += oracle_num_keep(b - a, ratio);
+    }
+    return total;
+}
+
+/* Selection with a per-window quota: oracle_select on each window's scores,
+ * indices shifted to head positions and concatenated in window order (so
+ * they ascend). Returns the number kept, or -1. */
+int64_t oracle_select_quota(const double *S, int64_t T, int64_t window, double ratio, int32_t *idx)
+{
+    int64_t wl = oracle_window_len(T, window);
+    int64_t nw = oracle_num_windows(T, window);
+    int64_t n = 0;
+    for (int64_t j = 0; j < nw; ++j) {
+        int64_t a = j * wl;
+        int64_t b = a + wl < T ? a + wl : T;
+        int64_t q = oracle_num_keep(b - a, ratio);
+        if (oracle_select(S + a, b - a, q, idx + n) != 0) return -1;
+        for (int64_t k = 0; k < q; ++k) idx[n + k] += (int32_t)a;
+        n += q;
+    }
+    return n;
+}
+
+/* Steps 1-4 for one head with per-window quotas. Returns the kept count or -1. */
+int64_t oracle_compress_head_quota(const uint16_t *K, const uint16_t *V, int64_t T, int64_t d, double ratio,
+                                   int mode, int64_t window, double *C, double *S, int32_t *idx,
+                                   uint16_t *K_out, uint16_t *V_out)
+{
+    oracle_centroids(K, T, d, window, C);
+    oracle_scores(K, T, d, window, mode, C, S);
+    int64_t n = oracle_select_quota(S, T, window, ratio, idx);
+    if (n < 0) return -1;
+    if (K_out) oracle_gather(K, d, idx, n, K_out);
+    if (V_out) oracle_gather(V, d, idx, n, V_out);
+    return n;
+}

@@ -346,3 +346,135 @@ def test_compress_head_n_matches_the_ratio_form():
         a = oracle.compress_head(K, K, r, "l2", 0)
         b = oracle.compress_head_n(K, K, oracle.num_keep(500, r), "l2", 0)
         np.testing.assert_array_equal(a["idx"], b["idx"])
+
+
+# ---- cluster summaries ("RefineKV" project page, method overview step 1) ----
+
+def test_window_means_hand_case():
+    # rows (0,0),(2,0) | (1,1),(3,3) | (5,-1), clusters of 2: means (1,0),
+    # (2,2), (5,-1); radii: |(2,0)-(1,0)| = 1, |(3,3)-(2,2)| = sqrt 2, 0
+    X = _bf16([[0, 0], [2, 0], [1, 1], [3, 3], [5, -1]])
+    M, R = oracle.window_means(X, 2)
+    assert M.tolist() == [[1.0, 0.0], [2.0, 2.0], [5.0, -1.0]]
+    assert R[0] == 1.0 and R[1] == math.sqrt(2.0) and R[2] == 0.0
+
+
+@pytest.mark.parametrize("window", [1, 3, 10, 64, 0])
+def test_window_means_equal_library_mean_and_max_distance(window):
+    g = torch.Generator().manual_seed(11 + window)
+    T, d = 157, 16
+    X = (torch.randn(T, d, generator=g) * 3).to(torch.bfloat16)
+    M, R = oracle.window_means(X, window)
+    x = _f64(X)
+    wl = T if window <= 0 or window >= T else window
+    starts = list(range(0, T, wl))
+    assert M.shape == (len(starts), d) and R.shape == (len(starts),)
+    for j, a in enumerate(starts):
+        rows = x[a:a + wl]
+        mean = np.mean(rows, axis=0)
+        np.testing.assert_allclose(M[j], mean, rtol=1e-12, atol=1e-12)
+        assert R[j] == pytest.approx(cdist(rows, mean[None, :]).max(), rel=1e-12, abs=1e-12)
+
+
+def test_window_means_translation_exact():
+    # small integers: every sum is exact, so adding v to every row shifts each
+    # mean by exactly v and leaves every radius unchanged
+    g = torch.Generator().manual_seed(5)
+    X = torch.randint(-20, 20, (40, 8), generator=g).to(torch.float32)
+    v = torch.randint(-50, 50, (8,), generator=g).to(torch.float32)
+    M0, R0 = oracle.window_means(X.to(torch.bfloat16), 8)
+    M1, R1 = oracle.window_means((X + v).to(torch.bfloat16), 8)
+    np.testing.assert_array_equal(M1, M0 + v.numpy().astype(np.float64))
+    np.testing.assert_array_equal(R1, R0)
+
+
+def test_radius_bounds_every_members_logit_deviation():
+    # the reading behind the radius: |q.x_t - q.mean| <= |q| * radius for
+    # every member t and any query q, with equality for q along the farthest
+    # member's offset
+    g = torch.Generator().manual_seed(8)
+    X = torch.randn(50, 32, generator=g).to(torch.bfloat16)
+    M, R = oracle.window_means(X, 10)
+    x = _f64(X)
+    q = np.random.default_rng(0).normal(size=(20, 32))
+    for j in range(5):
+        dev = np.abs((x[10 * j:10 * j + 10] - M[j]) @ q.T)
+        assert np.all(dev <= np.linalg.norm(q, axis=1) * R[j] * (1 + 1e-12))
+        off = x[10 * j:10 * j + 10] - M[j]
+        far = off[np.argmax(np.linalg.norm(off, axis=1))]
+        assert abs(far @ far) / np.linalg.norm(far) == pytest.approx(R[j], rel=1e-12)
+
+
+def test_window_means_without_radius():
+    X = _bf16([[1, 2], [3, 4], [5, 6]])
+    M, R = oracle.window_means(X, 2, radius=False)
+    assert R is None and M.tolist() == [[2.0, 3.0], [5.0, 6.0]]
+
+
+# ---- per-window quota (a reading of WindowedManifoldKV's selection) ----
+
+def test_select_quota_hand_cases():
+    # two windows of 4, keep 2 each: (5,1,3,3) keeps 0 and the lower of the
+    # tied 3s (2); (2,9,0,4) keeps 5 and 7
+    assert oracle.select_quota(np.array([5, 1, 3, 3, 2, 9, 0, 4.0]), 4, 0.5).tolist() == [0, 2, 5, 7]
+    # windows (1,2), (3,4), (5): floor(2*0.5+0.5) = 1 and floor(1*0.5+0.5) = 1
+    # each, so the higher of each pair and the lone last token
+    assert oracle.select_quota(np.array([1, 2, 3, 4, 5.0]), 2, 0.5).tolist() == [1, 3, 4]
+    assert oracle.num_keep_quota(5, 0.5, 2) == 3
+    # the same scores under one global top-3 keep the three largest instead
+    assert oracle.select(np.array([1, 2, 3, 4, 5.0]), 3).tolist() == [2, 3, 4]
+
+
+def test_select_quota_brute_force():
+    rng = np.random.default_rng(3)
+    for trial in range(200):
+        T = int(rng.integers(0, 40))
+        W = int(rng.integers(1, 12))
+        r = float(rng.choice([0.0, 0.25, 0.5, 0.7, 1.0]))
+        s = rng.integers(0, 5, size=T).astype(np.float64)  # many ties
+        want = []
+        for a in range(0, T, W):
+            seg = s[a:a + W]
+            q = math.floor(len(seg) * (1 - r) + 0.5)
+            order = sorted(range(len(seg)), key=lambda t: (-seg[t], t))
+            want += sorted(a + t for t in order[:q])
+        assert oracle.select_quota(s, W, r).tolist() == want, (T, W, r)
+
+
+@pytest.mark.parametrize("T", [1, 7, 100, 4096, 5000])
+@pytest.mark.parametrize("W", [1, 3, 256, 4096])
+@pytest.mark.parametrize("r", [0.2, 0.5, 0.75])
+def test_num_keep_quota_closed_form(T, W, r):
+    q = lambda n: min(max(math.floor(n * (1 - r) + 0.5), 0), n)
+    nw = -(-T // W)
+    assert oracle.num_keep_quota(T, r, W) == (nw - 1) * q(W) + q(T - (nw - 1) * W)
+
+
+def test_select_quota_special_cases():
+    rng = np.random.default_rng(4)
+    s = rng.normal(size=300)
+    # a window covering the head is the global selection
+    for W in (300, 301, 0):
+        np.testing.assert_array_equal(oracle.select_quota(s, W, 0.3), oracle.select(s, oracle.num_keep(300, 0.3)))
+    # one-token windows keep every token for r <= 1/2 and none above
+    assert oracle.select_quota(s, 1, 0.5).tolist() == list(range(300))
+    assert oracle.select_quota(s, 1, 0.51).size == 0
+
+
+def test_compress_head_quota_rows_and_counts():
+    w = synthkv.WORKLOADS["single-layer-h8-t4096"]
+    K, V, _ = synthkv.make_kv(w, seed=2, device="cpu", heads=[1])
+    K, V = K[0, :3001], V[0, :3001]
+    out = oracle.compress_head_quota(K, V, 0.4, "l2", 512)
+    idx = out["idx"]
+    assert idx.shape[0] == oracle.num_keep_quota(3001, 0.4, 512)
+    assert np.all(np.diff(idx) > 0)
+    for a in range(0, 3001, 512):
+        n = min(512, 3001 - a)
+        assert int(((idx >= a) & (idx < a + n)).sum()) == oracle.num_keep(n, 0.4)
+    kb = K.contiguous().view(torch.int16).numpy().view(np.uint16)
+    vb = V.contiguous().view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(out["K_out"], kb[idx])
+    np.testing.assert_array_equal(out["V_out"], vb[idx])
+    # the scores are the windowed ones; only the selection differs
+    np.testing.assert_array_equal(out["S"], oracle.scores(K, oracle.centroids(K, 512), 512, "l2"))
