@@ -46,7 +46,8 @@ EXPORTED = (
     "mkv_select_topk", "mkv_compact", "mkv_compress", "mkv_compress_num_stages",
     "mkv_compress_profiled", "mkv_compress_host", "mkv_device_status", "mkv_status_string",
     "mkv_compress_noalloc", "mkv_compress_single_pass", "mkv_set_single_pass", "mkv_layer_budgets",
-    "mkv_inject_stalled_windows",
+    "mkv_inject_stalled_windows", "mkv_window_means", "mkv_num_keep_quota", "mkv_select_quota",
+    "mkv_compress_quota",
 )
 
 
@@ -103,6 +104,10 @@ def load(build_if_missing: bool = True):
             "mkv_device_status": (i32, [vp, vp, ctypes.POINTER(u32)]),
             "mkv_compress_noalloc": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
             "mkv_status_string": (ctypes.c_char_p, [i32]),
+            "mkv_window_means": (i32, [vp, MkvShape, i32, vp, vp, vp, sz, vp]),
+            "mkv_num_keep_quota": (i32, [i32, f64, i32]),
+            "mkv_select_quota": (i32, [vp, MkvShape, f64, i32, i32, vp, vp, vp, sz, vp]),
+            "mkv_compress_quota": (i32, [vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -208,6 +213,14 @@ def mkv_centroid(K, window, C, workspace, seq_lens=None, stream=None):
                                workspace.numel(), _stream(stream)), "mkv_centroid")
 
 
+def mkv_window_means(X, window, mean, workspace, radius=None, seq_lens=None, stream=None):
+    """Cluster summaries of a bf16 cache X (keys or values): fp32 window means
+    [batch, heads, nw, 128] and, optionally, fp32 radii [batch, heads, nw]."""
+    _need_cuda(X, mean, radius, workspace, seq_lens)
+    _check(load().mkv_window_means(_ptr(X), shape_of(X, seq_lens), int(window), _ptr(mean), _ptr(radius),
+                                   _ptr(workspace), workspace.numel(), _stream(stream)), "mkv_window_means")
+
+
 def mkv_score(K, C, window, mode, S, workspace, seq_lens=None, stream=None):
     _need_cuda(K, C, S, workspace, seq_lens)
     _check(load().mkv_score(_ptr(K), _ptr(C), shape_of(K, seq_lens), int(window), _MODES[mode], _ptr(S),
@@ -234,6 +247,26 @@ def mkv_compress(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept
     _check(load().mkv_compress(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _ptr(n_keep), _MODES[mode],
                                int(window), int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx), _ptr(kept),
                                _ptr(workspace), workspace.numel(), _stream(stream)), "mkv_compress")
+
+
+def mkv_num_keep_quota(T: int, ratio: float, window: int) -> int:
+    return int(load().mkv_num_keep_quota(int(T), float(ratio), int(window)))
+
+
+def mkv_select_quota(S, shape: MkvShape, ratio, window, keep_stride, idx, kept, workspace, stream=None):
+    _need_cuda(S, idx, kept, workspace)
+    _check(load().mkv_select_quota(_ptr(S), shape, float(ratio), int(window), int(keep_stride), _ptr(idx),
+                                   _ptr(kept), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mkv_select_quota")
+
+
+def mkv_compress_quota(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, workspace, seq_lens=None,
+                       stream=None):
+    _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens)
+    _check(load().mkv_compress_quota(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _MODES[mode],
+                                     int(window), int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx),
+                                     _ptr(kept), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mkv_compress_quota")
 
 
 def mkv_compress_profiled(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, workspace, events,

@@ -43,6 +43,15 @@ int32_t host_num_keep(int32_t T, double ratio)
 
 bool ratio_ok(double r) { return r >= 0.0 && r <= 1.0; }  // false for NaN
 
+// Kept tokens of a T-token head when each window keeps its own share.
+int64_t host_num_keep_quota(int32_t T, double ratio, int32_t window)
+{
+    if (T <= 0) return 0;
+    if (window <= 0 || window >= T) return host_num_keep(T, ratio);
+    const int32_t nw = (int32_t)(((int64_t)T + window - 1) / window);
+    return (int64_t)(nw - 1) * host_num_keep(window, ratio) + host_num_keep(T - (nw - 1) * window, ratio);
+}
+
 // Shape checks shared by all entry points. Returns MKV_OK or the error.
 mkv_status check_shape(const mkv_shape &s)
 {
@@ -82,12 +91,17 @@ T *region(void *ws, size_t off)
 mkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MKV_OK : MKV_ERR_CUDA; }
 
 // Checks of mkv_compact / mkv_compress outputs.
+// quota_window > 0: per-window quotas, whose kept count bounds the stride.
 mkv_status check_outputs(const mkv_shape &s, double ratio, const int32_t *n_keep, int32_t keep_stride,
                          const void *K, const void *V, const void *K_out, const void *V_out,
-                         const int32_t *idx, const int32_t *kept, bool need_kv)
+                         const int32_t *idx, const int32_t *kept, bool need_kv, int32_t quota_window = 0)
 {
     if (!ratio_ok(ratio) || keep_stride < 0) return MKV_ERR_INVALID_ARG;
-    if (!n_keep && keep_stride < host_num_keep(s.t_max, ratio)) return MKV_ERR_INVALID_ARG;
+    if (quota_window > 0) {
+        if (keep_stride < host_num_keep_quota(s.t_max, ratio, quota_window)) return MKV_ERR_INVALID_ARG;
+    } else if (!n_keep && keep_stride < host_num_keep(s.t_max, ratio)) {
+        return MKV_ERR_INVALID_ARG;
+    }
     if (n_keep && !aligned(n_keep, 4)) return MKV_ERR_INVALID_ARG;
     if ((K_out == nullptr) != (V_out == nullptr)) return MKV_ERR_INVALID_ARG;
     if (need_kv && !K_out) return MKV_ERR_INVALID_ARG;
@@ -104,12 +118,14 @@ mkv_status check_outputs(const mkv_shape &s, double ratio, const int32_t *n_keep
 mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio, const int32_t *n_keep,
                         mkv_mode mode, int32_t window, int32_t keep_stride, void *K_out, void *V_out,
                         int32_t *idx, int32_t *kept, void *ws, size_t ws_bytes, cudaStream_t st,
-                        void *const *events, bool stall_windows = false)
+                        void *const *events, bool stall_windows = false, bool quota = false)
 {
     mkv_status rc = check_shape(s);
     if (rc != MKV_OK) return rc;
     if (!K || !V || window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE)) return MKV_ERR_INVALID_ARG;
-    rc = check_outputs(s, ratio, n_keep, keep_stride, K, V, K_out, V_out, idx, kept, false);
+    // per-window quotas; one window per head is the ordinary selection
+    quota = quota && window > 0 && window < s.t_max;
+    rc = check_outputs(s, ratio, n_keep, keep_stride, K, V, K_out, V_out, idx, kept, false, quota ? window : 0);
     if (rc != MKV_OK) return rc;
     const Geometry g = make_geometry(s.batch, s.heads, s.t_max, window);
     const Layout L = make_layout(g);
@@ -157,10 +173,13 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     // a3 (+ a4 when the head's scores fit shared memory), then a4, a5
     int32_t *idx_w = idx ? idx : region<int32_t>(ws, L.idx);
     const int32_t idx_stride = idx ? keep_stride : g.t_max;
-    const bool emit = select_emits_indices(g);
-    if ((e = launch_select(g, S, s.seq_lens, ratio, n_keep, keep_stride, cut, emit ? nullptr : chunk, kept_w,
-                           emit ? idx_w : nullptr, idx_stride, status, st)) != cudaSuccess)
-        return cuda_status(e);
+    const bool emit = quota || select_emits_indices(g);
+    if (quota)
+        e = launch_select_quota(g, S, s.seq_lens, ratio, keep_stride, kept_w, idx_w, idx_stride, status, st);
+    else
+        e = launch_select(g, S, s.seq_lens, ratio, n_keep, keep_stride, cut, emit ? nullptr : chunk, kept_w,
+                          emit ? idx_w : nullptr, idx_stride, status, st);
+    if (e != cudaSuccess) return cuda_status(e);
     if (!mark(4)) return MKV_ERR_CUDA;
     if (!emit &&
         (e = launch_compact(g, S, cut, chunk, s.seq_lens, keep_stride, idx_w, idx_stride, status, st)) != cudaSuccess)
@@ -274,6 +293,27 @@ mkv_status mkv_centroid(const void *K, mkv_shape shape, int32_t window, float *C
     return cuda_status(e);
 }
 
+mkv_status mkv_window_means(const void *X, mkv_shape shape, int32_t window, float *mean, float *radius,
+                            void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    mkv_status rc = check_shape(shape);
+    if (rc != MKV_OK) return rc;
+    if (!X || !mean || window < 0 || !aligned(X, 16) || !aligned(mean, 16)) return MKV_ERR_INVALID_ARG;
+    if (radius && !aligned(radius, 4)) return MKV_ERR_INVALID_ARG;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window);
+    const bool small = window > 0 && window <= kSmallWindowMax;
+    if (radius && !small) return MKV_ERR_UNSUPPORTED;
+    const Layout L = make_layout(g);
+    if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
+    if (empty(shape)) return MKV_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t *status = region<uint32_t>(workspace, L.status);
+    if (small) return cuda_status(launch_small_window_means(g.pg, X, shape.seq_lens, mean, radius, status, st));
+    cudaError_t e = launch_piece_sums(g.pg, X, shape.seq_lens, region<float>(workspace, L.partial), status, st);
+    if (e == cudaSuccess) e = launch_window_means(g.pg, region<float>(workspace, L.partial), shape.seq_lens, mean, status, st);
+    return cuda_status(e);
+}
+
 mkv_status mkv_score(const void *K, const float *C, mkv_shape shape, int32_t window, mkv_mode mode, float *S,
                      void *workspace, size_t workspace_bytes, mkv_stream_t stream)
 {
@@ -333,6 +373,38 @@ mkv_status mkv_compress(const void *K, const void *V, mkv_shape shape, double ra
 {
     return run_compress(K, V, shape, ratio, n_keep, mode, window, keep_stride, K_out, V_out, idx, kept, workspace,
                         workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int32_t mkv_num_keep_quota(int32_t T, double ratio, int32_t window)
+{
+    if (T < 0 || window < 0 || !ratio_ok(ratio)) return -1;
+    return (int32_t)host_num_keep_quota(T, ratio, window);
+}
+
+mkv_status mkv_select_quota(const float *S, mkv_shape shape, double ratio, int32_t window, int32_t keep_stride,
+                            int32_t *idx, int32_t *kept, void *workspace, size_t workspace_bytes,
+                            mkv_stream_t stream)
+{
+    mkv_status rc = check_shape(shape);
+    if (rc != MKV_OK) return rc;
+    if (!S || !idx || !kept || !aligned(S, 4) || !aligned(idx, 4) || !aligned(kept, 4)) return MKV_ERR_INVALID_ARG;
+    if (!ratio_ok(ratio) || window < 0 || keep_stride < host_num_keep_quota(shape.t_max, ratio, window))
+        return MKV_ERR_INVALID_ARG;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window);
+    const Layout L = make_step_layout(g);
+    if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
+    if (empty(shape)) return MKV_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t *status = region<uint32_t>(workspace, L.status);
+    return cuda_status(launch_select_quota(g, S, shape.seq_lens, ratio, keep_stride, kept, idx, keep_stride, status, st));
+}
+
+mkv_status mkv_compress_quota(const void *K, const void *V, mkv_shape shape, double ratio, mkv_mode mode,
+                              int32_t window, int32_t keep_stride, void *K_out, void *V_out, int32_t *idx,
+                              int32_t *kept, void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    return run_compress(K, V, shape, ratio, nullptr, mode, window, keep_stride, K_out, V_out, idx, kept, workspace,
+                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr, false, true);
 }
 
 int32_t mkv_compress_num_stages(void) { return kCompressStages; }

@@ -20,6 +20,14 @@ __device__ __forceinline__ uint4 ld_stream(const void *p)
     return r;
 }
 
+// 16-byte non-coherent load that stays in L1 (for rows read twice in a row).
+__device__ __forceinline__ uint4 ld_nc(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ void st_v4(void *p, uint4 v)
 {
     *reinterpret_cast<uint4 *>(p) = v;

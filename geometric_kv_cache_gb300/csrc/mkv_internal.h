@@ -18,6 +18,7 @@ constexpr int kMinPieceRows = 256;     // pieces are 256 * 2^k tokens (a window 
 constexpr int kMaxPiecesPerWindow = 64;  // ... the fewest that keep a window within this many pieces
 constexpr int kGroupPieces = 32;       // pieces per first-level group of a window's sum
 constexpr uint32_t kNoneKey = 0xFFFFFFFFu;  // mkv_cut.key meaning "keep nothing"
+constexpr int kSmallWindowMax = 128;   // cluster summaries of windows up to this long run one group per window
 
 // Piece decomposition of the centroid / score work: item = (head, window,
 // piece), head-major. Depends only on the shape and the window (never on
@@ -81,6 +82,17 @@ bool select_emits_indices(const Geometry &g);
 cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_lens, double ratio,
                           const int32_t *n_keep, int32_t keep_stride, mkv_cut *cut, int2 *chunk_info,
                           int32_t *kept, int32_t *idx, int32_t idx_stride, uint32_t *status, cudaStream_t st);
+// Per-window-quota selection: every window keeps n_keep(|w|, ratio) of its
+// own tokens (window 0 or >= t_max: one window, the ordinary selection);
+// writes the ascending kept indices to idx[head * idx_stride + slot] and the
+// kept counts.
+cudaError_t launch_select_quota(const Geometry &g, const float *S, const int32_t *seq_lens, double ratio,
+                                int32_t keep_stride, int32_t *kept, int32_t *idx, int32_t idx_stride,
+                                uint32_t *status, cudaStream_t st);
+// Means (and, with radius, the largest distance of a member to its mean) of
+// the windows of a bf16 tensor, 0 < window <= kSmallWindowMax.
+cudaError_t launch_small_window_means(const PieceGeometry &g, const void *X, const int32_t *seq_lens, float *mean,
+                                      float *radius, uint32_t *status, cudaStream_t st);
 cudaError_t launch_chunk_offsets(const Geometry &g, const float *S, const mkv_cut *cut,
                                  const int32_t *seq_lens, double ratio, const int32_t *n_keep,
                                  int32_t keep_stride, int2 *chunk_info, int32_t *kept,

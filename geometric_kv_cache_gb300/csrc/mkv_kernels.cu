@@ -84,11 +84,19 @@ __device__ int chunk_offsets_block(const float *srow, int T, mkv_cut cut, int nc
 // launch gives dynamic shared memory for t_max scores (IN_SMEM), the head's
 // scores are copied there once and every pass reads shared memory; otherwise
 // the passes read global memory (L2), four loads in flight per thread.
-template <bool IN_SMEM>
+//
+// QUOTA (the per-window-quota selection): the item is a (head, window) pair
+// instead of a head; each window of W tokens keeps its own share
+// n_keep(|w|, ratio) of its tokens, selected among them alone, and writes
+// its indices at slot w * n_keep(W, ratio) of the head's row (every window
+// before the last is full, so the offset has this closed form). The CTA of
+// window 0 writes the head's kept count. idx is required, cut_out and
+// chunk_info unused.
+template <bool IN_SMEM, bool QUOTA>
 __global__ void __launch_bounds__(kSelectThreads, 2)
 k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int heads, int t_max,
-         double ratio, const int32_t *__restrict__ n_keep, int keep_stride, int64_t n_heads,
-         mkv_cut *__restrict__ cut_out, int2 *__restrict__ chunk_info, int nch_max,
+         double ratio, const int32_t *__restrict__ n_keep, int keep_stride, int64_t n_items, int window,
+         int nwin_max, mkv_cut *__restrict__ cut_out, int2 *__restrict__ chunk_info, int nch_max,
          int32_t *__restrict__ kept_out, int32_t *__restrict__ idx, int idx_stride, uint32_t *status)
 {
     extern __shared__ __align__(16) float s_scores[];
@@ -98,16 +106,40 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
     __shared__ uint32_t s_min[kSelectThreads / 32], s_max[kSelectThreads / 32];
     const int lane = threadIdx.x & 31;
     constexpr int kUnroll = 4;
-    for (int64_t head = blockIdx.x; head < n_heads; head += gridDim.x) {
-        const int T = head_len(seq_lens, head, heads, t_max, status, threadIdx.x == 0);
-        const int nk = n_keep ? n_keep[head] : num_keep_dev(T, ratio);
-        if (nk < 0 || nk > T || (keep_stride >= 0 && nk > keep_stride)) {
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+        int64_t head = item;
+        int T, nk, seg = 0;  // segment [seg, seg + T) of the head's tokens
+        int32_t *idx_head = nullptr;
+        if (QUOTA) {
+            head = item / nwin_max;
+            const int w = (int)(item - head * nwin_max);
+            const int Th = head_len(seq_lens, head, heads, t_max, status, threadIdx.x == 0 && w == 0);
+            const int nw = (Th + window - 1) / window;
+            const int q_full = num_keep_dev(window, ratio);
+            const int total = nw > 0 ? (nw - 1) * q_full + num_keep_dev(Th - (nw - 1) * window, ratio) : 0;
+            if (w == 0 && threadIdx.x == 0) {
+                if (total > keep_stride) atomicOr(status, MKV_DEV_BAD_N_KEEP);
+                if (kept_out) kept_out[head] = total > keep_stride ? 0 : total;
+            }
+            seg = w * window;
+            if (seg >= Th || total > keep_stride) continue;  // the same for every thread
+            T = min(window, Th - seg);
+            nk = num_keep_dev(T, ratio);
+            idx_head = idx + head * idx_stride + (int64_t)w * q_full;
+        } else {
+            T = head_len(seq_lens, head, heads, t_max, status, threadIdx.x == 0);
+            nk = n_keep ? n_keep[head] : num_keep_dev(T, ratio);
+            if (idx) idx_head = idx + head * idx_stride;
+        }
+        // output slots this segment may use
+        const int cap = QUOTA ? nk : keep_stride;
+        if (!QUOTA && (nk < 0 || nk > T || (keep_stride >= 0 && nk > keep_stride))) {
             if (threadIdx.x == 0) {
                 atomicOr(status, MKV_DEV_BAD_N_KEEP);
                 mkv_cut none;
                 none.key = kNoneKey;
                 none.ties = 0;
-                cut_out[head] = none;
+                if (cut_out) cut_out[head] = none;
                 if (kept_out) kept_out[head] = 0;
             }
             if (chunk_info) {
@@ -116,10 +148,10 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
             }
             continue;
         }
-        const float *grow = S + (size_t)head * t_max;
+        const float *grow = S + (size_t)head * t_max + seg;
         const float *srow = grow;
         if (IN_SMEM) {
-            if ((t_max & 3) == 0) {  // 16-byte aligned rows
+            if ((reinterpret_cast<uintptr_t>(grow) & 15) == 0) {  // 16-byte aligned segment
                 const float4 *g4 = reinterpret_cast<const float4 *>(grow);
                 float4 *s4 = reinterpret_cast<float4 *>(s_scores);
                 for (int i = threadIdx.x; i < T / 4; i += kSelectThreads) s4[i] = __ldcg(g4 + i);
@@ -219,14 +251,13 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
         mkv_cut cut;
         cut.key = prefix;
         cut.ties = need;
-        if (threadIdx.x == 0) cut_out[head] = cut;
-        if (idx) {
+        if (threadIdx.x == 0 && cut_out) cut_out[head] = cut;
+        if (idx_head) {
             // Emit the kept indices in ascending order straight from the
             // scores in hand: rounds of 16 consecutive tokens per thread, two
             // CTA scans per round (tie rank, output slot), counts carried
             // across rounds.
             uint32_t kept = 0, ties_before = 0;
-            int32_t *idx_head = idx + head * idx_stride;
             for (int a = 0; a < T && nk > 0; a += kSelectThreads * 16) {
                 const int t0 = a + threadIdx.x * 16;
                 uint32_t gtm = 0, eqm = 0;
@@ -249,7 +280,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
                 uint32_t k_total = 0;
                 uint32_t slot = kept + block_exclusive_scan<kSelectThreads>(__popc(keepm), s_warp, &k_total);
                 for (uint32_t m = keepm; m; m &= m - 1, ++slot) {
-                    if (slot < (uint32_t)keep_stride) idx_head[slot] = t0 + __ffs(m) - 1;
+                    if (slot < (uint32_t)cap) idx_head[slot] = seg + t0 + __ffs(m) - 1;
                     else atomicOr(status, MKV_DEV_INTERNAL);
                 }
                 kept += k_total;
@@ -257,7 +288,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
             }
             if (threadIdx.x == 0) {
                 if ((int)kept != nk) atomicOr(status, MKV_DEV_INTERNAL);
-                if (kept_out) kept_out[head] = (int32_t)kept;
+                if (!QUOTA && kept_out) kept_out[head] = (int32_t)kept;
             }
         } else if (chunk_info) {
             const int kept = nk > 0 ? chunk_offsets_block(srow, T, cut, nch_max, chunk_info + head * nch_max, s_warp) : 0;
@@ -434,17 +465,43 @@ cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_
     if (g.n_heads == 0) return cudaSuccess;
     const size_t smem = (size_t)g.t_max * sizeof(float);
     if (g.t_max <= kSelectSmemScores) {
-        cudaError_t e = cudaFuncSetAttribute(k_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        auto *kern = k_select<true, false>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        const int grid = grid_for_items(reinterpret_cast<const void *>(k_select<true>), kSelectThreads, smem, g.n_heads);
-        k_select<true><<<grid, kSelectThreads, smem, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride,
-                                                            g.n_heads, cut, chunk_info, g.nch, kept, idx, idx_stride,
-                                                            status);
+        const int grid = grid_for_items(reinterpret_cast<const void *>(kern), kSelectThreads, smem, g.n_heads);
+        kern<<<grid, kSelectThreads, smem, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride, g.n_heads,
+                                                 0, 1, cut, chunk_info, g.nch, kept, idx, idx_stride, status);
     } else {
-        const int grid = grid_for(k_select<false>, kSelectThreads, g.n_heads);
-        k_select<false><<<grid, kSelectThreads, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride,
-                                                         g.n_heads, cut, chunk_info, g.nch, kept, idx, idx_stride,
-                                                         status);
+        auto *kern = k_select<false, false>;
+        const int grid = grid_for(kern, kSelectThreads, g.n_heads);
+        kern<<<grid, kSelectThreads, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride, g.n_heads, 0,
+                                              1, cut, chunk_info, g.nch, kept, idx, idx_stride, status);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_select_quota(const Geometry &g, const float *S, const int32_t *seq_lens, double ratio,
+                                int32_t keep_stride, int32_t *kept, int32_t *idx, int32_t idx_stride,
+                                uint32_t *status, cudaStream_t st)
+{
+    const PieceGeometry &p = g.pg;
+    const int64_t items = g.n_heads * p.nwin_max;
+    if (items == 0) return cudaSuccess;
+    // one window per head (window 0 or >= t_max) is the ordinary selection
+    const int wl = (p.window <= 0 || p.window >= g.t_max) ? g.t_max : p.window;
+    if (wl <= kSelectSmemScores) {
+        auto *kern = k_select<true, true>;
+        const size_t smem = (size_t)wl * sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const int grid = grid_for_items(reinterpret_cast<const void *>(kern), kSelectThreads, smem, items);
+        kern<<<grid, kSelectThreads, smem, st>>>(S, seq_lens, g.heads, g.t_max, ratio, nullptr, keep_stride, items,
+                                                 wl, p.nwin_max, nullptr, nullptr, 0, kept, idx, idx_stride, status);
+    } else {
+        auto *kern = k_select<false, true>;
+        const int grid = grid_for(kern, kSelectThreads, items);
+        kern<<<grid, kSelectThreads, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, nullptr, keep_stride, items,
+                                              wl, p.nwin_max, nullptr, nullptr, 0, kept, idx, idx_stride, status);
     }
     return cudaGetLastError();
 }

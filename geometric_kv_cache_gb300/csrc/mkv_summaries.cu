@@ -1,0 +1,143 @@
+// sm_103a cluster summaries: per-window means of a bf16 cache (keys or
+// values) for short windows, with each window's radius.
+//
+// "RefineKV: Query-Adaptive KV Cache Compression via Attention-Error Bounds"
+// (project page), method overview, step 1 (Summarize): the cache is cut
+// into contiguous clusters (10 keys in its Figure 2), and each cluster's
+// mean key and mean value are cached with metadata. Here the clusters are
+// the windows [jW, min((j+1)W, T)), and the radius max_t |x_t - mean|_2 is
+// the metadata a query-time bound on logit deviation needs
+// (|q.k_t - q.mean| <= |q| radius). Longer windows use the piece kernels of
+// the centroid step (mkv_piece.cu) instead.
+//
+// Layout: one window per 8-lane group. Lane q of a group owns dims
+// [8q, 8q+8) and [64+8q, 64+8q+8) of every row (two 16-byte loads per row,
+// each group reading whole 128-byte lines). Sums run per dim in token order
+// in fp32, so no lane talks to another for the mean. The radius pass re-reads
+// the window's rows (from L1/L2), sums its 16 squared offsets per lane, then
+// sums over the group with an xor butterfly (the same bits on every lane).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mkv_device.cuh"
+#include "mkv_internal.h"
+
+namespace mkv {
+namespace {
+
+constexpr int kSumThreads = 256;
+constexpr int kWindowsPerCta = kSumThreads / 8;
+constexpr int kBatchRows = 4;  // rows in flight per lane
+using namespace dev;
+
+__device__ __forceinline__ void load_row(const uint8_t *row, uint4 &lo, uint4 &hi)
+{
+    lo = ld_nc(row);
+    hi = ld_nc(row + 128);
+}
+
+__global__ void __launch_bounds__(kSumThreads)
+k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ seq_lens, int heads, int t_max,
+                     int window, int nwin_max, int64_t n_items, float *__restrict__ mean,
+                     float *__restrict__ radius, uint32_t *status)
+{
+    const int grp = threadIdx.x >> 3, q = threadIdx.x & 7;
+    for (int64_t base = (int64_t)blockIdx.x * kWindowsPerCta; base < n_items;
+         base += (int64_t)gridDim.x * kWindowsPerCta) {
+        const int64_t item = base + grp;
+        int n = 0;
+        int64_t head = 0;
+        int j = 0;
+        if (item < n_items) {
+            head = item / nwin_max;
+            j = (int)(item - head * nwin_max);
+            const int T = head_len(seq_lens, head, heads, t_max, status, q == 0 && j == 0);
+            n = min(window, T - j * window);
+        }
+        const uint8_t *row0 = X + ((size_t)head * t_max + (size_t)j * window) * kRowBytes + q * 16;
+        float m[16] = {0.f};
+        if (n > 0) {
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+            for (int t0 = 0; t0 < n; t0 += kBatchRows) {
+                uint4 lo[kBatchRows], hi[kBatchRows];
+#pragma unroll
+                for (int u = 0; u < kBatchRows; ++u)
+                    if (t0 + u < n) load_row(row0 + (size_t)(t0 + u) * kRowBytes, lo[u], hi[u]);
+#pragma unroll
+                for (int u = 0; u < kBatchRows; ++u) {
+                    if (t0 + u < n) {
+                        float f[8];
+                        bf16x8_to_f32(lo[u], f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+                        bf16x8_to_f32(hi[u], f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[8 + i] += f[i];
+                    }
+                }
+            }
+            const float fn = (float)n;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m[i] = __fdiv_rn(acc[i], fn);
+            float4 *out = reinterpret_cast<float4 *>(mean + ((size_t)head * nwin_max + j) * kHeadDim);
+            out[2 * q] = make_float4(m[0], m[1], m[2], m[3]);
+            out[2 * q + 1] = make_float4(m[4], m[5], m[6], m[7]);
+            out[16 + 2 * q] = make_float4(m[8], m[9], m[10], m[11]);
+            out[16 + 2 * q + 1] = make_float4(m[12], m[13], m[14], m[15]);
+        }
+        if (radius) {
+            // every lane of the warp runs the same rows (the butterfly below
+            // needs all 32), rows past a group's window count as nothing
+            const int n_warp = __reduce_max_sync(kFull, (unsigned)max(n, 0));
+            float rmax = 0.f;
+            for (int t0 = 0; t0 < n_warp; t0 += kBatchRows) {
+                uint4 lo[kBatchRows], hi[kBatchRows];
+#pragma unroll
+                for (int u = 0; u < kBatchRows; ++u)
+                    if (t0 + u < n) load_row(row0 + (size_t)(t0 + u) * kRowBytes, lo[u], hi[u]);
+#pragma unroll
+                for (int u = 0; u < kBatchRows; ++u) {
+                    float ss = 0.f;
+                    if (t0 + u < n) {
+                        float f[8];
+                        bf16x8_to_f32(lo[u], f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float dlt = f[i] - m[i];
+                            ss = fmaf(dlt, dlt, ss);
+                        }
+                        bf16x8_to_f32(hi[u], f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float dlt = f[i] - m[8 + i];
+                            ss = fmaf(dlt, dlt, ss);
+                        }
+                    }
+                    ss += __shfl_xor_sync(kFull, ss, 1);
+                    ss += __shfl_xor_sync(kFull, ss, 2);
+                    ss += __shfl_xor_sync(kFull, ss, 4);
+                    if (t0 + u < n) rmax = fmaxf(rmax, sqrtf(ss));
+                }
+            }
+            if (n > 0 && q == 0) radius[(size_t)head * nwin_max + j] = rmax;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_small_window_means(const PieceGeometry &g, const void *X, const int32_t *seq_lens, float *mean,
+                                      float *radius, uint32_t *status, cudaStream_t st)
+{
+    const int64_t items = g.n_heads * g.nwin_max;
+    if (items == 0) return cudaSuccess;
+    const int grid = grid_for_items(reinterpret_cast<const void *>(k_small_window_means), kSumThreads, 0,
+                                    (items + kWindowsPerCta - 1) / kWindowsPerCta);
+    k_small_window_means<<<grid, kSumThreads, 0, st>>>(static_cast<const uint8_t *>(X), seq_lens, g.heads, g.t_max,
+                                                       g.window, g.nwin_max, items, mean, radius, status);
+    return cudaGetLastError();
+}
+
+}  // namespace mkv

@@ -123,6 +123,24 @@ size_t mkv_workspace_size(mkv_shape shape, int32_t window);
 mkv_status mkv_centroid(const void *K, mkv_shape shape, int32_t window, float *C,
                         void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
+/* Cluster summaries ("RefineKV: Query-Adaptive KV Cache Compression via
+ * Attention-Error Bounds", project page, method overview step 1, Summarize:
+ * contiguous clusters, their mean keys and mean values, and metadata). X is
+ * a bf16 cache -- keys or values -- in the cache layout; the clusters are the
+ * windows of `window` tokens (the last one holding the rest; window 0 or
+ * >= t_max is one cluster per head). mean: fp32 [batch, heads, nw,
+ * head_dim] with nw = mkv_num_windows(t_max, window); mean[h][j] is the
+ * window's mean row, summed in fp32 in token order for windows of at most
+ * 128 tokens and as mkv_centroid sums for longer ones (then bit-identical
+ * to mkv_centroid). radius (NULL, or fp32 [batch, heads, nw]; windows of at
+ * most 128 tokens only, else MKV_ERR_UNSUPPORTED): radius[h][j] =
+ * max over the window's rows of |x_t - mean[h][j]|_2, the metadata behind a
+ * bound on how far a member's logit can drift from the mean's
+ * (|q.x_t - q.mean| <= |q| radius). Windows a short head does not have are
+ * not written. */
+mkv_status mkv_window_means(const void *X, mkv_shape shape, int32_t window, float *mean, float *radius,
+                            void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
 /* Scores (abstract: Euclidean distance to the key centroid; cosine baseline).
  * C as written by mkv_centroid. S: fp32 [batch, heads, t_max]; S[h][t] for
  * t < T_b is the score of token t against its window's centroid (fp32,
@@ -156,6 +174,33 @@ mkv_status mkv_compress(const void *K, const void *V, mkv_shape shape, double ra
                         const int32_t *n_keep, mkv_mode mode, int32_t window, int32_t keep_stride,
                         void *K_out, void *V_out, int32_t *idx, int32_t *kept,
                         void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
+/* Per-window-quota variant of WindowedManifoldKV (a reading of the
+ * abstract, which makes the centroid per window and says nothing more about
+ * the selection): instead of one top-n_keep per head, every window keeps its
+ * own share n_keep(|w|, ratio) of its tokens, the highest-scoring within it
+ * (ties to the lower index). mkv_num_keep_quota gives a T-token head's kept
+ * count, (nw-1)*n_keep(W, ratio) + n_keep(T-(nw-1)W, ratio); -1 on a bad
+ * argument. With window 0 or >= T it equals mkv_num_keep. */
+int32_t mkv_num_keep_quota(int32_t T, double ratio, int32_t window);
+
+/* Selection with per-window quotas, from scores S (as written by mkv_score
+ * with the same window): the kept indices of head h, ascending, into
+ * idx[h * keep_stride + slot] (window j's at slots from j * n_keep(W,
+ * ratio)), their count into kept[h]. keep_stride must be at least
+ * mkv_num_keep_quota(t_max, ratio, window). Needs the workspace's status
+ * word only. */
+mkv_status mkv_select_quota(const float *S, mkv_shape shape, double ratio, int32_t window, int32_t keep_stride,
+                            int32_t *idx, int32_t *kept, void *workspace, size_t workspace_bytes,
+                            mkv_stream_t stream);
+
+/* mkv_compress with per-window quotas: same centroids and scores, the
+ * selection of mkv_select_quota, then the row gather. Outputs as for
+ * mkv_compress (idx and kept may be NULL); keep_stride as for
+ * mkv_select_quota. */
+mkv_status mkv_compress_quota(const void *K, const void *V, mkv_shape shape, double ratio, mkv_mode mode,
+                              int32_t window, int32_t keep_stride, void *K_out, void *V_out, int32_t *idx,
+                              int32_t *kept, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
 /* Number of stages mkv_compress_profiled brackets with events: 6, one per
  * kernel -- piece sums (a1), window means (a1), scores (a2), top-k select

@@ -90,6 +90,10 @@ def _load():
         lib.oracle_select_quota.argtypes = [vp, i64, i64, f64, vp]
         lib.oracle_compress_head_quota.restype = i64
         lib.oracle_compress_head_quota.argtypes = [vp, vp, i64, i64, f64, i32, i64, vp, vp, vp, vp, vp]
+        lib.oracle_oja_scores.restype = None
+        lib.oracle_oja_scores.argtypes = [vp, i64, i64, vp, i64, vp, i64, vp]
+        lib.oracle_compress_head_oja.restype = i64
+        lib.oracle_compress_head_oja.argtypes = [vp, vp, i64, i64, vp, i64, vp, i64, i64, vp, vp, vp, vp]
         _lib = lib
         return lib
 
@@ -284,3 +288,34 @@ def compress_head_quota(K, V, ratio: float, mode="l2", window: int = 0):
     if got != n:
         raise ValueError("oracle_compress_head_quota failed")
     return {"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}
+
+
+def oja_scores(K, Q, U) -> np.ndarray:
+    """OjaKV reconstruction-error scores of one head: K [T, d] bf16 keys,
+    Q [M, d] bf16 query-window rows, U [d, r] basis (float; fp32 values are
+    used exactly). Returns float64 [T]."""
+    k, q = _bits(K), _bits(Q)
+    T, d = k.shape
+    u = np.ascontiguousarray(np.asarray(U, dtype=np.float64).reshape(d, -1))
+    if q.shape[1] != d:
+        raise ValueError("Q and K must share the head dim")
+    E = np.zeros(max(T, 1), dtype=np.float64)
+    _load().oracle_oja_scores(_ptr(k), T, d, _ptr(q), q.shape[0], _ptr(u), u.shape[1], _ptr(E))
+    return E[:T]
+
+
+def compress_head_oja(K, V, Q, U, n_keep: int):
+    """OjaKV full-rank selection of one head: dict(S, idx, K_out, V_out)."""
+    k, v, q = _bits(K), _bits(V), _bits(Q)
+    T, d = k.shape
+    u = np.ascontiguousarray(np.asarray(U, dtype=np.float64).reshape(d, -1))
+    E = np.zeros(max(T, 1), dtype=np.float64)
+    n = int(n_keep)
+    idx = np.zeros(max(n, 1), dtype=np.int32)
+    ko = np.zeros((max(n, 1), d), dtype=np.uint16)
+    vo = np.zeros((max(n, 1), d), dtype=np.uint16)
+    got = _load().oracle_compress_head_oja(_ptr(k), _ptr(v), T, d, _ptr(q), q.shape[0], _ptr(u), u.shape[1], n,
+                                           _ptr(E), _ptr(idx), _ptr(ko), _ptr(vo))
+    if got != n:
+        raise ValueError("oracle_compress_head_oja failed")
+    return {"S": E[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}

@@ -395,3 +395,63 @@ int64_t oracle_compress_head_quota(const uint16_t *K, const uint16_t *V, int64_t
     if (V_out) oracle_gather(V, d, idx, n, V_out);
     return n;
 }
+
+/* OjaKV reconstruction-error score, "OjaKV: Context-Aware Online Low-Rank
+ * KV Cache Compression" (deep notes of the ACL 2026 Findings paper), method
+ * details, error-based token selection for the hybrid storage: the residual
+ * r_t = k_t - U U^T k_t is the part of key t its low-rank reconstruction
+ * misses, and
+ *     e_t = (1/|W|) * sum over (head h, query q) in W of |q_{h,q}^T r_t / sqrt(d)|
+ * weighs it by the recent query window W of every query head that reads
+ * this KV head. The tokens with the largest errors stay at full rank (the
+ * top-k of the normalised errors; a per-head normaliser does not change the
+ * order, so the selection is the top-n_keep of e itself).
+ * K: T x d bf16 bits; Q: M x d bf16 bits, the window's query rows (group
+ * heads x recent positions, flattened, |W| = M); U: d x r doubles,
+ * row-major (column j is basis vector j). E: T doubles. */
+void oracle_oja_scores(const uint16_t *K, int64_t T, int64_t d, const uint16_t *Q, int64_t M,
+                       const double *U, int64_t r, double *E)
+{
+    double *k = (double *)malloc((size_t)d * sizeof(double));
+    double *y = (double *)malloc((size_t)(r > 0 ? r : 1) * sizeof(double));
+    double *res = (double *)malloc((size_t)d * sizeof(double));
+    if (!k || !y || !res) { free(k); free(y); free(res); return; }
+    double sqrt_d = sqrt((double)d);
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t i = 0; i < d; ++i) k[i] = oracle_bf16_to_double(K[t * d + i]);
+        for (int64_t j = 0; j < r; ++j) {          /* y = U^T k */
+            double s = 0.0;
+            for (int64_t i = 0; i < d; ++i) s += U[i * r + j] * k[i];
+            y[j] = s;
+        }
+        for (int64_t i = 0; i < d; ++i) {          /* r_t = k - U y */
+            double s = 0.0;
+            for (int64_t j = 0; j < r; ++j) s += U[i * r + j] * y[j];
+            res[i] = k[i] - s;
+        }
+        double acc = 0.0;
+        for (int64_t m = 0; m < M; ++m) {
+            double dot = 0.0;
+            for (int64_t i = 0; i < d; ++i) dot += oracle_bf16_to_double(Q[m * d + i]) * res[i];
+            acc += fabs(dot / sqrt_d);
+        }
+        E[t] = M > 0 ? acc / (double)M : 0.0;
+    }
+    free(k);
+    free(y);
+    free(res);
+}
+
+/* OjaKV's full-rank selection for one head: errors, top-n_keep (ties to the
+ * lower index, ascending), and the kept K/V rows. Returns n_keep or -1. */
+int64_t oracle_compress_head_oja(const uint16_t *K, const uint16_t *V, int64_t T, int64_t d, const uint16_t *Q,
+                                 int64_t M, const double *U, int64_t r, int64_t n_keep, double *E, int32_t *idx,
+                                 uint16_t *K_out, uint16_t *V_out)
+{
+    if (n_keep < 0 || n_keep > T) return -1;
+    oracle_oja_scores(K, T, d, Q, M, U, r, E);
+    if (oracle_select(E, T, n_keep, idx) != 0) return -1;
+    if (K_out) oracle_gather(K, d, idx, n_keep, K_out);
+    if (V_out) oracle_gather(V, d, idx, n_keep, V_out);
+    return n_keep;
+}

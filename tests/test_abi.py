@@ -150,3 +150,55 @@ def test_layer_budgets_match_the_oracle():
     for bad in ((0.0, 2.0), (2.0, 0.5), (float("nan"), 2.0)):
         with pytest.raises(mkv.MKVError):
             mkv.mkv_layer_budgets([0, 1], bad[0], bad[1], 10, [10, 10])
+
+
+def test_num_keep_quota_matches_the_oracle():
+    for T in (0, 1, 2, 7, 100, 1023, 4096, 5000):
+        for W in (0, 1, 3, 10, 256, 4096, 10000):
+            for r in (0.0, 0.2, 0.5, 0.75, 1.0):
+                assert mkv.mkv_num_keep_quota(T, r, W) == oracle.num_keep_quota(T, r, W), (T, W, r)
+    assert mkv.mkv_num_keep_quota(-1, 0.5, 4) == -1
+    assert mkv.mkv_num_keep_quota(10, 0.5, -4) == -1
+    assert mkv.mkv_num_keep_quota(10, 2.0, 4) == -1
+
+
+def test_window_means_and_quota_calls_reject_bad_arguments():
+    lib = mkv.load()
+    vp = ctypes.c_void_p
+    shp = _shape()
+    big = 1 << 40
+    # radius only for windows of at most 128 tokens
+    assert lib.mkv_window_means(vp(A), shp, 129, vp(A), vp(A), vp(A), big, None) == mkv.MKV_ERR_UNSUPPORTED
+    assert lib.mkv_window_means(vp(A), shp, 0, vp(A), vp(A), vp(A), big, None) == mkv.MKV_ERR_UNSUPPORTED
+    assert lib.mkv_window_means(vp(A), shp, -1, vp(A), None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_window_means(vp(A + 8), shp, 10, vp(A), None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_window_means(vp(A), shp, 10, vp(A + 4), None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_window_means(vp(A), shp, 10, vp(A), vp(A + 2), vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_window_means(vp(A), shp, 10, vp(A), None, vp(A), 16, None) == mkv.MKV_ERR_WORKSPACE
+    assert lib.mkv_window_means(vp(A), _shape(head_dim=64), 10, vp(A), None, vp(A), big, None) == \
+        mkv.MKV_ERR_UNSUPPORTED
+    # the quota selection needs room for every window's share
+    need = mkv.mkv_num_keep_quota(shp.t_max, 0.5, 3)
+    assert need > mkv.mkv_num_keep(shp.t_max, 0.5)
+    assert lib.mkv_select_quota(vp(A), shp, 0.5, 3, need - 1, vp(A), vp(A), vp(A), big, None) == \
+        mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_select_quota(vp(A), shp, 0.5, 3, need, None, vp(A), vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_select_quota(vp(A), shp, 0.5, -3, need, vp(A), vp(A), vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_compress_quota(vp(A), vp(A), shp, 0.5, 0, 3, need - 1, vp(A), vp(A), None, None, vp(A), big,
+                                  None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_compress_quota(vp(A), vp(A), shp, 0.5, 0, 3, need, vp(A), vp(A), None, None, vp(A), 1024,
+                                  None) == mkv.MKV_ERR_WORKSPACE
+    assert lib.mkv_compress_quota(vp(A), vp(A), _shape(batch=0), 0.5, 0, 3, need, vp(A), vp(A), None, None, vp(A),
+                                  big, None) == mkv.MKV_OK
+
+
+def test_quota_stride_bound_is_the_quota_total():
+    # one-token windows at ratio 0.8 keep nothing: a zero stride is enough,
+    # though the global selection of the same shape would need 205 slots
+    lib = mkv.load()
+    vp = ctypes.c_void_p
+    shp = _shape(batch=0)
+    assert mkv.mkv_num_keep_quota(shp.t_max, 0.8, 1) == 0
+    assert lib.mkv_compress_quota(vp(A), vp(A), shp, 0.8, 0, 1, 0, vp(A), vp(A), None, None, vp(A), 1 << 40,
+                                  None) == mkv.MKV_OK
+    assert _compress(shp, ratio=0.8, keep_stride=0) == mkv.MKV_ERR_INVALID_ARG

@@ -478,3 +478,101 @@ def test_compress_head_quota_rows_and_counts():
     np.testing.assert_array_equal(out["V_out"], vb[idx])
     # the scores are the windowed ones; only the selection differs
     np.testing.assert_array_equal(out["S"], oracle.scores(K, oracle.centroids(K, 512), 512, "l2"))
+
+
+# ---- OjaKV reconstruction-error score (OjaKV deep notes, method details) ----
+
+def _orthonormal(d, r, seed):
+    a = np.random.default_rng(seed).normal(size=(d, max(r, 1)))
+    q, _ = np.linalg.qr(a)
+    return q[:, :r]
+
+
+def _oja_inputs(T=60, M=12, d=32, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    K = (torch.randn(T, d, generator=g) * 2).to(torch.bfloat16)
+    Q = torch.randn(M, d, generator=g).to(torch.bfloat16)
+    return K, Q
+
+
+def test_oja_hand_case():
+    # U spans the first axis: k = (3,4) leaves r = (0,4); queries (1,2) and
+    # (0,-1) give |8| and |-4|, mean 6, over sqrt 2; k = (1,0) lies in the
+    # span (error 0); k = (0,2) gives |4|, |-2|, mean 3, over sqrt 2
+    E = oracle.oja_scores(_bf16([[3, 4], [1, 0], [0, 2]]), _bf16([[1, 2], [0, -1]]), np.array([[1.0], [0.0]]))
+    assert E[0] == pytest.approx(6 / math.sqrt(2), rel=1e-15)
+    assert E[1] == 0.0
+    assert E[2] == pytest.approx(3 / math.sqrt(2), rel=1e-15)
+
+
+def test_oja_without_a_basis_is_the_mean_absolute_attention_logit():
+    # r = 0: nothing is reconstructed, e_t = mean_q |q.k_t| / sqrt(d)
+    K, Q = _oja_inputs()
+    E = oracle.oja_scores(K, Q, np.zeros((32, 0)))
+    want = np.abs(_f64(Q) @ _f64(K).T).mean(axis=0) / math.sqrt(32)
+    np.testing.assert_allclose(E, want, rtol=1e-12)
+
+
+def test_oja_full_rank_basis_leaves_no_error():
+    K, Q = _oja_inputs()
+    E = oracle.oja_scores(K, Q, _orthonormal(32, 32, 1))
+    scale = np.abs(_f64(Q)).sum(axis=1).mean() * np.abs(_f64(K)).max() / math.sqrt(32)
+    assert np.all(E <= 1e-12 * scale)
+
+
+def test_oja_keys_inside_and_outside_the_span():
+    # U = the first 8 standard axes: keys zero beyond dim 8 are reconstructed
+    # exactly (error exactly 0); keys zero in dims < 8 are untouched
+    K, Q = _oja_inputs()
+    U = np.eye(32)[:, :8]
+    k = _f64(K)
+    inside = torch.from_numpy(np.where(np.arange(32) < 8, k, 0.0)).to(torch.bfloat16)
+    outside = torch.from_numpy(np.where(np.arange(32) >= 8, k, 0.0)).to(torch.bfloat16)
+    assert np.all(oracle.oja_scores(inside, Q, U) == 0.0)
+    want = np.abs(_f64(Q) @ _f64(outside).T).mean(axis=0) / math.sqrt(32)
+    np.testing.assert_allclose(oracle.oja_scores(outside, Q, U), want, rtol=1e-12)
+
+
+def test_oja_depends_on_the_span_only():
+    # U and U R (R orthogonal r x r) span the same space: same errors; a
+    # transposed or half-applied projector would break this
+    K, Q = _oja_inputs(seed=2)
+    U = _orthonormal(32, 10, 3)
+    R = _orthonormal(10, 10, 4)
+    np.testing.assert_allclose(oracle.oja_scores(K, Q, U @ R), oracle.oja_scores(K, Q, U), rtol=1e-10, atol=1e-13)
+
+
+def test_oja_symmetries():
+    K, Q = _oja_inputs(seed=5)
+    U = _orthonormal(32, 6, 6)
+    E = oracle.oja_scores(K, Q, U)
+    # the sign of a query does not matter; doubling every key doubles the
+    # errors exactly (powers of two scale every fp64 operation exactly)
+    np.testing.assert_array_equal(oracle.oja_scores(K, (-Q.float()).to(torch.bfloat16), U), E)
+    np.testing.assert_array_equal(oracle.oja_scores((K.float() * 2).to(torch.bfloat16), Q, U), 2 * E)
+    # the order of the window's queries does not matter (a mean)
+    perm = torch.randperm(Q.shape[0], generator=torch.Generator().manual_seed(0))
+    np.testing.assert_allclose(oracle.oja_scores(K, Q[perm], U), E, rtol=1e-13)
+
+
+def test_oja_equals_the_projected_query_form():
+    # q.(k - U U^T k) = (q - U U^T q).k because U U^T is symmetric (for any U,
+    # orthonormal or not): the form the GPU computes
+    K, Q = _oja_inputs(seed=7)
+    U = np.random.default_rng(8).normal(size=(32, 5)) * 0.3
+    P = np.eye(32) - U @ U.T
+    want = np.abs((_f64(Q) @ P) @ _f64(K).T).mean(axis=0) / math.sqrt(32)
+    np.testing.assert_allclose(oracle.oja_scores(K, Q, U), want, rtol=1e-10, atol=1e-12)
+
+
+def test_oja_selection_keeps_the_largest_errors():
+    K, Q = _oja_inputs(T=200, seed=9)
+    V = (K.float() + 1).to(torch.bfloat16)
+    U = _orthonormal(32, 8, 10)
+    out = oracle.compress_head_oja(K, V, Q, U, 50)
+    E = oracle.oja_scores(K, Q, U)
+    np.testing.assert_array_equal(out["S"], E)
+    order = sorted(range(200), key=lambda t: (-E[t], t))
+    assert out["idx"].tolist() == sorted(order[:50])
+    kb = K.contiguous().view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(out["K_out"], kb[out["idx"]])
