@@ -47,7 +47,7 @@ EXPORTED = (
     "mkv_compress_profiled", "mkv_compress_host", "mkv_device_status", "mkv_status_string",
     "mkv_compress_noalloc", "mkv_compress_single_pass", "mkv_set_single_pass", "mkv_layer_budgets",
     "mkv_inject_stalled_windows", "mkv_window_means", "mkv_num_keep_quota", "mkv_select_quota",
-    "mkv_compress_quota",
+    "mkv_compress_quota", "mkv_oja_workspace_size", "mkv_oja_score", "mkv_compress_oja",
 )
 
 
@@ -105,6 +105,10 @@ def load(build_if_missing: bool = True):
             "mkv_compress_noalloc": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
             "mkv_status_string": (ctypes.c_char_p, [i32]),
             "mkv_window_means": (i32, [vp, MkvShape, i32, vp, vp, vp, sz, vp]),
+            "mkv_oja_workspace_size": (sz, [MkvShape, i32]),
+            "mkv_oja_score": (i32, [vp, vp, vp, MkvShape, i32, i32, vp, vp, sz, vp]),
+            "mkv_compress_oja": (i32, [vp, vp, vp, vp, MkvShape, i32, i32, f64, vp, i32, vp, vp, vp, vp, vp, sz,
+                                       vp]),
             "mkv_num_keep_quota": (i32, [i32, f64, i32]),
             "mkv_select_quota": (i32, [vp, MkvShape, f64, i32, i32, vp, vp, vp, sz, vp]),
             "mkv_compress_quota": (i32, [vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
@@ -267,6 +271,33 @@ def mkv_compress_quota(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx
                                      int(window), int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx),
                                      _ptr(kept), _ptr(workspace), workspace.numel(), _stream(stream)),
            "mkv_compress_quota")
+
+
+def mkv_oja_workspace_size(shape: MkvShape, n_query: int) -> int:
+    return int(load().mkv_oja_workspace_size(shape, int(n_query)))
+
+
+def oja_workspace_for(K: torch.Tensor, n_query: int, seq_lens=None) -> torch.Tensor:
+    n = mkv_oja_workspace_size(shape_of(K, seq_lens), n_query)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=K.device)
+
+
+def mkv_oja_score(K, Q, U, S, workspace, seq_lens=None, stream=None):
+    """OjaKV-style reconstruction-error scores: K [B, H, T, 128] bf16,
+    Q [B, H, n_query, 128] bf16, U [B, H, 128, rank] fp32 -> S [B, H, T]."""
+    _need_cuda(K, Q, U, S, workspace, seq_lens)
+    _check(load().mkv_oja_score(_ptr(K), _ptr(Q), _ptr(U), shape_of(K, seq_lens), int(Q.shape[-2]),
+                                int(U.shape[-1]), _ptr(S), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mkv_oja_score")
+
+
+def mkv_compress_oja(K, V, Q, U, ratio, keep_stride, K_out, V_out, idx, kept, workspace, seq_lens=None, n_keep=None,
+                     stream=None):
+    _need_cuda(K, V, Q, U, K_out, V_out, idx, kept, workspace, seq_lens, n_keep)
+    _check(load().mkv_compress_oja(_ptr(K), _ptr(V), _ptr(Q), _ptr(U), shape_of(K, seq_lens), int(Q.shape[-2]),
+                                   int(U.shape[-1]), float(ratio), _ptr(n_keep), int(keep_stride), _ptr(K_out),
+                                   _ptr(V_out), _ptr(idx), _ptr(kept), _ptr(workspace), workspace.numel(),
+                                   _stream(stream)), "mkv_compress_oja")
 
 
 def mkv_compress_profiled(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, workspace, events,

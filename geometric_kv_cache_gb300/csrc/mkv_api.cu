@@ -407,6 +407,89 @@ mkv_status mkv_compress_quota(const void *K, const void *V, mkv_shape shape, dou
                         workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr, false, true);
 }
 
+size_t mkv_oja_workspace_size(mkv_shape shape, int32_t n_query)
+{
+    if (check_shape(shape) != MKV_OK || n_query < 16 || n_query > 256 || n_query % 16) return 0;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, 0);
+    return make_layout(g).total + round_up(oja_operand_bytes(g.n_heads, n_query), kAlign);
+}
+
+namespace {
+
+// Checks shared by the OjaKV entry points; on success *g and *L describe the
+// problem and the workspace.
+mkv_status oja_checks(const void *K, const void *Q, const float *U, const mkv_shape &s, int32_t n_query, int32_t rank,
+                      void *ws, size_t ws_bytes, Geometry *g, Layout *L)
+{
+    mkv_status rc = check_shape(s);
+    if (rc != MKV_OK) return rc;
+    if (!K || !Q || (rank > 0 && !U)) return MKV_ERR_INVALID_ARG;
+    if (!aligned(K, 16) || !aligned(Q, 16) || (U && !aligned(U, 4))) return MKV_ERR_INVALID_ARG;
+    if (n_query < 16 || n_query > 256 || n_query % 16 || rank < 0 || rank > kHeadDim) return MKV_ERR_INVALID_ARG;
+    *g = make_geometry(s.batch, s.heads, s.t_max, 0);
+    // TMA row coordinates are 32-bit
+    if ((uint64_t)g->n_heads * (uint64_t)s.t_max >= (1ull << 31) ||
+        (uint64_t)g->n_heads * 2u * (uint64_t)n_query >= (1ull << 31))
+        return MKV_ERR_UNSUPPORTED;
+    *L = make_layout(*g);
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < L->total + round_up(oja_operand_bytes(g->n_heads, n_query), kAlign))
+        return MKV_ERR_WORKSPACE;
+    return MKV_OK;
+}
+
+}  // namespace
+
+mkv_status mkv_oja_score(const void *K, const void *Q, const float *U, mkv_shape shape, int32_t n_query, int32_t rank,
+                         float *S, void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    Geometry g;
+    Layout L;
+    mkv_status rc = oja_checks(K, Q, U, shape, n_query, rank, workspace, workspace_bytes, &g, &L);
+    if (rc != MKV_OK) return rc;
+    if (!S || !aligned(S, 4)) return MKV_ERR_INVALID_ARG;
+    if (empty(shape)) return MKV_OK;
+    return cuda_status(launch_oja_scores(g, K, Q, U, shape.seq_lens, n_query, rank, region<void>(workspace, L.total), S,
+                                         region<uint32_t>(workspace, L.status), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mkv_status mkv_compress_oja(const void *K, const void *V, const void *Q, const float *U, mkv_shape shape,
+                            int32_t n_query, int32_t rank, double ratio, const int32_t *n_keep, int32_t keep_stride,
+                            void *K_out, void *V_out, int32_t *idx, int32_t *kept, void *workspace,
+                            size_t workspace_bytes, mkv_stream_t stream)
+{
+    Geometry g;
+    Layout L;
+    mkv_status rc = oja_checks(K, Q, U, shape, n_query, rank, workspace, workspace_bytes, &g, &L);
+    if (rc != MKV_OK) return rc;
+    if (!V) return MKV_ERR_INVALID_ARG;
+    rc = check_outputs(shape, ratio, n_keep, keep_stride, K, V, K_out, V_out, idx, kept, false);
+    if (rc != MKV_OK) return rc;
+    if (empty(shape)) return MKV_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t *status = region<uint32_t>(workspace, L.status);
+    float *S = region<float>(workspace, L.score);
+    cudaError_t e = launch_oja_scores(g, K, Q, U, shape.seq_lens, n_query, rank, region<void>(workspace, L.total), S,
+                                      status, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    // the selection back end of mkv_compress on these scores
+    int32_t *kept_w = kept ? kept : region<int32_t>(workspace, L.kept);
+    int32_t *idx_w = idx ? idx : region<int32_t>(workspace, L.idx);
+    const int32_t idx_stride = idx ? keep_stride : g.t_max;
+    mkv_cut *cut = region<mkv_cut>(workspace, L.cut);
+    int2 *chunk = region<int2>(workspace, L.chunk);
+    const bool emit = select_emits_indices(g);
+    if ((e = launch_select(g, S, shape.seq_lens, ratio, n_keep, keep_stride, cut, emit ? nullptr : chunk, kept_w,
+                           emit ? idx_w : nullptr, idx_stride, status, st)) != cudaSuccess)
+        return cuda_status(e);
+    if (!emit &&
+        (e = launch_compact(g, S, cut, chunk, shape.seq_lens, keep_stride, idx_w, idx_stride, status, st)) != cudaSuccess)
+        return cuda_status(e);
+    if (K_out &&
+        (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st)) != cudaSuccess)
+        return cuda_status(e);
+    return MKV_OK;
+}
+
 int32_t mkv_compress_num_stages(void) { return kCompressStages; }
 
 int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)

@@ -93,6 +93,13 @@ cudaError_t launch_select_quota(const Geometry &g, const float *S, const int32_t
 // the windows of a bf16 tensor, 0 < window <= kSmallWindowMax.
 cudaError_t launch_small_window_means(const PieceGeometry &g, const void *X, const int32_t *seq_lens, float *mean,
                                       float *radius, uint32_t *status, cudaStream_t st);
+// OjaKV-style reconstruction-error scores (mkv_oja.cu): the projected query
+// rows (hi + lo bf16, oja_operand_bytes in `qhl`), then the tcgen05
+// contraction writing S[head * t_max + t] for t < T_head.
+size_t oja_operand_bytes(int64_t n_heads, int32_t n_query);
+int oja_stages(int32_t n_query);
+cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, const float *U, const int32_t *seq_lens,
+                              int32_t n_query, int32_t rank, void *qhl, float *S, uint32_t *status, cudaStream_t st);
 cudaError_t launch_chunk_offsets(const Geometry &g, const float *S, const mkv_cut *cut,
                                  const int32_t *seq_lens, double ratio, const int32_t *n_keep,
                                  int32_t keep_stride, int2 *chunk_info, int32_t *kept,

@@ -1,0 +1,487 @@
+// sm_103a OjaKV-style reconstruction-error scores on the 5th-generation
+// tensor cores (tcgen05 + TMA + TMEM).
+//
+// "OjaKV: Context-Aware Online Low-Rank KV Cache Compression" (deep notes of
+// the ACL 2026 Findings paper), method details, error-based token
+// selection: with r_t = k_t - U U^T k_t the part of key t that the low-rank
+// basis U misses,
+//     e_t = (1/M) sum over the M rows q of the recent query window of |q . r_t| / sqrt(d),
+// and the tokens with the largest e_t stay at full rank.
+//
+// U U^T is symmetric, so q . r_t = (P q) . k_t with P = I - U U^T, for any U.
+// The work therefore splits into
+//  1. k_oja_project: P q for the M query rows of every head, in fp32 (CUDA
+//     cores; M x d x r per head, tiny next to the cache), stored as a pair of
+//     bf16 operands hi + lo with hi = bf16(Pq) and lo = bf16(Pq - hi), so
+//     that hi + lo holds Pq to about 2^-17 relative;
+//  2. k_oja_scores: a dense contraction of every key against the 2M operand
+//     rows -- D[t][m] = k_t . hi_m + k_t . lo_m -- on tcgen05.mma (kind::f16,
+//     bf16 x bf16 -> fp32 in TMEM), then e_t = scale * sum_m |D[t][m]|.
+//     Keys are bf16 and exact in the MMA, so the only rounding beyond fp32
+//     accumulation is the split's 2^-17.
+//
+// k_oja_scores is a persistent, warp-specialised kernel, one CTA per SM:
+//  * warp 0 (one thread): TMA producer. A tile is 128 tokens x 128 dims
+//    (32 KB) loaded as two 128-byte-swizzled boxes of 64 dims into a ring of
+//    shared-memory stages (full/empty mbarriers). When the head changes, it
+//    also loads that head's 2 x M operand rows (after the MMAs of the
+//    previous head have drained).
+//  * warp 1: allocates the TMEM accumulators (two buffers of M fp32
+//    columns); its lane 0 issues the MMAs (M_mma = 128 tokens on the TMEM
+//    lanes, N_mma = M query rows, 8 K-steps of 16 dims, twice for hi and
+//    lo) and commits them to the stage's empty barrier and the buffer's
+//    full barrier.
+//  * warps 2-5: epilogue. The warp with rank w (= warp id mod 4) owns TMEM
+//    lanes 32w..32w+31, i.e. one token per thread: it reads its row of M
+//    accumulators (tcgen05.ld 32x32b), sums their absolute values in column
+//    order, scales, stores e_t, and frees the buffer.
+// Every tile of 128 tokens costs 16 MMAs of 128 x M x 16 against 32 KB read
+// from HBM: the contraction keeps pace with HBM for M up to about 128
+// (2 x 128 flop per key byte, against a bf16 ridge near 280).
+//
+// Every mbarrier wait is bounded (1 s of %globaltimer). On a timeout the
+// kernel sets MKV_DEV_TIMEOUT, every role leaves its loop, the producer
+// waits (bounded) for its own copies in flight, the MMA thread waits for its
+// MMAs to complete, and the TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "mkv_device.cuh"
+#include "mkv_internal.h"
+
+namespace mkv {
+namespace {
+
+using namespace dev;
+
+constexpr int kTok = 128;                    // tokens per tile: the MMA's M, the TMEM lanes
+constexpr int kHalfBytes = kTok * 128;       // one 64-dim box of a tile: 128 rows x 128 B
+constexpr int kTileBytes = 2 * kHalfBytes;   // 32 KB
+constexpr int kMaxStages = 6;
+constexpr int kOjaThreads = 192;             // producer warp, MMA warp, 4 epilogue warps
+constexpr int kProjRows = 16;                // query rows per projection CTA
+constexpr int kProjThreads = 256;
+constexpr uint64_t kOjaWaitNs = 1000000000ull;
+constexpr int kSmemBudget = 227 * 1024;
+
+// ------------------------------------------------------ 1: P q, hi + lo --
+
+// Item = (head, block of 16 query rows). U [d, r] is staged in shared
+// memory with row stride r|1 (odd: both access patterns below are free of
+// bank conflicts), the rows of Q as fp32. y = U^T q and p = q - U y, summed
+// in index order; hi = bf16(p), lo = bf16(p - hi) (the difference is exact).
+__global__ void __launch_bounds__(kProjThreads)
+k_oja_project(const __nv_bfloat16 *__restrict__ Q, const float *__restrict__ U, int n_query, int rank,
+              int64_t n_items, __nv_bfloat16 *__restrict__ qhl)
+{
+    extern __shared__ float sm[];
+    const int us = rank | 1;
+    float *sU = sm;                       // [128][us]
+    float *sq = sU + kHeadDim * us;       // [16][128]
+    float *sy = sq + kProjRows * kHeadDim;  // [16][rank]
+    const int blocks = n_query / kProjRows;
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int64_t head = item / blocks;
+        const int m0 = (int)(item - head * blocks) * kProjRows;
+        const float *Uh = U + head * kHeadDim * rank;
+        for (int o = threadIdx.x; o < kHeadDim * rank; o += kProjThreads) {
+            const int i = o / rank, j = o - i * rank;
+            sU[i * us + j] = Uh[o];
+        }
+        const __nv_bfloat16 *Qh = Q + ((size_t)head * n_query + m0) * kHeadDim;
+        for (int o = threadIdx.x; o < kProjRows * kHeadDim; o += kProjThreads) sq[o] = __bfloat162float(Qh[o]);
+        __syncthreads();
+        for (int o = threadIdx.x; o < kProjRows * rank; o += kProjThreads) {
+            const int m = o / rank, j = o - m * rank;
+            float acc = 0.f;
+            for (int i = 0; i < kHeadDim; ++i) acc = fmaf(sq[m * kHeadDim + i], sU[i * us + j], acc);
+            sy[o] = acc;
+        }
+        __syncthreads();
+        for (int o = threadIdx.x; o < kProjRows * kHeadDim; o += kProjThreads) {
+            const int m = o >> 7, i = o & 127;
+            float acc = 0.f;
+            for (int j = 0; j < rank; ++j) acc = fmaf(sU[i * us + j], sy[m * rank + j], acc);
+            const float p = sq[o] - acc;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(p);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
+            const size_t row = (size_t)head * 2 * n_query + m0 + m;
+            qhl[row * kHeadDim + i] = hi;
+            qhl[(row + n_query) * kHeadDim + i] = lo;
+        }
+        __syncthreads();  // shared memory is reused by the next item
+    }
+}
+
+// ----------------------------------------------- 2: tcgen05 contraction --
+
+__device__ __forceinline__ uint32_t saddr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void bar_init(uint64_t *b, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive(uint64_t *b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+
+__device__ __forceinline__ void bar_expect(uint64_t *b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+
+// Bounded wait for phase `parity` of b. On timeout: flag, raise the CTA's
+// abort flag, return false. An abortable wait also returns false as soon as
+// another role raised the abort flag.
+__device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity, uint32_t *status, volatile uint32_t *abort_flag,
+                                         bool abortable)
+{
+    const uint32_t a = saddr(b);
+    const uint64_t t0 = global_ns();
+    for (uint32_t spin = 0;; ++spin) {
+        uint32_t done;
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                     : "=r"(done)
+                     : "r"(a), "r"(parity)
+                     : "memory");
+        if (done) return true;
+        if ((spin & 63u) == 63u) {
+            if (abortable && *abort_flag) return false;
+            if (global_ns() - t0 > kOjaWaitNs) {
+                atomicOr(status, MKV_DEV_TIMEOUT);
+                *abort_flag = 1u;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *b)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            saddr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(saddr(b))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzle layout TMA writes: rows of 128 B, 8-row groups 1024 B apart
+// (stride byte offset), leading byte offset unused for this layout,
+// descriptor version 1, layout type 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTok >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *b)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(b))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Sum of |x| over 16 consecutive accumulator columns of this thread's lane.
+__device__ __forceinline__ float tmem_abs_sum16(uint32_t taddr, float s)
+{
+    uint32_t v[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s += fabsf(__uint_as_float(v[i]));
+    return s;
+}
+
+struct TileWalk {
+    int64_t first, last;  // this CTA's tile range [first, last)
+    int tph;              // tiles per head
+};
+
+__device__ __forceinline__ TileWalk tile_range(int64_t n_heads, int t_max)
+{
+    TileWalk w;
+    w.tph = (t_max + kTok - 1) / kTok;
+    const int64_t total = n_heads * w.tph;
+    w.first = total * blockIdx.x / gridDim.x;
+    w.last = total * (blockIdx.x + 1) / gridDim.x;
+    return w;
+}
+
+__global__ void __launch_bounds__(kOjaThreads, 1)
+k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+             const int32_t *__restrict__ seq_lens, int heads, int t_max, int64_t n_heads, int n_query, int stages,
+             uint32_t tmem_cols, float scale, float *__restrict__ S, uint32_t *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *kring = smem;                              // stages x 32 KB
+    uint8_t *qbuf = smem + (size_t)stages * kTileBytes;  // [hi, lo][dims 0-63, 64-127][n_query rows x 128 B]
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], qfull, qempty, tfull[2], tempty[2], drain;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile uint32_t abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t q_block = (uint32_t)n_query * 128u;  // bytes of one [half] block of operand rows
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            bar_init(&full[s], 1);
+            bar_init(&empty[s], 1);
+        }
+        bar_init(&qfull, 1);
+        bar_init(&qempty, 1);
+        for (int b = 0; b < 2; ++b) {
+            bar_init(&tfull[b], 1);
+            bar_init(&tempty[b], 4);
+        }
+        bar_init(&drain, 1);
+        abort_flag = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base_sh)),
+                     "r"(tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    const TileWalk walk = tile_range(n_heads, t_max);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------- TMA producer --
+            uint32_t seq = 0, qseq = 0;
+            uint32_t last_parity[kMaxStages];
+            int64_t cur = -1;
+            for (int64_t tile = walk.first; tile < walk.last; ++tile) {
+                const int64_t head = tile / walk.tph;
+                const int t0 = (int)(tile - head * walk.tph) * kTok;
+                if (t0 >= head_len(seq_lens, head, heads, t_max, status, false)) continue;
+                if (head != cur) {
+                    if (qseq > 0 && !bar_wait(&qempty, (qseq - 1) & 1u, status, &abort_flag, true)) break;
+                    bar_expect(&qfull, 4u * q_block);
+                    for (int split = 0; split < 2; ++split)
+                        for (int half = 0; half < 2; ++half)
+                            tma_load_2d(qbuf + (split * 2 + half) * q_block, &tmap_q, half * 64,
+                                        (int)((head * 2 + split) * n_query), &qfull);
+                    ++qseq;
+                    cur = head;
+                }
+                const int s = (int)(seq % (uint32_t)stages);
+                if (seq >= (uint32_t)stages &&
+                    !bar_wait(&empty[s], ((seq / stages) - 1) & 1u, status, &abort_flag, true))
+                    break;
+                bar_expect(&full[s], (uint32_t)kTileBytes);
+                const int row = (int)(head * t_max + t0);
+                tma_load_2d(kring + (size_t)s * kTileBytes, &tmap_k, 0, row, &full[s]);
+                tma_load_2d(kring + (size_t)s * kTileBytes + kHalfBytes, &tmap_k, 64, row, &full[s]);
+                last_parity[s] = (seq / stages) & 1u;
+                ++seq;
+            }
+            // Every copy issued lands before the CTA may exit (bounded; after
+            // a normal run these phases are long complete).
+            const uint32_t issued = seq < (uint32_t)stages ? seq : (uint32_t)stages;
+            for (uint32_t s = 0; s < issued; ++s) bar_wait(&full[s], last_parity[s], status, &abort_flag, false);
+            if (qseq > 0) bar_wait(&qfull, (qseq - 1) & 1u, status, &abort_flag, false);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer --
+            const uint32_t idesc = idesc_bf16(n_query);
+            const uint32_t k_base = saddr(kring), q_base = saddr(qbuf);
+            uint32_t seq = 0, tcount = 0, qseq = 0;
+            int64_t cur = -1;
+            for (int64_t tile = walk.first; tile < walk.last; ++tile) {
+                const int64_t head = tile / walk.tph;
+                const int t0 = (int)(tile - head * walk.tph) * kTok;
+                if (t0 >= head_len(seq_lens, head, heads, t_max, status, false)) continue;
+                const uint32_t b = tcount & 1u, use = tcount >> 1;
+                if (use > 0 && !bar_wait(&tempty[b], (use - 1) & 1u, status, &abort_flag, true)) break;
+                fence_after();
+                if (head != cur) {
+                    if (qseq > 0) mma_commit(&qempty);  // the previous head's operand rows are free once its MMAs end
+                    if (!bar_wait(&qfull, qseq & 1u, status, &abort_flag, true)) break;
+                    ++qseq;
+                    cur = head;
+                }
+                const int s = (int)(seq % (uint32_t)stages);
+                if (!bar_wait(&full[s], (seq / stages) & 1u, status, &abort_flag, true)) break;
+                fence_after();
+                const uint32_t d_tmem = tmem + b * (uint32_t)n_query;
+                uint32_t accum = 0;
+                for (int half = 0; half < 2; ++half) {
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc(k_base + s * kTileBytes + half * kHalfBytes + kk * 32);
+                        for (int split = 0; split < 2; ++split) {
+                            const uint64_t bd = sdesc(q_base + (split * 2 + half) * q_block + kk * 32);
+                            mma_bf16(d_tmem, a, bd, idesc, accum);
+                            accum = 1;
+                        }
+                    }
+                }
+                mma_commit(&empty[s]);
+                mma_commit(&tfull[b]);
+                ++seq;
+                ++tcount;
+            }
+            // all MMAs issued by this thread complete before TMEM is freed
+            mma_commit(&drain);
+            bar_wait(&drain, 0, status, &abort_flag, false);
+        }
+    } else {
+        // ----------------------------------------------------- epilogue --
+        const uint32_t rank = (uint32_t)(warp & 3);  // TMEM lanes 32*rank .. 32*rank+31
+        uint32_t tcount = 0;
+        for (int64_t tile = walk.first; tile < walk.last; ++tile) {
+            const int64_t head = tile / walk.tph;
+            const int t0 = (int)(tile - head * walk.tph) * kTok;
+            const int T = head_len(seq_lens, head, heads, t_max, status, false);
+            if (t0 >= T) continue;
+            const uint32_t b = tcount & 1u, use = tcount >> 1;
+            if (!bar_wait(&tfull[b], use & 1u, status, &abort_flag, true)) break;
+            fence_after();
+            const uint32_t taddr = tmem + ((rank * 32u) << 16) + b * (uint32_t)n_query;
+            float acc = 0.f;
+            for (int c = 0; c < n_query; c += 16) acc = tmem_abs_sum16(taddr + (uint32_t)c, acc);
+            fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(&tempty[b]);
+            const int t = t0 + (int)rank * 32 + lane;
+            if (t < T) S[(size_t)head * t_max + t] = acc * scale;
+            ++tcount;
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
+    }
+}
+
+// --------------------------------------------------------------- host side --
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, 128] with 256-byte rows; boxes of 64 dims x box_rows
+// rows in the 128-byte swizzle layout.
+bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
+    const cuuint32_t box[2] = {64u, box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sms_of_current_device()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+size_t oja_operand_bytes(int64_t n_heads, int32_t n_query)
+{
+    return (size_t)n_heads * 2 * (size_t)n_query * kRowBytes;
+}
+
+int oja_stages(int32_t n_query)
+{
+    const int left = kSmemBudget - 1024 - 4 * n_query * 128;
+    const int s = left / kTileBytes;
+    return s > kMaxStages ? kMaxStages : s;
+}
+
+cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, const float *U, const int32_t *seq_lens,
+                              int32_t n_query, int32_t rank, void *qhl, float *S, uint32_t *status, cudaStream_t st)
+{
+    if (g.n_heads == 0 || g.t_max == 0) return cudaSuccess;
+    // 1: projected query rows, hi + lo
+    const int64_t items = g.n_heads * (n_query / kProjRows);
+    const size_t psmem = (size_t)(kHeadDim * (rank | 1) + kProjRows * kHeadDim + kProjRows * rank) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_oja_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+    if (e != cudaSuccess) return e;
+    const int pgrid = grid_for_items(reinterpret_cast<const void *>(k_oja_project), kProjThreads, psmem, items);
+    k_oja_project<<<pgrid, kProjThreads, psmem, st>>>(static_cast<const __nv_bfloat16 *>(Q), U, n_query, rank, items,
+                                                      static_cast<__nv_bfloat16 *>(qhl));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 2: the contraction
+    CUtensorMap mk, mq;
+    if (!make_map(&mk, K, (uint64_t)g.n_heads * g.t_max, kTok) ||
+        !make_map(&mq, qhl, (uint64_t)g.n_heads * 2 * n_query, (uint32_t)n_query))
+        return cudaErrorInvalidValue;
+    const int stages = oja_stages(n_query);
+    if (stages < 2) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + (size_t)stages * kTileBytes + 4 * (size_t)n_query * 128;
+    if ((e = cudaFuncSetAttribute(k_oja_scores, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+    uint32_t cols = 32;
+    while (cols < 2u * (uint32_t)n_query) cols *= 2;
+    const int64_t tiles = g.n_heads * ((g.t_max + kTok - 1) / kTok);
+    const int sms = sms_of_current_device();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    const float scale = (float)(1.0 / ((double)n_query * 11.313708498984760390));  // 1 / (M sqrt(128))
+    k_oja_scores<<<grid, kOjaThreads, smem, st>>>(mk, mq, seq_lens, g.heads, g.t_max, g.n_heads, n_query, stages, cols,
+                                                  scale, S, status);
+    return cudaGetLastError();
+}
+
+}  // namespace mkv

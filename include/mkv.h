@@ -202,6 +202,36 @@ mkv_status mkv_compress_quota(const void *K, const void *V, mkv_shape shape, dou
                               int32_t window, int32_t keep_stride, void *K_out, void *V_out, int32_t *idx,
                               int32_t *kept, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
+/* OjaKV-style reconstruction-error scores ("OjaKV: Context-Aware Online
+ * Low-Rank KV Cache Compression", deep notes of the ACL 2026 Findings paper,
+ * method details, error-based token selection for the hybrid storage):
+ *     e_t = (1/M) sum_m |q_m . (k_t - U U^T k_t)| / sqrt(head_dim),
+ * the error the low-rank basis U leaves in key t, weighed by the M rows q_m
+ * of the recent query window of the query heads that read this KV head.
+ * K: bf16 cache. Q: bf16 [batch, heads, n_query, head_dim], the window's
+ * query rows per KV head (group heads x recent positions, flattened; any
+ * order). U: fp32 [batch, heads, head_dim, rank], row-major (column j is
+ * basis vector j); it need not be orthonormal (the formula is used as is);
+ * may be NULL when rank = 0. n_query: a multiple of 16 in [16, 256]; rank in
+ * [0, head_dim]. S: fp32 [batch, heads, t_max], written for t < T_b.
+ * Computed as (P q_m) . k_t with P = I - U U^T: P q_m in fp32, split into
+ * two bf16 operands (hi + lo, about 2^-17 relative), contracted with the
+ * keys on the tensor cores in fp32. The workspace must hold
+ * mkv_oja_workspace_size(shape, n_query) bytes. MKV_ERR_UNSUPPORTED when
+ * batch*heads*t_max or batch*heads*2*n_query reaches 2^31 (32-bit TMA
+ * coordinates). */
+size_t mkv_oja_workspace_size(mkv_shape shape, int32_t n_query);
+mkv_status mkv_oja_score(const void *K, const void *Q, const float *U, mkv_shape shape, int32_t n_query,
+                         int32_t rank, float *S, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
+/* OjaKV's full-rank selection: the scores of mkv_oja_score, then the
+ * top-n_keep selection, compaction and gather of mkv_compress (keep the
+ * largest errors; ties to the lower index; outputs as for mkv_compress). */
+mkv_status mkv_compress_oja(const void *K, const void *V, const void *Q, const float *U, mkv_shape shape,
+                            int32_t n_query, int32_t rank, double ratio, const int32_t *n_keep,
+                            int32_t keep_stride, void *K_out, void *V_out, int32_t *idx, int32_t *kept,
+                            void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
 /* Number of stages mkv_compress_profiled brackets with events: 6, one per
  * kernel -- piece sums (a1), window means (a1), scores (a2), top-k select
  * (a3; also emits the kept indices when a head's scores fit in shared

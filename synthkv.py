@@ -199,3 +199,31 @@ def random_scores(n_heads: int, t: int, seed: int, tie_fraction: float = 0.0,
             pos = torch.randperm(t, generator=g, device=device)[:n]
             s[h, pos] = float(s[h, pos[0]].item())
     return s
+
+
+def make_oja_inputs(w: KVWorkload, seed: int, n_query: int, rank: int, device="cpu",
+                    heads: Optional[Sequence[int]] = None, query_scale: float = 1.0):
+    """Query windows and low-rank bases for the OjaKV-style scorer.
+
+    Returns (Q, U): Q bf16 [L*B, H, n_query, d] (the recent query rows of the
+    query heads that read each KV head, N(0, query_scale^2)), and U fp32
+    [L*B, H, d, rank] with orthonormal columns (a QR factor of a Gaussian
+    matrix, drawn on the CPU so both sides see the same basis). With
+    ``heads``, only those flat heads: [len(heads), n_query, d] and
+    [len(heads), d, rank]."""
+    ids = list(range(w.n_heads)) if heads is None else list(heads)
+    d = w.head_dim
+    Q = torch.empty((len(ids), n_query, d), dtype=torch.bfloat16, device=device)
+    U = torch.empty((len(ids), d, rank), dtype=torch.float32)
+    for j, h in enumerate(ids):
+        g = torch.Generator(device=device).manual_seed(_mix(seed, 0x0A, h))
+        Q[j].copy_((query_scale * torch.randn(n_query, d, generator=g, device=device)).to(torch.bfloat16))
+        if rank:
+            gc = torch.Generator().manual_seed(_mix(seed, 0x0B, h))
+            a = torch.randn(d, rank, generator=gc, dtype=torch.float64)
+            U[j].copy_(torch.linalg.qr(a).Q.to(torch.float32))
+    U = U.to(device)
+    if heads is None:
+        Q = Q.view(w.rows, w.heads, n_query, d)
+        U = U.view(w.rows, w.heads, d, rank)
+    return Q, U

@@ -202,3 +202,37 @@ def test_quota_stride_bound_is_the_quota_total():
     assert lib.mkv_compress_quota(vp(A), vp(A), shp, 0.8, 0, 1, 0, vp(A), vp(A), None, None, vp(A), 1 << 40,
                                   None) == mkv.MKV_OK
     assert _compress(shp, ratio=0.8, keep_stride=0) == mkv.MKV_ERR_INVALID_ARG
+
+
+def test_oja_calls_reject_bad_arguments():
+    lib = mkv.load()
+    vp = ctypes.c_void_p
+    shp = _shape()
+    big = 1 << 40
+    ws_need = mkv.mkv_oja_workspace_size(shp, 128)
+    assert ws_need > mkv.mkv_workspace_size(shp)
+    assert mkv.mkv_oja_workspace_size(shp, 100) == 0 and mkv.mkv_oja_workspace_size(shp, 512) == 0
+
+    def score(K=A, Q=A, U=A, shape=shp, n_query=128, rank=64, S=A, ws=A, ws_bytes=big):
+        return lib.mkv_oja_score(vp(K) if K else None, vp(Q) if Q else None, vp(U) if U else None, shape, n_query,
+                                 rank, vp(S) if S else None, vp(ws) if ws else None, ws_bytes, None)
+
+    assert score(n_query=100) == mkv.MKV_ERR_INVALID_ARG
+    assert score(n_query=0) == mkv.MKV_ERR_INVALID_ARG
+    assert score(n_query=272) == mkv.MKV_ERR_INVALID_ARG
+    assert score(rank=129) == mkv.MKV_ERR_INVALID_ARG
+    assert score(rank=-1) == mkv.MKV_ERR_INVALID_ARG
+    assert score(U=0) == mkv.MKV_ERR_INVALID_ARG
+    assert score(U=0, rank=0, shape=_shape(batch=0)) == mkv.MKV_OK
+    assert score(K=A + 8) == mkv.MKV_ERR_INVALID_ARG
+    assert score(Q=A + 8) == mkv.MKV_ERR_INVALID_ARG
+    assert score(S=0) == mkv.MKV_ERR_INVALID_ARG
+    assert score(ws_bytes=ws_need - 1) == mkv.MKV_ERR_WORKSPACE
+    assert score(ws=A + 16) == mkv.MKV_ERR_WORKSPACE
+    assert score(shape=_shape(head_dim=64)) == mkv.MKV_ERR_UNSUPPORTED
+    # 32-bit TMA row coordinates
+    assert score(shape=_shape(batch=1024, heads=64, t_max=32768)) == mkv.MKV_ERR_UNSUPPORTED
+    assert lib.mkv_compress_oja(vp(A), None, vp(A), vp(A), shp, 128, 64, 0.5, None, 512, vp(A), vp(A), None, None,
+                                vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert lib.mkv_compress_oja(vp(A), vp(A), vp(A), vp(A), shp, 128, 64, 0.5, None, 100, vp(A), vp(A), None, None,
+                                vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
