@@ -429,6 +429,148 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------ the widened paths (NEXT) --
+
+def _timed(fn, steps, stream, torch):
+    """Mean ms of fn() over `steps` calls, CUDA events on the launching stream."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_secondary(args):
+    """One JSON line for a widened path (rank 0, one GPU): the OjaKV scorer
+    and its selection, the cluster summaries, or the per-window quota."""
+    import torch
+
+    import geometric_kv_cache_gb300 as mkv
+
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mkv.load()
+    stream = torch.cuda.current_stream(dev)
+    peaks = measured_peaks()
+    hbm = peaks["hbm_gbs"]
+    steps = args.steps
+    if args.path == "oja":
+        w = synthkv.WORKLOADS[args.workload]
+        K, V, lens = synthkv.make_kv(w, seed=args.seed, device=dev)
+        M, r, ratio = args.oja_queries, args.oja_rank, 0.5
+        Q, U = synthkv.make_oja_inputs(w, args.seed, M, r, device=dev)
+        T = w.t_max
+        ks = mkv.mkv_num_keep(T, ratio)
+        ws = mkv.oja_workspace_for(K, M, lens)
+        S = torch.empty(K.shape[:3], device=dev)
+        Ko = torch.empty((w.rows, w.heads, ks, 128), dtype=torch.bfloat16, device=dev)
+        Vo = torch.empty_like(Ko)
+        idx = torch.empty((w.rows, w.heads, ks), dtype=torch.int32, device=dev)
+        kept = torch.empty((w.rows, w.heads), dtype=torch.int32, device=dev)
+
+        def step():
+            mkv.mkv_compress_oja(K, V, Q, U, ratio, ks, Ko, Vo, idx, kept, ws, lens, stream=stream)
+
+        def score():
+            mkv.mkv_oja_score(K, Q, U, S, ws, lens, stream=stream)
+        for _ in range(max(3, args.warmup)):
+            step()
+            score()
+        with ClockSampler(dev.index or 0) as clocks:
+            ms = _timed(step, steps, stream, torch)
+        ms_score = _timed(score, steps, stream, torch)
+        if mkv.mkv_device_status(ws, stream) != 0:
+            raise RuntimeError("device status nonzero")
+        tokens = w.n_heads * T
+        kbytes = tokens * (256 + 4)
+        flops = 2.0 * 2 * M * 128 * tokens
+        achieved = kbytes / (ms_score / 1e3) / 1e9
+        tflops = flops / (ms_score / 1e3) / 1e12
+        line = {"metric": "OjaKV-style full-rank selection: KV tokens scored (reconstruction error over the query "
+                          "window) + selected + compacted per second",
+                "value": tokens / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16 x bf16 -> f32 (tcgen05), f32",
+                "data": "synthetic (seeded)",
+                "config": {"workload": w.name, "heads_total": w.n_heads, "t": T, "n_query": M, "rank": r,
+                           "ratio": ratio, "keep_per_head": ks},
+                "roofline": {"bound": "hbm", "kernel": "oja_score (k_oja_project + k_oja_scores)",
+                             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                             "peak_source": peaks["source"], "ms_per_launch": ms_score,
+                             "algorithmic_bytes_per_launch": kbytes,
+                             "tensor": {"achieved_tflops": tflops, "flops_per_launch": flops,
+                                        "note": "2 x 2 x n_query x 128 flop per token (hi and lo operand rows)"}},
+                "clocks": clocks.summary(), "gpu_launches": steps * 4}
+    elif args.path == "summaries":
+        w = synthkv.WORKLOADS[args.workload]
+        K, V, lens = synthkv.make_kv(w, seed=args.seed, device=dev)
+        W = args.cluster
+        nw = mkv.mkv_num_windows(w.t_max, W)
+        ws = mkv.workspace_for(K, W, lens)
+        Km = torch.empty((w.rows, w.heads, nw, 128), device=dev)
+        Vm = torch.empty_like(Km)
+        Kr = torch.empty((w.rows, w.heads, nw), device=dev)
+
+        def step():
+            mkv.mkv_window_means(K, W, Km, ws, radius=Kr, seq_lens=lens, stream=stream)
+            mkv.mkv_window_means(V, W, Vm, ws, seq_lens=lens, stream=stream)
+        for _ in range(max(3, args.warmup)):
+            step()
+        with ClockSampler(dev.index or 0) as clocks:
+            ms = _timed(step, steps, stream, torch)
+        if mkv.mkv_device_status(ws, stream) != 0:
+            raise RuntimeError("device status nonzero")
+        tokens = w.n_heads * w.t_max
+        nbytes = 2 * tokens * 256 + w.n_heads * nw * (2 * 512 + 4)
+        achieved = nbytes / (ms / 1e3) / 1e9
+        line = {"metric": "cluster summaries (mean K, mean V, K radius per cluster): KV tokens summarised per second",
+                "value": tokens / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "dtype": "f32", "data": "synthetic (seeded)",
+                "config": {"workload": w.name, "heads_total": w.n_heads, "t": w.t_max, "cluster": W},
+                "roofline": {"bound": "hbm", "kernel": "k_small_window_means (K with radius, then V)",
+                             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                             "peak_source": peaks["source"], "algorithmic_bytes_per_launch": nbytes},
+                "clocks": clocks.summary(), "gpu_launches": steps * 2}
+    else:  # quota
+        w = synthkv.WORKLOADS["qwen3-8b-kv-t64k-w4096"] if args.workload == synthkv.BENCH_WORKLOAD else \
+            synthkv.WORKLOADS[args.workload]
+        K, V, lens = synthkv.make_kv(w, seed=args.seed, device=dev)
+        mode, window, ratio = w.runs[0]
+        window = window or 4096
+        ks = mkv.mkv_num_keep_quota(w.t_max, ratio, window)
+        ws = mkv.workspace_for(K, window, lens)
+        Ko = torch.empty((w.rows, w.heads, ks, 128), dtype=torch.bfloat16, device=dev)
+        Vo = torch.empty_like(Ko)
+        idx = torch.empty((w.rows, w.heads, ks), dtype=torch.int32, device=dev)
+        kept = torch.empty((w.rows, w.heads), dtype=torch.int32, device=dev)
+
+        def step():
+            mkv.mkv_compress_quota(K, V, ratio, mode, window, ks, Ko, Vo, idx, kept, ws, lens, stream=stream)
+        for _ in range(max(3, args.warmup)):
+            step()
+        with ClockSampler(dev.index or 0) as clocks:
+            ms = _timed(step, steps, stream, torch)
+        if mkv.mkv_device_status(ws, stream) != 0:
+            raise RuntimeError("device status nonzero")
+        tokens = w.n_heads * w.t_max
+        nbytes = 4 * tokens * 128 + 8 * w.n_heads * ks * 128
+        achieved = nbytes / (ms / 1e3) / 1e9
+        line = {"metric": "WindowedManifoldKV with per-window quotas: KV tokens scored+compacted per second",
+                "value": tokens / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "dtype": "f32", "data": "synthetic (seeded)",
+                "config": {"workload": w.name, "heads_total": w.n_heads, "t": w.t_max, "mode": mode,
+                           "window": window, "ratio": ratio, "keep_per_head": ks},
+                "hbm": {"path_bytes_per_step": nbytes, "achieved_gbs": achieved, "frac_of_measured": achieved / hbm,
+                        "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS},
+                "clocks": clocks.summary(), "gpu_launches": steps * 5}
+    line["path"] = args.path
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,6 +585,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle time for --impl reference")
+    ap.add_argument("--path", choices=["manifold", "oja", "summaries", "quota"], default="manifold",
+                    help="manifold: the headline path; the others time a widened path (one GPU, own JSON line)")
+    ap.add_argument("--oja-queries", type=int, default=128, help="query-window rows per KV head (--path oja)")
+    ap.add_argument("--oja-rank", type=int, default=64, help="basis rank (--path oja)")
+    ap.add_argument("--cluster", type=int, default=10, help="cluster length (--path summaries)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
                     help="per-kernel DRAM bytes per launch from an ncu capture (null when absent)")
     args = ap.parse_args(argv)
@@ -461,6 +608,8 @@ def main(argv=None):
             args.traffic = t.get("bytes_per_launch")
     if args.impl == "reference":
         run_reference(args)
+    elif args.path != "manifold":
+        run_secondary(args)
     else:
         run_ours(args)
 

@@ -47,7 +47,7 @@ EXPORTED = (
     "mkv_compress_profiled", "mkv_compress_host", "mkv_device_status", "mkv_status_string",
     "mkv_compress_noalloc", "mkv_compress_single_pass", "mkv_set_single_pass", "mkv_layer_budgets",
     "mkv_inject_stalled_windows", "mkv_window_means", "mkv_num_keep_quota", "mkv_select_quota",
-    "mkv_compress_quota", "mkv_oja_workspace_size", "mkv_oja_score", "mkv_compress_oja",
+    "mkv_compress_quota", "mkv_oja_workspace_size", "mkv_oja_score", "mkv_compress_oja", "mkv_oja_score_profiled",
 )
 
 
@@ -107,6 +107,7 @@ def load(build_if_missing: bool = True):
             "mkv_window_means": (i32, [vp, MkvShape, i32, vp, vp, vp, sz, vp]),
             "mkv_oja_workspace_size": (sz, [MkvShape, i32]),
             "mkv_oja_score": (i32, [vp, vp, vp, MkvShape, i32, i32, vp, vp, sz, vp]),
+            "mkv_oja_score_profiled": (i32, [vp, vp, vp, MkvShape, i32, i32, vp, vp, sz, vp, ctypes.POINTER(vp), i32]),
             "mkv_compress_oja": (i32, [vp, vp, vp, vp, MkvShape, i32, i32, f64, vp, i32, vp, vp, vp, vp, vp, sz,
                                        vp]),
             "mkv_num_keep_quota": (i32, [i32, f64, i32]),
@@ -289,6 +290,19 @@ def mkv_oja_score(K, Q, U, S, workspace, seq_lens=None, stream=None):
     _check(load().mkv_oja_score(_ptr(K), _ptr(Q), _ptr(U), shape_of(K, seq_lens), int(Q.shape[-2]),
                                 int(U.shape[-1]), _ptr(S), _ptr(workspace), workspace.numel(), _stream(stream)),
            "mkv_oja_score")
+
+
+def mkv_oja_score_profiled(K, Q, U, S, workspace, events, seq_lens=None, stream=None):
+    """mkv_oja_score with three torch.cuda.Event objects recorded around its
+    two kernels (query projection, contraction)."""
+    _need_cuda(K, Q, U, S, workspace, seq_lens)
+    s = torch.cuda.current_stream() if stream is None else stream
+    for e in events:
+        e.record(s)  # creates the event handles lazily; re-recorded below
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(load().mkv_oja_score_profiled(_ptr(K), _ptr(Q), _ptr(U), shape_of(K, seq_lens), int(Q.shape[-2]),
+                                         int(U.shape[-1]), _ptr(S), _ptr(workspace), workspace.numel(),
+                                         _stream(s), arr, len(events)), "mkv_oja_score_profiled")
 
 
 def mkv_compress_oja(K, V, Q, U, ratio, keep_stride, K_out, V_out, idx, kept, workspace, seq_lens=None, n_keep=None,

@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <vector>
 
 #include "mkv_internal.h"
@@ -89,6 +90,45 @@ T *region(void *ws, size_t off)
 }
 
 mkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MKV_OK : MKV_ERR_CUDA; }
+
+// mkv_compress_host splits the batch rows into up to this many chunks, so
+// that the copies of one chunk overlap the kernels and copies of others.
+constexpr int32_t kHostChunks = 8;
+
+// Library-owned copy streams and events of one device (created on first use,
+// kept for the life of the process; the mutex serialises enqueueing).
+// Keys and values are copied in on two streams (two copy engines move more
+// than one), the results out on a third.
+struct CopyStreams {
+    std::mutex mu;
+    cudaStream_t in[2] = {nullptr, nullptr}, out = nullptr;
+    cudaEvent_t start = nullptr, out_done = nullptr;
+    cudaEvent_t in_done[2][kHostChunks + 1] = {};
+    cudaEvent_t comp_done[kHostChunks] = {};
+};
+
+CopyStreams *copy_streams()
+{
+    static std::mutex mu;
+    static CopyStreams *table[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (table[dev]) return table[dev];
+    CopyStreams *cs = new CopyStreams();
+    const unsigned ef = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&cs->in[0], cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&cs->in[1], cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&cs->out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&cs->start, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&cs->out_done, ef) == cudaSuccess;
+    for (int k = 0; k < 2; ++k)
+        for (int i = 0; ok && i <= kHostChunks; ++i) ok = cudaEventCreateWithFlags(&cs->in_done[k][i], ef) == cudaSuccess;
+    for (int i = 0; ok && i < kHostChunks; ++i) ok = cudaEventCreateWithFlags(&cs->comp_done[i], ef) == cudaSuccess;
+    if (!ok) return nullptr;  // (the partial set is leaked; a CUDA error here is not recoverable anyway)
+    table[dev] = cs;
+    return cs;
+}
 
 // Checks of mkv_compact / mkv_compress outputs.
 // quota_window > 0: per-window quotas, whose kept count bounds the stride.
@@ -424,7 +464,7 @@ mkv_status oja_checks(const void *K, const void *Q, const float *U, const mkv_sh
     mkv_status rc = check_shape(s);
     if (rc != MKV_OK) return rc;
     if (!K || !Q || (rank > 0 && !U)) return MKV_ERR_INVALID_ARG;
-    if (!aligned(K, 16) || !aligned(Q, 16) || (U && !aligned(U, 4))) return MKV_ERR_INVALID_ARG;
+    if (!aligned(K, 16) || !aligned(Q, 16) || (U && !aligned(U, 16))) return MKV_ERR_INVALID_ARG;
     if (n_query < 16 || n_query > 256 || n_query % 16 || rank < 0 || rank > kHeadDim) return MKV_ERR_INVALID_ARG;
     *g = make_geometry(s.batch, s.heads, s.t_max, 0);
     // TMA row coordinates are 32-bit
@@ -450,6 +490,22 @@ mkv_status mkv_oja_score(const void *K, const void *Q, const float *U, mkv_shape
     if (empty(shape)) return MKV_OK;
     return cuda_status(launch_oja_scores(g, K, Q, U, shape.seq_lens, n_query, rank, region<void>(workspace, L.total), S,
                                          region<uint32_t>(workspace, L.status), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mkv_status mkv_oja_score_profiled(const void *K, const void *Q, const float *U, mkv_shape shape, int32_t n_query,
+                                  int32_t rank, float *S, void *workspace, size_t workspace_bytes, mkv_stream_t stream,
+                                  void *const *events, int32_t n_events)
+{
+    if (!events || n_events < 3 || !events[0] || !events[1] || !events[2]) return MKV_ERR_INVALID_ARG;
+    Geometry g;
+    Layout L;
+    mkv_status rc = oja_checks(K, Q, U, shape, n_query, rank, workspace, workspace_bytes, &g, &L);
+    if (rc != MKV_OK) return rc;
+    if (!S || !aligned(S, 4)) return MKV_ERR_INVALID_ARG;
+    if (empty(shape)) return MKV_OK;
+    return cuda_status(launch_oja_scores(g, K, Q, U, shape.seq_lens, n_query, rank, region<void>(workspace, L.total), S,
+                                         region<uint32_t>(workspace, L.status), reinterpret_cast<cudaStream_t>(stream),
+                                         events));
 }
 
 mkv_status mkv_compress_oja(const void *K, const void *V, const void *Q, const float *U, mkv_shape shape,
@@ -600,24 +656,66 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
     if (window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE)) return MKV_ERR_INVALID_ARG;
     const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window);
     if ((rc = check_ws(make_layout(g), workspace, workspace_bytes)) != MKV_OK) return rc;
+    if (empty(shape)) return MKV_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t in_bytes = (size_t)g.n_heads * shape.t_max * kRowBytes;
-    const size_t out_rows = (size_t)g.n_heads * keep_stride;
-    if (in_bytes && (cudaMemcpyAsync(dK, hK, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-                     cudaMemcpyAsync(dV, hV, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess))
+    CopyStreams *cs = copy_streams();
+    if (!cs) return MKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(cs->mu);
+    // rows of the batch per chunk: up to kHostChunks chunks
+    const int32_t per = (shape.batch + kHostChunks - 1) / kHostChunks;
+    const int32_t chunks = (shape.batch + per - 1) / per;
+    const size_t in_row = (size_t)shape.heads * shape.t_max * kRowBytes;      // bytes of one batch row of K
+    const size_t out_row = (size_t)shape.heads * keep_stride * kRowBytes;     // of K_out
+    const size_t idx_row = (size_t)shape.heads * keep_stride * sizeof(int32_t);
+    const size_t kept_row = (size_t)shape.heads * sizeof(int32_t);
+    auto bytes_at = [](const void *p, size_t off) { return static_cast<const uint8_t *>(p) + off; };
+    auto wbytes_at = [](void *p, size_t off) { return static_cast<uint8_t *>(p) + off; };
+    // the copies wait for earlier work on the caller's stream (earlier users of the buffers)
+    if (cudaEventRecord(cs->start, st) != cudaSuccess || cudaStreamWaitEvent(cs->in[0], cs->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(cs->in[1], cs->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(cs->out, cs->start, 0) != cudaSuccess)
         return MKV_ERR_CUDA;
-    rc = run_compress(dK, dV, shape, ratio, nullptr, mode, window, keep_stride, dK_out, dV_out, d_idx, d_kept,
-                      workspace, workspace_bytes, st, nullptr);
-    if (rc != MKV_OK) return rc;
-    if (out_rows && hK_out && cudaMemcpyAsync(hK_out, dK_out, out_rows * kRowBytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    for (int32_t c = 0; c < chunks; ++c) {
+        const int32_t r0 = c * per, rows = std::min(per, shape.batch - r0);
+        const size_t ib = (size_t)rows * in_row, io = (size_t)r0 * in_row;
+        if (cudaMemcpyAsync(wbytes_at(dK, io), bytes_at(hK, io), ib, cudaMemcpyHostToDevice, cs->in[0]) != cudaSuccess ||
+            cudaMemcpyAsync(wbytes_at(dV, io), bytes_at(hV, io), ib, cudaMemcpyHostToDevice, cs->in[1]) != cudaSuccess ||
+            cudaEventRecord(cs->in_done[0][c], cs->in[0]) != cudaSuccess ||
+            cudaEventRecord(cs->in_done[1][c], cs->in[1]) != cudaSuccess ||
+            cudaStreamWaitEvent(st, cs->in_done[0][c], 0) != cudaSuccess ||
+            cudaStreamWaitEvent(st, cs->in_done[1][c], 0) != cudaSuccess)
+            return MKV_ERR_CUDA;
+        mkv_shape sub = shape;
+        sub.batch = rows;
+        sub.seq_lens = shape.seq_lens ? shape.seq_lens + r0 : nullptr;
+        const size_t oo = (size_t)r0 * out_row;
+        int32_t *ci = reinterpret_cast<int32_t *>(wbytes_at(d_idx, (size_t)r0 * idx_row));
+        int32_t *ck = reinterpret_cast<int32_t *>(wbytes_at(d_kept, (size_t)r0 * kept_row));
+        rc = run_compress(bytes_at(dK, io), bytes_at(dV, io), sub, ratio, nullptr, mode, window, keep_stride,
+                          wbytes_at(dK_out, oo), wbytes_at(dV_out, oo), ci, ck, workspace, workspace_bytes, st, nullptr);
+        if (rc != MKV_OK) return rc;
+        if (cudaEventRecord(cs->comp_done[c], st) != cudaSuccess || cudaStreamWaitEvent(cs->out, cs->comp_done[c], 0) != cudaSuccess)
+            return MKV_ERR_CUDA;
+        const size_t ob = (size_t)rows * out_row;
+        if (hK_out && ob && cudaMemcpyAsync(wbytes_at(hK_out, oo), wbytes_at(dK_out, oo), ob, cudaMemcpyDeviceToHost, cs->out) != cudaSuccess)
+            return MKV_ERR_CUDA;
+        if (hV_out && ob && cudaMemcpyAsync(wbytes_at(hV_out, oo), wbytes_at(dV_out, oo), ob, cudaMemcpyDeviceToHost, cs->out) != cudaSuccess)
+            return MKV_ERR_CUDA;
+        if (h_idx && rows * idx_row &&
+            cudaMemcpyAsync(wbytes_at(h_idx, (size_t)r0 * idx_row), ci, (size_t)rows * idx_row, cudaMemcpyDeviceToHost,
+                            cs->out) != cudaSuccess)
+            return MKV_ERR_CUDA;
+        if (h_kept && cudaMemcpyAsync(wbytes_at(h_kept, (size_t)r0 * kept_row), ck, (size_t)rows * kept_row,
+                                      cudaMemcpyDeviceToHost, cs->out) != cudaSuccess)
+            return MKV_ERR_CUDA;
+    }
+    // the caller's stream resumes once every copy has landed
+    if (cudaEventRecord(cs->out_done, cs->out) != cudaSuccess || cudaStreamWaitEvent(st, cs->out_done, 0) != cudaSuccess)
         return MKV_ERR_CUDA;
-    if (out_rows && hV_out && cudaMemcpyAsync(hV_out, dV_out, out_rows * kRowBytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return MKV_ERR_CUDA;
-    if (out_rows && h_idx && cudaMemcpyAsync(h_idx, d_idx, out_rows * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return MKV_ERR_CUDA;
-    if (g.n_heads && h_kept &&
-        cudaMemcpyAsync(h_kept, d_kept, (size_t)g.n_heads * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return MKV_ERR_CUDA;
+    for (int k = 0; k < 2; ++k)
+        if (cudaEventRecord(cs->in_done[k][kHostChunks], cs->in[k]) != cudaSuccess ||
+            cudaStreamWaitEvent(st, cs->in_done[k][kHostChunks], 0) != cudaSuccess)
+            return MKV_ERR_CUDA;
     return MKV_OK;
 }
 

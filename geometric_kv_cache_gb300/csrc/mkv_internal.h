@@ -99,7 +99,8 @@ cudaError_t launch_small_window_means(const PieceGeometry &g, const void *X, con
 size_t oja_operand_bytes(int64_t n_heads, int32_t n_query);
 int oja_stages(int32_t n_query);
 cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, const float *U, const int32_t *seq_lens,
-                              int32_t n_query, int32_t rank, void *qhl, float *S, uint32_t *status, cudaStream_t st);
+                              int32_t n_query, int32_t rank, void *qhl, float *S, uint32_t *status, cudaStream_t st,
+                              void *const *events = nullptr);
 cudaError_t launch_chunk_offsets(const Geometry &g, const float *S, const mkv_cut *cut,
                                  const int32_t *seq_lens, double ratio, const int32_t *n_keep,
                                  int32_t keep_stride, int2 *chunk_info, int32_t *kept,

@@ -26,18 +26,20 @@
 //    shared-memory stages (full/empty mbarriers). When the head changes, it
 //    also loads that head's 2 x M operand rows (after the MMAs of the
 //    previous head have drained).
-//  * warp 1: allocates the TMEM accumulators (two buffers of M fp32
-//    columns); its lane 0 issues the MMAs (M_mma = 128 tokens on the TMEM
-//    lanes, N_mma = M query rows, 8 K-steps of 16 dims, twice for hi and
-//    lo) and commits them to the stage's empty barrier and the buffer's
-//    full barrier.
+//  * warp 1: allocates the TMEM accumulators (two buffers); its lane 0
+//    issues the MMAs -- M_mma = 128 tokens on the TMEM lanes, 8 K-steps of
+//    16 dims, each one MMA with N_mma = 2M operand rows (hi and lo stacked,
+//    M <= 128) or two with N_mma = M accumulating hi and lo together
+//    (M > 128) -- and commits them to the stage's empty barrier and the
+//    buffer's full barrier. An MMA costs about the same issue time for any
+//    N up to 128, so fewer, wider MMAs per tile are what keeps pace with HBM.
 //  * warps 2-5: epilogue. The warp with rank w (= warp id mod 4) owns TMEM
-//    lanes 32w..32w+31, i.e. one token per thread: it reads its row of M
-//    accumulators (tcgen05.ld 32x32b), sums their absolute values in column
-//    order, scales, stores e_t, and frees the buffer.
-// Every tile of 128 tokens costs 16 MMAs of 128 x M x 16 against 32 KB read
-// from HBM: the contraction keeps pace with HBM for M up to about 128
-// (2 x 128 flop per key byte, against a bf16 ridge near 280).
+//    lanes 32w..32w+31, i.e. one token per thread: it reads its row of the
+//    accumulator (tcgen05.ld 32x32b), adds the hi and lo halves of each
+//    query column, sums their absolute values in column order, scales,
+//    stores e_t, and frees the buffer.
+// Every tile of 128 tokens costs 8 MMAs of 128 x 2M x 16 against 32 KB read
+// from HBM (2 x 2M flop per key byte, against a bf16 ridge near 280).
 //
 // Every mbarrier wait is bounded (1 s of %globaltimer). On a timeout the
 // kernel sets MKV_DEV_TIMEOUT, every role leaves its loop, the producer
@@ -64,55 +66,121 @@ constexpr int kHalfBytes = kTok * 128;       // one 64-dim box of a tile: 128 ro
 constexpr int kTileBytes = 2 * kHalfBytes;   // 32 KB
 constexpr int kMaxStages = 6;
 constexpr int kOjaThreads = 192;             // producer warp, MMA warp, 4 epilogue warps
-constexpr int kProjRows = 16;                // query rows per projection CTA
 constexpr int kProjThreads = 256;
 constexpr uint64_t kOjaWaitNs = 1000000000ull;
 constexpr int kSmemBudget = 227 * 1024;
 
 // ------------------------------------------------------ 1: P q, hi + lo --
 
-// Item = (head, block of 16 query rows). U [d, r] is staged in shared
-// memory with row stride r|1 (odd: both access patterns below are free of
-// bank conflicts), the rows of Q as fp32. y = U^T q and p = q - U y, summed
-// in index order; hi = bf16(p), lo = bf16(p - hi) (the difference is exact).
+// Item = (head, block of `rows` query rows: 32, or 16 when n_query is not a
+// multiple of 32). U [d, r] is staged in shared memory with row stride r|1
+// (odd: the column reads of both phases are free of bank conflicts), the
+// rows of Q and of y = U^T q as fp32 rows of 16-byte-aligned stride; global
+// loads are 16-byte vectors, eight in flight per thread. Each thread then
+// computes 8 rows of one output column, reading the 8 rows' operands as
+// 16-byte broadcasts:
+//   y[m][j] = sum_i q[m][i] U[i][j]   (i in order)
+//   p[m][i] = q[m][i] - sum_j U[i][j] y[m][j]   (j in order)
+// and writes hi = bf16(p), lo = bf16(p - hi) (the difference is exact).
+constexpr int kProjBlock = 8;  // rows per thread
+
 __global__ void __launch_bounds__(kProjThreads)
-k_oja_project(const __nv_bfloat16 *__restrict__ Q, const float *__restrict__ U, int n_query, int rank,
+k_oja_project(const __nv_bfloat16 *__restrict__ Q, const float *__restrict__ U, int n_query, int rank, int rows,
               int64_t n_items, __nv_bfloat16 *__restrict__ qhl)
 {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int us = rank | 1;
-    float *sU = sm;                       // [128][us]
-    float *sq = sU + kHeadDim * us;       // [16][128]
-    float *sy = sq + kProjRows * kHeadDim;  // [16][rank]
-    const int blocks = n_query / kProjRows;
+    const int ys = (rank + 3) & ~3;       // y row stride (16-byte aligned rows)
+    float *sq = sm;                       // [rows][128]
+    float *sy = sq + rows * kHeadDim;     // [rows][ys]
+    float *sU = sy + rows * ys;           // [128][us]
+    const int blocks = n_query / rows;
+    const int n4 = kHeadDim * rank / 4;   // float4s of one head's basis
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int64_t head = item / blocks;
-        const int m0 = (int)(item - head * blocks) * kProjRows;
-        const float *Uh = U + head * kHeadDim * rank;
-        for (int o = threadIdx.x; o < kHeadDim * rank; o += kProjThreads) {
-            const int i = o / rank, j = o - i * rank;
-            sU[i * us + j] = Uh[o];
+        const int m0 = (int)(item - head * blocks) * rows;
+        const float4 *U4 = reinterpret_cast<const float4 *>(U + head * kHeadDim * rank);
+        for (int base = 0; base < n4; base += kProjThreads * 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int o = base + u * kProjThreads + (int)threadIdx.x;
+                if (o < n4) v[u] = __ldg(U4 + o);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int o = base + u * kProjThreads + (int)threadIdx.x;
+                if (o < n4) {
+                    const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int e = 4 * o + c, i = e / rank;
+                        sU[i * us + (e - i * rank)] = f[c];
+                    }
+                }
+            }
         }
-        const __nv_bfloat16 *Qh = Q + ((size_t)head * n_query + m0) * kHeadDim;
-        for (int o = threadIdx.x; o < kProjRows * kHeadDim; o += kProjThreads) sq[o] = __bfloat162float(Qh[o]);
+        const uint4 *Q4 = reinterpret_cast<const uint4 *>(Q + ((size_t)head * n_query + m0) * kHeadDim);
+        for (int o = threadIdx.x; o < rows * kHeadDim / 8; o += kProjThreads) {
+            float f[8];
+            bf16x8_to_f32(__ldg(Q4 + o), f);
+            float4 *dst = reinterpret_cast<float4 *>(sq + 8 * o);
+            dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+            dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+        for (int o = threadIdx.x; o < rows * (ys - rank); o += kProjThreads)  // zero the y padding
+            sy[(o / (ys - rank)) * ys + rank + o % (ys - rank)] = 0.f;
         __syncthreads();
-        for (int o = threadIdx.x; o < kProjRows * rank; o += kProjThreads) {
-            const int m = o / rank, j = o - m * rank;
-            float acc = 0.f;
-            for (int i = 0; i < kHeadDim; ++i) acc = fmaf(sq[m * kHeadDim + i], sU[i * us + j], acc);
-            sy[o] = acc;
+        // y: (rows / 8) x rank items of 8 rows x 1 column
+        for (int o = threadIdx.x; o < (rows / kProjBlock) * rank; o += kProjThreads) {
+            const int mg = o / rank, j = o - mg * rank;
+            const float *q0 = sq + mg * kProjBlock * kHeadDim;
+            float acc[kProjBlock] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int i = 0; i < kHeadDim; i += 4) {
+                const float u0 = sU[i * us + j], u1 = sU[(i + 1) * us + j], u2 = sU[(i + 2) * us + j],
+                            u3 = sU[(i + 3) * us + j];
+#pragma unroll
+                for (int r = 0; r < kProjBlock; ++r) {
+                    const float4 qv = *reinterpret_cast<const float4 *>(q0 + r * kHeadDim + i);
+                    acc[r] = fmaf(qv.x, u0, acc[r]);
+                    acc[r] = fmaf(qv.y, u1, acc[r]);
+                    acc[r] = fmaf(qv.z, u2, acc[r]);
+                    acc[r] = fmaf(qv.w, u3, acc[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kProjBlock; ++r) sy[(mg * kProjBlock + r) * ys + j] = acc[r];
         }
         __syncthreads();
-        for (int o = threadIdx.x; o < kProjRows * kHeadDim; o += kProjThreads) {
-            const int m = o >> 7, i = o & 127;
-            float acc = 0.f;
-            for (int j = 0; j < rank; ++j) acc = fmaf(sU[i * us + j], sy[m * rank + j], acc);
-            const float p = sq[o] - acc;
-            const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-            const size_t row = (size_t)head * 2 * n_query + m0 + m;
-            qhl[row * kHeadDim + i] = hi;
-            qhl[(row + n_query) * kHeadDim + i] = lo;
+        // p: (rows / 8) x 128 items of 8 rows x 1 dim
+        for (int o = threadIdx.x; o < (rows / kProjBlock) * kHeadDim; o += kProjThreads) {
+            const int mg = o >> 7, i = o & 127;
+            const float *ui = sU + i * us, *y0 = sy + mg * kProjBlock * ys;
+            float acc[kProjBlock] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < ys; j += 4) {
+                // the padding columns of y are zero; U's padding reads are in
+                // bounds (row stride >= rank) and meet a zero factor
+                const float u0 = j < rank ? ui[j] : 0.f, u1 = j + 1 < rank ? ui[j + 1] : 0.f,
+                            u2 = j + 2 < rank ? ui[j + 2] : 0.f, u3 = j + 3 < rank ? ui[j + 3] : 0.f;
+#pragma unroll
+                for (int r = 0; r < kProjBlock; ++r) {
+                    const float4 yv = *reinterpret_cast<const float4 *>(y0 + r * ys + j);
+                    acc[r] = fmaf(u0, yv.x, acc[r]);
+                    acc[r] = fmaf(u1, yv.y, acc[r]);
+                    acc[r] = fmaf(u2, yv.z, acc[r]);
+                    acc[r] = fmaf(u3, yv.w, acc[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kProjBlock; ++r) {
+                const int m = mg * kProjBlock + r;
+                const float pv = sq[m * kHeadDim + i] - acc[r];
+                const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
+                const size_t row = (size_t)head * 2 * n_query + m0 + m;
+                qhl[row * kHeadDim + i] = hi;
+                qhl[(row + n_query) * kHeadDim + i] = lo;
+            }
         }
         __syncthreads();  // shared memory is reused by the next item
     }
@@ -210,19 +278,31 @@ __device__ __forceinline__ void mma_commit(uint64_t *b)
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Sum of |x| over 16 consecutive accumulator columns of this thread's lane.
-__device__ __forceinline__ float tmem_abs_sum16(uint32_t taddr, float s)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
 {
-    uint32_t v[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
         "%15}, [%16];"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr));
+}
+
+// 16 consecutive query columns of this thread's lane. Stacked: the hi and
+// lo partial dot products sit n columns apart and are added first; either
+// way the absolute values are added to s in column order.
+__device__ __forceinline__ float tmem_abs_sum16(uint32_t taddr, uint32_t n, bool stacked, float s)
+{
+    uint32_t v[2][16];
+    tmem_ld16(taddr, v[0]);
+    if (stacked) tmem_ld16(taddr + n, v[1]);
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) s += fabsf(__uint_as_float(v[i]));
+    for (int i = 0; i < 16; ++i) {
+        float x = __uint_as_float(v[0][i]);
+        if (stacked) x += __uint_as_float(v[1][i]);
+        s += fabsf(x);
+    }
     return s;
 }
 
@@ -249,12 +329,14 @@ k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *kring = smem;                              // stages x 32 KB
-    uint8_t *qbuf = smem + (size_t)stages * kTileBytes;  // [hi, lo][dims 0-63, 64-127][n_query rows x 128 B]
+    uint8_t *qbuf = smem + (size_t)stages * kTileBytes;  // [dims 0-63, 64-127][hi, lo][n_query rows x 128 B]
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], qfull, qempty, tfull[2], tempty[2], drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile uint32_t abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t q_block = (uint32_t)n_query * 128u;  // bytes of one [half] block of operand rows
+    const uint32_t q_block = (uint32_t)n_query * 128u;  // bytes of one [half][split] block of operand rows
+    const bool stacked = 2 * n_query <= 256;
+    const int acc_cols = stacked ? 2 * n_query : n_query;  // fp32 columns of one accumulator
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -298,7 +380,7 @@ k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
                     bar_expect(&qfull, 4u * q_block);
                     for (int split = 0; split < 2; ++split)
                         for (int half = 0; half < 2; ++half)
-                            tma_load_2d(qbuf + (split * 2 + half) * q_block, &tmap_q, half * 64,
+                            tma_load_2d(qbuf + (half * 2 + split) * q_block, &tmap_q, half * 64,
                                         (int)((head * 2 + split) * n_query), &qfull);
                     ++qseq;
                     cur = head;
@@ -323,8 +405,22 @@ k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------- MMA issuer --
-            const uint32_t idesc = idesc_bf16(n_query);
-            const uint32_t k_base = saddr(kring), q_base = saddr(qbuf);
+            // Descriptors of stage 0's first K-step and of the operand rows;
+            // every other one differs by an address offset (in 16-byte units,
+            // the low field of the descriptor). Operand rows sit in shared
+            // memory as [dims 0-63, 64-127][hi, lo][n_query rows x 128 B], so
+            // hi and lo of one half are 2M contiguous rows: one N = 2M
+            // operand when that fits an MMA (M <= 128), else two of N = M.
+            const uint32_t idesc = idesc_bf16(stacked ? 2 * n_query : n_query);
+            const uint64_t a_desc0 = sdesc(saddr(kring)), b_desc0 = sdesc(saddr(qbuf));
+            uint64_t a_step[8], b_step[8];
+#pragma unroll
+            for (int step = 0; step < 8; ++step) {
+                const int half = step >> 2, kk = step & 3;
+                a_step[step] = (uint64_t)((half * kHalfBytes + kk * 32) >> 4);
+                b_step[step] = (uint64_t)((half * 2 * q_block + kk * 32) >> 4);
+            }
+            const uint64_t lo_step = q_block >> 4;
             uint32_t seq = 0, tcount = 0, qseq = 0;
             int64_t cur = -1;
             for (int64_t tile = walk.first; tile < walk.last; ++tile) {
@@ -343,16 +439,18 @@ k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
                 const int s = (int)(seq % (uint32_t)stages);
                 if (!bar_wait(&full[s], (seq / stages) & 1u, status, &abort_flag, true)) break;
                 fence_after();
-                const uint32_t d_tmem = tmem + b * (uint32_t)n_query;
-                uint32_t accum = 0;
-                for (int half = 0; half < 2; ++half) {
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc(k_base + s * kTileBytes + half * kHalfBytes + kk * 32);
-                        for (int split = 0; split < 2; ++split) {
-                            const uint64_t bd = sdesc(q_base + (split * 2 + half) * q_block + kk * 32);
-                            mma_bf16(d_tmem, a, bd, idesc, accum);
-                            accum = 1;
-                        }
+                const uint32_t d_tmem = tmem + b * (uint32_t)acc_cols;
+                const uint64_t a0 = a_desc0 + (uint64_t)((s * kTileBytes) >> 4);
+                if (stacked) {
+                    // one MMA per K-step: N = 2M operand rows (hi then lo)
+#pragma unroll
+                    for (int step = 0; step < 8; ++step)
+                        mma_bf16(d_tmem, a0 + a_step[step], b_desc0 + b_step[step], idesc, step ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int step = 0; step < 8; ++step) {
+                        mma_bf16(d_tmem, a0 + a_step[step], b_desc0 + b_step[step], idesc, step ? 1u : 0u);
+                        mma_bf16(d_tmem, a0 + a_step[step], b_desc0 + b_step[step] + lo_step, idesc, 1u);
                     }
                 }
                 mma_commit(&empty[s]);
@@ -376,9 +474,10 @@ k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
             const uint32_t b = tcount & 1u, use = tcount >> 1;
             if (!bar_wait(&tfull[b], use & 1u, status, &abort_flag, true)) break;
             fence_after();
-            const uint32_t taddr = tmem + ((rank * 32u) << 16) + b * (uint32_t)n_query;
+            const uint32_t taddr = tmem + ((rank * 32u) << 16) + b * (uint32_t)acc_cols;
             float acc = 0.f;
-            for (int c = 0; c < n_query; c += 16) acc = tmem_abs_sum16(taddr + (uint32_t)c, acc);
+            for (int c = 0; c < n_query; c += 16)
+                acc = tmem_abs_sum16(taddr + (uint32_t)c, (uint32_t)n_query, stacked, acc);
             fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive(&tempty[b]);
@@ -450,18 +549,25 @@ int oja_stages(int32_t n_query)
 }
 
 cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, const float *U, const int32_t *seq_lens,
-                              int32_t n_query, int32_t rank, void *qhl, float *S, uint32_t *status, cudaStream_t st)
+                              int32_t n_query, int32_t rank, void *qhl, float *S, uint32_t *status, cudaStream_t st,
+                              void *const *events)
 {
     if (g.n_heads == 0 || g.t_max == 0) return cudaSuccess;
+    auto mark = [&](int i) -> cudaError_t {
+        return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+    };
+    cudaError_t e;
+    if ((e = mark(0)) != cudaSuccess) return e;
     // 1: projected query rows, hi + lo
-    const int64_t items = g.n_heads * (n_query / kProjRows);
-    const size_t psmem = (size_t)(kHeadDim * (rank | 1) + kProjRows * kHeadDim + kProjRows * rank) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(k_oja_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+    const int rows = n_query % 32 == 0 ? 32 : 16;
+    const int64_t items = g.n_heads * (n_query / rows);
+    const size_t psmem = (size_t)(rows * kHeadDim + rows * ((rank + 3) & ~3) + kHeadDim * (rank | 1)) * sizeof(float);
+    e = cudaFuncSetAttribute(k_oja_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
     if (e != cudaSuccess) return e;
     const int pgrid = grid_for_items(reinterpret_cast<const void *>(k_oja_project), kProjThreads, psmem, items);
-    k_oja_project<<<pgrid, kProjThreads, psmem, st>>>(static_cast<const __nv_bfloat16 *>(Q), U, n_query, rank, items,
-                                                      static_cast<__nv_bfloat16 *>(qhl));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k_oja_project<<<pgrid, kProjThreads, psmem, st>>>(static_cast<const __nv_bfloat16 *>(Q), U, n_query, rank, rows,
+                                                      items, static_cast<__nv_bfloat16 *>(qhl));
+    if ((e = cudaGetLastError()) != cudaSuccess || (e = mark(1)) != cudaSuccess) return e;
     // 2: the contraction
     CUtensorMap mk, mq;
     if (!make_map(&mk, K, (uint64_t)g.n_heads * g.t_max, kTok) ||
@@ -472,8 +578,13 @@ cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, c
     const size_t smem = 1024 + (size_t)stages * kTileBytes + 4 * (size_t)n_query * 128;
     if ((e = cudaFuncSetAttribute(k_oja_scores, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
+    // independent accumulators per tile: as many (up to 4) as two buffers of
+    // them fit in the 512 TMEM columns
+    // two accumulator buffers of 2M columns (hi and lo side by side) for
+    // M <= 128, of M columns (hi and lo summed by the MMAs) above
+    const int acc_cols = 2 * n_query <= 256 ? 2 * n_query : n_query;
     uint32_t cols = 32;
-    while (cols < 2u * (uint32_t)n_query) cols *= 2;
+    while (cols < (uint32_t)(2 * acc_cols)) cols *= 2;
     const int64_t tiles = g.n_heads * ((g.t_max + kTok - 1) / kTok);
     const int sms = sms_of_current_device();
     if (sms <= 0) return cudaErrorInvalidDevice;
@@ -481,7 +592,8 @@ cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, c
     const float scale = (float)(1.0 / ((double)n_query * 11.313708498984760390));  // 1 / (M sqrt(128))
     k_oja_scores<<<grid, kOjaThreads, smem, st>>>(mk, mq, seq_lens, g.heads, g.t_max, g.n_heads, n_query, stages, cols,
                                                   scale, S, status);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return mark(2);
 }
 
 }  // namespace mkv

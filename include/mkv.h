@@ -211,8 +211,8 @@ mkv_status mkv_compress_quota(const void *K, const void *V, mkv_shape shape, dou
  * K: bf16 cache. Q: bf16 [batch, heads, n_query, head_dim], the window's
  * query rows per KV head (group heads x recent positions, flattened; any
  * order). U: fp32 [batch, heads, head_dim, rank], row-major (column j is
- * basis vector j); it need not be orthonormal (the formula is used as is);
- * may be NULL when rank = 0. n_query: a multiple of 16 in [16, 256]; rank in
+ * basis vector j), 16-byte aligned; it need not be orthonormal (the formula
+ * is used as is); may be NULL when rank = 0. n_query: a multiple of 16 in [16, 256]; rank in
  * [0, head_dim]. S: fp32 [batch, heads, t_max], written for t < T_b.
  * Computed as (P q_m) . k_t with P = I - U U^T: P q_m in fp32, split into
  * two bf16 operands (hi + lo, about 2^-17 relative), contracted with the
@@ -223,6 +223,14 @@ mkv_status mkv_compress_quota(const void *K, const void *V, mkv_shape shape, dou
 size_t mkv_oja_workspace_size(mkv_shape shape, int32_t n_query);
 mkv_status mkv_oja_score(const void *K, const void *Q, const float *U, mkv_shape shape, int32_t n_query,
                          int32_t rank, float *S, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
+/* mkv_oja_score recording caller-created CUDA events (cudaEvent_t as void*)
+ * on `stream`: events[0] before the query projection kernel, events[1]
+ * between it and the tensor-core contraction, events[2] after; n_events >= 3.
+ * Nothing is recorded for an empty shape. */
+mkv_status mkv_oja_score_profiled(const void *K, const void *Q, const float *U, mkv_shape shape, int32_t n_query,
+                                  int32_t rank, float *S, void *workspace, size_t workspace_bytes,
+                                  mkv_stream_t stream, void *const *events, int32_t n_events);
 
 /* OjaKV's full-rank selection: the scores of mkv_oja_score, then the
  * top-n_keep selection, compaction and gather of mkv_compress (keep the
@@ -286,7 +294,16 @@ mkv_status mkv_compress_profiled(const void *K, const void *V, mkv_shape shape, 
  * buffers hK_out, hV_out [batch, heads, keep_stride, head_dim] and h_idx,
  * h_kept [batch*heads(, keep_stride)]; any of the four host outputs may be
  * NULL. Device output buffers dK_out, dV_out, d_idx, d_kept are required.
- * Every copy is one cudaMemcpyAsync on `stream`; nothing synchronises. */
+ * The batch rows are processed in up to 8 chunks: chunk c's host-to-device
+ * copies run on two library-owned copy-in streams (keys on one, values on
+ * the other), its kernels on `stream`, its device-to-host copies on a
+ * copy-out stream, so copies of different chunks overlap each other and the
+ * kernels. The copy streams first wait for
+ * the work already on `stream`, and `stream` waits for every copy before
+ * anything enqueued after this call, so the call behaves as if it were all on
+ * `stream`. The three streams and their events are created on a device's first
+ * call and kept until the process exits. Every copy is one cudaMemcpyAsync;
+ * nothing synchronises the host. */
 mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV, mkv_shape shape,
                              double ratio, mkv_mode mode, int32_t window, int32_t keep_stride,
                              void *dK_out, void *dV_out, int32_t *d_idx, int32_t *d_kept,

@@ -118,7 +118,7 @@ def _check(name, K, V, lens, Q, U, ratio, sample=None):
     return S, idx, kept
 
 
-@pytest.mark.parametrize("n_query,rank", [(128, 64), (16, 0), (48, 16), (256, 128), (128, 1), (64, 127)])
+@pytest.mark.parametrize("n_query,rank", [(128, 64), (16, 0), (48, 16), (256, 96), (128, 1), (64, 127)])
 def test_oja_scores_and_selection_match_the_oracle(n_query, rank):
     K, V, lens, Q, U = _case(n_query=n_query, rank=rank, seed=n_query + rank)
     _check(f"oja-M{n_query}-r{rank}", K, V, lens, Q, U, 0.5)
@@ -154,6 +154,25 @@ def test_oja_zero_basis_gives_the_mean_absolute_logit():
     for h in range(2):
         tol = score_tolerance(K[0, h], Q[0, h], U[0, h, :, :0], want[0, h])
         assert np.all(np.abs(got[0, h] - want[0, h]) <= tol)
+
+
+def test_oja_full_rank_basis_leaves_only_rounding():
+    # rank = d with an orthonormal basis: every residual is 0, so every
+    # score must lie within its rounding bound of 0 (a selection among such
+    # scores ranks rounding noise and is not compared)
+    K, V, lens, Q, U = _case(rows=2, heads=2, t_max=1500, n_query=64, rank=128, seed=4)
+    ws = mkv.oja_workspace_for(K, 64, lens)
+    S = torch.zeros(K.shape[:3], device=DEV)
+    mkv.mkv_oja_score(K, Q, U, S, ws, lens)
+    assert mkv.mkv_device_status(ws) == 0
+    lens_c = lens.cpu().numpy()
+    for b in range(2):
+        for h in range(2):
+            Th = int(lens_c[b])
+            E = oracle.oja_scores(K[b, h, :Th].cpu(), Q[b, h].cpu(), U[b, h].cpu().numpy())
+            tol = score_tolerance(K[b, h, :Th], Q[b, h], U[b, h], E)
+            assert np.all(np.abs(S[b, h, :Th].double().cpu().numpy() - E) <= tol)
+            assert np.all(np.abs(S[b, h, :Th].double().cpu().numpy()) <= 2 * tol)
 
 
 def test_oja_is_deterministic():

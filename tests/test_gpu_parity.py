@@ -320,6 +320,46 @@ def test_deterministic_and_paths_agree():
         assert torch.equal(hVo[bb, hh, :n], a[1][bb, hh, :n].cpu())
 
 
+def test_host_path_chunks_overlap_and_join_the_callers_stream():
+    # 11 batch rows: 6 chunks of 2, the last one short; two calls back to back
+    # on a side stream with different inputs, results read after
+    # synchronising that stream only
+    w = synthkv.WORKLOADS["ragged-b8-llama-kv-t8k-32k"].scaled("host", layers=1, batch=11, heads=2, t_max=5000,
+                                                                 t_min=100)
+    K1, V1, lens = synthkv.make_kv(w, seed=7, device=DEV)
+    K2, V2, _ = synthkv.make_kv(w, seed=8, device=DEV)
+    ratio, mode, window = 0.4, "l2", 0
+    ks = mkv.mkv_num_keep(w.t_max, ratio)
+    want = [_run_fused(K, V, ratio, mode, window, lens) for K, V in ((K1, V1), (K2, V2))]
+    side = torch.cuda.Stream()
+    dK, dV = torch.empty_like(K1), torch.empty_like(V1)
+    dKo = torch.empty((11, 2, ks, 128), dtype=torch.bfloat16, device=DEV)
+    dVo = torch.empty_like(dKo)
+    didx = torch.empty((11, 2, ks), dtype=torch.int32, device=DEV)
+    dkept = torch.empty((11, 2), dtype=torch.int32, device=DEV)
+    ws = mkv.workspace_for(K1, window, lens)
+    outs = []
+    hosts = [(K1.cpu().pin_memory(), V1.cpu().pin_memory()), (K2.cpu().pin_memory(), V2.cpu().pin_memory())]
+    torch.cuda.synchronize()
+    for hK, hV in hosts:
+        hKo = torch.zeros(dKo.shape, dtype=torch.bfloat16).pin_memory()
+        hVo = torch.zeros_like(hKo).pin_memory()
+        hidx = torch.zeros(didx.shape, dtype=torch.int32).pin_memory()
+        hkept = torch.zeros(dkept.shape, dtype=torch.int32).pin_memory()
+        mkv.mkv_compress_host(hK, hV, dK, dV, ratio, mode, window, ks, dKo, dVo, didx, dkept, hKo, hVo, hidx,
+                              hkept, ws, lens, stream=side)
+        outs.append((hKo, hVo, hidx, hkept))
+    side.synchronize()
+    assert mkv.mkv_device_status(ws, side) == 0
+    for (Ko, Vo, idx, kept, _), (hKo, hVo, hidx, hkept) in zip(want, outs):
+        kk = kept.cpu()
+        assert torch.equal(hkept, kk)
+        live = torch.arange(ks)[None, None, :] < kk[..., None]
+        assert torch.equal(torch.where(live, hidx, 0), torch.where(live, idx.cpu(), 0))
+        assert torch.equal(torch.where(live[..., None], hKo, 0), torch.where(live[..., None], Ko.cpu(), 0))
+        assert torch.equal(torch.where(live[..., None], hVo, 0), torch.where(live[..., None], Vo.cpu(), 0))
+
+
 # ------------------------------------------------------ full-size workloads --
 
 def _full_size(name, runs=None, sample=4):
