@@ -33,11 +33,13 @@
 //    (M > 128) -- and commits them to the stage's empty barrier and the
 //    buffer's full barrier. An MMA costs about the same issue time for any
 //    N up to 128, so fewer, wider MMAs per tile are what keeps pace with HBM.
-//  * warps 2-5: epilogue. The warp with rank w (= warp id mod 4) owns TMEM
-//    lanes 32w..32w+31, i.e. one token per thread: it reads its row of the
-//    accumulator (tcgen05.ld 32x32b), adds the hi and lo halves of each
-//    query column, sums their absolute values in column order, scales,
-//    stores e_t, and frees the buffer.
+//  * warps 2-9: epilogue, two groups of 4 warps when M is a multiple of 64
+//    (else warps 2-5 alone). The warp with rank w (= warp id mod 4) owns
+//    TMEM lanes 32w..32w+31, i.e. one token per thread: it reads its half of
+//    the token's accumulator row (tcgen05.ld 32x32b, 64 columns per wait),
+//    adds the hi and lo halves of each query column and sums their absolute
+//    values in column order; the second group's partial sum is added to the
+//    first's (through shared memory), which scales and stores e_t.
 // Every tile of 128 tokens costs 8 MMAs of 128 x 2M x 16 against 32 KB read
 // from HBM (2 x 2M flop per key byte, against a bf16 ridge near 280).
 //
@@ -65,7 +67,7 @@ constexpr int kTok = 128;                    // tokens per tile: the MMA's M, th
 constexpr int kHalfBytes = kTok * 128;       // one 64-dim box of a tile: 128 rows x 128 B
 constexpr int kTileBytes = 2 * kHalfBytes;   // 32 KB
 constexpr int kMaxStages = 6;
-constexpr int kOjaThreads = 192;             // producer warp, MMA warp, 4 epilogue warps
+constexpr int kOjaThreads = 320;             // producer warp, MMA warp, 8 epilogue warps
 constexpr int kProjThreads = 256;
 constexpr uint64_t kOjaWaitNs = 1000000000ull;
 constexpr int kSmemBudget = 227 * 1024;
@@ -288,20 +290,35 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
         : "r"(taddr));
 }
 
-// 16 consecutive query columns of this thread's lane. Stacked: the hi and
-// lo partial dot products sit n columns apart and are added first; either
-// way the absolute values are added to s in column order.
-__device__ __forceinline__ float tmem_abs_sum16(uint32_t taddr, uint32_t n, bool stacked, float s)
+// Query columns [c0, c0 + cw) of this thread's lane (cw a multiple of 16),
+// read 64 at a time per wait. Stacked: the hi and lo partial dot products
+// sit n columns apart and are added first; either way the absolute values
+// are added in column order.
+__device__ __forceinline__ float tmem_abs_sum(uint32_t taddr, uint32_t n, bool stacked, int c0, int cw)
 {
-    uint32_t v[2][16];
-    tmem_ld16(taddr, v[0]);
-    if (stacked) tmem_ld16(taddr + n, v[1]);
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    float s = 0.f;
+    for (int c = c0; c < c0 + cw; c += 64) {
+        const int nb = min(64, c0 + cw - c);
+        uint32_t h[4][16], l[4][16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        float x = __uint_as_float(v[0][i]);
-        if (stacked) x += __uint_as_float(v[1][i]);
-        s += fabsf(x);
+        for (int k = 0; k < 4; ++k) {
+            if (16 * k < nb) {
+                tmem_ld16(taddr + (uint32_t)(c + 16 * k), h[k]);
+                if (stacked) tmem_ld16(taddr + n + (uint32_t)(c + 16 * k), l[k]);
+            }
+        }
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (16 * k < nb) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float x = __uint_as_float(h[k][i]);
+                    if (stacked) x += __uint_as_float(l[k][i]);
+                    s += fabsf(x);
+                }
+            }
+        }
     }
     return s;
 }
@@ -330,13 +347,19 @@ k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *kring = smem;                              // stages x 32 KB
     uint8_t *qbuf = smem + (size_t)stages * kTileBytes;  // [dims 0-63, 64-127][hi, lo][n_query rows x 128 B]
-    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], qfull, qempty, tfull[2], tempty[2], drain;
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], qfull, qempty, tfull[2], tempty[2], pready[2],
+        drain;
+    __shared__ float part[2][kTok];  // the second epilogue group's partial sums, per accumulator buffer
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile uint32_t abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t q_block = (uint32_t)n_query * 128u;  // bytes of one [half][split] block of operand rows
     const bool stacked = 2 * n_query <= 256;
     const int acc_cols = stacked ? 2 * n_query : n_query;  // fp32 columns of one accumulator
+    // epilogue groups of 4 warps (one per TMEM lane quadrant), each summing
+    // an equal share of the query columns: two when the share is a multiple
+    // of 32 columns
+    const int groups = n_query % 64 == 0 ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -347,7 +370,8 @@ k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         bar_init(&qempty, 1);
         for (int b = 0; b < 2; ++b) {
             bar_init(&tfull[b], 1);
-            bar_init(&tempty[b], 4);
+            bar_init(&tempty[b], 4 * groups);
+            bar_init(&pready[b], 4);
         }
         bar_init(&drain, 1);
         abort_flag = 0u;
@@ -464,26 +488,48 @@ k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         }
     } else {
         // ----------------------------------------------------- epilogue --
+        // Group g (warps 2-5: g = 0, warps 6-9: g = 1) sums query columns
+        // [g * cw, (g + 1) * cw); group 1 hands its partial sums to group 0
+        // through `part` (pready), and group 0 frees the accumulator buffer
+        // only after reading them, so a slot of `part` is never rewritten
+        // before it is read.
+        const int grp = (warp - 2) >> 2;
         const uint32_t rank = (uint32_t)(warp & 3);  // TMEM lanes 32*rank .. 32*rank+31
+        const int cw = n_query / groups;
         uint32_t tcount = 0;
-        for (int64_t tile = walk.first; tile < walk.last; ++tile) {
-            const int64_t head = tile / walk.tph;
-            const int t0 = (int)(tile - head * walk.tph) * kTok;
-            const int T = head_len(seq_lens, head, heads, t_max, status, false);
-            if (t0 >= T) continue;
-            const uint32_t b = tcount & 1u, use = tcount >> 1;
-            if (!bar_wait(&tfull[b], use & 1u, status, &abort_flag, true)) break;
-            fence_after();
-            const uint32_t taddr = tmem + ((rank * 32u) << 16) + b * (uint32_t)acc_cols;
-            float acc = 0.f;
-            for (int c = 0; c < n_query; c += 16)
-                acc = tmem_abs_sum16(taddr + (uint32_t)c, (uint32_t)n_query, stacked, acc);
-            fence_before();
-            __syncwarp();
-            if (lane == 0) bar_arrive(&tempty[b]);
-            const int t = t0 + (int)rank * 32 + lane;
-            if (t < T) S[(size_t)head * t_max + t] = acc * scale;
-            ++tcount;
+        if (grp < groups) {
+            for (int64_t tile = walk.first; tile < walk.last; ++tile) {
+                const int64_t head = tile / walk.tph;
+                const int t0 = (int)(tile - head * walk.tph) * kTok;
+                const int T = head_len(seq_lens, head, heads, t_max, status, false);
+                if (t0 >= T) continue;
+                const uint32_t b = tcount & 1u, use = tcount >> 1;
+                if (!bar_wait(&tfull[b], use & 1u, status, &abort_flag, true)) break;
+                fence_after();
+                const uint32_t taddr = tmem + ((rank * 32u) << 16) + b * (uint32_t)acc_cols;
+                float acc = tmem_abs_sum(taddr, (uint32_t)n_query, stacked, grp * cw, cw);
+                const int row = (int)rank * 32 + lane;
+                if (grp == 1) {
+                    part[b][row] = acc;
+                    fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        bar_arrive(&pready[b]);
+                        bar_arrive(&tempty[b]);
+                    }
+                } else {
+                    if (groups == 2) {
+                        if (!bar_wait(&pready[b], use & 1u, status, &abort_flag, true)) break;
+                        acc += part[b][row];
+                    }
+                    fence_before();
+                    __syncwarp();
+                    if (lane == 0) bar_arrive(&tempty[b]);
+                    const int t = t0 + row;
+                    if (t < T) S[(size_t)head * t_max + t] = acc * scale;
+                }
+                ++tcount;
+            }
         }
     }
     fence_before();
@@ -543,7 +589,8 @@ size_t oja_operand_bytes(int64_t n_heads, int32_t n_query)
 
 int oja_stages(int32_t n_query)
 {
-    const int left = kSmemBudget - 1024 - 4 * n_query * 128;
+    // alignment slack, up to 2 KB of static shared memory, the operand rows
+    const int left = kSmemBudget - 1024 - 2048 - 4 * n_query * 128;
     const int s = left / kTileBytes;
     return s > kMaxStages ? kMaxStages : s;
 }
