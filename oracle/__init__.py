@@ -94,6 +94,8 @@ def _load():
         lib.oracle_oja_scores.argtypes = [vp, i64, i64, vp, i64, vp, i64, vp]
         lib.oracle_compress_head_oja.restype = i64
         lib.oracle_compress_head_oja.argtypes = [vp, vp, i64, i64, vp, i64, vp, i64, i64, vp, vp, vp, vp]
+        lib.oracle_compact_in_place.restype = i32
+        lib.oracle_compact_in_place.argtypes = [vp, i64, i64, vp, i64]
         _lib = lib
         return lib
 
@@ -319,3 +321,13 @@ def compress_head_oja(K, V, Q, U, n_keep: int):
     if got != n:
         raise ValueError("oracle_compress_head_oja failed")
     return {"S": E[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}
+
+
+def compact_in_place(X, idx) -> np.ndarray:
+    """In-place compaction of a bf16 [T, d] head: a copy of X (uint16 bits)
+    with rows [0, len(idx)) replaced by X[idx] and the rest unchanged."""
+    x = _bits(X).copy()
+    i = np.ascontiguousarray(idx, dtype=np.int32)
+    if _load().oracle_compact_in_place(_ptr(x), x.shape[0], x.shape[1], _ptr(i), i.shape[0]) != 0:
+        raise ValueError("oracle_compact_in_place: indices not strictly ascending in [0, T)")
+    return x

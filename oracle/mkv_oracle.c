@@ -455,3 +455,18 @@ int64_t oracle_compress_head_oja(const uint16_t *K, const uint16_t *V, int64_t T
     if (V_out) oracle_gather(V, d, idx, n_keep, V_out);
     return n_keep;
 }
+
+/* In-place compaction (the memory-saving form of step 4): the kept rows are
+ * moved to the front of the head's own rows, X[j] = X[idx[j]] for j < n;
+ * rows from n on keep their contents. Done one row at a time in ascending j,
+ * which is safe because idx ascends from 0, so idx[j] >= j: every source row
+ * is read before anything overwrites it. Returns 0, or -1 if idx is not
+ * strictly ascending or leaves [0, T). */
+int oracle_compact_in_place(uint16_t *X, int64_t T, int64_t d, const int32_t *idx, int64_t n)
+{
+    for (int64_t j = 0; j < n; ++j)
+        if (idx[j] < 0 || idx[j] >= T || (j > 0 && idx[j] <= idx[j - 1])) return -1;
+    for (int64_t j = 0; j < n; ++j)
+        if (idx[j] != j) memcpy(X + j * d, X + (int64_t)idx[j] * d, (size_t)d * sizeof *X);
+    return 0;
+}

@@ -576,3 +576,32 @@ def test_oja_selection_keeps_the_largest_errors():
     assert out["idx"].tolist() == sorted(order[:50])
     kb = K.contiguous().view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(out["K_out"], kb[out["idx"]])
+
+
+# ---- in-place compaction (the memory-saving form of the gather) ----
+
+def test_compact_in_place_hand_case():
+    X = np.arange(12, dtype=np.uint16).reshape(6, 2)  # rows (0,1) (2,3) ... (10,11)
+    out = oracle.compact_in_place(X, [1, 2, 4])
+    assert out.tolist() == [[2, 3], [4, 5], [8, 9], [6, 7], [8, 9], [10, 11]]
+    # the input is not modified
+    assert X[0].tolist() == [0, 1]
+
+
+def test_compact_in_place_equals_gather_then_tail():
+    rng = np.random.default_rng(12)
+    for _ in range(100):
+        T = int(rng.integers(0, 60))
+        n = int(rng.integers(0, T + 1))
+        idx = np.sort(rng.choice(T, size=n, replace=False)).astype(np.int32)
+        X = rng.integers(0, 65535, size=(T, 8)).astype(np.uint16)
+        out = oracle.compact_in_place(X, idx)
+        np.testing.assert_array_equal(out[:n], oracle.gather(X, idx))
+        np.testing.assert_array_equal(out[n:], X[n:])
+
+
+def test_compact_in_place_rejects_unordered_indices():
+    X = np.zeros((4, 2), dtype=np.uint16)
+    for bad in ([2, 1], [0, 0], [4], [-1]):
+        with pytest.raises(ValueError):
+            oracle.compact_in_place(X, bad)
