@@ -535,6 +535,45 @@ def run_secondary(args):
                              "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                              "peak_source": peaks["source"], "algorithmic_bytes_per_launch": nbytes},
                 "clocks": clocks.summary(), "gpu_launches": steps * 2}
+    elif args.path == "inplace":
+        w, mode, window, ratio = workload_run(args.workload, args.layers)
+        K0, V0, lens = synthkv.make_kv(w, seed=args.seed, device=dev)
+        K, V = K0.clone(), V0.clone()
+        ws = mkv.workspace_for(K, window, lens)
+        kept = torch.empty((w.rows, w.heads), dtype=torch.int32, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+        def step(i=None):
+            if i is not None:
+                evs[i][0].record(stream)
+            mkv.mkv_compress_inplace(K, V, ratio, mode, window, ws, kept=kept, seq_lens=lens, stream=stream)
+            if i is not None:
+                evs[i][1].record(stream)
+        for _ in range(max(3, args.warmup)):
+            K.copy_(K0), V.copy_(V0)
+            step()
+        torch.cuda.synchronize()
+        with ClockSampler(dev.index or 0) as clocks:
+            # every step compresses a fresh copy of the cache; the restore
+            # copies run between the event pairs, outside the timed spans
+            for i in range(steps):
+                K.copy_(K0), V.copy_(V0)
+                step(i)
+            torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+        if mkv.mkv_device_status(ws, stream) != 0:
+            raise RuntimeError("device status nonzero")
+        lens_list = lens.cpu().tolist()
+        nb = path_bytes(lens_list, w.heads, ratio, w.head_dim)
+        achieved = nb["path"] / (ms / 1e3) / 1e9
+        line = {"metric": "in-place ManifoldKV compression: KV tokens scored+compacted per second (no output buffers)",
+                "value": nb["tokens"] / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "dtype": "f32", "data": "synthetic (seeded)",
+                "config": {"workload": w.name, "heads_total": w.n_heads, "t": w.t_max, "mode": mode,
+                           "window": window, "ratio": ratio},
+                "hbm": {"path_bytes_per_step": nb["path"], "achieved_gbs": achieved,
+                        "frac_of_measured": achieved / hbm, "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS},
+                "clocks": clocks.summary(), "gpu_launches": steps * 4}
     else:  # quota
         w = synthkv.WORKLOADS["qwen3-8b-kv-t64k-w4096"] if args.workload == synthkv.BENCH_WORKLOAD else \
             synthkv.WORKLOADS[args.workload]
@@ -585,7 +624,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle time for --impl reference")
-    ap.add_argument("--path", choices=["manifold", "oja", "summaries", "quota"], default="manifold",
+    ap.add_argument("--path", choices=["manifold", "oja", "summaries", "quota", "inplace"], default="manifold",
                     help="manifold: the headline path; the others time a widened path (one GPU, own JSON line)")
     ap.add_argument("--oja-queries", type=int, default=128, help="query-window rows per KV head (--path oja)")
     ap.add_argument("--oja-rank", type=int, default=64, help="basis rank (--path oja)")

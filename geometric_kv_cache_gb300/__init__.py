@@ -48,6 +48,7 @@ EXPORTED = (
     "mkv_compress_noalloc", "mkv_compress_single_pass", "mkv_set_single_pass", "mkv_layer_budgets",
     "mkv_inject_stalled_windows", "mkv_window_means", "mkv_num_keep_quota", "mkv_select_quota",
     "mkv_compress_quota", "mkv_oja_workspace_size", "mkv_oja_score", "mkv_compress_oja", "mkv_oja_score_profiled",
+    "mkv_compress_inplace",
 )
 
 
@@ -106,6 +107,7 @@ def load(build_if_missing: bool = True):
             "mkv_status_string": (ctypes.c_char_p, [i32]),
             "mkv_window_means": (i32, [vp, MkvShape, i32, vp, vp, vp, sz, vp]),
             "mkv_oja_workspace_size": (sz, [MkvShape, i32]),
+            "mkv_compress_inplace": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, vp, vp, vp, sz, vp]),
             "mkv_oja_score": (i32, [vp, vp, vp, MkvShape, i32, i32, vp, vp, sz, vp]),
             "mkv_oja_score_profiled": (i32, [vp, vp, vp, MkvShape, i32, i32, vp, vp, sz, vp, ctypes.POINTER(vp), i32]),
             "mkv_compress_oja": (i32, [vp, vp, vp, vp, MkvShape, i32, i32, f64, vp, i32, vp, vp, vp, vp, vp, sz,
@@ -312,6 +314,16 @@ def mkv_compress_oja(K, V, Q, U, ratio, keep_stride, K_out, V_out, idx, kept, wo
                                    int(U.shape[-1]), float(ratio), _ptr(n_keep), int(keep_stride), _ptr(K_out),
                                    _ptr(V_out), _ptr(idx), _ptr(kept), _ptr(workspace), workspace.numel(),
                                    _stream(stream)), "mkv_compress_oja")
+
+
+def mkv_compress_inplace(K, V, ratio, mode, window, workspace, idx=None, kept=None, seq_lens=None, n_keep=None,
+                         stream=None):
+    """Compress K and V in place: rows [0, kept) of every head become the
+    kept rows; idx [B, H, t_max] and kept [B, H] are optional outputs."""
+    _need_cuda(K, V, idx, kept, workspace, seq_lens, n_keep)
+    _check(load().mkv_compress_inplace(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _ptr(n_keep),
+                                       _MODES[mode], int(window), _ptr(idx), _ptr(kept), _ptr(workspace),
+                                       workspace.numel(), _stream(stream)), "mkv_compress_inplace")
 
 
 def mkv_compress_profiled(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, workspace, events,

@@ -158,7 +158,7 @@ mkv_status check_outputs(const mkv_shape &s, double ratio, const int32_t *n_keep
 mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio, const int32_t *n_keep,
                         mkv_mode mode, int32_t window, int32_t keep_stride, void *K_out, void *V_out,
                         int32_t *idx, int32_t *kept, void *ws, size_t ws_bytes, cudaStream_t st,
-                        void *const *events, bool stall_windows = false, bool quota = false)
+                        void *const *events, bool stall_windows = false, bool quota = false, bool in_place = false)
 {
     mkv_status rc = check_shape(s);
     if (rc != MKV_OK) return rc;
@@ -225,9 +225,15 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
         (e = launch_compact(g, S, cut, chunk, s.seq_lens, keep_stride, idx_w, idx_stride, status, st)) != cudaSuccess)
         return cuda_status(e);
     if (!mark(5)) return MKV_ERR_CUDA;
-    if (K_out &&
-        (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st)) != cudaSuccess)
+    if (in_place) {
+        if ((e = launch_gather_inplace(g, idx_w, idx_stride, kept_w, s.seq_lens, const_cast<void *>(K),
+                                       const_cast<void *>(V), status, st)) != cudaSuccess)
+            return cuda_status(e);
+    } else if (K_out &&
+               (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st)) !=
+                   cudaSuccess) {
         return cuda_status(e);
+    }
     if (!mark(6)) return MKV_ERR_CUDA;
     return MKV_OK;
 }
@@ -544,6 +550,16 @@ mkv_status mkv_compress_oja(const void *K, const void *V, const void *Q, const f
         (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st)) != cudaSuccess)
         return cuda_status(e);
     return MKV_OK;
+}
+
+mkv_status mkv_compress_inplace(void *K, void *V, mkv_shape shape, double ratio, const int32_t *n_keep, mkv_mode mode,
+                                int32_t window, int32_t *idx, int32_t *kept, void *workspace, size_t workspace_bytes,
+                                mkv_stream_t stream)
+{
+    // the kept rows land at the front of each head's own rows: the output
+    // stride is t_max and the outputs are K and V themselves
+    return run_compress(K, V, shape, ratio, n_keep, mode, window, shape.t_max, nullptr, nullptr, idx, kept, workspace,
+                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr, false, false, true);
 }
 
 int32_t mkv_compress_num_stages(void) { return kCompressStages; }

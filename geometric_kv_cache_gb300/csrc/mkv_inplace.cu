@@ -1,0 +1,120 @@
+// sm_103a in-place compaction: the kept K/V rows of every head are moved to
+// the front of the head's own rows (the memory-saving form of the gather
+// that ends the ManifoldKV-style path: the retained tokens form the
+// compressed cache, "ManifoldKV: Training-Free KV Cache Compression via
+// Euclidean Outlier Detection", ICML 2026 poster 62526, abstract).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mkv_device.cuh"
+#include "mkv_internal.h"
+
+namespace mkv {
+namespace {
+
+constexpr int kStreamThreads = 256;
+constexpr int kSlots = kStreamThreads / 16;  // rows per CTA per load step
+using namespace dev;
+
+// ----------------------------------------------------------- in place --
+
+// 16-byte load through L2 only: the rows read here are written by the same
+// kernel, so the non-coherent (read-only) path must not be used.
+__device__ __forceinline__ uint4 ld_cg(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p)
+                 : "memory");
+    return r;
+}
+
+constexpr int kInplaceRows = 64;                 // output slots per chunk
+constexpr int kInplaceR = kInplaceRows / kSlots;  // rows per half-warp per chunk
+
+struct Chunk {
+    uint4 k[kInplaceR], v[kInplaceR];
+    int dst[kInplaceR];  // destination row, or -1 (no slot, or the row is already in place)
+};
+
+__device__ __forceinline__ void inplace_load(Chunk &c, int chunk, int n, int T, const int32_t *ih, const uint8_t *Kh,
+                                             const uint8_t *Vh, int hw, uint32_t *status)
+{
+#pragma unroll
+    for (int u = 0; u < kInplaceR; ++u) {
+        const int j = chunk * kInplaceRows + u * kSlots + hw;
+        c.dst[u] = -1;
+        if (j < n) {
+            const int src = ih[j];
+            if (src < j || src >= T) {
+                atomicOr(status, MKV_DEV_INTERNAL);  // not an ascending index list: the move would be unsafe
+            } else if (src != j) {
+                c.dst[u] = j;
+                c.k[u] = ld_cg(Kh + (size_t)src * kRowBytes);
+                c.v[u] = ld_cg(Vh + (size_t)src * kRowBytes);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void inplace_store(const Chunk &c, uint8_t *Kh, uint8_t *Vh)
+{
+#pragma unroll
+    for (int u = 0; u < kInplaceR; ++u) {
+        if (c.dst[u] >= 0) {
+            st_stream(Kh + (size_t)c.dst[u] * kRowBytes, c.k[u]);
+            st_stream(Vh + (size_t)c.dst[u] * kRowBytes, c.v[u]);
+        }
+    }
+}
+
+// In-place compaction: row j of each head becomes row idx[j] (j < kept), in
+// the head's own K and V rows. Row r is read by at most one slot j <= r
+// (idx ascends from 0, so idx[j] >= j) and written by slot r, so walking the
+// slots in chunks of 64 in ascending order is safe when chunk c's loads are
+// performed before chunk c's stores (a CTA barrier between them): every
+// earlier reader of a row chunk c overwrites sits in chunk c or before. The
+// loads of chunk c+1 read rows at or beyond its own slots, which no earlier
+// chunk writes, so they are issued before chunk c's stores (two chunks in
+// flight). One CTA walks one head; heads are spread over the persistent grid.
+__global__ void __launch_bounds__(kStreamThreads)
+k_gather_inplace(const int32_t *__restrict__ idx, int idx_stride, const int32_t *__restrict__ kept,
+                 const int32_t *__restrict__ seq_lens, int heads, int t_max, int64_t n_heads, uint8_t *K, uint8_t *V,
+                 uint32_t *status)
+{
+    const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+    for (int64_t head = blockIdx.x; head < n_heads; head += gridDim.x) {
+        const int T = head_len(seq_lens, head, heads, t_max, status, false);
+        const int n = min(kept[head], T);
+        if (n <= 0) continue;  // the same for every thread
+        const int32_t *ih = idx + head * idx_stride;
+        uint8_t *Kh = K + (size_t)head * t_max * kRowBytes + l16 * 16;
+        uint8_t *Vh = V + (size_t)head * t_max * kRowBytes + l16 * 16;
+        const int nch = (n + kInplaceRows - 1) / kInplaceRows;
+        Chunk a, b;
+        inplace_load(a, 0, n, T, ih, Kh, Vh, hw, status);
+        for (int c = 0; c < nch; c += 2) {
+            __syncthreads();  // chunk c's loads are performed CTA-wide
+            if (c + 1 < nch) inplace_load(b, c + 1, n, T, ih, Kh, Vh, hw, status);
+            inplace_store(a, Kh, Vh);
+            if (c + 1 >= nch) break;
+            __syncthreads();  // chunk c+1's loads are performed CTA-wide
+            if (c + 2 < nch) inplace_load(a, c + 2, n, T, ih, Kh, Vh, hw, status);
+            inplace_store(b, Kh, Vh);
+        }
+        __syncthreads();  // the next head starts with every store of this one issued
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gather_inplace(const Geometry &g, const int32_t *idx, int32_t idx_stride, const int32_t *kept,
+                                  const int32_t *seq_lens, void *K, void *V, uint32_t *status, cudaStream_t st)
+{
+    if (g.n_heads == 0) return cudaSuccess;
+    const int grid = grid_for_items(reinterpret_cast<const void *>(k_gather_inplace), kStreamThreads, 0, g.n_heads);
+    k_gather_inplace<<<grid, kStreamThreads, 0, st>>>(idx, idx_stride, kept, seq_lens, g.heads, g.t_max, g.n_heads,
+                                                      static_cast<uint8_t *>(K), static_cast<uint8_t *>(V), status);
+    return cudaGetLastError();
+}
+
+}  // namespace mkv

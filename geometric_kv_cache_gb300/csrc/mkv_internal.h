@@ -93,6 +93,10 @@ cudaError_t launch_select_quota(const Geometry &g, const float *S, const int32_t
 // the windows of a bf16 tensor, 0 < window <= kSmallWindowMax.
 cudaError_t launch_small_window_means(const PieceGeometry &g, const void *X, const int32_t *seq_lens, float *mean,
                                       float *radius, uint32_t *status, cudaStream_t st);
+// In place: K/V rows [head][j] = K/V[head][idx[head * idx_stride + j]] for
+// j < kept[head], inside the head's own rows (idx ascending).
+cudaError_t launch_gather_inplace(const Geometry &g, const int32_t *idx, int32_t idx_stride, const int32_t *kept,
+                                  const int32_t *seq_lens, void *K, void *V, uint32_t *status, cudaStream_t st);
 // OjaKV-style reconstruction-error scores (mkv_oja.cu): the projected query
 // rows (hi + lo bf16, oja_operand_bytes in `qhl`), then the tcgen05
 // contraction writing S[head * t_max + t] for t < T_head.

@@ -240,6 +240,18 @@ mkv_status mkv_compress_oja(const void *K, const void *V, const void *Q, const f
                             int32_t keep_stride, void *K_out, void *V_out, int32_t *idx, int32_t *kept,
                             void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
+/* mkv_compress that writes the compacted cache over the input (the
+ * memory-saving form: no output buffers). After the call, rows
+ * [0, kept[h]) of head h in K and V hold K/V[h][idx[h][j]], j < kept[h], in
+ * ascending token order; rows from kept[h] on are unchanged. idx
+ * [batch*heads, t_max] and kept [batch*heads] may be NULL (not returned).
+ * Scores and selection are those of mkv_compress; the move runs one CTA per
+ * head through chunks of 64 rows in ascending order (a row is always read
+ * before it is overwritten, as idx[j] >= j). */
+mkv_status mkv_compress_inplace(void *K, void *V, mkv_shape shape, double ratio, const int32_t *n_keep,
+                                mkv_mode mode, int32_t window, int32_t *idx, int32_t *kept, void *workspace,
+                                size_t workspace_bytes, mkv_stream_t stream);
+
 /* Number of stages mkv_compress_profiled brackets with events: 6, one per
  * kernel -- piece sums (a1), window means (a1), scores (a2), top-k select
  * (a3; also emits the kept indices when a head's scores fit in shared

@@ -236,3 +236,18 @@ def test_oja_calls_reject_bad_arguments():
                                 vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
     assert lib.mkv_compress_oja(vp(A), vp(A), vp(A), vp(A), shp, 128, 64, 0.5, None, 100, vp(A), vp(A), None, None,
                                 vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+
+
+def test_in_place_compress_rejects_bad_arguments():
+    lib = mkv.load()
+    vp = ctypes.c_void_p
+    shp = _shape()
+    big = 1 << 40
+    f = lib.mkv_compress_inplace
+    assert f(None, vp(A), shp, 0.5, None, 0, 0, None, None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert f(vp(A + 8), vp(A), shp, 0.5, None, 0, 0, None, None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert f(vp(A), vp(A), shp, 1.5, None, 0, 0, None, None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert f(vp(A), vp(A), shp, 0.5, None, 9, 0, None, None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert f(vp(A), vp(A), shp, 0.5, None, 0, 0, vp(A + 2), None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
+    assert f(vp(A), vp(A), shp, 0.5, None, 0, 0, None, None, vp(A), 64, None) == mkv.MKV_ERR_WORKSPACE
+    assert f(vp(A), vp(A), _shape(batch=0), 0.5, None, 0, 0, None, None, vp(A), big, None) == mkv.MKV_OK

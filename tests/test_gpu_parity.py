@@ -360,6 +360,51 @@ def test_host_path_chunks_overlap_and_join_the_callers_stream():
         assert torch.equal(torch.where(live[..., None], hVo, 0), torch.where(live[..., None], Vo.cpu(), 0))
 
 
+def _check_in_place(K, V, lens, ratio, mode, window):
+    """mkv_compress_inplace against mkv_compress on the same cache."""
+    Ko, Vo, idx, kept, st = _run_fused(K, V, ratio, mode, window, lens)
+    assert st == 0
+    B, H, T, D = K.shape
+    Ki, Vi = K.clone(), V.clone()
+    idx_i = torch.full((B, H, T), -7, dtype=torch.int32, device=DEV)
+    kept_i = torch.full((B, H), -7, dtype=torch.int32, device=DEV)
+    ws = mkv.workspace_for(K, window, lens)
+    mkv.mkv_compress_inplace(Ki, Vi, ratio, mode, window, ws, idx_i, kept_i, lens)
+    assert mkv.mkv_device_status(ws) == 0
+    assert torch.equal(kept_i, kept)
+    ks = idx.shape[2]
+    slot = torch.arange(T, device=DEV)[None, None, :]
+    live = slot < kept[..., None]
+    assert torch.equal(torch.where(live[..., :ks], idx_i[..., :ks], 0), torch.where(live[..., :ks], idx, 0))
+    # rows [0, kept) are the compacted cache, every other row is untouched
+    front = live[..., None]
+    assert torch.equal(Ki[..., :ks, :][front[..., :ks, :].expand(-1, -1, -1, D)],
+                       Ko[front[..., :ks, :].expand(-1, -1, -1, D)])
+    assert torch.equal(Vi[..., :ks, :][front[..., :ks, :].expand(-1, -1, -1, D)],
+                       Vo[front[..., :ks, :].expand(-1, -1, -1, D)])
+    rest = ~front.expand(-1, -1, -1, D)
+    assert torch.equal(Ki[rest], K[rest]) and torch.equal(Vi[rest], V[rest])
+
+
+@pytest.mark.parametrize("mode,window,ratio", [("l2", 0, 0.5), ("cosine", 3000, 0.2), ("l2", 700, 0.9),
+                                               ("l2", 0, 0.0), ("l2", 0, 1.0)])
+def test_in_place_compaction_matches_the_out_of_place_path(mode, window, ratio):
+    w = synthkv.WORKLOADS["ragged-b8-llama-kv-t8k-32k"].scaled("inplace", layers=1, batch=3, heads=3, t_max=9001,
+                                                                 t_min=1)
+    K, V, lens = synthkv.make_kv(w, seed=13, device=DEV)
+    _check_in_place(K, V, lens, ratio, mode, window)
+
+
+def test_in_place_compaction_full_size():
+    w = synthkv.WORKLOADS["llama3.1-8b-kv-t16k"]
+    torch.cuda.empty_cache()
+    K, V, lens = synthkv.make_kv(w, seed=0, device=DEV)
+    mode, window, ratio = w.runs[0]
+    _check_in_place(K, V, lens, ratio, mode, window)
+    del K, V
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------ full-size workloads --
 
 def _full_size(name, runs=None, sample=4):
