@@ -257,7 +257,7 @@ def run_ours(args):
     lens_list = lens.cpu().tolist()
     single = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
     select_emits = T <= 40960  # select writes the kept indices itself (no compaction kernel)
-    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single == 1 else 2)
+    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single in (1, 2) else 2)
 
     def step():
         mkv.mkv_compress(K, V, ratio, mode, window, ks, K_out, V_out, idx, kept, ws, lens, stream=stream)
@@ -362,7 +362,8 @@ def run_ours(args):
         "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "kv_heads": w.heads,
                    "heads_total": w.n_heads, "t": T, "head_dim": w.head_dim, "mode": mode,
                    "window": window, "ratio": ratio, "keep_per_head": ks,
-                   "single_pass_centroid_score": single == 1,
+                   "centroid_score_path": {0: "three kernels (K read twice)", 1: "single pass (K read once)",
+                                           2: "head groups (K read from HBM once, again from L2)"}.get(single, "?"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "no flush: K+V (%.1f GB) exceed the 129 MB L2" % (2 * K.numel() * 2 / 1e9)},
         "hbm": {"path_bytes_per_step": nbytes["path"], "achieved_gbs": hbm_gbs,
@@ -375,7 +376,7 @@ def run_ours(args):
         "stages_ms": dict(zip(STAGES, stage_ms)),
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * ((2 if single == 1 else 4) + (0 if select_emits else 1)),
+        "gpu_launches": args.steps * ((2 if single in (1, 2) else 4) + (0 if select_emits else 1)),
         "clocks": clocks.summary(),
     }
     if world > 1:

@@ -48,7 +48,7 @@ EXPORTED = (
     "mkv_compress_noalloc", "mkv_compress_single_pass", "mkv_set_single_pass", "mkv_layer_budgets",
     "mkv_inject_stalled_windows", "mkv_window_means", "mkv_num_keep_quota", "mkv_select_quota",
     "mkv_compress_quota", "mkv_oja_workspace_size", "mkv_oja_score", "mkv_compress_oja", "mkv_oja_score_profiled",
-    "mkv_compress_inplace",
+    "mkv_compress_inplace", "mkv_set_head_groups", "mkv_centroid_score",
 )
 
 
@@ -96,6 +96,8 @@ def load(build_if_missing: bool = True):
             "mkv_compress_num_stages": (i32, []),
             "mkv_compress_single_pass": (i32, [MkvShape, i32, i32]),
             "mkv_set_single_pass": (i32, [i32]),
+            "mkv_set_head_groups": (i32, [i32]),
+            "mkv_centroid_score": (i32, [vp, MkvShape, i32, i32, vp, vp, vp, sz, vp]),
             "mkv_layer_budgets": (i32, [vp, i32, f64, f64, ctypes.c_int64, vp, vp]),
             "mkv_inject_stalled_windows": (i32, [vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
             "mkv_compress_profiled": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp,
@@ -189,6 +191,11 @@ def mkv_set_single_pass(enable: bool) -> bool:
     return bool(load().mkv_set_single_pass(1 if enable else 0))
 
 
+def mkv_set_head_groups(enable: bool) -> bool:
+    """Allow or forbid the head-group kernel; returns the previous setting."""
+    return bool(load().mkv_set_head_groups(1 if enable else 0))
+
+
 def mkv_layer_budgets(sensitivity, r: float, gamma: float, total: int, cap):
     """Per-layer kept-token budgets (host helper). Returns (status, budgets)
     with budgets an int32 list of one entry per layer; status 1 means the caps
@@ -226,6 +233,13 @@ def mkv_window_means(X, window, mean, workspace, radius=None, seq_lens=None, str
     _need_cuda(X, mean, radius, workspace, seq_lens)
     _check(load().mkv_window_means(_ptr(X), shape_of(X, seq_lens), int(window), _ptr(mean), _ptr(radius),
                                    _ptr(workspace), workspace.numel(), _stream(stream)), "mkv_window_means")
+
+
+def mkv_centroid_score(K, window, mode, C, S, workspace, seq_lens=None, stream=None):
+    """Steps a1 + a2 as mkv_compress runs them (C and S as mkv_centroid / mkv_score write them)."""
+    _need_cuda(K, C, S, workspace, seq_lens)
+    _check(load().mkv_centroid_score(_ptr(K), shape_of(K, seq_lens), int(window), _MODES[mode], _ptr(C), _ptr(S),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)), "mkv_centroid_score")
 
 
 def mkv_score(K, C, window, mode, S, workspace, seq_lens=None, stream=None):

@@ -24,6 +24,10 @@ constexpr size_t kAlign = 256;
 // currently faster for every measured shape.
 std::atomic<int> g_single_pass_enabled{0};
 
+// Whether mkv_compress may use the head-group kernel (one read of K from
+// HBM, global centroids, heads short enough for L2). On by default.
+std::atomic<int> g_head_groups_enabled{1};
+
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -154,6 +158,59 @@ mkv_status check_outputs(const mkv_shape &s, double ratio, const int32_t *n_keep
     return MKV_OK;
 }
 
+// a1 + a2 as mkv_compress runs them: the head-group kernel (global
+// centroids whose heads fit in L2, K read from HBM once), the single-pass
+// kernel (opt-in), or piece sums + window means + scores. All write the same
+// bits to C and S. `mark(i)` records the caller's stage events 1..3.
+template <typename Mark>
+mkv_status run_centroid_score(const Geometry &g, const Layout &L, const void *K, const mkv_shape &s, mkv_mode mode,
+                              void *ws, float *C, float *S, cudaStream_t st, Mark &mark, bool stall_windows)
+{
+    uint32_t *status = region<uint32_t>(ws, L.status);
+    float *partial = region<float>(ws, L.partial);
+    cudaError_t e = cudaSuccess;
+    const int grid =
+        (stall_windows || g_single_pass_enabled.load(std::memory_order_relaxed)) ? single_pass_grid((int)mode) : 0;
+    bool single = grid > 0 && grid >= g.pg.ppw;
+    if (stall_windows && !single) return MKV_ERR_UNSUPPORTED;
+    const HeadGroupPlan plan = (!single && g_head_groups_enabled.load(std::memory_order_relaxed))
+                                   ? head_group_plan(g.pg, (int)mode, L.centroid - L.counters)
+                                   : HeadGroupPlan{};
+    if (plan.groups > 0) {
+        e = launch_head_groups(g.pg, plan, K, s.seq_lens, (int)mode, partial, region<uint32_t>(ws, L.counters), C, S,
+                               status, st);
+        if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer CTAs fit right now: the three-kernel path
+            (void)cudaGetLastError();
+            e = cudaSuccess;
+        } else {
+            if (e != cudaSuccess) return cuda_status(e);
+            single = true;
+            if (!mark(1) || !mark(2) || !mark(3)) return MKV_ERR_CUDA;
+        }
+    } else if (single) {
+        e = launch_single_pass(g.pg, grid, K, s.seq_lens, (int)mode, partial, region<float>(ws, L.gsum),
+                               region<uint32_t>(ws, L.counters), C, S, status, st, stall_windows);
+        if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer CTAs fit right now
+            (void)cudaGetLastError();
+            single = false;
+            e = cudaSuccess;
+        } else {
+            if (e != cudaSuccess) return cuda_status(e);
+            if (!mark(1) || !mark(2) || !mark(3)) return MKV_ERR_CUDA;
+        }
+    }
+    if (!single) {
+        if ((e = launch_piece_sums(g.pg, K, s.seq_lens, partial, status, st)) != cudaSuccess) return cuda_status(e);
+        if (!mark(1)) return MKV_ERR_CUDA;
+        if ((e = launch_window_means(g.pg, partial, s.seq_lens, C, status, st)) != cudaSuccess) return cuda_status(e);
+        if (!mark(2)) return MKV_ERR_CUDA;
+        if ((e = launch_piece_scores(g.pg, K, C, s.seq_lens, (int)mode, S, status, st)) != cudaSuccess)
+            return cuda_status(e);
+        if (!mark(3)) return MKV_ERR_CUDA;
+    }
+    return MKV_OK;
+}
+
 // The fused launch sequence; events (optional) bracket every kernel.
 mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio, const int32_t *n_keep,
                         mkv_mode mode, int32_t window, int32_t keep_stride, void *K_out, void *V_out,
@@ -173,7 +230,6 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     if (rc != MKV_OK) return rc;
     if (empty(s)) return MKV_OK;
     uint32_t *status = region<uint32_t>(ws, L.status);
-    float *partial = region<float>(ws, L.partial);
     float *C = region<float>(ws, L.centroid);
     float *S = region<float>(ws, L.score);
     mkv_cut *cut = region<mkv_cut>(ws, L.cut);
@@ -184,32 +240,9 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     };
     cudaError_t e = cudaSuccess;
     if (!mark(0)) return MKV_ERR_CUDA;
-    // a1 + a2: one pass over K when enabled and every window's pieces fit the
-    // resident grid; else piece sums, window means, scores (same bits)
-    const int grid =
-        (stall_windows || g_single_pass_enabled.load(std::memory_order_relaxed)) ? single_pass_grid((int)mode) : 0;
-    bool single = grid > 0 && grid >= g.pg.ppw;
-    if (stall_windows && !single) return MKV_ERR_UNSUPPORTED;
-    if (single) {
-        e = launch_single_pass(g.pg, grid, K, s.seq_lens, (int)mode, partial, region<float>(ws, L.gsum),
-                               region<uint32_t>(ws, L.counters), C, S, status, st, stall_windows);
-        if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer CTAs fit right now
-            (void)cudaGetLastError();
-            single = false;
-            e = cudaSuccess;
-        }
-        if (e != cudaSuccess) return cuda_status(e);
-        if (!mark(1) || !mark(2) || !mark(3)) return MKV_ERR_CUDA;
-    }
-    if (!single) {
-        if ((e = launch_piece_sums(g.pg, K, s.seq_lens, partial, status, st)) != cudaSuccess) return cuda_status(e);
-        if (!mark(1)) return MKV_ERR_CUDA;
-        if ((e = launch_window_means(g.pg, partial, s.seq_lens, C, status, st)) != cudaSuccess) return cuda_status(e);
-        if (!mark(2)) return MKV_ERR_CUDA;
-        if ((e = launch_piece_scores(g.pg, K, C, s.seq_lens, (int)mode, S, status, st)) != cudaSuccess)
-            return cuda_status(e);
-        if (!mark(3)) return MKV_ERR_CUDA;
-    }
+    // a1 + a2 (C and S are workspace regions here)
+    rc = run_centroid_score(g, L, K, s, mode, ws, C, S, st, mark, stall_windows);
+    if (rc != MKV_OK) return rc;
     // a3 (+ a4 when the head's scores fit shared memory), then a4, a5
     int32_t *idx_w = idx ? idx : region<int32_t>(ws, L.idx);
     const int32_t idx_stride = idx ? keep_stride : g.t_max;
@@ -358,6 +391,21 @@ mkv_status mkv_window_means(const void *X, mkv_shape shape, int32_t window, floa
     cudaError_t e = launch_piece_sums(g.pg, X, shape.seq_lens, region<float>(workspace, L.partial), status, st);
     if (e == cudaSuccess) e = launch_window_means(g.pg, region<float>(workspace, L.partial), shape.seq_lens, mean, status, st);
     return cuda_status(e);
+}
+
+mkv_status mkv_centroid_score(const void *K, mkv_shape shape, int32_t window, mkv_mode mode, float *C, float *S,
+                              void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    mkv_status rc = check_shape(shape);
+    if (rc != MKV_OK) return rc;
+    if (!K || !C || !S || window < 0 || !aligned(K, 16) || !aligned(C, 16) || !aligned(S, 4)) return MKV_ERR_INVALID_ARG;
+    if (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE) return MKV_ERR_INVALID_ARG;
+    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window);
+    const Layout L = make_layout(g);
+    if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
+    if (empty(shape)) return MKV_OK;
+    auto mark = [](int) { return true; };
+    return run_centroid_score(g, L, K, shape, mode, workspace, C, S, reinterpret_cast<cudaStream_t>(stream), mark, false);
 }
 
 mkv_status mkv_score(const void *K, const float *C, mkv_shape shape, int32_t window, mkv_mode mode, float *S,
@@ -567,11 +615,22 @@ int32_t mkv_compress_num_stages(void) { return kCompressStages; }
 int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
 {
     if (check_shape(shape) != MKV_OK || window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE)) return -1;
-    if (!g_single_pass_enabled.load(std::memory_order_relaxed)) return 0;
     const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window);
-    const int grid = single_pass_grid((int)mode);
-    if (grid <= 0) return -1;
-    return grid >= g.pg.ppw ? 1 : 0;
+    if (g_single_pass_enabled.load(std::memory_order_relaxed)) {
+        const int grid = single_pass_grid((int)mode);
+        if (grid <= 0) return -1;
+        if (grid >= g.pg.ppw) return 1;
+    }
+    if (g_head_groups_enabled.load(std::memory_order_relaxed)) {
+        const Layout L = make_layout(g);
+        if (head_group_plan(g.pg, (int)mode, L.centroid - L.counters).groups > 0) return 2;
+    }
+    return 0;
+}
+
+int32_t mkv_set_head_groups(int32_t enable)
+{
+    return g_head_groups_enabled.exchange(enable ? 1 : 0);
 }
 
 mkv_status mkv_inject_stalled_windows(const void *K, const void *V, mkv_shape shape, double ratio, mkv_mode mode,

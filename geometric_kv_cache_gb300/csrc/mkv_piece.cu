@@ -21,6 +21,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "mkv_device.cuh"
 #include "mkv_internal.h"
 
@@ -799,6 +801,167 @@ k_single_pass(PieceGeometry g, FusedPointers F)
     }
 }
 
+// ------------------------------------------------------ head groups --
+
+// 16-byte non-coherent load carrying an L2 eviction policy (createpolicy).
+__device__ __forceinline__ uint4 ld_policy(const void *p, uint64_t pol)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
+
+// load_rows with an L2 eviction policy on every load.
+template <int N>
+__device__ __forceinline__ void load_rows_policy(const uint8_t *base, int len, int i0, uint4 v[2 * N], uint64_t pol)
+{
+    const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+        const int r = slot + (i0 + u) * kRowSlots;
+        const uint8_t *row = base + (size_t)(r < len ? r : 0) * kRowBytes;
+        v[2 * u] = ld_policy(row + q * 16, pol);
+        v[2 * u + 1] = ld_policy(row + 128 + q * 16, pol);
+    }
+}
+//
+// One read of K from HBM for a1 + a2 with a global centroid per head: a
+// group of `gsize` CTAs shares a head. Pass 1: each CTA sums its pieces p =
+// rank, rank + gsize, ... (exactly the arithmetic of k_piece_sums) and writes
+// the piece sums; the group then meets at a barrier (an arrival counter in
+// global memory, polled with a time bound). Each CTA forms the head's mean
+// from all piece sums (exactly k_window_means' order) and, in pass 2,
+// re-reads its own pieces and scores them (exactly k_piece_scores). Only a
+// few heads are in flight at a time -- one per group -- so the host picks
+// the group count such that their keys fit in L2 and pass 2 reads L2, not
+// HBM. The CTAs of one group do the same number of rounds; the kernel is
+// launched cooperatively (all CTAs resident), so every arrival comes.
+// Pass 1 loads carry an L2 evict-last policy and pass 2 loads evict-first,
+// so the rows of the heads in flight stay in L2 until their second read
+// (measured: 0.30 ms against 0.33 ms for the three kernels on 256 heads of
+// 16K tokens; without the policies pass 2 missed L2 on about a third of its
+// rows). Same bits as the three-kernel path.
+constexpr int kBatchG = 8;  // rows per lane in flight
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 2)
+k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize)
+{
+    extern __shared__ float dyn[];      // red [kWarps][128], mean [128]; the rest only caps CTAs per SM
+    float *red = dyn;
+    float *cmean = dyn + kWarps * kHeadDim;
+    __shared__ uint32_t s_ok;
+    const int groups = gridDim.x / gsize;
+    const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
+    if (group >= groups) return;  // a launch is always a whole number of groups
+    const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
+    uint64_t keep_l2, drop_l2;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep_l2));
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(drop_l2));
+    uint32_t round = 0;
+    for (int64_t head = group; head < g.n_heads; head += groups, ++round) {
+        const int T = head_len(P.seq_lens, head, g.heads, g.t_max, P.status, threadIdx.x == 0 && rank == 0);
+        const int np = (T + g.piece_rows - 1) / g.piece_rows;
+        // pass 1: piece sums
+        for (int p = rank; p < np; p += gsize) {
+            const int a = p * g.piece_rows, len = min(g.piece_rows, T - a);
+            const uint8_t *base = P.K + ((size_t)head * g.t_max + a) * kRowBytes;
+            const int nrows = (len + kRowSlots - 1) / kRowSlots;
+            float acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+            for (int i0 = 0; i0 < nrows; i0 += kBatchG) {
+                uint4 v[2 * kBatchG];
+                load_rows_policy<kBatchG>(base, len, i0, v, keep_l2);
+#pragma unroll
+                for (int u = 0; u < kBatchG; ++u) {
+                    if (slot + (i0 + u) * kRowSlots < len) {
+                        float f[16];
+                        bf16x8_to_f32(v[2 * u], f);
+                        bf16x8_to_f32(v[2 * u + 1], f + 8);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[j] += f[j];
+                    }
+                }
+            }
+            finish_sum(acc, red, P.partial + (head * g.ppw + p) * kHeadDim);
+            if (threadIdx.x < kHeadDim) __threadfence();  // the piece sum is visible GPU-wide before the arrival
+            __syncthreads();  // red is free again
+        }
+        // the group's barrier for this head
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(&gcnt[group], 1u);
+            const uint32_t target = (round + 1) * (uint32_t)gsize;
+            const uint64_t t0 = global_ns();
+            uint32_t ok = 1;
+            for (uint32_t spin = 0; ld_acquire(&gcnt[group]) < target; ++spin) {
+                if ((spin & 63u) == 63u && global_ns() - t0 > kWaitNs) {
+                    atomicOr(P.status, MKV_DEV_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+            }
+            s_ok = ok;
+        }
+        __syncthreads();
+        if (s_ok && T > 0) {  // the same for every thread
+            if (threadIdx.x < kHeadDim) {
+                // k_window_means' order (pieces of a group of 32 in order,
+                // then the groups), with a whole group's loads in flight
+                const int ng = (np + kGroupPieces - 1) / kGroupPieces;
+                const float *pw = P.partial + head * (int64_t)g.ppw * kHeadDim + threadIdx.x;
+                float tot = 0.f;
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int n = min(kGroupPieces, np - gi * kGroupPieces);
+                    float v[kGroupPieces];
+#pragma unroll
+                    for (int j = 0; j < kGroupPieces; ++j)
+                        v[j] = j < n ? __ldcg(pw + (int64_t)(gi * kGroupPieces + j) * kHeadDim) : 0.f;
+                    float gs = 0.f;
+#pragma unroll
+                    for (int j = 0; j < kGroupPieces; ++j)
+                        if (j < n) gs += v[j];
+                    tot += gs;
+                }
+                cmean[threadIdx.x] = __fdiv_rn(tot, (float)T);
+            }
+            __syncthreads();
+            float c[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = cmean[q * 8 + j];
+                c[8 + j] = cmean[64 + q * 8 + j];
+            }
+            const float nc = MODE == MKV_MODE_COSINE ? centroid_norm(c) : 0.f;
+            // pass 2: scores of the same pieces (their rows are L2 hits)
+            for (int p = rank; p < np; p += gsize) {
+                const int a = p * g.piece_rows, len = min(g.piece_rows, T - a);
+                const uint8_t *base = P.K + ((size_t)head * g.t_max + a) * kRowBytes;
+                float *srow = P.S + (size_t)head * g.t_max + a;
+                const int nrows = (len + kRowSlots - 1) / kRowSlots;
+                for (int i0 = 0; i0 < nrows; i0 += kBatchG) {
+                    uint4 v[2 * kBatchG];
+                    load_rows_policy<kBatchG>(base, len, i0, v, drop_l2);
+#pragma unroll
+                    for (int u = 0; u < kBatchG; ++u) {
+                        const int r = slot + (i0 + u) * kRowSlots;
+                        float f[16];
+                        bf16x8_to_f32(v[2 * u], f);
+                        bf16x8_to_f32(v[2 * u + 1], f + 8);
+                        const float sc = score_of<MODE>(f, c, nc);
+                        if (r < len && q == 0) srow[r] = sc;
+                    }
+                }
+            }
+            if (rank == 0 && threadIdx.x < kHeadDim) P.C[head * kHeadDim + threadIdx.x] = cmean[threadIdx.x];
+        }
+        __syncthreads();  // cmean is rewritten for the next head
+    }
+}
+
 Pointers make_pointers(const void *K, const int32_t *seq_lens, float *partial, float *C, float *S, uint32_t *status)
 {
     Pointers P;
@@ -849,6 +1012,64 @@ cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, 
     const void *fn = mode == MKV_MODE_L2 ? reinterpret_cast<const void *>(k_single_pass<MKV_MODE_L2>)
                                          : reinterpret_cast<const void *>(k_single_pass<MKV_MODE_COSINE>);
     return cudaLaunchCooperativeKernel(fn, dim3((unsigned)grid), dim3(kFusedThreads), args, sizeof(FusedShared), st);
+}
+
+// Dynamic shared memory of k_head_groups: red and the mean, padded so that
+// at most two CTAs share an SM (the grid is then spread over all SMs).
+constexpr size_t kGroupSmem = 80 * 1024;
+
+HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
+{
+    HeadGroupPlan plan;
+    if (g.nwin_max != 1 || g.n_heads == 0 || g.t_max == 0) return plan;  // global centroids only
+    const void *fn = mode == MKV_MODE_L2 ? reinterpret_cast<const void *>(k_head_groups<MKV_MODE_L2>)
+                                         : reinterpret_cast<const void *>(k_head_groups<MKV_MODE_COSINE>);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
+        return plan;
+    const int resident = resident_grid(fn, kThreads, kGroupSmem);
+    int dev = 0, l2 = 0;
+    if (resident < 16 || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0)
+        return plan;
+    // Heads in flight (one per group) must fit in 60% of L2. Among group
+    // sizes of 8..64 CTAs, take the one with the least modelled time:
+    // rounds (heads per group) x (the busiest CTA's pieces + 2 for the
+    // barrier, the mean and the L2 pass), with the groups filling at least
+    // 3/4 of the resident grid (else the three-kernel path keeps more SMs
+    // busy).
+    const double head_bytes = (double)g.t_max * kRowBytes;
+    const int64_t fit = (int64_t)(0.6 * (double)l2 / head_bytes);
+    double best = 0.0;
+    for (int gsize = 8; gsize <= 64; ++gsize) {
+        const int64_t groups = std::min<int64_t>(std::min<int64_t>(fit, resident / gsize), g.n_heads);
+        if (groups < 1 || 4 * groups * gsize < 3 * (int64_t)resident) continue;
+        if ((size_t)groups * sizeof(uint32_t) > counters) continue;
+        const int64_t rounds = (g.n_heads + groups - 1) / groups;
+        const int ppc = (g.ppw + gsize - 1) / gsize;
+        const double cost = (double)rounds * (ppc + 2);
+        if (plan.groups == 0 || cost < best) {
+            best = cost;
+            plan.groups = (int)groups;
+            plan.gsize = gsize;
+        }
+    }
+    return plan;
+}
+
+cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan, const void *K,
+                               const int32_t *seq_lens, int mode, float *partial, uint32_t *cnt, float *C, float *S,
+                               uint32_t *status, cudaStream_t st)
+{
+    cudaError_t e = cudaMemsetAsync(cnt, 0, (size_t)plan.groups * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    Pointers P = make_pointers(K, seq_lens, partial, C, S, status);
+    PieceGeometry gg = g;
+    int gsize = plan.gsize;
+    void *args[] = {&gg, &P, &cnt, &gsize};
+    const void *fn = mode == MKV_MODE_L2 ? reinterpret_cast<const void *>(k_head_groups<MKV_MODE_L2>)
+                                         : reinterpret_cast<const void *>(k_head_groups<MKV_MODE_COSINE>);
+    return cudaLaunchCooperativeKernel(fn, dim3((unsigned)(plan.groups * plan.gsize)), dim3(kThreads), args,
+                                       kGroupSmem, st);
 }
 
 cudaError_t launch_piece_sums(const PieceGeometry &g, const void *K, const int32_t *seq_lens, float *partial,

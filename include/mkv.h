@@ -141,6 +141,12 @@ mkv_status mkv_centroid(const void *K, mkv_shape shape, int32_t window, float *C
 mkv_status mkv_window_means(const void *X, mkv_shape shape, int32_t window, float *mean, float *radius,
                             void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
+/* Steps a1 and a2 together, as mkv_compress runs them (the head-group, the
+ * single-pass or the three-kernel path; see mkv_compress_single_pass):
+ * C and S as written by mkv_centroid and mkv_score, the same bits. */
+mkv_status mkv_centroid_score(const void *K, mkv_shape shape, int32_t window, mkv_mode mode, float *C, float *S,
+                              void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
 /* Scores (abstract: Euclidean distance to the key centroid; cosine baseline).
  * C as written by mkv_centroid. S: fp32 [batch, heads, t_max]; S[h][t] for
  * t < T_b is the score of token t against its window's centroid (fp32,
@@ -256,16 +262,25 @@ mkv_status mkv_compress_inplace(void *K, void *V, mkv_shape shape, double ratio,
  * kernel -- piece sums (a1), window means (a1), scores (a2), top-k select
  * (a3; also emits the kept indices when a head's scores fit in shared
  * memory, t_max <= 40960), compaction into ascending indices (a4; empty when
- * select emitted them), row gather of K and V (a5). With the single-pass
- * kernel enabled and in use, stage 0 is that kernel and stages 1-2 are
+ * select emitted them), row gather of K and V (a5). When the single-pass or
+ * the head-group kernel is in use, stage 0 is that kernel and stages 1-2 are
  * empty. */
 int32_t mkv_compress_num_stages(void);
 
-/* 1 if mkv_compress on the current device reads K once (the single-pass
- * centroid + score kernel) for this shape, window and mode; 0 if it uses the
+/* Which a1 + a2 path mkv_compress takes on the current device for this
+ * shape, window and mode: 1 the single-pass kernel (opt-in, K read once),
+ * 2 the head-group kernel (default for global centroids when the heads in
+ * flight fit in L2: K read from HBM once, the second read hits L2), 0 the
  * three-kernel path (K read twice); -1 on a bad argument or CUDA error.
- * Both give bit-identical results. */
+ * All give bit-identical results. */
 int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode);
+
+/* Allow (1, the default) or forbid (0) the head-group kernel in
+ * mkv_compress, process-wide; returns the previous setting. With a global
+ * centroid, groups of CTAs share a head: they sum its pieces, meet at a
+ * bounded arrival barrier, form the mean and score the pieces again while
+ * their rows are still in L2 -- one HBM read of K instead of two. */
+int32_t mkv_set_head_groups(int32_t enable);
 
 /* Per-layer kept-token budgets for the n_keep array (host helper). The
  * budget mapping of "RippleKV" (gist.science explainer of arXiv 2608.08684),

@@ -490,7 +490,9 @@ def test_single_pass_is_used_for_the_bench_shape_when_enabled():
         assert mkv.mkv_compress_single_pass(small, 4096, "cosine") == 1
     finally:
         mkv.mkv_set_single_pass(prev)
-    assert mkv.mkv_compress_single_pass(small, 0, "l2") == (1 if prev else 0)
+    # single pass off: the bench shape (global centroids, 4 MB heads) takes
+    # the head-group kernel
+    assert mkv.mkv_compress_single_pass(small, 0, "l2") == (1 if prev else 2)
     assert mkv.load().mkv_compress_single_pass(small, -1, 0) == -1
 
 
@@ -516,6 +518,67 @@ def test_single_pass_and_three_kernel_paths_give_the_same_bits():
             r, hh = divmod(h, w.heads)
             n = int(a[3][r, hh])
             assert torch.equal(a[2][r, hh, :n], b.idx[r, hh, :n])
+
+
+def test_head_groups_are_used_only_where_they_fit():
+    bench = mkv.MkvShape(32, 8, 16384, 128, None)
+    assert mkv.mkv_compress_single_pass(bench, 0, "l2") == 2
+    assert mkv.mkv_compress_single_pass(bench, 0, "cosine") == 2
+    assert mkv.mkv_compress_single_pass(bench, 4096, "l2") == 0        # windows: three kernels
+    assert mkv.mkv_compress_single_pass(mkv.MkvShape(40, 10, 131072, 128, None), 0, "l2") == 0  # 32 MB heads
+    prev = mkv.mkv_set_head_groups(False)
+    try:
+        assert mkv.mkv_compress_single_pass(bench, 0, "l2") == 0
+    finally:
+        mkv.mkv_set_head_groups(prev)
+
+
+def _paths_agree(K, V, lens, mode, ratio):
+    """mkv_centroid_score and mkv_compress with and without head groups: the
+    same bits."""
+    B, H, T, D = K.shape
+    out = []
+    for enable in (True, False):
+        prev = mkv.mkv_set_head_groups(enable)
+        try:
+            used = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), 0, mode)
+            ws = mkv.workspace_for(K, 0, lens)
+            C = torch.full((B, H, 1, D), float("nan"), device=DEV)
+            S = torch.full((B, H, T), float("nan"), device=DEV)
+            mkv.mkv_centroid_score(K, 0, mode, C, S, ws, lens)
+            assert mkv.mkv_device_status(ws) == 0
+            out.append((used, C, S, _run_fused(K, V, ratio, mode, 0, lens)))
+        finally:
+            mkv.mkv_set_head_groups(prev)
+    (u1, C1, S1, f1), (u0, C0, S0, f0) = out
+    assert u1 == 2 and u0 == 0
+    live = torch.arange(T, device=DEV)[None, None, :] < lens[:, None, None]
+    has = (lens > 0)[:, None, None, None].expand_as(C1)
+    assert torch.equal(S1[live.expand_as(S1)], S0[live.expand_as(S0)])
+    assert torch.equal(C1[has], C0[has])
+    assert f1[4] == 0 and f0[4] == 0
+    for x, y in zip(f1[:4], f0[:4]):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("mode", ["l2", "cosine"])
+def test_head_group_and_three_kernel_paths_give_the_same_bits(mode):
+    # ragged lengths from 1 to 20000 (pieces of 512 tokens), 24 heads
+    w = synthkv.WORKLOADS["ragged-b8-llama-kv-t8k-32k"].scaled("hg", layers=2, batch=3, heads=4, t_max=20000,
+                                                                 t_min=1)
+    K, V, lens = synthkv.make_kv(w, seed=21, device=DEV)
+    _paths_agree(K, V, lens, mode, 0.4)
+
+
+def test_head_groups_with_few_short_heads_and_the_bench_shape():
+    # 5 heads of 300 tokens (fewer heads than groups, one piece each)
+    w = synthkv.WORKLOADS["single-layer-h8-t4096"].scaled("hg-few", heads=5, t_max=300)
+    K, V, lens = synthkv.make_kv(w, seed=22, device=DEV)
+    _paths_agree(K, V, lens, "l2", 0.5)
+    # a quarter of the bench workload (64 heads x 16384)
+    w = synthkv.WORKLOADS["llama3.1-8b-kv-t16k"].scaled("hg-bench", layers=8)
+    K, V, lens = synthkv.make_kv(w, seed=23, device=DEV)
+    _paths_agree(K, V, lens, "l2", 0.5)
 
 
 def test_per_layer_budgets_end_to_end():
