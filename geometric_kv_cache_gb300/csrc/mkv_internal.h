@@ -73,12 +73,13 @@ int single_pass_grid(int mode);
 cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, const int32_t *seq_lens, int mode,
                                float *partial, float *gsum, uint32_t *cnt, float *C, float *S, uint32_t *status,
                                cudaStream_t st, bool stall_windows = false);
-// Head groups (one read of K from HBM for a1 + a2, global centroids): the
-// plan has groups = 0 when the shape does not qualify (windows, heads too
-// long for L2, too few resident CTAs, or too little counter space).
+// Head groups (one read of K from HBM for a1 + a2): the plan has groups = 0
+// when the shape does not qualify (a global centroid over a head too long
+// for L2, too few resident CTAs, or too little counter space).
 struct HeadGroupPlan {
     int groups = 0;
-    int gsize = 0;
+    int gsize = 0;  // CTAs per group
+    int wb = 0;     // windows per unit
 };
 HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counter_bytes);
 cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan, const void *K,

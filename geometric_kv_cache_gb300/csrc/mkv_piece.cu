@@ -827,16 +827,17 @@ __device__ __forceinline__ void load_rows_policy(const uint8_t *base, int len, i
     }
 }
 //
-// One read of K from HBM for a1 + a2 with a global centroid per head: a
-// group of `gsize` CTAs shares a head. Pass 1: each CTA sums its pieces p =
-// rank, rank + gsize, ... (exactly the arithmetic of k_piece_sums) and writes
-// the piece sums; the group then meets at a barrier (an arrival counter in
-// global memory, polled with a time bound). Each CTA forms the head's mean
-// from all piece sums (exactly k_window_means' order) and, in pass 2,
-// re-reads its own pieces and scores them (exactly k_piece_scores). Only a
-// few heads are in flight at a time -- one per group -- so the host picks
-// the group count such that their keys fit in L2 and pass 2 reads L2, not
-// HBM. The CTAs of one group do the same number of rounds; the kernel is
+// One read of K from HBM for a1 + a2: a group of `gsize` CTAs shares a
+// unit -- a block of `wb` consecutive windows of one head (a global
+// centroid is one window: the unit is the whole head). Pass 1: each CTA sums
+// its piece slots f = rank, rank + gsize, ... (exactly the arithmetic of
+// k_piece_sums) and writes the piece sums; the group then meets at a barrier
+// (an arrival counter in global memory, polled with a time bound). Each CTA
+// forms the unit's window means from all piece sums (exactly k_window_means'
+// order) and, in pass 2, re-reads its own pieces and scores them (exactly
+// k_piece_scores). Only one unit per group is in flight, so the host picks
+// the group count and unit size such that their keys fit in L2 and pass 2
+// reads L2, not HBM. The CTAs of one group do the same number of rounds; the kernel is
 // launched cooperatively (all CTAs resident), so every arrival comes.
 // Pass 1 loads carry an L2 evict-last policy and pass 2 loads evict-first,
 // so the rows of the heads in flight stay in L2 until their second read
@@ -847,9 +848,9 @@ constexpr int kBatchG = 8;  // rows per lane in flight
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2)
-k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize)
+k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
 {
-    extern __shared__ float dyn[];      // red [kWarps][128], mean [128]; the rest only caps CTAs per SM
+    extern __shared__ float dyn[];  // red [kWarps][128], means [wb][128]; the rest only caps CTAs per SM
     float *red = dyn;
     float *cmean = dyn + kWarps * kHeadDim;
     __shared__ uint32_t s_ok;
@@ -860,14 +861,24 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize)
     uint64_t keep_l2, drop_l2;
     asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep_l2));
     asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(drop_l2));
+    const int upw = (g.nwin_max + wb - 1) / wb;  // units (blocks of wb windows) per head
+    const int64_t n_units = g.n_heads * upw;
     uint32_t round = 0;
-    for (int64_t head = group; head < g.n_heads; head += groups, ++round) {
-        const int T = head_len(P.seq_lens, head, g.heads, g.t_max, P.status, threadIdx.x == 0 && rank == 0);
-        const int np = (T + g.piece_rows - 1) / g.piece_rows;
-        // pass 1: piece sums
-        for (int p = rank; p < np; p += gsize) {
-            const int a = p * g.piece_rows, len = min(g.piece_rows, T - a);
-            const uint8_t *base = P.K + ((size_t)head * g.t_max + a) * kRowBytes;
+    for (int64_t unit = group; unit < n_units; unit += groups, ++round) {
+        const int64_t head = unit / upw;
+        const int w0 = (int)(unit - head * upw) * wb;
+        const int T = head_len(P.seq_lens, head, g.heads, g.t_max, P.status, threadIdx.x == 0 && rank == 0 && w0 == 0);
+        const int wl = window_len(T, g.window);
+        const int nw = T > 0 ? (T + wl - 1) / wl : 0;
+        const int nwu = max(0, min(w0 + wb, nw) - w0);  // windows of this unit that exist
+        const int nf = nwu * g.ppw;                      // piece slots of the unit
+        // pass 1: piece sums; piece slot f is window w0 + f / ppw, piece f % ppw
+        for (int f = rank; f < nf; f += gsize) {
+            const int w = w0 + f / g.ppw, p = f - (f / g.ppw) * g.ppw;
+            const int wstart = w * wl, wlen = min(wl, T - wstart), off = p * g.piece_rows;
+            if (off >= wlen) continue;  // past the window's last piece (the same for every thread)
+            const int len = min(g.piece_rows, wlen - off);
+            const uint8_t *base = P.K + ((size_t)head * g.t_max + wstart + off) * kRowBytes;
             const int nrows = (len + kRowSlots - 1) / kRowSlots;
             float acc[16];
 #pragma unroll
@@ -878,19 +889,19 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize)
 #pragma unroll
                 for (int u = 0; u < kBatchG; ++u) {
                     if (slot + (i0 + u) * kRowSlots < len) {
-                        float f[16];
-                        bf16x8_to_f32(v[2 * u], f);
-                        bf16x8_to_f32(v[2 * u + 1], f + 8);
+                        float f16[16];
+                        bf16x8_to_f32(v[2 * u], f16);
+                        bf16x8_to_f32(v[2 * u + 1], f16 + 8);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[j] += f[j];
+                        for (int j = 0; j < 16; ++j) acc[j] += f16[j];
                     }
                 }
             }
-            finish_sum(acc, red, P.partial + (head * g.ppw + p) * kHeadDim);
+            finish_sum(acc, red, P.partial + ((head * g.nwin_max + w) * (int64_t)g.ppw + p) * kHeadDim);
             if (threadIdx.x < kHeadDim) __threadfence();  // the piece sum is visible GPU-wide before the arrival
             __syncthreads();  // red is free again
         }
-        // the group's barrier for this head
+        // the group's barrier for this unit
         if (threadIdx.x == 0) {
             __threadfence();
             atomicAdd(&gcnt[group], 1u);
@@ -907,40 +918,50 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize)
             s_ok = ok;
         }
         __syncthreads();
-        if (s_ok && T > 0) {  // the same for every thread
-            if (threadIdx.x < kHeadDim) {
-                // k_window_means' order (pieces of a group of 32 in order,
-                // then the groups), with a whole group's loads in flight
+        if (s_ok && nwu > 0) {  // the same for every thread
+            // window means in k_window_means' order (pieces of a group of 32
+            // in order, then the groups), a group's loads in flight at once;
+            // threads t and t + 128 take alternate windows
+            for (int j = threadIdx.x >> 7; j < nwu; j += kThreads / kHeadDim) {
+                const int d = threadIdx.x & (kHeadDim - 1);
+                const int w = w0 + j;
+                const int wlen = min(wl, T - w * wl);
+                const int np = (wlen + g.piece_rows - 1) / g.piece_rows;
                 const int ng = (np + kGroupPieces - 1) / kGroupPieces;
-                const float *pw = P.partial + head * (int64_t)g.ppw * kHeadDim + threadIdx.x;
+                const float *pw = P.partial + (head * g.nwin_max + w) * (int64_t)g.ppw * kHeadDim + d;
                 float tot = 0.f;
                 for (int gi = 0; gi < ng; ++gi) {
                     const int n = min(kGroupPieces, np - gi * kGroupPieces);
                     float v[kGroupPieces];
 #pragma unroll
-                    for (int j = 0; j < kGroupPieces; ++j)
-                        v[j] = j < n ? __ldcg(pw + (int64_t)(gi * kGroupPieces + j) * kHeadDim) : 0.f;
+                    for (int k = 0; k < kGroupPieces; ++k)
+                        v[k] = k < n ? __ldcg(pw + (int64_t)(gi * kGroupPieces + k) * kHeadDim) : 0.f;
                     float gs = 0.f;
 #pragma unroll
-                    for (int j = 0; j < kGroupPieces; ++j)
-                        if (j < n) gs += v[j];
+                    for (int k = 0; k < kGroupPieces; ++k)
+                        if (k < n) gs += v[k];
                     tot += gs;
                 }
-                cmean[threadIdx.x] = __fdiv_rn(tot, (float)T);
+                const float m = __fdiv_rn(tot, (float)wlen);
+                cmean[j * kHeadDim + d] = m;
+                if (rank == 0) P.C[(head * g.nwin_max + w) * kHeadDim + d] = m;
             }
             __syncthreads();
-            float c[16];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                c[j] = cmean[q * 8 + j];
-                c[8 + j] = cmean[64 + q * 8 + j];
-            }
-            const float nc = MODE == MKV_MODE_COSINE ? centroid_norm(c) : 0.f;
             // pass 2: scores of the same pieces (their rows are L2 hits)
-            for (int p = rank; p < np; p += gsize) {
-                const int a = p * g.piece_rows, len = min(g.piece_rows, T - a);
-                const uint8_t *base = P.K + ((size_t)head * g.t_max + a) * kRowBytes;
-                float *srow = P.S + (size_t)head * g.t_max + a;
+            for (int f = rank; f < nf; f += gsize) {
+                const int jw = f / g.ppw, w = w0 + jw, p = f - jw * g.ppw;
+                const int wstart = w * wl, wlen = min(wl, T - wstart), off = p * g.piece_rows;
+                if (off >= wlen) continue;
+                const int len = min(g.piece_rows, wlen - off);
+                float c[16];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    c[j] = cmean[jw * kHeadDim + q * 8 + j];
+                    c[8 + j] = cmean[jw * kHeadDim + 64 + q * 8 + j];
+                }
+                const float nc = MODE == MKV_MODE_COSINE ? centroid_norm(c) : 0.f;
+                const uint8_t *base = P.K + ((size_t)head * g.t_max + wstart + off) * kRowBytes;
+                float *srow = P.S + (size_t)head * g.t_max + wstart + off;
                 const int nrows = (len + kRowSlots - 1) / kRowSlots;
                 for (int i0 = 0; i0 < nrows; i0 += kBatchG) {
                     uint4 v[2 * kBatchG];
@@ -948,17 +969,16 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize)
 #pragma unroll
                     for (int u = 0; u < kBatchG; ++u) {
                         const int r = slot + (i0 + u) * kRowSlots;
-                        float f[16];
-                        bf16x8_to_f32(v[2 * u], f);
-                        bf16x8_to_f32(v[2 * u + 1], f + 8);
-                        const float sc = score_of<MODE>(f, c, nc);
+                        float f16[16];
+                        bf16x8_to_f32(v[2 * u], f16);
+                        bf16x8_to_f32(v[2 * u + 1], f16 + 8);
+                        const float sc = score_of<MODE>(f16, c, nc);
                         if (r < len && q == 0) srow[r] = sc;
                     }
                 }
             }
-            if (rank == 0 && threadIdx.x < kHeadDim) P.C[head * kHeadDim + threadIdx.x] = cmean[threadIdx.x];
         }
-        __syncthreads();  // cmean is rewritten for the next head
+        __syncthreads();  // the means are rewritten for the next unit
     }
 }
 
@@ -1014,14 +1034,17 @@ cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, 
     return cudaLaunchCooperativeKernel(fn, dim3((unsigned)grid), dim3(kFusedThreads), args, sizeof(FusedShared), st);
 }
 
-// Dynamic shared memory of k_head_groups: red and the mean, padded so that
-// at most two CTAs share an SM (the grid is then spread over all SMs).
+// Dynamic shared memory of k_head_groups: red and the unit's means, padded
+// so that at most two CTAs share an SM (the grid is then spread over all
+// SMs); a unit holds at most kMaxUnitWindows windows.
 constexpr size_t kGroupSmem = 80 * 1024;
+constexpr int kMaxUnitWindows = 64;
+static_assert((kWarps + kMaxUnitWindows) * kHeadDim * sizeof(float) <= kGroupSmem, "means must fit");
 
 HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
 {
     HeadGroupPlan plan;
-    if (g.nwin_max != 1 || g.n_heads == 0 || g.t_max == 0) return plan;  // global centroids only
+    if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max == 0) return plan;
     const void *fn = mode == MKV_MODE_L2 ? reinterpret_cast<const void *>(k_head_groups<MKV_MODE_L2>)
                                          : reinterpret_cast<const void *>(k_head_groups<MKV_MODE_COSINE>);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
@@ -1031,26 +1054,33 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
     if (resident < 16 || cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0)
         return plan;
-    // Heads in flight (one per group) must fit in 60% of L2. Among group
-    // sizes of 8..64 CTAs, take the one with the least modelled time:
-    // rounds (heads per group) x (the busiest CTA's pieces + 2 for the
-    // barrier, the mean and the L2 pass), with the groups filling at least
-    // 3/4 of the resident grid (else the three-kernel path keeps more SMs
-    // busy).
-    const double head_bytes = (double)g.t_max * kRowBytes;
-    const int64_t fit = (int64_t)(0.6 * (double)l2 / head_bytes);
+    // Units (blocks of wb windows) in flight, one per group, must fit in 60%
+    // of L2. Among group sizes of 8..64 CTAs and unit sizes of 1..kMaxUnit
+    // windows, take the least modelled time: rounds (units per group) x (the
+    // busiest CTA's pieces + 2 for the barrier, the means and the L2 pass),
+    // with the groups filling at least 3/4 of the resident grid (else the
+    // three-kernel path keeps more SMs busy).
+    const int wl_max = (g.window <= 0 || g.window >= g.t_max) ? g.t_max : g.window;
+    if (wl_max < kMinPieceRows) return plan;  // windows shorter than a piece: barrier-bound rounds
+    const double window_bytes = (double)wl_max * kRowBytes;
+    const double budget = 0.6 * (double)l2;
     double best = 0.0;
-    for (int gsize = 8; gsize <= 64; ++gsize) {
-        const int64_t groups = std::min<int64_t>(std::min<int64_t>(fit, resident / gsize), g.n_heads);
-        if (groups < 1 || 4 * groups * gsize < 3 * (int64_t)resident) continue;
-        if ((size_t)groups * sizeof(uint32_t) > counters) continue;
-        const int64_t rounds = (g.n_heads + groups - 1) / groups;
-        const int ppc = (g.ppw + gsize - 1) / gsize;
-        const double cost = (double)rounds * (ppc + 2);
-        if (plan.groups == 0 || cost < best) {
-            best = cost;
-            plan.groups = (int)groups;
-            plan.gsize = gsize;
+    for (int wb = 1; wb <= std::min(g.nwin_max, kMaxUnitWindows); ++wb) {
+        const int64_t fit = (int64_t)(budget / (window_bytes * wb));
+        const int64_t units = g.n_heads * ((g.nwin_max + wb - 1) / wb);
+        for (int gsize = 8; gsize <= 64; ++gsize) {
+            const int64_t groups = std::min<int64_t>(std::min<int64_t>(fit, resident / gsize), units);
+            if (groups < 1 || 4 * groups * gsize < 3 * (int64_t)resident) continue;
+            if ((size_t)groups * sizeof(uint32_t) > counters) continue;
+            const int64_t rounds = (units + groups - 1) / groups;
+            const int ppc = (wb * g.ppw + gsize - 1) / gsize;
+            const double cost = (double)rounds * (ppc + 2);
+            if (plan.groups == 0 || cost < best) {
+                best = cost;
+                plan.groups = (int)groups;
+                plan.gsize = gsize;
+                plan.wb = wb;
+            }
         }
     }
     return plan;
@@ -1064,8 +1094,8 @@ cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan
     if (e != cudaSuccess) return e;
     Pointers P = make_pointers(K, seq_lens, partial, C, S, status);
     PieceGeometry gg = g;
-    int gsize = plan.gsize;
-    void *args[] = {&gg, &P, &cnt, &gsize};
+    int gsize = plan.gsize, wb = plan.wb;
+    void *args[] = {&gg, &P, &cnt, &gsize, &wb};
     const void *fn = mode == MKV_MODE_L2 ? reinterpret_cast<const void *>(k_head_groups<MKV_MODE_L2>)
                                          : reinterpret_cast<const void *>(k_head_groups<MKV_MODE_COSINE>);
     return cudaLaunchCooperativeKernel(fn, dim3((unsigned)(plan.groups * plan.gsize)), dim3(kThreads), args,

@@ -524,8 +524,10 @@ def test_head_groups_are_used_only_where_they_fit():
     bench = mkv.MkvShape(32, 8, 16384, 128, None)
     assert mkv.mkv_compress_single_pass(bench, 0, "l2") == 2
     assert mkv.mkv_compress_single_pass(bench, 0, "cosine") == 2
-    assert mkv.mkv_compress_single_pass(bench, 4096, "l2") == 0        # windows: three kernels
+    assert mkv.mkv_compress_single_pass(bench, 4096, "l2") == 2        # windows: blocks of windows per group
     assert mkv.mkv_compress_single_pass(mkv.MkvShape(40, 10, 131072, 128, None), 0, "l2") == 0  # 32 MB heads
+    assert mkv.mkv_compress_single_pass(mkv.MkvShape(40, 10, 131072, 128, None), 8192, "l2") == 2  # 2 MB windows
+    assert mkv.mkv_compress_single_pass(bench, 100, "l2") == 0         # windows shorter than a piece
     prev = mkv.mkv_set_head_groups(False)
     try:
         assert mkv.mkv_compress_single_pass(bench, 0, "l2") == 0
@@ -533,29 +535,34 @@ def test_head_groups_are_used_only_where_they_fit():
         mkv.mkv_set_head_groups(prev)
 
 
-def _paths_agree(K, V, lens, mode, ratio):
+def _paths_agree(K, V, lens, mode, ratio, window=0):
     """mkv_centroid_score and mkv_compress with and without head groups: the
     same bits."""
     B, H, T, D = K.shape
+    nw = mkv.mkv_num_windows(T, window)
     out = []
     for enable in (True, False):
         prev = mkv.mkv_set_head_groups(enable)
         try:
-            used = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), 0, mode)
-            ws = mkv.workspace_for(K, 0, lens)
-            C = torch.full((B, H, 1, D), float("nan"), device=DEV)
+            used = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
+            ws = mkv.workspace_for(K, window, lens)
+            C = torch.full((B, H, nw, D), float("nan"), device=DEV)
             S = torch.full((B, H, T), float("nan"), device=DEV)
-            mkv.mkv_centroid_score(K, 0, mode, C, S, ws, lens)
+            mkv.mkv_centroid_score(K, window, mode, C, S, ws, lens)
             assert mkv.mkv_device_status(ws) == 0
-            out.append((used, C, S, _run_fused(K, V, ratio, mode, 0, lens)))
+            out.append((used, C, S, _run_fused(K, V, ratio, mode, window, lens)))
         finally:
             mkv.mkv_set_head_groups(prev)
     (u1, C1, S1, f1), (u0, C0, S0, f0) = out
     assert u1 == 2 and u0 == 0
     live = torch.arange(T, device=DEV)[None, None, :] < lens[:, None, None]
-    has = (lens > 0)[:, None, None, None].expand_as(C1)
     assert torch.equal(S1[live.expand_as(S1)], S0[live.expand_as(S0)])
-    assert torch.equal(C1[has], C0[has])
+    # the windows each head has (a window past a short head is not written)
+    wl = torch.where(torch.tensor(window, device=DEV) > 0,
+                     torch.clamp(lens, max=max(window, 1)), lens).clamp(min=1)
+    have = torch.where(lens > 0, (lens + wl - 1) // wl, torch.zeros_like(lens))
+    hw = (torch.arange(nw, device=DEV)[None, :] < have[:, None])[:, None, :, None].expand_as(C1)
+    assert torch.equal(C1[hw], C0[hw])
     assert f1[4] == 0 and f0[4] == 0
     for x, y in zip(f1[:4], f0[:4]):
         assert torch.equal(x, y)
@@ -568,6 +575,16 @@ def test_head_group_and_three_kernel_paths_give_the_same_bits(mode):
                                                                  t_min=1)
     K, V, lens = synthkv.make_kv(w, seed=21, device=DEV)
     _paths_agree(K, V, lens, mode, 0.4)
+
+
+@pytest.mark.parametrize("mode,window", [("l2", 4096), ("cosine", 3000), ("l2", 700), ("l2", 256)])
+def test_head_groups_on_windowed_caches_give_the_same_bits(mode, window):
+    # ragged lengths 1..20000 with windows of 1..4096 tokens (blocks of
+    # windows per group round)
+    w = synthkv.WORKLOADS["ragged-b8-llama-kv-t8k-32k"].scaled("hgw", layers=2, batch=3, heads=4, t_max=20000,
+                                                                 t_min=1)
+    K, V, lens = synthkv.make_kv(w, seed=24, device=DEV)
+    _paths_agree(K, V, lens, mode, 0.3, window)
 
 
 def test_head_groups_with_few_short_heads_and_the_bench_shape():
