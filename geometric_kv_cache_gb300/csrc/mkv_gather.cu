@@ -17,34 +17,38 @@ namespace mkv {
 namespace {
 
 constexpr int kStreamThreads = 256;
-constexpr int kSlots = kStreamThreads / 16;    // rows per CTA per load step
 using namespace dev;
 
-// Item = (head, block of 64 output slots). Half-warps copy rows, 16 bytes per
-// lane: K_out[h][j] = K[h][idx[h][j]], V_out likewise, for j < kept[h]; four
-// rows of K and of V in flight per lane. No CTA barrier anywhere.
+// Item = (head, block of 64 output slots). Groups of LPR lanes (LPR = d / 8:
+// 16 bytes per lane) copy rows: K_out[h][j] = K[h][idx[h][j]], V_out
+// likewise, for j < kept[h]; 64 / (256 / LPR) rows of K and of V in flight
+// per lane. No CTA barrier anywhere.
 constexpr int kGatherRows = 64;
 
+template <int LPR>
 __global__ void __launch_bounds__(kStreamThreads)
 k_gather_rows(const int32_t *__restrict__ idx, int idx_stride, const int32_t *__restrict__ kept, int t_max,
               int keep_stride, int blocks_per_head, int64_t n_items, const uint8_t *__restrict__ K,
               const uint8_t *__restrict__ V, uint8_t *__restrict__ K_out, uint8_t *__restrict__ V_out,
               uint32_t *status)
 {
-    const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+    constexpr int RB = LPR * 16;                 // row bytes
+    constexpr int SLOTS = kStreamThreads / LPR;  // rows per CTA per load step
+    constexpr int R = kGatherRows / SLOTS;       // rows per lane group
+    const int hw = threadIdx.x / LPR, lr = threadIdx.x % LPR;
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int64_t head = item / blocks_per_head;
         const int j0 = (int)(item - head * blocks_per_head) * kGatherRows;
         const int n = min(kGatherRows, min(kept[head], keep_stride) - j0);
         if (n <= 0) continue;
         const int32_t *ih = idx + head * idx_stride + j0;
-        const size_t in_head = (size_t)head * t_max * kRowBytes + l16 * 16;
-        const size_t out_head = ((size_t)head * keep_stride + j0) * kRowBytes + l16 * 16;
-        uint4 kv[kGatherRows / kSlots], vv[kGatherRows / kSlots];
-        int src[kGatherRows / kSlots];
+        const size_t in_head = (size_t)head * t_max * RB + lr * 16;
+        const size_t out_head = ((size_t)head * keep_stride + j0) * RB + lr * 16;
+        uint4 kv[R], vv[R];
+        int src[R];
 #pragma unroll
-        for (int u = 0; u < kGatherRows / kSlots; ++u) {
-            const int j = u * kSlots + hw;
+        for (int u = 0; u < R; ++u) {
+            const int j = u * SLOTS + hw;
             src[u] = j < n ? ih[j] : -1;
             if (src[u] >= t_max) {
                 atomicOr(status, MKV_DEV_INTERNAL);
@@ -52,21 +56,31 @@ k_gather_rows(const int32_t *__restrict__ idx, int idx_stride, const int32_t *__
             }
         }
 #pragma unroll
-        for (int u = 0; u < kGatherRows / kSlots; ++u) {
+        for (int u = 0; u < R; ++u) {
             if (src[u] >= 0) {
-                const size_t off = in_head + (size_t)src[u] * kRowBytes;
+                const size_t off = in_head + (size_t)src[u] * RB;
                 kv[u] = ld_stream(K + off);
                 vv[u] = ld_stream(V + off);
             }
         }
 #pragma unroll
-        for (int u = 0; u < kGatherRows / kSlots; ++u) {
+        for (int u = 0; u < R; ++u) {
             if (src[u] >= 0) {
-                const size_t off = out_head + (size_t)(u * kSlots + hw) * kRowBytes;
+                const size_t off = out_head + (size_t)(u * SLOTS + hw) * RB;
                 st_stream(K_out + off, kv[u]);
                 st_stream(V_out + off, vv[u]);
             }
         }
+    }
+}
+
+const void *gather_fn(int d)
+{
+    switch (d) {
+    case 64: return (const void *)k_gather_rows<8>;
+    case 128: return (const void *)k_gather_rows<16>;
+    case 256: return (const void *)k_gather_rows<32>;
+    default: return nullptr;
     }
 }
 
@@ -79,12 +93,16 @@ cudaError_t launch_gather(const Geometry &g, const int32_t *idx, int32_t idx_str
     const int bph = (keep_stride + kGatherRows - 1) / kGatherRows;
     const int64_t items = g.n_heads * bph;
     if (items == 0) return cudaSuccess;
-    const int grid = grid_for_items(reinterpret_cast<const void *>(k_gather_rows), kStreamThreads, 0, items);
-    k_gather_rows<<<grid, kStreamThreads, 0, st>>>(idx, idx_stride, kept, g.t_max, keep_stride, bph, items,
-                                                   static_cast<const uint8_t *>(K), static_cast<const uint8_t *>(V),
-                                                   static_cast<uint8_t *>(K_out), static_cast<uint8_t *>(V_out),
-                                                   status);
-    return cudaGetLastError();
+    const void *fn = gather_fn(g.d);
+    if (!fn) return cudaErrorInvalidValue;
+    const int grid = grid_for_items(fn, kStreamThreads, 0, items);
+    int t_max = g.t_max;
+    int64_t n_items = items;
+    int bph_arg = bph;
+    const uint8_t *Kb = static_cast<const uint8_t *>(K), *Vb = static_cast<const uint8_t *>(V);
+    uint8_t *Ko = static_cast<uint8_t *>(K_out), *Vo = static_cast<uint8_t *>(V_out);
+    void *args[] = {&idx, &idx_stride, &kept, &t_max, &keep_stride, &bph_arg, &n_items, &Kb, &Vb, &Ko, &Vo, &status};
+    return cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kStreamThreads), args, 0, st);
 }
 
 }  // namespace mkv

@@ -169,29 +169,35 @@ __device__ __forceinline__ int64_t cursor_item(const Cursor &c, const Steps &st)
 
 // ------------------------------------------------------------ arithmetic --
 
+// Head dims. A row of D = 64 * NB bf16 values is read by the 8 lanes of its
+// row group; lane q owns NB blocks of 8 dims, [64k + 8q, 64k + 8q + 8) for
+// k < NB, the 16 bytes at byte offset 128k + 16q of the row. Its per-thread
+// arrays hold 8 * NB values in that order (block k at [8k, 8k + 8)).
+
 // Combine the per-thread accumulators into the piece sum, written to out[]
-// (128 floats) by threads 0..127. `red` is [kWarps][128] shared scratch; the
+// (D floats) by threads 0..D-1. `red` is [kWarps][D] shared scratch; the
 // caller synchronises before `red` is reused.
-__device__ __forceinline__ void finish_sum(float acc[16], float *red, float *out)
+template <int NB = 2>
+__device__ __forceinline__ void finish_sum(float acc[8 * NB], float *red, float *out)
 {
+    constexpr int D = 64 * NB;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = threadIdx.x & 7;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 8 * NB; ++j) {
         acc[j] += __shfl_xor_sync(kFull, acc[j], 8);
         acc[j] += __shfl_xor_sync(kFull, acc[j], 16);
     }
     if (lane < 8) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            red[warp * kHeadDim + q * 8 + j] = acc[j];
-            red[warp * kHeadDim + 64 + q * 8 + j] = acc[8 + j];
-        }
+        for (int k = 0; k < NB; ++k)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) red[warp * D + 64 * k + q * 8 + j] = acc[8 * k + j];
     }
     __syncthreads();
-    if (threadIdx.x < kHeadDim) {
+    if (threadIdx.x < D) {
         float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += red[w * kHeadDim + threadIdx.x];
+        for (int w = 0; w < kWarps; ++w) s += red[w * D + threadIdx.x];
         out[threadIdx.x] = s;
     }
 }
@@ -199,13 +205,13 @@ __device__ __forceinline__ void finish_sum(float acc[16], float *red, float *out
 // Score of one row from the thread's 16 dims f, centroid dims c and the
 // centroid norm nc (cosine only). Reduces over the row's 8 lanes, so all 32
 // lanes of the warp must call it.
-template <int MODE>
-__device__ __forceinline__ float score_of(const float f[16], const float c[16], float nc)
+template <int MODE, int NB = 2>
+__device__ __forceinline__ float score_of(const float f[8 * NB], const float c[8 * NB], float nc)
 {
     if (MODE == MKV_MODE_L2) {
         float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 8 * NB; ++j) {
             const float d = f[j] - c[j];
             acc = fmaf(d, d, acc);
         }
@@ -216,7 +222,7 @@ __device__ __forceinline__ float score_of(const float f[16], const float c[16], 
     } else {
         float dot = 0.f, kk = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 8 * NB; ++j) {
             dot = fmaf(f[j], c[j], dot);
             kk = fmaf(f[j], f[j], kk);
         }
@@ -232,41 +238,51 @@ __device__ __forceinline__ float score_of(const float f[16], const float c[16], 
 }
 
 // Centroid norm for cosine (all 32 lanes call it).
-__device__ __forceinline__ float centroid_norm(const float c[16])
+template <int NB = 2>
+__device__ __forceinline__ float centroid_norm(const float c[8 * NB])
 {
     float cc = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) cc = fmaf(c[j], c[j], cc);
+    for (int j = 0; j < 8 * NB; ++j) cc = fmaf(c[j], c[j], cc);
     cc += __shfl_xor_sync(kFull, cc, 4);
     cc += __shfl_xor_sync(kFull, cc, 2);
     cc += __shfl_xor_sync(kFull, cc, 1);
     return __fsqrt_rn(cc);
 }
 
-// The thread's 16 centroid dims from cw (L2 reads: another CTA may have
+// The thread's 8 * NB centroid dims from cw (L2 reads: another CTA may have
 // written them during this kernel).
-__device__ __forceinline__ void load_centroid(const float *cw, float c[16])
+template <int NB = 2>
+__device__ __forceinline__ void load_centroid(const float *cw, float c[8 * NB])
 {
     const int q = threadIdx.x & 7;
-    const float4 a = __ldcg(reinterpret_cast<const float4 *>(cw + q * 8));
-    const float4 b = __ldcg(reinterpret_cast<const float4 *>(cw + q * 8 + 4));
-    const float4 d = __ldcg(reinterpret_cast<const float4 *>(cw + 64 + q * 8));
-    const float4 e = __ldcg(reinterpret_cast<const float4 *>(cw + 64 + q * 8 + 4));
-    c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
-    c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
-    c[8] = d.x; c[9] = d.y; c[10] = d.z; c[11] = d.w;
-    c[12] = e.x; c[13] = e.y; c[14] = e.z; c[15] = e.w;
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+        const float4 a = __ldcg(reinterpret_cast<const float4 *>(cw + 64 * k + q * 8));
+        const float4 b = __ldcg(reinterpret_cast<const float4 *>(cw + 64 * k + q * 8 + 4));
+        c[8 * k + 0] = a.x; c[8 * k + 1] = a.y; c[8 * k + 2] = a.z; c[8 * k + 3] = a.w;
+        c[8 * k + 4] = b.x; c[8 * k + 5] = b.y; c[8 * k + 6] = b.z; c[8 * k + 7] = b.w;
+    }
 }
 
-// Sum of n (<= kGroupPieces) consecutive 128-float records, record order,
+// The thread's 8 * NB dims of a row from its NB 16-byte chunks.
+template <int NB = 2>
+__device__ __forceinline__ void row_to_f32(const uint4 *v, float f[8 * NB])
+{
+#pragma unroll
+    for (int k = 0; k < NB; ++k) bf16x8_to_f32(v[k], f + 8 * k);
+}
+
+// Sum of n (<= kGroupPieces) consecutive D-float records, record order,
 // dim d; loads issued in batches of 8 ahead of their adds.
+template <int D = 128>
 __device__ __forceinline__ float ordered_sum(const float *first, int n, int d)
 {
     float s = 0.f;
     for (int j0 = 0; j0 < n; j0 += 8) {
         float v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = j0 + j < n ? __ldcg(first + (int64_t)(j0 + j) * kHeadDim + d) : 0.f;
+        for (int j = 0; j < 8; ++j) v[j] = j0 + j < n ? __ldcg(first + (int64_t)(j0 + j) * D + d) : 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (j0 + j < n) s += v[j];
@@ -285,80 +301,74 @@ struct Pointers {
 
 // ------------------------------------------------------------- kernels --
 
-// Rows r = slot + 32 * (i0 + u), u < kBatch, of a piece starting at `base`
-// (this thread's two 16-byte chunks of each), loaded before use.
-constexpr int kBatch = 4;
-
-template <int N>
-__device__ __forceinline__ void load_rows(const uint8_t *base, int len, int i0, uint4 v[2 * N])
+// Rows r = slot + 32 * (i0 + u), u < N, of a piece starting at `base`
+// (this thread's NB 16-byte chunks of each, chunk k of row u at v[NB u + k]),
+// loaded before use.
+template <int N, int NB = 2>
+__device__ __forceinline__ void load_rows(const uint8_t *base, int len, int i0, uint4 v[NB * N])
 {
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
 #pragma unroll
     for (int u = 0; u < N; ++u) {
         const int r = slot + (i0 + u) * kRowSlots;
-        const uint8_t *row = base + (size_t)(r < len ? r : 0) * kRowBytes;
-        v[2 * u] = ld_stream(row + q * 16);
-        v[2 * u + 1] = ld_stream(row + 128 + q * 16);
+        const uint8_t *row = base + (size_t)(r < len ? r : 0) * (128 * NB);
+#pragma unroll
+        for (int k = 0; k < NB; ++k) v[NB * u + k] = ld_stream(row + 128 * k + q * 16);
     }
 }
 
-__device__ __forceinline__ void load_batch(const uint8_t *base, int len, int i0, uint4 v[2 * kBatch])
-{
-    const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-        const int r = slot + (i0 + u) * kRowSlots;
-        const uint8_t *row = base + (size_t)(r < len ? r : 0) * kRowBytes;
-        v[2 * u] = ld_stream(row + q * 16);
-        v[2 * u + 1] = ld_stream(row + 128 + q * 16);
-    }
-}
+// Rows in flight per lane in the streaming kernels: 8 / NB (the same bytes
+// for every head dim).
+template <int NB>
+__host__ __device__ constexpr int batch_rows() { return 8 / NB; }
 
 // a1, first half: piece sums. The first batch of the next piece is loaded
 // before the current piece's CTA reduction, so the loads stay in flight
 // across piece boundaries.
-__global__ void __launch_bounds__(kThreads, 3)
+template <int NB>
+__global__ void __launch_bounds__(kThreads, NB > 2 ? 2 : 3)
 k_piece_sums(PieceGeometry g, Pointers P)
 {
-    __shared__ float red[kWarps * kHeadDim];
+    constexpr int D = 64 * NB, RB = 2 * D, B = batch_rows<NB>();
+    __shared__ float red[kWarps * D];
     const Steps st = make_steps(g);
     const int slot = threadIdx.x >> 3;
     Cursor cur = first_cursor(g, st, P.seq_lens, P.status);
-    uint4 v[2 * kBatch];
-    if (!cur.done) load_batch(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * kRowBytes, cur.pc.len, 0, v);
+    uint4 v[NB * B];
+    if (!cur.done) load_rows<B, NB>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
     while (!cur.done) {
         const Piece pc = cur.pc;
         const int64_t item = cursor_item(cur, st);
-        const uint8_t *base = P.K + ((size_t)pc.head * g.t_max + pc.a) * kRowBytes;
+        const uint8_t *base = P.K + ((size_t)pc.head * g.t_max + pc.a) * RB;
         const int nrows = (pc.len + kRowSlots - 1) / kRowSlots;  // rows per slot (upper bound)
-        float acc[16];
+        float acc[8 * NB];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-        for (int i0 = 0; i0 < nrows; i0 += kBatch) {
+        for (int j = 0; j < 8 * NB; ++j) acc[j] = 0.f;
+        for (int i0 = 0; i0 < nrows; i0 += B) {
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
+            for (int u = 0; u < B; ++u) {
                 if (slot + (i0 + u) * kRowSlots < pc.len) {
-                    float f[16];
-                    bf16x8_to_f32(v[2 * u], f);
-                    bf16x8_to_f32(v[2 * u + 1], f + 8);
+                    float f[8 * NB];
+                    row_to_f32<NB>(v + NB * u, f);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[j] += f[j];
+                    for (int j = 0; j < 8 * NB; ++j) acc[j] += f[j];
                 }
             }
-            if (i0 + kBatch < nrows) load_batch(base, pc.len, i0 + kBatch, v);
+            if (i0 + B < nrows) load_rows<B, NB>(base, pc.len, i0 + B, v);
         }
         advance(cur, st, g, P.seq_lens, P.status);
-        if (!cur.done) load_batch(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * kRowBytes, cur.pc.len, 0, v);
-        finish_sum(acc, red, P.partial + item * kHeadDim);
+        if (!cur.done) load_rows<B, NB>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
+        finish_sum<NB>(acc, red, P.partial + item * D);
         __syncthreads();  // red is free again
     }
 }
 
-// a1, second half: window means. One 128-thread CTA per (head, window),
+// a1, second half: window means. One D-thread CTA per (head, window),
 // thread d for dim d: the groups of 32 piece sums in piece order, then the
 // groups in group order, divided by the window's token count (the same order
-// as the single-pass kernel).
-__global__ void __launch_bounds__(kHeadDim)
+// as the single-pass and head-group kernels).
+template <int D>
+__global__ void __launch_bounds__(D)
 k_window_means(PieceGeometry g, Pointers P)
 {
     const int64_t win = blockIdx.x;
@@ -372,49 +382,49 @@ k_window_means(PieceGeometry g, Pointers P)
     const int wlen = (int)min((int64_t)wl, (int64_t)T - wstart);
     const int np = (wlen + g.piece_rows - 1) / g.piece_rows;
     const int ng = (np + kGroupPieces - 1) / kGroupPieces;
-    const float *pw = P.partial + win * (int64_t)g.ppw * kHeadDim;
+    const float *pw = P.partial + win * (int64_t)g.ppw * D;
     float tot = 0.f;
     for (int gi = 0; gi < ng; ++gi)
-        tot += ordered_sum(pw + (int64_t)gi * kGroupPieces * kHeadDim, min(kGroupPieces, np - gi * kGroupPieces),
-                           threadIdx.x);
-    P.C[win * kHeadDim + threadIdx.x] = __fdiv_rn(tot, (float)wlen);
+        tot += ordered_sum<D>(pw + (int64_t)gi * kGroupPieces * D, min(kGroupPieces, np - gi * kGroupPieces),
+                              threadIdx.x);
+    P.C[win * D + threadIdx.x] = __fdiv_rn(tot, (float)wlen);
 }
 
 // a2: scores of every piece against its window's mean in C. As in
 // k_piece_sums, the next piece's first batch is loaded as soon as the current
 // piece's last batch is consumed, before the next centroid is read.
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 3)
+template <int MODE, int NB>
+__global__ void __launch_bounds__(kThreads, NB > 2 ? 2 : 3)
 k_piece_scores(PieceGeometry g, Pointers P)
 {
+    constexpr int D = 64 * NB, RB = 2 * D, B = batch_rows<NB>();
     const Steps st = make_steps(g);
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
     Cursor cur = first_cursor(g, st, P.seq_lens, P.status);
-    uint4 v[2 * kBatch];
-    if (!cur.done) load_batch(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * kRowBytes, cur.pc.len, 0, v);
+    uint4 v[NB * B];
+    if (!cur.done) load_rows<B, NB>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
     while (!cur.done) {
         const Piece pc = cur.pc;
-        const uint8_t *base = P.K + ((size_t)pc.head * g.t_max + pc.a) * kRowBytes;
+        const uint8_t *base = P.K + ((size_t)pc.head * g.t_max + pc.a) * RB;
         float *srow = P.S + (size_t)pc.head * g.t_max + pc.a;
-        float c[16];
-        load_centroid(P.C + (pc.head * g.nwin_max + pc.w) * kHeadDim, c);
-        const float nc = MODE == MKV_MODE_COSINE ? centroid_norm(c) : 0.f;
+        float c[8 * NB];
+        load_centroid<NB>(P.C + (pc.head * g.nwin_max + pc.w) * D, c);
+        const float nc = MODE == MKV_MODE_COSINE ? centroid_norm<NB>(c) : 0.f;
         const int nrows = (pc.len + kRowSlots - 1) / kRowSlots;
-        for (int i0 = 0; i0 < nrows; i0 += kBatch) {
+        for (int i0 = 0; i0 < nrows; i0 += B) {
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
+            for (int u = 0; u < B; ++u) {
                 const int r = slot + (i0 + u) * kRowSlots;
-                float f[16];
-                bf16x8_to_f32(v[2 * u], f);
-                bf16x8_to_f32(v[2 * u + 1], f + 8);
-                const float s = score_of<MODE>(f, c, nc);
+                float f[8 * NB];
+                row_to_f32<NB>(v + NB * u, f);
+                const float s = score_of<MODE, NB>(f, c, nc);
                 if (r < pc.len && q == 0) srow[r] = s;
             }
-            if (i0 + kBatch < nrows) load_batch(base, pc.len, i0 + kBatch, v);
+            if (i0 + B < nrows) load_rows<B, NB>(base, pc.len, i0 + B, v);
         }
         // the next piece's first batch goes out before its centroid is read
         advance(cur, st, g, P.seq_lens, P.status);
-        if (!cur.done) load_batch(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * kRowBytes, cur.pc.len, 0, v);
+        if (!cur.done) load_rows<B, NB>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
     }
 }
 
@@ -814,16 +824,16 @@ __device__ __forceinline__ uint4 ld_policy(const void *p, uint64_t pol)
 }
 
 // load_rows with an L2 eviction policy on every load.
-template <int N>
-__device__ __forceinline__ void load_rows_policy(const uint8_t *base, int len, int i0, uint4 v[2 * N], uint64_t pol)
+template <int N, int NB>
+__device__ __forceinline__ void load_rows_policy(const uint8_t *base, int len, int i0, uint4 v[NB * N], uint64_t pol)
 {
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
 #pragma unroll
     for (int u = 0; u < N; ++u) {
         const int r = slot + (i0 + u) * kRowSlots;
-        const uint8_t *row = base + (size_t)(r < len ? r : 0) * kRowBytes;
-        v[2 * u] = ld_policy(row + q * 16, pol);
-        v[2 * u + 1] = ld_policy(row + 128 + q * 16, pol);
+        const uint8_t *row = base + (size_t)(r < len ? r : 0) * (128 * NB);
+#pragma unroll
+        for (int k = 0; k < NB; ++k) v[NB * u + k] = ld_policy(row + 128 * k + q * 16, pol);
     }
 }
 //
@@ -844,15 +854,15 @@ __device__ __forceinline__ void load_rows_policy(const uint8_t *base, int len, i
 // (measured: 0.30 ms against 0.33 ms for the three kernels on 256 heads of
 // 16K tokens; without the policies pass 2 missed L2 on about a third of its
 // rows). Same bits as the three-kernel path.
-constexpr int kBatchG = 8;  // rows per lane in flight
-
-template <int MODE>
+template <int MODE, int NB>
 __global__ void __launch_bounds__(kThreads, 2)
 k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
 {
-    extern __shared__ float dyn[];  // red [kWarps][128], means [wb][128]; the rest only caps CTAs per SM
+    constexpr int D = 64 * NB, RB = 2 * D;
+    constexpr int kBatchG = 16 / NB;  // rows per lane in flight (256 bytes per lane for every head dim)
+    extern __shared__ float dyn[];    // red [kWarps][D], means [wb][D]; the rest only caps CTAs per SM
     float *red = dyn;
-    float *cmean = dyn + kWarps * kHeadDim;
+    float *cmean = dyn + kWarps * D;
     __shared__ uint32_t s_ok;
     const int groups = gridDim.x / gsize;
     const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
@@ -878,27 +888,26 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
             const int wstart = w * wl, wlen = min(wl, T - wstart), off = p * g.piece_rows;
             if (off >= wlen) continue;  // past the window's last piece (the same for every thread)
             const int len = min(g.piece_rows, wlen - off);
-            const uint8_t *base = P.K + ((size_t)head * g.t_max + wstart + off) * kRowBytes;
+            const uint8_t *base = P.K + ((size_t)head * g.t_max + wstart + off) * RB;
             const int nrows = (len + kRowSlots - 1) / kRowSlots;
-            float acc[16];
+            float acc[8 * NB];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+            for (int j = 0; j < 8 * NB; ++j) acc[j] = 0.f;
             for (int i0 = 0; i0 < nrows; i0 += kBatchG) {
-                uint4 v[2 * kBatchG];
-                load_rows_policy<kBatchG>(base, len, i0, v, keep_l2);
+                uint4 v[NB * kBatchG];
+                load_rows_policy<kBatchG, NB>(base, len, i0, v, keep_l2);
 #pragma unroll
                 for (int u = 0; u < kBatchG; ++u) {
                     if (slot + (i0 + u) * kRowSlots < len) {
-                        float f16[16];
-                        bf16x8_to_f32(v[2 * u], f16);
-                        bf16x8_to_f32(v[2 * u + 1], f16 + 8);
+                        float fr[8 * NB];
+                        row_to_f32<NB>(v + NB * u, fr);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[j] += f16[j];
+                        for (int j = 0; j < 8 * NB; ++j) acc[j] += fr[j];
                     }
                 }
             }
-            finish_sum(acc, red, P.partial + ((head * g.nwin_max + w) * (int64_t)g.ppw + p) * kHeadDim);
-            if (threadIdx.x < kHeadDim) __threadfence();  // the piece sum is visible GPU-wide before the arrival
+            finish_sum<NB>(acc, red, P.partial + ((head * g.nwin_max + w) * (int64_t)g.ppw + p) * D);
+            if (threadIdx.x < D) __threadfence();  // the piece sum is visible GPU-wide before the arrival
             __syncthreads();  // red is free again
         }
         // the group's barrier for this unit
@@ -921,21 +930,21 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
         if (s_ok && nwu > 0) {  // the same for every thread
             // window means in k_window_means' order (pieces of a group of 32
             // in order, then the groups), a group's loads in flight at once;
-            // threads t and t + 128 take alternate windows
-            for (int j = threadIdx.x >> 7; j < nwu; j += kThreads / kHeadDim) {
-                const int d = threadIdx.x & (kHeadDim - 1);
+            // threads t, t + D, ... take successive windows
+            for (int j = threadIdx.x / D; j < nwu; j += kThreads / D) {
+                const int d = threadIdx.x % D;
                 const int w = w0 + j;
                 const int wlen = min(wl, T - w * wl);
                 const int np = (wlen + g.piece_rows - 1) / g.piece_rows;
                 const int ng = (np + kGroupPieces - 1) / kGroupPieces;
-                const float *pw = P.partial + (head * g.nwin_max + w) * (int64_t)g.ppw * kHeadDim + d;
+                const float *pw = P.partial + (head * g.nwin_max + w) * (int64_t)g.ppw * D + d;
                 float tot = 0.f;
                 for (int gi = 0; gi < ng; ++gi) {
                     const int n = min(kGroupPieces, np - gi * kGroupPieces);
                     float v[kGroupPieces];
 #pragma unroll
                     for (int k = 0; k < kGroupPieces; ++k)
-                        v[k] = k < n ? __ldcg(pw + (int64_t)(gi * kGroupPieces + k) * kHeadDim) : 0.f;
+                        v[k] = k < n ? __ldcg(pw + (int64_t)(gi * kGroupPieces + k) * D) : 0.f;
                     float gs = 0.f;
 #pragma unroll
                     for (int k = 0; k < kGroupPieces; ++k)
@@ -943,8 +952,8 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
                     tot += gs;
                 }
                 const float m = __fdiv_rn(tot, (float)wlen);
-                cmean[j * kHeadDim + d] = m;
-                if (rank == 0) P.C[(head * g.nwin_max + w) * kHeadDim + d] = m;
+                cmean[j * D + d] = m;
+                if (rank == 0) P.C[(head * g.nwin_max + w) * D + d] = m;
             }
             __syncthreads();
             // pass 2: scores of the same pieces (their rows are L2 hits)
@@ -953,26 +962,24 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
                 const int wstart = w * wl, wlen = min(wl, T - wstart), off = p * g.piece_rows;
                 if (off >= wlen) continue;
                 const int len = min(g.piece_rows, wlen - off);
-                float c[16];
+                float c[8 * NB];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    c[j] = cmean[jw * kHeadDim + q * 8 + j];
-                    c[8 + j] = cmean[jw * kHeadDim + 64 + q * 8 + j];
-                }
-                const float nc = MODE == MKV_MODE_COSINE ? centroid_norm(c) : 0.f;
-                const uint8_t *base = P.K + ((size_t)head * g.t_max + wstart + off) * kRowBytes;
+                for (int k = 0; k < NB; ++k)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) c[8 * k + j] = cmean[jw * D + 64 * k + q * 8 + j];
+                const float nc = MODE == MKV_MODE_COSINE ? centroid_norm<NB>(c) : 0.f;
+                const uint8_t *base = P.K + ((size_t)head * g.t_max + wstart + off) * RB;
                 float *srow = P.S + (size_t)head * g.t_max + wstart + off;
                 const int nrows = (len + kRowSlots - 1) / kRowSlots;
                 for (int i0 = 0; i0 < nrows; i0 += kBatchG) {
-                    uint4 v[2 * kBatchG];
-                    load_rows_policy<kBatchG>(base, len, i0, v, drop_l2);
+                    uint4 v[NB * kBatchG];
+                    load_rows_policy<kBatchG, NB>(base, len, i0, v, drop_l2);
 #pragma unroll
                     for (int u = 0; u < kBatchG; ++u) {
                         const int r = slot + (i0 + u) * kRowSlots;
-                        float f16[16];
-                        bf16x8_to_f32(v[2 * u], f16);
-                        bf16x8_to_f32(v[2 * u + 1], f16 + 8);
-                        const float sc = score_of<MODE>(f16, c, nc);
+                        float fr[8 * NB];
+                        row_to_f32<NB>(v + NB * u, fr);
+                        const float sc = score_of<MODE, NB>(fr, c, nc);
                         if (r < len && q == 0) srow[r] = sc;
                     }
                 }
@@ -1034,20 +1041,67 @@ cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, 
     return cudaLaunchCooperativeKernel(fn, dim3((unsigned)grid), dim3(kFusedThreads), args, sizeof(FusedShared), st);
 }
 
+namespace {
+
 // Dynamic shared memory of k_head_groups: red and the unit's means, padded
 // so that at most two CTAs share an SM (the grid is then spread over all
 // SMs); a unit holds at most kMaxUnitWindows windows.
 constexpr size_t kGroupSmem = 80 * 1024;
 constexpr int kMaxUnitWindows = 64;
-static_assert((kWarps + kMaxUnitWindows) * kHeadDim * sizeof(float) <= kGroupSmem, "means must fit");
+constexpr int kMaxDim = 256;
+static_assert((kWarps + kMaxUnitWindows) * kMaxDim * sizeof(float) <= kGroupSmem, "means must fit");
+
+// The kernel instance for a head dim (64 * NB) and mode.
+const void *head_groups_fn(int d, int mode)
+{
+    const bool l2 = mode == MKV_MODE_L2;
+    switch (d) {
+    case 64: return l2 ? (const void *)k_head_groups<MKV_MODE_L2, 1> : (const void *)k_head_groups<MKV_MODE_COSINE, 1>;
+    case 128: return l2 ? (const void *)k_head_groups<MKV_MODE_L2, 2> : (const void *)k_head_groups<MKV_MODE_COSINE, 2>;
+    case 256: return l2 ? (const void *)k_head_groups<MKV_MODE_L2, 4> : (const void *)k_head_groups<MKV_MODE_COSINE, 4>;
+    default: return nullptr;
+    }
+}
+
+const void *piece_scores_fn(int d, int mode)
+{
+    const bool l2 = mode == MKV_MODE_L2;
+    switch (d) {
+    case 64: return l2 ? (const void *)k_piece_scores<MKV_MODE_L2, 1> : (const void *)k_piece_scores<MKV_MODE_COSINE, 1>;
+    case 128: return l2 ? (const void *)k_piece_scores<MKV_MODE_L2, 2> : (const void *)k_piece_scores<MKV_MODE_COSINE, 2>;
+    case 256: return l2 ? (const void *)k_piece_scores<MKV_MODE_L2, 4> : (const void *)k_piece_scores<MKV_MODE_COSINE, 4>;
+    default: return nullptr;
+    }
+}
+
+const void *piece_sums_fn(int d)
+{
+    switch (d) {
+    case 64: return (const void *)k_piece_sums<1>;
+    case 128: return (const void *)k_piece_sums<2>;
+    case 256: return (const void *)k_piece_sums<4>;
+    default: return nullptr;
+    }
+}
+
+const void *window_means_fn(int d)
+{
+    switch (d) {
+    case 64: return (const void *)k_window_means<64>;
+    case 128: return (const void *)k_window_means<128>;
+    case 256: return (const void *)k_window_means<256>;
+    default: return nullptr;
+    }
+}
+
+}  // namespace
 
 HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
 {
     HeadGroupPlan plan;
     if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max == 0) return plan;
-    const void *fn = mode == MKV_MODE_L2 ? reinterpret_cast<const void *>(k_head_groups<MKV_MODE_L2>)
-                                         : reinterpret_cast<const void *>(k_head_groups<MKV_MODE_COSINE>);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
+    const void *fn = head_groups_fn(g.d, mode);
+    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
         return plan;
     const int resident = resident_grid(fn, kThreads, kGroupSmem);
     int dev = 0, l2 = 0;
@@ -1062,7 +1116,7 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
     // three-kernel path keeps more SMs busy).
     const int wl_max = (g.window <= 0 || g.window >= g.t_max) ? g.t_max : g.window;
     if (wl_max < kMinPieceRows) return plan;  // windows shorter than a piece: barrier-bound rounds
-    const double window_bytes = (double)wl_max * kRowBytes;
+    const double window_bytes = (double)wl_max * 2.0 * g.d;
     const double budget = 0.6 * (double)l2;
     double best = 0.0;
     for (int wb = 1; wb <= std::min(g.nwin_max, kMaxUnitWindows); ++wb) {
@@ -1090,14 +1144,14 @@ cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan
                                const int32_t *seq_lens, int mode, float *partial, uint32_t *cnt, float *C, float *S,
                                uint32_t *status, cudaStream_t st)
 {
+    const void *fn = head_groups_fn(g.d, mode);
+    if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(cnt, 0, (size_t)plan.groups * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
     Pointers P = make_pointers(K, seq_lens, partial, C, S, status);
     PieceGeometry gg = g;
     int gsize = plan.gsize, wb = plan.wb;
     void *args[] = {&gg, &P, &cnt, &gsize, &wb};
-    const void *fn = mode == MKV_MODE_L2 ? reinterpret_cast<const void *>(k_head_groups<MKV_MODE_L2>)
-                                         : reinterpret_cast<const void *>(k_head_groups<MKV_MODE_COSINE>);
     return cudaLaunchCooperativeKernel(fn, dim3((unsigned)(plan.groups * plan.gsize)), dim3(kThreads), args,
                                        kGroupSmem, st);
 }
@@ -1106,9 +1160,13 @@ cudaError_t launch_piece_sums(const PieceGeometry &g, const void *K, const int32
                               uint32_t *status, cudaStream_t st)
 {
     if (g.n_items == 0) return cudaSuccess;
-    const int grid = grid_for_items(reinterpret_cast<const void *>(k_piece_sums), kThreads, 0, g.n_items);
-    k_piece_sums<<<grid, kThreads, 0, st>>>(g, make_pointers(K, seq_lens, partial, nullptr, nullptr, status));
-    return cudaGetLastError();
+    const void *fn = piece_sums_fn(g.d);
+    if (!fn) return cudaErrorInvalidValue;
+    const int grid = grid_for_items(fn, kThreads, 0, g.n_items);
+    PieceGeometry gg = g;
+    Pointers P = make_pointers(K, seq_lens, partial, nullptr, nullptr, status);
+    void *args[] = {&gg, &P};
+    return cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kThreads), args, 0, st);
 }
 
 cudaError_t launch_window_means(const PieceGeometry &g, const float *partial, const int32_t *seq_lens, float *C,
@@ -1116,26 +1174,25 @@ cudaError_t launch_window_means(const PieceGeometry &g, const float *partial, co
 {
     const int64_t wins = g.n_heads * g.nwin_max;
     if (wins == 0) return cudaSuccess;
-    k_window_means<<<(unsigned)wins, kHeadDim, 0, st>>>(
-        g, make_pointers(nullptr, seq_lens, const_cast<float *>(partial), C, nullptr, status));
-    return cudaGetLastError();
+    const void *fn = window_means_fn(g.d);
+    if (!fn) return cudaErrorInvalidValue;
+    PieceGeometry gg = g;
+    Pointers P = make_pointers(nullptr, seq_lens, const_cast<float *>(partial), C, nullptr, status);
+    void *args[] = {&gg, &P};
+    return cudaLaunchKernel(fn, dim3((unsigned)wins), dim3((unsigned)g.d), args, 0, st);
 }
 
 cudaError_t launch_piece_scores(const PieceGeometry &g, const void *K, const float *C, const int32_t *seq_lens,
                                 int mode, float *S, uint32_t *status, cudaStream_t st)
 {
     if (g.n_items == 0) return cudaSuccess;
-    const Pointers P = make_pointers(K, seq_lens, nullptr, const_cast<float *>(C), S, status);
-    if (mode == MKV_MODE_L2) {
-        const int grid = grid_for_items(reinterpret_cast<const void *>(k_piece_scores<MKV_MODE_L2>), kThreads, 0,
-                                        g.n_items);
-        k_piece_scores<MKV_MODE_L2><<<grid, kThreads, 0, st>>>(g, P);
-    } else {
-        const int grid = grid_for_items(reinterpret_cast<const void *>(k_piece_scores<MKV_MODE_COSINE>), kThreads, 0,
-                                        g.n_items);
-        k_piece_scores<MKV_MODE_COSINE><<<grid, kThreads, 0, st>>>(g, P);
-    }
-    return cudaGetLastError();
+    const void *fn = piece_scores_fn(g.d, mode);
+    if (!fn) return cudaErrorInvalidValue;
+    const int grid = grid_for_items(fn, kThreads, 0, g.n_items);
+    PieceGeometry gg = g;
+    Pointers P = make_pointers(K, seq_lens, nullptr, const_cast<float *>(C), S, status);
+    void *args[] = {&gg, &P};
+    return cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kThreads), args, 0, st);
 }
 
 }  // namespace mkv

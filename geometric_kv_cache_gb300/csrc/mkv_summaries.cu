@@ -11,8 +11,8 @@
 // the centroid step (mkv_piece.cu) instead.
 //
 // Layout: one window per 8-lane group. Lane q of a group owns dims
-// [8q, 8q+8) and [64+8q, 64+8q+8) of every row (two 16-byte loads per row,
-// each group reading whole 128-byte lines). Sums run per dim in token order
+// [64k + 8q, 64k + 8q + 8) of every row for k < d/64 (one 16-byte load per
+// 64 dims, each group reading whole 128-byte lines). Sums run per dim in token order
 // in fp32, so no lane talks to another for the mean. The radius pass re-reads
 // the window's rows (from L1/L2), sums its 16 squared offsets per lane, then
 // sums over the group with an xor butterfly (the same bits on every lane).
@@ -30,17 +30,24 @@ constexpr int kWindowsPerCta = kSumThreads / 8;
 constexpr int kBatchRows = 4;  // rows in flight per lane
 using namespace dev;
 
-__device__ __forceinline__ void load_row(const uint8_t *row, uint4 &lo, uint4 &hi)
+// This lane's NB 16-byte chunks of a row (chunk k at byte 128k of the lane's
+// first chunk).
+template <int NB>
+__device__ __forceinline__ void load_row(const uint8_t *row, uint4 (&v)[NB])
 {
-    lo = ld_nc(row);
-    hi = ld_nc(row + 128);
+#pragma unroll
+    for (int k = 0; k < NB; ++k) v[k] = ld_nc(row + 128 * k);
 }
 
+// Lane q of a window's group owns dims [64k + 8q, 64k + 8q + 8), k < NB
+// (head dim 64 NB).
+template <int NB>
 __global__ void __launch_bounds__(kSumThreads)
 k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ seq_lens, int heads, int t_max,
                      int window, int nwin_max, int64_t n_items, float *__restrict__ mean,
                      float *__restrict__ radius, uint32_t *status)
 {
+    constexpr int D = 64 * NB, RB = 2 * D;
     const int grp = threadIdx.x >> 3, q = threadIdx.x & 7;
     for (int64_t base = (int64_t)blockIdx.x * kWindowsPerCta; base < n_items;
          base += (int64_t)gridDim.x * kWindowsPerCta) {
@@ -54,38 +61,39 @@ k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ 
             const int T = head_len(seq_lens, head, heads, t_max, status, q == 0 && j == 0);
             n = min(window, T - j * window);
         }
-        const uint8_t *row0 = X + ((size_t)head * t_max + (size_t)j * window) * kRowBytes + q * 16;
-        float m[16] = {0.f};
+        const uint8_t *row0 = X + ((size_t)head * t_max + (size_t)j * window) * RB + q * 16;
+        float m[8 * NB] = {0.f};
         if (n > 0) {
-            float acc[16];
+            float acc[8 * NB];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+            for (int i = 0; i < 8 * NB; ++i) acc[i] = 0.f;
             for (int t0 = 0; t0 < n; t0 += kBatchRows) {
-                uint4 lo[kBatchRows], hi[kBatchRows];
+                uint4 v[kBatchRows][NB];
 #pragma unroll
                 for (int u = 0; u < kBatchRows; ++u)
-                    if (t0 + u < n) load_row(row0 + (size_t)(t0 + u) * kRowBytes, lo[u], hi[u]);
+                    if (t0 + u < n) load_row<NB>(row0 + (size_t)(t0 + u) * RB, v[u]);
 #pragma unroll
                 for (int u = 0; u < kBatchRows; ++u) {
                     if (t0 + u < n) {
-                        float f[8];
-                        bf16x8_to_f32(lo[u], f);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[i] += f[i];
-                        bf16x8_to_f32(hi[u], f);
+                        for (int k = 0; k < NB; ++k) {
+                            float f[8];
+                            bf16x8_to_f32(v[u][k], f);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[8 + i] += f[i];
+                            for (int i = 0; i < 8; ++i) acc[8 * k + i] += f[i];
+                        }
                     }
                 }
             }
             const float fn = (float)n;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) m[i] = __fdiv_rn(acc[i], fn);
-            float4 *out = reinterpret_cast<float4 *>(mean + ((size_t)head * nwin_max + j) * kHeadDim);
-            out[2 * q] = make_float4(m[0], m[1], m[2], m[3]);
-            out[2 * q + 1] = make_float4(m[4], m[5], m[6], m[7]);
-            out[16 + 2 * q] = make_float4(m[8], m[9], m[10], m[11]);
-            out[16 + 2 * q + 1] = make_float4(m[12], m[13], m[14], m[15]);
+            for (int i = 0; i < 8 * NB; ++i) m[i] = __fdiv_rn(acc[i], fn);
+            float4 *out = reinterpret_cast<float4 *>(mean + ((size_t)head * nwin_max + j) * D);
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                out[16 * k + 2 * q] = make_float4(m[8 * k], m[8 * k + 1], m[8 * k + 2], m[8 * k + 3]);
+                out[16 * k + 2 * q + 1] = make_float4(m[8 * k + 4], m[8 * k + 5], m[8 * k + 6], m[8 * k + 7]);
+            }
         }
         if (radius) {
             // every lane of the warp runs the same rows (the butterfly below
@@ -93,26 +101,23 @@ k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ 
             const int n_warp = __reduce_max_sync(kFull, (unsigned)max(n, 0));
             float rmax = 0.f;
             for (int t0 = 0; t0 < n_warp; t0 += kBatchRows) {
-                uint4 lo[kBatchRows], hi[kBatchRows];
+                uint4 v[kBatchRows][NB];
 #pragma unroll
                 for (int u = 0; u < kBatchRows; ++u)
-                    if (t0 + u < n) load_row(row0 + (size_t)(t0 + u) * kRowBytes, lo[u], hi[u]);
+                    if (t0 + u < n) load_row<NB>(row0 + (size_t)(t0 + u) * RB, v[u]);
 #pragma unroll
                 for (int u = 0; u < kBatchRows; ++u) {
                     float ss = 0.f;
                     if (t0 + u < n) {
-                        float f[8];
-                        bf16x8_to_f32(lo[u], f);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float dlt = f[i] - m[i];
-                            ss = fmaf(dlt, dlt, ss);
-                        }
-                        bf16x8_to_f32(hi[u], f);
+                        for (int k = 0; k < NB; ++k) {
+                            float f[8];
+                            bf16x8_to_f32(v[u][k], f);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float dlt = f[i] - m[8 + i];
-                            ss = fmaf(dlt, dlt, ss);
+                            for (int i = 0; i < 8; ++i) {
+                                const float dlt = f[i] - m[8 * k + i];
+                                ss = fmaf(dlt, dlt, ss);
+                            }
                         }
                     }
                     ss += __shfl_xor_sync(kFull, ss, 1);
@@ -126,6 +131,16 @@ k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ 
     }
 }
 
+const void *small_window_means_fn(int d)
+{
+    switch (d) {
+    case 64: return (const void *)k_small_window_means<1>;
+    case 128: return (const void *)k_small_window_means<2>;
+    case 256: return (const void *)k_small_window_means<4>;
+    default: return nullptr;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_small_window_means(const PieceGeometry &g, const void *X, const int32_t *seq_lens, float *mean,
@@ -133,11 +148,14 @@ cudaError_t launch_small_window_means(const PieceGeometry &g, const void *X, con
 {
     const int64_t items = g.n_heads * g.nwin_max;
     if (items == 0) return cudaSuccess;
-    const int grid = grid_for_items(reinterpret_cast<const void *>(k_small_window_means), kSumThreads, 0,
-                                    (items + kWindowsPerCta - 1) / kWindowsPerCta);
-    k_small_window_means<<<grid, kSumThreads, 0, st>>>(static_cast<const uint8_t *>(X), seq_lens, g.heads, g.t_max,
-                                                       g.window, g.nwin_max, items, mean, radius, status);
-    return cudaGetLastError();
+    const void *fn = small_window_means_fn(g.d);
+    if (!fn) return cudaErrorInvalidValue;
+    const int grid = grid_for_items(fn, kSumThreads, 0, (items + kWindowsPerCta - 1) / kWindowsPerCta);
+    const uint8_t *Xb = static_cast<const uint8_t *>(X);
+    int heads = g.heads, t_max = g.t_max, window = g.window, nwin_max = g.nwin_max;
+    int64_t n_items = items;
+    void *args[] = {&Xb, &seq_lens, &heads, &t_max, &window, &nwin_max, &n_items, &mean, &radius, &status};
+    return cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kSumThreads), args, 0, st);
 }
 
 }  // namespace mkv

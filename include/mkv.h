@@ -14,7 +14,8 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * Cache layout. A cache is bf16 [batch, heads, t_max, head_dim], head_dim
- *   innermost and contiguous (one 256-byte row per token at head_dim 128).
+ *   innermost and contiguous (one 2*head_dim-byte row per token: 128, 256 or
+ *   512 bytes at head_dim 64, 128, 256).
  *   "batch" counts (layer, sequence) rows: callers fold layers into it, so a
  *   "head" is one (layer, sequence, KV head) triple, and every head is
  *   processed independently. Head h = b*heads + j covers tokens
@@ -48,7 +49,8 @@
  *   that shape and window. The status word must be zero before the first
  *   call (allocate the workspace zeroed, or call mkv_device_status once).
  *   Calls that share a workspace must not overlap on the GPU.
- * Supported. head_dim = 128 only (else MKV_ERR_UNSUPPORTED); t_max <= 2^30.
+ * Supported. head_dim 64, 128 or 256 (else MKV_ERR_UNSUPPORTED; the OjaKV
+ *   scorer needs 128); t_max <= 2^30.
  *   Scores must not be NaN (inputs with NaN/Inf are outside the contract).
  */
 #ifndef MKV_H_
@@ -67,7 +69,7 @@ typedef struct CUstream_st *mkv_stream_t;
 typedef enum {
     MKV_OK = 0,
     MKV_ERR_INVALID_ARG = 1, /* null / misaligned pointer, negative size, ratio outside [0,1], ... */
-    MKV_ERR_UNSUPPORTED = 2, /* head_dim other than 128, t_max above 2^30 */
+    MKV_ERR_UNSUPPORTED = 2, /* head_dim other than 64/128/256 (128 for OjaKV), t_max above 2^30 */
     MKV_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than required */
     MKV_ERR_CUDA = 4,        /* a CUDA call or launch failed */
     MKV_ERR_DEVICE = 5       /* mkv_device_status only: the status word is nonzero */

@@ -56,7 +56,7 @@ def test_workspace_size_grows_with_the_problem():
     assert 256 < small < big
     # scores alone need 4 bytes per token
     assert big >= 2 * 8 * 65536 * 4
-    assert mkv.mkv_workspace_size(_shape(head_dim=64)) == 0
+    assert mkv.mkv_workspace_size(_shape(head_dim=96)) == 0
     assert mkv.mkv_workspace_size(_shape(batch=-1)) == 0
 
 
@@ -75,7 +75,7 @@ def _compress(shape, ratio=0.5, mode=0, window=0, keep_stride=512, K=A, V=A, Ko=
 
 
 @pytest.mark.parametrize("kwargs,status", [
-    (dict(shape=_shape(head_dim=64)), mkv.MKV_ERR_UNSUPPORTED),
+    (dict(shape=_shape(head_dim=96)), mkv.MKV_ERR_UNSUPPORTED),
     (dict(shape=_shape(t_max=(1 << 30) + 1)), mkv.MKV_ERR_UNSUPPORTED),
     (dict(shape=_shape(heads=-1)), mkv.MKV_ERR_INVALID_ARG),
     (dict(shape=_shape(), ratio=1.5), mkv.MKV_ERR_INVALID_ARG),
@@ -175,7 +175,7 @@ def test_window_means_and_quota_calls_reject_bad_arguments():
     assert lib.mkv_window_means(vp(A), shp, 10, vp(A + 4), None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
     assert lib.mkv_window_means(vp(A), shp, 10, vp(A), vp(A + 2), vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
     assert lib.mkv_window_means(vp(A), shp, 10, vp(A), None, vp(A), 16, None) == mkv.MKV_ERR_WORKSPACE
-    assert lib.mkv_window_means(vp(A), _shape(head_dim=64), 10, vp(A), None, vp(A), big, None) == \
+    assert lib.mkv_window_means(vp(A), _shape(head_dim=96), 10, vp(A), None, vp(A), big, None) == \
         mkv.MKV_ERR_UNSUPPORTED
     # the quota selection needs room for every window's share
     need = mkv.mkv_num_keep_quota(shp.t_max, 0.5, 3)
@@ -229,7 +229,7 @@ def test_oja_calls_reject_bad_arguments():
     assert score(S=0) == mkv.MKV_ERR_INVALID_ARG
     assert score(ws_bytes=ws_need - 1) == mkv.MKV_ERR_WORKSPACE
     assert score(ws=A + 16) == mkv.MKV_ERR_WORKSPACE
-    assert score(shape=_shape(head_dim=64)) == mkv.MKV_ERR_UNSUPPORTED
+    assert score(shape=_shape(head_dim=96)) == mkv.MKV_ERR_UNSUPPORTED
     # 32-bit TMA row coordinates
     assert score(shape=_shape(batch=1024, heads=64, t_max=32768)) == mkv.MKV_ERR_UNSUPPORTED
     assert lib.mkv_compress_oja(vp(A), None, vp(A), vp(A), shp, 128, 64, 0.5, None, 512, vp(A), vp(A), None, None,
@@ -251,3 +251,19 @@ def test_in_place_compress_rejects_bad_arguments():
     assert f(vp(A), vp(A), shp, 0.5, None, 0, 0, vp(A + 2), None, vp(A), big, None) == mkv.MKV_ERR_INVALID_ARG
     assert f(vp(A), vp(A), shp, 0.5, None, 0, 0, None, None, vp(A), 64, None) == mkv.MKV_ERR_WORKSPACE
     assert f(vp(A), vp(A), _shape(batch=0), 0.5, None, 0, 0, None, None, vp(A), big, None) == mkv.MKV_OK
+
+
+def test_head_dims():
+    # 64, 128 and 256 are supported by the streaming path (workspace grows
+    # with d); other dims are refused; the OjaKV scorer is built for 128
+    sizes = [mkv.mkv_workspace_size(_shape(head_dim=d)) for d in (64, 128, 256)]
+    assert 0 < sizes[0] < sizes[1] < sizes[2]
+    for d in (0, 32, 96, 192, 512):
+        assert mkv.mkv_workspace_size(_shape(head_dim=d)) == 0
+        assert _compress(_shape(head_dim=d)) in (mkv.MKV_ERR_UNSUPPORTED, mkv.MKV_ERR_INVALID_ARG)
+    lib = mkv.load()
+    vp = ctypes.c_void_p
+    assert lib.mkv_oja_score(vp(A), vp(A), vp(A), _shape(head_dim=64), 128, 8, vp(A), vp(A), 1 << 40, None) == \
+        mkv.MKV_ERR_UNSUPPORTED
+    assert _compress(_shape(head_dim=64, batch=0)) == mkv.MKV_OK
+    assert _compress(_shape(head_dim=256, batch=0)) == mkv.MKV_OK
