@@ -326,7 +326,9 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         barrier()
         e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps)
-        h2d = hK.numel() * 2 + hV.numel() * 2
+        # keys cross the link in full; values only for the kept rows (the
+        # gather reads them from the pinned host buffer)
+        h2d = hK.numel() * 2 + nbytes["kept"] * w.head_dim * 2
         d2h = hKo.numel() * 2 + hVo.numel() * 2 + hidx.numel() * 4 + hkept.numel() * 4
         e2e = {"value": tokens_all / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}

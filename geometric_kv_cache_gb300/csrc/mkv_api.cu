@@ -751,6 +751,18 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
     const size_t kept_row = (size_t)shape.heads * sizeof(int32_t);
     auto bytes_at = [](const void *p, size_t off) { return static_cast<const uint8_t *>(p) + off; };
     auto wbytes_at = [](void *p, size_t off) { return static_cast<uint8_t *>(p) + off; };
+    // Values are only read for the kept rows (the gather): when hV is pinned
+    // host memory the device can address, the gather reads those rows
+    // straight from it and only they cross the link; otherwise V is copied.
+    const uint8_t *v_host_dev = nullptr;
+    {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, hV) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
+            attr.devicePointer != nullptr)
+            v_host_dev = static_cast<const uint8_t *>(attr.devicePointer);
+        else
+            (void)cudaGetLastError();
+    }
     // the copies wait for earlier work on the caller's stream (earlier users of the buffers)
     if (cudaEventRecord(cs->start, st) != cudaSuccess || cudaStreamWaitEvent(cs->in[0], cs->start, 0) != cudaSuccess ||
         cudaStreamWaitEvent(cs->in[1], cs->start, 0) != cudaSuccess ||
@@ -760,7 +772,8 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
         const int32_t r0 = c * per, rows = std::min(per, shape.batch - r0);
         const size_t ib = (size_t)rows * in_row, io = (size_t)r0 * in_row;
         if (cudaMemcpyAsync(wbytes_at(dK, io), bytes_at(hK, io), ib, cudaMemcpyHostToDevice, cs->in[0]) != cudaSuccess ||
-            cudaMemcpyAsync(wbytes_at(dV, io), bytes_at(hV, io), ib, cudaMemcpyHostToDevice, cs->in[1]) != cudaSuccess ||
+            (!v_host_dev &&
+             cudaMemcpyAsync(wbytes_at(dV, io), bytes_at(hV, io), ib, cudaMemcpyHostToDevice, cs->in[1]) != cudaSuccess) ||
             cudaEventRecord(cs->in_done[0][c], cs->in[0]) != cudaSuccess ||
             cudaEventRecord(cs->in_done[1][c], cs->in[1]) != cudaSuccess ||
             cudaStreamWaitEvent(st, cs->in_done[0][c], 0) != cudaSuccess ||
@@ -772,7 +785,8 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
         const size_t oo = (size_t)r0 * out_row;
         int32_t *ci = reinterpret_cast<int32_t *>(wbytes_at(d_idx, (size_t)r0 * idx_row));
         int32_t *ck = reinterpret_cast<int32_t *>(wbytes_at(d_kept, (size_t)r0 * kept_row));
-        rc = run_compress(bytes_at(dK, io), bytes_at(dV, io), sub, ratio, nullptr, mode, window, keep_stride,
+        const void *vsrc = v_host_dev ? static_cast<const void *>(v_host_dev + io) : bytes_at(dV, io);
+        rc = run_compress(bytes_at(dK, io), vsrc, sub, ratio, nullptr, mode, window, keep_stride,
                           wbytes_at(dK_out, oo), wbytes_at(dV_out, oo), ci, ck, workspace, workspace_bytes, st, nullptr);
         if (rc != MKV_OK) return rc;
         if (cudaEventRecord(cs->comp_done[c], st) != cudaSuccess || cudaStreamWaitEvent(cs->out, cs->comp_done[c], 0) != cudaSuccess)

@@ -327,7 +327,10 @@ mkv_status mkv_compress_profiled(const void *K, const void *V, mkv_shape shape, 
  * copies run on two library-owned copy-in streams (keys on one, values on
  * the other), its kernels on `stream`, its device-to-host copies on a
  * copy-out stream, so copies of different chunks overlap each other and the
- * kernels. The copy streams first wait for
+ * kernels. Values are read only for the kept rows: when hV is pinned host
+ * memory the device can address (cudaHostAlloc / cudaHostRegister), the
+ * gather reads the kept value rows straight from it and dV is not used, so
+ * only those rows cross the host link. The copy streams first wait for
  * the work already on `stream`, and `stream` waits for every copy before
  * anything enqueued after this call, so the call behaves as if it were all on
  * `stream`. The three streams and their events are created on a device's first

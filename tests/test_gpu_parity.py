@@ -360,6 +360,37 @@ def test_host_path_chunks_overlap_and_join_the_callers_stream():
         assert torch.equal(torch.where(live[..., None], hVo, 0), torch.where(live[..., None], Vo.cpu(), 0))
 
 
+def test_host_path_with_pageable_values_copies_them():
+    # a pageable hV is not addressable by the device: the values are copied
+    # (the pinned case reads the kept rows in place; both give the same rows)
+    w = synthkv.WORKLOADS["ragged-b8-llama-kv-t8k-32k"].scaled("host2", layers=1, batch=5, heads=2, t_max=3000,
+                                                                 t_min=100)
+    K, V, lens = synthkv.make_kv(w, seed=9, device=DEV)
+    ratio, mode, window = 0.5, "cosine", 0
+    Ko, Vo, idx, kept, _ = _run_fused(K, V, ratio, mode, window, lens)
+    ks = idx.shape[2]
+    for pinned in (True, False):
+        hK = K.cpu().pin_memory()
+        hV = V.cpu().pin_memory() if pinned else V.cpu().clone()
+        assert hV.is_pinned() == pinned
+        dK, dV = torch.empty_like(K), torch.zeros_like(V)
+        dKo, dVo = torch.empty_like(Ko), torch.empty_like(Vo)
+        didx, dkept = torch.empty_like(idx), torch.empty_like(kept)
+        hKo = torch.zeros(Ko.shape, dtype=torch.bfloat16).pin_memory()
+        hVo = torch.zeros_like(hKo).pin_memory()
+        ws = mkv.workspace_for(K, window, lens)
+        mkv.mkv_compress_host(hK, hV, dK, dV, ratio, mode, window, ks, dKo, dVo, didx, dkept, hKo, hVo, None, None,
+                              ws, lens)
+        torch.cuda.synchronize()
+        assert mkv.mkv_device_status(ws) == 0
+        live = (torch.arange(ks)[None, None, :] < kept.cpu()[..., None])[..., None]
+        assert torch.equal(torch.where(live, hVo, 0), torch.where(live, Vo.cpu(), 0))
+        assert torch.equal(torch.where(live, hKo, 0), torch.where(live, Ko.cpu(), 0))
+        # with pinned values the device copy of V is never written
+        if pinned:
+            assert not torch.any(dV.view(torch.int16) != 0)
+
+
 def _check_in_place(K, V, lens, ratio, mode, window):
     """mkv_compress_inplace against mkv_compress on the same cache."""
     Ko, Vo, idx, kept, st = _run_fused(K, V, ratio, mode, window, lens)
