@@ -97,7 +97,7 @@ mkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MKV_OK : MKV_E
 
 // mkv_compress_host splits the batch rows into up to this many chunks, so
 // that the copies of one chunk overlap the kernels and copies of others.
-constexpr int32_t kHostChunks = 8;
+constexpr int32_t kHostChunks = 16;
 
 // Library-owned copy streams and events of one device (created on first use,
 // kept for the life of the process; the mutex serialises enqueueing).

@@ -323,7 +323,7 @@ mkv_status mkv_compress_profiled(const void *K, const void *V, mkv_shape shape, 
  * buffers hK_out, hV_out [batch, heads, keep_stride, head_dim] and h_idx,
  * h_kept [batch*heads(, keep_stride)]; any of the four host outputs may be
  * NULL. Device output buffers dK_out, dV_out, d_idx, d_kept are required.
- * The batch rows are processed in up to 8 chunks: chunk c's host-to-device
+ * The batch rows are processed in up to 16 chunks: chunk c's host-to-device
  * copies run on two library-owned copy-in streams (keys on one, values on
  * the other), its kernels on `stream`, its device-to-host copies on a
  * copy-out stream, so copies of different chunks overlap each other and the
