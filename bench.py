@@ -381,7 +381,9 @@ def run_ours(args):
         "stages_ms": dict(zip(STAGES, stage_ms)),
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * ((2 if single in (1, 2) else 4) + (0 if select_emits else 1)),
+        # per step: a1 + a2 (one kernel, or piece sums + window means + scores),
+        # select, compaction when select did not emit the indices, gather
+        "gpu_launches": args.steps * ((1 if single in (1, 2) else 3) + 1 + (0 if select_emits else 1) + 1),
         "clocks": clocks.summary(),
     }
     if world > 1:
@@ -579,7 +581,10 @@ def run_secondary(args):
                            "window": window, "ratio": ratio},
                 "hbm": {"path_bytes_per_step": nb["path"], "achieved_gbs": achieved,
                         "frac_of_measured": achieved / hbm, "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS},
-                "clocks": clocks.summary(), "gpu_launches": steps * 4}
+                "clocks": clocks.summary(),
+                # a1 + a2 (one kernel or three), select, in-place move
+                "gpu_launches": steps * ((1 if mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
+                                          in (1, 2) else 3) + 2)}
     else:  # quota
         w = synthkv.WORKLOADS["qwen3-8b-kv-t64k-w4096"] if args.workload == synthkv.BENCH_WORKLOAD else \
             synthkv.WORKLOADS[args.workload]
@@ -611,7 +616,10 @@ def run_secondary(args):
                            "window": window, "ratio": ratio, "keep_per_head": ks},
                 "hbm": {"path_bytes_per_step": nbytes, "achieved_gbs": achieved, "frac_of_measured": achieved / hbm,
                         "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS},
-                "clocks": clocks.summary(), "gpu_launches": steps * 5}
+                "clocks": clocks.summary(),
+                # a1 + a2 (one kernel or three), quota select, gather
+                "gpu_launches": steps * ((1 if mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
+                                          in (1, 2) else 3) + 2)}
     line["path"] = args.path
     print(json.dumps(line), flush=True)
 

@@ -5,8 +5,9 @@
 //
 // K_out[h][j] = K[h][idx[h][j]] and V_out likewise, bit copies. This is the
 // path's dominant kernel (8 bytes per kept element of K and V read and
-// written), a plain HBM-bound copy: 16-byte non-coherent loads, streaming
-// (evict-first) stores, a persistent grid over (head, 64-slot) items.
+// written), a plain HBM-bound copy: 16-byte non-coherent loads, plain
+// 16-byte stores (measured 1.5% faster here than evict-first streaming
+// stores), a persistent grid over (head, 64-slot) items.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -67,8 +68,8 @@ k_gather_rows(const int32_t *__restrict__ idx, int idx_stride, const int32_t *__
         for (int u = 0; u < R; ++u) {
             if (src[u] >= 0) {
                 const size_t off = out_head + (size_t)(u * SLOTS + hw) * RB;
-                st_stream(K_out + off, kv[u]);
-                st_stream(V_out + off, vv[u]);
+                st_v4(K_out + off, kv[u]);
+                st_v4(V_out + off, vv[u]);
             }
         }
     }
