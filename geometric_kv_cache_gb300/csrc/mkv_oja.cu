@@ -74,114 +74,143 @@ constexpr int kSmemBudget = 227 * 1024;
 
 // ------------------------------------------------------ 1: P q, hi + lo --
 
-// Item = (head, block of `rows` query rows: 32, or 16 when n_query is not a
-// multiple of 32). U [d, r] is staged in shared memory with row stride r|1
-// (odd: the column reads of both phases are free of bank conflicts), the
-// rows of Q and of y = U^T q as fp32 rows of 16-byte-aligned stride; global
-// loads are 16-byte vectors, eight in flight per thread. Each thread then
-// computes 8 rows of one output column, reading the 8 rows' operands as
-// 16-byte broadcasts:
-//   y[m][j] = sum_i q[m][i] U[i][j]   (i in order)
-//   p[m][i] = q[m][i] - sum_j U[i][j] y[m][j]   (j in order)
-// and writes hi = bf16(p), lo = bf16(p - hi) (the difference is exact).
-constexpr int kProjBlock = 8;  // rows per thread
+// Item = (head, block of `rows` query rows: 64, 32 or 16, the largest that
+// divides n_query); the block has rows / 8 warps. Shared memory holds q as
+// fp32 rows of stride 132, U [d, r] with its columns padded with zeros to rp
+// = r rounded up to 4 and a row stride of 4 x odd words, and y = U^T q as rows
+// of stride rp. Every shared load is a 16-byte vector and each thread keeps an
+// 8 x 4 tile of sums in registers:
+//   y[m][j] = sum_i q[m][i] U[i][j]   (i in order; 8 rows x 4 adjacent columns)
+//   p[m][i] = q[m][i] - sum_j U[i][j] y[m][j]   (j in order; 8 rows x dims
+//             lane + 32c, c < 4, so that a warp's U rows are consecutive)
+// and writes hi = bf16(p), lo = bf16(p - hi) (the difference is exact). The
+// zero padding adds fma(0, 0, s) terms, which leave every sum unchanged.
+constexpr int kProjBlock = 8;     // rows per thread
+constexpr int kProjQStride = 132; // fp32 words per staged q row
+
+__host__ __device__ constexpr int proj_rank_pad(int rank) { return (rank + 3) & ~3; }
+// a row stride of 4 x odd words: the 8 lanes of a quarter warp reading 16
+// bytes from 8 consecutive rows hit 32 distinct banks
+__host__ __device__ constexpr int proj_u_stride(int rank)
+{
+    return (proj_rank_pad(rank) / 4) % 2 == 1 ? proj_rank_pad(rank) : proj_rank_pad(rank) + 4;
+}
 
 __global__ void __launch_bounds__(kProjThreads)
 k_oja_project(const __nv_bfloat16 *__restrict__ Q, const float *__restrict__ U, int n_query, int rank, int rows,
               int64_t n_items, __nv_bfloat16 *__restrict__ qhl)
 {
     extern __shared__ __align__(16) float sm[];
-    const int us = rank | 1;
-    const int ys = (rank + 3) & ~3;       // y row stride (16-byte aligned rows)
-    float *sq = sm;                       // [rows][128]
-    float *sy = sq + rows * kHeadDim;     // [rows][ys]
-    float *sU = sy + rows * ys;           // [128][us]
-    const int blocks = n_query / rows;
-    const int n4 = kHeadDim * rank / 4;   // float4s of one head's basis
+    const int rp = proj_rank_pad(rank), us = proj_u_stride(rank);
+    float *sq = sm;                          // [rows][132]
+    float *sU = sq + rows * kProjQStride;    // [128][us]
+    float *sy = sU + kHeadDim * us;          // [rows][rp]
+    const int blocks = n_query / rows, nthr = (int)blockDim.x, tid = (int)threadIdx.x;
+    const int n4 = kHeadDim * rank / 4;      // float4s of one head's basis
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int64_t head = item / blocks;
         const int m0 = (int)(item - head * blocks) * rows;
         const float4 *U4 = reinterpret_cast<const float4 *>(U + head * kHeadDim * rank);
-        for (int base = 0; base < n4; base += kProjThreads * 8) {
+        for (int base = 0; base < n4; base += nthr * 8) {
             float4 v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int o = base + u * kProjThreads + (int)threadIdx.x;
+                const int o = base + u * nthr + tid;
                 if (o < n4) v[u] = __ldg(U4 + o);
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int o = base + u * kProjThreads + (int)threadIdx.x;
+                const int o = base + u * nthr + tid;
                 if (o < n4) {
-                    const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int e = 4 * o + c, i = e / rank;
-                        sU[i * us + (e - i * rank)] = f[c];
-                    }
+                    // element e = 4o + c sits at row e / rank, column e % rank
+                    int i = (4 * o) / rank, j = 4 * o - i * rank;
+                    sU[i * us + j] = v[u].x;
+                    if (++j == rank) j = 0, ++i;
+                    sU[i * us + j] = v[u].y;
+                    if (++j == rank) j = 0, ++i;
+                    sU[i * us + j] = v[u].z;
+                    if (++j == rank) j = 0, ++i;
+                    sU[i * us + j] = v[u].w;
                 }
             }
         }
+        for (int o = tid; o < kHeadDim * (rp - rank); o += nthr)  // zero the padding columns
+            sU[(o / (rp - rank)) * us + rank + o % (rp - rank)] = 0.f;
         const uint4 *Q4 = reinterpret_cast<const uint4 *>(Q + ((size_t)head * n_query + m0) * kHeadDim);
-        for (int o = threadIdx.x; o < rows * kHeadDim / 8; o += kProjThreads) {
+        for (int o = tid; o < rows * kHeadDim / 8; o += nthr) {
             float f[8];
             bf16x8_to_f32(__ldg(Q4 + o), f);
-            float4 *dst = reinterpret_cast<float4 *>(sq + 8 * o);
+            float4 *dst = reinterpret_cast<float4 *>(sq + (o >> 4) * kProjQStride + 8 * (o & 15));
             dst[0] = make_float4(f[0], f[1], f[2], f[3]);
             dst[1] = make_float4(f[4], f[5], f[6], f[7]);
         }
-        for (int o = threadIdx.x; o < rows * (ys - rank); o += kProjThreads)  // zero the y padding
-            sy[(o / (ys - rank)) * ys + rank + o % (ys - rank)] = 0.f;
         __syncthreads();
-        // y: (rows / 8) x rank items of 8 rows x 1 column
-        for (int o = threadIdx.x; o < (rows / kProjBlock) * rank; o += kProjThreads) {
-            const int mg = o / rank, j = o - mg * rank;
-            const float *q0 = sq + mg * kProjBlock * kHeadDim;
-            float acc[kProjBlock] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // y: (rows / 8) x (rp / 4) tiles
+        for (int o = tid; o < (rows / kProjBlock) * (rp / 4); o += nthr) {
+            const int mg = o / (rp / 4), j0 = 4 * (o - mg * (rp / 4));
+            const float *q0 = sq + mg * kProjBlock * kProjQStride;
+            float acc[kProjBlock][4];
+#pragma unroll
+            for (int r = 0; r < kProjBlock; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
             for (int i = 0; i < kHeadDim; i += 4) {
-                const float u0 = sU[i * us + j], u1 = sU[(i + 1) * us + j], u2 = sU[(i + 2) * us + j],
-                            u3 = sU[(i + 3) * us + j];
+                float4 u[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) u[c] = *reinterpret_cast<const float4 *>(sU + (i + c) * us + j0);
 #pragma unroll
                 for (int r = 0; r < kProjBlock; ++r) {
-                    const float4 qv = *reinterpret_cast<const float4 *>(q0 + r * kHeadDim + i);
-                    acc[r] = fmaf(qv.x, u0, acc[r]);
-                    acc[r] = fmaf(qv.y, u1, acc[r]);
-                    acc[r] = fmaf(qv.z, u2, acc[r]);
-                    acc[r] = fmaf(qv.w, u3, acc[r]);
+                    const float4 qv = *reinterpret_cast<const float4 *>(q0 + r * kProjQStride + i);
+                    const float qs[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        acc[r][0] = fmaf(qs[c], u[c].x, acc[r][0]);
+                        acc[r][1] = fmaf(qs[c], u[c].y, acc[r][1]);
+                        acc[r][2] = fmaf(qs[c], u[c].z, acc[r][2]);
+                        acc[r][3] = fmaf(qs[c], u[c].w, acc[r][3]);
+                    }
                 }
             }
 #pragma unroll
-            for (int r = 0; r < kProjBlock; ++r) sy[(mg * kProjBlock + r) * ys + j] = acc[r];
+            for (int r = 0; r < kProjBlock; ++r)
+                *reinterpret_cast<float4 *>(sy + (mg * kProjBlock + r) * rp + j0) =
+                    make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         }
         __syncthreads();
-        // p: (rows / 8) x 128 items of 8 rows x 1 dim
-        for (int o = threadIdx.x; o < (rows / kProjBlock) * kHeadDim; o += kProjThreads) {
-            const int mg = o >> 7, i = o & 127;
-            const float *ui = sU + i * us, *y0 = sy + mg * kProjBlock * ys;
-            float acc[kProjBlock] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int j = 0; j < ys; j += 4) {
-                // the padding columns of y are zero; U's padding reads are in
-                // bounds (row stride >= rank) and meet a zero factor
-                const float u0 = j < rank ? ui[j] : 0.f, u1 = j + 1 < rank ? ui[j + 1] : 0.f,
-                            u2 = j + 2 < rank ? ui[j + 2] : 0.f, u3 = j + 3 < rank ? ui[j + 3] : 0.f;
+        // p: (rows / 8) x 32 tiles, one warp per 8 rows
+        for (int o = tid; o < (rows / kProjBlock) * 32; o += nthr) {
+            const int mg = o >> 5, lane = o & 31;
+            const float *y0 = sy + mg * kProjBlock * rp;
+            float acc[kProjBlock][4];
+#pragma unroll
+            for (int r = 0; r < kProjBlock; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+            for (int j = 0; j < rp; j += 4) {
+                float4 u[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) u[c] = *reinterpret_cast<const float4 *>(sU + (lane + 32 * c) * us + j);
 #pragma unroll
                 for (int r = 0; r < kProjBlock; ++r) {
-                    const float4 yv = *reinterpret_cast<const float4 *>(y0 + r * ys + j);
-                    acc[r] = fmaf(u0, yv.x, acc[r]);
-                    acc[r] = fmaf(u1, yv.y, acc[r]);
-                    acc[r] = fmaf(u2, yv.z, acc[r]);
-                    acc[r] = fmaf(u3, yv.w, acc[r]);
+                    const float4 yv = *reinterpret_cast<const float4 *>(y0 + r * rp + j);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        acc[r][c] = fmaf(u[c].x, yv.x, acc[r][c]);
+                        acc[r][c] = fmaf(u[c].y, yv.y, acc[r][c]);
+                        acc[r][c] = fmaf(u[c].z, yv.z, acc[r][c]);
+                        acc[r][c] = fmaf(u[c].w, yv.w, acc[r][c]);
+                    }
                 }
             }
 #pragma unroll
             for (int r = 0; r < kProjBlock; ++r) {
                 const int m = mg * kProjBlock + r;
-                const float pv = sq[m * kHeadDim + i] - acc[r];
-                const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
                 const size_t row = (size_t)head * 2 * n_query + m0 + m;
-                qhl[row * kHeadDim + i] = hi;
-                qhl[(row + n_query) * kHeadDim + i] = lo;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int i = lane + 32 * c;
+                    const float pv = sq[m * kProjQStride + i] - acc[r][c];
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
+                    qhl[row * kHeadDim + i] = hi;
+                    qhl[(row + n_query) * kHeadDim + i] = lo;
+                }
             }
         }
         __syncthreads();  // shared memory is reused by the next item
@@ -606,13 +635,15 @@ cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, c
     cudaError_t e;
     if ((e = mark(0)) != cudaSuccess) return e;
     // 1: projected query rows, hi + lo
-    const int rows = n_query % 32 == 0 ? 32 : 16;
+    const int rows = n_query % 64 == 0 ? 64 : (n_query % 32 == 0 ? 32 : 16);
     const int64_t items = g.n_heads * (n_query / rows);
-    const size_t psmem = (size_t)(rows * kHeadDim + rows * ((rank + 3) & ~3) + kHeadDim * (rank | 1)) * sizeof(float);
+    const int pthreads = rows / kProjBlock * 32;
+    const size_t psmem =
+        (size_t)(rows * kProjQStride + kHeadDim * proj_u_stride(rank) + rows * proj_rank_pad(rank)) * sizeof(float);
     e = cudaFuncSetAttribute(k_oja_project, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
     if (e != cudaSuccess) return e;
-    const int pgrid = grid_for_items(reinterpret_cast<const void *>(k_oja_project), kProjThreads, psmem, items);
-    k_oja_project<<<pgrid, kProjThreads, psmem, st>>>(static_cast<const __nv_bfloat16 *>(Q), U, n_query, rank, rows,
+    const int pgrid = grid_for_items(reinterpret_cast<const void *>(k_oja_project), pthreads, psmem, items);
+    k_oja_project<<<pgrid, pthreads, psmem, st>>>(static_cast<const __nv_bfloat16 *>(Q), U, n_query, rank, rows,
                                                       items, static_cast<__nv_bfloat16 *>(qhl));
     if ((e = cudaGetLastError()) != cudaSuccess || (e = mark(1)) != cudaSuccess) return e;
     // 2: the contraction
