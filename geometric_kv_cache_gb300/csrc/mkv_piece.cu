@@ -854,20 +854,47 @@ __device__ __forceinline__ void load_rows_policy(const uint8_t *base, int len, i
 // (measured: 0.30 ms against 0.33 ms for the three kernels on 256 heads of
 // 16K tokens; without the policies pass 2 missed L2 on about a third of its
 // rows). Same bits as the three-kernel path.
+// Dynamic shared memory of k_head_groups: the pass-1 stash of per-warp piece
+// sums, then (same bytes) the unit's means; padded so that at most two CTAs
+// share an SM (the grid is then spread over all SMs). A unit holds at most
+// kMaxUnitWindows windows.
+constexpr size_t kGroupSmem = 80 * 1024;
+constexpr int kMaxUnitWindows = 64;
+constexpr int kMaxDim = 256;
+static_assert(kMaxUnitWindows * kMaxDim * sizeof(float) <= kGroupSmem, "means must fit");
+// pieces the stash holds for head dim D
+__host__ __device__ constexpr int stash_slots(int D) { return (int)(kGroupSmem / sizeof(float)) / (kWarps * D); }
+constexpr int kMaxSlots = stash_slots(64);
+
 template <int MODE, int NB>
 __global__ void __launch_bounds__(kThreads, 2)
 k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
 {
     constexpr int D = 64 * NB, RB = 2 * D;
     constexpr int kBatchG = 16 / NB;  // rows per lane in flight (256 bytes per lane for every head dim)
-    extern __shared__ float dyn[];    // red [kWarps][D], means [wb][D]; the rest only caps CTAs per SM
-    float *red = dyn;
-    float *cmean = dyn + kWarps * D;
+    constexpr int kSlots = stash_slots(D);
+    extern __shared__ float dyn[];    // pass 1: stash [kSlots][kWarps][D]; pass 2: means [wb][D]
+    float *stash = dyn;
+    float *cmean = dyn;
     __shared__ uint32_t s_ok;
+    __shared__ int64_t s_off[kMaxSlots];  // partial-sum offset of each stashed piece
     const int groups = gridDim.x / gsize;
     const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
     if (group >= groups) return;  // a launch is always a whole number of groups
-    const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
+    const int slot = threadIdx.x >> 3, q = threadIdx.x & 7, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // the stash's piece sums: warps in order (finish_sum's order), then free
+    auto flush = [&](int ns) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < ns * D; e += kThreads) {
+            const int j = e / D, d = e - j * D;
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) sum += stash[(j * kWarps + w) * D + d];
+            P.partial[s_off[j] + d] = sum;
+        }
+        __threadfence();  // the piece sums are visible GPU-wide before the arrival
+        __syncthreads();
+    };
     uint64_t keep_l2, drop_l2;
     asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep_l2));
     asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(drop_l2));
@@ -882,7 +909,11 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
         const int nw = T > 0 ? (T + wl - 1) / wl : 0;
         const int nwu = max(0, min(w0 + wb, nw) - w0);  // windows of this unit that exist
         const int nf = nwu * g.ppw;                      // piece slots of the unit
-        // pass 1: piece sums; piece slot f is window w0 + f / ppw, piece f % ppw
+        // pass 1: piece sums; piece slot f is window w0 + f / ppw, piece f % ppw.
+        // Each warp combines its 4 row slots by shuffles (as finish_sum does)
+        // and stashes the result; the CTA adds the warps once per kSlots
+        // pieces, so warps only meet at a CTA barrier there.
+        int ns = 0;
         for (int f = rank; f < nf; f += gsize) {
             const int w = w0 + f / g.ppw, p = f - (f / g.ppw) * g.ppw;
             const int wstart = w * wl, wlen = min(wl, T - wstart), off = p * g.piece_rows;
@@ -906,10 +937,24 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
                     }
                 }
             }
-            finish_sum<NB>(acc, red, P.partial + ((head * g.nwin_max + w) * (int64_t)g.ppw + p) * D);
-            if (threadIdx.x < D) __threadfence();  // the piece sum is visible GPU-wide before the arrival
-            __syncthreads();  // red is free again
+#pragma unroll
+            for (int j = 0; j < 8 * NB; ++j) {
+                acc[j] += __shfl_xor_sync(kFull, acc[j], 8);
+                acc[j] += __shfl_xor_sync(kFull, acc[j], 16);
+            }
+            if (lane < 8) {
+#pragma unroll
+                for (int k = 0; k < NB; ++k)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) stash[(ns * kWarps + warp) * D + 64 * k + q * 8 + j] = acc[8 * k + j];
+            }
+            if (threadIdx.x == 0) s_off[ns] = ((head * g.nwin_max + w) * (int64_t)g.ppw + p) * D;
+            if (++ns == kSlots) {
+                flush(ns);
+                ns = 0;
+            }
         }
+        if (ns > 0) flush(ns);
         // the group's barrier for this unit
         if (threadIdx.x == 0) {
             __threadfence();
@@ -1043,13 +1088,6 @@ cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, 
 
 namespace {
 
-// Dynamic shared memory of k_head_groups: red and the unit's means, padded
-// so that at most two CTAs share an SM (the grid is then spread over all
-// SMs); a unit holds at most kMaxUnitWindows windows.
-constexpr size_t kGroupSmem = 80 * 1024;
-constexpr int kMaxUnitWindows = 64;
-constexpr int kMaxDim = 256;
-static_assert((kWarps + kMaxUnitWindows) * kMaxDim * sizeof(float) <= kGroupSmem, "means must fit");
 
 // The kernel instance for a head dim (64 * NB) and mode.
 const void *head_groups_fn(int d, int mode)
