@@ -58,6 +58,11 @@ def _load():
         lib = ctypes.CDLL(build())
         i64, f64, vp, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
         lib.oracle_bf16_to_double.restype = f64
+        lib.oracle_e4m3_to_double.restype = f64
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_bf16.restype = i32
+        lib.oracle_e4m3_to_bf16.argtypes = [vp, i64, vp]
+        lib.oracle_gather_bytes.argtypes = [vp, i64, vp, i64, vp]
         lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_num_keep.restype = i64
         lib.oracle_num_keep.argtypes = [i64, f64]
@@ -100,10 +105,36 @@ def _load():
         return lib
 
 
+def _is_fp8(x) -> bool:
+    return hasattr(x, "dtype") and str(x.dtype) == "torch.float8_e4m3fn"
+
+
+def _codes(x) -> np.ndarray:
+    """The E4M3 codes of a torch float8_e4m3fn tensor as a C-contiguous uint8 array."""
+    import torch
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.uint8).numpy())
+
+
+def e4m3_to_double(code: int) -> float:
+    return _load().oracle_e4m3_to_double(int(code) & 0xFF)
+
+
+def e4m3_to_bf16_bits(codes) -> np.ndarray:
+    """Exact widening of E4M3 codes (uint8 array) to bf16 bit patterns."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(c.shape, dtype=np.uint16)
+    if _load().oracle_e4m3_to_bf16(_ptr(c), c.size, _ptr(out)) != 0:
+        raise ValueError("NaN E4M3 code (outside the contract)")
+    return out
+
+
 def _bits(x) -> np.ndarray:
     """bf16 data as a C-contiguous uint16 array of raw bit patterns.
 
-    Accepts a numpy uint16/int16 array or a torch bfloat16 tensor (on the CPU)."""
+    Accepts a numpy uint16/int16 array or a torch bfloat16 tensor (on the
+    CPU); a torch float8_e4m3fn tensor is widened exactly to bf16 first."""
+    if _is_fp8(x):
+        return e4m3_to_bf16_bits(_codes(x))
     if hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16":
         import torch
         x = x.detach().cpu().contiguous().view(torch.int16).numpy()
@@ -117,6 +148,26 @@ def _bits(x) -> np.ndarray:
 
 def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _fp8_rows(res: dict, K, V) -> dict:
+    """For fp8 inputs, replace the kept rows (computed on the exact bf16
+    widening) by byte copies of the fp8 rows at the same indices."""
+    if not _is_fp8(K):
+        return res
+    res = dict(res)
+    res["K_out"] = gather_bytes(_codes(K), res["idx"])
+    res["V_out"] = gather_bytes(_codes(V), res["idx"])
+    return res
+
+
+def gather_bytes(X: np.ndarray, idx) -> np.ndarray:
+    """Rows X[idx] of a uint8 [T, row_bytes] array (any element type)."""
+    x = np.ascontiguousarray(X, dtype=np.uint8)
+    i = np.ascontiguousarray(idx, dtype=np.int32)
+    out = np.zeros((i.shape[0], x.shape[1]), dtype=np.uint8)
+    _load().oracle_gather_bytes(_ptr(x), x.shape[1], _ptr(i), i.shape[0], _ptr(out))
+    return out
 
 
 def bf16_to_double(bits: int) -> float:
@@ -190,14 +241,16 @@ def compress_head(K, V, ratio: float, mode="l2", window: int = 0):
                                        _ptr(C), _ptr(S), _ptr(idx), _ptr(ko), _ptr(vo))
     if got != n:
         raise ValueError("oracle_compress_head failed")
-    return {"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}
+    return _fp8_rows({"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n],
+                      "V_out": vo[:n]}, K, V)
 
 
 def compress_heads(K, V, lens, ratio: float, mode="l2", window: int = 0, keep_stride=None):
     """All steps for a [n_heads, t_stride, d] cache with per-head lengths.
 
     Returns (idx int32 [n, keep_stride], kept int32 [n], K_out, V_out uint16
-    [n, keep_stride, d]); entries past a head's kept count are zero."""
+    [n, keep_stride, d], or uint8 codes for float8_e4m3fn inputs); entries
+    past a head's kept count are zero."""
     k, v = _bits(K), _bits(V)
     n_heads, t_stride, d = k.shape
     ln = np.ascontiguousarray(lens, dtype=np.int32).reshape(-1)
@@ -214,6 +267,14 @@ def compress_heads(K, V, lens, ratio: float, mode="l2", window: int = 0, keep_st
                                        _ptr(idx), _ptr(kept), _ptr(ko), _ptr(vo))
     if rc != 0:
         raise ValueError("oracle_compress_heads failed")
+    if _is_fp8(K):  # the kept rows as fp8 bytes at the same indices
+        kc, vc = _codes(K), _codes(V)
+        ko = np.zeros((n_heads, max(keep_stride, 1), d), dtype=np.uint8)
+        vo = np.zeros_like(ko)
+        for h in range(n_heads):
+            n = int(kept[h])
+            ko[h, :n] = gather_bytes(kc[h], idx[h, :n])
+            vo[h, :n] = gather_bytes(vc[h], idx[h, :n])
     return idx[:, :keep_stride], kept, ko[:, :keep_stride], vo[:, :keep_stride]
 
 
@@ -243,7 +304,8 @@ def compress_head_n(K, V, n_keep: int, mode="l2", window: int = 0):
                                          _ptr(idx), _ptr(ko), _ptr(vo))
     if got != n:
         raise ValueError("oracle_compress_head_n failed")
-    return {"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}
+    return _fp8_rows({"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n],
+                      "V_out": vo[:n]}, K, V)
 
 
 def window_means(X, window: int, radius: bool = True):
@@ -289,7 +351,8 @@ def compress_head_quota(K, V, ratio: float, mode="l2", window: int = 0):
                                              _ptr(C), _ptr(S), _ptr(idx), _ptr(ko), _ptr(vo))
     if got != n:
         raise ValueError("oracle_compress_head_quota failed")
-    return {"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n], "V_out": vo[:n]}
+    return _fp8_rows({"C": C[: num_windows(T, window)], "S": S[:T], "idx": idx[:n], "K_out": ko[:n],
+                      "V_out": vo[:n]}, K, V)
 
 
 def oja_scores(K, Q, U) -> np.ndarray:
@@ -325,7 +388,16 @@ def compress_head_oja(K, V, Q, U, n_keep: int):
 
 def compact_in_place(X, idx) -> np.ndarray:
     """In-place compaction of a bf16 [T, d] head: a copy of X (uint16 bits)
-    with rows [0, len(idx)) replaced by X[idx] and the rest unchanged."""
+    with rows [0, len(idx)) replaced by X[idx] and the rest unchanged. For a
+    float8_e4m3fn head the result is uint8 codes: rows are moved whole, so
+    each row's bytes are moved as d / 2 uint16 pairs."""
+    if _is_fp8(X):
+        c = _codes(X)
+        x = np.ascontiguousarray(c).view(np.uint16).copy()
+        i = np.ascontiguousarray(idx, dtype=np.int32)
+        if _load().oracle_compact_in_place(_ptr(x), x.shape[0], x.shape[1], _ptr(i), i.shape[0]) != 0:
+            raise ValueError("oracle_compact_in_place: indices not strictly ascending in [0, T)")
+        return x.view(np.uint8)
     x = _bits(X).copy()
     i = np.ascontiguousarray(idx, dtype=np.int32)
     if _load().oracle_compact_in_place(_ptr(x), x.shape[0], x.shape[1], _ptr(i), i.shape[0]) != 0:

@@ -32,7 +32,10 @@
  *
  * Everything is fp64, summed in token order, with no blocking or reordering.
  * Keys arrive as raw bfloat16 bit patterns (uint16); decoding them to double
- * is exact. Compile with -ffp-contract=off so every operation rounds once.
+ * is exact. fp8 (E4M3) caches are widened exactly to bfloat16 first
+ * (oracle_e4m3_to_bf16) and their kept rows are copied as bytes
+ * (oracle_gather_bytes). Compile with -ffp-contract=off so every operation
+ * rounds once.
  */
 #include <math.h>
 #include <stdint.h>
@@ -50,6 +53,45 @@ double oracle_bf16_to_double(uint16_t bits)
     float f;
     memcpy(&f, &w, sizeof f);
     return (double)f;
+}
+
+/* fp8 caches hold OCP 8-bit floating point E4M3 codes (the "OCP 8-bit
+ * Floating Point Specification (OFP8)", E4M3 encoding; torch's
+ * float8_e4m3fn): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 is subnormal, m * 2^-9; no infinities; S.1111.111 is NaN.
+ * The method runs on the decoded values, which this returns exactly (NaN
+ * for the NaN codes, which are outside the contract). */
+double oracle_e4m3_to_double(uint8_t code)
+{
+    int neg = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + (double)m, e - 10); /* (1 + m/8) 2^(e-7) */
+    return neg ? -v : v;
+}
+
+/* Every finite E4M3 value is a bfloat16 value (3 mantissa bits fit in 7, and
+ * 2^-9 .. 448 lies inside bf16's normal range), so an fp8 cache widens to a
+ * bf16 cache exactly and every step below runs on it unchanged. Writes the
+ * bf16 bit patterns of n codes; returns -1 (nothing defined) on a NaN code. */
+int oracle_e4m3_to_bf16(const uint8_t *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double v = oracle_e4m3_to_double(x[i]);
+        if (v != v) return -1;
+        float f = (float)v; /* exact */
+        uint32_t w;
+        memcpy(&w, &f, sizeof w);
+        if (w & 0xFFFFu) return -1; /* cannot happen for a finite E4M3 value */
+        out[i] = (uint16_t)(w >> 16);
+    }
+    return 0;
+}
+
+/* Step 4 for caches of any element type: row idx[j] of X (row_bytes bytes
+ * per row) copied to row j of out. */
+void oracle_gather_bytes(const uint8_t *X, int64_t row_bytes, const int32_t *idx, int64_t n, uint8_t *out)
+{
+    for (int64_t j = 0; j < n; ++j) memcpy(out + j * row_bytes, X + (int64_t)idx[j] * row_bytes, (size_t)row_bytes);
 }
 
 /* Step 3, reading of "% compression": the percentage is the share removed,

@@ -153,24 +153,37 @@ def _head_kv(w: KVWorkload, seed: int, head: int, t_len: int, device, pad_value:
     return k.to(torch.bfloat16), v.to(torch.bfloat16), torch.sort(planted).values
 
 
+# Largest finite magnitude of float8_e4m3fn; torch's cast turns anything
+# beyond it into NaN, so fp8 caches are clamped to it first.
+E4M3_MAX = 448.0
+
+
 def make_kv(w: KVWorkload, seed: int = 0, device="cpu", pad_value: float = 300.0,
-            heads: Optional[Sequence[int]] = None, with_planted: bool = False):
+            heads: Optional[Sequence[int]] = None, with_planted: bool = False, dtype=torch.bfloat16):
     """Generate the cache of a workload.
 
-    Returns (K, V, seq_lens) with K, V bf16 [L*B, H, t_max, d] on ``device``
-    and seq_lens int32 [L*B] on ``device``. With ``heads`` (flat head indices
-    in [0, L*B*H)), only those heads are generated and K, V have shape
-    [len(heads), t_max, d]; each head's data does not depend on which other
-    heads are generated. With ``with_planted`` a list of the planted token
-    positions per generated head is returned as a fourth element."""
+    Returns (K, V, seq_lens) with K, V [L*B, H, t_max, d] on ``device`` and
+    seq_lens int32 [L*B] on ``device``. K and V are bf16, or, with ``dtype``
+    torch.float8_e4m3fn, the same values clamped to +-448 and rounded to
+    E4M3 by torch's cast. With ``heads`` (flat head indices in [0, L*B*H)),
+    only those heads are generated and K, V have shape [len(heads), t_max,
+    d]; each head's data does not depend on which other heads are generated.
+    With ``with_planted`` a list of the planted token positions per
+    generated head is returned as a fourth element."""
     lens = seq_lengths(w, seed)
     ids = list(range(w.n_heads)) if heads is None else list(heads)
-    K = torch.empty((len(ids), w.t_max, w.head_dim), dtype=torch.bfloat16, device=device)
+    fp8 = dtype == torch.float8_e4m3fn
+    if dtype not in (torch.bfloat16, torch.float8_e4m3fn):
+        raise ValueError(f"unsupported cache dtype {dtype}")
+    K = torch.empty((len(ids), w.t_max, w.head_dim), dtype=dtype, device=device)
     V = torch.empty_like(K)
     planted = []
     for j, h in enumerate(ids):
         t_len = int(lens[h // w.heads])
         k, v, p = _head_kv(w, seed, h, t_len, device, pad_value)
+        if fp8:
+            k = k.float().clamp(-E4M3_MAX, E4M3_MAX)
+            v = v.float().clamp(-E4M3_MAX, E4M3_MAX)
         K[j].copy_(k)
         V[j].copy_(v)
         planted.append(p.cpu())

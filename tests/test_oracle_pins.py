@@ -605,3 +605,90 @@ def test_compact_in_place_rejects_unordered_indices():
     for bad in ([2, 1], [0, 0], [4], [-1]):
         with pytest.raises(ValueError):
             oracle.compact_in_place(X, bad)
+
+
+# --- fp8 (E4M3) caches ---------------------------------------------------------
+# Decoding follows the OCP 8-bit floating point specification (OFP8), E4M3:
+# 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals m * 2^-9 at
+# exponent field 0, no infinities, S.1111.111 = NaN.
+
+E4M3_TABLE = [  # code, value, why
+    (0x00, 0.0, "zero"),
+    (0x01, 2.0 ** -9, "smallest subnormal: m = 1 at exponent field 0"),
+    (0x07, 7 * 2.0 ** -9, "largest subnormal"),
+    (0x08, 2.0 ** -6, "smallest normal: exponent field 1, 2^(1-7)"),
+    (0x38, 1.0, "exponent field 7 = bias"),
+    (0x3F, 1.875, "1 + 7/8"),
+    (0x40, 2.0, "exponent field 8"),
+    (0x77, 240.0, "1.875 * 2^7"),
+    (0x7E, 448.0, "largest finite: 1.75 * 2^8 (1.875 * 2^8 is the NaN code)"),
+    (0x80, -0.0, "negative zero"),
+    (0xB8, -1.0, "sign bit"),
+    (0xFE, -448.0, "most negative finite"),
+]
+
+
+def test_e4m3_decode_table():
+    for code, value, why in E4M3_TABLE:
+        got = oracle.e4m3_to_double(code)
+        assert got == value and math.copysign(1.0, got) == math.copysign(1.0, value), (hex(code), why)
+    assert math.isnan(oracle.e4m3_to_double(0x7F)) and math.isnan(oracle.e4m3_to_double(0xFF))
+
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(int(c)) for c in codes])
+    finite = np.isfinite(ref)
+    assert finite.sum() == 254
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.isnan(got[~finite]).all()
+
+
+def test_e4m3_widening_to_bf16_is_exact():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    bits = oracle.e4m3_to_bf16_bits(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.bfloat16)
+    assert np.array_equal(bits.view(np.int16), ref.view(torch.int16).numpy())
+    with pytest.raises(ValueError):
+        oracle.e4m3_to_bf16_bits(np.array([0x7F], dtype=np.uint8))
+
+
+def _fp8(x):
+    return torch.tensor(x, dtype=torch.float32).to(torch.float8_e4m3fn)
+
+
+def test_fp8_hand_case():
+    # keys (0,0), (2,0), (0,2), (6,6) are exact in E4M3: centroid (2,2),
+    # distances sqrt(8), 2, 2, sqrt(32); r = 0.25 keeps {0, 1, 3} (the tie
+    # between tokens 1 and 2 goes to the lower index)
+    K = _fp8([[0, 0], [2, 0], [0, 2], [6, 6]])
+    V = _fp8([[1, -1], [2, -2], [3, -3], [4, -4]])
+    res = oracle.compress_head(K, V, 0.25, "l2", 0)
+    assert np.array_equal(res["C"], [[2.0, 2.0]])
+    assert np.array_equal(res["S"], [math.sqrt(8), 2.0, 2.0, math.sqrt(32)])
+    assert res["idx"].tolist() == [0, 1, 3]
+    codes = V.view(torch.uint8).numpy()
+    assert res["V_out"].dtype == np.uint8 and np.array_equal(res["V_out"], codes[[0, 1, 3]])
+
+
+@pytest.mark.parametrize("mode,window", [("l2", 0), ("cosine", 0), ("l2", 37), ("cosine", 100)])
+def test_fp8_head_equals_its_bf16_widening(mode, window):
+    # the method runs on the decoded values: an fp8 head and its exact bf16
+    # widening give the same centroids, scores and kept set, and the kept
+    # rows are the fp8 rows at those indices
+    g = torch.Generator().manual_seed(5)
+    K = (torch.randn(301, 16, generator=g) * 3).clamp(-448, 448).to(torch.float8_e4m3fn)
+    V = (torch.randn(301, 16, generator=g) * 3).clamp(-448, 448).to(torch.float8_e4m3fn)
+    a = oracle.compress_head(K, V, 0.4, mode, window)
+    b = oracle.compress_head(K.to(torch.bfloat16), V.to(torch.bfloat16), 0.4, mode, window)
+    assert np.array_equal(a["C"], b["C"]) and np.array_equal(a["S"], b["S"]) and np.array_equal(a["idx"], b["idx"])
+    kc = K.view(torch.uint8).numpy()
+    assert np.array_equal(a["K_out"], kc[a["idx"]])
+    # batched form and the in-place form agree with the per-head one
+    idx, kept, ko, vo = oracle.compress_heads(K[None], V[None], [301], 0.4, mode, window)
+    assert int(kept[0]) == len(a["idx"]) and np.array_equal(idx[0, :kept[0]], a["idx"])
+    assert np.array_equal(ko[0, :kept[0]], a["K_out"]) and np.array_equal(vo[0, :kept[0]], a["V_out"])
+    x = oracle.compact_in_place(V, a["idx"])
+    n = len(a["idx"])
+    assert np.array_equal(x[:n], a["V_out"]) and np.array_equal(x[n:], V.view(torch.uint8).numpy()[n:])
