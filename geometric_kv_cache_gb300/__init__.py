@@ -54,7 +54,11 @@ EXPORTED = (
 
 class MkvShape(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("t_max", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("seq_lens", ctypes.c_void_p)]
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32), ("seq_lens", ctypes.c_void_p)]
+
+
+# mkv_dtype of each supported cache element type
+DTYPES = {torch.bfloat16: 0, torch.float8_e4m3fn: 1}
 
 
 class MKVError(RuntimeError):
@@ -142,6 +146,14 @@ def _check(status: int, where: str):
         raise MKVError(status, where)
 
 
+def _cache_types(*ts):
+    """The cache tensors of one call (K, V and the compacted outputs) share one
+    element type: the library reads them all with the shape's dtype."""
+    types = {t.dtype for t in ts if t is not None}
+    if len(types) > 1 or not types <= set(DTYPES):
+        raise ValueError("K, V and the output caches must share one dtype: bf16 or float8_e4m3fn")
+
+
 def _need_cuda(*ts):
     for t in ts:
         if t is not None and not t.is_cuda:
@@ -151,13 +163,13 @@ def _need_cuda(*ts):
 
 
 def shape_of(K: torch.Tensor, seq_lens: Optional[torch.Tensor] = None) -> MkvShape:
-    """mkv_shape of a [batch, heads, t_max, head_dim] bf16 cache."""
-    if K.dim() != 4 or K.dtype != torch.bfloat16:
-        raise ValueError("K must be a bf16 tensor [batch, heads, t_max, head_dim]")
+    """mkv_shape of a [batch, heads, t_max, head_dim] bf16 or float8_e4m3fn cache."""
+    if K.dim() != 4 or K.dtype not in DTYPES:
+        raise ValueError("K must be a bf16 or float8_e4m3fn tensor [batch, heads, t_max, head_dim]")
     if seq_lens is not None and (seq_lens.dtype != torch.int32 or seq_lens.numel() != K.shape[0]):
         raise ValueError("seq_lens must be int32 [batch]")
     b, h, t, d = K.shape
-    return MkvShape(b, h, t, d, None if seq_lens is None else seq_lens.data_ptr())
+    return MkvShape(b, h, t, d, DTYPES[K.dtype], None if seq_lens is None else seq_lens.data_ptr())
 
 
 def mkv_status_string(status: int) -> str:
@@ -257,6 +269,7 @@ def mkv_select_topk(S, shape: MkvShape, ratio, cut, workspace, n_keep=None, stre
 def mkv_compact(S, cut, K, V, shape: MkvShape, ratio, keep_stride, idx, kept, K_out, V_out, workspace,
                 n_keep=None, stream=None):
     _need_cuda(S, cut, K, V, idx, kept, K_out, V_out, workspace, n_keep)
+    _cache_types(K, V, K_out, V_out)
     _check(load().mkv_compact(_ptr(S), _ptr(cut), _ptr(K), _ptr(V), shape, float(ratio), _ptr(n_keep),
                               int(keep_stride), _ptr(idx), _ptr(kept), _ptr(K_out), _ptr(V_out), _ptr(workspace),
                               workspace.numel(), _stream(stream)), "mkv_compact")
@@ -265,6 +278,7 @@ def mkv_compact(S, cut, K, V, shape: MkvShape, ratio, keep_stride, idx, kept, K_
 def mkv_compress(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, workspace, seq_lens=None,
                  n_keep=None, stream=None):
     _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens, n_keep)
+    _cache_types(K, V, K_out, V_out)
     _check(load().mkv_compress(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _ptr(n_keep), _MODES[mode],
                                int(window), int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx), _ptr(kept),
                                _ptr(workspace), workspace.numel(), _stream(stream)), "mkv_compress")
@@ -284,6 +298,7 @@ def mkv_select_quota(S, shape: MkvShape, ratio, window, keep_stride, idx, kept, 
 def mkv_compress_quota(K, V, ratio, mode, window, keep_stride, K_out, V_out, idx, kept, workspace, seq_lens=None,
                        stream=None):
     _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens)
+    _cache_types(K, V, K_out, V_out)
     _check(load().mkv_compress_quota(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _MODES[mode],
                                      int(window), int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx),
                                      _ptr(kept), _ptr(workspace), workspace.numel(), _stream(stream)),
@@ -335,6 +350,7 @@ def mkv_compress_inplace(K, V, ratio, mode, window, workspace, idx=None, kept=No
     """Compress K and V in place: rows [0, kept) of every head become the
     kept rows; idx [B, H, t_max] and kept [B, H] are optional outputs."""
     _need_cuda(K, V, idx, kept, workspace, seq_lens, n_keep)
+    _cache_types(K, V)
     _check(load().mkv_compress_inplace(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _ptr(n_keep),
                                        _MODES[mode], int(window), _ptr(idx), _ptr(kept), _ptr(workspace),
                                        workspace.numel(), _stream(stream)), "mkv_compress_inplace")
@@ -344,6 +360,7 @@ def mkv_compress_profiled(K, V, ratio, mode, window, keep_stride, K_out, V_out, 
                           seq_lens=None, n_keep=None, stream=None):
     """mkv_compress with torch.cuda.Event objects recorded around each kernel."""
     _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens, n_keep)
+    _cache_types(K, V, K_out, V_out)
     st = torch.cuda.current_stream() if stream is None else stream
     for e in events:
         if not e.cuda_event:  # torch creates the CUDA event on its first record
@@ -359,6 +376,7 @@ def mkv_compress_host(hK, hV, dK, dV, ratio, mode, window, keep_stride, dK_out, 
                       hK_out, hV_out, h_idx, h_kept, workspace, seq_lens=None, stream=None):
     """Host-resident cache: H2D copies, compress and D2H copies in one call."""
     _need_cuda(dK, dV, dK_out, dV_out, d_idx, d_kept, workspace, seq_lens)
+    _cache_types(hK, hV, dK, dV, dK_out, dV_out, hK_out, hV_out)
     for t in (hK, hV, hK_out, hV_out, h_idx, h_kept):
         if t is not None and (t.is_cuda or not t.is_contiguous()):
             raise ValueError("host buffers must be contiguous CPU tensors (pinned for asynchrony)")
@@ -377,6 +395,7 @@ def mkv_compress_noalloc(K, V, ratio, mode, window, keep_stride, K_out, V_out, i
     calls must not overlap on the GPU. ``status_out`` (int32/uint32 [1] on
     the device, optional) receives the call's device status bits."""
     _need_cuda(K, V, K_out, V_out, idx, kept, status_out, seq_lens, n_keep)
+    _cache_types(K, V, K_out, V_out)
     _check(load().mkv_compress_noalloc(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _ptr(n_keep),
                                        _MODES[mode], int(window), int(keep_stride), _ptr(K_out), _ptr(V_out),
                                        _ptr(idx), _ptr(kept), _ptr(status_out), _stream(stream)),
@@ -388,6 +407,7 @@ def mkv_inject_stalled_windows(K, V, ratio, mode, window, keep_stride, K_out, V_
     """Failure injection: the single-pass kernel with no window ever
     completing; every wait between CTAs must run out (MKV_DEV_TIMEOUT)."""
     _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens)
+    _cache_types(K, V, K_out, V_out)
     _check(load().mkv_inject_stalled_windows(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _MODES[mode],
                                              int(window), int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx),
                                              _ptr(kept), _ptr(workspace), workspace.numel(), _stream(stream)),

@@ -61,13 +61,18 @@ int64_t host_num_keep_quota(int32_t T, double ratio, int32_t window)
 mkv_status check_shape(const mkv_shape &s)
 {
     if (s.batch < 0 || s.heads < 0 || s.t_max < 0 || s.head_dim <= 0) return MKV_ERR_INVALID_ARG;
-    if (!supported_head_dim(s.head_dim)) return MKV_ERR_UNSUPPORTED;
+    if (!supported_head_dim(s.head_dim) || elem_bytes(s.dtype) == 0) return MKV_ERR_UNSUPPORTED;
     if (s.t_max > (1 << 30)) return MKV_ERR_UNSUPPORTED;
     if (s.seq_lens && !aligned(s.seq_lens, 4)) return MKV_ERR_INVALID_ARG;
     return MKV_OK;
 }
 
 bool empty(const mkv_shape &s) { return s.batch == 0 || s.heads == 0 || s.t_max == 0; }
+
+Geometry geometry_of(const mkv_shape &s, int32_t window)
+{
+    return make_geometry(s.batch, s.heads, s.t_max, window, s.head_dim, elem_bytes(s.dtype));
+}
 
 mkv_status check_ws(const Layout &L, void *ws, size_t ws_bytes)
 {
@@ -169,7 +174,8 @@ mkv_status run_centroid_score(const Geometry &g, const Layout &L, const void *K,
     uint32_t *status = region<uint32_t>(ws, L.status);
     float *partial = region<float>(ws, L.partial);
     cudaError_t e = cudaSuccess;
-    const int grid = g.d == kHeadDim && (stall_windows || g_single_pass_enabled.load(std::memory_order_relaxed))
+    const int grid = g.d == kHeadDim && g.es == 2 &&
+                             (stall_windows || g_single_pass_enabled.load(std::memory_order_relaxed))
                          ? single_pass_grid((int)mode)
                          : 0;
     bool single = grid > 0 && grid >= g.pg.ppw;
@@ -225,7 +231,7 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     quota = quota && window > 0 && window < s.t_max;
     rc = check_outputs(s, ratio, n_keep, keep_stride, K, V, K_out, V_out, idx, kept, false, quota ? window : 0);
     if (rc != MKV_OK) return rc;
-    const Geometry g = make_geometry(s.batch, s.heads, s.t_max, window, s.head_dim);
+    const Geometry g = geometry_of(s, window);
     const Layout L = make_layout(g);
     rc = check_ws(L, ws, ws_bytes);
     if (rc != MKV_OK) return rc;
@@ -276,11 +282,13 @@ constexpr int32_t kCompressStages = 6;
 
 }  // namespace
 
-Geometry make_geometry(int32_t batch, int32_t heads, int32_t t_max, int32_t window, int32_t head_dim)
+Geometry make_geometry(int32_t batch, int32_t heads, int32_t t_max, int32_t window, int32_t head_dim, int32_t es)
 {
     Geometry g;
     g.d = head_dim;
     g.pg.d = head_dim;
+    g.es = es;
+    g.pg.es = es;
     g.n_heads = (int64_t)batch * heads;
     g.heads = heads;
     g.t_max = t_max;
@@ -354,7 +362,7 @@ int32_t mkv_num_windows(int32_t t_max, int32_t window)
 size_t mkv_workspace_size(mkv_shape shape, int32_t window)
 {
     if (check_shape(shape) != MKV_OK || window < 0) return 0;
-    return make_layout(make_geometry(shape.batch, shape.heads, shape.t_max, window, shape.head_dim)).total;
+    return make_layout(geometry_of(shape, window)).total;
 }
 
 mkv_status mkv_centroid(const void *K, mkv_shape shape, int32_t window, float *C, void *workspace,
@@ -363,7 +371,7 @@ mkv_status mkv_centroid(const void *K, mkv_shape shape, int32_t window, float *C
     mkv_status rc = check_shape(shape);
     if (rc != MKV_OK) return rc;
     if (!K || !C || window < 0 || !aligned(K, 16) || !aligned(C, 16)) return MKV_ERR_INVALID_ARG;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window, shape.head_dim);
+    const Geometry g = geometry_of(shape, window);
     const Layout L = make_layout(g);
     if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
     if (empty(shape)) return MKV_OK;
@@ -382,7 +390,7 @@ mkv_status mkv_window_means(const void *X, mkv_shape shape, int32_t window, floa
     if (rc != MKV_OK) return rc;
     if (!X || !mean || window < 0 || !aligned(X, 16) || !aligned(mean, 16)) return MKV_ERR_INVALID_ARG;
     if (radius && !aligned(radius, 4)) return MKV_ERR_INVALID_ARG;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window, shape.head_dim);
+    const Geometry g = geometry_of(shape, window);
     const bool small = window > 0 && window <= kSmallWindowMax;
     if (radius && !small) return MKV_ERR_UNSUPPORTED;
     const Layout L = make_layout(g);
@@ -403,7 +411,7 @@ mkv_status mkv_centroid_score(const void *K, mkv_shape shape, int32_t window, mk
     if (rc != MKV_OK) return rc;
     if (!K || !C || !S || window < 0 || !aligned(K, 16) || !aligned(C, 16) || !aligned(S, 4)) return MKV_ERR_INVALID_ARG;
     if (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE) return MKV_ERR_INVALID_ARG;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window, shape.head_dim);
+    const Geometry g = geometry_of(shape, window);
     const Layout L = make_layout(g);
     if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
     if (empty(shape)) return MKV_OK;
@@ -418,7 +426,7 @@ mkv_status mkv_score(const void *K, const float *C, mkv_shape shape, int32_t win
     if (rc != MKV_OK) return rc;
     if (!K || !C || !S || window < 0 || !aligned(K, 16) || !aligned(C, 16) || !aligned(S, 4)) return MKV_ERR_INVALID_ARG;
     if (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE) return MKV_ERR_INVALID_ARG;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window, shape.head_dim);
+    const Geometry g = geometry_of(shape, window);
     const Layout L = make_step_layout(g);
     if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
     if (empty(shape)) return MKV_OK;
@@ -433,7 +441,7 @@ mkv_status mkv_select_topk(const float *S, mkv_shape shape, double ratio, const 
     if (rc != MKV_OK) return rc;
     if (!S || !cut || !aligned(S, 4) || !aligned(cut, 8) || !ratio_ok(ratio)) return MKV_ERR_INVALID_ARG;
     if (n_keep && !aligned(n_keep, 4)) return MKV_ERR_INVALID_ARG;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, 0, shape.head_dim);
+    const Geometry g = geometry_of(shape, 0);
     const Layout L = make_step_layout(g);
     if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
     if (empty(shape)) return MKV_OK;
@@ -450,7 +458,7 @@ mkv_status mkv_compact(const float *S, const mkv_cut *cut, const void *K, const 
     if (!S || !cut || !idx || !kept || !aligned(S, 4) || !aligned(cut, 8)) return MKV_ERR_INVALID_ARG;
     rc = check_outputs(shape, ratio, n_keep, keep_stride, K, V, K_out, V_out, idx, kept, false);
     if (rc != MKV_OK) return rc;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, 0, shape.head_dim);
+    const Geometry g = geometry_of(shape, 0);
     const Layout L = make_step_layout(g);
     if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
     if (empty(shape)) return MKV_OK;
@@ -487,7 +495,7 @@ mkv_status mkv_select_quota(const float *S, mkv_shape shape, double ratio, int32
     if (!S || !idx || !kept || !aligned(S, 4) || !aligned(idx, 4) || !aligned(kept, 4)) return MKV_ERR_INVALID_ARG;
     if (!ratio_ok(ratio) || window < 0 || keep_stride < host_num_keep_quota(shape.t_max, ratio, window))
         return MKV_ERR_INVALID_ARG;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window, shape.head_dim);
+    const Geometry g = geometry_of(shape, window);
     const Layout L = make_step_layout(g);
     if ((rc = check_ws(L, workspace, workspace_bytes)) != MKV_OK) return rc;
     if (empty(shape)) return MKV_OK;
@@ -506,9 +514,10 @@ mkv_status mkv_compress_quota(const void *K, const void *V, mkv_shape shape, dou
 
 size_t mkv_oja_workspace_size(mkv_shape shape, int32_t n_query)
 {
-    if (check_shape(shape) != MKV_OK || shape.head_dim != kHeadDim || n_query < 16 || n_query > 256 || n_query % 16)
+    if (check_shape(shape) != MKV_OK || shape.head_dim != kHeadDim || shape.dtype != MKV_DTYPE_BF16 || n_query < 16 ||
+        n_query > 256 || n_query % 16)
         return 0;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, 0, shape.head_dim);
+    const Geometry g = geometry_of(shape, 0);
     return make_layout(g).total + round_up(oja_operand_bytes(g.n_heads, n_query), kAlign);
 }
 
@@ -521,11 +530,12 @@ mkv_status oja_checks(const void *K, const void *Q, const float *U, const mkv_sh
 {
     mkv_status rc = check_shape(s);
     if (rc != MKV_OK) return rc;
-    if (s.head_dim != kHeadDim) return MKV_ERR_UNSUPPORTED;  // the contraction is built for 128 dims
+    // the contraction is built for 128 bf16 dims
+    if (s.head_dim != kHeadDim || s.dtype != MKV_DTYPE_BF16) return MKV_ERR_UNSUPPORTED;
     if (!K || !Q || (rank > 0 && !U)) return MKV_ERR_INVALID_ARG;
     if (!aligned(K, 16) || !aligned(Q, 16) || (U && !aligned(U, 16))) return MKV_ERR_INVALID_ARG;
     if (n_query < 16 || n_query > 256 || n_query % 16 || rank < 0 || rank > kHeadDim) return MKV_ERR_INVALID_ARG;
-    *g = make_geometry(s.batch, s.heads, s.t_max, 0, s.head_dim);
+    *g = geometry_of(s, 0);
     // TMA row coordinates are 32-bit
     if ((uint64_t)g->n_heads * (uint64_t)s.t_max >= (1ull << 31) ||
         (uint64_t)g->n_heads * 2u * (uint64_t)n_query >= (1ull << 31))
@@ -620,8 +630,8 @@ int32_t mkv_compress_num_stages(void) { return kCompressStages; }
 int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
 {
     if (check_shape(shape) != MKV_OK || window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE)) return -1;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window, shape.head_dim);
-    if (g.d == kHeadDim && g_single_pass_enabled.load(std::memory_order_relaxed)) {
+    const Geometry g = geometry_of(shape, window);
+    if (g.d == kHeadDim && g.es == 2 && g_single_pass_enabled.load(std::memory_order_relaxed)) {
         const int grid = single_pass_grid((int)mode);
         if (grid <= 0) return -1;
         if (grid >= g.pg.ppw) return 1;
@@ -734,7 +744,7 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
     rc = check_outputs(shape, ratio, nullptr, keep_stride, dK, dV, dK_out, dV_out, d_idx, d_kept, true);
     if (rc != MKV_OK) return rc;
     if (window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE)) return MKV_ERR_INVALID_ARG;
-    const Geometry g = make_geometry(shape.batch, shape.heads, shape.t_max, window, shape.head_dim);
+    const Geometry g = geometry_of(shape, window);
     if ((rc = check_ws(make_layout(g), workspace, workspace_bytes)) != MKV_OK) return rc;
     if (empty(shape)) return MKV_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -744,7 +754,7 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
     // rows of the batch per chunk: up to kHostChunks chunks
     const int32_t per = (shape.batch + kHostChunks - 1) / kHostChunks;
     const int32_t chunks = (shape.batch + per - 1) / per;
-    const size_t row_bytes = (size_t)shape.head_dim * 2;
+    const size_t row_bytes = (size_t)shape.head_dim * elem_bytes(shape.dtype);
     const size_t in_row = (size_t)shape.heads * shape.t_max * row_bytes;      // bytes of one batch row of K
     const size_t out_row = (size_t)shape.heads * keep_stride * row_bytes;     // of K_out
     const size_t idx_row = (size_t)shape.heads * keep_stride * sizeof(int32_t);
@@ -831,7 +841,9 @@ const char *mkv_status_string(int32_t status)
     switch (status) {
     case MKV_OK: return "MKV_OK";
     case MKV_ERR_INVALID_ARG: return "MKV_ERR_INVALID_ARG: bad argument (null or misaligned pointer, size, ratio, window or stride)";
-    case MKV_ERR_UNSUPPORTED: return "MKV_ERR_UNSUPPORTED: head_dim must be 64, 128 or 256 (128 for the OjaKV scorer) and t_max at most 2^30";
+    case MKV_ERR_UNSUPPORTED:
+        return "MKV_ERR_UNSUPPORTED: head_dim must be 64, 128 or 256, dtype bf16 or fp8 E4M3 (bf16 and 128 dims for "
+               "the OjaKV scorer) and t_max at most 2^30";
     case MKV_ERR_WORKSPACE: return "MKV_ERR_WORKSPACE: workspace missing, misaligned or smaller than mkv_workspace_size";
     case MKV_ERR_CUDA: return "MKV_ERR_CUDA: a CUDA call or kernel launch failed";
     case MKV_ERR_DEVICE: return "MKV_ERR_DEVICE: a kernel reported bad device-side input (see the status bits)";

@@ -52,6 +52,70 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float f[8])
     }
 }
 
+// Eight E4M3 codes (OCP 8-bit floating point, E4M3: sign, 4 exponent bits
+// with bias 7, 3 mantissa bits, subnormals at exponent field 0), widened
+// exactly to fp32. Code b read as the fp32 pattern (b & 0x7F) << 20 with its
+// sign moved to bit 31 has the same exponent field and mantissa bits, so its
+// value is the code's value times 2^-120 (also for the subnormal codes, which
+// land on fp32 subnormals); one multiplication by 2^120 without flush to
+// zero restores it exactly. The NaN codes are outside the contract (they
+// decode to +-480).
+__device__ __forceinline__ float e4m3_scaled(uint32_t pattern)
+{
+    float r;
+    asm("mul.rn.f32 %0, %1, 0f7B800000;" : "=f"(r) : "f"(__uint_as_float(pattern)));  // * 2^120
+    return r;
+}
+
+__device__ __forceinline__ void e4m3x8_to_f32(const uint2 v, float f[8])
+{
+    const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t x = w[i];
+        f[4 * i + 0] = e4m3_scaled(((x & 0x7Fu) << 20) | ((x & 0x80u) << 24));
+        f[4 * i + 1] = e4m3_scaled(((x & 0x7F00u) << 12) | ((x & 0x8000u) << 16));
+        f[4 * i + 2] = e4m3_scaled(((x & 0x7F0000u) << 4) | ((x & 0x800000u) << 8));
+        f[4 * i + 3] = e4m3_scaled(((x >> 4) & 0x07F00000u) | (x & 0x80000000u));
+    }
+}
+
+__device__ __forceinline__ uint2 ld_stream8(const void *p)
+{
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+// A cache row split into chunks of 8 consecutive elements: 16 bytes of bf16
+// (ES = 2) or 8 bytes of E4M3 (ES = 1). Lane q of a row's 8 lanes takes the
+// chunks at elements 64k + 8q, k < d / 64, whatever the element type.
+template <int ES>
+struct Chunk;
+
+__device__ __forceinline__ uint2 ld_nc8(const void *p)
+{
+    uint2 r;
+    asm("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+template <>
+struct Chunk<2> {
+    using raw = uint4;
+    static __device__ __forceinline__ raw load(const void *p) { return ld_stream(p); }
+    static __device__ __forceinline__ raw load_l1(const void *p) { return ld_nc(p); }
+    static __device__ __forceinline__ void to_f32(const raw &v, float f[8]) { bf16x8_to_f32(v, f); }
+};
+
+template <>
+struct Chunk<1> {
+    using raw = uint2;
+    static __device__ __forceinline__ raw load(const void *p) { return ld_stream8(p); }
+    static __device__ __forceinline__ raw load_l1(const void *p) { return ld_nc8(p); }
+    static __device__ __forceinline__ void to_f32(const raw &v, float f[8]) { e4m3x8_to_f32(v, f); }
+};
+
 // Sum over the 16 lanes of a half-warp (all 32 lanes must call it).
 __device__ __forceinline__ float half_warp_sum(float v)
 {

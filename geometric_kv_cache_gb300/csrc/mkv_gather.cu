@@ -20,8 +20,8 @@ namespace {
 constexpr int kStreamThreads = 256;
 using namespace dev;
 
-// Item = (head, block of 64 output slots). Groups of LPR lanes (LPR = d / 8:
-// 16 bytes per lane) copy rows: K_out[h][j] = K[h][idx[h][j]], V_out
+// Item = (head, block of 64 output slots). Groups of LPR lanes (LPR = row
+// bytes / 16: 16 bytes per lane) copy rows: K_out[h][j] = K[h][idx[h][j]], V_out
 // likewise, for j < kept[h]; 64 / (256 / LPR) rows of K and of V in flight
 // per lane. No CTA barrier anywhere.
 constexpr int kGatherRows = 64;
@@ -75,12 +75,14 @@ k_gather_rows(const int32_t *__restrict__ idx, int idx_stride, const int32_t *__
     }
 }
 
-const void *gather_fn(int d)
+// The kernel for a row of `row_bytes` bytes (head dim x element size).
+const void *gather_fn(int row_bytes)
 {
-    switch (d) {
-    case 64: return (const void *)k_gather_rows<8>;
-    case 128: return (const void *)k_gather_rows<16>;
-    case 256: return (const void *)k_gather_rows<32>;
+    switch (row_bytes) {
+    case 64: return (const void *)k_gather_rows<4>;
+    case 128: return (const void *)k_gather_rows<8>;
+    case 256: return (const void *)k_gather_rows<16>;
+    case 512: return (const void *)k_gather_rows<32>;
     default: return nullptr;
     }
 }
@@ -94,7 +96,7 @@ cudaError_t launch_gather(const Geometry &g, const int32_t *idx, int32_t idx_str
     const int bph = (keep_stride + kGatherRows - 1) / kGatherRows;
     const int64_t items = g.n_heads * bph;
     if (items == 0) return cudaSuccess;
-    const void *fn = gather_fn(g.d);
+    const void *fn = gather_fn(g.d * g.es);
     if (!fn) return cudaErrorInvalidValue;
     const int grid = grid_for_items(fn, kStreamThreads, 0, items);
     int t_max = g.t_max;

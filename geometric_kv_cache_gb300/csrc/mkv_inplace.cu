@@ -31,14 +31,14 @@ constexpr int kInplaceRows = 64;  // output slots per chunk
 
 // One chunk of a lane group's rows: R rows of K and V, their destinations.
 template <int R>
-struct Chunk {
+struct MoveChunk {
     uint4 k[R], v[R];
     int dst[R];  // destination row, or -1 (no slot, or the row is already in place)
 };
 
 // Groups of LPR lanes (16 bytes each) cover a row of RB = 16 LPR bytes.
 template <int LPR>
-__device__ __forceinline__ void inplace_load(Chunk<kInplaceRows * LPR / kStreamThreads> &c, int chunk, int n, int T,
+__device__ __forceinline__ void inplace_load(MoveChunk<kInplaceRows * LPR / kStreamThreads> &c, int chunk, int n, int T,
                                              const int32_t *ih, const uint8_t *Kh, const uint8_t *Vh, int hw,
                                              uint32_t *status)
 {
@@ -61,7 +61,7 @@ __device__ __forceinline__ void inplace_load(Chunk<kInplaceRows * LPR / kStreamT
 }
 
 template <int LPR>
-__device__ __forceinline__ void inplace_store(const Chunk<kInplaceRows * LPR / kStreamThreads> &c, uint8_t *Kh,
+__device__ __forceinline__ void inplace_store(const MoveChunk<kInplaceRows * LPR / kStreamThreads> &c, uint8_t *Kh,
                                               uint8_t *Vh)
 {
     constexpr int RB = LPR * 16, R = kInplaceRows * LPR / kStreamThreads;
@@ -99,7 +99,7 @@ k_gather_inplace(const int32_t *__restrict__ idx, int idx_stride, const int32_t 
         uint8_t *Kh = K + (size_t)head * t_max * RB + lr * 16;
         uint8_t *Vh = V + (size_t)head * t_max * RB + lr * 16;
         const int nch = (n + kInplaceRows - 1) / kInplaceRows;
-        Chunk<R> a, b;
+        MoveChunk<R> a, b;
         inplace_load<LPR>(a, 0, n, T, ih, Kh, Vh, hw, status);
         for (int c = 0; c < nch; c += 2) {
             __syncthreads();  // chunk c's loads are performed CTA-wide
@@ -114,12 +114,14 @@ k_gather_inplace(const int32_t *__restrict__ idx, int idx_stride, const int32_t 
     }
 }
 
-const void *inplace_fn(int d)
+// The kernel for a row of `row_bytes` bytes (head dim x element size).
+const void *inplace_fn(int row_bytes)
 {
-    switch (d) {
-    case 64: return (const void *)k_gather_inplace<8>;
-    case 128: return (const void *)k_gather_inplace<16>;
-    case 256: return (const void *)k_gather_inplace<32>;
+    switch (row_bytes) {
+    case 64: return (const void *)k_gather_inplace<4>;
+    case 128: return (const void *)k_gather_inplace<8>;
+    case 256: return (const void *)k_gather_inplace<16>;
+    case 512: return (const void *)k_gather_inplace<32>;
     default: return nullptr;
     }
 }
@@ -130,7 +132,7 @@ cudaError_t launch_gather_inplace(const Geometry &g, const int32_t *idx, int32_t
                                   const int32_t *seq_lens, void *K, void *V, uint32_t *status, cudaStream_t st)
 {
     if (g.n_heads == 0) return cudaSuccess;
-    const void *fn = inplace_fn(g.d);
+    const void *fn = inplace_fn(g.d * g.es);
     if (!fn) return cudaErrorInvalidValue;
     const int grid = grid_for_items(fn, kStreamThreads, 0, g.n_heads);
     int heads = g.heads, t_max = g.t_max;

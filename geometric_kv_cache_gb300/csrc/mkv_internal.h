@@ -14,6 +14,8 @@ constexpr int kHeadDim = 128;          // the head dim of the single-pass and Oj
 constexpr int kRowBytes = kHeadDim * 2;  // one bf16 row at that head dim
 // head dims the streaming kernels support (rows of 128, 256, 512 bytes)
 constexpr bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+// bytes per cache element of an mkv_dtype (0: not a supported type)
+constexpr int elem_bytes(int32_t dtype) { return dtype == MKV_DTYPE_BF16 ? 2 : dtype == MKV_DTYPE_FP8_E4M3 ? 1 : 0; }
 constexpr int kCompactChunk = 4096;    // tokens per compaction CTA (256 threads x 16)
 constexpr int kStageRows = 64;         // piece lengths are multiples of this
 constexpr int kMinPieceRows = 256;     // pieces are 256 * 2^k tokens (a window shorter than that is one piece) ...
@@ -32,6 +34,7 @@ struct PieceGeometry {
     int32_t t_max = 0;
     int32_t window = 0;    // 0 = global
     int32_t d = kHeadDim;  // head dim (64, 128 or 256)
+    int32_t es = 2;        // bytes per cache element (2 bf16, 1 E4M3)
     int32_t nwin_max = 0;  // windows of a head of t_max tokens
     int32_t piece_rows = 0;  // tokens per piece (256 * 2^k)
     int32_t ppw = 0;       // pieces per window (upper bound)
@@ -45,6 +48,7 @@ struct Geometry {
     int32_t t_max = 0;
     int32_t nch = 0;       // compaction chunks per head (upper bound)
     int32_t d = kHeadDim;  // head dim
+    int32_t es = 2;        // bytes per cache element
 };
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
@@ -53,7 +57,8 @@ struct Layout {
            idx = 0, total = 0;
 };
 
-Geometry make_geometry(int32_t batch, int32_t heads, int32_t t_max, int32_t window, int32_t head_dim = kHeadDim);
+Geometry make_geometry(int32_t batch, int32_t heads, int32_t t_max, int32_t window, int32_t head_dim = kHeadDim,
+                       int32_t es = 2);
 Layout make_layout(const Geometry &g);
 
 // Occupancy helpers (kernels loop over their items, persistent style).

@@ -265,12 +265,12 @@ __device__ __forceinline__ void load_centroid(const float *cw, float c[8 * NB])
     }
 }
 
-// The thread's 8 * NB dims of a row from its NB 16-byte chunks.
-template <int NB = 2>
-__device__ __forceinline__ void row_to_f32(const uint4 *v, float f[8 * NB])
+// The thread's 8 * NB dims of a row from its NB chunks (ES: element bytes).
+template <int NB = 2, int ES = 2>
+__device__ __forceinline__ void row_to_f32(const typename Chunk<ES>::raw *v, float f[8 * NB])
 {
 #pragma unroll
-    for (int k = 0; k < NB; ++k) bf16x8_to_f32(v[k], f + 8 * k);
+    for (int k = 0; k < NB; ++k) Chunk<ES>::to_f32(v[k], f + 8 * k);
 }
 
 // Sum of n (<= kGroupPieces) consecutive D-float records, record order,
@@ -302,18 +302,18 @@ struct Pointers {
 // ------------------------------------------------------------- kernels --
 
 // Rows r = slot + 32 * (i0 + u), u < N, of a piece starting at `base`
-// (this thread's NB 16-byte chunks of each, chunk k of row u at v[NB u + k]),
-// loaded before use.
-template <int N, int NB = 2>
-__device__ __forceinline__ void load_rows(const uint8_t *base, int len, int i0, uint4 v[NB * N])
+// (this thread's NB chunks of 8 elements of ES bytes each, elements 64k + 8q;
+// chunk k of row u at v[NB u + k]), loaded before use.
+template <int N, int NB = 2, int ES = 2>
+__device__ __forceinline__ void load_rows(const uint8_t *base, int len, int i0, typename Chunk<ES>::raw v[NB * N])
 {
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
 #pragma unroll
     for (int u = 0; u < N; ++u) {
         const int r = slot + (i0 + u) * kRowSlots;
-        const uint8_t *row = base + (size_t)(r < len ? r : 0) * (128 * NB);
+        const uint8_t *row = base + (size_t)(r < len ? r : 0) * (64 * NB * ES);
 #pragma unroll
-        for (int k = 0; k < NB; ++k) v[NB * u + k] = ld_stream(row + 128 * k + q * 16);
+        for (int k = 0; k < NB; ++k) v[NB * u + k] = Chunk<ES>::load(row + (64 * k + 8 * q) * ES);
     }
 }
 
@@ -325,17 +325,18 @@ __host__ __device__ constexpr int batch_rows() { return 8 / NB; }
 // a1, first half: piece sums. The first batch of the next piece is loaded
 // before the current piece's CTA reduction, so the loads stay in flight
 // across piece boundaries.
-template <int NB>
+template <int NB, int ES>
 __global__ void __launch_bounds__(kThreads, NB > 2 ? 2 : 3)
 k_piece_sums(PieceGeometry g, Pointers P)
 {
-    constexpr int D = 64 * NB, RB = 2 * D, B = batch_rows<NB>();
+    constexpr int D = 64 * NB, RB = ES * D, B = batch_rows<NB>();
+    using Raw = typename Chunk<ES>::raw;
     __shared__ float red[kWarps * D];
     const Steps st = make_steps(g);
     const int slot = threadIdx.x >> 3;
     Cursor cur = first_cursor(g, st, P.seq_lens, P.status);
-    uint4 v[NB * B];
-    if (!cur.done) load_rows<B, NB>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
+    Raw v[NB * B];
+    if (!cur.done) load_rows<B, NB, ES>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
     while (!cur.done) {
         const Piece pc = cur.pc;
         const int64_t item = cursor_item(cur, st);
@@ -349,15 +350,15 @@ k_piece_sums(PieceGeometry g, Pointers P)
             for (int u = 0; u < B; ++u) {
                 if (slot + (i0 + u) * kRowSlots < pc.len) {
                     float f[8 * NB];
-                    row_to_f32<NB>(v + NB * u, f);
+                    row_to_f32<NB, ES>(v + NB * u, f);
 #pragma unroll
                     for (int j = 0; j < 8 * NB; ++j) acc[j] += f[j];
                 }
             }
-            if (i0 + B < nrows) load_rows<B, NB>(base, pc.len, i0 + B, v);
+            if (i0 + B < nrows) load_rows<B, NB, ES>(base, pc.len, i0 + B, v);
         }
         advance(cur, st, g, P.seq_lens, P.status);
-        if (!cur.done) load_rows<B, NB>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
+        if (!cur.done) load_rows<B, NB, ES>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
         finish_sum<NB>(acc, red, P.partial + item * D);
         __syncthreads();  // red is free again
     }
@@ -393,16 +394,17 @@ k_window_means(PieceGeometry g, Pointers P)
 // a2: scores of every piece against its window's mean in C. As in
 // k_piece_sums, the next piece's first batch is loaded as soon as the current
 // piece's last batch is consumed, before the next centroid is read.
-template <int MODE, int NB>
+template <int MODE, int NB, int ES>
 __global__ void __launch_bounds__(kThreads, NB > 2 ? 2 : 3)
 k_piece_scores(PieceGeometry g, Pointers P)
 {
-    constexpr int D = 64 * NB, RB = 2 * D, B = batch_rows<NB>();
+    constexpr int D = 64 * NB, RB = ES * D, B = batch_rows<NB>();
+    using Raw = typename Chunk<ES>::raw;
     const Steps st = make_steps(g);
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
     Cursor cur = first_cursor(g, st, P.seq_lens, P.status);
-    uint4 v[NB * B];
-    if (!cur.done) load_rows<B, NB>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
+    Raw v[NB * B];
+    if (!cur.done) load_rows<B, NB, ES>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
     while (!cur.done) {
         const Piece pc = cur.pc;
         const uint8_t *base = P.K + ((size_t)pc.head * g.t_max + pc.a) * RB;
@@ -416,15 +418,15 @@ k_piece_scores(PieceGeometry g, Pointers P)
             for (int u = 0; u < B; ++u) {
                 const int r = slot + (i0 + u) * kRowSlots;
                 float f[8 * NB];
-                row_to_f32<NB>(v + NB * u, f);
+                row_to_f32<NB, ES>(v + NB * u, f);
                 const float s = score_of<MODE, NB>(f, c, nc);
                 if (r < pc.len && q == 0) srow[r] = s;
             }
-            if (i0 + B < nrows) load_rows<B, NB>(base, pc.len, i0 + B, v);
+            if (i0 + B < nrows) load_rows<B, NB, ES>(base, pc.len, i0 + B, v);
         }
         // the next piece's first batch goes out before its centroid is read
         advance(cur, st, g, P.seq_lens, P.status);
-        if (!cur.done) load_rows<B, NB>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
+        if (!cur.done) load_rows<B, NB, ES>(P.K + ((size_t)cur.pc.head * g.t_max + cur.pc.a) * RB, cur.pc.len, 0, v);
     }
 }
 
@@ -813,8 +815,13 @@ k_single_pass(PieceGeometry g, FusedPointers F)
 
 // ------------------------------------------------------ head groups --
 
-// 16-byte non-coherent load carrying an L2 eviction policy (createpolicy).
-__device__ __forceinline__ uint4 ld_policy(const void *p, uint64_t pol)
+// Non-coherent load of one chunk (16 bytes of bf16, 8 of E4M3) carrying an
+// L2 eviction policy (createpolicy).
+template <int ES>
+__device__ __forceinline__ typename Chunk<ES>::raw ld_policy(const void *p, uint64_t pol);
+
+template <>
+__device__ __forceinline__ uint4 ld_policy<2>(const void *p, uint64_t pol)
 {
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
@@ -823,17 +830,28 @@ __device__ __forceinline__ uint4 ld_policy(const void *p, uint64_t pol)
     return r;
 }
 
+template <>
+__device__ __forceinline__ uint2 ld_policy<1>(const void *p, uint64_t pol)
+{
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+        : "=r"(r.x), "=r"(r.y)
+        : "l"(p), "l"(pol));
+    return r;
+}
+
 // load_rows with an L2 eviction policy on every load.
-template <int N, int NB>
-__device__ __forceinline__ void load_rows_policy(const uint8_t *base, int len, int i0, uint4 v[NB * N], uint64_t pol)
+template <int N, int NB, int ES>
+__device__ __forceinline__ void load_rows_policy(const uint8_t *base, int len, int i0,
+                                                 typename Chunk<ES>::raw v[NB * N], uint64_t pol)
 {
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
 #pragma unroll
     for (int u = 0; u < N; ++u) {
         const int r = slot + (i0 + u) * kRowSlots;
-        const uint8_t *row = base + (size_t)(r < len ? r : 0) * (128 * NB);
+        const uint8_t *row = base + (size_t)(r < len ? r : 0) * (64 * NB * ES);
 #pragma unroll
-        for (int k = 0; k < NB; ++k) v[NB * u + k] = ld_policy(row + 128 * k + q * 16, pol);
+        for (int k = 0; k < NB; ++k) v[NB * u + k] = ld_policy<ES>(row + (64 * k + 8 * q) * ES, pol);
     }
 }
 //
@@ -866,11 +884,12 @@ static_assert(kMaxUnitWindows * kMaxDim * sizeof(float) <= kGroupSmem, "means mu
 __host__ __device__ constexpr int stash_slots(int D) { return (int)(kGroupSmem / sizeof(float)) / (kWarps * D); }
 constexpr int kMaxSlots = stash_slots(64);
 
-template <int MODE, int NB>
+template <int MODE, int NB, int ES>
 __global__ void __launch_bounds__(kThreads, 2)
 k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
 {
-    constexpr int D = 64 * NB, RB = 2 * D;
+    constexpr int D = 64 * NB, RB = ES * D;
+    using Raw = typename Chunk<ES>::raw;
     constexpr int kBatchG = 16 / NB;  // rows per lane in flight (256 bytes per lane for every head dim)
     constexpr int kSlots = stash_slots(D);
     extern __shared__ float dyn[];    // pass 1: stash [kSlots][kWarps][D]; pass 2: means [wb][D]
@@ -925,13 +944,13 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
 #pragma unroll
             for (int j = 0; j < 8 * NB; ++j) acc[j] = 0.f;
             for (int i0 = 0; i0 < nrows; i0 += kBatchG) {
-                uint4 v[NB * kBatchG];
-                load_rows_policy<kBatchG, NB>(base, len, i0, v, keep_l2);
+                Raw v[NB * kBatchG];
+                load_rows_policy<kBatchG, NB, ES>(base, len, i0, v, keep_l2);
 #pragma unroll
                 for (int u = 0; u < kBatchG; ++u) {
                     if (slot + (i0 + u) * kRowSlots < len) {
                         float fr[8 * NB];
-                        row_to_f32<NB>(v + NB * u, fr);
+                        row_to_f32<NB, ES>(v + NB * u, fr);
 #pragma unroll
                         for (int j = 0; j < 8 * NB; ++j) acc[j] += fr[j];
                     }
@@ -1017,13 +1036,13 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
                 float *srow = P.S + (size_t)head * g.t_max + wstart + off;
                 const int nrows = (len + kRowSlots - 1) / kRowSlots;
                 for (int i0 = 0; i0 < nrows; i0 += kBatchG) {
-                    uint4 v[NB * kBatchG];
-                    load_rows_policy<kBatchG, NB>(base, len, i0, v, drop_l2);
+                    Raw v[NB * kBatchG];
+                    load_rows_policy<kBatchG, NB, ES>(base, len, i0, v, drop_l2);
 #pragma unroll
                     for (int u = 0; u < kBatchG; ++u) {
                         const int r = slot + (i0 + u) * kRowSlots;
                         float fr[8 * NB];
-                        row_to_f32<NB>(v + NB * u, fr);
+                        row_to_f32<NB, ES>(v + NB * u, fr);
                         const float sc = score_of<MODE, NB>(fr, c, nc);
                         if (r < len && q == 0) srow[r] = sc;
                     }
@@ -1089,37 +1108,55 @@ cudaError_t launch_single_pass(const PieceGeometry &g, int grid, const void *K, 
 namespace {
 
 
-// The kernel instance for a head dim (64 * NB) and mode.
-const void *head_groups_fn(int d, int mode)
+// The kernel instance for a head dim (64 * NB), element size and mode.
+template <int ES>
+const void *head_groups_fn_es(int d, int mode)
 {
     const bool l2 = mode == MKV_MODE_L2;
     switch (d) {
-    case 64: return l2 ? (const void *)k_head_groups<MKV_MODE_L2, 1> : (const void *)k_head_groups<MKV_MODE_COSINE, 1>;
-    case 128: return l2 ? (const void *)k_head_groups<MKV_MODE_L2, 2> : (const void *)k_head_groups<MKV_MODE_COSINE, 2>;
-    case 256: return l2 ? (const void *)k_head_groups<MKV_MODE_L2, 4> : (const void *)k_head_groups<MKV_MODE_COSINE, 4>;
+    case 64: return l2 ? (const void *)k_head_groups<MKV_MODE_L2, 1, ES> : (const void *)k_head_groups<MKV_MODE_COSINE, 1, ES>;
+    case 128: return l2 ? (const void *)k_head_groups<MKV_MODE_L2, 2, ES> : (const void *)k_head_groups<MKV_MODE_COSINE, 2, ES>;
+    case 256: return l2 ? (const void *)k_head_groups<MKV_MODE_L2, 4, ES> : (const void *)k_head_groups<MKV_MODE_COSINE, 4, ES>;
     default: return nullptr;
     }
 }
 
-const void *piece_scores_fn(int d, int mode)
+const void *head_groups_fn(int d, int es, int mode)
+{
+    return es == 2 ? head_groups_fn_es<2>(d, mode) : es == 1 ? head_groups_fn_es<1>(d, mode) : nullptr;
+}
+
+template <int ES>
+const void *piece_scores_fn_es(int d, int mode)
 {
     const bool l2 = mode == MKV_MODE_L2;
     switch (d) {
-    case 64: return l2 ? (const void *)k_piece_scores<MKV_MODE_L2, 1> : (const void *)k_piece_scores<MKV_MODE_COSINE, 1>;
-    case 128: return l2 ? (const void *)k_piece_scores<MKV_MODE_L2, 2> : (const void *)k_piece_scores<MKV_MODE_COSINE, 2>;
-    case 256: return l2 ? (const void *)k_piece_scores<MKV_MODE_L2, 4> : (const void *)k_piece_scores<MKV_MODE_COSINE, 4>;
+    case 64: return l2 ? (const void *)k_piece_scores<MKV_MODE_L2, 1, ES> : (const void *)k_piece_scores<MKV_MODE_COSINE, 1, ES>;
+    case 128: return l2 ? (const void *)k_piece_scores<MKV_MODE_L2, 2, ES> : (const void *)k_piece_scores<MKV_MODE_COSINE, 2, ES>;
+    case 256: return l2 ? (const void *)k_piece_scores<MKV_MODE_L2, 4, ES> : (const void *)k_piece_scores<MKV_MODE_COSINE, 4, ES>;
     default: return nullptr;
     }
 }
 
-const void *piece_sums_fn(int d)
+const void *piece_scores_fn(int d, int es, int mode)
+{
+    return es == 2 ? piece_scores_fn_es<2>(d, mode) : es == 1 ? piece_scores_fn_es<1>(d, mode) : nullptr;
+}
+
+template <int ES>
+const void *piece_sums_fn_es(int d)
 {
     switch (d) {
-    case 64: return (const void *)k_piece_sums<1>;
-    case 128: return (const void *)k_piece_sums<2>;
-    case 256: return (const void *)k_piece_sums<4>;
+    case 64: return (const void *)k_piece_sums<1, ES>;
+    case 128: return (const void *)k_piece_sums<2, ES>;
+    case 256: return (const void *)k_piece_sums<4, ES>;
     default: return nullptr;
     }
+}
+
+const void *piece_sums_fn(int d, int es)
+{
+    return es == 2 ? piece_sums_fn_es<2>(d) : es == 1 ? piece_sums_fn_es<1>(d) : nullptr;
 }
 
 const void *window_means_fn(int d)
@@ -1138,7 +1175,7 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
 {
     HeadGroupPlan plan;
     if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max == 0) return plan;
-    const void *fn = head_groups_fn(g.d, mode);
+    const void *fn = head_groups_fn(g.d, g.es, mode);
     if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
         return plan;
     const int resident = resident_grid(fn, kThreads, kGroupSmem);
@@ -1154,7 +1191,7 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
     // three-kernel path keeps more SMs busy).
     const int wl_max = (g.window <= 0 || g.window >= g.t_max) ? g.t_max : g.window;
     if (wl_max < kMinPieceRows) return plan;  // windows shorter than a piece: barrier-bound rounds
-    const double window_bytes = (double)wl_max * 2.0 * g.d;
+    const double window_bytes = (double)wl_max * g.es * g.d;
     const double budget = 0.6 * (double)l2;
     double best = 0.0;
     for (int wb = 1; wb <= std::min(g.nwin_max, kMaxUnitWindows); ++wb) {
@@ -1182,7 +1219,7 @@ cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan
                                const int32_t *seq_lens, int mode, float *partial, uint32_t *cnt, float *C, float *S,
                                uint32_t *status, cudaStream_t st)
 {
-    const void *fn = head_groups_fn(g.d, mode);
+    const void *fn = head_groups_fn(g.d, g.es, mode);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(cnt, 0, (size_t)plan.groups * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
@@ -1198,7 +1235,7 @@ cudaError_t launch_piece_sums(const PieceGeometry &g, const void *K, const int32
                               uint32_t *status, cudaStream_t st)
 {
     if (g.n_items == 0) return cudaSuccess;
-    const void *fn = piece_sums_fn(g.d);
+    const void *fn = piece_sums_fn(g.d, g.es);
     if (!fn) return cudaErrorInvalidValue;
     const int grid = grid_for_items(fn, kThreads, 0, g.n_items);
     PieceGeometry gg = g;
@@ -1224,7 +1261,7 @@ cudaError_t launch_piece_scores(const PieceGeometry &g, const void *K, const flo
                                 int mode, float *S, uint32_t *status, cudaStream_t st)
 {
     if (g.n_items == 0) return cudaSuccess;
-    const void *fn = piece_scores_fn(g.d, mode);
+    const void *fn = piece_scores_fn(g.d, g.es, mode);
     if (!fn) return cudaErrorInvalidValue;
     const int grid = grid_for_items(fn, kThreads, 0, g.n_items);
     PieceGeometry gg = g;

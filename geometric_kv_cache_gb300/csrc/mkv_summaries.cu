@@ -1,5 +1,5 @@
-// sm_103a cluster summaries: per-window means of a bf16 cache (keys or
-// values) for short windows, with each window's radius.
+// sm_103a cluster summaries: per-window means of a cache (keys or values,
+// bf16 or E4M3) for short windows, with each window's radius.
 //
 // "RefineKV: Query-Adaptive KV Cache Compression via Attention-Error Bounds"
 // (project page), method overview, step 1 (Summarize): the cache is cut
@@ -12,7 +12,7 @@
 //
 // Layout: one window per 8-lane group. Lane q of a group owns dims
 // [64k + 8q, 64k + 8q + 8) of every row for k < d/64 (one 16-byte load per
-// 64 dims, each group reading whole 128-byte lines). Sums run per dim in token order
+// 64 bf16 dims, 8-byte for E4M3, each group reading whole lines). Sums run per dim in token order
 // in fp32, so no lane talks to another for the mean. The radius pass re-reads
 // the window's rows (from L1/L2), sums its 16 squared offsets per lane, then
 // sums over the group with an xor butterfly (the same bits on every lane).
@@ -30,24 +30,25 @@ constexpr int kWindowsPerCta = kSumThreads / 8;
 constexpr int kBatchRows = 4;  // rows in flight per lane
 using namespace dev;
 
-// This lane's NB 16-byte chunks of a row (chunk k at byte 128k of the lane's
-// first chunk).
-template <int NB>
-__device__ __forceinline__ void load_row(const uint8_t *row, uint4 (&v)[NB])
+// This lane's NB chunks of 8 elements of a row (chunk k at element 64k of
+// the lane's first chunk).
+template <int NB, int ES>
+__device__ __forceinline__ void load_row(const uint8_t *row, typename Chunk<ES>::raw (&v)[NB])
 {
 #pragma unroll
-    for (int k = 0; k < NB; ++k) v[k] = ld_nc(row + 128 * k);
+    for (int k = 0; k < NB; ++k) v[k] = Chunk<ES>::load_l1(row + 64 * ES * k);
 }
 
 // Lane q of a window's group owns dims [64k + 8q, 64k + 8q + 8), k < NB
 // (head dim 64 NB).
-template <int NB>
+template <int NB, int ES>
 __global__ void __launch_bounds__(kSumThreads)
 k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ seq_lens, int heads, int t_max,
                      int window, int nwin_max, int64_t n_items, float *__restrict__ mean,
                      float *__restrict__ radius, uint32_t *status)
 {
-    constexpr int D = 64 * NB, RB = 2 * D;
+    constexpr int D = 64 * NB, RB = ES * D;
+    using Raw = typename Chunk<ES>::raw;
     const int grp = threadIdx.x >> 3, q = threadIdx.x & 7;
     for (int64_t base = (int64_t)blockIdx.x * kWindowsPerCta; base < n_items;
          base += (int64_t)gridDim.x * kWindowsPerCta) {
@@ -61,24 +62,24 @@ k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ 
             const int T = head_len(seq_lens, head, heads, t_max, status, q == 0 && j == 0);
             n = min(window, T - j * window);
         }
-        const uint8_t *row0 = X + ((size_t)head * t_max + (size_t)j * window) * RB + q * 16;
+        const uint8_t *row0 = X + ((size_t)head * t_max + (size_t)j * window) * RB + q * 8 * ES;
         float m[8 * NB] = {0.f};
         if (n > 0) {
             float acc[8 * NB];
 #pragma unroll
             for (int i = 0; i < 8 * NB; ++i) acc[i] = 0.f;
             for (int t0 = 0; t0 < n; t0 += kBatchRows) {
-                uint4 v[kBatchRows][NB];
+                Raw v[kBatchRows][NB];
 #pragma unroll
                 for (int u = 0; u < kBatchRows; ++u)
-                    if (t0 + u < n) load_row<NB>(row0 + (size_t)(t0 + u) * RB, v[u]);
+                    if (t0 + u < n) load_row<NB, ES>(row0 + (size_t)(t0 + u) * RB, v[u]);
 #pragma unroll
                 for (int u = 0; u < kBatchRows; ++u) {
                     if (t0 + u < n) {
 #pragma unroll
                         for (int k = 0; k < NB; ++k) {
                             float f[8];
-                            bf16x8_to_f32(v[u][k], f);
+                            Chunk<ES>::to_f32(v[u][k], f);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) acc[8 * k + i] += f[i];
                         }
@@ -101,10 +102,10 @@ k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ 
             const int n_warp = __reduce_max_sync(kFull, (unsigned)max(n, 0));
             float rmax = 0.f;
             for (int t0 = 0; t0 < n_warp; t0 += kBatchRows) {
-                uint4 v[kBatchRows][NB];
+                Raw v[kBatchRows][NB];
 #pragma unroll
                 for (int u = 0; u < kBatchRows; ++u)
-                    if (t0 + u < n) load_row<NB>(row0 + (size_t)(t0 + u) * RB, v[u]);
+                    if (t0 + u < n) load_row<NB, ES>(row0 + (size_t)(t0 + u) * RB, v[u]);
 #pragma unroll
                 for (int u = 0; u < kBatchRows; ++u) {
                     float ss = 0.f;
@@ -112,7 +113,7 @@ k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ 
 #pragma unroll
                         for (int k = 0; k < NB; ++k) {
                             float f[8];
-                            bf16x8_to_f32(v[u][k], f);
+                            Chunk<ES>::to_f32(v[u][k], f);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
                                 const float dlt = f[i] - m[8 * k + i];
@@ -131,14 +132,20 @@ k_small_window_means(const uint8_t *__restrict__ X, const int32_t *__restrict__ 
     }
 }
 
-const void *small_window_means_fn(int d)
+template <int ES>
+const void *small_window_means_fn_es(int d)
 {
     switch (d) {
-    case 64: return (const void *)k_small_window_means<1>;
-    case 128: return (const void *)k_small_window_means<2>;
-    case 256: return (const void *)k_small_window_means<4>;
+    case 64: return (const void *)k_small_window_means<1, ES>;
+    case 128: return (const void *)k_small_window_means<2, ES>;
+    case 256: return (const void *)k_small_window_means<4, ES>;
     default: return nullptr;
     }
+}
+
+const void *small_window_means_fn(int d, int es)
+{
+    return es == 2 ? small_window_means_fn_es<2>(d) : es == 1 ? small_window_means_fn_es<1>(d) : nullptr;
 }
 
 }  // namespace
@@ -148,7 +155,7 @@ cudaError_t launch_small_window_means(const PieceGeometry &g, const void *X, con
 {
     const int64_t items = g.n_heads * g.nwin_max;
     if (items == 0) return cudaSuccess;
-    const void *fn = small_window_means_fn(g.d);
+    const void *fn = small_window_means_fn(g.d, g.es);
     if (!fn) return cudaErrorInvalidValue;
     const int grid = grid_for_items(fn, kSumThreads, 0, (items + kWindowsPerCta - 1) / kWindowsPerCta);
     const uint8_t *Xb = static_cast<const uint8_t *>(X);

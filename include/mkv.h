@@ -13,9 +13,14 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- * Cache layout. A cache is bf16 [batch, heads, t_max, head_dim], head_dim
- *   innermost and contiguous (one 2*head_dim-byte row per token: 128, 256 or
- *   512 bytes at head_dim 64, 128, 256).
+ * Cache layout. A cache is [batch, heads, t_max, head_dim] of bf16 or of
+ *   fp8 E4M3 codes (shape.dtype), head_dim innermost and contiguous (one row
+ *   of head_dim elements per token: 128, 256 or 512 bytes at head_dim 64,
+ *   128, 256 in bf16, half that in E4M3). Keys and values share the type;
+ *   centroids, scores and summaries are fp32 on the decoded values (E4M3
+ *   decodes exactly). A per-tensor scale that the caller keeps beside an
+ *   E4M3 cache changes no kept set: l2 scores scale with it and cosine scores
+ *   do not change; C, S and means come out in stored units.
  *   "batch" counts (layer, sequence) rows: callers fold layers into it, so a
  *   "head" is one (layer, sequence, KV head) triple, and every head is
  *   processed independently. Head h = b*heads + j covers tokens
@@ -49,8 +54,8 @@
  *   that shape and window. The status word must be zero before the first
  *   call (allocate the workspace zeroed, or call mkv_device_status once).
  *   Calls that share a workspace must not overlap on the GPU.
- * Supported. head_dim 64, 128 or 256 (else MKV_ERR_UNSUPPORTED; the OjaKV
- *   scorer needs 128); t_max <= 2^30.
+ * Supported. head_dim 64, 128 or 256 and dtype bf16 or E4M3 (else
+ *   MKV_ERR_UNSUPPORTED; the OjaKV scorer needs 128 and bf16); t_max <= 2^30.
  *   Scores must not be NaN (inputs with NaN/Inf are outside the contract).
  */
 #ifndef MKV_H_
@@ -69,7 +74,7 @@ typedef struct CUstream_st *mkv_stream_t;
 typedef enum {
     MKV_OK = 0,
     MKV_ERR_INVALID_ARG = 1, /* null / misaligned pointer, negative size, ratio outside [0,1], ... */
-    MKV_ERR_UNSUPPORTED = 2, /* head_dim other than 64/128/256 (128 for OjaKV), t_max above 2^30 */
+    MKV_ERR_UNSUPPORTED = 2, /* head_dim other than 64/128/256, an unknown dtype (OjaKV: 128, bf16), t_max above 2^30 */
     MKV_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than required */
     MKV_ERR_CUDA = 4,        /* a CUDA call or launch failed */
     MKV_ERR_DEVICE = 5       /* mkv_device_status only: the status word is nonzero */
@@ -86,12 +91,21 @@ typedef enum {
     MKV_MODE_COSINE = 1  /* s_t = 1 - cos(k_t, c); 1 when |k_t||c| = 0 (the cosine baseline, abstract) */
 } mkv_mode;
 
-/* Shape of a cache. seq_lens: device int32 [batch], or NULL for all t_max. */
+/* Element type of a cache. */
+typedef enum {
+    MKV_DTYPE_BF16 = 0,     /* bfloat16 */
+    MKV_DTYPE_FP8_E4M3 = 1  /* OCP 8-bit floating point E4M3 (torch.float8_e4m3fn): the method runs on the
+                               decoded values, which fp32 holds exactly; the NaN codes are outside the contract */
+} mkv_dtype;
+
+/* Shape of a cache. dtype: an mkv_dtype (0 = bf16). seq_lens: device int32
+ * [batch], or NULL for all t_max. */
 typedef struct {
     int32_t batch;
     int32_t heads;
     int32_t t_max;
     int32_t head_dim;
+    int32_t dtype;
     const int32_t *seq_lens;
 } mkv_shape;
 
@@ -117,7 +131,7 @@ int32_t mkv_num_windows(int32_t t_max, int32_t window);
 size_t mkv_workspace_size(mkv_shape shape, int32_t window);
 
 /* Key centroids (abstract: the key centroid; per-window centroids for
- * WindowedManifoldKV). K: bf16 cache. C: fp32 [batch, heads, nw, head_dim]
+ * WindowedManifoldKV). K: key cache. C: fp32 [batch, heads, nw, head_dim]
  * with nw = mkv_num_windows(t_max, window); window j of head h gets the mean
  * of its keys, accumulated in fp32 in a fixed order (the result does not
  * depend on the GPU or the grid). Windows a short head does not have are not
@@ -128,7 +142,7 @@ mkv_status mkv_centroid(const void *K, mkv_shape shape, int32_t window, float *C
 /* Cluster summaries ("RefineKV: Query-Adaptive KV Cache Compression via
  * Attention-Error Bounds", project page, method overview step 1, Summarize:
  * contiguous clusters, their mean keys and mean values, and metadata). X is
- * a bf16 cache -- keys or values -- in the cache layout; the clusters are the
+ * a cache -- keys or values -- in the cache layout; the clusters are the
  * windows of `window` tokens (the last one holding the rest; window 0 or
  * >= t_max is one cluster per head). mean: fp32 [batch, heads, nw,
  * head_dim] with nw = mkv_num_windows(t_max, window); mean[h][j] is the
@@ -166,8 +180,8 @@ mkv_status mkv_select_topk(const float *S, mkv_shape shape, double ratio, const 
 /* Compaction and gather. From S and cut, emit per head the kept token indices
  * in ascending order into idx [batch*heads, keep_stride] and their count into
  * kept [batch*heads], and copy the kept rows bit for bit: K_out[h][j] =
- * K[h][idx[h][j]], V_out likewise, both bf16 [batch, heads, keep_stride,
- * head_dim]. Slots at or past kept[h] are not written. K_out and V_out may be
+ * K[h][idx[h][j]], V_out likewise, both [batch, heads, keep_stride,
+ * head_dim] of the cache's type. Slots at or past kept[h] are not written. K_out and V_out may be
  * NULL together (indices only); then K and V may be NULL too. With n_keep
  * NULL, keep_stride must be at least mkv_num_keep(t_max, ratio). */
 mkv_status mkv_compact(const float *S, const mkv_cut *cut, const void *K, const void *V,

@@ -42,7 +42,11 @@ def report(name: str, **fields):
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    """Raw element bits: uint16 for bf16, the uint8 codes for float8_e4m3fn."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
 
 
 def score_tol(S: np.ndarray, mode: str) -> np.ndarray:
@@ -109,7 +113,7 @@ def compare_head(ora: dict, T: int, S_gpu=None, idx_gpu=None, kept_gpu=None, K_h
 
 
 class StepBuffers:
-    """Device buffers of the step-wise API for a cache K [B, H, T, 128]."""
+    """Device buffers of the step-wise API for a cache K [B, H, T, D] (bf16 or E4M3)."""
 
     def __init__(self, K, window, ratio, seq_lens=None, keep_stride=None):
         B, H, T, D = K.shape
@@ -122,7 +126,7 @@ class StepBuffers:
         self.keep_stride = mkv.mkv_num_keep(T, ratio) if keep_stride is None else keep_stride
         self.idx = torch.full((B, H, max(self.keep_stride, 1)), -7, dtype=torch.int32, device=dev)
         self.kept = torch.full((B, H), -7, dtype=torch.int32, device=dev)
-        self.K_out = torch.zeros((B, H, max(self.keep_stride, 1), D), dtype=torch.bfloat16, device=dev)
+        self.K_out = torch.zeros((B, H, max(self.keep_stride, 1), D), dtype=K.dtype, device=dev)
         self.V_out = torch.zeros_like(self.K_out)
         self.ws = mkv.workspace_for(K, window, seq_lens)
 

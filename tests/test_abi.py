@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import geometric_kv_cache_gb300 as mkv
 import oracle
@@ -46,8 +47,8 @@ def test_num_windows_matches_the_oracle_tiling():
             assert mkv.mkv_num_windows(T, w) == oracle.num_windows(T, w), (T, w)
 
 
-def _shape(batch=2, heads=8, t_max=1024, head_dim=128, seq_lens=None):
-    return mkv.MkvShape(batch, heads, t_max, head_dim, seq_lens)
+def _shape(batch=2, heads=8, t_max=1024, head_dim=128, seq_lens=None, dtype=0):
+    return mkv.MkvShape(batch, heads, t_max, head_dim, dtype, seq_lens)
 
 
 def test_workspace_size_grows_with_the_problem():
@@ -267,3 +268,23 @@ def test_head_dims():
         mkv.MKV_ERR_UNSUPPORTED
     assert _compress(_shape(head_dim=64, batch=0)) == mkv.MKV_OK
     assert _compress(_shape(head_dim=256, batch=0)) == mkv.MKV_OK
+
+
+def test_cache_dtypes():
+    # bf16 (0) and E4M3 (1) caches share one workspace layout; other types are unsupported
+    assert mkv.mkv_workspace_size(_shape(dtype=1)) == mkv.mkv_workspace_size(_shape(dtype=0)) > 0
+    for bad in (2, -1, 7):
+        assert mkv.mkv_workspace_size(_shape(dtype=bad)) == 0
+        assert mkv.load().mkv_centroid(None, _shape(dtype=bad), 0, None, None, 0, None) == mkv.MKV_ERR_UNSUPPORTED
+    # the OjaKV scorer is bf16 only
+    assert mkv.mkv_oja_workspace_size(_shape(dtype=1), 128) == 0
+    assert mkv.mkv_oja_workspace_size(_shape(dtype=0), 128) > 0
+    assert mkv.load().mkv_oja_score(None, None, None, _shape(dtype=1), 128, 8, None, None, 0, None) == \
+        mkv.MKV_ERR_UNSUPPORTED
+    # the binding maps torch dtypes and refuses mixed caches
+    K = torch.zeros((1, 2, 8, 64), dtype=torch.float8_e4m3fn)
+    assert mkv.shape_of(K).dtype == 1 and mkv.shape_of(K.to(torch.bfloat16)).dtype == 0
+    with pytest.raises(ValueError):
+        mkv.shape_of(K.float())
+    with pytest.raises(ValueError):
+        mkv._cache_types(K, K.to(torch.bfloat16))

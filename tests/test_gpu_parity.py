@@ -514,7 +514,7 @@ def test_full_size_phi4():
 def test_single_pass_is_used_for_the_bench_shape_when_enabled():
     # 256-token pieces, at most 64 per window: the single-pass kernel runs
     # whenever it is enabled and the resident grid holds that many CTAs.
-    small = mkv.MkvShape(32, 8, 16384, 128, None)
+    small = mkv.MkvShape(32, 8, 16384, 128, 0, None)
     prev = mkv.mkv_set_single_pass(True)
     try:
         assert mkv.mkv_compress_single_pass(small, 0, "l2") == 1
@@ -552,12 +552,12 @@ def test_single_pass_and_three_kernel_paths_give_the_same_bits():
 
 
 def test_head_groups_are_used_only_where_they_fit():
-    bench = mkv.MkvShape(32, 8, 16384, 128, None)
+    bench = mkv.MkvShape(32, 8, 16384, 128, 0, None)
     assert mkv.mkv_compress_single_pass(bench, 0, "l2") == 2
     assert mkv.mkv_compress_single_pass(bench, 0, "cosine") == 2
     assert mkv.mkv_compress_single_pass(bench, 4096, "l2") == 2        # windows: blocks of windows per group
-    assert mkv.mkv_compress_single_pass(mkv.MkvShape(40, 10, 131072, 128, None), 0, "l2") == 0  # 32 MB heads
-    assert mkv.mkv_compress_single_pass(mkv.MkvShape(40, 10, 131072, 128, None), 8192, "l2") == 2  # 2 MB windows
+    assert mkv.mkv_compress_single_pass(mkv.MkvShape(40, 10, 131072, 128, 0, None), 0, "l2") == 0  # 32 MB heads
+    assert mkv.mkv_compress_single_pass(mkv.MkvShape(40, 10, 131072, 128, 0, None), 8192, "l2") == 2  # 2 MB windows
     assert mkv.mkv_compress_single_pass(bench, 100, "l2") == 0         # windows shorter than a piece
     prev = mkv.mkv_set_head_groups(False)
     try:

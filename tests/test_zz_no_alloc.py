@@ -71,7 +71,7 @@ def test_no_alloc_refuses_problems_beyond_its_scratch():
     # 512 heads x 32K tokens need more scratch than the fixed 32 MiB array:
     # the call returns MKV_ERR_UNSUPPORTED on the host, before touching any
     # pointer (so none is needed here, and no GPU).
-    shape = mkv.MkvShape(64, 8, 32768, 128, None)
+    shape = mkv.MkvShape(64, 8, 32768, 128, 0, None)
     assert mkv.mkv_workspace_size(shape, 0) > 32 << 20
     rc = mkv.load().mkv_compress_noalloc(None, None, shape, 0.5, None, 0, 0, 16384, None, None, None, None, None,
                                          None)
