@@ -46,6 +46,7 @@ METRIC = "KV tokens scored+compacted/sec and achieved HBM GB/s vs ~8 TB/s peak"
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+CACHE_DTYPE_NAMES = ("bf16", "fp8")  # --dtype: bf16, or E4M3 codes (torch.float8_e4m3fn)
 STAGES = ["piece_sums", "window_means", "piece_scores", "select", "compact", "gather"]
 
 
@@ -68,26 +69,26 @@ def keep_count(T: int, ratio: float) -> int:
     return mkv.mkv_num_keep(T, ratio)
 
 
-def path_bytes(lens, heads: int, ratio: float, d: int = 128, k_reads: int = 2) -> dict:
+def path_bytes(lens, heads: int, ratio: float, d: int = 128, k_reads: int = 2, es: int = 2) -> dict:
     """Algorithmic bytes of one step as the metric defines them: K read twice
-    (centroid, score) plus the kept K and V rows read and written. Per kernel:
-    the bytes each must move -- piece sums read K, scores read K and write 4 B
-    per token, the gather reads and writes the kept K and V rows (with
-    k_reads == 1, the single-pass kernel in stage 0 reads K once and writes
-    the scores)."""
+    (centroid, score) plus the kept K and V rows read and written (es bytes
+    per element: 2 for bf16, 1 for E4M3). Per kernel: the bytes each must
+    move -- piece sums read K, scores read K and write 4 B per token, the
+    gather reads and writes the kept K and V rows (with k_reads == 1, the
+    single-pass kernel in stage 0 reads K once and writes the scores)."""
     tok = sum(int(t) for t in lens) * heads
     keep = sum(keep_count(int(t), ratio) for t in lens) * heads
-    k_read = 2 * tok * d
+    k_read = es * tok * d
     return {
         "tokens": tok,
         "kept": keep,
-        "path": 2 * k_read + 8 * keep * d,
+        "path": 2 * k_read + 4 * es * keep * d,
         "piece_sums": k_read + (4 * tok if k_reads == 1 else 0),
         "window_means": 0,
         "piece_scores": 0 if k_reads == 1 else k_read + 4 * tok,
         "select": 0,
         "compact": 0,
-        "gather": 8 * keep * d,
+        "gather": 4 * es * keep * d,
     }
 
 
@@ -247,10 +248,12 @@ def run_ours(args):
     if args.no_head_groups:
         mkv.mkv_set_head_groups(False)
     w, mode, window, ratio = workload_run(args.workload, args.layers)
-    K, V, lens = synthkv.make_kv(w, seed=rank_seed(args.seed, rank), device=dev)
+    cache_dtype = {"bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}[args.dtype]
+    K, V, lens = synthkv.make_kv(w, seed=rank_seed(args.seed, rank), device=dev, dtype=cache_dtype)
+    es = K.element_size()
     T = w.t_max
     ks = mkv.mkv_num_keep(T, ratio)
-    K_out = torch.empty((w.rows, w.heads, ks, w.head_dim), dtype=torch.bfloat16, device=dev)
+    K_out = torch.empty((w.rows, w.heads, ks, w.head_dim), dtype=cache_dtype, device=dev)
     V_out = torch.empty_like(K_out)
     idx = torch.empty((w.rows, w.heads, ks), dtype=torch.int32, device=dev)
     kept = torch.empty((w.rows, w.heads), dtype=torch.int32, device=dev)
@@ -259,7 +262,7 @@ def run_ours(args):
     lens_list = lens.cpu().tolist()
     single = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
     select_emits = T <= 40960  # select writes the kept indices itself (no compaction kernel)
-    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single in (1, 2) else 2)
+    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single in (1, 2) else 2, es=es)
 
     def step():
         mkv.mkv_compress(K, V, ratio, mode, window, ks, K_out, V_out, idx, kept, ws, lens, stream=stream)
@@ -308,7 +311,7 @@ def run_ours(args):
     if not args.no_e2e:
         hK = K.cpu().pin_memory()
         hV = V.cpu().pin_memory()
-        hKo = torch.empty(K_out.shape, dtype=torch.bfloat16).pin_memory()
+        hKo = torch.empty(K_out.shape, dtype=cache_dtype).pin_memory()
         hVo = torch.empty_like(hKo).pin_memory()
         hidx = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
         hkept = torch.empty(kept.shape, dtype=torch.int32).pin_memory()
@@ -331,8 +334,8 @@ def run_ours(args):
         e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps)
         # keys cross the link in full; values only for the kept rows (the
         # gather reads them from the pinned host buffer)
-        h2d = hK.numel() * 2 + nbytes["kept"] * w.head_dim * 2
-        d2h = hKo.numel() * 2 + hVo.numel() * 2 + hidx.numel() * 4 + hkept.numel() * 4
+        h2d = hK.numel() * es + nbytes["kept"] * w.head_dim * es
+        d2h = hKo.numel() * es + hVo.numel() * es + hidx.numel() * 4 + hkept.numel() * 4
         e2e = {"value": tokens_all / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
         if mkv.mkv_device_status(ws, stream) != 0:
@@ -362,15 +365,16 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "io_dtype": "bf16",
+        "io_dtype": args.dtype if args.dtype == "bf16" else "fp8_e4m3",
         "data": "synthetic (seeded; Llama-3.1-8B-shaped KV cache, random keys with outlier channels)",
         "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "kv_heads": w.heads,
+                   "cache_dtype": args.dtype if args.dtype == "bf16" else "fp8_e4m3",
                    "heads_total": w.n_heads, "t": T, "head_dim": w.head_dim, "mode": mode,
                    "window": window, "ratio": ratio, "keep_per_head": ks,
                    "centroid_score_path": {0: "three kernels (K read twice)", 1: "single pass (K read once)",
                                            2: "head groups (K read from HBM once, again from L2)"}.get(single, "?"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "no flush: K+V (%.1f GB) exceed the 129 MB L2" % (2 * K.numel() * 2 / 1e9)},
+                   "l2": "no flush: K+V (%.1f GB) exceed the 129 MB L2" % (2 * K.numel() * es / 1e9)},
         "hbm": {"path_bytes_per_step": nbytes["path"], "achieved_gbs": hbm_gbs,
                 "frac_of_nominal_8000": hbm_gbs / world / NOMINAL_HBM_GBS,
                 "frac_of_measured": hbm_gbs / world / peaks["hbm_gbs"]},
@@ -645,6 +649,8 @@ def main(argv=None):
     ap.add_argument("--oja-queries", type=int, default=128, help="query-window rows per KV head (--path oja)")
     ap.add_argument("--oja-rank", type=int, default=64, help="basis rank (--path oja)")
     ap.add_argument("--cluster", type=int, default=10, help="cluster length (--path summaries)")
+    ap.add_argument("--dtype", choices=sorted(CACHE_DTYPE_NAMES), default="bf16",
+                    help="cache element type: bf16, or fp8 (E4M3 codes; the ManifoldKV path only)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
                     help="per-kernel DRAM bytes per launch from an ncu capture (null when absent)")
     args = ap.parse_args(argv)
@@ -659,8 +665,11 @@ def main(argv=None):
             src = os.path.join(ROOT, "bench.py")
         with open(src, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
-        if t.get("workload") == args.workload and not args.layers and t.get("kernel_source_sha256_16") == sha:
+        if (t.get("workload") == args.workload and not args.layers and t.get("kernel_source_sha256_16") == sha
+                and t.get("cache_dtype", "bf16") == args.dtype):
             args.traffic = t.get("bytes_per_launch")
+    if args.dtype != "bf16" and (args.impl == "reference" or args.path != "manifold"):
+        ap.error("--dtype fp8 applies to the ManifoldKV path of our arm only")
     if args.impl == "reference":
         run_reference(args)
     elif args.path != "manifold":

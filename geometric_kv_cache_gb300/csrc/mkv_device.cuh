@@ -54,17 +54,19 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float f[8])
 
 // Eight E4M3 codes (OCP 8-bit floating point, E4M3: sign, 4 exponent bits
 // with bias 7, 3 mantissa bits, subnormals at exponent field 0), widened
-// exactly to fp32. Code b read as the fp32 pattern (b & 0x7F) << 20 with its
-// sign moved to bit 31 has the same exponent field and mantissa bits, so its
-// value is the code's value times 2^-120 (also for the subnormal codes, which
-// land on fp32 subnormals); one multiplication by 2^120 without flush to
-// zero restores it exactly. The NaN codes are outside the contract (they
-// decode to +-480).
-__device__ __forceinline__ float e4m3_scaled(uint32_t pattern)
+// exactly to fp32: the conversion instruction takes two codes to two fp16
+// (every finite E4M3 value, 2^-9 .. 448, is an fp16 value), and fp16 ->
+// fp32 is exact. Element order is kept: the code in the lower byte becomes
+// the lower half. The NaN codes are outside the contract.
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint16_t codes)
 {
-    float r;
-    asm("mul.rn.f32 %0, %1, 0f7B800000;" : "=f"(r) : "f"(__uint_as_float(pattern)));  // * 2^120
-    return r;
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(codes));
+    float lo, hi;
+    asm("{ .reg .f16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
+    return make_float2(lo, hi);
 }
 
 __device__ __forceinline__ void e4m3x8_to_f32(const uint2 v, float f[8])
@@ -72,11 +74,12 @@ __device__ __forceinline__ void e4m3x8_to_f32(const uint2 v, float f[8])
     const uint32_t w[2] = {v.x, v.y};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        const uint32_t x = w[i];
-        f[4 * i + 0] = e4m3_scaled(((x & 0x7Fu) << 20) | ((x & 0x80u) << 24));
-        f[4 * i + 1] = e4m3_scaled(((x & 0x7F00u) << 12) | ((x & 0x8000u) << 16));
-        f[4 * i + 2] = e4m3_scaled(((x & 0x7F0000u) << 4) | ((x & 0x800000u) << 8));
-        f[4 * i + 3] = e4m3_scaled(((x >> 4) & 0x07F00000u) | (x & 0x80000000u));
+        const float2 a = e4m3x2_to_f32((uint16_t)(w[i] & 0xFFFFu));
+        const float2 b = e4m3x2_to_f32((uint16_t)(w[i] >> 16));
+        f[4 * i + 0] = a.x;
+        f[4 * i + 1] = a.y;
+        f[4 * i + 2] = b.x;
+        f[4 * i + 3] = b.y;
     }
 }
 

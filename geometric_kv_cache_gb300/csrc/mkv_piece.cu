@@ -317,10 +317,11 @@ __device__ __forceinline__ void load_rows(const uint8_t *base, int len, int i0, 
     }
 }
 
-// Rows in flight per lane in the streaming kernels: 8 / NB (the same bytes
-// for every head dim).
-template <int NB>
-__host__ __device__ constexpr int batch_rows() { return 8 / NB; }
+// Rows in flight per lane in the streaming kernels: 128 bytes per lane for
+// every head dim and element type (8 / NB rows of bf16, 16 / NB of E4M3), at
+// most 8 rows (a 256-token piece gives each row slot 8 rows).
+template <int NB, int ES = 2>
+__host__ __device__ constexpr int batch_rows() { return 16 / (NB * ES) < 8 ? 16 / (NB * ES) : 8; }
 
 // a1, first half: piece sums. The first batch of the next piece is loaded
 // before the current piece's CTA reduction, so the loads stay in flight
@@ -329,7 +330,7 @@ template <int NB, int ES>
 __global__ void __launch_bounds__(kThreads, NB > 2 ? 2 : 3)
 k_piece_sums(PieceGeometry g, Pointers P)
 {
-    constexpr int D = 64 * NB, RB = ES * D, B = batch_rows<NB>();
+    constexpr int D = 64 * NB, RB = ES * D, B = batch_rows<NB, ES>();
     using Raw = typename Chunk<ES>::raw;
     __shared__ float red[kWarps * D];
     const Steps st = make_steps(g);
@@ -398,7 +399,7 @@ template <int MODE, int NB, int ES>
 __global__ void __launch_bounds__(kThreads, NB > 2 ? 2 : 3)
 k_piece_scores(PieceGeometry g, Pointers P)
 {
-    constexpr int D = 64 * NB, RB = ES * D, B = batch_rows<NB>();
+    constexpr int D = 64 * NB, RB = ES * D, B = batch_rows<NB, ES>();
     using Raw = typename Chunk<ES>::raw;
     const Steps st = make_steps(g);
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
