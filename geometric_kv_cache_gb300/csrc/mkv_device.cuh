@@ -83,6 +83,33 @@ __device__ __forceinline__ void e4m3x8_to_f32(const uint2 v, float f[8])
     }
 }
 
+// Two E4M3 codes to two fp16 values (exact), lower byte to lower half.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes)
+{
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)codes));
+    return h;
+}
+
+// a0 += lower half of h, a1 += upper half, each in fp32 with one rounding:
+// the mixed-precision add widens its fp16 operand exactly, so the bits are
+// those of widening first and adding in fp32.
+__device__ __forceinline__ void add_f16x2(uint32_t h, float &a0, float &a1)
+{
+    asm("{ .reg .f16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.f16 %0, lo, %0; add.rn.f32.f16 %1, hi, %1; }"
+        : "+f"(a0), "+f"(a1)
+        : "r"(h));
+}
+
+// d0 = (lower half of h) - c0, d1 = (upper half) - c1, in fp32 with one
+// rounding each (the fp16 operand is widened exactly).
+__device__ __forceinline__ void sub_f16x2(uint32_t h, float c0, float c1, float &d0, float &d1)
+{
+    asm("{ .reg .f16 lo, hi; mov.b32 {lo, hi}, %4; sub.rn.f32.f16 %0, lo, %2; sub.rn.f32.f16 %1, hi, %3; }"
+        : "=f"(d0), "=f"(d1)
+        : "f"(c0), "f"(c1), "r"(h));
+}
+
 __device__ __forceinline__ uint2 ld_stream8(const void *p)
 {
     uint2 r;
@@ -109,6 +136,22 @@ struct Chunk<2> {
     static __device__ __forceinline__ raw load(const void *p) { return ld_stream(p); }
     static __device__ __forceinline__ raw load_l1(const void *p) { return ld_nc(p); }
     static __device__ __forceinline__ void to_f32(const raw &v, float f[8]) { bf16x8_to_f32(v, f); }
+    // acc[i] += element i (fp32)
+    static __device__ __forceinline__ void add_to(const raw &v, float acc[8])
+    {
+        float f[8];
+        bf16x8_to_f32(v, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+    }
+    // d[i] = element i - c[i] (fp32)
+    static __device__ __forceinline__ void sub_from(const raw &v, const float c[8], float d[8])
+    {
+        float f[8];
+        bf16x8_to_f32(v, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d[i] = f[i] - c[i];
+    }
 };
 
 template <>
@@ -117,6 +160,26 @@ struct Chunk<1> {
     static __device__ __forceinline__ raw load(const void *p) { return ld_stream8(p); }
     static __device__ __forceinline__ raw load_l1(const void *p) { return ld_nc8(p); }
     static __device__ __forceinline__ void to_f32(const raw &v, float f[8]) { e4m3x8_to_f32(v, f); }
+    // The same results as to_f32 followed by fp32 adds / subtractions, with
+    // the fp16 -> fp32 widening folded into mixed-precision instructions.
+    static __device__ __forceinline__ void add_to(const raw &v, float acc[8])
+    {
+        const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            add_f16x2(e4m3x2_to_f16x2(w[i] & 0xFFFFu), acc[4 * i + 0], acc[4 * i + 1]);
+            add_f16x2(e4m3x2_to_f16x2(w[i] >> 16), acc[4 * i + 2], acc[4 * i + 3]);
+        }
+    }
+    static __device__ __forceinline__ void sub_from(const raw &v, const float c[8], float d[8])
+    {
+        const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            sub_f16x2(e4m3x2_to_f16x2(w[i] & 0xFFFFu), c[4 * i + 0], c[4 * i + 1], d[4 * i + 0], d[4 * i + 1]);
+            sub_f16x2(e4m3x2_to_f16x2(w[i] >> 16), c[4 * i + 2], c[4 * i + 3], d[4 * i + 2], d[4 * i + 3]);
+        }
+    }
 };
 
 // Sum over the 16 lanes of a half-warp (all 32 lanes must call it).

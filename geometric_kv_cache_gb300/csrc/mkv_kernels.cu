@@ -29,21 +29,23 @@ namespace mkv {
 namespace {
 
 constexpr int kStreamThreads = 256;            // compaction CTAs
-constexpr int kSelectThreads = 512;
+constexpr int kSelectThreads = 512;    // select CTAs whose head's scores sit in shared memory (two per SM)
+constexpr int kSelectThreadsL2 = 1024; // select CTAs that pass over the scores in L2 (one per SM)
 constexpr int kSelectSmemScores = 40960;  // heads up to this many tokens are selected from shared memory
 using namespace dev;
 
 // ------------------------------------------------------ a3: radix select --
 
-// Per-chunk kept counts and their exclusive scan for one head (all threads of
-// the 1024-thread CTA call it): chunk_info[c] = {first output slot of chunk c,
-// ties at the cut key in chunks before c}; returns the head's kept count.
+// Per-chunk kept counts and their exclusive scan for one head (all NT threads
+// of the CTA call it): chunk_info[c] = {first output slot of chunk c, ties at
+// the cut key in chunks before c}; returns the head's kept count.
+template <int NT>
 __device__ int chunk_offsets_block(const float *srow, int T, mkv_cut cut, int nch_max,
                                    int2 *__restrict__ info, uint32_t *s_warp)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nch = (T + kCompactChunk - 1) / kCompactChunk;
-    for (int c = warp; c < nch; c += kSelectThreads / 32) {
+    for (int c = warp; c < nch; c += NT / 32) {
         const int a = c * kCompactChunk, b = min(a + kCompactChunk, T);
         uint32_t gt = 0, eq = 0;
         for (int t = a + lane; t < b; t += 32) {
@@ -92,8 +94,8 @@ __device__ int chunk_offsets_block(const float *srow, int T, mkv_cut cut, int nc
 // before the last is full, so the offset has this closed form). The CTA of
 // window 0 writes the head's kept count. idx is required, cut_out and
 // chunk_info unused.
-template <bool IN_SMEM, bool QUOTA>
-__global__ void __launch_bounds__(kSelectThreads, 2)
+template <bool IN_SMEM, bool QUOTA, int NT>
+__global__ void __launch_bounds__(NT, NT > 512 ? 1 : 2)
 k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int heads, int t_max,
          double ratio, const int32_t *__restrict__ n_keep, int keep_stride, int64_t n_items, int window,
          int nwin_max, mkv_cut *__restrict__ cut_out, int2 *__restrict__ chunk_info, int nch_max,
@@ -103,7 +105,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
     __shared__ uint32_t hist[2048];
     __shared__ uint32_t s_warp[32];
     __shared__ uint32_t s_digit, s_above;
-    __shared__ uint32_t s_min[kSelectThreads / 32], s_max[kSelectThreads / 32];
+    __shared__ uint32_t s_min[NT / 32], s_max[NT / 32];
     const int lane = threadIdx.x & 31;
     constexpr int kUnroll = 4;
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -144,7 +146,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
             }
             if (chunk_info) {
                 const int nch = (T + kCompactChunk - 1) / kCompactChunk;
-                for (int c = threadIdx.x; c < nch; c += kSelectThreads) chunk_info[head * nch_max + c] = make_int2(-1, -1);
+                for (int c = threadIdx.x; c < nch; c += NT) chunk_info[head * nch_max + c] = make_int2(-1, -1);
             }
             continue;
         }
@@ -154,10 +156,10 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
             if ((reinterpret_cast<uintptr_t>(grow) & 15) == 0) {  // 16-byte aligned segment
                 const float4 *g4 = reinterpret_cast<const float4 *>(grow);
                 float4 *s4 = reinterpret_cast<float4 *>(s_scores);
-                for (int i = threadIdx.x; i < T / 4; i += kSelectThreads) s4[i] = __ldcg(g4 + i);
-                for (int i = (T & ~3) + threadIdx.x; i < T; i += kSelectThreads) s_scores[i] = __ldcg(grow + i);
+                for (int i = threadIdx.x; i < T / 4; i += NT) s4[i] = __ldcg(g4 + i);
+                for (int i = (T & ~3) + threadIdx.x; i < T; i += NT) s_scores[i] = __ldcg(grow + i);
             } else {
-                for (int i = threadIdx.x; i < T; i += kSelectThreads) s_scores[i] = __ldcg(grow + i);
+                for (int i = threadIdx.x; i < T; i += NT) s_scores[i] = __ldcg(grow + i);
             }
             __syncthreads();
             srow = s_scores;
@@ -170,7 +172,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
             // there and the first pass spreads over all its bins (no
             // warp-aggregation needed for the histogram atomics).
             uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-            for (int t = threadIdx.x; t < T; t += kSelectThreads) {
+            for (int t = threadIdx.x; t < T; t += NT) {
                 const uint32_t u = score_key(srow[t]);
                 kmin = min(kmin, u);
                 kmax = max(kmax, u);
@@ -187,7 +189,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
             __syncthreads();
             kmin = s_min[0];
             kmax = s_max[0];
-            for (int w = 1; w < kSelectThreads / 32; ++w) {
+            for (int w = 1; w < NT / 32; ++w) {
                 kmin = min(kmin, s_min[w]);
                 kmax = max(kmax, s_max[w]);
             }
@@ -203,29 +205,29 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
                     const int width = min(11, lo);
                     const int shift = lo - width;
                     const int nb = 1 << width;
-                    for (int i = threadIdx.x; i < nb; i += kSelectThreads) hist[i] = 0;
+                    for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0;
                     __syncthreads();
-                    for (int base = 0; base < T; base += kSelectThreads * kUnroll) {
+                    for (int base = 0; base < T; base += NT * kUnroll) {
                         uint32_t u[kUnroll];
 #pragma unroll
                         for (int k = 0; k < kUnroll; ++k) {
-                            const int t = base + k * kSelectThreads + threadIdx.x;
+                            const int t = base + k * NT + threadIdx.x;
                             u[k] = t < T ? score_key(srow[t]) : 0u;
                         }
 #pragma unroll
                         for (int k = 0; k < kUnroll; ++k) {
-                            const int t = base + k * kSelectThreads + threadIdx.x;
+                            const int t = base + k * NT + threadIdx.x;
                             if (t < T && (u[k] & pmask) == prefix) atomicAdd(&hist[(u[k] >> shift) & (uint32_t)(nb - 1)], 1u);
                         }
                     }
                     __syncthreads();
                     // Thread i owns bpt bins in descending order from nb-1-i*bpt.
-                    const int bpt = nb > kSelectThreads ? nb / kSelectThreads : 1;
+                    const int bpt = nb > NT ? nb / NT : 1;
                     const int hi = nb - 1 - (int)threadIdx.x * bpt;
                     uint32_t local = 0;
                     if (hi >= 0)
                         for (int j = 0; j < bpt; ++j) local += hist[hi - j];
-                    uint32_t above = block_exclusive_scan<kSelectThreads>(local, s_warp, nullptr);
+                    uint32_t above = block_exclusive_scan<NT>(local, s_warp, nullptr);
                     if (hi >= 0) {
                         for (int j = 0; j < bpt; ++j) {
                             const uint32_t h = hist[hi - j];
@@ -258,7 +260,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
             // CTA scans per round (tie rank, output slot), counts carried
             // across rounds.
             uint32_t kept = 0, ties_before = 0;
-            for (int a = 0; a < T && nk > 0; a += kSelectThreads * 16) {
+            for (int a = 0; a < T && nk > 0; a += NT * 16) {
                 const int t0 = a + threadIdx.x * 16;
                 uint32_t gtm = 0, eqm = 0;
 #pragma unroll
@@ -271,14 +273,14 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
                     }
                 }
                 uint32_t eq_total = 0;
-                uint32_t rank = ties_before + block_exclusive_scan<kSelectThreads>(__popc(eqm), s_warp, &eq_total);
+                uint32_t rank = ties_before + block_exclusive_scan<NT>(__popc(eqm), s_warp, &eq_total);
                 uint32_t keepm = gtm;
                 for (uint32_t m = eqm; m; m &= m - 1) {
                     if (rank < (uint32_t)cut.ties) keepm |= m & (~m + 1);
                     ++rank;
                 }
                 uint32_t k_total = 0;
-                uint32_t slot = kept + block_exclusive_scan<kSelectThreads>(__popc(keepm), s_warp, &k_total);
+                uint32_t slot = kept + block_exclusive_scan<NT>(__popc(keepm), s_warp, &k_total);
                 for (uint32_t m = keepm; m; m &= m - 1, ++slot) {
                     if (slot < (uint32_t)cap) idx_head[slot] = seg + t0 + __ffs(m) - 1;
                     else atomicOr(status, MKV_DEV_INTERNAL);
@@ -291,7 +293,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
                 if (!QUOTA && kept_out) kept_out[head] = (int32_t)kept;
             }
         } else if (chunk_info) {
-            const int kept = nk > 0 ? chunk_offsets_block(srow, T, cut, nch_max, chunk_info + head * nch_max, s_warp) : 0;
+            const int kept = nk > 0 ? chunk_offsets_block<NT>(srow, T, cut, nch_max, chunk_info + head * nch_max, s_warp) : 0;
             if (threadIdx.x == 0) {
                 if (kept != nk) atomicOr(status, MKV_DEV_INTERNAL);
                 if (kept_out) kept_out[head] = kept;
@@ -317,7 +319,7 @@ k_chunk_offsets(const float *__restrict__ S, const mkv_cut *__restrict__ cuts,
         const bool bad = nk < 0 || nk > T || (keep_stride >= 0 && nk > keep_stride);
         int kept = 0;
         if (!bad && cut.key != kNoneKey) {
-            kept = chunk_offsets_block(S + (size_t)head * t_max, T, cut, nch_max, chunk_info + head * nch_max, s_warp);
+            kept = chunk_offsets_block<kSelectThreads>(S + (size_t)head * t_max, T, cut, nch_max, chunk_info + head * nch_max, s_warp);
         } else {
             // Mark every chunk of a skipped head so the gather leaves it alone.
             const int nch = (T + kCompactChunk - 1) / kCompactChunk;
@@ -465,16 +467,16 @@ cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_
     if (g.n_heads == 0) return cudaSuccess;
     const size_t smem = (size_t)g.t_max * sizeof(float);
     if (g.t_max <= kSelectSmemScores) {
-        auto *kern = k_select<true, false>;
+        auto *kern = k_select<true, false, kSelectThreads>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         const int grid = grid_for_items(reinterpret_cast<const void *>(kern), kSelectThreads, smem, g.n_heads);
         kern<<<grid, kSelectThreads, smem, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride, g.n_heads,
                                                  0, 1, cut, chunk_info, g.nch, kept, idx, idx_stride, status);
     } else {
-        auto *kern = k_select<false, false>;
-        const int grid = grid_for(kern, kSelectThreads, g.n_heads);
-        kern<<<grid, kSelectThreads, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride, g.n_heads, 0,
+        auto *kern = k_select<false, false, kSelectThreadsL2>;
+        const int grid = grid_for(kern, kSelectThreadsL2, g.n_heads);
+        kern<<<grid, kSelectThreadsL2, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride, g.n_heads, 0,
                                               1, cut, chunk_info, g.nch, kept, idx, idx_stride, status);
     }
     return cudaGetLastError();
@@ -490,7 +492,7 @@ cudaError_t launch_select_quota(const Geometry &g, const float *S, const int32_t
     // one window per head (window 0 or >= t_max) is the ordinary selection
     const int wl = (p.window <= 0 || p.window >= g.t_max) ? g.t_max : p.window;
     if (wl <= kSelectSmemScores) {
-        auto *kern = k_select<true, true>;
+        auto *kern = k_select<true, true, kSelectThreads>;
         const size_t smem = (size_t)wl * sizeof(float);
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -498,9 +500,9 @@ cudaError_t launch_select_quota(const Geometry &g, const float *S, const int32_t
         kern<<<grid, kSelectThreads, smem, st>>>(S, seq_lens, g.heads, g.t_max, ratio, nullptr, keep_stride, items,
                                                  wl, p.nwin_max, nullptr, nullptr, 0, kept, idx, idx_stride, status);
     } else {
-        auto *kern = k_select<false, true>;
-        const int grid = grid_for(kern, kSelectThreads, items);
-        kern<<<grid, kSelectThreads, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, nullptr, keep_stride, items,
+        auto *kern = k_select<false, true, kSelectThreadsL2>;
+        const int grid = grid_for(kern, kSelectThreadsL2, items);
+        kern<<<grid, kSelectThreadsL2, 0, st>>>(S, seq_lens, g.heads, g.t_max, ratio, nullptr, keep_stride, items,
                                               wl, p.nwin_max, nullptr, nullptr, 0, kept, idx, idx_stride, status);
     }
     return cudaGetLastError();

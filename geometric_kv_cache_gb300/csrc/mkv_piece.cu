@@ -273,6 +273,37 @@ __device__ __forceinline__ void row_to_f32(const typename Chunk<ES>::raw *v, flo
     for (int k = 0; k < NB; ++k) Chunk<ES>::to_f32(v[k], f + 8 * k);
 }
 
+// acc += the thread's 8 * NB dims of a row (fp32 adds in dim order).
+template <int NB, int ES>
+__device__ __forceinline__ void row_accumulate(const typename Chunk<ES>::raw *v, float acc[8 * NB])
+{
+#pragma unroll
+    for (int k = 0; k < NB; ++k) Chunk<ES>::add_to(v[k], acc + 8 * k);
+}
+
+// score_of on a row still in its cache encoding. L2 subtracts the centroid
+// straight from the encoded elements (the same roundings as widening first).
+template <int MODE, int NB, int ES>
+__device__ __forceinline__ float score_row(const typename Chunk<ES>::raw *v, const float c[8 * NB], float nc)
+{
+    if (MODE == MKV_MODE_L2) {
+        float d[8 * NB];
+#pragma unroll
+        for (int k = 0; k < NB; ++k) Chunk<ES>::sub_from(v[k], c + 8 * k, d + 8 * k);
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8 * NB; ++j) acc = fmaf(d[j], d[j], acc);
+        acc += __shfl_xor_sync(kFull, acc, 4);
+        acc += __shfl_xor_sync(kFull, acc, 2);
+        acc += __shfl_xor_sync(kFull, acc, 1);
+        return __fsqrt_rn(acc);
+    } else {
+        float f[8 * NB];
+        row_to_f32<NB, ES>(v, f);
+        return score_of<MODE, NB>(f, c, nc);
+    }
+}
+
 // Sum of n (<= kGroupPieces) consecutive D-float records, record order,
 // dim d; loads issued in batches of 8 ahead of their adds.
 template <int D = 128>
@@ -349,12 +380,7 @@ k_piece_sums(PieceGeometry g, Pointers P)
         for (int i0 = 0; i0 < nrows; i0 += B) {
 #pragma unroll
             for (int u = 0; u < B; ++u) {
-                if (slot + (i0 + u) * kRowSlots < pc.len) {
-                    float f[8 * NB];
-                    row_to_f32<NB, ES>(v + NB * u, f);
-#pragma unroll
-                    for (int j = 0; j < 8 * NB; ++j) acc[j] += f[j];
-                }
+                if (slot + (i0 + u) * kRowSlots < pc.len) row_accumulate<NB, ES>(v + NB * u, acc);
             }
             if (i0 + B < nrows) load_rows<B, NB, ES>(base, pc.len, i0 + B, v);
         }
@@ -418,9 +444,7 @@ k_piece_scores(PieceGeometry g, Pointers P)
 #pragma unroll
             for (int u = 0; u < B; ++u) {
                 const int r = slot + (i0 + u) * kRowSlots;
-                float f[8 * NB];
-                row_to_f32<NB, ES>(v + NB * u, f);
-                const float s = score_of<MODE, NB>(f, c, nc);
+                const float s = score_row<MODE, NB, ES>(v + NB * u, c, nc);
                 if (r < pc.len && q == 0) srow[r] = s;
             }
             if (i0 + B < nrows) load_rows<B, NB, ES>(base, pc.len, i0 + B, v);
@@ -949,12 +973,7 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
                 load_rows_policy<kBatchG, NB, ES>(base, len, i0, v, keep_l2);
 #pragma unroll
                 for (int u = 0; u < kBatchG; ++u) {
-                    if (slot + (i0 + u) * kRowSlots < len) {
-                        float fr[8 * NB];
-                        row_to_f32<NB, ES>(v + NB * u, fr);
-#pragma unroll
-                        for (int j = 0; j < 8 * NB; ++j) acc[j] += fr[j];
-                    }
+                    if (slot + (i0 + u) * kRowSlots < len) row_accumulate<NB, ES>(v + NB * u, acc);
                 }
             }
 #pragma unroll
@@ -1042,9 +1061,7 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
 #pragma unroll
                     for (int u = 0; u < kBatchG; ++u) {
                         const int r = slot + (i0 + u) * kRowSlots;
-                        float fr[8 * NB];
-                        row_to_f32<NB, ES>(v + NB * u, fr);
-                        const float sc = score_of<MODE, NB>(fr, c, nc);
+                        const float sc = score_row<MODE, NB, ES>(v + NB * u, c, nc);
                         if (r < len && q == 0) srow[r] = sc;
                     }
                 }
