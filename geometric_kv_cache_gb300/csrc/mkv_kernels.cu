@@ -31,6 +31,7 @@ namespace {
 constexpr int kStreamThreads = 256;            // compaction CTAs
 constexpr int kSelectThreads = 512;    // select CTAs whose head's scores sit in shared memory (two per SM)
 constexpr int kSelectThreadsL2 = 1024; // select CTAs that pass over the scores in L2 (one per SM)
+constexpr int kSelectCandidates = 1024; // keys a radix pass may collect for the later passes
 constexpr int kSelectSmemScores = 40960;  // heads up to this many tokens are selected from shared memory
 using namespace dev;
 
@@ -104,8 +105,9 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
     extern __shared__ __align__(16) float s_scores[];
     __shared__ uint32_t hist[2048];
     __shared__ uint32_t s_warp[32];
-    __shared__ uint32_t s_digit, s_above;
+    __shared__ uint32_t s_digit, s_above, s_count, s_ncand;
     __shared__ uint32_t s_min[NT / 32], s_max[NT / 32];
+    __shared__ uint32_t s_cand[kSelectCandidates];
     const int lane = threadIdx.x & 31;
     constexpr int kUnroll = 4;
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -152,14 +154,39 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
         }
         const float *grow = S + (size_t)head * t_max + seg;
         const float *srow = grow;
+        // Smallest and largest key of the head: bits above their highest
+        // differing bit are common to every key, so the digits start there
+        // and the first pass spreads over all its bins. Taken while the
+        // scores are copied to shared memory, else in a pass of their own.
+        uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+        auto see = [&](float v) {
+            const uint32_t u = score_key(v);
+            kmin = min(kmin, u);
+            kmax = max(kmax, u);
+        };
         if (IN_SMEM) {
             if ((reinterpret_cast<uintptr_t>(grow) & 15) == 0) {  // 16-byte aligned segment
                 const float4 *g4 = reinterpret_cast<const float4 *>(grow);
                 float4 *s4 = reinterpret_cast<float4 *>(s_scores);
-                for (int i = threadIdx.x; i < T / 4; i += NT) s4[i] = __ldcg(g4 + i);
-                for (int i = (T & ~3) + threadIdx.x; i < T; i += NT) s_scores[i] = __ldcg(grow + i);
+                for (int i = threadIdx.x; i < T / 4; i += NT) {
+                    const float4 v = __ldcg(g4 + i);
+                    s4[i] = v;
+                    see(v.x);
+                    see(v.y);
+                    see(v.z);
+                    see(v.w);
+                }
+                for (int i = (T & ~3) + threadIdx.x; i < T; i += NT) {
+                    const float v = __ldcg(grow + i);
+                    s_scores[i] = v;
+                    see(v);
+                }
             } else {
-                for (int i = threadIdx.x; i < T; i += NT) s_scores[i] = __ldcg(grow + i);
+                for (int i = threadIdx.x; i < T; i += NT) {
+                    const float v = __ldcg(grow + i);
+                    s_scores[i] = v;
+                    see(v);
+                }
             }
             __syncthreads();
             srow = s_scores;
@@ -167,16 +194,8 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
         uint32_t prefix = 0, pmask = 0;
         int need = nk;
         if (nk > 0) {
-            // Smallest and largest key of the head: bits above their highest
-            // differing bit are common to every key, so the digits start
-            // there and the first pass spreads over all its bins (no
-            // warp-aggregation needed for the histogram atomics).
-            uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-            for (int t = threadIdx.x; t < T; t += NT) {
-                const uint32_t u = score_key(srow[t]);
-                kmin = min(kmin, u);
-                kmax = max(kmax, u);
-            }
+            if (!IN_SMEM)
+                for (int t = threadIdx.x; t < T; t += NT) see(srow[t]);
 #pragma unroll
             for (int o = 16; o; o >>= 1) {
                 kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
@@ -200,24 +219,46 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
                 const int hb = 31 - __clz(kmin ^ kmax);  // highest differing bit
                 pmask = hb == 31 ? 0u : ~((2u << hb) - 1u);
                 prefix = kmin & pmask;
+                // Keys that match the prefix so far: once there are at most
+                // kSelectCandidates of them (the count of the previous pass's
+                // chosen bin), a full pass also copies them into s_cand and
+                // the later passes scan that list instead of all T keys.
+                uint32_t match = (uint32_t)T;
+                bool listed = false;
+                int ncand = 0;
 #pragma unroll 1
                 for (int lo = hb + 1; lo > 0;) {
                     const int width = min(11, lo);
                     const int shift = lo - width;
                     const int nb = 1 << width;
+                    const bool build = !listed && shift > 0 && match <= (uint32_t)kSelectCandidates;
                     for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0;
+                    if (threadIdx.x == 0) s_ncand = 0;
                     __syncthreads();
-                    for (int base = 0; base < T; base += NT * kUnroll) {
-                        uint32_t u[kUnroll];
-#pragma unroll
-                        for (int k = 0; k < kUnroll; ++k) {
-                            const int t = base + k * NT + threadIdx.x;
-                            u[k] = t < T ? score_key(srow[t]) : 0u;
+                    if (listed) {
+                        for (int i = threadIdx.x; i < ncand; i += NT) {
+                            const uint32_t u = s_cand[i];
+                            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (uint32_t)(nb - 1)], 1u);
                         }
+                    } else {
+                        for (int base = 0; base < T; base += NT * kUnroll) {
+                            uint32_t u[kUnroll];
 #pragma unroll
-                        for (int k = 0; k < kUnroll; ++k) {
-                            const int t = base + k * NT + threadIdx.x;
-                            if (t < T && (u[k] & pmask) == prefix) atomicAdd(&hist[(u[k] >> shift) & (uint32_t)(nb - 1)], 1u);
+                            for (int k = 0; k < kUnroll; ++k) {
+                                const int t = base + k * NT + threadIdx.x;
+                                u[k] = t < T ? score_key(srow[t]) : 0u;
+                            }
+#pragma unroll
+                            for (int k = 0; k < kUnroll; ++k) {
+                                const int t = base + k * NT + threadIdx.x;
+                                if (t < T && (u[k] & pmask) == prefix) {
+                                    atomicAdd(&hist[(u[k] >> shift) & (uint32_t)(nb - 1)], 1u);
+                                    if (build) {
+                                        const uint32_t c = atomicAdd(&s_ncand, 1u);
+                                        if (c < (uint32_t)kSelectCandidates) s_cand[c] = u[k];
+                                    }
+                                }
+                            }
                         }
                     }
                     __syncthreads();
@@ -234,6 +275,7 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
                             if (above < (uint32_t)need && (uint32_t)need <= above + h) {
                                 s_digit = (uint32_t)(hi - j);
                                 s_above = above;
+                                s_count = h;
                             }
                             above += h;
                         }
@@ -242,6 +284,11 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
                     prefix |= s_digit << shift;
                     pmask |= (uint32_t)(nb - 1) << shift;
                     need -= (int)s_above;
+                    match = s_count;
+                    if (build && s_ncand <= (uint32_t)kSelectCandidates) {  // (always: the count was known)
+                        listed = true;
+                        ncand = (int)s_ncand;
+                    }
                     __syncthreads();
                     lo = shift;
                 }
@@ -256,35 +303,68 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
         if (threadIdx.x == 0 && cut_out) cut_out[head] = cut;
         if (idx_head) {
             // Emit the kept indices in ascending order straight from the
-            // scores in hand: rounds of 16 consecutive tokens per thread, two
-            // CTA scans per round (tie rank, output slot), counts carried
-            // across rounds.
+            // scores in hand. A round covers 16 * NT tokens; warp w takes 16
+            // steps of 32 consecutive tokens from a + 512 w (lane l reads
+            // token step + l: no bank conflicts). Counts of keys above and at
+            // the cut per warp, scanned over the warps, give each warp's
+            // first tie rank and first output slot; within the warp,
+            // ballots and popcounts place every kept token, so consecutive
+            // kept tokens land in consecutive slots (coalesced stores).
+            // Counts are carried across rounds.
+            const int warp = threadIdx.x >> 5;
+            const uint32_t lt = (1u << lane) - 1u;
             uint32_t kept = 0, ties_before = 0;
             for (int a = 0; a < T && nk > 0; a += NT * 16) {
-                const int t0 = a + threadIdx.x * 16;
-                uint32_t gtm = 0, eqm = 0;
-#pragma unroll
+                const int wb = a + warp * 512;
+                uint32_t ngt = 0, neq = 0;
+#pragma unroll 4
                 for (int j = 0; j < 16; ++j) {
-                    const int t = t0 + j;
-                    if (t < T) {
-                        const uint32_t u = score_key(srow[t]);
-                        gtm |= (uint32_t)(u > cut.key) << j;
-                        eqm |= (uint32_t)(u == cut.key) << j;
+                    const int t = wb + j * 32 + lane;
+                    const uint32_t u = t < T ? score_key(srow[t]) : 0u;
+                    ngt += __popc(__ballot_sync(kFull, t < T && u > cut.key));
+                    neq += __popc(__ballot_sync(kFull, t < T && u == cut.key));
+                }
+                if (lane == 0) {
+                    s_warp[warp] = neq;
+                    s_min[warp] = ngt;  // reused as per-warp scratch
+                }
+                __syncthreads();
+                uint32_t tie_base = ties_before, eq_total = 0;
+                for (int w = 0; w < NT / 32; ++w) {
+                    const uint32_t e = s_warp[w];
+                    if (w < warp) tie_base += e;
+                    eq_total += e;
+                }
+                // ties of this warp that are kept, then the warp's first slot
+                const uint32_t keep_ties_w =
+                    (uint32_t)min(max((int)cut.ties - (int)tie_base, 0), (int)neq);
+                __syncthreads();
+                if (lane == 0) s_max[warp] = s_min[warp] + keep_ties_w;
+                __syncthreads();
+                uint32_t slot = kept, k_total = 0;
+                for (int w = 0; w < NT / 32; ++w) {
+                    const uint32_t k = s_max[w];
+                    if (w < warp) slot += k;
+                    k_total += k;
+                }
+                uint32_t rank = tie_base;
+#pragma unroll 4
+                for (int j = 0; j < 16; ++j) {
+                    const int t = wb + j * 32 + lane;
+                    const uint32_t u = t < T ? score_key(srow[t]) : 0u;
+                    const bool gt = t < T && u > cut.key, eq = t < T && u == cut.key;
+                    const uint32_t eqb = __ballot_sync(kFull, eq);
+                    const bool keep = gt || (eq && rank + __popc(eqb & lt) < (uint32_t)cut.ties);
+                    const uint32_t kb = __ballot_sync(kFull, keep);
+                    if (keep) {
+                        const uint32_t sl = slot + __popc(kb & lt);
+                        if (sl < (uint32_t)cap) idx_head[sl] = seg + t;
+                        else atomicOr(status, MKV_DEV_INTERNAL);
                     }
+                    rank += __popc(eqb);
+                    slot += __popc(kb);
                 }
-                uint32_t eq_total = 0;
-                uint32_t rank = ties_before + block_exclusive_scan<NT>(__popc(eqm), s_warp, &eq_total);
-                uint32_t keepm = gtm;
-                for (uint32_t m = eqm; m; m &= m - 1) {
-                    if (rank < (uint32_t)cut.ties) keepm |= m & (~m + 1);
-                    ++rank;
-                }
-                uint32_t k_total = 0;
-                uint32_t slot = kept + block_exclusive_scan<NT>(__popc(keepm), s_warp, &k_total);
-                for (uint32_t m = keepm; m; m &= m - 1, ++slot) {
-                    if (slot < (uint32_t)cap) idx_head[slot] = seg + t0 + __ffs(m) - 1;
-                    else atomicOr(status, MKV_DEV_INTERNAL);
-                }
+                __syncthreads();  // s_warp, s_min and s_max are rewritten next round
                 kept += k_total;
                 ties_before += eq_total;
             }
