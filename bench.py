@@ -543,7 +543,7 @@ def run_secondary(args):
                 "value": tokens / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": args.warmup,
                 "ms_per_step": ms, "higher_is_better": True, "dtype": "f32", "data": "synthetic (seeded)",
                 "config": {"workload": w.name, "heads_total": w.n_heads, "t": w.t_max, "cluster": W},
-                "roofline": {"bound": "hbm", "kernel": "k_small_window_means (K with radius, then V)",
+                "roofline": {"bound": "hbm", "kernel": "k_small_window_regs (K with radius, then V; clusters of at most 16 rows)" if args.cluster <= 16 else "k_small_window_means (K with radius, then V)",
                              "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                              "peak_source": peaks["source"], "algorithmic_bytes_per_launch": nbytes},
                 "clocks": clocks.summary(), "gpu_launches": steps * 2}
