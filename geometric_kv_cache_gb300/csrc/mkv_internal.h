@@ -89,6 +89,7 @@ struct HeadGroupPlan {
     int groups = 0;
     int gsize = 0;  // CTAs per group
     int wb = 0;     // windows per unit
+    uint32_t stagger_ns = 0;  // start delay step: group g waits (g mod 4) steps
 };
 HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counter_bytes);
 cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan, const void *K,

@@ -911,7 +911,7 @@ constexpr int kMaxSlots = stash_slots(64);
 
 template <int MODE, int NB, int ES>
 __global__ void __launch_bounds__(kThreads, 2)
-k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
+k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, uint32_t stagger_ns)
 {
     constexpr int D = 64 * NB, RB = ES * D;
     using Raw = typename Chunk<ES>::raw;
@@ -925,6 +925,15 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb)
     const int groups = gridDim.x / gsize;
     const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
     if (group >= groups) return;  // a launch is always a whole number of groups
+    // Every group does the same work per round, so groups that start
+    // together stay in phase: all read HBM (pass 1) at once, then all read L2
+    // (pass 2). Starting groups (group mod 4) stagger steps late spreads the
+    // phases (measured on 256 heads x 16K: 0.311 -> 0.300 ms).
+    if (stagger_ns) {
+        const uint64_t t0 = global_ns(), wait = (uint64_t)(group & 3) * stagger_ns;
+        while (global_ns() - t0 < wait) {
+        }
+    }
     const int slot = threadIdx.x >> 3, q = threadIdx.x & 7, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // the stash's piece sums: warps in order (finish_sum's order), then free
     auto flush = [&](int ns) {
@@ -1230,6 +1239,14 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
             }
         }
     }
+    if (plan.groups > 0) {
+        // the stagger step: a third of the time the units in flight take to
+        // stream from HBM (at 6.5 TB/s), when every group has 4 rounds or more
+        const int64_t units = g.n_heads * ((g.nwin_max + plan.wb - 1) / plan.wb);
+        const int64_t rounds = (units + plan.groups - 1) / plan.groups;
+        const double round_ns = (double)plan.groups * plan.wb * window_bytes / 6500.0;  // 6.5 TB/s = 6500 B/ns
+        plan.stagger_ns = rounds >= 4 ? (uint32_t)std::min(20000.0, round_ns / 3.0) : 0u;
+    }
     return plan;
 }
 
@@ -1244,7 +1261,8 @@ cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan
     Pointers P = make_pointers(K, seq_lens, partial, C, S, status);
     PieceGeometry gg = g;
     int gsize = plan.gsize, wb = plan.wb;
-    void *args[] = {&gg, &P, &cnt, &gsize, &wb};
+    uint32_t stagger = plan.stagger_ns;
+    void *args[] = {&gg, &P, &cnt, &gsize, &wb, &stagger};
     return cudaLaunchCooperativeKernel(fn, dim3((unsigned)(plan.groups * plan.gsize)), dim3(kThreads), args,
                                        kGroupSmem, st);
 }
