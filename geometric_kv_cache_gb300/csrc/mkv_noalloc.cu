@@ -65,8 +65,14 @@ extern "C" mkv_status mkv_compress_noalloc(const void *K, const void *V, mkv_sha
     // before it enqueues anything.
     rc = mkv_compress(K, V, shape, ratio, n_keep, mode, window, keep_stride, K_out, V_out, idx, kept, scratch,
                       (size_t)MKV_NOALLOC_SCRATCH_BYTES, stream);
-    if (rc != MKV_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (rc == MKV_ERR_CUDA) {
+        // kernels may have run and set status bits: try to leave the shared
+        // word at zero so that the next call does not report them
+        (void)cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st);
+        return rc;
+    }
+    if (rc != MKV_OK) return rc;
     if (status_out && cudaMemcpyAsync(status_out, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
         return MKV_ERR_CUDA;
     // Leave the status word at zero for the next call.

@@ -382,8 +382,10 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
  *   other's results. Serialise them.
  *   Outputs and arguments: as for mkv_compress. status_out (device, nullable)
  *   receives the device status word of this call (MKV_DEV_* bits); the call
- *   then resets the word to zero. After MKV_ERR_CUDA the word may still hold
- *   that call's bits. The call allocates and frees nothing. */
+ *   then resets the word to zero. After MKV_ERR_CUDA the call still tries to
+ *   reset it (best effort: the failed call's bits are not reported, and a
+ *   sticky CUDA error can prevent the reset). The call allocates and frees
+ *   nothing. */
 mkv_status mkv_compress_noalloc(const void *K, const void *V, mkv_shape shape, double ratio,
                                 const int32_t *n_keep, mkv_mode mode, int32_t window, int32_t keep_stride,
                                 void *K_out, void *V_out, int32_t *idx, int32_t *kept, uint32_t *status_out,
