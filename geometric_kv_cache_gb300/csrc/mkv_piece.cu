@@ -1240,10 +1240,22 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
         }
     }
     if (plan.groups > 0) {
-        // the stagger step: a third of the time the units in flight take to
-        // stream from HBM (at 6.5 TB/s), when every group has 4 rounds or more
         const int64_t units = g.n_heads * ((g.nwin_max + plan.wb - 1) / plan.wb);
         const int64_t rounds = (units + plan.groups - 1) / plan.groups;
+        // With several rounds per group the work, not the launch count,
+        // decides: keep the head groups only if their modelled time is below
+        // the three kernels' (every piece read twice over the same CTAs, in
+        // the same piece-time units). Measured ratios follow the model up to
+        // head dim 128: 0.84 on 256 x 16K global (model 0.83), 0.84 on the
+        // Qwen and Phi-4 windowed shapes (0.78, 0.77), 1.07-1.16 on the
+        // ragged batch of 2048 heads up to 32K (1.06: two pieces per CTA per
+        // round). At head dim 256 the piece kernels keep half the head-group
+        // kernel's bytes in flight per lane, so the model does not hold there
+        // (64 x 16K: head groups 0.156 ms, three kernels 0.187).
+        const double three = 2.0 * (double)g.n_heads * g.nwin_max * g.ppw / (double)resident;
+        if (g.d <= 128 && rounds >= 4 && best >= three) return HeadGroupPlan{};
+        // the stagger step: a third of the time the units in flight take to
+        // stream from HBM (at 6.5 TB/s), when every group has 4 rounds or more
         const double round_ns = (double)plan.groups * plan.wb * window_bytes / 6500.0;  // 6.5 TB/s = 6500 B/ns
         plan.stagger_ns = rounds >= 4 ? (uint32_t)std::min(20000.0, round_ns / 3.0) : 0u;
     }

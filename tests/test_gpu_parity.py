@@ -559,6 +559,9 @@ def test_head_groups_are_used_only_where_they_fit():
     assert mkv.mkv_compress_single_pass(mkv.MkvShape(40, 10, 131072, 128, 0, None), 0, "l2") == 0  # 32 MB heads
     assert mkv.mkv_compress_single_pass(mkv.MkvShape(40, 10, 131072, 128, 0, None), 8192, "l2") == 2  # 2 MB windows
     assert mkv.mkv_compress_single_pass(bench, 100, "l2") == 0         # windows shorter than a piece
+    # the ragged workload's shape (2048 heads up to 32K, 512-row pieces): two
+    # pieces per CTA per round do not pay for the rounds, the three kernels run
+    assert mkv.mkv_compress_single_pass(mkv.MkvShape(256, 8, 32768, 128, 0, None), 0, "l2") == 0
     prev = mkv.mkv_set_head_groups(False)
     try:
         assert mkv.mkv_compress_single_pass(bench, 0, "l2") == 0
