@@ -1252,8 +1252,11 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
         // round). At head dim 256 the piece kernels keep half the head-group
         // kernel's bytes in flight per lane, so the model does not hold there
         // (64 x 16K: head groups 0.156 ms, three kernels 0.187).
+        // E4M3 caches: decoding, not HBM, bounds both passes, so a saved read
+        // of K does not pay for the rounds (256 x 16K: head groups 0.250 ms,
+        // three kernels 0.243; cosine 0.294 against 0.289).
         const double three = 2.0 * (double)g.n_heads * g.nwin_max * g.ppw / (double)resident;
-        if (g.d <= 128 && rounds >= 4 && best >= three) return HeadGroupPlan{};
+        if (rounds >= 4 && (g.es == 1 || (g.d <= 128 && best >= three))) return HeadGroupPlan{};
         // the stagger step: a third of the time the units in flight take to
         // stream from HBM (at 6.5 TB/s), when every group has 4 rounds or more
         const double round_ns = (double)plan.groups * plan.wb * window_bytes / 6500.0;  // 6.5 TB/s = 6500 B/ns

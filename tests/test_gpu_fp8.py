@@ -249,7 +249,8 @@ def test_fp8_full_size_llama():
     w = synthkv.WORKLOADS["llama3.1-8b-kv-t16k"]
     torch.cuda.empty_cache()
     K, V, lens = synthkv.make_kv(w, seed=0, device=DEV, dtype=F8)
-    assert mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), 0, "l2") == 2
+    # E4M3 caches with several rounds per head group take the three kernels
+    assert mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), 0, "l2") == 0
     Ko, Vo, idx, kept = _fused(K, V, 0.5, "l2", 0, lens)
     assert torch.all(kept == w.t_max // 2)
     ii = idx.long()
