@@ -285,10 +285,11 @@ int32_t mkv_compress_num_stages(void);
 
 /* Which a1 + a2 path mkv_compress takes on the current device for this
  * shape, window and mode: 1 the single-pass kernel (opt-in, K read once),
- * 2 the head-group kernel (the default when a unit of windows fits in L2 and,
- * for head dims up to 128 with several rounds per group, its modelled cost is
- * below the three kernels': K read from HBM once, the second read hits L2), 0
- * the three-kernel path (K read twice); -1 on a bad argument or CUDA error.
+ * 2 the head-group kernel (the default when a unit of windows fits in L2
+ * and, with several rounds per group, the cache is bf16 and, for head dims up
+ * to 128, its modelled cost is below the three kernels': K read from HBM
+ * once, the second read hits L2), 0 the three-kernel path (K read twice); -1
+ * on a bad argument or CUDA error.
  * All give bit-identical results. */
 int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode);
 
