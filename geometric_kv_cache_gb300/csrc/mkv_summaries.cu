@@ -12,10 +12,13 @@
 //
 // Layout: one window per 8-lane group. Lane q of a group owns dims
 // [64k + 8q, 64k + 8q + 8) of every row for k < d/64 (one 16-byte load per
-// 64 bf16 dims, 8-byte for E4M3, each group reading whole lines). Sums run per dim in token order
-// in fp32, so no lane talks to another for the mean. The radius pass re-reads
-// the window's rows (from L1/L2), sums its 16 squared offsets per lane, then
-// sums over the group with an xor butterfly (the same bits on every lane).
+// 64 bf16 dims, 8-byte for E4M3, each group reading whole lines). Sums run
+// per dim in token order in fp32, so no lane talks to another for the mean.
+// The radius sums each row's squared offsets per lane, then over the group
+// with an xor butterfly (the same bits on every lane). Windows of at most 16
+// rows keep their rows in registers from the mean to the radius
+// (k_small_window_regs); longer ones re-read them from L1/L2
+// (k_small_window_means). Both give the same bits.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
