@@ -260,6 +260,15 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s
     return before_warp + x - v;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream drains;
+// it must wait here before it reads that kernel's outputs (a no-op for an
+// ordinary launch). The previous kernel allows the early launch with
+// pdl_trigger() (persistent kernels call it at their start: the dependent
+// CTAs can only become resident as theirs exit).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Nanoseconds since an arbitrary origin (the GPU's global timer); bounds
 // every wait in the kernels.
 __device__ __forceinline__ uint64_t global_ns()

@@ -37,6 +37,7 @@ k_gather_rows(const int32_t *__restrict__ idx, int idx_stride, const int32_t *__
     constexpr int SLOTS = kStreamThreads / LPR;  // rows per CTA per load step
     constexpr int R = kGatherRows / SLOTS;       // rows per lane group
     const int hw = threadIdx.x / LPR, lr = threadIdx.x % LPR;
+    pdl_wait();  // the indices of the previous kernel are complete
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int64_t head = item / blocks_per_head;
         const int j0 = (int)(item - head * blocks_per_head) * kGatherRows;
@@ -105,7 +106,18 @@ cudaError_t launch_gather(const Geometry &g, const int32_t *idx, int32_t idx_str
     const uint8_t *Kb = static_cast<const uint8_t *>(K), *Vb = static_cast<const uint8_t *>(V);
     uint8_t *Ko = static_cast<uint8_t *>(K_out), *Vo = static_cast<uint8_t *>(V_out);
     void *args[] = {&idx, &idx_stride, &kept, &t_max, &keep_stride, &bph_arg, &n_items, &Kb, &Vb, &Ko, &Vo, &status};
-    return cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kStreamThreads), args, 0, st);
+    // launched as a programmatic dependent of the select / compaction kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kStreamThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace mkv

@@ -110,6 +110,8 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
     __shared__ uint32_t s_cand[kSelectCandidates];
     const int lane = threadIdx.x & 31;
     constexpr int kUnroll = 4;
+    pdl_wait();     // the scores of the previous kernel are complete
+    pdl_trigger();  // the gather may start launching as this kernel's CTAs exit
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
         int64_t head = item;
         int T, nk, seg = 0;  // segment [seg, seg + T) of the head's tokens
@@ -551,8 +553,20 @@ cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         const int grid = grid_for_items(reinterpret_cast<const void *>(kern), kSelectThreads, smem, g.n_heads);
-        kern<<<grid, kSelectThreads, smem, st>>>(S, seq_lens, g.heads, g.t_max, ratio, n_keep, keep_stride, g.n_heads,
-                                                 0, 1, cut, chunk_info, g.nch, kept, idx, idx_stride, status);
+        // launched as a programmatic dependent of the score kernel
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kSelectThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, S, seq_lens, (int)g.heads, (int)g.t_max, ratio, n_keep, (int)keep_stride,
+                               (int64_t)g.n_heads, 0, 1, cut, chunk_info, (int)g.nch, kept, idx, (int)idx_stride, status);
+        if (e != cudaSuccess) return e;
     } else {
         auto *kern = k_select<false, false, kSelectThreadsL2>;
         const int grid = grid_for(kern, kSelectThreadsL2, g.n_heads);

@@ -924,6 +924,7 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, ui
     __shared__ int64_t s_off[kMaxSlots];  // partial-sum offset of each stashed piece
     const int groups = gridDim.x / gsize;
     const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
+    pdl_trigger();  // the select may start launching as this kernel's CTAs exit
     if (group >= groups) return;  // a launch is always a whole number of groups
     // Every group does the same work per round, so groups that start
     // together stay in phase: all read HBM (pass 1) at once, then all read L2
