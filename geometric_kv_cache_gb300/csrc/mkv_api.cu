@@ -270,8 +270,8 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
                                        const_cast<void *>(V), status, st)) != cudaSuccess)
             return cuda_status(e);
     } else if (K_out &&
-               (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st)) !=
-                   cudaSuccess) {
+               (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st,
+                                  !quota && emit && select_single_wave(g))) != cudaSuccess) {
         return cuda_status(e);
     }
     if (!mark(6)) return MKV_ERR_CUDA;

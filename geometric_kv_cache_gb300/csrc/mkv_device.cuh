@@ -264,8 +264,8 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s
 // serialization may start while the previous kernel on the stream drains;
 // it must wait here before it reads that kernel's outputs (a no-op for an
 // ordinary launch). The previous kernel allows the early launch with
-// pdl_trigger() (persistent kernels call it at their start: the dependent
-// CTAs can only become resident as theirs exit).
+// pdl_trigger(); persistent kernels call it when a CTA starts its last item,
+// since dependent CTAs that wait through many rounds slow those rounds down.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

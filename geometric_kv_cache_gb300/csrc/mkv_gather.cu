@@ -92,7 +92,7 @@ const void *gather_fn(int row_bytes)
 
 cudaError_t launch_gather(const Geometry &g, const int32_t *idx, int32_t idx_stride, const int32_t *kept,
                           int32_t keep_stride, const void *K, const void *V, void *K_out, void *V_out,
-                          uint32_t *status, cudaStream_t st)
+                          uint32_t *status, cudaStream_t st, bool pdl)
 {
     const int bph = (keep_stride + kGatherRows - 1) / kGatherRows;
     const int64_t items = g.n_heads * bph;
@@ -106,7 +106,7 @@ cudaError_t launch_gather(const Geometry &g, const int32_t *idx, int32_t idx_str
     const uint8_t *Kb = static_cast<const uint8_t *>(K), *Vb = static_cast<const uint8_t *>(V);
     uint8_t *Ko = static_cast<uint8_t *>(K_out), *Vo = static_cast<uint8_t *>(V_out);
     void *args[] = {&idx, &idx_stride, &kept, &t_max, &keep_stride, &bph_arg, &n_items, &Kb, &Vb, &Ko, &Vo, &status};
-    // launched as a programmatic dependent of the select / compaction kernel
+    // with pdl: launched as a programmatic dependent of a one-wave select
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kStreamThreads);
@@ -116,7 +116,7 @@ cudaError_t launch_gather(const Geometry &g, const int32_t *idx, int32_t idx_str
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

@@ -101,6 +101,11 @@ cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan
 // needed); else with chunk_info it computes the per-chunk output offsets and
 // the kept counts for k_compact (the fused path's fourth pass).
 bool select_emits_indices(const Geometry &g);
+// True when the shared-memory select gives every head a CTA at once (one
+// wave): then it and the gather after it run as programmatic dependent
+// launches (measured to hide the launch gaps there, and to slow down a
+// select of many rounds).
+bool select_single_wave(const Geometry &g);
 cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_lens, double ratio,
                           const int32_t *n_keep, int32_t keep_stride, mkv_cut *cut, int2 *chunk_info,
                           int32_t *kept, int32_t *idx, int32_t idx_stride, uint32_t *status, cudaStream_t st);
@@ -138,6 +143,6 @@ cudaError_t launch_compact(const Geometry &g, const float *S, const mkv_cut *cut
 // K_out/V_out rows [head][j] = K/V[head][idx[head * idx_stride + j]] for j < kept[head].
 cudaError_t launch_gather(const Geometry &g, const int32_t *idx, int32_t idx_stride, const int32_t *kept,
                           int32_t keep_stride, const void *K, const void *V, void *K_out, void *V_out,
-                          uint32_t *status, cudaStream_t st);
+                          uint32_t *status, cudaStream_t st, bool pdl = false);
 
 }  // namespace mkv

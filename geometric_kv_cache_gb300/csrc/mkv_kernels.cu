@@ -110,9 +110,11 @@ k_select(const float *__restrict__ S, const int32_t *__restrict__ seq_lens, int 
     __shared__ uint32_t s_cand[kSelectCandidates];
     const int lane = threadIdx.x & 31;
     constexpr int kUnroll = 4;
-    pdl_wait();     // the scores of the previous kernel are complete
-    pdl_trigger();  // the gather may start launching as this kernel's CTAs exit
+    pdl_wait();  // the scores of the previous kernel are complete
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+        // the gather may start launching once every CTA is on its last item
+        // (earlier, its waiting CTAs would slow a select of many rounds)
+        if (item + gridDim.x >= n_items) pdl_trigger();
         int64_t head = item;
         int T, nk, seg = 0;  // segment [seg, seg + T) of the head's tokens
         int32_t *idx_head = nullptr;
@@ -542,6 +544,18 @@ int grid_for(Kern kernel, int threads, int64_t items)
 
 bool select_emits_indices(const Geometry &g) { return g.t_max <= kSelectSmemScores; }
 
+bool select_single_wave(const Geometry &g)
+{
+    if (g.n_heads == 0 || g.t_max > kSelectSmemScores) return false;
+    auto *kern = k_select<true, false, kSelectThreads>;
+    const size_t smem = (size_t)g.t_max * sizeof(float);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return grid_for_items(reinterpret_cast<const void *>(kern), kSelectThreads, smem, g.n_heads) >= g.n_heads;
+}
+
 cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_lens, double ratio,
                           const int32_t *n_keep, int32_t keep_stride, mkv_cut *cut, int2 *chunk_info,
                           int32_t *kept, int32_t *idx, int32_t idx_stride, uint32_t *status, cudaStream_t st)
@@ -563,7 +577,7 @@ cudaError_t launch_select(const Geometry &g, const float *S, const int32_t *seq_
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = grid >= g.n_heads ? 1 : 0;  // one wave only (select_single_wave)
         e = cudaLaunchKernelEx(&cfg, kern, S, seq_lens, (int)g.heads, (int)g.t_max, ratio, n_keep, (int)keep_stride,
                                (int64_t)g.n_heads, 0, 1, cut, chunk_info, (int)g.nch, kept, idx, (int)idx_stride, status);
         if (e != cudaSuccess) return e;

@@ -924,7 +924,6 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, ui
     __shared__ int64_t s_off[kMaxSlots];  // partial-sum offset of each stashed piece
     const int groups = gridDim.x / gsize;
     const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
-    pdl_trigger();  // the select may start launching as this kernel's CTAs exit
     if (group >= groups) return;  // a launch is always a whole number of groups
     // Every group does the same work per round, so groups that start
     // together stay in phase: all read HBM (pass 1) at once, then all read L2
@@ -956,6 +955,8 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, ui
     const int64_t n_units = g.n_heads * upw;
     uint32_t round = 0;
     for (int64_t unit = group; unit < n_units; unit += groups, ++round) {
+        // the select may start launching once every CTA is on its last unit
+        if (unit + groups >= n_units) pdl_trigger();
         const int64_t head = unit / upw;
         const int w0 = (int)(unit - head * upw) * wb;
         const int T = head_len(P.seq_lens, head, g.heads, g.t_max, P.status, threadIdx.x == 0 && rank == 0 && w0 == 0);
