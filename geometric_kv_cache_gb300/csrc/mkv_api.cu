@@ -609,8 +609,8 @@ mkv_status mkv_compress_oja(const void *K, const void *V, const void *Q, const f
     if (!emit &&
         (e = launch_compact(g, S, cut, chunk, shape.seq_lens, keep_stride, idx_w, idx_stride, status, st)) != cudaSuccess)
         return cuda_status(e);
-    if (K_out &&
-        (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st)) != cudaSuccess)
+    if (K_out && (e = launch_gather(g, idx_w, idx_stride, kept_w, keep_stride, K, V, K_out, V_out, status, st,
+                                    emit && select_single_wave(g))) != cudaSuccess)
         return cuda_status(e);
     return MKV_OK;
 }
