@@ -262,6 +262,26 @@ def oracle_throughput(K_host, V_host, lens, heads_per_row, ratio, mode, window, 
     return tokens / spent, min(done, limit), tokens, spent
 
 
+def host_cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def host_threads():
     """Host cores this process may use."""
     try:
@@ -391,7 +411,7 @@ def run_ours(args):
                                                       budget_s=args.cpu_budget / 2)
         tps, done, tok, spent = oracle_throughput(hKc, hVc, lens_list, w.heads, ratio, mode, window,
                                                   budget_s=args.cpu_budget / 2, chunk=1, threads=nt)
-        cpu = {"value": tps, "unit": UNIT, "cores": nt, "kind": "oracle",
+        cpu = {"value": tps, "unit": UNIT, "cores": nt, "cpu_model": host_cpu_model(), "kind": "oracle",
                "sample": f"the {w.n_heads} heads cycled for {spent:.1f} s of wall time ({tok} token rows), fp64 C "
                          f"oracle, {nt} threads over heads",
                "single_thread": {"value": tps1, "cores": 1,
@@ -493,7 +513,8 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; same generator and workload)",
         "config": {"workload": w.name, "heads_total": w.n_heads, "t": w.t_max, "head_dim": w.head_dim,
                    "mode": mode, "window": window, "ratio": ratio, "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(batches), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(batches), "cpu_model": host_cpu_model(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
