@@ -551,7 +551,7 @@ def run_secondary(args):
     hbm = peaks["hbm_gbs"]
     steps = args.steps
     if args.path == "oja":
-        w = synthkv.WORKLOADS[args.workload]
+        w = workload_run(args.workload, args.layers)[0]
         K, V, lens = synthkv.make_kv(w, seed=args.seed, device=dev)
         M, r, ratio = args.oja_queries, args.oja_rank, 0.5
         Q, U = synthkv.make_oja_inputs(w, args.seed, M, r, device=dev)
@@ -597,7 +597,7 @@ def run_secondary(args):
                                         "note": "2 x 2 x n_query x 128 flop per token (hi and lo operand rows)"}},
                 "clocks": clocks.summary(), "gpu_launches": steps * 4}
     elif args.path == "summaries":
-        w = synthkv.WORKLOADS[args.workload]
+        w = workload_run(args.workload, args.layers)[0]
         K, V, lens = synthkv.make_kv(w, seed=args.seed, device=dev)
         W = args.cluster
         nw = mkv.mkv_num_windows(w.t_max, W)
@@ -669,8 +669,8 @@ def run_secondary(args):
                 "gpu_launches": steps * ((1 if mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
                                           in (1, 2) else 3) + 2)}
     else:  # quota
-        w = synthkv.WORKLOADS["qwen3-8b-kv-t64k-w4096"] if args.workload == synthkv.BENCH_WORKLOAD else \
-            synthkv.WORKLOADS[args.workload]
+        w = workload_run("qwen3-8b-kv-t64k-w4096" if args.workload == synthkv.BENCH_WORKLOAD else args.workload,
+                         args.layers)[0]
         K, V, lens = synthkv.make_kv(w, seed=args.seed, device=dev)
         mode, window, ratio = w.runs[0]
         window = window or 4096
