@@ -42,7 +42,12 @@
  *   pointers must be 16-byte aligned; float / int32 arrays 4-byte aligned; the
  *   workspace 256-byte aligned.
  * Streams. All work is enqueued on `stream` (NULL = the legacy default
- *   stream); results are valid in stream order.
+ *   stream); results are valid in stream order. Inside a call some kernels
+ *   start as programmatic dependent launches of the previous one, and some
+ *   kernels allow the next launch on the stream to start early; a kernel the
+ *   caller launches right after a call with programmatic stream
+ *   serialization must wait for its dependency (cudaGridDependencySynchronize)
+ *   before it reads the call's outputs, as it must after any kernel.
  * Errors. Arguments are checked on the host before anything is enqueued; a
  *   bad argument returns a status and enqueues nothing. A failed launch
  *   returns MKV_ERR_CUDA. Problems only the GPU can see (a seq_lens entry
