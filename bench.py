@@ -737,13 +737,18 @@ def main(argv=None):
     if args.traffic_json and os.path.exists(args.traffic_json):
         with open(args.traffic_json) as f:
             t = json.load(f)
-        # counters only count while the kernels they were taken on are unchanged
-        src = os.path.join(ROOT, t.get("kernel_source", "geometric_kv_cache_gb300/csrc/mkv_gather.cu"))
-        if not os.path.exists(src):
-            t = {}
-            src = os.path.join(ROOT, "bench.py")
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        # counters only count while the kernels they were taken on are unchanged:
+        # the sha256 of the kernel's source files, concatenated in the listed order
+        srcs = t.get("kernel_source", "geometric_kv_cache_gb300/csrc/mkv_gather.cu")
+        srcs = [os.path.join(ROOT, x) for x in (srcs if isinstance(srcs, list) else [srcs])]
+        h = hashlib.sha256()
+        for src in srcs:
+            if not os.path.exists(src):
+                t = {}
+                break
+            with open(src, "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()[:16]
         if (t.get("workload") == args.workload and not args.layers and t.get("kernel_source_sha256_16") == sha
                 and t.get("cache_dtype", "bf16") == args.dtype):
             args.traffic = t.get("bytes_per_launch")

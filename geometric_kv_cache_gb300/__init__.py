@@ -48,7 +48,7 @@ EXPORTED = (
     "mkv_compress_noalloc", "mkv_compress_single_pass", "mkv_set_single_pass", "mkv_layer_budgets",
     "mkv_inject_stalled_windows", "mkv_window_means", "mkv_num_keep_quota", "mkv_select_quota",
     "mkv_compress_quota", "mkv_oja_workspace_size", "mkv_oja_score", "mkv_compress_oja", "mkv_oja_score_profiled",
-    "mkv_compress_inplace", "mkv_set_head_groups", "mkv_centroid_score",
+    "mkv_compress_inplace", "mkv_set_head_groups", "mkv_set_fused", "mkv_centroid_score",
 )
 
 
@@ -101,6 +101,7 @@ def load(build_if_missing: bool = True):
             "mkv_compress_single_pass": (i32, [MkvShape, i32, i32]),
             "mkv_set_single_pass": (i32, [i32]),
             "mkv_set_head_groups": (i32, [i32]),
+            "mkv_set_fused": (i32, [i32, i32]),
             "mkv_centroid_score": (i32, [vp, MkvShape, i32, i32, vp, vp, vp, sz, vp]),
             "mkv_layer_budgets": (i32, [vp, i32, f64, f64, ctypes.c_int64, vp, vp]),
             "mkv_inject_stalled_windows": (i32, [vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
@@ -206,6 +207,13 @@ def mkv_set_single_pass(enable: bool) -> bool:
 def mkv_set_head_groups(enable: bool) -> bool:
     """Allow or forbid the head-group kernel; returns the previous setting."""
     return bool(load().mkv_set_head_groups(1 if enable else 0))
+
+
+def mkv_set_fused(scorer_ctas: int, lookahead: int = 0) -> int:
+    """Allow (scorer_ctas > 0) or forbid (0) the fused whole-path kernel in
+    mkv_compress; lookahead > 0 sets how many heads the selects run ahead of
+    the gathers. Returns the previous scorer budget."""
+    return int(load().mkv_set_fused(int(scorer_ctas), int(lookahead)))
 
 
 def mkv_layer_budgets(sensitivity, r: float, gamma: float, total: int, cap):

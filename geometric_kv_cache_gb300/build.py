@@ -18,6 +18,7 @@ OUT_DIR = os.path.join(PKG_DIR, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libmkv.so")
 SOURCES = ["mkv_kernels.cu", "mkv_gather.cu", "mkv_inplace.cu", "mkv_summaries.cu", "mkv_oja.cu", "mkv_piece.cu", "mkv_api.cu", "mkv_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "mkv_internal.h"), os.path.join(CSRC, "mkv_device.cuh"),
+           os.path.join(CSRC, "mkv_select.cuh"), os.path.join(CSRC, "mkv_gather.cuh"),
            os.path.join(os.path.dirname(PKG_DIR), "include", "mkv.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

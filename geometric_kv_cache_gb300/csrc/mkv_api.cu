@@ -27,6 +27,10 @@ std::atomic<int> g_single_pass_enabled{0};
 // Whether mkv_compress may use the head-group kernel (one read of K from
 // HBM, global centroids, heads short enough for L2). On by default.
 std::atomic<int> g_head_groups_enabled{1};
+// The fused whole-path kernel (mkv_set_fused): the scorer CTA budget (0: off)
+// and the selects taken ahead of the gathers.
+std::atomic<int> g_fused_scorers{0};
+std::atomic<int> g_fused_lookahead{48};
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -246,13 +250,27 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
         return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
     };
     cudaError_t e = cudaSuccess;
+    int32_t *idx_w = idx ? idx : region<int32_t>(ws, L.idx);
+    const int32_t idx_stride = idx ? keep_stride : g.t_max;
+    // the whole path in one launch, when asked for and the shape allows it
+    const int scorers = g_fused_scorers.load(std::memory_order_relaxed);
+    if (scorers > 0 && !events && !stall_windows && !quota && !in_place && K_out &&
+        g_head_groups_enabled.load(std::memory_order_relaxed) && !g_single_pass_enabled.load(std::memory_order_relaxed)) {
+        const FusedPlan fp = fused_plan(g.pg, (int)mode, L.centroid - L.counters, scorers,
+                                        g_fused_lookahead.load(std::memory_order_relaxed));
+        if (fp.grid > 0) {
+            e = launch_fused(g.pg, fp, (int)mode, K, V, s.seq_lens, region<float>(ws, L.partial),
+                             region<uint32_t>(ws, L.counters), C, S, ratio, n_keep, keep_stride, kept_w, idx_w,
+                             idx_stride, K_out, V_out, status, st);
+            if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e);
+            (void)cudaGetLastError();  // fewer CTAs fit right now: the separate kernels
+        }
+    }
     if (!mark(0)) return MKV_ERR_CUDA;
     // a1 + a2 (C and S are workspace regions here)
     rc = run_centroid_score(g, L, K, s, mode, ws, C, S, st, mark, stall_windows);
     if (rc != MKV_OK) return rc;
     // a3 (+ a4 when the head's scores fit shared memory), then a4, a5
-    int32_t *idx_w = idx ? idx : region<int32_t>(ws, L.idx);
-    const int32_t idx_stride = idx ? keep_stride : g.t_max;
     const bool emit = quota || select_emits_indices(g);
     if (quota)
         e = launch_select_quota(g, S, s.seq_lens, ratio, keep_stride, kept_w, idx_w, idx_stride, status, st);
@@ -638,6 +656,10 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
     }
     if (g_head_groups_enabled.load(std::memory_order_relaxed)) {
         const Layout L = make_layout(g);
+        const int scorers = g_fused_scorers.load(std::memory_order_relaxed);
+        if (scorers > 0 && fused_plan(g.pg, (int)mode, L.centroid - L.counters, scorers,
+                                      g_fused_lookahead.load(std::memory_order_relaxed)).grid > 0)
+            return 3;
         if (head_group_plan(g.pg, (int)mode, L.centroid - L.counters).groups > 0) return 2;
     }
     return 0;
@@ -646,6 +668,12 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
 int32_t mkv_set_head_groups(int32_t enable)
 {
     return g_head_groups_enabled.exchange(enable ? 1 : 0);
+}
+
+int32_t mkv_set_fused(int32_t scorer_ctas, int32_t lookahead)
+{
+    if (lookahead > 0) g_fused_lookahead.store(lookahead);
+    return g_fused_scorers.exchange(scorer_ctas > 0 ? scorer_ctas : 0);
 }
 
 mkv_status mkv_inject_stalled_windows(const void *K, const void *V, mkv_shape shape, double ratio, mkv_mode mode,

@@ -13,19 +13,15 @@
 
 #include "mkv_device.cuh"
 #include "mkv_internal.h"
+#include "mkv_gather.cuh"
 
 namespace mkv {
 namespace {
 
-constexpr int kStreamThreads = 256;
+constexpr int kStreamThreads = kGatherThreads;
 using namespace dev;
 
-// Item = (head, block of 64 output slots). Groups of LPR lanes (LPR = row
-// bytes / 16: 16 bytes per lane) copy rows: K_out[h][j] = K[h][idx[h][j]], V_out
-// likewise, for j < kept[h]; 64 / (256 / LPR) rows of K and of V in flight
-// per lane. No CTA barrier anywhere.
-constexpr int kGatherRows = 64;
-
+// gather_item (one (head, 64-slot) item) is in mkv_gather.cuh.
 template <int LPR>
 __global__ void __launch_bounds__(kStreamThreads)
 k_gather_rows(const int32_t *__restrict__ idx, int idx_stride, const int32_t *__restrict__ kept, int t_max,
@@ -33,47 +29,10 @@ k_gather_rows(const int32_t *__restrict__ idx, int idx_stride, const int32_t *__
               const uint8_t *__restrict__ V, uint8_t *__restrict__ K_out, uint8_t *__restrict__ V_out,
               uint32_t *status)
 {
-    constexpr int RB = LPR * 16;                 // row bytes
-    constexpr int SLOTS = kStreamThreads / LPR;  // rows per CTA per load step
-    constexpr int R = kGatherRows / SLOTS;       // rows per lane group
-    const int hw = threadIdx.x / LPR, lr = threadIdx.x % LPR;
     pdl_wait();  // the indices of the previous kernel are complete
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int64_t head = item / blocks_per_head;
-        const int j0 = (int)(item - head * blocks_per_head) * kGatherRows;
-        const int n = min(kGatherRows, min(kept[head], keep_stride) - j0);
-        if (n <= 0) continue;
-        const int32_t *ih = idx + head * idx_stride + j0;
-        const size_t in_head = (size_t)head * t_max * RB + lr * 16;
-        const size_t out_head = ((size_t)head * keep_stride + j0) * RB + lr * 16;
-        uint4 kv[R], vv[R];
-        int src[R];
-#pragma unroll
-        for (int u = 0; u < R; ++u) {
-            const int j = u * SLOTS + hw;
-            src[u] = j < n ? ih[j] : -1;
-            if (src[u] >= t_max) {
-                atomicOr(status, MKV_DEV_INTERNAL);
-                src[u] = -1;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < R; ++u) {
-            if (src[u] >= 0) {
-                const size_t off = in_head + (size_t)src[u] * RB;
-                kv[u] = ld_stream(K + off);
-                vv[u] = ld_stream(V + off);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < R; ++u) {
-            if (src[u] >= 0) {
-                const size_t off = out_head + (size_t)(u * SLOTS + hw) * RB;
-                st_v4(K_out + off, kv[u]);
-                st_v4(V_out + off, vv[u]);
-            }
-        }
-    }
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x)
+        gather_item<LPR, false>(item, idx, idx_stride, kept, t_max, keep_stride, blocks_per_head, K, V, K_out, V_out,
+                                status);
 }
 
 // The kernel for a row of `row_bytes` bytes (head dim x element size).

@@ -92,6 +92,19 @@ struct HeadGroupPlan {
     uint32_t stagger_ns = 0;  // start delay step: group g waits (g mod 4) steps
 };
 HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counter_bytes);
+// The fused whole-path kernel (global centroids, heads of at most 20480
+// tokens): scorer head groups within `scorer_ctas` CTAs, every resident CTA
+// a select / gather worker afterwards; grid 0 when it does not apply.
+struct FusedPlan {
+    HeadGroupPlan hg;
+    int grid = 0;       // resident CTAs of the launch
+    int lookahead = 0;  // selects taken ahead of the gathers, in heads
+};
+FusedPlan fused_plan(const PieceGeometry &g, int mode, size_t counter_bytes, int scorer_ctas, int lookahead);
+cudaError_t launch_fused(const PieceGeometry &g, const FusedPlan &fp, int mode, const void *K, const void *V,
+                         const int32_t *seq_lens, float *partial, uint32_t *cnt, float *C, float *S, double ratio,
+                         const int32_t *n_keep, int32_t keep_stride, int32_t *kept, int32_t *idx, int32_t idx_stride,
+                         void *K_out, void *V_out, uint32_t *status, cudaStream_t st);
 cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan, const void *K,
                                const int32_t *seq_lens, int mode, float *partial, uint32_t *cnt, float *C, float *S,
                                uint32_t *status, cudaStream_t st);

@@ -1,4 +1,7 @@
-// Centroid and score kernels (steps a1 and a2).
+// Centroid and score kernels (steps a1 and a2), and the opt-in kernel that
+// runs the whole path in one launch (k_fused_path: the head groups' scoring
+// followed, through per-head counters, by the select and gather device
+// functions of mkv_select.cuh and mkv_gather.cuh).
 //
 // Method: "ManifoldKV: Training-Free KV Cache Compression via Euclidean
 // Outlier Detection" (ICML 2026 poster 62526), abstract: every token is
@@ -25,6 +28,8 @@
 
 #include "mkv_device.cuh"
 #include "mkv_internal.h"
+#include "mkv_select.cuh"
+#include "mkv_gather.cuh"
 
 namespace mkv {
 namespace {
@@ -909,9 +914,15 @@ static_assert(kMaxUnitWindows * kMaxDim * sizeof(float) <= kGroupSmem, "means mu
 __host__ __device__ constexpr int stash_slots(int D) { return (int)(kGroupSmem / sizeof(float)) / (kWarps * D); }
 constexpr int kMaxSlots = stash_slots(64);
 
+//
+// head_groups_run is one CTA's share (group `group` of `groups`, rank `rank`
+// in it). With head_done, every CTA of the group adds 1 to head_done[head]
+// once the unit's scores it wrote are visible GPU-wide (units are whole heads
+// there: a group's count reaches gsize when the head's scores are complete).
 template <int MODE, int NB, int ES>
-__global__ void __launch_bounds__(kThreads, 2)
-k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, uint32_t stagger_ns)
+__device__ __forceinline__ void head_groups_run(const PieceGeometry &g, const Pointers &P, uint32_t *gcnt, int gsize,
+                                                int wb, uint32_t stagger_ns, int groups, int group, int rank,
+                                                uint32_t *head_done)
 {
     constexpr int D = 64 * NB, RB = ES * D;
     using Raw = typename Chunk<ES>::raw;
@@ -922,9 +933,6 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, ui
     float *cmean = dyn;
     __shared__ uint32_t s_ok;
     __shared__ int64_t s_off[kMaxSlots];  // partial-sum offset of each stashed piece
-    const int groups = gridDim.x / gsize;
-    const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
-    if (group >= groups) return;  // a launch is always a whole number of groups
     // Every group does the same work per round, so groups that start
     // together stay in phase: all read HBM (pass 1) at once, then all read L2
     // (pass 2). Starting groups (group mod 4) stagger steps late spreads the
@@ -1078,7 +1086,136 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, ui
                 }
             }
         }
+        if (head_done) {  // this CTA's scores of the unit are visible before the count
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) atomicAdd(&head_done[head], 1u);
+        }
         __syncthreads();  // the means are rewritten for the next unit
+    }
+}
+
+template <int MODE, int NB, int ES>
+__global__ void __launch_bounds__(kThreads, 2)
+k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, uint32_t stagger_ns)
+{
+    const int groups = gridDim.x / gsize;
+    const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
+    if (group >= groups) return;  // a launch is always a whole number of groups
+    head_groups_run<MODE, NB, ES>(g, P, gcnt, gsize, wb, stagger_ns, groups, group, rank, nullptr);
+}
+
+// The whole path in one cooperative launch (global centroids, heads of at
+// most kFusedMaxT tokens). CTAs [0, groups * gsize) first score the heads as
+// head groups do (units are whole heads; head_done[h] reaches gsize when the
+// scores of head h are complete). Every CTA -- the scorers once their units
+// are done -- then takes tickets from one counter, in this order: the
+// selects of heads 0 .. L-1, then for each head h the select of head h + L
+// (if any) and the gather items of head h (128 output slots each for rows of
+// 256 bytes). A select waits for its head's scores and publishes
+// sel_done[h]; a gather item waits for sel_done[h]. Selects thus run about L heads ahead of the gathers while
+// the scorers still stream K, and the gathers fill HBM while the scorers are
+// in their L2 pass, barriers and means. Scorers wait only on their own
+// group, selects only on scorers, gathers only on selects taken earlier in
+// ticket order, so with every CTA resident each wait ends; each is also
+// bounded in time (a wait that runs out sets MKV_DEV_TIMEOUT and its work is
+// skipped: the head keeps no rows). The arithmetic is that of the head-group,
+// select and gather kernels, so the outputs are the same bits.
+constexpr int kFusedMaxT = (int)(kGroupSmem / sizeof(float));  // the select keeps a head's scores in shared memory
+// output slots per gather ticket: 8 rows of K and 8 of V in flight per lane
+// (128 slots for 256-byte rows)
+__host__ __device__ constexpr int fused_gather_rows(int row_bytes) { return 8 * kGatherThreads * 16 / row_bytes; }
+static_assert(kThreads == kGatherThreads, "gather items assume the head-group CTA size");
+
+struct TailArgs {
+    const uint8_t *V;
+    uint8_t *K_out, *V_out;
+    const int32_t *n_keep;
+    int32_t *kept, *idx;
+    uint32_t *head_done, *sel_done, *ticket;
+    double ratio;
+    int keep_stride, idx_stride, bph, lookahead;
+};
+
+// Thread 0 waits until *flag >= target (bounded); 1 when it got there. With
+// `abortable` it also gives up once any wait of the launch has timed out, so
+// that a failure drains in about one wait bound (a timeout bit already set
+// when the CTA started is not taken for one of this launch).
+__device__ __forceinline__ uint32_t wait_count(const uint32_t *flag, uint32_t target, uint32_t *status, bool abortable)
+{
+    const uint64_t t0 = global_ns();
+    for (uint32_t spin = 0; ld_acquire(flag) < target; ++spin) {
+        if ((spin & 63u) == 63u) {
+            if (abortable && timed_out(status)) return 0u;
+            if (global_ns() - t0 > kWaitNs) {
+                atomicOr(status, MKV_DEV_TIMEOUT);
+                return 0u;
+            }
+            __nanosleep(256);
+        }
+    }
+    return 1u;
+}
+
+template <int MODE, int NB, int ES>
+__global__ void __launch_bounds__(kThreads, 2)
+k_fused_path(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int groups, uint32_t stagger_ns, TailArgs A)
+{
+    constexpr int LPR = 4 * NB * ES;  // lanes per row: row bytes / 16
+    __shared__ uint32_t s_ticket, s_go, s_abortable;
+    if (threadIdx.x == 0) s_abortable = timed_out(P.status) ? 0u : 1u;  // read before any wait of this CTA
+    __syncthreads();
+    if ((int)blockIdx.x < groups * gsize)
+        head_groups_run<MODE, NB, ES>(g, P, gcnt, gsize, 1, stagger_ns, groups, (int)blockIdx.x / gsize,
+                                      (int)blockIdx.x % gsize, A.head_done);
+    const int64_t n_heads = g.n_heads, L = A.lookahead, blk = (int64_t)A.bph + 1;
+    const int64_t n_tickets = L + n_heads * blk;
+    // Thread 0 claims the next ticket while the CTA works on the current one.
+    // A claimed ticket waits, at worst, on a select with a lower ticket, so
+    // the chain of waits always ends at a ticket that can run.
+    uint32_t next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(A.ticket, 1u);
+    for (;;) {
+        __syncthreads();  // s_ticket and s_go of the previous ticket are read; shared memory is free
+        if (threadIdx.x == 0) {
+            s_ticket = next;
+            if ((int64_t)next < n_tickets) next = atomicAdd(A.ticket, 1u);
+        }
+        __syncthreads();
+        const int64_t t = s_ticket;
+        if (t >= n_tickets) break;  // the same for every thread
+        int64_t head;
+        int item = -1;  // -1: the head's select; else its gather item
+        if (t < L) {
+            head = t;
+        } else {
+            const int64_t u = t - L, h = u / blk, r = u - h * blk;
+            if (r == 0) {
+                head = h + L;
+                if (head >= n_heads) continue;
+            } else {
+                head = h;
+                item = (int)r - 1;
+            }
+        }
+        if (threadIdx.x == 0)
+            s_go = item < 0 ? wait_count(A.head_done + head, (uint32_t)gsize, P.status, s_abortable != 0u)
+                            : wait_count(A.sel_done + head, 1u, P.status, s_abortable != 0u);
+        __syncthreads();
+        if (item < 0) {
+            if (s_go)
+                select_item<true, false, kThreads>(head, P.S, P.seq_lens, g.heads, g.t_max, A.ratio, A.n_keep,
+                                                   A.keep_stride, 0, g.nwin_max, nullptr, nullptr, 0, A.kept, A.idx,
+                                                   A.idx_stride, P.status);
+            else if (threadIdx.x == 0)
+                A.kept[head] = 0;  // its gather items copy nothing
+            __threadfence();  // the indices and the kept count are visible before the flag
+            __syncthreads();
+            if (threadIdx.x == 0) atomicExch(A.sel_done + head, 1u);
+        } else if (s_go) {
+            gather_item<LPR, true, fused_gather_rows(16 * LPR)>(head * A.bph + item, A.idx, A.idx_stride, A.kept, g.t_max,
+                                                         A.keep_stride, A.bph, P.K, A.V, A.K_out, A.V_out, P.status);
+        }
     }
 }
 
@@ -1156,6 +1293,23 @@ const void *head_groups_fn(int d, int es, int mode)
 }
 
 template <int ES>
+const void *fused_fn_es(int d, int mode)
+{
+    const bool l2 = mode == MKV_MODE_L2;
+    switch (d) {
+    case 64: return l2 ? (const void *)k_fused_path<MKV_MODE_L2, 1, ES> : (const void *)k_fused_path<MKV_MODE_COSINE, 1, ES>;
+    case 128: return l2 ? (const void *)k_fused_path<MKV_MODE_L2, 2, ES> : (const void *)k_fused_path<MKV_MODE_COSINE, 2, ES>;
+    case 256: return l2 ? (const void *)k_fused_path<MKV_MODE_L2, 4, ES> : (const void *)k_fused_path<MKV_MODE_COSINE, 4, ES>;
+    default: return nullptr;
+    }
+}
+
+const void *fused_fn(int d, int es, int mode)
+{
+    return es == 2 ? fused_fn_es<2>(d, mode) : es == 1 ? fused_fn_es<1>(d, mode) : nullptr;
+}
+
+template <int ES>
 const void *piece_scores_fn_es(int d, int mode)
 {
     const bool l2 = mode == MKV_MODE_L2;
@@ -1200,14 +1354,14 @@ const void *window_means_fn(int d)
 
 }  // namespace
 
-HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
+namespace {
+
+// Group count, group size and unit size for `resident` CTAs; `alone` applies
+// the comparison with the three-kernel path (the head-group kernel on its
+// own), which the fused kernel does not take.
+HeadGroupPlan plan_groups(const PieceGeometry &g, int resident, size_t counters, bool alone)
 {
     HeadGroupPlan plan;
-    if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max == 0) return plan;
-    const void *fn = head_groups_fn(g.d, g.es, mode);
-    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
-        return plan;
-    const int resident = resident_grid(fn, kThreads, kGroupSmem);
     int dev = 0, l2 = 0;
     if (resident < 16 || cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0)
@@ -1258,13 +1412,78 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
         // of K does not pay for the rounds (256 x 16K: head groups 0.250 ms,
         // three kernels 0.243; cosine 0.294 against 0.289).
         const double three = 2.0 * (double)g.n_heads * g.nwin_max * g.ppw / (double)resident;
-        if (rounds >= 4 && (g.es == 1 || (g.d <= 128 && best >= three))) return HeadGroupPlan{};
+        if (alone && rounds >= 4 && (g.es == 1 || (g.d <= 128 && best >= three))) return HeadGroupPlan{};
         // the stagger step: a third of the time the units in flight take to
         // stream from HBM (at 6.5 TB/s), when every group has 4 rounds or more
         const double round_ns = (double)plan.groups * plan.wb * window_bytes / 6500.0;  // 6.5 TB/s = 6500 B/ns
         plan.stagger_ns = rounds >= 4 ? (uint32_t)std::min(20000.0, round_ns / 3.0) : 0u;
     }
     return plan;
+}
+
+}  // namespace
+
+HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
+{
+    if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max == 0) return HeadGroupPlan{};
+    const void *fn = head_groups_fn(g.d, g.es, mode);
+    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
+        return HeadGroupPlan{};
+    return plan_groups(g, resident_grid(fn, kThreads, kGroupSmem), counters, true);
+}
+
+FusedPlan fused_plan(const PieceGeometry &g, int mode, size_t counters, int scorer_ctas, int lookahead)
+{
+    FusedPlan fp;
+    // whole heads as units, and each head's scores fit the select's shared memory
+    if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max != 1 || g.t_max > kFusedMaxT || scorer_ctas <= 0) return fp;
+    const void *fn = fused_fn(g.d, g.es, mode);
+    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
+        return fp;
+    const int resident = resident_grid(fn, kThreads, kGroupSmem);
+    if (resident < 16) return fp;
+    const HeadGroupPlan hp = plan_groups(g, std::min(scorer_ctas, resident), counters, false);
+    if (hp.groups == 0 || hp.wb != 1) return fp;
+    // counters: the groups' arrivals, head_done, sel_done and the ticket
+    if (((size_t)hp.groups + 2 * (size_t)g.n_heads + 1) * sizeof(uint32_t) > counters) return fp;
+    fp.hg = hp;
+    fp.grid = resident;
+    fp.lookahead = (int)std::max<int64_t>(1, std::min<int64_t>(lookahead > 0 ? lookahead : 48, g.n_heads));
+    return fp;
+}
+
+cudaError_t launch_fused(const PieceGeometry &g, const FusedPlan &fp, int mode, const void *K, const void *V,
+                         const int32_t *seq_lens, float *partial, uint32_t *cnt, float *C, float *S, double ratio,
+                         const int32_t *n_keep, int32_t keep_stride, int32_t *kept, int32_t *idx, int32_t idx_stride,
+                         void *K_out, void *V_out, uint32_t *status, cudaStream_t st)
+{
+    const void *fn = fused_fn(g.d, g.es, mode);
+    if (!fn || fp.grid <= 0) return cudaErrorInvalidValue;
+    const size_t words = (size_t)fp.hg.groups + 2 * (size_t)g.n_heads + 1;
+    cudaError_t e = cudaMemsetAsync(cnt, 0, words * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    Pointers P = make_pointers(K, seq_lens, partial, C, S, status);
+    TailArgs A;
+    A.V = static_cast<const uint8_t *>(V);
+    A.K_out = static_cast<uint8_t *>(K_out);
+    A.V_out = static_cast<uint8_t *>(V_out);
+    A.n_keep = n_keep;
+    A.kept = kept;
+    A.idx = idx;
+    A.head_done = cnt + fp.hg.groups;
+    A.sel_done = A.head_done + g.n_heads;
+    A.ticket = A.sel_done + g.n_heads;
+    A.ratio = ratio;
+    A.keep_stride = keep_stride;
+    A.idx_stride = idx_stride;
+    const int rows = fused_gather_rows(g.d * g.es);
+    A.bph = (keep_stride + rows - 1) / rows;
+    A.lookahead = fp.lookahead;
+    PieceGeometry gg = g;
+    int gsize = fp.hg.gsize, groups = fp.hg.groups;
+    uint32_t stagger = fp.hg.stagger_ns;
+    void *args[] = {&gg, &P, &cnt, &gsize, &groups, &stagger, &A};
+    return cudaLaunchCooperativeKernel(fn, dim3((unsigned)fp.grid), dim3(kThreads), args, kGroupSmem, st);
 }
 
 cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan, const void *K,
