@@ -320,9 +320,13 @@ def run_ours(args):
     ws = mkv.workspace_for(K, window, lens)
     stream = torch.cuda.current_stream(dev)
     lens_list = lens.cpu().tolist()
+    if args.fused > 0:
+        mkv.mkv_set_fused(args.fused, args.fused_lookahead)
     single = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
+    if args.fused > 0 and single != 3:
+        raise SystemExit("--fused: the fused kernel does not apply to this workload (global centroids, t <= 20480)")
     select_emits = T <= 40960  # select writes the kept indices itself (no compaction kernel)
-    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single in (1, 2) else 2, es=es)
+    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single in (1, 2, 3) else 2, es=es)
 
     def step():
         mkv.mkv_compress(K, V, ratio, mode, window, ks, K_out, V_out, idx, kept, ws, lens, stream=stream)
@@ -349,7 +353,9 @@ def run_ours(args):
     tokens_all = sum_over_ranks(float(nbytes["tokens"]))
     value = tokens_all / (ms / 1e3)
 
-    # per-kernel durations inside the real call (events on the launching stream)
+    # per-kernel durations inside the real call (events on the launching stream);
+    # the profiled call runs the separate kernels, so with --fused the one
+    # kernel's time is the step's (one launch after a counter reset)
     ns = mkv.mkv_compress_num_stages()
     prof_steps = max(10, min(args.steps, 200))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(prof_steps)]
@@ -363,7 +369,10 @@ def run_ours(args):
     dom = max((j for j in range(ns) if nbytes[STAGES[j]] > 0), key=lambda j: stage_ms[j])
     peaks = measured_peaks()
     dom_name = STAGES[dom]
-    achieved = nbytes[dom_name] / (stage_ms[dom] / 1e3) / 1e9
+    dom_bytes, dom_ms = nbytes[dom_name], stage_ms[dom]
+    if single == 3:  # the one kernel moves K once, writes the scores, and gathers
+        dom_name, dom_bytes, dom_ms = "fused_path", nbytes["piece_sums"] + nbytes["gather"], ms_local
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     traffic = args.traffic.get(dom_name) if args.traffic else None
 
     # end to end through the host-buffer entry point
@@ -437,7 +446,10 @@ def run_ours(args):
                    "heads_total": w.n_heads, "t": T, "head_dim": w.head_dim, "mode": mode,
                    "window": window, "ratio": ratio, "keep_per_head": ks,
                    "centroid_score_path": {0: "three kernels (K read twice)", 1: "single pass (K read once)",
-                                           2: "head groups (K read from HBM once, again from L2)"}.get(single, "?"),
+                                           2: "head groups (K read from HBM once, again from L2)",
+                                           3: "fused whole path (one launch: head groups, selects, gathers; "
+                                              f"scorer budget {args.fused}, lookahead {args.fused_lookahead})"
+                                           }.get(single, "?"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "no flush: K+V (%.1f GB) exceed the 129 MB L2" % (2 * K.numel() * es / 1e9)},
         "hbm": {"path_bytes_per_step": nbytes["path"], "achieved_gbs": hbm_gbs,
@@ -445,14 +457,15 @@ def run_ours(args):
                 "frac_of_measured": hbm_gbs / world / peaks["hbm_gbs"]},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                     "traffic": traffic, "algorithmic_bytes_per_launch": nbytes[dom_name],
-                     "ms_per_launch": stage_ms[dom]},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes,
+                     "ms_per_launch": dom_ms},
         "stages_ms": dict(zip(STAGES, stage_ms)),
         "cpu_baseline": cpu,
         "e2e": e2e,
         # per step: a1 + a2 (one kernel, or piece sums + window means + scores),
         # select, compaction when select did not emit the indices, gather
-        "gpu_launches": args.steps * ((1 if single in (1, 2) else 3) + 1 + (0 if select_emits else 1) + 1),
+        "gpu_launches": args.steps * (1 if single == 3 else
+                                      (1 if single in (1, 2) else 3) + 1 + (0 if select_emits else 1) + 1),
         "clocks": clocks.summary(),
     }
     if world > 1:
@@ -730,6 +743,9 @@ def main(argv=None):
     ap.add_argument("--cluster", type=int, default=10, help="cluster length (--path summaries)")
     ap.add_argument("--dtype", choices=sorted(CACHE_DTYPE_NAMES), default="bf16",
                     help="cache element type: bf16, or fp8 (E4M3 codes; the ManifoldKV path only)")
+    ap.add_argument("--fused", type=int, default=0,
+                    help="time the opt-in fused whole-path kernel with this scorer CTA budget (0: the default path)")
+    ap.add_argument("--fused-lookahead", type=int, default=48, help="selects ahead of the gathers (--fused)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
                     help="per-kernel DRAM bytes per launch from an ncu capture (null when absent)")
     args = ap.parse_args(argv)
