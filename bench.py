@@ -320,10 +320,10 @@ def run_ours(args):
     ws = mkv.workspace_for(K, window, lens)
     stream = torch.cuda.current_stream(dev)
     lens_list = lens.cpu().tolist()
-    if args.fused > 0:
-        mkv.mkv_set_fused(args.fused, args.fused_lookahead)
+    if args.fused is not None:
+        mkv.mkv_set_fused(args.fused, args.fused_selectors)
     single = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
-    if args.fused > 0 and single != 3:
+    if args.fused is not None and args.fused > 0 and single != 3:
         raise SystemExit("--fused: the fused kernel does not apply to this workload (global centroids, t <= 20480)")
     select_emits = T <= 40960  # select writes the kept indices itself (no compaction kernel)
     nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single in (1, 2, 3) else 2, es=es)
@@ -448,8 +448,9 @@ def run_ours(args):
                    "centroid_score_path": {0: "three kernels (K read twice)", 1: "single pass (K read once)",
                                            2: "head groups (K read from HBM once, again from L2)",
                                            3: "fused whole path (one launch: head groups, selects, gathers; "
-                                              f"scorer budget {args.fused}, lookahead {args.fused_lookahead})"
-                                           }.get(single, "?"),
+                                              + ("the library's own rule" if args.fused is None else
+                                                 f"scorer budget {args.fused}, {args.fused_selectors} selector CTAs")
+                                              + ")"}.get(single, "?"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "no flush: K+V (%.1f GB) exceed the 129 MB L2" % (2 * K.numel() * es / 1e9)},
         "hbm": {"path_bytes_per_step": nbytes["path"], "achieved_gbs": hbm_gbs,
@@ -743,9 +744,10 @@ def main(argv=None):
     ap.add_argument("--cluster", type=int, default=10, help="cluster length (--path summaries)")
     ap.add_argument("--dtype", choices=sorted(CACHE_DTYPE_NAMES), default="bf16",
                     help="cache element type: bf16, or fp8 (E4M3 codes; the ManifoldKV path only)")
-    ap.add_argument("--fused", type=int, default=0,
-                    help="time the opt-in fused whole-path kernel with this scorer CTA budget (0: the default path)")
-    ap.add_argument("--fused-lookahead", type=int, default=48, help="selects ahead of the gathers (--fused)")
+    ap.add_argument("--fused", type=int, default=None,
+                    help="fused whole-path kernel: N > 0 with N scorer CTAs, 0 never (the separate kernels); "
+                         "default: the library's own shape rule")
+    ap.add_argument("--fused-selectors", type=int, default=32, help="CTAs that run the selects (--fused N > 0)")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
                     help="per-kernel DRAM bytes per launch from an ncu capture (null when absent)")
     args = ap.parse_args(argv)
@@ -753,21 +755,20 @@ def main(argv=None):
     if args.traffic_json and os.path.exists(args.traffic_json):
         with open(args.traffic_json) as f:
             t = json.load(f)
-        # counters only count while the kernels they were taken on are unchanged:
-        # the sha256 of the kernel's source files, concatenated in the listed order
-        srcs = t.get("kernel_source", "geometric_kv_cache_gb300/csrc/mkv_gather.cu")
-        srcs = [os.path.join(ROOT, x) for x in (srcs if isinstance(srcs, list) else [srcs])]
-        h = hashlib.sha256()
-        for src in srcs:
-            if not os.path.exists(src):
-                t = {}
-                break
-            with open(src, "rb") as f:
-                h.update(f.read())
-        sha = h.hexdigest()[:16]
-        if (t.get("workload") == args.workload and not args.layers and t.get("kernel_source_sha256_16") == sha
-                and t.get("cache_dtype", "bf16") == args.dtype):
-            args.traffic = t.get("bytes_per_launch")
+        # a kernel's counters count only while its source files are unchanged:
+        # the sha256 of those files, concatenated in the listed order
+        if (t.get("workload") == args.workload and not args.layers and t.get("cache_dtype", "bf16") == args.dtype):
+            args.traffic = {}
+            for name, k in t.get("kernels", {}).items():
+                h = hashlib.sha256()
+                srcs = [os.path.join(ROOT, x) for x in k.get("sources", [])]
+                if not srcs or not all(os.path.exists(x) for x in srcs):
+                    continue
+                for src in srcs:
+                    with open(src, "rb") as f:
+                        h.update(f.read())
+                if h.hexdigest()[:16] == k.get("sha256_16"):
+                    args.traffic[name] = k.get("bytes_per_launch")
     if args.dtype != "bf16" and (args.impl == "reference" or args.path != "manifold"):
         ap.error("--dtype fp8 applies to the ManifoldKV path of our arm only")
     if args.impl == "reference":

@@ -209,11 +209,12 @@ def mkv_set_head_groups(enable: bool) -> bool:
     return bool(load().mkv_set_head_groups(1 if enable else 0))
 
 
-def mkv_set_fused(scorer_ctas: int, lookahead: int = 0) -> int:
-    """Allow (scorer_ctas > 0) or forbid (0) the fused whole-path kernel in
-    mkv_compress; lookahead > 0 sets how many heads the selects run ahead of
-    the gathers. Returns the previous scorer budget."""
-    return int(load().mkv_set_fused(int(scorer_ctas), int(lookahead)))
+def mkv_set_fused(scorer_ctas: int, select_ctas: int = 0) -> int:
+    """When mkv_compress runs the fused whole-path kernel: scorer_ctas < 0 on
+    its own shape rule (the default), > 0 wherever it applies with that scorer
+    budget (select_ctas > 0 sets the selector CTAs), 0 never. Returns the
+    previous scorer setting."""
+    return int(load().mkv_set_fused(int(scorer_ctas), int(select_ctas)))
 
 
 def mkv_layer_budgets(sensitivity, r: float, gamma: float, total: int, cap):

@@ -27,10 +27,36 @@ std::atomic<int> g_single_pass_enabled{0};
 // Whether mkv_compress may use the head-group kernel (one read of K from
 // HBM, global centroids, heads short enough for L2). On by default.
 std::atomic<int> g_head_groups_enabled{1};
-// The fused whole-path kernel (mkv_set_fused): the scorer CTA budget (0: off)
-// and the selects taken ahead of the gathers.
-std::atomic<int> g_fused_scorers{0};
-std::atomic<int> g_fused_lookahead{48};
+// The fused whole-path kernel (mkv_set_fused): the scorer CTA budget (0: off,
+// < 0: automatic) and the selector CTAs of a forced budget.
+std::atomic<int> g_fused_scorers{-1};
+std::atomic<int> g_fused_selectors{32};
+
+// Scorer and selector budgets of the fused kernel for this shape; scorers 0
+// when it is not to run. Automatic: bf16 caches, head dim 128, global
+// centroids and 12288 < t_max (<= 20480, the kernel's own limit), where it
+// was measured faster than the separate kernels on GB300 (256 heads x 16K:
+// 0.620 against 0.649 ms; 64 x 16K: 0.187 against 0.204) -- not at 8K tokens
+// (512 x 8K: 0.687 against 0.648) nor for E4M3 caches (256 x 16K: 0.558
+// against 0.42), whose scoring is decode-bound. There it uses 3/4 of the
+// resident grid for scoring and max(16, heads / 16) selector CTAs (fewer
+// than 16 made the selects the bottleneck: 1.03 ms with 8).
+struct FusedBudget {
+    int scorers = 0, selectors = 0;
+};
+FusedBudget fused_budget(const Geometry &g)
+{
+    FusedBudget b;
+    const int sc = g_fused_scorers.load(std::memory_order_relaxed);
+    if (sc > 0) {
+        b.scorers = sc;
+        b.selectors = g_fused_selectors.load(std::memory_order_relaxed);
+    } else if (sc < 0 && g.es == 2 && g.d == kHeadDim && g.pg.nwin_max == 1 && g.t_max > 12288) {
+        b.scorers = -1;  // 3/4 of the resident grid (fused_plan)
+        b.selectors = (int)std::max<int64_t>(16, (g.n_heads + 15) / 16);
+    }
+    return b;
+}
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -253,11 +279,10 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     int32_t *idx_w = idx ? idx : region<int32_t>(ws, L.idx);
     const int32_t idx_stride = idx ? keep_stride : g.t_max;
     // the whole path in one launch, when asked for and the shape allows it
-    const int scorers = g_fused_scorers.load(std::memory_order_relaxed);
-    if (scorers > 0 && !events && !stall_windows && !quota && !in_place && K_out &&
+    const FusedBudget fb = fused_budget(g);
+    if (fb.scorers != 0 && !events && !stall_windows && !quota && !in_place && K_out &&
         g_head_groups_enabled.load(std::memory_order_relaxed) && !g_single_pass_enabled.load(std::memory_order_relaxed)) {
-        const FusedPlan fp = fused_plan(g.pg, (int)mode, L.centroid - L.counters, scorers,
-                                        g_fused_lookahead.load(std::memory_order_relaxed));
+        const FusedPlan fp = fused_plan(g.pg, (int)mode, L.centroid - L.counters, fb.scorers, fb.selectors);
         if (fp.grid > 0) {
             e = launch_fused(g.pg, fp, (int)mode, K, V, s.seq_lens, region<float>(ws, L.partial),
                              region<uint32_t>(ws, L.counters), C, S, ratio, n_keep, keep_stride, kept_w, idx_w,
@@ -656,9 +681,8 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
     }
     if (g_head_groups_enabled.load(std::memory_order_relaxed)) {
         const Layout L = make_layout(g);
-        const int scorers = g_fused_scorers.load(std::memory_order_relaxed);
-        if (scorers > 0 && fused_plan(g.pg, (int)mode, L.centroid - L.counters, scorers,
-                                      g_fused_lookahead.load(std::memory_order_relaxed)).grid > 0)
+        const FusedBudget fb = fused_budget(g);
+        if (fb.scorers != 0 && fused_plan(g.pg, (int)mode, L.centroid - L.counters, fb.scorers, fb.selectors).grid > 0)
             return 3;
         if (head_group_plan(g.pg, (int)mode, L.centroid - L.counters).groups > 0) return 2;
     }
@@ -670,10 +694,10 @@ int32_t mkv_set_head_groups(int32_t enable)
     return g_head_groups_enabled.exchange(enable ? 1 : 0);
 }
 
-int32_t mkv_set_fused(int32_t scorer_ctas, int32_t lookahead)
+int32_t mkv_set_fused(int32_t scorer_ctas, int32_t select_ctas)
 {
-    if (lookahead > 0) g_fused_lookahead.store(lookahead);
-    return g_fused_scorers.exchange(scorer_ctas > 0 ? scorer_ctas : 0);
+    if (select_ctas > 0) g_fused_selectors.store(select_ctas);
+    return g_fused_scorers.exchange(scorer_ctas > 0 ? scorer_ctas : scorer_ctas < 0 ? -1 : 0);
 }
 
 mkv_status mkv_inject_stalled_windows(const void *K, const void *V, mkv_shape shape, double ratio, mkv_mode mode,

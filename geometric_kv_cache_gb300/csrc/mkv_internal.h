@@ -93,14 +93,16 @@ struct HeadGroupPlan {
 };
 HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counter_bytes);
 // The fused whole-path kernel (global centroids, heads of at most 20480
-// tokens): scorer head groups within `scorer_ctas` CTAs, every resident CTA
-// a select / gather worker afterwards; grid 0 when it does not apply.
+// tokens): scorer head groups within `scorer_ctas` CTAs (< 0: 3/4 of the
+// resident grid), `select_ctas`
+// selector CTAs, every warp a gatherer afterwards; grid 0 when it does not
+// apply.
 struct FusedPlan {
     HeadGroupPlan hg;
-    int grid = 0;       // resident CTAs of the launch
-    int lookahead = 0;  // selects taken ahead of the gathers, in heads
+    int grid = 0;         // resident CTAs of the launch
+    int select_ctas = 0;  // CTAs that run the selects
 };
-FusedPlan fused_plan(const PieceGeometry &g, int mode, size_t counter_bytes, int scorer_ctas, int lookahead);
+FusedPlan fused_plan(const PieceGeometry &g, int mode, size_t counter_bytes, int scorer_ctas, int select_ctas);
 cudaError_t launch_fused(const PieceGeometry &g, const FusedPlan &fp, int mode, const void *K, const void *V,
                          const int32_t *seq_lens, float *partial, uint32_t *cnt, float *C, float *S, double ratio,
                          const int32_t *n_keep, int32_t keep_stride, int32_t *kept, int32_t *idx, int32_t idx_stride,

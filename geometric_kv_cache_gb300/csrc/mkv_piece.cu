@@ -1106,38 +1106,40 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, ui
 }
 
 // The whole path in one cooperative launch (global centroids, heads of at
-// most kFusedMaxT tokens). CTAs [0, groups * gsize) first score the heads as
-// head groups do (units are whole heads; head_done[h] reaches gsize when the
-// scores of head h are complete). Every CTA -- the scorers once their units
-// are done -- then takes tickets from one counter, in this order: the
-// selects of heads 0 .. L-1, then for each head h the select of head h + L
-// (if any) and the gather items of head h (128 output slots each for rows of
-// 256 bytes). A select waits for its head's scores and publishes
-// sel_done[h]; a gather item waits for sel_done[h]. Selects thus run about L heads ahead of the gathers while
-// the scorers still stream K, and the gathers fill HBM while the scorers are
-// in their L2 pass, barriers and means. Scorers wait only on their own
-// group, selects only on scorers, gathers only on selects taken earlier in
-// ticket order, so with every CTA resident each wait ends; each is also
+// most kFusedMaxT tokens), in three roles:
+//  * scorers, CTAs [0, groups * gsize): the heads' centroids and scores as
+//    head groups compute them (units are whole heads; head_done[h] reaches
+//    gsize when the scores of head h are complete);
+//  * selectors, the last select_ctas CTAs (after their scoring, if they are
+//    also scorers): the heads' selects in head order from one ticket
+//    counter, each waiting for its head's scores and publishing sel_done[h];
+//  * gatherers, every warp of every CTA once its other roles are done: gather
+//    items of one warp each (16 output slots for rows of 256 bytes, 8 rows of
+//    K and of V in flight per lane) from a second ticket counter, head-major,
+//    each waiting for sel_done of its head. A warp claims its next item while
+//    it copies the current one and meets no other warp, so many independent
+//    item chains per SM hide each other's latency.
+// Scorers wait only on their own group, selectors only on scorers, gatherers
+// only on selectors, so with every CTA resident each wait ends; each is also
 // bounded in time (a wait that runs out sets MKV_DEV_TIMEOUT and its work is
 // skipped: the head keeps no rows). The arithmetic is that of the head-group,
 // select and gather kernels, so the outputs are the same bits.
 constexpr int kFusedMaxT = (int)(kGroupSmem / sizeof(float));  // the select keeps a head's scores in shared memory
-// output slots per gather ticket: 8 rows of K and 8 of V in flight per lane
-// (128 slots for 256-byte rows)
-__host__ __device__ constexpr int fused_gather_rows(int row_bytes) { return 8 * kGatherThreads * 16 / row_bytes; }
-static_assert(kThreads == kGatherThreads, "gather items assume the head-group CTA size");
+// output slots of a warp's gather item: 8 rows of K and 8 of V in flight per
+// lane (16 slots for 256-byte rows)
+__host__ __device__ constexpr int fused_gather_rows(int row_bytes) { return 8 * 32 * 16 / row_bytes; }
 
 struct TailArgs {
     const uint8_t *V;
     uint8_t *K_out, *V_out;
     const int32_t *n_keep;
     int32_t *kept, *idx;
-    uint32_t *head_done, *sel_done, *ticket;
+    uint32_t *head_done, *sel_done, *sel_ticket, *gather_ticket;
     double ratio;
-    int keep_stride, idx_stride, bph, lookahead;
+    int keep_stride, idx_stride, bph, select_ctas;
 };
 
-// Thread 0 waits until *flag >= target (bounded); 1 when it got there. With
+// One thread waits until *flag >= target (bounded); 1 when it got there. With
 // `abortable` it also gives up once any wait of the launch has timed out, so
 // that a failure drains in about one wait bound (a timeout bit already set
 // when the CTA started is not taken for one of this launch).
@@ -1157,52 +1159,81 @@ __device__ __forceinline__ uint32_t wait_count(const uint32_t *flag, uint32_t ta
     return 1u;
 }
 
+// One warp's item of ROWS output slots (groups of LPR lanes per row, ROWS /
+// (32 / LPR) rows of K and of V in flight per lane), for indices and kept
+// counts written earlier in the same launch: both are read through L2 only
+// (__ldcg), the indices at once with the count (only slots below both
+// keep_stride and idx_stride, so every load stays inside the head's index
+// row) and then masked by it. No barrier: warps run independent items.
+template <int LPR, int ROWS>
+__device__ __forceinline__ void gather_warp_item(int64_t head, int item, const int32_t *idx, int idx_stride,
+                                                 const int32_t *kept, int t_max, int keep_stride,
+                                                 const uint8_t *__restrict__ K, const uint8_t *__restrict__ V,
+                                                 uint8_t *__restrict__ K_out, uint8_t *__restrict__ V_out,
+                                                 uint32_t *status)
+{
+    constexpr int RB = LPR * 16, SL = 32 / LPR, R = ROWS / SL;
+    static_assert(R * SL == ROWS, "ROWS must be a multiple of the rows a warp step covers");
+    const int lane = threadIdx.x & 31, hw = lane / LPR, lr = lane % LPR;
+    const int j0 = item * ROWS;
+    const int cap = min(ROWS, min(keep_stride, idx_stride) - j0);
+    const int32_t *ih = idx + head * idx_stride + j0;
+    int src[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+        const int j = u * SL + hw;
+        src[u] = j < cap ? __ldcg(ih + j) : -1;
+    }
+    const int n = min(cap, __ldcg(kept + head) - j0);
+    const size_t in_head = (size_t)head * t_max * RB + lr * 16;
+    const size_t out_head = ((size_t)head * keep_stride + j0) * RB + lr * 16;
+    uint4 kv[R], vv[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+        if (u * SL + hw >= n) src[u] = -1;
+        if (src[u] >= t_max) {
+            atomicOr(status, MKV_DEV_INTERNAL);
+            src[u] = -1;
+        }
+        if (src[u] >= 0) {
+            const size_t off = in_head + (size_t)src[u] * RB;
+            kv[u] = ld_stream(K + off);
+            vv[u] = ld_stream(V + off);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+        if (src[u] >= 0) {
+            const size_t off = out_head + (size_t)(u * SL + hw) * RB;
+            st_v4(K_out + off, kv[u]);
+            st_v4(V_out + off, vv[u]);
+        }
+    }
+}
+
 template <int MODE, int NB, int ES>
 __global__ void __launch_bounds__(kThreads, 2)
 k_fused_path(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int groups, uint32_t stagger_ns, TailArgs A)
 {
     constexpr int LPR = 4 * NB * ES;  // lanes per row: row bytes / 16
+    constexpr int ROWS = fused_gather_rows(16 * LPR);
     __shared__ uint32_t s_ticket, s_go, s_abortable;
     if (threadIdx.x == 0) s_abortable = timed_out(P.status) ? 0u : 1u;  // read before any wait of this CTA
     __syncthreads();
+    const bool abortable = s_abortable != 0u;
     if ((int)blockIdx.x < groups * gsize)
         head_groups_run<MODE, NB, ES>(g, P, gcnt, gsize, 1, stagger_ns, groups, (int)blockIdx.x / gsize,
                                       (int)blockIdx.x % gsize, A.head_done);
-    const int64_t n_heads = g.n_heads, L = A.lookahead, blk = (int64_t)A.bph + 1;
-    const int64_t n_tickets = L + n_heads * blk;
-    // Thread 0 claims the next ticket while the CTA works on the current one.
-    // A claimed ticket waits, at worst, on a select with a lower ticket, so
-    // the chain of waits always ends at a ticket that can run.
-    uint32_t next = 0;
-    if (threadIdx.x == 0) next = atomicAdd(A.ticket, 1u);
-    for (;;) {
-        __syncthreads();  // s_ticket and s_go of the previous ticket are read; shared memory is free
-        if (threadIdx.x == 0) {
-            s_ticket = next;
-            if ((int64_t)next < n_tickets) next = atomicAdd(A.ticket, 1u);
-        }
-        __syncthreads();
-        const int64_t t = s_ticket;
-        if (t >= n_tickets) break;  // the same for every thread
-        int64_t head;
-        int item = -1;  // -1: the head's select; else its gather item
-        if (t < L) {
-            head = t;
-        } else {
-            const int64_t u = t - L, h = u / blk, r = u - h * blk;
-            if (r == 0) {
-                head = h + L;
-                if (head >= n_heads) continue;
-            } else {
-                head = h;
-                item = (int)r - 1;
-            }
-        }
-        if (threadIdx.x == 0)
-            s_go = item < 0 ? wait_count(A.head_done + head, (uint32_t)gsize, P.status, s_abortable != 0u)
-                            : wait_count(A.sel_done + head, 1u, P.status, s_abortable != 0u);
-        __syncthreads();
-        if (item < 0) {
+    const int64_t n_heads = g.n_heads;
+    if ((int)blockIdx.x >= (int)gridDim.x - A.select_ctas) {
+        for (;;) {
+            __syncthreads();  // s_ticket and s_go of the previous select are read; shared memory is free
+            if (threadIdx.x == 0) s_ticket = atomicAdd(A.sel_ticket, 1u);
+            __syncthreads();
+            const int64_t head = s_ticket;
+            if (head >= n_heads) break;  // the same for every thread
+            if (threadIdx.x == 0) s_go = wait_count(A.head_done + head, (uint32_t)gsize, P.status, abortable);
+            __syncthreads();
             if (s_go)
                 select_item<true, false, kThreads>(head, P.S, P.seq_lens, g.heads, g.t_max, A.ratio, A.n_keep,
                                                    A.keep_stride, 0, g.nwin_max, nullptr, nullptr, 0, A.kept, A.idx,
@@ -1212,10 +1243,28 @@ k_fused_path(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int groups,
             __threadfence();  // the indices and the kept count are visible before the flag
             __syncthreads();
             if (threadIdx.x == 0) atomicExch(A.sel_done + head, 1u);
-        } else if (s_go) {
-            gather_item<LPR, true, fused_gather_rows(16 * LPR)>(head * A.bph + item, A.idx, A.idx_stride, A.kept, g.t_max,
-                                                         A.keep_stride, A.bph, P.K, A.V, A.K_out, A.V_out, P.status);
         }
+    }
+    // gatherer: every warp on its own
+    const int lane = threadIdx.x & 31;
+    const int64_t n_items = n_heads * A.bph;
+    uint32_t next = 0;
+    if (lane == 0) next = atomicAdd(A.gather_ticket, 1u);
+    next = __shfl_sync(kFull, next, 0);
+    while ((int64_t)next < n_items) {
+        const int64_t t = next, head = t / A.bph;
+        const int item = (int)(t - head * A.bph);
+        uint32_t claim = 0, go = 0;
+        if (lane == 0) {
+            claim = atomicAdd(A.gather_ticket, 1u);  // the next item, claimed while this one is copied
+            go = wait_count(A.sel_done + head, 1u, P.status, abortable);
+        }
+        go = __shfl_sync(kFull, go, 0);
+        __syncwarp();  // the lanes' reads of the indices come after lane 0's acquire of the flag
+        if (go)
+            gather_warp_item<LPR, ROWS>(head, item, A.idx, A.idx_stride, A.kept, g.t_max, A.keep_stride, P.K, A.V,
+                                        A.K_out, A.V_out, P.status);
+        next = __shfl_sync(kFull, claim, 0);
     }
 }
 
@@ -1432,23 +1481,25 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
     return plan_groups(g, resident_grid(fn, kThreads, kGroupSmem), counters, true);
 }
 
-FusedPlan fused_plan(const PieceGeometry &g, int mode, size_t counters, int scorer_ctas, int lookahead)
+FusedPlan fused_plan(const PieceGeometry &g, int mode, size_t counters, int scorer_ctas, int select_ctas)
 {
     FusedPlan fp;
     // whole heads as units, and each head's scores fit the select's shared memory
-    if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max != 1 || g.t_max > kFusedMaxT || scorer_ctas <= 0) return fp;
+    if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max != 1 || g.t_max > kFusedMaxT || scorer_ctas == 0) return fp;
     const void *fn = fused_fn(g.d, g.es, mode);
     if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
         return fp;
     const int resident = resident_grid(fn, kThreads, kGroupSmem);
     if (resident < 16) return fp;
-    const HeadGroupPlan hp = plan_groups(g, std::min(scorer_ctas, resident), counters, false);
+    // a negative budget: 3/4 of the resident grid
+    const HeadGroupPlan hp = plan_groups(g, scorer_ctas < 0 ? resident * 3 / 4 : std::min(scorer_ctas, resident),
+                                         counters, false);
     if (hp.groups == 0 || hp.wb != 1) return fp;
-    // counters: the groups' arrivals, head_done, sel_done and the ticket
-    if (((size_t)hp.groups + 2 * (size_t)g.n_heads + 1) * sizeof(uint32_t) > counters) return fp;
+    // counters: the groups' arrivals, head_done, sel_done and the two tickets
+    if (((size_t)hp.groups + 2 * (size_t)g.n_heads + 2) * sizeof(uint32_t) > counters) return fp;
     fp.hg = hp;
     fp.grid = resident;
-    fp.lookahead = (int)std::max<int64_t>(1, std::min<int64_t>(lookahead > 0 ? lookahead : 48, g.n_heads));
+    fp.select_ctas = std::max(1, std::min(select_ctas > 0 ? select_ctas : 32, resident));
     return fp;
 }
 
@@ -1459,7 +1510,7 @@ cudaError_t launch_fused(const PieceGeometry &g, const FusedPlan &fp, int mode, 
 {
     const void *fn = fused_fn(g.d, g.es, mode);
     if (!fn || fp.grid <= 0) return cudaErrorInvalidValue;
-    const size_t words = (size_t)fp.hg.groups + 2 * (size_t)g.n_heads + 1;
+    const size_t words = (size_t)fp.hg.groups + 2 * (size_t)g.n_heads + 2;
     cudaError_t e = cudaMemsetAsync(cnt, 0, words * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
     Pointers P = make_pointers(K, seq_lens, partial, C, S, status);
@@ -1472,13 +1523,14 @@ cudaError_t launch_fused(const PieceGeometry &g, const FusedPlan &fp, int mode, 
     A.idx = idx;
     A.head_done = cnt + fp.hg.groups;
     A.sel_done = A.head_done + g.n_heads;
-    A.ticket = A.sel_done + g.n_heads;
+    A.sel_ticket = A.sel_done + g.n_heads;
+    A.gather_ticket = A.sel_ticket + 1;
     A.ratio = ratio;
     A.keep_stride = keep_stride;
     A.idx_stride = idx_stride;
     const int rows = fused_gather_rows(g.d * g.es);
     A.bph = (keep_stride + rows - 1) / rows;
-    A.lookahead = fp.lookahead;
+    A.select_ctas = fp.select_ctas;
     PieceGeometry gg = g;
     int gsize = fp.hg.gsize, groups = fp.hg.groups;
     uint32_t stagger = fp.hg.stagger_ns;

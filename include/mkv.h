@@ -293,9 +293,9 @@ int32_t mkv_compress_num_stages(void);
  * 2 the head-group kernel (the default when a unit of windows fits in L2
  * and, with several rounds per group, the cache is bf16 and, for head dims up
  * to 128, its modelled cost is below the three kernels': K read from HBM
- * once, the second read hits L2), 3 the fused whole-path kernel (opt-in,
- * mkv_set_fused: every step in one launch), 0 the three-kernel path (K read
- * twice); -1 on a bad argument or CUDA error.
+ * once, the second read hits L2), 3 the fused whole-path kernel (every step
+ * in one launch; see mkv_set_fused), 0 the three-kernel path (K read twice);
+ * -1 on a bad argument or CUDA error.
  * All give bit-identical results. */
 int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode);
 
@@ -306,20 +306,25 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
  * their rows are still in L2 -- one HBM read of K instead of two. */
 int32_t mkv_set_head_groups(int32_t enable);
 
-/* Allow (scorer_ctas > 0) or forbid (<= 0, the default) the fused whole-path
- * kernel in mkv_compress, process-wide; returns the previous scorer budget.
- * It applies to global centroids (window 0 or >= t_max) with t_max <= 20480,
- * without per-window quotas, in-place compaction or caller events, and when
- * head groups are allowed and the single-pass kernel is not. One cooperative
- * launch then runs every step: head groups of at most scorer_ctas CTAs score
- * the heads (K read from HBM once); every CTA then takes, from one ticket
- * counter, the selects (lookahead heads ahead; lookahead <= 0 keeps the
- * current value, 48 at start) and the 64-slot gather items, each waiting
- * (bounded; a wait that runs out sets MKV_DEV_TIMEOUT in the status word and
- * that head keeps no rows) for the step it depends on. The outputs are the
- * same bits as the separate kernels'. When the whole grid cannot be resident
- * at launch, mkv_compress runs the separate kernels instead. */
-int32_t mkv_set_fused(int32_t scorer_ctas, int32_t lookahead);
+/* Choose, process-wide, when mkv_compress runs the fused whole-path kernel;
+ * returns the previous scorer setting. scorer_ctas < 0 (the default): on its
+ * own rule -- bf16 caches, head dim 128, global centroids and 12288 < t_max
+ * <= 20480, the shapes where it was measured faster than the separate
+ * kernels on GB300 -- with 3/4 of the resident grid scoring and max(16,
+ * heads / 16) selector CTAs. scorer_ctas > 0: wherever it applies, with that
+ * scorer budget and select_ctas selector CTAs (select_ctas <= 0 keeps the
+ * current value, 32 at start). scorer_ctas == 0: never. It applies to global
+ * centroids (window 0 or >= t_max) with t_max <= 20480, without per-window
+ * quotas, in-place compaction or caller events, and when head groups are
+ * allowed and the single-pass kernel is not. One cooperative launch then
+ * runs every step: head groups score the heads (K read from HBM once), the
+ * selector CTAs run the selects in head order, and every warp then copies
+ * gather items on its own, each step waiting (bounded; a wait that runs out
+ * sets MKV_DEV_TIMEOUT in the status word and that head keeps no rows) for
+ * the one it depends on. The outputs are the same bits as the separate
+ * kernels'. When the whole grid cannot be resident at launch, mkv_compress
+ * runs the separate kernels instead. */
+int32_t mkv_set_fused(int32_t scorer_ctas, int32_t select_ctas);
 
 /* Per-layer kept-token budgets for the n_keep array (host helper). The
  * budget mapping of "RippleKV" (gist.science explainer of arXiv 2608.08684),

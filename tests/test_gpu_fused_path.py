@@ -1,10 +1,10 @@
 """GPU parity of the fused whole-path kernel (opt-in, mkv_set_fused): one
-cooperative launch whose scorer head groups, selects and gathers hand work
-over through bounded waits. Its outputs must be the separate kernels' bits
+cooperative launch whose scorer head groups, selector CTAs and gatherer
+warps hand work over through bounded waits. Its outputs must be the separate kernels' bits
 (every head, every output row) on bf16 and E4M3 caches, head dims 64 / 128 /
 256, ragged lengths with empty and sub-piece heads, a per-head n_keep array,
 both score modes, the largest t_max it takes, and small and large scorer
-budgets and lookaheads; a small case is also checked head by head against
+and selector budgets; a small case is also checked head by head against
 the fp64 oracle."""
 import numpy as np
 import pytest
@@ -44,11 +44,11 @@ def _compress(K, V, lens, ratio, mode, keep_stride, n_keep=None):
     return status, (kept, idx, u8(Ko), u8(Vo))
 
 
-def _both(K, V, lens, ratio, mode, keep_stride, n_keep=None, scorers=152, lookahead=48):
+def _both(K, V, lens, ratio, mode, keep_stride, n_keep=None, scorers=152, selectors=32):
     """(separate kernels, fused kernel) outputs; asserts the fused path was taken."""
     mkv.mkv_set_fused(0)
     st0, a = _compress(K, V, lens, ratio, mode, keep_stride, n_keep)
-    mkv.mkv_set_fused(scorers, lookahead)
+    mkv.mkv_set_fused(scorers, selectors)
     try:
         assert mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), 0, mode) == 3
         st1, b = _compress(K, V, lens, ratio, mode, keep_stride, n_keep)
@@ -75,10 +75,10 @@ def test_fused_equals_separate_kernels_llama_shape(mode, ratio):
     _same(a, b)
 
 
-@pytest.mark.parametrize("scorers,lookahead", [(16, 1), (96, 7), (288, 200)])
-def test_fused_scorer_budgets_and_lookaheads(scorers, lookahead):
+@pytest.mark.parametrize("scorers,selectors", [(16, 1), (96, 7), (288, 400)])
+def test_fused_scorer_and_selector_budgets(scorers, selectors):
     K, V, lens = _cache("fused-budget", 1, layers=4, t_max=9000)
-    a, b = _both(K, V, None, 0.4, "l2", mkv.mkv_num_keep(K.shape[2], 0.4), scorers=scorers, lookahead=lookahead)
+    a, b = _both(K, V, None, 0.4, "l2", mkv.mkv_num_keep(K.shape[2], 0.4), scorers=scorers, selectors=selectors)
     _same(a, b)
 
 
@@ -123,7 +123,7 @@ def test_fused_largest_t_max_and_the_fallback_above_it():
 
 
 def test_fused_small_case_against_the_oracle():
-    """Two heads (fewer than the lookahead): the fused outputs head by head
+    """Two heads (fewer than the selector CTAs): the fused outputs head by head
     against the fp64 oracle, under the same tolerances as the other paths."""
     K, V, lens = _cache("fused-oracle", 6, layers=1, heads=2, t_max=3000)
     ratio, mode = 0.3, "l2"
@@ -142,3 +142,32 @@ def test_fused_small_case_against_the_oracle():
     for h in range(H):
         compare_head(ora[h], 3000, idx_gpu=idx.reshape(H, -1)[h].cpu().numpy(), kept_gpu=kept.flatten()[h].item(),
                      K_head=Kf[h], V_head=Vf[h], Kout_gpu=bits(kf[h]), Vout_gpu=bits(vf[h]), mode=mode)
+
+
+def test_fused_kernel_own_rule():
+    """The default setting runs the fused kernel where it was measured faster:
+    bf16, head dim 128, global centroids, 12288 < t_max <= 20480."""
+    prev = mkv.mkv_set_fused(-1)
+    try:
+        q = mkv.mkv_compress_single_pass
+        assert q(mkv.MkvShape(32, 8, 16384, 128, 0, None), 0, "l2") == 3
+        assert q(mkv.MkvShape(32, 8, 16384, 128, 0, None), 0, "cosine") == 3
+        assert q(mkv.MkvShape(8, 8, 20480, 128, 0, None), 0, "l2") == 3
+        assert q(mkv.MkvShape(8, 8, 20480, 128, 0, None), 20480, "l2") == 3     # one window covers the head
+        assert q(mkv.MkvShape(64, 8, 8192, 128, 0, None), 0, "l2") != 3          # 8K tokens
+        assert q(mkv.MkvShape(32, 8, 16384, 128, 0, None), 4096, "l2") == 2      # windows
+        assert q(mkv.MkvShape(8, 8, 20481, 128, 0, None), 0, "l2") != 3          # above the kernel's limit
+        assert q(mkv.MkvShape(8, 8, 16384, 64, 0, None), 0, "l2") != 3           # other head dims
+        assert q(mkv.MkvShape(32, 8, 16384, 128, 1, None), 0, "l2") != 3         # E4M3 caches
+    finally:
+        mkv.mkv_set_fused(prev)
+    K, V, lens = _cache("fused-rule", 7, layers=2)
+    prev = mkv.mkv_set_fused(-1)
+    try:
+        assert mkv.mkv_compress_single_pass(mkv.shape_of(K), 0, "l2") == 3
+        st1, b = _compress(K, V, None, 0.5, "l2", mkv.mkv_num_keep(K.shape[2], 0.5))
+    finally:
+        mkv.mkv_set_fused(0)
+    st0, a = _compress(K, V, None, 0.5, "l2", mkv.mkv_num_keep(K.shape[2], 0.5))
+    assert st0 == 0 and st1 == 0
+    _same(a, b)

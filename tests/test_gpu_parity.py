@@ -522,8 +522,13 @@ def test_single_pass_is_used_for_the_bench_shape_when_enabled():
     finally:
         mkv.mkv_set_single_pass(prev)
     # single pass off: the bench shape (global centroids, 4 MB heads) takes
-    # the head-group kernel
-    assert mkv.mkv_compress_single_pass(small, 0, "l2") == (1 if prev else 2)
+    # the fused kernel (its own rule), and the head-group kernel without it
+    assert mkv.mkv_compress_single_pass(small, 0, "l2") == (1 if prev else 3)
+    prev_fused = mkv.mkv_set_fused(0)
+    try:
+        assert mkv.mkv_compress_single_pass(small, 0, "l2") == (1 if prev else 2)
+    finally:
+        mkv.mkv_set_fused(prev_fused)
     assert mkv.load().mkv_compress_single_pass(small, -1, 0) == -1
 
 
@@ -553,6 +558,16 @@ def test_single_pass_and_three_kernel_paths_give_the_same_bits():
 
 def test_head_groups_are_used_only_where_they_fit():
     bench = mkv.MkvShape(32, 8, 16384, 128, 0, None)
+    # the fused kernel's own rule takes the bench shape's global centroids (3)
+    assert mkv.mkv_compress_single_pass(bench, 0, "l2") == 3
+    prev_fused = mkv.mkv_set_fused(0)
+    try:
+        _head_group_rules(bench)
+    finally:
+        mkv.mkv_set_fused(prev_fused)
+
+
+def _head_group_rules(bench):
     assert mkv.mkv_compress_single_pass(bench, 0, "l2") == 2
     assert mkv.mkv_compress_single_pass(bench, 0, "cosine") == 2
     assert mkv.mkv_compress_single_pass(bench, 4096, "l2") == 2        # windows: blocks of windows per group
@@ -575,6 +590,7 @@ def _paths_agree(K, V, lens, mode, ratio, window=0):
     B, H, T, D = K.shape
     nw = mkv.mkv_num_windows(T, window)
     out = []
+    prev_fused = mkv.mkv_set_fused(0)  # these two paths alone (the fused kernel has its own tests)
     for enable in (True, False):
         prev = mkv.mkv_set_head_groups(enable)
         try:
@@ -587,6 +603,7 @@ def _paths_agree(K, V, lens, mode, ratio, window=0):
             out.append((used, C, S, _run_fused(K, V, ratio, mode, window, lens)))
         finally:
             mkv.mkv_set_head_groups(prev)
+    mkv.mkv_set_fused(prev_fused)
     (u1, C1, S1, f1), (u0, C0, S0, f0) = out
     assert u1 == 2 and u0 == 0
     live = torch.arange(T, device=DEV)[None, None, :] < lens[:, None, None]
