@@ -721,6 +721,32 @@ def run_secondary(args):
     print(json.dumps(line), flush=True)
 
 
+def load_traffic(path, workload, layers, dtype, root=ROOT):
+    """Per-kernel DRAM bytes per launch from an ncu record (profiles/traffic.json),
+    for the bench's own workload, layer count and cache type only. A kernel's
+    figure counts only while its source files are unchanged: the sha256 of
+    those files, concatenated in the listed order, must match the record.
+    Returns {kernel: bytes} (possibly empty), or None without a record."""
+    if not path or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    if t.get("workload") != workload or layers or t.get("cache_dtype", "bf16") != dtype:
+        return None
+    out = {}
+    for name, k in t.get("kernels", {}).items():
+        srcs = [os.path.join(root, x) for x in k.get("sources", [])]
+        if not srcs or not all(os.path.exists(x) for x in srcs):
+            continue
+        h = hashlib.sha256()
+        for src in srcs:
+            with open(src, "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] == k.get("sha256_16"):
+            out[name] = k.get("bytes_per_launch")
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -751,24 +777,7 @@ def main(argv=None):
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
                     help="per-kernel DRAM bytes per launch from an ncu capture (null when absent)")
     args = ap.parse_args(argv)
-    args.traffic = None
-    if args.traffic_json and os.path.exists(args.traffic_json):
-        with open(args.traffic_json) as f:
-            t = json.load(f)
-        # a kernel's counters count only while its source files are unchanged:
-        # the sha256 of those files, concatenated in the listed order
-        if (t.get("workload") == args.workload and not args.layers and t.get("cache_dtype", "bf16") == args.dtype):
-            args.traffic = {}
-            for name, k in t.get("kernels", {}).items():
-                h = hashlib.sha256()
-                srcs = [os.path.join(ROOT, x) for x in k.get("sources", [])]
-                if not srcs or not all(os.path.exists(x) for x in srcs):
-                    continue
-                for src in srcs:
-                    with open(src, "rb") as f:
-                        h.update(f.read())
-                if h.hexdigest()[:16] == k.get("sha256_16"):
-                    args.traffic[name] = k.get("bytes_per_launch")
+    args.traffic = load_traffic(args.traffic_json, args.workload, args.layers, args.dtype)
     if args.dtype != "bf16" and (args.impl == "reference" or args.path != "manifold"):
         ap.error("--dtype fp8 applies to the ManifoldKV path of our arm only")
     if args.impl == "reference":

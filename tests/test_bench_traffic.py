@@ -1,0 +1,39 @@
+"""The bench's ncu traffic record: a kernel's DRAM bytes are reported only for
+the recorded workload and cache type, and only while the kernel's source
+files hash to the recorded value (so a changed kernel reports null)."""
+import hashlib
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _record(tmp_path, sources, sha, workload="w", dtype="bf16"):
+    p = tmp_path / "traffic.json"
+    p.write_text(json.dumps({"workload": workload, "cache_dtype": dtype,
+                             "kernels": {"k": {"sources": sources, "sha256_16": sha, "bytes_per_launch": 123}}}))
+    return str(p)
+
+
+def test_traffic_counts_only_for_unchanged_sources(tmp_path):
+    a, b = tmp_path / "a.cu", tmp_path / "b.cuh"
+    a.write_bytes(b"kernel a\n")
+    b.write_bytes(b"header b\n")
+    sha = hashlib.sha256(b"kernel a\nheader b\n").hexdigest()[:16]
+    rec = _record(tmp_path, ["a.cu", "b.cuh"], sha)
+    assert bench.load_traffic(rec, "w", 0, "bf16", root=str(tmp_path)) == {"k": 123}
+    assert bench.load_traffic(rec, "other", 0, "bf16", root=str(tmp_path)) is None
+    assert bench.load_traffic(rec, "w", 8, "bf16", root=str(tmp_path)) is None      # --layers changes the workload
+    assert bench.load_traffic(rec, "w", 0, "fp8", root=str(tmp_path)) is None
+    b.write_bytes(b"header b, changed\n")
+    assert bench.load_traffic(rec, "w", 0, "bf16", root=str(tmp_path)) == {}
+    assert bench.load_traffic(str(tmp_path / "missing.json"), "w", 0, "bf16") is None
+
+
+def test_committed_record_matches_the_gather_sources():
+    rec = os.path.join(ROOT, "profiles", "traffic.json")
+    got = bench.load_traffic(rec, "llama3.1-8b-kv-t16k", 0, "bf16")
+    assert got is not None and got.get("gather", 0) > 0
