@@ -1089,7 +1089,10 @@ __device__ __forceinline__ void head_groups_run(const PieceGeometry &g, const Po
         if (head_done) {  // this CTA's scores of the unit are visible before the count
             __threadfence();
             __syncthreads();
-            if (threadIdx.x == 0) atomicAdd(&head_done[head], 1u);
+            if (threadIdx.x == 0) {
+                __threadfence();  // the publishing thread's own fence: the count releases the CTA's writes
+                atomicAdd(&head_done[head], 1u);
+            }
         }
         __syncthreads();  // the means are rewritten for the next unit
     }
@@ -1242,7 +1245,10 @@ k_fused_path(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int groups,
                 A.kept[head] = 0;  // its gather items copy nothing
             __threadfence();  // the indices and the kept count are visible before the flag
             __syncthreads();
-            if (threadIdx.x == 0) atomicExch(A.sel_done + head, 1u);
+            if (threadIdx.x == 0) {
+                __threadfence();  // the publishing thread's own fence: the flag releases the CTA's writes
+                atomicExch(A.sel_done + head, 1u);
+            }
         }
     }
     // gatherer: every warp on its own
