@@ -252,7 +252,8 @@ mkv_status run_centroid_score(const Geometry &g, const Layout &L, const void *K,
 mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio, const int32_t *n_keep,
                         mkv_mode mode, int32_t window, int32_t keep_stride, void *K_out, void *V_out,
                         int32_t *idx, int32_t *kept, void *ws, size_t ws_bytes, cudaStream_t st,
-                        void *const *events, bool stall_windows = false, bool quota = false, bool in_place = false)
+                        void *const *events, bool stall_windows = false, bool quota = false, bool in_place = false,
+                        bool allow_fused = true)
 {
     mkv_status rc = check_shape(s);
     if (rc != MKV_OK) return rc;
@@ -280,7 +281,7 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     const int32_t idx_stride = idx ? keep_stride : g.t_max;
     // the whole path in one launch, when asked for and the shape allows it
     const FusedBudget fb = fused_budget(g);
-    if (fb.scorers != 0 && !events && !stall_windows && !quota && !in_place && K_out &&
+    if (fb.scorers != 0 && allow_fused && !events && !stall_windows && !quota && !in_place && K_out &&
         g_head_groups_enabled.load(std::memory_order_relaxed) && !g_single_pass_enabled.load(std::memory_order_relaxed)) {
         const FusedPlan fp = fused_plan(g.pg, (int)mode, L.centroid - L.counters, fb.scorers, fb.selectors);
         if (fp.grid > 0) {
@@ -848,8 +849,11 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
         int32_t *ci = reinterpret_cast<int32_t *>(wbytes_at(d_idx, (size_t)r0 * idx_row));
         int32_t *ck = reinterpret_cast<int32_t *>(wbytes_at(d_kept, (size_t)r0 * kept_row));
         const void *vsrc = v_host_dev ? static_cast<const void *>(v_host_dev + io) : bytes_at(dV, io);
+        // the separate kernels: with the host link as the limit, the fused
+        // kernel's overlap of scoring and gathering buys nothing here
         rc = run_compress(bytes_at(dK, io), vsrc, sub, ratio, nullptr, mode, window, keep_stride,
-                          wbytes_at(dK_out, oo), wbytes_at(dV_out, oo), ci, ck, workspace, workspace_bytes, st, nullptr);
+                          wbytes_at(dK_out, oo), wbytes_at(dV_out, oo), ci, ck, workspace, workspace_bytes, st, nullptr,
+                          false, false, false, false);
         if (rc != MKV_OK) return rc;
         if (cudaEventRecord(cs->comp_done[c], st) != cudaSuccess || cudaStreamWaitEvent(cs->out, cs->comp_done[c], 0) != cudaSuccess)
             return MKV_ERR_CUDA;

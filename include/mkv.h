@@ -323,7 +323,8 @@ int32_t mkv_set_head_groups(int32_t enable);
  * sets MKV_DEV_TIMEOUT in the status word and that head keeps no rows) for
  * the one it depends on. The outputs are the same bits as the separate
  * kernels'. When the whole grid cannot be resident at launch, mkv_compress
- * runs the separate kernels instead. */
+ * runs the separate kernels instead. mkv_compress_host always runs the
+ * separate kernels (the host link, not the kernels, bounds it). */
 int32_t mkv_set_fused(int32_t scorer_ctas, int32_t select_ctas);
 
 /* Per-layer kept-token budgets for the n_keep array (host helper). The
