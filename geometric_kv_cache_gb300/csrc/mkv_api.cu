@@ -279,7 +279,7 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     cudaError_t e = cudaSuccess;
     int32_t *idx_w = idx ? idx : region<int32_t>(ws, L.idx);
     const int32_t idx_stride = idx ? keep_stride : g.t_max;
-    // the whole path in one launch, when asked for and the shape allows it
+    // the whole path in one launch, when the fused setting and the shape allow it
     const FusedBudget fb = fused_budget(g);
     if (fb.scorers != 0 && allow_fused && !events && !stall_windows && !quota && !in_place && K_out &&
         g_head_groups_enabled.load(std::memory_order_relaxed) && !g_single_pass_enabled.load(std::memory_order_relaxed)) {
