@@ -1,11 +1,16 @@
 """Throughput of the ManifoldKV-style compression path on GB300.
 
 One step = one mkv_compress over the whole synthetic cache of the bench
-workload (Llama-3.1-8B-shaped KV: 32 layers x 8 KV heads, d=128, T=16384,
-bf16; global L2 centroid; 50% compression): centroid, score, top-k select,
-compaction and K/V gather for all 256 heads.
+workload: centroid, score, top-k select, compaction and K/V gather for every
+head. By default that is the largest workload, Phi-4-shaped KV (40 layers x
+10 KV heads, d=128, T=131072, bf16: 400 heads, 26.8 GB of K and V) with its
+first run, WindowedManifoldKV (L2 distance to per-window centroids of 8192
+tokens) at 50% compression. ``--workload`` and ``--run`` pick any workload
+and any of its runs (mode, window, ratio); ``--mode``, ``--window`` and
+``--ratio`` override single fields.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--run I] [--mode l2|cosine] [--window W] [--ratio R]
 
 Prints one JSON line (rank 0). ``value`` is KV token rows (one per layer,
 KV head and position) scored and compacted per second over all ranks, inputs
@@ -17,8 +22,10 @@ the launching stream inside the real call. ``cpu_baseline`` is the fp64
 oracle on the host cores on a sample of the same cache.
 
 ``--impl reference`` times the oracle (the only reference implementation of
-this path) on the host cores on samples of the same workload and prints the
-same JSON line with ``"impl": "reference"``.
+this path) on the host cores on a sample of the same workload and prints the
+same JSON line with ``"impl": "reference"``. Both CPU legs time the oracle
+the same way (oracle_sample_rate): a step runs the sample's heads split into
+one contiguous batch per host thread.
 
 Under torchrun (N > 1) every rank compresses its own cache of the same shape
 (heads are independent; no collective touches the data path); the step time
@@ -52,15 +59,17 @@ STAGES = ["piece_sums", "window_means", "piece_scores", "select", "compact", "ga
 
 # ----------------------------------------------------------------- helpers --
 
-def workload_run(name: str, layers: int = 0):
-    """The workload and its first (mode, window, ratio) run; ``layers`` > 0
-    keeps the shape of each layer but changes the layer count (a smaller
-    case for profiler captures)."""
+def workload_run(name: str, layers: int = 0, run: int = 0, mode=None, window=None, ratio=None):
+    """The workload and its run number ``run`` (mode, window, ratio), each
+    field replaced when given; ``layers`` > 0 keeps the shape of each layer
+    but changes the layer count (a smaller case for profiler captures)."""
     w = synthkv.WORKLOADS[name]
     if layers and layers != w.layers:
         w = w.scaled(f"{w.name}-{layers}layers", layers=layers)
-    mode, window, ratio = w.runs[0]
-    return w, mode, window, ratio
+    if not 0 <= run < len(w.runs):
+        raise SystemExit(f"--run {run}: {w.name} has runs 0..{len(w.runs) - 1}: {list(w.runs)}")
+    m, wd, r = w.runs[run]
+    return w, (m if mode is None else mode), (wd if window is None else window), (r if ratio is None else ratio)
 
 
 def keep_count(T: int, ratio: float) -> int:
@@ -206,60 +215,84 @@ def barrier():
 
 # ----------------------------------------------------------- CPU oracle leg --
 
-def oracle_throughput(K_host, V_host, lens, heads_per_row, ratio, mode, window, budget_s=12.0,
-                      max_heads=None, chunk=8, threads=1):
-    """Time the oracle (as it stands) on heads of a host cache until
-    ``budget_s`` has passed; returns (tokens/s, heads done, tokens, seconds).
-    With ``threads`` > 1, batches of ``chunk`` heads run concurrently on that
-    many host threads (each batch is one call into the C oracle, which
-    releases the interpreter lock), and the rate is over wall time."""
+def oracle_sample_rate(Kf, Vf, hl, ratio, mode, window, threads, steps=None, warmup=1, budget_s=None):
+    """Time the oracle, as it stands, on one sample of heads: Kf, Vf [m, T, d]
+    host tensors, hl their lengths. A step runs the m heads split into one
+    contiguous batch per host thread (``threads`` at most; each batch is one
+    call into the C oracle, which releases the interpreter lock) and waits
+    for all of them. After ``warmup`` untimed steps it times ``steps`` steps,
+    or, with ``budget_s``, steps until that much time has passed (at least 3).
+    Returns (token rows per second over the mean step time, threads used,
+    list of step seconds)."""
     import concurrent.futures as cf
 
     import numpy as np
 
     import oracle
-    n, T, D = K_host.shape[0] * K_host.shape[1], K_host.shape[2], K_host.shape[3]
-    Kf = K_host.reshape(n, T, D)
-    Vf = V_host.reshape(n, T, D)
-    hl = np.repeat(np.asarray(lens, dtype=np.int32), heads_per_row)
-    stride = keep_count(T, ratio)
-    limit = n if max_heads is None else min(n, max_heads)
+    m = Kf.shape[0]
+    hl = np.asarray(hl, dtype=np.int32)
+    stride = keep_count(int(Kf.shape[1]), ratio)
+    bounds = np.linspace(0, m, min(max(1, threads), m) + 1).astype(int)
+    batches = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
 
-    def run(a, m):
-        oracle.compress_heads(Kf[a:a + m], Vf[a:a + m], hl[a:a + m], ratio, mode, window, stride)
-        return int(hl[a:a + m].sum())
+    def run(ab):
+        a, b = ab
+        oracle.compress_heads(Kf[a:b], Vf[a:b], hl[a:b], ratio, mode, window, stride)
 
-    done, tokens, spent = 0, 0, 0.0
-    if threads <= 1:
-        while done < limit and spent < budget_s:
-            m = min(chunk, limit - done)
+    times = []
+    with cf.ThreadPoolExecutor(max_workers=len(batches)) as pool:
+        for _ in range(warmup):
+            list(pool.map(run, batches))
+        t_all = time.perf_counter()
+        while True:
             t0 = time.perf_counter()
-            tokens += run(done, m)
-            spent += time.perf_counter() - t0
-            done += m
-        return tokens / spent, done, tokens, spent
-    # waves of one batch per thread, cycling over the heads (after one
-    # untimed wave) until the budget is spent and every head was done once
-    with cf.ThreadPoolExecutor(max_workers=threads) as pool:
-        nxt = 0
+            list(pool.map(run, batches))
+            times.append(time.perf_counter() - t0)
+            if steps is not None and len(times) >= steps:
+                break
+            if steps is None and len(times) >= 3 and time.perf_counter() - t_all >= (budget_s or 0.0):
+                break
+    tok = int(hl.sum())
+    return tok / (sum(times) / len(times)), len(batches), times
 
-        def wave():
-            nonlocal nxt
-            batch = []
-            for _ in range(threads):
-                m = min(chunk, limit - nxt)
-                batch.append(pool.submit(run, nxt, m))
-                nxt = (nxt + m) % limit
-            return sum(f.result() for f in batch)
 
-        wave()
-        nxt = 0
-        t0 = time.perf_counter()
-        while done < limit or time.perf_counter() - t0 < budget_s:
-            tokens += wave()
-            done += threads * chunk
-        spent = time.perf_counter() - t0
-    return tokens / spent, min(done, limit), tokens, spent
+def oracle_sample_size(t_head_s: float, threads: int, target_step_s: float, n_heads: int) -> int:
+    """Heads in a sample whose step (one batch per thread) takes about
+    ``target_step_s``, given one head's single-thread time; a multiple of the
+    thread count where the workload allows."""
+    per = max(1, int(round(target_step_s / max(t_head_s, 1e-9))))
+    return max(1, min(n_heads, per * threads))
+
+
+def cpu_baseline_leg(K, V, lens_list, w, ratio, mode, window, budget_s):
+    """The cpu_baseline object: the oracle, as it stands, on the host cores
+    on a sample of the first heads of the same (device) cache, timed by
+    oracle_sample_rate on every host thread, with the single-thread rate
+    beside it. The sample is sized so that one step takes about half a
+    second; a third of ``budget_s`` goes to the single-thread figure."""
+    import numpy as np
+
+    import oracle
+    n, T, D = w.n_heads, K.shape[2], K.shape[3]
+    Kd, Vd = K.reshape(n, T, D), V.reshape(n, T, D)
+    hl_all = np.repeat(np.asarray(lens_list, dtype=np.int32), w.heads)
+    nt = host_threads()
+    K0, V0 = Kd[:1].cpu(), Vd[:1].cpu()
+    t0 = time.perf_counter()
+    oracle.compress_heads(K0, V0, hl_all[:1], ratio, mode, window, keep_count(T, ratio))
+    t_head = max(time.perf_counter() - t0, 1e-6)
+    m = oracle_sample_size(t_head, nt, 0.5, n)
+    Kh, Vh = Kd[:m].cpu(), Vd[:m].cpu()
+    m1 = max(1, min(m, int(round(0.5 / t_head))))
+    tps1, _, times1 = oracle_sample_rate(Kh[:m1], Vh[:m1], hl_all[:m1], ratio, mode, window, 1, budget_s=budget_s / 3)
+    tps, used, times = oracle_sample_rate(Kh, Vh, hl_all[:m], ratio, mode, window, nt, budget_s=2 * budget_s / 3)
+    tok = int(hl_all[:m].sum())
+    return {"value": tps, "unit": UNIT, "cores": used, "cpu_model": host_cpu_model(), "kind": "oracle",
+            "sample": f"the first {m} of {n} heads ({tok} token rows) per step, split into {used} batches, one host "
+                      f"thread each; {len(times)} steps of {statistics.mean(times):.3f} s (mean), fp64 C oracle",
+            "single_thread": {"value": tps1, "cores": 1,
+                              "sample": f"the first {m1} heads per step, {len(times1)} steps of "
+                                        f"{statistics.mean(times1):.3f} s (mean)"}}
 
 
 def host_cpu_model():
@@ -307,7 +340,7 @@ def run_ours(args):
     mkv.load()
     if args.no_head_groups:
         mkv.mkv_set_head_groups(False)
-    w, mode, window, ratio = workload_run(args.workload, args.layers)
+    w, mode, window, ratio = workload_run(args.workload, args.layers, args.run, args.mode, args.window, args.ratio)
     cache_dtype = {"bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}[args.dtype]
     K, V, lens = synthkv.make_kv(w, seed=rank_seed(args.seed, rank), device=dev, dtype=cache_dtype)
     es = K.element_size()
@@ -413,18 +446,7 @@ def run_ours(args):
     # CPU baseline: the oracle on a bounded sample of the same cache (rank 0, N=1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        hKc = hK if e2e is not None else K.cpu()
-        hVc = hV if e2e is not None else V.cpu()
-        nt = host_threads()
-        tps1, done1, tok1, spent1 = oracle_throughput(hKc, hVc, lens_list, w.heads, ratio, mode, window,
-                                                      budget_s=args.cpu_budget / 2)
-        tps, done, tok, spent = oracle_throughput(hKc, hVc, lens_list, w.heads, ratio, mode, window,
-                                                  budget_s=args.cpu_budget / 2, chunk=1, threads=nt)
-        cpu = {"value": tps, "unit": UNIT, "cores": nt, "cpu_model": host_cpu_model(), "kind": "oracle",
-               "sample": f"the {w.n_heads} heads cycled for {spent:.1f} s of wall time ({tok} token rows), fp64 C "
-                         f"oracle, {nt} threads over heads",
-               "single_thread": {"value": tps1, "cores": 1,
-                                 "sample": f"first {done1} of {w.n_heads} heads ({tok1} token rows, {spent1:.1f} s)"}}
+        cpu = cpu_baseline_leg(K, V, lens_list, w, ratio, mode, window, args.cpu_budget)
 
     hbm_gbs = nbytes["path"] * (world) / (ms / 1e3) / 1e9
     line = {
@@ -440,8 +462,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32",
         "io_dtype": args.dtype if args.dtype == "bf16" else "fp8_e4m3",
-        "data": "synthetic (seeded; Llama-3.1-8B-shaped KV cache, random keys with outlier channels)",
-        "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "kv_heads": w.heads,
+        "data": synthkv.describe(w),
+        "config": {"workload": w.name, "run": args.run, "layers": w.layers, "batch": w.batch, "kv_heads": w.heads,
                    "cache_dtype": args.dtype if args.dtype == "bf16" else "fp8_e4m3",
                    "heads_total": w.n_heads, "t": T, "head_dim": w.head_dim, "mode": mode,
                    "window": window, "ratio": ratio, "keep_per_head": ks,
@@ -484,50 +506,34 @@ def run_reference(args):
     import numpy as np
 
     import oracle
-    w, mode, window, ratio = workload_run(args.workload, args.layers)
+    w, mode, window, ratio = workload_run(args.workload, args.layers, args.run, args.mode, args.window, args.ratio)
     lens = synthkv.seq_lengths(w, args.seed).tolist()
     oracle.build()
-    # one head to size the per-step sample so the whole run takes about a minute
+    # one head sizes the sample, so that the whole run takes about ref_budget
     K1, V1, _ = synthkv.make_kv(w, seed=args.seed, heads=[0])
     t0 = time.perf_counter()
     oracle.compress_heads(K1, V1, np.array([lens[0]], np.int32), ratio, mode, window)
-    t_head = time.perf_counter() - t0
+    t_head = max(time.perf_counter() - t0, 1e-6)
     nt = host_threads()
-    per_step = int(max(1, min(w.n_heads, round(args.ref_budget * nt / max(1, args.steps + args.warmup) / t_head))))
+    per_step = oracle_sample_size(t_head, nt, args.ref_budget / max(1, args.steps + args.warmup), w.n_heads)
     ids = list(range(per_step))
     K, V, _ = synthkv.make_kv(w, seed=args.seed, heads=ids)
     hl = np.array([lens[h // w.heads] for h in ids], np.int32)
-    # a step: the sample's heads in nt batches, one host thread each (every
-    # batch is one call into the C oracle, which releases the interpreter lock)
-    import concurrent.futures as cf
-    bounds = np.linspace(0, per_step, min(nt, per_step) + 1).astype(int)
-    batches = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
-
-    def step(pool):
-        list(pool.map(lambda ab: oracle.compress_heads(K[ab[0]:ab[1]], V[ab[0]:ab[1]], hl[ab[0]:ab[1]], ratio, mode,
-                                                       window), batches))
-
-    with cf.ThreadPoolExecutor(max_workers=len(batches)) as pool:
-        for _ in range(args.warmup):
-            step(pool)
-        times = []
-        for _ in range(args.steps):
-            t0 = time.perf_counter()
-            step(pool)
-            times.append(time.perf_counter() - t0)
+    value, used, times = oracle_sample_rate(K, V, hl, ratio, mode, window, nt, steps=args.steps, warmup=args.warmup)
     sec = sum(times) / len(times)
     tok = int(hl.sum())
-    value = tok / sec
-    sample = (f"{per_step} of {w.n_heads} heads per step ({tok} token rows), fp64 C oracle, "
-              f"{len(batches)} threads over heads")
+    sample = (f"the first {per_step} of {w.n_heads} heads ({tok} token rows) per step, split into {used} batches, "
+              f"one host thread each, fp64 C oracle")
     line = {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; same generator and workload)",
-        "config": {"workload": w.name, "heads_total": w.n_heads, "t": w.t_max, "head_dim": w.head_dim,
-                   "mode": mode, "window": window, "ratio": ratio, "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(batches), "cpu_model": host_cpu_model(),
+        "vs_baseline": None, "dtype": "f64",
+        "data": synthkv.describe(w) + "; the same recipe drawn on the CPU",
+        "config": {"workload": w.name, "run": args.run, "heads_total": w.n_heads, "t": w.t_max,
+                   "head_dim": w.head_dim, "mode": mode, "window": window, "ratio": ratio,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "cpu_model": host_cpu_model(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -683,8 +689,7 @@ def run_secondary(args):
                 "gpu_launches": steps * ((1 if mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
                                           in (1, 2) else 3) + 2)}
     else:  # quota
-        w = workload_run("qwen3-8b-kv-t64k-w4096" if args.workload == synthkv.BENCH_WORKLOAD else args.workload,
-                         args.layers)[0]
+        w = workload_run(args.workload, args.layers)[0]
         K, V, lens = synthkv.make_kv(w, seed=args.seed, device=dev)
         mode, window, ratio = w.runs[0]
         window = window or 4096
@@ -721,30 +726,36 @@ def run_secondary(args):
     print(json.dumps(line), flush=True)
 
 
-def load_traffic(path, workload, layers, dtype, root=ROOT):
+def load_traffic(path, workload, layers, dtype, run=None, root=ROOT):
     """Per-kernel DRAM bytes per launch from an ncu record (profiles/traffic.json),
-    for the bench's own workload, layer count and cache type only. A kernel's
-    figure counts only while its source files are unchanged: the sha256 of
-    those files, concatenated in the listed order, must match the record.
-    Returns {kernel: bytes} (possibly empty), or None without a record."""
-    if not path or not os.path.exists(path):
+    for the bench's own workload, run (mode, window, ratio), layer count and
+    cache type only. The record holds one entry per captured (workload, run,
+    cache type); a kernel's figure counts only while its source files are
+    unchanged: the sha256 of those files, concatenated in the listed order,
+    must match the record. Returns {kernel: bytes} (possibly empty), or None
+    without a matching entry."""
+    if not path or not os.path.exists(path) or layers:
         return None
     with open(path) as f:
         t = json.load(f)
-    if t.get("workload") != workload or layers or t.get("cache_dtype", "bf16") != dtype:
-        return None
-    out = {}
-    for name, k in t.get("kernels", {}).items():
-        srcs = [os.path.join(root, x) for x in k.get("sources", [])]
-        if not srcs or not all(os.path.exists(x) for x in srcs):
+    for rec in t.get("records", []):
+        if rec.get("workload") != workload or rec.get("cache_dtype", "bf16") != dtype:
             continue
-        h = hashlib.sha256()
-        for src in srcs:
-            with open(src, "rb") as f:
-                h.update(f.read())
-        if h.hexdigest()[:16] == k.get("sha256_16"):
-            out[name] = k.get("bytes_per_launch")
-    return out
+        if run is not None and rec.get("run") is not None and list(rec["run"]) != list(run):
+            continue
+        out = {}
+        for name, k in rec.get("kernels", {}).items():
+            srcs = [os.path.join(root, x) for x in k.get("sources", [])]
+            if not srcs or not all(os.path.exists(x) for x in srcs):
+                continue
+            h = hashlib.sha256()
+            for src in srcs:
+                with open(src, "rb") as f:
+                    h.update(f.read())
+            if h.hexdigest()[:16] == k.get("sha256_16"):
+                out[name] = k.get("bytes_per_launch")
+        return out
+    return None
 
 
 def main(argv=None):
@@ -753,7 +764,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=synthkv.BENCH_WORKLOAD, choices=sorted(synthkv.WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(synthkv.WORKLOADS),
+                    help=f"default: {synthkv.BENCH_WORKLOAD} (ManifoldKV path), {synthkv.SECONDARY_WORKLOAD} "
+                         "(--path oja/summaries/inplace), qwen3-8b-kv-t64k-w4096 (--path quota)")
+    ap.add_argument("--run", type=int, default=0, help="which of the workload's runs (mode, window, ratio)")
+    ap.add_argument("--mode", choices=["l2", "cosine"], default=None, help="override the run's score mode")
+    ap.add_argument("--window", type=int, default=None, help="override the run's window (0 = global)")
+    ap.add_argument("--ratio", type=float, default=None, help="override the run's compression ratio")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -777,7 +794,14 @@ def main(argv=None):
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
                     help="per-kernel DRAM bytes per launch from an ncu capture (null when absent)")
     args = ap.parse_args(argv)
-    args.traffic = load_traffic(args.traffic_json, args.workload, args.layers, args.dtype)
+    if args.workload is None:
+        args.workload = (synthkv.BENCH_WORKLOAD if args.path == "manifold" else
+                         "qwen3-8b-kv-t64k-w4096" if args.path == "quota" else synthkv.SECONDARY_WORKLOAD)
+    if args.path == "manifold":
+        _, m, wd, r = workload_run(args.workload, 0, args.run, args.mode, args.window, args.ratio)
+        args.traffic = load_traffic(args.traffic_json, args.workload, args.layers, args.dtype, run=(m, wd, r))
+    else:
+        args.traffic = None
     if args.dtype != "bf16" and (args.impl == "reference" or args.path != "manifold"):
         ap.error("--dtype fp8 applies to the ManifoldKV path of our arm only")
     if args.impl == "reference":

@@ -49,6 +49,7 @@ EXPORTED = (
     "mkv_inject_stalled_windows", "mkv_window_means", "mkv_num_keep_quota", "mkv_select_quota",
     "mkv_compress_quota", "mkv_oja_workspace_size", "mkv_oja_score", "mkv_compress_oja", "mkv_oja_score_profiled",
     "mkv_compress_inplace", "mkv_set_head_groups", "mkv_set_fused", "mkv_centroid_score",
+    "mkv_inject_stalled_fused",
 )
 
 
@@ -105,6 +106,7 @@ def load(build_if_missing: bool = True):
             "mkv_centroid_score": (i32, [vp, MkvShape, i32, i32, vp, vp, vp, sz, vp]),
             "mkv_layer_budgets": (i32, [vp, i32, f64, f64, ctypes.c_int64, vp, vp]),
             "mkv_inject_stalled_windows": (i32, [vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
+            "mkv_inject_stalled_fused": (i32, [vp, vp, MkvShape, f64, i32, i32, vp, vp, vp, vp, i32, vp, sz, vp]),
             "mkv_compress_profiled": (i32, [vp, vp, MkvShape, f64, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp,
                                             ctypes.POINTER(vp), i32]),
             "mkv_compress_host": (i32, [vp, vp, vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp,
@@ -421,6 +423,19 @@ def mkv_inject_stalled_windows(K, V, ratio, mode, window, keep_stride, K_out, V_
                                              int(window), int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx),
                                              _ptr(kept), _ptr(workspace), workspace.numel(), _stream(stream)),
            "mkv_inject_stalled_windows")
+
+
+def mkv_inject_stalled_fused(K, V, ratio, mode, keep_stride, K_out, V_out, idx, kept, stage, workspace,
+                             seq_lens=None, stream=None):
+    """Failure injection: the fused whole-path kernel with one wait that
+    cannot end (stage 0: scorer group 0's barrier; stage 1: head 0's select);
+    it must run out (MKV_DEV_TIMEOUT) and the rest of the launch drain."""
+    _need_cuda(K, V, K_out, V_out, idx, kept, workspace, seq_lens)
+    _cache_types(K, V, K_out, V_out)
+    _check(load().mkv_inject_stalled_fused(_ptr(K), _ptr(V), shape_of(K, seq_lens), float(ratio), _MODES[mode],
+                                           int(keep_stride), _ptr(K_out), _ptr(V_out), _ptr(idx), _ptr(kept),
+                                           int(stage), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mkv_inject_stalled_fused")
 
 
 def mkv_device_status(workspace, stream=None) -> int:

@@ -253,7 +253,7 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
                         mkv_mode mode, int32_t window, int32_t keep_stride, void *K_out, void *V_out,
                         int32_t *idx, int32_t *kept, void *ws, size_t ws_bytes, cudaStream_t st,
                         void *const *events, bool stall_windows = false, bool quota = false, bool in_place = false,
-                        bool allow_fused = true)
+                        bool allow_fused = true, int stall_fused = -1)
 {
     mkv_status rc = check_shape(s);
     if (rc != MKV_OK) return rc;
@@ -279,19 +279,25 @@ mkv_status run_compress(const void *K, const void *V, mkv_shape s, double ratio,
     cudaError_t e = cudaSuccess;
     int32_t *idx_w = idx ? idx : region<int32_t>(ws, L.idx);
     const int32_t idx_stride = idx ? keep_stride : g.t_max;
-    // the whole path in one launch, when the fused setting and the shape allow it
-    const FusedBudget fb = fused_budget(g);
+    // the whole path in one launch, when the fused setting and the shape allow
+    // it (a stall injection takes it wherever the kernel can run the shape)
+    FusedBudget fb = fused_budget(g);
+    if (stall_fused >= 0 && fb.scorers == 0) {
+        fb.scorers = -1;
+        fb.selectors = (int)std::max<int64_t>(16, (g.n_heads + 15) / 16);
+    }
     if (fb.scorers != 0 && allow_fused && !events && !stall_windows && !quota && !in_place && K_out &&
         g_head_groups_enabled.load(std::memory_order_relaxed) && !g_single_pass_enabled.load(std::memory_order_relaxed)) {
         const FusedPlan fp = fused_plan(g.pg, (int)mode, L.centroid - L.counters, fb.scorers, fb.selectors);
         if (fp.grid > 0) {
             e = launch_fused(g.pg, fp, (int)mode, K, V, s.seq_lens, region<float>(ws, L.partial),
                              region<uint32_t>(ws, L.counters), C, S, ratio, n_keep, keep_stride, kept_w, idx_w,
-                             idx_stride, K_out, V_out, status, st);
-            if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e);
+                             idx_stride, K_out, V_out, status, st, stall_fused);
+            if (e != cudaErrorCooperativeLaunchTooLarge || stall_fused >= 0) return cuda_status(e);
             (void)cudaGetLastError();  // fewer CTAs fit right now: the separate kernels
         }
     }
+    if (stall_fused >= 0) return MKV_ERR_UNSUPPORTED;  // the fused kernel cannot run this shape here
     if (!mark(0)) return MKV_ERR_CUDA;
     // a1 + a2 (C and S are workspace regions here)
     rc = run_centroid_score(g, L, K, s, mode, ws, C, S, st, mark, stall_windows);
@@ -707,6 +713,17 @@ mkv_status mkv_inject_stalled_windows(const void *K, const void *V, mkv_shape sh
 {
     return run_compress(K, V, shape, ratio, nullptr, mode, window, keep_stride, K_out, V_out, idx, kept, workspace,
                         workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr, true);
+}
+
+mkv_status mkv_inject_stalled_fused(const void *K, const void *V, mkv_shape shape, double ratio, mkv_mode mode,
+                                    int32_t keep_stride, void *K_out, void *V_out, int32_t *idx, int32_t *kept,
+                                    int32_t stage, void *workspace, size_t workspace_bytes, mkv_stream_t stream)
+{
+    if (stage != 0 && stage != 1) return MKV_ERR_INVALID_ARG;
+    if (!K_out || !V_out) return MKV_ERR_INVALID_ARG;
+    return run_compress(K, V, shape, ratio, nullptr, mode, 0, keep_stride, K_out, V_out, idx, kept, workspace,
+                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr, false, false, false, true,
+                        stage);
 }
 
 int32_t mkv_layer_budgets(const double *sensitivity, int32_t layers, double r, double gamma, int64_t total,

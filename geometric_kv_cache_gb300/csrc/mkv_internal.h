@@ -96,7 +96,9 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counter_b
 // tokens): scorer head groups within `scorer_ctas` CTAs (< 0: 3/4 of the
 // resident grid), `select_ctas`
 // selector CTAs, every warp a gatherer afterwards; grid 0 when it does not
-// apply.
+// apply. launch_fused's `stall` injects a wait that cannot end (failure
+// tests only): 0 the barrier of scorer group 0, 1 the select of head 0; -1
+// none.
 struct FusedPlan {
     HeadGroupPlan hg;
     int grid = 0;         // resident CTAs of the launch
@@ -106,7 +108,7 @@ FusedPlan fused_plan(const PieceGeometry &g, int mode, size_t counter_bytes, int
 cudaError_t launch_fused(const PieceGeometry &g, const FusedPlan &fp, int mode, const void *K, const void *V,
                          const int32_t *seq_lens, float *partial, uint32_t *cnt, float *C, float *S, double ratio,
                          const int32_t *n_keep, int32_t keep_stride, int32_t *kept, int32_t *idx, int32_t idx_stride,
-                         void *K_out, void *V_out, uint32_t *status, cudaStream_t st);
+                         void *K_out, void *V_out, uint32_t *status, cudaStream_t st, int stall = -1);
 cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan, const void *K,
                                const int32_t *seq_lens, int mode, float *partial, uint32_t *cnt, float *C, float *S,
                                uint32_t *status, cudaStream_t st);

@@ -919,10 +919,18 @@ constexpr int kMaxSlots = stash_slots(64);
 // in it). With head_done, every CTA of the group adds 1 to head_done[head]
 // once the unit's scores it wrote are visible GPU-wide (units are whole heads
 // there: a group's count reaches gsize when the head's scores are complete).
+//
+// A group barrier that runs out (or, with `abortable`, finds that another
+// wait of the launch has run out) skips the unit's means and scores, and its
+// CTA does not count the head in head_done: a head's count then never
+// reaches gsize, so nothing downstream reads its scores. `barrier_extra`
+// raises this group's barrier target above its CTA count (failure
+// injection: 0 in every ordinary launch).
 template <int MODE, int NB, int ES>
 __device__ __forceinline__ void head_groups_run(const PieceGeometry &g, const Pointers &P, uint32_t *gcnt, int gsize,
                                                 int wb, uint32_t stagger_ns, int groups, int group, int rank,
-                                                uint32_t *head_done)
+                                                uint32_t *head_done, bool abortable = false,
+                                                uint32_t barrier_extra = 0)
 {
     constexpr int D = 64 * NB, RB = ES * D;
     using Raw = typename Chunk<ES>::raw;
@@ -1017,14 +1025,20 @@ __device__ __forceinline__ void head_groups_run(const PieceGeometry &g, const Po
         if (threadIdx.x == 0) {
             __threadfence();
             atomicAdd(&gcnt[group], 1u);
-            const uint32_t target = (round + 1) * (uint32_t)gsize;
+            const uint32_t target = (round + 1) * (uint32_t)gsize + barrier_extra;
             const uint64_t t0 = global_ns();
             uint32_t ok = 1;
             for (uint32_t spin = 0; ld_acquire(&gcnt[group]) < target; ++spin) {
-                if ((spin & 63u) == 63u && global_ns() - t0 > kWaitNs) {
-                    atomicOr(P.status, MKV_DEV_TIMEOUT);
-                    ok = 0;
-                    break;
+                if ((spin & 63u) == 63u) {
+                    if (abortable && timed_out(P.status)) {
+                        ok = 0;
+                        break;
+                    }
+                    if (global_ns() - t0 > kWaitNs) {
+                        atomicOr(P.status, MKV_DEV_TIMEOUT);
+                        ok = 0;
+                        break;
+                    }
                 }
             }
             s_ok = ok;
@@ -1086,7 +1100,7 @@ __device__ __forceinline__ void head_groups_run(const PieceGeometry &g, const Po
                 }
             }
         }
-        if (head_done) {  // this CTA's scores of the unit are visible before the count
+        if (head_done && s_ok) {  // this CTA's scores of the unit are visible before the count
             __threadfence();
             __syncthreads();
             if (threadIdx.x == 0) {
@@ -1140,6 +1154,11 @@ struct TailArgs {
     uint32_t *head_done, *sel_done, *sel_ticket, *gather_ticket;
     double ratio;
     int keep_stride, idx_stride, bph, select_ctas;
+    // failure injection (-1 in every ordinary launch): the scorer group whose
+    // barrier target is one above its CTA count, and the head whose select
+    // waits for one scorer more than the group has
+    int stall_group;
+    int64_t stall_head;
 };
 
 // One thread waits until *flag >= target (bounded); 1 when it got there. With
@@ -1224,9 +1243,11 @@ k_fused_path(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int groups,
     if (threadIdx.x == 0) s_abortable = timed_out(P.status) ? 0u : 1u;  // read before any wait of this CTA
     __syncthreads();
     const bool abortable = s_abortable != 0u;
-    if ((int)blockIdx.x < groups * gsize)
-        head_groups_run<MODE, NB, ES>(g, P, gcnt, gsize, 1, stagger_ns, groups, (int)blockIdx.x / gsize,
-                                      (int)blockIdx.x % gsize, A.head_done);
+    if ((int)blockIdx.x < groups * gsize) {
+        const int group = (int)blockIdx.x / gsize;
+        head_groups_run<MODE, NB, ES>(g, P, gcnt, gsize, 1, stagger_ns, groups, group, (int)blockIdx.x % gsize,
+                                      A.head_done, abortable, group == A.stall_group ? 1u : 0u);
+    }
     const int64_t n_heads = g.n_heads;
     if ((int)blockIdx.x >= (int)gridDim.x - A.select_ctas) {
         for (;;) {
@@ -1235,7 +1256,9 @@ k_fused_path(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int groups,
             __syncthreads();
             const int64_t head = s_ticket;
             if (head >= n_heads) break;  // the same for every thread
-            if (threadIdx.x == 0) s_go = wait_count(A.head_done + head, (uint32_t)gsize, P.status, abortable);
+            if (threadIdx.x == 0)
+                s_go = wait_count(A.head_done + head, (uint32_t)gsize + (head == A.stall_head ? 1u : 0u), P.status,
+                                  abortable);
             __syncthreads();
             if (s_go)
                 select_item<true, false, kThreads>(head, P.S, P.seq_lens, g.heads, g.t_max, A.ratio, A.n_keep,
@@ -1512,7 +1535,7 @@ FusedPlan fused_plan(const PieceGeometry &g, int mode, size_t counters, int scor
 cudaError_t launch_fused(const PieceGeometry &g, const FusedPlan &fp, int mode, const void *K, const void *V,
                          const int32_t *seq_lens, float *partial, uint32_t *cnt, float *C, float *S, double ratio,
                          const int32_t *n_keep, int32_t keep_stride, int32_t *kept, int32_t *idx, int32_t idx_stride,
-                         void *K_out, void *V_out, uint32_t *status, cudaStream_t st)
+                         void *K_out, void *V_out, uint32_t *status, cudaStream_t st, int stall)
 {
     const void *fn = fused_fn(g.d, g.es, mode);
     if (!fn || fp.grid <= 0) return cudaErrorInvalidValue;
@@ -1537,6 +1560,8 @@ cudaError_t launch_fused(const PieceGeometry &g, const FusedPlan &fp, int mode, 
     const int rows = fused_gather_rows(g.d * g.es);
     A.bph = (keep_stride + rows - 1) / rows;
     A.select_ctas = fp.select_ctas;
+    A.stall_group = stall == 0 ? 0 : -1;
+    A.stall_head = stall == 1 ? 0 : -1;
     PieceGeometry gg = g;
     int gsize = fp.hg.gsize, groups = fp.hg.groups;
     uint32_t stagger = fp.hg.stagger_ns;

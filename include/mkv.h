@@ -125,7 +125,11 @@ typedef struct {
 } mkv_cut;
 
 /* Kept tokens out of T at compression `ratio` (host helper; same rounding as
- * the kernels). Returns -1 for T < 0 or ratio outside [0, 1]. */
+ * the kernels). Returns -1 for T < 0 or ratio outside [0, 1].
+ * Source: the ManifoldKV abstract quotes its results "at 20% compression" and
+ * "at 50% compression"; the percentage is read as the share of tokens
+ * removed, so n_keep = round(T * (1 - ratio)), halves rounding up (the
+ * workload text fixes 3277 kept of 4096 at 20%). */
 int32_t mkv_num_keep(int32_t T, double ratio);
 
 /* Windows per head of t_max tokens (0 if t_max = 0). */
@@ -182,7 +186,9 @@ mkv_status mkv_score(const void *K, const float *C, mkv_shape shape, int32_t win
 mkv_status mkv_select_topk(const float *S, mkv_shape shape, double ratio, const int32_t *n_keep,
                            mkv_cut *cut, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
-/* Compaction and gather. From S and cut, emit per head the kept token indices
+/* Compaction and gather (abstract: the method decides which past tokens
+ * the cache retains; lay summary: the retained far-from-ordinary tokens form
+ * the smaller cache). From S and cut, emit per head the kept token indices
  * in ascending order into idx [batch*heads, keep_stride] and their count into
  * kept [batch*heads], and copy the kept rows bit for bit: K_out[h][j] =
  * K[h][idx[h][j]], V_out likewise, both [batch, heads, keep_stride,
@@ -195,8 +201,12 @@ mkv_status mkv_compact(const float *S, const mkv_cut *cut, const void *K, const 
                        void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
 /* The whole path (centroid -> score -> select -> compact + gather) in one
- * call, intermediates in the workspace. Outputs as for mkv_compact; idx and
- * kept may be NULL (not returned). */
+ * call, intermediates in the workspace (abstract: rank the cached keys by
+ * their distance to the key centroid -- per window for WindowedManifoldKV --
+ * and keep the most distant share; the cosine-to-centroid scorer is the
+ * baseline switch; lay summary: only the unusual, far-away tokens stay in
+ * the compressed cache). Outputs as for mkv_compact; idx and kept may be
+ * NULL (not returned). */
 mkv_status mkv_compress(const void *K, const void *V, mkv_shape shape, double ratio,
                         const int32_t *n_keep, mkv_mode mode, int32_t window, int32_t keep_stride,
                         void *K_out, void *V_out, int32_t *idx, int32_t *kept,
@@ -385,6 +395,23 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
                              void *hK_out, void *hV_out, int32_t *h_idx, int32_t *h_kept,
                              void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
+/* Failure injection for tests of the fused whole-path kernel's bounded waits
+ * (no counterpart in the paper). Runs mkv_compress through the fused kernel
+ * (global centroids; with the automatic budgets when its own rule would not
+ * take the shape) with one wait that cannot end: stage 0 raises the
+ * barrier target of scorer group 0 above its CTA count, stage 1 makes the
+ * select of head 0 wait for one scorer more than its group has. The wait
+ * runs out after its bound (about 1 s) and sets MKV_DEV_TIMEOUT; every other
+ * wait of the launch then gives up at once, so the launch ends in about one
+ * bound and the context stays usable. A head whose scoring or select did not
+ * complete keeps no rows (kept = 0): no select runs on stale scores. The
+ * other outputs are not meaningful. MKV_ERR_INVALID_ARG for another stage or
+ * without K_out/V_out; MKV_ERR_UNSUPPORTED when the fused kernel cannot run
+ * the shape (window is 0 here). */
+mkv_status mkv_inject_stalled_fused(const void *K, const void *V, mkv_shape shape, double ratio, mkv_mode mode,
+                                    int32_t keep_stride, void *K_out, void *V_out, int32_t *idx, int32_t *kept,
+                                    int32_t stage, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
+
 /* Size of the library-owned scratch array used by mkv_compress_noalloc. */
 #define MKV_NOALLOC_SCRATCH_BYTES (32u << 20)
 
@@ -399,19 +426,28 @@ mkv_status mkv_compress_host(const void *hK, const void *hV, void *dK, void *dV,
  * image. Every GPU that loads the library holds that array until the process
  * exits, whether or not this call is used.
  *   Limits: the problem must fit, i.e. mkv_workspace_size(shape, window) <=
- *   MKV_NOALLOC_SCRATCH_BYTES (about 6.6M token rows, heads x t_max, per call at window 0).
- *   Larger problems return MKV_ERR_UNSUPPORTED and enqueue nothing; split
- *   them into several calls over groups of heads.
+ *   MKV_NOALLOC_SCRATCH_BYTES. At head dim 128 and window 0 the workspace
+ *   takes about 10 bytes per token row (heads x t_max: scores, fallback
+ *   indices, partial sums, compaction offsets), so one call holds about
+ *   3.3M token rows at t_max 4K-16K (202 heads of 16384 tokens) and about
+ *   3.9M at 64K-128K (30 heads of 131072). Larger problems return
+ *   MKV_ERR_UNSUPPORTED and enqueue nothing; split them into several calls
+ *   over groups of heads, sized with mkv_workspace_size.
  *   Set-up: the first call on a device, with that device current, looks up the
- *   array's device address once (cudaGetSymbolAddress). Make that first call
- *   before any stream capture.
+ *   array's device address once (cudaGetSymbolAddress) and keeps it for the
+ *   life of the process. Make that first call before any stream capture. Do
+ *   not call this entry point again on a device after cudaDeviceReset there:
+ *   the kept address would be stale.
  *   Sharing: every call uses the same array, and it keeps the last call's
  *   contents. Calls that can overlap on the GPU (different streams, or
  *   different host threads, on one device) race on it and corrupt each
  *   other's results. Serialise them.
  *   Outputs and arguments: as for mkv_compress. status_out (device, nullable)
  *   receives the device status word of this call (MKV_DEV_* bits); the call
- *   then resets the word to zero. After MKV_ERR_CUDA the call still tries to
+ *   then resets the word to zero. With status_out NULL those bits are
+ *   discarded (there is no workspace to query afterwards), including
+ *   MKV_DEV_TIMEOUT: callers that need device-side error detection must pass
+ *   status_out. After MKV_ERR_CUDA the call still tries to
  *   reset it (best effort: the failed call's bits are not reported, and a
  *   sticky CUDA error can prevent the reset). The call allocates and frees
  *   nothing. */

@@ -55,6 +55,7 @@ class KVWorkload:
     drift_every: int = 0                 # 0 = no mean drift
     drift_std: float = 0.25
     runs: tuple = ()                     # ((mode, window, ratio), ...): mode in {"l2", "cosine"}, window 0 = global
+    model: str = ""                      # the model whose KV shape this follows
 
     @property
     def rows(self) -> int:
@@ -77,26 +78,44 @@ class KVWorkload:
 WORKLOADS = {
     "single-layer-h8-t4096": KVWorkload(
         name="single-layer-h8-t4096", layers=1, batch=1, heads=8, t_max=4096,
-        sigma=0.5, planted=16, runs=(("l2", 0, 0.2),)),
+        sigma=0.5, planted=16, runs=(("l2", 0, 0.2),), model=""),
     "llama3.1-8b-kv-t16k": KVWorkload(
         name="llama3.1-8b-kv-t16k", layers=32, batch=1, heads=8, t_max=16384,
-        sigma=0.5, outlier_channels=4, runs=(("l2", 0, 0.5),)),
+        sigma=0.5, outlier_channels=4, runs=(("l2", 0, 0.5),), model="Llama-3.1-8B"),
     "qwen3-8b-kv-t64k-w4096": KVWorkload(
         name="qwen3-8b-kv-t64k-w4096", layers=36, batch=1, heads=8, t_max=65536,
         sigma=0.5, outlier_channels=4, drift_every=8192,
-        runs=(("l2", 4096, 0.25),)),
+        runs=(("l2", 4096, 0.25),), model="Qwen3-8B"),
     "ragged-b8-llama-kv-t8k-32k": KVWorkload(
         name="ragged-b8-llama-kv-t8k-32k", layers=32, batch=8, heads=8,
         t_max=32768, t_min=8192, sigma=0.5, planted=32,
-        runs=(("l2", 0, 0.2), ("l2", 0, 0.5), ("cosine", 0, 0.2), ("cosine", 0, 0.5))),
+        runs=(("l2", 0, 0.2), ("l2", 0, 0.5), ("cosine", 0, 0.2), ("cosine", 0, 0.5)), model="Llama-3.1-8B"),
     "phi4-kv-t128k": KVWorkload(
         name="phi4-kv-t128k", layers=40, batch=1, heads=10, t_max=131072,
         sigma=0.7, outlier_channels=4, drift_every=16384,
-        runs=(("l2", 8192, 0.5), ("l2", 0, 0.5), ("cosine", 0, 0.5))),
+        runs=(("l2", 8192, 0.5), ("l2", 0, 0.5), ("cosine", 0, 0.5)), model="Phi-4"),
 }
 
-# The workload whose throughput the bench reports.
-BENCH_WORKLOAD = "llama3.1-8b-kv-t16k"
+# The workload whose throughput the bench reports by default: the largest
+# one, Phi-4-shaped at 131072 tokens (where the windowed centroids matter).
+BENCH_WORKLOAD = "phi4-kv-t128k"
+# The workload the widened paths (OjaKV, summaries, in-place) run on by default.
+SECONDARY_WORKLOAD = "llama3.1-8b-kv-t16k"
+
+
+def describe(w: KVWorkload) -> str:
+    """One line naming the workload's shape and key distribution."""
+    T = f"T={w.t_max}" if w.t_min is None else f"T~U{{{w.t_min}..{w.t_max}}} per sequence"
+    parts = [f"N(0,1) keys", f"lognormal(0,{w.sigma}) token norms"]
+    if w.outlier_channels:
+        parts.append(f"{w.outlier_channels} outlier channels x{w.outlier_scale:g}")
+    if w.planted:
+        parts.append(f"{w.planted} planted tokens per head at norm {w.planted_norm:g}")
+    if w.drift_every:
+        parts.append(f"mean drift every {w.drift_every} tokens")
+    shape = f"{w.layers} layers x {w.batch} seq x {w.heads} KV heads, d={w.head_dim}, {T}"
+    kind = f"{w.model}-shaped KV cache" if w.model else "KV cache"
+    return f"synthetic (seeded; {kind}: {shape}; " + ", ".join(parts) + "; V ~ N(0,1))"
 
 
 def _mix(seed: int, *keys: int) -> int:

@@ -1,11 +1,20 @@
-"""GPU parity of the fused whole-path kernel (opt-in, mkv_set_fused): one
-cooperative launch whose scorer head groups, selector CTAs and gatherer
-warps hand work over through bounded waits. Its outputs must be the separate kernels' bits
+"""GPU parity of the fused whole-path kernel: one cooperative launch whose
+scorer head groups, selector CTAs and gatherer warps hand work over through
+bounded waits. mkv_compress takes it by default under its own shape rule
+(bf16, head dim 128, global centroids, 12288 < t_max <= 20480);
+mkv_set_fused forces scorer/selector budgets wherever it applies, or turns
+it off (this module turns it off and forces it per test, then restores the
+previous setting). Its outputs must be the separate kernels' bits
 (every head, every output row) on bf16 and E4M3 caches, head dims 64 / 128 /
 256, ragged lengths with empty and sub-piece heads, a per-head n_keep array,
 both score modes, the largest t_max it takes, and small and large scorer
 and selector budgets; a small case is also checked head by head against
-the fp64 oracle."""
+the fp64 oracle. Its bounded waits are made to run out on purpose (a
+host-side injection, no fault): the launch must drain in about one wait
+bound, report MKV_DEV_TIMEOUT, keep no rows for the heads it could not
+finish, and leave the context usable."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -170,4 +179,47 @@ def test_fused_kernel_own_rule():
         mkv.mkv_set_fused(0)
     st0, a = _compress(K, V, None, 0.5, "l2", mkv.mkv_num_keep(K.shape[2], 0.5))
     assert st0 == 0 and st1 == 0
+    _same(a, b)
+
+
+@pytest.mark.parametrize("stage", [0, 1])
+def test_fused_stalled_wait_times_out_and_drains(stage):
+    # One wait that cannot end: stage 0 raises scorer group 0's barrier
+    # target above its CTA count (head 0 is group 0's first unit), stage 1
+    # makes head 0's select wait for one scorer more than its group has.
+    K, V, lens = _cache("fused-stall", 3, layers=4)  # 32 heads x 16384 tokens
+    ratio, mode = 0.5, "l2"
+    B, H, T, D = K.shape
+    ks = mkv.mkv_num_keep(T, ratio)
+    ref_status, ref = _compress(K, V, lens, ratio, mode, ks)  # separate kernels (fused off in this module)
+    assert ref_status == 0
+    Ko = torch.zeros((B, H, ks, D), dtype=K.dtype, device=DEV)
+    Vo = torch.zeros_like(Ko)
+    idx = torch.full((B, H, ks), -7, dtype=torch.int32, device=DEV)
+    kept = torch.full((B, H), -7, dtype=torch.int32, device=DEV)
+    ws = mkv.workspace_for(K, 0, lens)
+    assert mkv.mkv_device_status(ws) == 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    mkv.mkv_inject_stalled_fused(K, V, ratio, mode, ks, Ko, Vo, idx, kept, stage, ws, lens)
+    status = mkv.mkv_device_status(ws)  # synchronises the stream
+    elapsed = time.perf_counter() - t0
+    assert status & mkv.MKV_DEV_TIMEOUT
+    # one wait bound (1 s), not one per wait: the other waits gave up at once
+    assert elapsed < 2.5, f"the stalled launch took {elapsed:.2f} s"
+    kc = kept.reshape(-1).cpu()
+    assert int(kc[0]) == 0, "the stalled head kept rows"
+    assert bool(torch.all((kc == 0) | (kc == ks))), "a head kept a partial count"
+    # a head that kept rows was selected on its complete scores: its indices
+    # are the separate kernels' (no select ran on stale or partial scores)
+    done = torch.nonzero(kc == ks).flatten().tolist()
+    ref_idx = ref[1].reshape(B * H, ks)
+    got_idx = idx.reshape(B * H, ks)
+    for h in done:
+        assert torch.equal(got_idx[h], ref_idx[h]), f"head {h} kept other rows than the separate kernels"
+    if stage == 1:  # only head 0's select waited: every other head completed
+        assert len(done) == B * H - 1
+    # the context is still usable: an ordinary fused call on the same
+    # workspace gives the separate kernels' bits
+    a, b = _both(K, V, lens, ratio, mode, ks)
     _same(a, b)

@@ -11,7 +11,7 @@ import torch
 import geometric_kv_cache_gb300 as mkv
 import oracle
 import synthkv
-from parity_util import StepBuffers, bits, compare_head, oracle_heads, report
+from parity_util import StepBuffers, bits, check_in_place_vs_oracle, compare_head, oracle_heads, report
 
 pytestmark = pytest.mark.gpu
 
@@ -146,9 +146,12 @@ def test_in_place_and_quota(d):
     Ki, Vi = K.clone(), V.clone()
     ws = mkv.workspace_for(K, 0, lens)
     kept_i = torch.zeros_like(kept)
-    mkv.mkv_compress_inplace(Ki, Vi, ratio, "l2", 0, ws, kept=kept_i, seq_lens=lens)
+    idx_i = torch.full((B, H, T), -7, dtype=torch.int32, device=DEV)
+    mkv.mkv_compress_inplace(Ki, Vi, ratio, "l2", 0, ws, idx=idx_i, kept=kept_i, seq_lens=lens)
     assert mkv.mkv_device_status(ws) == 0
     assert torch.equal(kept_i, kept)
+    # every head against the oracle's in-place move (rows past kept untouched)
+    check_in_place_vs_oracle(K, V, Ki, Vi, kept_i, lens.cpu().numpy(), ratio, "l2", 0, idx_i=idx_i)
     ks = idx.shape[2]
     front = (torch.arange(ks, device=DEV)[None, None, :] < kept[..., None])[..., None].expand(-1, -1, -1, D)
     assert torch.equal(Ki[..., :ks, :][front], Ko[front]) and torch.equal(Vi[..., :ks, :][front], Vo[front])

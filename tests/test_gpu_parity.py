@@ -15,7 +15,7 @@ import torch
 import geometric_kv_cache_gb300 as mkv
 import oracle
 import synthkv
-from parity_util import StepBuffers, bits, compare_head, oracle_heads, report
+from parity_util import StepBuffers, bits, check_in_place_vs_oracle, compare_head, oracle_heads, report
 
 pytestmark = pytest.mark.gpu
 
@@ -391,8 +391,9 @@ def test_host_path_with_pageable_values_copies_them():
             assert not torch.any(dV.view(torch.int16) != 0)
 
 
-def _check_in_place(K, V, lens, ratio, mode, window):
-    """mkv_compress_inplace against mkv_compress on the same cache."""
+def _check_in_place(K, V, lens, ratio, mode, window, oracle_heads_=None):
+    """mkv_compress_inplace against the oracle's in-place move (every head,
+    or the listed ones) and against mkv_compress on the same cache."""
     Ko, Vo, idx, kept, st = _run_fused(K, V, ratio, mode, window, lens)
     assert st == 0
     B, H, T, D = K.shape
@@ -415,6 +416,9 @@ def _check_in_place(K, V, lens, ratio, mode, window):
                        Vo[front[..., :ks, :].expand(-1, -1, -1, D)])
     rest = ~front.expand(-1, -1, -1, D)
     assert torch.equal(Ki[rest], K[rest]) and torch.equal(Vi[rest], V[rest])
+    near = check_in_place_vs_oracle(K, V, Ki, Vi, kept_i, lens.cpu().numpy(), ratio, mode, window,
+                                    heads=oracle_heads_, idx_i=idx_i)
+    report(f"inplace:{mode}:w{window}:r{ratio}", shape=list(K.shape), near_cut_exceptions=near)
 
 
 @pytest.mark.parametrize("mode,window,ratio", [("l2", 0, 0.5), ("cosine", 3000, 0.2), ("l2", 700, 0.9),
@@ -431,7 +435,7 @@ def test_in_place_compaction_full_size():
     torch.cuda.empty_cache()
     K, V, lens = synthkv.make_kv(w, seed=0, device=DEV)
     mode, window, ratio = w.runs[0]
-    _check_in_place(K, V, lens, ratio, mode, window)
+    _check_in_place(K, V, lens, ratio, mode, window, oracle_heads_=[0, 77, w.n_heads - 1])
     del K, V
     torch.cuda.empty_cache()
 
@@ -471,7 +475,22 @@ def _full_size(name, runs=None, sample=4):
             m = live[r][..., None]
             assert torch.equal(torch.where(m, torch.gather(K[r], 1, gi), 0), torch.where(m, Ko[r], 0))
             assert torch.equal(torch.where(m, torch.gather(V[r], 1, gi), 0), torch.where(m, Vo[r], 0))
-        # sampled heads against the oracle
+        # a1 + a2 of the same call (mkv_centroid_score runs them as
+        # mkv_compress does) and the step-wise mkv_centroid + mkv_score:
+        # every head's full-T scores, bit-identical between the two paths
+        nw = max(mkv.mkv_num_windows(T, window), 1)
+        C1 = torch.zeros((w.rows, w.heads, nw, 128), dtype=torch.float32, device=DEV)
+        S1 = torch.zeros((w.rows, w.heads, T), dtype=torch.float32, device=DEV)
+        C2, S2 = torch.zeros_like(C1), torch.zeros_like(S1)
+        mkv.mkv_centroid_score(K, window, mode, C1, S1, ws, lens)
+        mkv.mkv_centroid(K, window, C2, ws, lens)
+        mkv.mkv_score(K, C2, window, mode, S2, ws, lens)
+        assert mkv.mkv_device_status(ws) == 0
+        tok_live = torch.arange(T, device=DEV)[None, None, :] < T_h[..., None]
+        assert torch.equal(S1[tok_live], S2[tok_live]), "compress-path and step-wise scores differ"
+        # sampled heads against the oracle: C and every score at the head's
+        # full length, the selection (also the top-n_keep of these scores)
+        # and the gathered rows
         ora = oracle_heads(K, V, lens_cpu, w.heads, heads, ratio, mode, window)
         Kf, Vf = K.reshape(n, T, 128), V.reshape(n, T, 128)
         near = 0
@@ -479,10 +498,14 @@ def _full_size(name, runs=None, sample=4):
             b, hh = divmod(h, w.heads)
             Th = int(lens_cpu[b])
             nk = int(kept[b, hh])
-            res = compare_head(ora[h], Th, idx_gpu=idx[b, hh].cpu().numpy(), kept_gpu=nk, K_head=Kf[h],
+            nwh = ora[h]["C"].shape[0]
+            res = compare_head(ora[h], Th, S_gpu=S1[b, hh].cpu().numpy(), C_gpu=C1[b, hh, :nwh].cpu().numpy(),
+                               key_scale=float(Kf[h, :Th].float().abs().mean().item()) if Th else 1.0,
+                               idx_gpu=idx[b, hh].cpu().numpy(), kept_gpu=nk, K_head=Kf[h],
                                V_head=Vf[h], Kout_gpu=bits(Ko[b, hh, :nk]), Vout_gpu=bits(Vo[b, hh, :nk]),
                                mode=mode)
             near += res["near_cut_exceptions"]
+        del C1, S1, C2, S2
         report(f"{name}:{mode}:w{window}:r{ratio}:full", heads_sampled=len(heads), near_cut_exceptions=near,
                heads_property_checked=n)
         del Ko, Vo, idx, kept, ws
