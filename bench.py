@@ -340,6 +340,8 @@ def run_ours(args):
     mkv.load()
     if args.no_head_groups:
         mkv.mkv_set_head_groups(False)
+    if args.ring is not None:
+        mkv.mkv_set_head_group_ring(bool(args.ring))
     w, mode, window, ratio = workload_run(args.workload, args.layers, args.run, args.mode, args.window, args.ratio)
     cache_dtype = {"bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}[args.dtype]
     K, V, lens = synthkv.make_kv(w, seed=rank_seed(args.seed, rank), device=dev, dtype=cache_dtype)
@@ -359,7 +361,7 @@ def run_ours(args):
     if args.fused is not None and args.fused > 0 and single != 3:
         raise SystemExit("--fused: the fused kernel does not apply to this workload (global centroids, t <= 20480)")
     select_emits = T <= 40960  # select writes the kept indices itself (no compaction kernel)
-    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single in (1, 2, 3) else 2, es=es)
+    nbytes = path_bytes(lens_list, w.heads, ratio, w.head_dim, k_reads=1 if single in (1, 2, 3, 4) else 2, es=es)
 
     def step():
         mkv.mkv_compress(K, V, ratio, mode, window, ks, K_out, V_out, idx, kept, ws, lens, stream=stream)
@@ -469,6 +471,8 @@ def run_ours(args):
                    "window": window, "ratio": ratio, "keep_per_head": ks,
                    "centroid_score_path": {0: "three kernels (K read twice)", 1: "single pass (K read once)",
                                            2: "head groups (K read from HBM once, again from L2)",
+                                           4: "head groups with a copy ring (K read from HBM once by bulk "
+                                              "copies, again from L2)",
                                            3: "fused whole path (one launch: head groups, selects, gathers; "
                                               + ("the library's own rule" if args.fused is None else
                                                  f"scorer budget {args.fused}, {args.fused_selectors} selector CTAs")
@@ -488,7 +492,7 @@ def run_ours(args):
         # per step: a1 + a2 (one kernel, or piece sums + window means + scores),
         # select, compaction when select did not emit the indices, gather
         "gpu_launches": args.steps * (1 if single == 3 else
-                                      (1 if single in (1, 2) else 3) + 1 + (0 if select_emits else 1) + 1),
+                                      (1 if single in (1, 2, 4) else 3) + 1 + (0 if select_emits else 1) + 1),
         "clocks": clocks.summary(),
     }
     if world > 1:
@@ -687,7 +691,7 @@ def run_secondary(args):
                 "clocks": clocks.summary(),
                 # a1 + a2 (one kernel or three), select, in-place move
                 "gpu_launches": steps * ((1 if mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
-                                          in (1, 2) else 3) + 2)}
+                                          in (1, 2, 4) else 3) + 2)}
     else:  # quota
         w = workload_run(args.workload, args.layers)[0]
         K, V, lens = synthkv.make_kv(w, seed=args.seed, device=dev)
@@ -721,7 +725,7 @@ def run_secondary(args):
                 "clocks": clocks.summary(),
                 # a1 + a2 (one kernel or three), quota select, gather
                 "gpu_launches": steps * ((1 if mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
-                                          in (1, 2) else 3) + 2)}
+                                          in (1, 2, 4) else 3) + 2)}
     line["path"] = args.path
     print(json.dumps(line), flush=True)
 
@@ -780,6 +784,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle time for --impl reference")
     ap.add_argument("--no-head-groups", action="store_true",
                     help="three-kernel centroid + score path instead of head groups (A/B)")
+    ap.add_argument("--ring", type=int, choices=[0, 1], default=None,
+                    help="copy-ring head-group kernel on (1) or off (0); default: the library's setting")
     ap.add_argument("--path", choices=["manifold", "oja", "summaries", "quota", "inplace"], default="manifold",
                     help="manifold: the headline path; the others time a widened path (one GPU, own JSON line)")
     ap.add_argument("--oja-queries", type=int, default=128, help="query-window rows per KV head (--path oja)")

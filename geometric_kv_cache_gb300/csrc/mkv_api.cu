@@ -27,6 +27,20 @@ std::atomic<int> g_single_pass_enabled{0};
 // Whether mkv_compress may use the head-group kernel (one read of K from
 // HBM, global centroids, heads short enough for L2). On by default.
 std::atomic<int> g_head_groups_enabled{1};
+// Whether the head groups may use the copy-ring kernel where it applies
+// (bf16, head dim 128; mkv_set_head_group_ring).
+std::atomic<int> g_head_group_ring{0};
+
+// The head-group plan mkv_compress takes: the copy-ring kernel where it
+// applies and is allowed, else the register kernel (groups 0: neither).
+HeadGroupPlan choose_head_groups(const PieceGeometry &pg, int mode, size_t counters)
+{
+    if (g_head_group_ring.load(std::memory_order_relaxed)) {
+        const HeadGroupPlan r = head_group_ring_plan(pg, mode, counters);
+        if (r.groups > 0) return r;
+    }
+    return head_group_plan(pg, mode, counters);
+}
 // The fused whole-path kernel (mkv_set_fused): the scorer CTA budget (0: off,
 // < 0: automatic) and the selector CTAs of a forced budget.
 std::atomic<int> g_fused_scorers{-1};
@@ -211,7 +225,7 @@ mkv_status run_centroid_score(const Geometry &g, const Layout &L, const void *K,
     bool single = grid > 0 && grid >= g.pg.ppw;
     if (stall_windows && !single) return MKV_ERR_UNSUPPORTED;
     const HeadGroupPlan plan = (!single && g_head_groups_enabled.load(std::memory_order_relaxed))
-                                   ? head_group_plan(g.pg, (int)mode, L.centroid - L.counters)
+                                   ? choose_head_groups(g.pg, (int)mode, L.centroid - L.counters)
                                    : HeadGroupPlan{};
     if (plan.groups > 0) {
         e = launch_head_groups(g.pg, plan, K, s.seq_lens, (int)mode, partial, region<uint32_t>(ws, L.counters), C, S,
@@ -691,7 +705,8 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
         const FusedBudget fb = fused_budget(g);
         if (fb.scorers != 0 && fused_plan(g.pg, (int)mode, L.centroid - L.counters, fb.scorers, fb.selectors).grid > 0)
             return 3;
-        if (head_group_plan(g.pg, (int)mode, L.centroid - L.counters).groups > 0) return 2;
+        const HeadGroupPlan hp = choose_head_groups(g.pg, (int)mode, L.centroid - L.counters);
+        if (hp.groups > 0) return hp.ring ? 4 : 2;
     }
     return 0;
 }
@@ -699,6 +714,11 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
 int32_t mkv_set_head_groups(int32_t enable)
 {
     return g_head_groups_enabled.exchange(enable ? 1 : 0);
+}
+
+int32_t mkv_set_head_group_ring(int32_t enable)
+{
+    return g_head_group_ring.exchange(enable ? 1 : 0);
 }
 
 int32_t mkv_set_fused(int32_t scorer_ctas, int32_t select_ctas)

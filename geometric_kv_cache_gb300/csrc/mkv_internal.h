@@ -90,8 +90,12 @@ struct HeadGroupPlan {
     int gsize = 0;  // CTAs per group
     int wb = 0;     // windows per unit
     uint32_t stagger_ns = 0;  // start delay step: group g waits (g mod 4) steps
+    bool ring = false;        // the copy-ring kernel (pass 1 streamed by a producer warp)
 };
 HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counter_bytes);
+// The plan of the copy-ring head-group kernel (bf16, head dim 128); groups 0
+// when it does not apply.
+HeadGroupPlan head_group_ring_plan(const PieceGeometry &g, int mode, size_t counter_bytes);
 // The fused whole-path kernel (global centroids, heads of at most 20480
 // tokens): scorer head groups within `scorer_ctas` CTAs (< 0: 3/4 of the
 // resident grid), `select_ctas`

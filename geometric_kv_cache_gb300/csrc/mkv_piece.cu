@@ -1122,6 +1122,271 @@ k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, ui
     head_groups_run<MODE, NB, ES>(g, P, gcnt, gsize, wb, stagger_ns, groups, group, rank, nullptr);
 }
 
+// ------------------------------------------- head groups with a copy ring --
+//
+// k_head_groups_ring: the head-group kernel (same units, groups, barrier,
+// means and pass 2, hence the same bits), with pass 1 fed by a producer warp
+// instead of the consumer warps' own loads. The producer streams the CTA's
+// pass-1 rows, piece by piece and unit after unit, into a ring of
+// kRingStages stages of kRingStageBytes with bulk asynchronous copies
+// (cp.async.bulk, an L2 evict-last hint so the rows stay for pass 2; a
+// "full" mbarrier per stage completes when its bytes land, an "empty" one
+// when all 8 consumer warps have added its rows up). It does not wait for
+// the group barrier, so while the consumers sit at the barrier, form the
+// means and re-read the unit from L2 in pass 2, the ring already fills with
+// the next unit's rows: HBM reads stay in flight through the whole round.
+// Consumers read their rows from shared memory with the row-slot mapping of
+// the register kernel (lane q of slot s adds rows s, s + 32, ... in order),
+// so every sum has the same order.
+constexpr int kRingStages = 3;
+constexpr uint32_t kRingStageBytes = 32 * 1024;
+constexpr int kRingWarps = kWarps + 1;                   // 8 consumer warps + the producer warp
+constexpr int kRingThreads = kRingWarps * 32;
+constexpr size_t kRingStash = 16 * 1024;                 // per-warp piece sums; then the unit's means
+constexpr size_t kRingSmem = kRingStages * kRingStageBytes + kRingStash + 2 * kRingStages * sizeof(uint64_t);
+// windows a unit may hold: their means must fit the stash buffer
+__host__ __device__ constexpr int ring_unit_windows(int D) { return (int)(kRingStash / (sizeof(float) * D)); }
+
+// One thread: expect `bytes` on `bar` and start the copy global -> shared
+// with an L2 cache policy.
+__device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
+// The 256 consumer threads only (the producer warp never joins).
+__device__ __forceinline__ void consumer_barrier()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
+
+template <int MODE, int NB>
+__global__ void __maxnreg__(112)
+k_head_groups_ring(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, uint32_t stagger_ns)
+{
+    constexpr int D = 64 * NB, RB = 2 * D;  // bf16 rows
+    constexpr int SR = (int)(kRingStageBytes / RB);        // rows per stage
+    constexpr int kSlots = (int)(kRingStash / (sizeof(float) * kWarps * D));
+    constexpr int kBatchG = 16 / NB;                      // pass-2 rows per lane in flight
+    static_assert(SR % kRowSlots == 0, "a stage must hold whole rounds of row slots");
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *ring = smem;
+    float *stash = reinterpret_cast<float *>(smem + kRingStages * kRingStageBytes);
+    float *cmean = stash;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRingStages * kRingStageBytes + kRingStash);
+    uint64_t *empty = full + kRingStages;
+    __shared__ uint32_t s_ok;
+    __shared__ int64_t s_off[kSlots];
+    const int groups = gridDim.x / gsize;
+    const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
+    if (group >= groups) return;  // a launch is always a whole number of groups
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRingStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (stagger_ns) {  // as in the register kernel: groups start (group mod 4) steps apart
+        const uint64_t t0 = global_ns(), wait = (uint64_t)(group & 3) * stagger_ns;
+        while (global_ns() - t0 < wait) {
+        }
+    }
+    const int upw = (g.nwin_max + wb - 1) / wb;  // units (blocks of wb windows) per head
+    const int64_t n_units = g.n_heads * upw;
+
+    if (warp == kWarps) {
+        // ---- producer: every pass-1 stage of the CTA's pieces, unit after unit
+        if (lane == 0) {
+            uint64_t keep_l2;
+            asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep_l2));
+            uint32_t seq = 0;
+            for (int64_t unit = group; unit < n_units; unit += groups) {
+                const int64_t head = unit / upw;
+                const int w0 = (int)(unit - head * upw) * wb;
+                const int T = head_len(P.seq_lens, head, g.heads, g.t_max, P.status, false);
+                const int wl = window_len(T, g.window);
+                const int nw = T > 0 ? (T + wl - 1) / wl : 0;
+                const int nf = max(0, min(w0 + wb, nw) - w0) * g.ppw;
+                for (int f = rank; f < nf; f += gsize) {
+                    const int w = w0 + f / g.ppw, p = f - (f / g.ppw) * g.ppw;
+                    const int wstart = w * wl, wlen = min(wl, T - wstart), off = p * g.piece_rows;
+                    if (off >= wlen) continue;
+                    const int len = min(g.piece_rows, wlen - off);
+                    const uint8_t *base = P.K + ((size_t)head * g.t_max + wstart + off) * RB;
+                    for (int r0 = 0; r0 < len; r0 += SR, ++seq) {
+                        const int st = (int)(seq % kRingStages);
+                        if (seq >= (uint32_t)kRingStages)
+                            mbar_wait(&empty[st], ((seq / kRingStages) - 1) & 1u, P.status, false);
+                        bulk_load_hint(ring + (size_t)st * kRingStageBytes, base + (size_t)r0 * RB,
+                                       (uint32_t)min(SR, len - r0) * RB, &full[st], keep_l2);
+                    }
+                }
+            }
+            // stay until the copies still in flight have landed (they normally
+            // have: the consumers wait for every stage)
+            for (uint32_t k = seq > (uint32_t)kRingStages ? seq - kRingStages : 0; k < seq; ++k)
+                mbar_wait(&full[k % kRingStages], (k / kRingStages) & 1u, P.status, false);
+        }
+        return;
+    }
+
+    // ---- consumers: threads 0..255
+    const int slot = threadIdx.x >> 3, q = threadIdx.x & 7;
+    auto flush = [&](int ns) {  // the stash's piece sums: warps in order, then free
+        consumer_barrier();
+        for (int e = threadIdx.x; e < ns * D; e += kThreads) {
+            const int j = e / D, d = e - j * D;
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) sum += stash[(j * kWarps + w) * D + d];
+            P.partial[s_off[j] + d] = sum;
+        }
+        __threadfence();  // the piece sums are visible GPU-wide before the arrival
+        consumer_barrier();
+    };
+    uint64_t drop_l2;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(drop_l2));
+    uint32_t round = 0, seq = 0;
+    for (int64_t unit = group; unit < n_units; unit += groups, ++round) {
+        if (unit + groups >= n_units) pdl_trigger();
+        const int64_t head = unit / upw;
+        const int w0 = (int)(unit - head * upw) * wb;
+        const int T = head_len(P.seq_lens, head, g.heads, g.t_max, P.status, threadIdx.x == 0 && rank == 0 && w0 == 0);
+        const int wl = window_len(T, g.window);
+        const int nw = T > 0 ? (T + wl - 1) / wl : 0;
+        const int nwu = max(0, min(w0 + wb, nw) - w0);
+        const int nf = nwu * g.ppw;
+        // pass 1: piece sums from the ring
+        int ns = 0;
+        for (int f = rank; f < nf; f += gsize) {
+            const int w = w0 + f / g.ppw, p = f - (f / g.ppw) * g.ppw;
+            const int wstart = w * wl, wlen = min(wl, T - wstart), off = p * g.piece_rows;
+            if (off >= wlen) continue;
+            const int len = min(g.piece_rows, wlen - off);
+            float acc[8 * NB];
+#pragma unroll
+            for (int j = 0; j < 8 * NB; ++j) acc[j] = 0.f;
+            for (int r0 = 0; r0 < len; r0 += SR, ++seq) {
+                const int st = (int)(seq % kRingStages);
+                mbar_wait(&full[st], (seq / kRingStages) & 1u, P.status, false);
+                const int rows = min(SR, len - r0);
+                const uint8_t *stage = ring + (size_t)st * kRingStageBytes;
+#pragma unroll
+                for (int i = 0; i < SR / kRowSlots; ++i) {
+                    const int r = slot + i * kRowSlots;
+                    if (r < rows) {
+                        uint4 v[NB];
+#pragma unroll
+                        for (int k = 0; k < NB; ++k)
+                            v[k] = *reinterpret_cast<const uint4 *>(stage + (size_t)r * RB + 128 * k + 16 * q);
+                        row_accumulate<NB, 2>(v, acc);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8 * NB; ++j) {
+                acc[j] += __shfl_xor_sync(kFull, acc[j], 8);
+                acc[j] += __shfl_xor_sync(kFull, acc[j], 16);
+            }
+            if (lane < 8) {
+#pragma unroll
+                for (int k = 0; k < NB; ++k)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) stash[(ns * kWarps + warp) * D + 64 * k + q * 8 + j] = acc[8 * k + j];
+            }
+            if (threadIdx.x == 0) s_off[ns] = ((head * g.nwin_max + w) * (int64_t)g.ppw + p) * D;
+            if (++ns == kSlots) {
+                flush(ns);
+                ns = 0;
+            }
+        }
+        if (ns > 0) flush(ns);
+        // the group's barrier for this unit
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(&gcnt[group], 1u);
+            const uint32_t target = (round + 1) * (uint32_t)gsize;
+            const uint64_t t0 = global_ns();
+            uint32_t ok = 1;
+            for (uint32_t spin = 0; ld_acquire(&gcnt[group]) < target; ++spin) {
+                if ((spin & 63u) == 63u && global_ns() - t0 > kWaitNs) {
+                    atomicOr(P.status, MKV_DEV_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+            }
+            s_ok = ok;
+        }
+        consumer_barrier();
+        if (s_ok && nwu > 0) {  // the same for every consumer thread
+            // window means in k_window_means' order (the register kernel's code)
+            for (int j = threadIdx.x / D; j < nwu; j += kThreads / D) {
+                const int d = threadIdx.x % D;
+                const int w = w0 + j;
+                const int wlen = min(wl, T - w * wl);
+                const int np = (wlen + g.piece_rows - 1) / g.piece_rows;
+                const int ng = (np + kGroupPieces - 1) / kGroupPieces;
+                const float *pw = P.partial + (head * g.nwin_max + w) * (int64_t)g.ppw * D + d;
+                float tot = 0.f;
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int n = min(kGroupPieces, np - gi * kGroupPieces);
+                    float v[kGroupPieces];
+#pragma unroll
+                    for (int k = 0; k < kGroupPieces; ++k)
+                        v[k] = k < n ? __ldcg(pw + (int64_t)(gi * kGroupPieces + k) * D) : 0.f;
+                    float gs = 0.f;
+#pragma unroll
+                    for (int k = 0; k < kGroupPieces; ++k)
+                        if (k < n) gs += v[k];
+                    tot += gs;
+                }
+                const float m = __fdiv_rn(tot, (float)wlen);
+                cmean[j * D + d] = m;
+                if (rank == 0) P.C[(head * g.nwin_max + w) * D + d] = m;
+            }
+            consumer_barrier();
+            // pass 2: scores of the same pieces (their rows are L2 hits)
+            for (int f = rank; f < nf; f += gsize) {
+                const int jw = f / g.ppw, w = w0 + jw, p = f - jw * g.ppw;
+                const int wstart = w * wl, wlen = min(wl, T - wstart), off = p * g.piece_rows;
+                if (off >= wlen) continue;
+                const int len = min(g.piece_rows, wlen - off);
+                float c[8 * NB];
+#pragma unroll
+                for (int k = 0; k < NB; ++k)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) c[8 * k + j] = cmean[jw * D + 64 * k + q * 8 + j];
+                const float nc = MODE == MKV_MODE_COSINE ? centroid_norm<NB>(c) : 0.f;
+                const uint8_t *base = P.K + ((size_t)head * g.t_max + wstart + off) * RB;
+                float *srow = P.S + (size_t)head * g.t_max + wstart + off;
+                const int nrows = (len + kRowSlots - 1) / kRowSlots;
+                for (int i0 = 0; i0 < nrows; i0 += kBatchG) {
+                    uint4 v[NB * kBatchG];
+                    load_rows_policy<kBatchG, NB, 2>(base, len, i0, v, drop_l2);
+#pragma unroll
+                    for (int u = 0; u < kBatchG; ++u) {
+                        const int r = slot + (i0 + u) * kRowSlots;
+                        const float sc = score_row<MODE, NB, 2>(v + NB * u, c, nc);
+                        if (r < len && q == 0) srow[r] = sc;
+                    }
+                }
+            }
+        }
+        consumer_barrier();  // the means are rewritten for the next unit
+    }
+}
+
 // The whole path in one cooperative launch (global centroids, heads of at
 // most kFusedMaxT tokens), in three roles:
 //  * scorers, CTAs [0, groups * gsize): the heads' centroids and scores as
@@ -1437,7 +1702,8 @@ namespace {
 // Group count, group size and unit size for `resident` CTAs; `alone` applies
 // the comparison with the three-kernel path (the head-group kernel on its
 // own), which the fused kernel does not take.
-HeadGroupPlan plan_groups(const PieceGeometry &g, int resident, size_t counters, bool alone)
+HeadGroupPlan plan_groups(const PieceGeometry &g, int resident, size_t counters, bool alone,
+                          int max_unit_windows = kMaxUnitWindows)
 {
     HeadGroupPlan plan;
     int dev = 0, l2 = 0;
@@ -1455,7 +1721,7 @@ HeadGroupPlan plan_groups(const PieceGeometry &g, int resident, size_t counters,
     const double window_bytes = (double)wl_max * g.es * g.d;
     const double budget = 0.6 * (double)l2;
     double best = 0.0;
-    for (int wb = 1; wb <= std::min(g.nwin_max, kMaxUnitWindows); ++wb) {
+    for (int wb = 1; wb <= std::min(g.nwin_max, max_unit_windows); ++wb) {
         const int64_t fit = (int64_t)(budget / (window_bytes * wb));
         const int64_t units = g.n_heads * ((g.nwin_max + wb - 1) / wb);
         for (int gsize = 8; gsize <= 64; ++gsize) {
@@ -1500,6 +1766,27 @@ HeadGroupPlan plan_groups(const PieceGeometry &g, int resident, size_t counters,
 }
 
 }  // namespace
+
+// The copy-ring head-group kernel of a mode (bf16 caches at head dim 128
+// only: other shapes run the register kernel); nullptr where it has none.
+const void *head_groups_ring_fn(int d, int es, int mode)
+{
+    if (d != 128 || es != 2) return nullptr;
+    return mode == MKV_MODE_L2 ? (const void *)k_head_groups_ring<MKV_MODE_L2, 2>
+                               : (const void *)k_head_groups_ring<MKV_MODE_COSINE, 2>;
+}
+
+HeadGroupPlan head_group_ring_plan(const PieceGeometry &g, int mode, size_t counters)
+{
+    if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max == 0) return HeadGroupPlan{};
+    const void *fn = head_groups_ring_fn(g.d, g.es, mode);
+    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem) != cudaSuccess)
+        return HeadGroupPlan{};
+    HeadGroupPlan plan = plan_groups(g, resident_grid(fn, kRingThreads, kRingSmem), counters, true,
+                                     ring_unit_windows(g.d));
+    plan.ring = plan.groups > 0;
+    return plan;
+}
 
 HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
 {
@@ -1573,7 +1860,7 @@ cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan
                                const int32_t *seq_lens, int mode, float *partial, uint32_t *cnt, float *C, float *S,
                                uint32_t *status, cudaStream_t st)
 {
-    const void *fn = head_groups_fn(g.d, g.es, mode);
+    const void *fn = plan.ring ? head_groups_ring_fn(g.d, g.es, mode) : head_groups_fn(g.d, g.es, mode);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(cnt, 0, (size_t)plan.groups * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
@@ -1582,8 +1869,9 @@ cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan
     int gsize = plan.gsize, wb = plan.wb;
     uint32_t stagger = plan.stagger_ns;
     void *args[] = {&gg, &P, &cnt, &gsize, &wb, &stagger};
-    return cudaLaunchCooperativeKernel(fn, dim3((unsigned)(plan.groups * plan.gsize)), dim3(kThreads), args,
-                                       kGroupSmem, st);
+    return cudaLaunchCooperativeKernel(fn, dim3((unsigned)(plan.groups * plan.gsize)),
+                                       dim3(plan.ring ? kRingThreads : kThreads), args,
+                                       plan.ring ? kRingSmem : kGroupSmem, st);
 }
 
 cudaError_t launch_piece_sums(const PieceGeometry &g, const void *K, const int32_t *seq_lens, float *partial,

@@ -300,7 +300,8 @@ int32_t mkv_compress_num_stages(void);
 
 /* Which a1 + a2 path mkv_compress takes on the current device for this
  * shape, window and mode: 1 the single-pass kernel (opt-in, K read once),
- * 2 the head-group kernel (the default when a unit of windows fits in L2
+ * 4 the head-group kernel with its pass 1 fed through a copy ring (see
+ * mkv_set_head_group_ring), 2 the head-group kernel (the default when a unit of windows fits in L2
  * and, with several rounds per group, the cache is bf16 and, for head dims up
  * to 128, its modelled cost is below the three kernels': K read from HBM
  * once, the second read hits L2), 3 the fused whole-path kernel (every step
@@ -315,6 +316,16 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
  * bounded arrival barrier, form the mean and score the pieces again while
  * their rows are still in L2 -- one HBM read of K instead of two. */
 int32_t mkv_set_head_groups(int32_t enable);
+
+/* Allow (1) or forbid (0) the copy-ring form of the head-group kernel,
+ * process-wide; returns the previous setting. It applies to bf16 caches at
+ * head dim 128 wherever head groups run (on their own, not inside the fused
+ * kernel): the same units, group barrier, means and L2 pass, but pass 1 is
+ * streamed into shared memory by a producer warp with bulk asynchronous
+ * copies, a ring of three 32 KB stages per CTA, which keeps running into the
+ * next unit while the other warps wait at the group barrier and re-read the
+ * unit from L2. The results are the same bits. */
+int32_t mkv_set_head_group_ring(int32_t enable);
 
 /* Choose, process-wide, when mkv_compress runs the fused whole-path kernel;
  * returns the previous scorer setting. scorer_ctas < 0 (the default): on its
