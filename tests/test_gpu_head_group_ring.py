@@ -25,7 +25,9 @@ def _cuda():
         pytest.skip("no CUDA device")
     mkv.load()
     prev = mkv.mkv_set_head_group_ring(False)
+    prev_fused = mkv.mkv_set_fused(0)  # the path query then names the a1 + a2 kernel mkv_centroid_score runs
     yield
+    mkv.mkv_set_fused(prev_fused)
     mkv.mkv_set_head_group_ring(prev)
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
