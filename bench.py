@@ -358,6 +358,7 @@ def run_ours(args):
     if args.fused is not None:
         mkv.mkv_set_fused(args.fused, args.fused_selectors)
     single = mkv.mkv_compress_single_pass(mkv.shape_of(K, lens), window, mode)
+    hg_plan = mkv.mkv_head_group_plan(mkv.shape_of(K, lens), window, mode)
     if args.fused is not None and args.fused > 0 and single != 3:
         raise SystemExit("--fused: the fused kernel does not apply to this workload (global centroids, t <= 20480)")
     select_emits = T <= 40960  # select writes the kept indices itself (no compaction kernel)
@@ -477,6 +478,7 @@ def run_ours(args):
                                               + ("the library's own rule" if args.fused is None else
                                                  f"scorer budget {args.fused}, {args.fused_selectors} selector CTAs")
                                               + ")"}.get(single, "?"),
+                   "head_group_plan": hg_plan,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "no flush: K+V (%.1f GB) exceed the 129 MB L2" % (2 * K.numel() * es / 1e9)},
         "hbm": {"path_bytes_per_step": nbytes["path"], "achieved_gbs": hbm_gbs,

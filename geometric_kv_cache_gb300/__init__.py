@@ -49,7 +49,7 @@ EXPORTED = (
     "mkv_inject_stalled_windows", "mkv_window_means", "mkv_num_keep_quota", "mkv_select_quota",
     "mkv_compress_quota", "mkv_oja_workspace_size", "mkv_oja_score", "mkv_compress_oja", "mkv_oja_score_profiled",
     "mkv_compress_inplace", "mkv_set_head_groups", "mkv_set_fused", "mkv_centroid_score",
-    "mkv_inject_stalled_fused", "mkv_set_head_group_ring",
+    "mkv_inject_stalled_fused", "mkv_set_head_group_ring", "mkv_head_group_plan",
 )
 
 
@@ -103,6 +103,7 @@ def load(build_if_missing: bool = True):
             "mkv_set_single_pass": (i32, [i32]),
             "mkv_set_head_groups": (i32, [i32]),
             "mkv_set_head_group_ring": (i32, [i32]),
+            "mkv_head_group_plan": (i32, [MkvShape, i32, i32, ctypes.POINTER(i32)]),
             "mkv_set_fused": (i32, [i32, i32]),
             "mkv_centroid_score": (i32, [vp, MkvShape, i32, i32, vp, vp, vp, sz, vp]),
             "mkv_layer_budgets": (i32, [vp, i32, f64, f64, ctypes.c_int64, vp, vp]),
@@ -216,6 +217,15 @@ def mkv_set_head_group_ring(enable: bool) -> bool:
     """Allow or forbid the copy-ring form of the head-group kernel (bf16,
     head dim 128); returns the previous setting."""
     return bool(load().mkv_set_head_group_ring(1 if enable else 0))
+
+
+def mkv_head_group_plan(shape, window: int, mode) -> Optional[dict]:
+    """The head-group plan on the current device (groups, CTAs per group,
+    windows per unit, copy ring), or None when head groups do not apply."""
+    out = (ctypes.c_int32 * 4)()
+    if load().mkv_head_group_plan(shape, int(window), _MODES[mode], out) != 0:
+        return None
+    return {"groups": out[0], "gsize": out[1], "windows_per_unit": out[2], "ring": bool(out[3])}
 
 
 def mkv_set_fused(scorer_ctas: int, select_ctas: int = 0) -> int:

@@ -711,6 +711,20 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
     return 0;
 }
 
+int32_t mkv_head_group_plan(mkv_shape shape, int32_t window, mkv_mode mode, int32_t *plan)
+{
+    if (!plan || check_shape(shape) != MKV_OK || window < 0 || (mode != MKV_MODE_L2 && mode != MKV_MODE_COSINE))
+        return -1;
+    const Geometry g = geometry_of(shape, window);
+    const Layout L = make_layout(g);
+    const HeadGroupPlan hp = choose_head_groups(g.pg, (int)mode, L.centroid - L.counters);
+    plan[0] = hp.groups;
+    plan[1] = hp.gsize;
+    plan[2] = hp.wb;
+    plan[3] = hp.ring ? 1 : 0;
+    return hp.groups > 0 ? 0 : -1;
+}
+
 int32_t mkv_set_head_groups(int32_t enable)
 {
     return g_head_groups_enabled.exchange(enable ? 1 : 0);

@@ -1780,7 +1780,10 @@ HeadGroupPlan head_group_ring_plan(const PieceGeometry &g, int mode, size_t coun
 {
     if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max == 0) return HeadGroupPlan{};
     const void *fn = head_groups_ring_fn(g.d, g.es, mode);
-    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem) != cudaSuccess)
+    // two CTAs of ~113 KB share an SM only with the whole carveout as shared memory
+    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+            cudaSuccess)
         return HeadGroupPlan{};
     HeadGroupPlan plan = plan_groups(g, resident_grid(fn, kRingThreads, kRingSmem), counters, true,
                                      ring_unit_windows(g.d));

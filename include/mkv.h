@@ -317,6 +317,13 @@ int32_t mkv_compress_single_pass(mkv_shape shape, int32_t window, mkv_mode mode)
  * their rows are still in L2 -- one HBM read of K instead of two. */
 int32_t mkv_set_head_groups(int32_t enable);
 
+/* The head-group plan mkv_centroid_score and mkv_compress's separate
+ * kernels would take on the current device (a diagnostic): plan[0] groups,
+ * plan[1] CTAs per group, plan[2] windows per unit, plan[3] 1 for the
+ * copy-ring kernel. Returns 0, or -1 (plan zeroed) when head groups do not
+ * apply or on a bad argument (plan untouched when it is NULL). */
+int32_t mkv_head_group_plan(mkv_shape shape, int32_t window, mkv_mode mode, int32_t *plan);
+
 /* Allow (1) or forbid (0) the copy-ring form of the head-group kernel,
  * process-wide; returns the previous setting. It applies to bf16 caches at
  * head dim 128 wherever head groups run (on their own, not inside the fused
