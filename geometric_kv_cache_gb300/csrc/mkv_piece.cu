@@ -906,6 +906,21 @@ __device__ __forceinline__ void load_rows_policy(const uint8_t *base, int len, i
 // sums, then (same bytes) the unit's means; padded so that at most two CTAs
 // share an SM (the grid is then spread over all SMs). A unit holds at most
 // kMaxUnitWindows windows.
+// Pieces of its own sequence a head-group CTA prefetches into L2 ahead of
+// its pass-1 loads (bulk L2 prefetches issued by one thread; the sequence runs
+// on into the CTA's next unit, so the prefetches keep HBM busy while the CTA
+// waits at the group barrier, forms the means and re-reads the unit from L2).
+#ifndef MKV_HG_PREFETCH
+#define MKV_HG_PREFETCH 0
+#endif
+constexpr int kHgPrefetch = MKV_HG_PREFETCH;
+// Share of L2 (percent) the head groups' units in flight may take.
+#ifndef MKV_HG_L2_BUDGET_PCT
+#define MKV_HG_L2_BUDGET_PCT 60
+#endif
+#ifndef MKV_RING_L2_BUDGET_PCT
+#define MKV_RING_L2_BUDGET_PCT 60
+#endif
 constexpr size_t kGroupSmem = 80 * 1024;
 constexpr int kMaxUnitWindows = 64;
 constexpr int kMaxDim = 256;
@@ -913,6 +928,59 @@ static_assert(kMaxUnitWindows * kMaxDim * sizeof(float) <= kGroupSmem, "means mu
 // pieces the stash holds for head dim D
 __host__ __device__ constexpr int stash_slots(int D) { return (int)(kGroupSmem / sizeof(float)) / (kWarps * D); }
 constexpr int kMaxSlots = stash_slots(64);
+
+// L2 prefetch of `bytes` (a multiple of 16) at `p` (16-byte aligned) with a
+// cache policy; asynchronous, completes on its own.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(pol)
+                 : "memory");
+}
+
+// The piece slots f = rank, rank + gsize, ... of a unit that a CTA of rank
+// `rank` takes, and their count (slots past the unit's windows excluded).
+struct UnitPieces {
+    int64_t head;
+    int T, wl, w0, nf;
+};
+__device__ __forceinline__ UnitPieces unit_pieces(const PieceGeometry &g, const Pointers &P, int64_t unit, int wb)
+{
+    const int upw = (g.nwin_max + wb - 1) / wb;
+    UnitPieces u;
+    u.head = unit / upw;
+    u.w0 = (int)(unit - u.head * upw) * wb;
+    u.T = head_len(P.seq_lens, u.head, g.heads, g.t_max, P.status, false);
+    u.wl = window_len(u.T, g.window);
+    const int nw = u.T > 0 ? (u.T + u.wl - 1) / u.wl : 0;
+    u.nf = max(0, min(u.w0 + wb, nw) - u.w0) * g.ppw;
+    return u;
+}
+
+// Prefetch the piece `ahead` places after slot number i (0-based, the CTA's
+// i-th slot of `unit`) in the CTA's sequence of slots, which runs on into
+// its later units; nothing when the sequence ends first or the slot lies
+// past its window's last piece.
+template <int RB>
+__device__ __forceinline__ void prefetch_ahead(const PieceGeometry &g, const Pointers &P, int64_t unit, int i,
+                                               int ahead, int rank, int gsize, int groups, int wb, int64_t n_units,
+                                               uint64_t pol)
+{
+    int j = i + ahead;
+    for (int64_t u = unit; u < n_units; u += groups) {
+        const UnitPieces up = unit_pieces(g, P, u, wb);
+        const int n = up.nf > rank ? (up.nf - rank - 1) / gsize + 1 : 0;
+        if (j < n) {
+            const int f = rank + j * gsize;
+            const int w = up.w0 + f / g.ppw, p = f - (f / g.ppw) * g.ppw;
+            const int wstart = w * up.wl, wlen = min(up.wl, up.T - wstart), off = p * g.piece_rows;
+            if (off < wlen)
+                prefetch_l2(P.K + ((size_t)up.head * g.t_max + wstart + off) * RB,
+                            (uint32_t)min(g.piece_rows, wlen - off) * RB, pol);
+            return;
+        }
+        j -= n;
+    }
+}
 
 //
 // head_groups_run is one CTA's share (group `group` of `groups`, rank `rank`
@@ -985,7 +1053,12 @@ __device__ __forceinline__ void head_groups_run(const PieceGeometry &g, const Po
         // and stashes the result; the CTA adds the warps once per kSlots
         // pieces, so warps only meet at a CTA barrier there.
         int ns = 0;
-        for (int f = rank; f < nf; f += gsize) {
+        if (kHgPrefetch > 0 && threadIdx.x == 0 && round == 0)  // the CTA's first slots
+            for (int a = 0; a < kHgPrefetch; ++a)
+                prefetch_ahead<RB>(g, P, unit, 0, a, rank, gsize, groups, wb, n_units, keep_l2);
+        for (int f = rank, i = 0; f < nf; f += gsize, ++i) {
+            if (kHgPrefetch > 0 && threadIdx.x == 0)
+                prefetch_ahead<RB>(g, P, unit, i, kHgPrefetch, rank, gsize, groups, wb, n_units, keep_l2);
             const int w = w0 + f / g.ppw, p = f - (f / g.ppw) * g.ppw;
             const int wstart = w * wl, wlen = min(wl, T - wstart), off = p * g.piece_rows;
             if (off >= wlen) continue;  // past the window's last piece (the same for every thread)
@@ -1166,14 +1239,16 @@ __device__ __forceinline__ void consumer_barrier()
     asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
 }
 
+// Two CTAs per SM: 18 warps spread over the four SM sub-partitions put five
+// warps of 9 on some, so a thread may hold at most 96 registers.
 template <int MODE, int NB>
-__global__ void __maxnreg__(112)
+__global__ void __launch_bounds__(kRingThreads, 2)
 k_head_groups_ring(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, uint32_t stagger_ns)
 {
     constexpr int D = 64 * NB, RB = 2 * D;  // bf16 rows
     constexpr int SR = (int)(kRingStageBytes / RB);        // rows per stage
     constexpr int kSlots = (int)(kRingStash / (sizeof(float) * kWarps * D));
-    constexpr int kBatchG = 16 / NB;                      // pass-2 rows per lane in flight
+    constexpr int kBatchG = 8 / NB;                       // pass-2 rows per lane in flight (96 registers)
     static_assert(SR % kRowSlots == 0, "a stage must hold whole rounds of row slots");
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
@@ -1703,7 +1778,7 @@ namespace {
 // the comparison with the three-kernel path (the head-group kernel on its
 // own), which the fused kernel does not take.
 HeadGroupPlan plan_groups(const PieceGeometry &g, int resident, size_t counters, bool alone,
-                          int max_unit_windows = kMaxUnitWindows)
+                          int max_unit_windows = kMaxUnitWindows, bool ring = false)
 {
     HeadGroupPlan plan;
     int dev = 0, l2 = 0;
@@ -1719,7 +1794,7 @@ HeadGroupPlan plan_groups(const PieceGeometry &g, int resident, size_t counters,
     const int wl_max = (g.window <= 0 || g.window >= g.t_max) ? g.t_max : g.window;
     if (wl_max < kMinPieceRows) return plan;  // windows shorter than a piece: barrier-bound rounds
     const double window_bytes = (double)wl_max * g.es * g.d;
-    const double budget = 0.6 * (double)l2;
+    const double budget = 0.01 * (ring ? MKV_RING_L2_BUDGET_PCT : MKV_HG_L2_BUDGET_PCT) * (double)l2;
     double best = 0.0;
     for (int wb = 1; wb <= std::min(g.nwin_max, max_unit_windows); ++wb) {
         const int64_t fit = (int64_t)(budget / (window_bytes * wb));
@@ -1786,7 +1861,7 @@ HeadGroupPlan head_group_ring_plan(const PieceGeometry &g, int mode, size_t coun
             cudaSuccess)
         return HeadGroupPlan{};
     HeadGroupPlan plan = plan_groups(g, resident_grid(fn, kRingThreads, kRingSmem), counters, true,
-                                     ring_unit_windows(g.d));
+                                     ring_unit_windows(g.d), true);
     plan.ring = plan.groups > 0;
     return plan;
 }
