@@ -40,6 +40,11 @@ def test_committed_record_matches_the_gather_sources():
     rec = os.path.join(ROOT, "profiles", "traffic.json")
     got = bench.load_traffic(rec, "llama3.1-8b-kv-t16k", 0, "bf16", ("l2", 0, 0.5))
     assert got is not None and got.get("gather", 0) > 0
+    # the default bench line (the Phi-4 workload's windowed run) has a record too
+    import synthkv
+    w, mode, window, ratio = bench.workload_run(synthkv.BENCH_WORKLOAD)
+    got = bench.load_traffic(rec, synthkv.BENCH_WORKLOAD, 0, "bf16", (mode, window, ratio))
+    assert got is not None and got.get("gather", 0) > 0
 
 
 def test_every_configured_run_resolves():
