@@ -922,9 +922,16 @@ constexpr int kHgPrefetch = MKV_HG_PREFETCH;
 #define MKV_RING_L2_BUDGET_PCT 60
 #endif
 constexpr size_t kGroupSmem = 80 * 1024;
+// CTAs per SM of the stand-alone head-group kernel: 2 (kGroupSmem of shared
+// memory, 16 / NB rows per lane in flight) or 3 (kGroupSmem3, 8 / NB rows).
+#ifndef MKV_HG_CTAS
+#define MKV_HG_CTAS 2
+#endif
+constexpr size_t kGroupSmem3 = 64 * 1024;
+constexpr size_t kHgSmem = MKV_HG_CTAS >= 3 ? kGroupSmem3 : kGroupSmem;
 constexpr int kMaxUnitWindows = 64;
 constexpr int kMaxDim = 256;
-static_assert(kMaxUnitWindows * kMaxDim * sizeof(float) <= kGroupSmem, "means must fit");
+static_assert(kMaxUnitWindows * kMaxDim * sizeof(float) <= kGroupSmem3, "means must fit");
 // pieces the stash holds for head dim D
 __host__ __device__ constexpr int stash_slots(int D) { return (int)(kGroupSmem / sizeof(float)) / (kWarps * D); }
 constexpr int kMaxSlots = stash_slots(64);
@@ -994,7 +1001,7 @@ __device__ __forceinline__ void prefetch_ahead(const PieceGeometry &g, const Poi
 // reaches gsize, so nothing downstream reads its scores. `barrier_extra`
 // raises this group's barrier target above its CTA count (failure
 // injection: 0 in every ordinary launch).
-template <int MODE, int NB, int ES>
+template <int MODE, int NB, int ES, int BATCH = 16 / NB, size_t SMEM = kGroupSmem>
 __device__ __forceinline__ void head_groups_run(const PieceGeometry &g, const Pointers &P, uint32_t *gcnt, int gsize,
                                                 int wb, uint32_t stagger_ns, int groups, int group, int rank,
                                                 uint32_t *head_done, bool abortable = false,
@@ -1002,8 +1009,8 @@ __device__ __forceinline__ void head_groups_run(const PieceGeometry &g, const Po
 {
     constexpr int D = 64 * NB, RB = ES * D;
     using Raw = typename Chunk<ES>::raw;
-    constexpr int kBatchG = 16 / NB;  // rows per lane in flight (256 bytes per lane for every head dim)
-    constexpr int kSlots = stash_slots(D);
+    constexpr int kBatchG = BATCH;  // rows per lane in flight (16 / NB: 256 bytes per lane for every head dim)
+    constexpr int kSlots = (int)(SMEM / sizeof(float)) / (kWarps * D);
     extern __shared__ float dyn[];    // pass 1: stash [kSlots][kWarps][D]; pass 2: means [wb][D]
     float *stash = dyn;
     float *cmean = dyn;
@@ -1186,13 +1193,14 @@ __device__ __forceinline__ void head_groups_run(const PieceGeometry &g, const Po
 }
 
 template <int MODE, int NB, int ES>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, MKV_HG_CTAS)
 k_head_groups(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int wb, uint32_t stagger_ns)
 {
     const int groups = gridDim.x / gsize;
     const int group = blockIdx.x / gsize, rank = blockIdx.x - group * gsize;
     if (group >= groups) return;  // a launch is always a whole number of groups
-    head_groups_run<MODE, NB, ES>(g, P, gcnt, gsize, wb, stagger_ns, groups, group, rank, nullptr);
+    head_groups_run<MODE, NB, ES, (MKV_HG_CTAS >= 3 ? 8 : 16) / NB, kHgSmem>(g, P, gcnt, gsize, wb, stagger_ns, groups,
+                                                                            group, rank, nullptr);
 }
 
 // ------------------------------------------- head groups with a copy ring --
@@ -1527,12 +1535,27 @@ __device__ __forceinline__ uint32_t wait_count(const uint32_t *flag, uint32_t ta
 // (__ldcg), the indices at once with the count (only slots below both
 // keep_stride and idx_stride, so every load stays inside the head's index
 // row) and then masked by it. No barrier: warps run independent items.
+// Whether the fused kernel's gathers load and store with an L2 evict-first
+// policy (their rows are not read again in the launch, while the scorers'
+// units must stay in L2 between their two passes).
+#ifndef MKV_FUSED_GATHER_EVICT_FIRST
+#define MKV_FUSED_GATHER_EVICT_FIRST 0
+#endif
+
+// 16-byte store carrying an L2 cache policy.
+__device__ __forceinline__ void st_policy(void *p, uint4 v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
 template <int LPR, int ROWS>
 __device__ __forceinline__ void gather_warp_item(int64_t head, int item, const int32_t *idx, int idx_stride,
                                                  const int32_t *kept, int t_max, int keep_stride,
                                                  const uint8_t *__restrict__ K, const uint8_t *__restrict__ V,
                                                  uint8_t *__restrict__ K_out, uint8_t *__restrict__ V_out,
-                                                 uint32_t *status)
+                                                 uint32_t *status, uint64_t pol)
 {
     constexpr int RB = LPR * 16, SL = 32 / LPR, R = ROWS / SL;
     static_assert(R * SL == ROWS, "ROWS must be a multiple of the rows a warp step covers");
@@ -1559,16 +1582,26 @@ __device__ __forceinline__ void gather_warp_item(int64_t head, int item, const i
         }
         if (src[u] >= 0) {
             const size_t off = in_head + (size_t)src[u] * RB;
-            kv[u] = ld_stream(K + off);
-            vv[u] = ld_stream(V + off);
+            if (MKV_FUSED_GATHER_EVICT_FIRST) {
+                kv[u] = ld_policy<2>(K + off, pol);
+                vv[u] = ld_policy<2>(V + off, pol);
+            } else {
+                kv[u] = ld_stream(K + off);
+                vv[u] = ld_stream(V + off);
+            }
         }
     }
 #pragma unroll
     for (int u = 0; u < R; ++u) {
         if (src[u] >= 0) {
             const size_t off = out_head + (size_t)(u * SL + hw) * RB;
-            st_v4(K_out + off, kv[u]);
-            st_v4(V_out + off, vv[u]);
+            if (MKV_FUSED_GATHER_EVICT_FIRST) {
+                st_policy(K_out + off, kv[u], pol);
+                st_policy(V_out + off, vv[u], pol);
+            } else {
+                st_v4(K_out + off, kv[u]);
+                st_v4(V_out + off, vv[u]);
+            }
         }
     }
 }
@@ -1616,6 +1649,8 @@ k_fused_path(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int groups,
     }
     // gatherer: every warp on its own
     const int lane = threadIdx.x & 31;
+    uint64_t drop_l2 = 0;
+    if (MKV_FUSED_GATHER_EVICT_FIRST) asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(drop_l2));
     const int64_t n_items = n_heads * A.bph;
     uint32_t next = 0;
     if (lane == 0) next = atomicAdd(A.gather_ticket, 1u);
@@ -1632,7 +1667,7 @@ k_fused_path(PieceGeometry g, Pointers P, uint32_t *gcnt, int gsize, int groups,
         __syncwarp();  // the lanes' reads of the indices come after lane 0's acquire of the flag
         if (go)
             gather_warp_item<LPR, ROWS>(head, item, A.idx, A.idx_stride, A.kept, g.t_max, A.keep_stride, P.K, A.V,
-                                        A.K_out, A.V_out, P.status);
+                                        A.K_out, A.V_out, P.status, drop_l2);
         next = __shfl_sync(kFull, claim, 0);
     }
 }
@@ -1870,9 +1905,9 @@ HeadGroupPlan head_group_plan(const PieceGeometry &g, int mode, size_t counters)
 {
     if (g.n_heads == 0 || g.t_max == 0 || g.nwin_max == 0) return HeadGroupPlan{};
     const void *fn = head_groups_fn(g.d, g.es, mode);
-    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGroupSmem) != cudaSuccess)
+    if (!fn || cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHgSmem) != cudaSuccess)
         return HeadGroupPlan{};
-    return plan_groups(g, resident_grid(fn, kThreads, kGroupSmem), counters, true);
+    return plan_groups(g, resident_grid(fn, kThreads, kHgSmem), counters, true);
 }
 
 FusedPlan fused_plan(const PieceGeometry &g, int mode, size_t counters, int scorer_ctas, int select_ctas)
@@ -1949,7 +1984,7 @@ cudaError_t launch_head_groups(const PieceGeometry &g, const HeadGroupPlan &plan
     void *args[] = {&gg, &P, &cnt, &gsize, &wb, &stagger};
     return cudaLaunchCooperativeKernel(fn, dim3((unsigned)(plan.groups * plan.gsize)),
                                        dim3(plan.ring ? kRingThreads : kThreads), args,
-                                       plan.ring ? kRingSmem : kGroupSmem, st);
+                                       plan.ring ? kRingSmem : kHgSmem, st);
 }
 
 cudaError_t launch_piece_sums(const PieceGeometry &g, const void *K, const int32_t *seq_lens, float *partial,
