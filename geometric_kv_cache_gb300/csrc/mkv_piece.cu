@@ -1539,7 +1539,7 @@ __device__ __forceinline__ uint32_t wait_count(const uint32_t *flag, uint32_t ta
 // policy (their rows are not read again in the launch, while the scorers'
 // units must stay in L2 between their two passes).
 #ifndef MKV_FUSED_GATHER_EVICT_FIRST
-#define MKV_FUSED_GATHER_EVICT_FIRST 0
+#define MKV_FUSED_GATHER_EVICT_FIRST 1
 #endif
 
 // 16-byte store carrying an L2 cache policy.
