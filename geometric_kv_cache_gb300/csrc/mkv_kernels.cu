@@ -115,13 +115,29 @@ k_compact(const float *__restrict__ S, const mkv_cut *__restrict__ cuts, const i
         const float *srow = S + (size_t)head * t_max;
         const int t0 = a + threadIdx.x * 16;
         uint32_t gtm = 0, eqm = 0;
+        auto classify = [&](float v, int j) {
+            const uint32_t u = score_key(v);
+            gtm |= (uint32_t)(u > cut.key) << j;
+            eqm |= (uint32_t)(u == cut.key) << j;
+        };
+        if (t0 + 16 <= T && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
+            // the thread's 16 scores as four 16-byte loads
+            const float4 *s4 = reinterpret_cast<const float4 *>(srow + t0);
+            float4 v[4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int t = t0 + j;
-            if (t < T) {
-                const uint32_t u = score_key(srow[t]);
-                gtm |= (uint32_t)(u > cut.key) << j;
-                eqm |= (uint32_t)(u == cut.key) << j;
+            for (int i = 0; i < 4; ++i) v[i] = s4[i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                classify(v[i].x, 4 * i);
+                classify(v[i].y, 4 * i + 1);
+                classify(v[i].z, 4 * i + 2);
+                classify(v[i].w, 4 * i + 3);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = t0 + j;
+                if (t < T) classify(srow[t], j);
             }
         }
         uint32_t rank = (uint32_t)info.y + block_exclusive_scan<kStreamThreads>(__popc(eqm), s_warp, nullptr);

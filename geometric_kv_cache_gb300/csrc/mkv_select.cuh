@@ -178,9 +178,29 @@ select_item(int64_t item, const float *__restrict__ S, const int32_t *__restrict
         }
         uint32_t prefix = 0, pmask = 0;
         int need = nk;
+        // scores in L2 (not in shared memory) are read as 16-byte vectors
+        // when the head's row allows it, kUnroll of them in flight per thread
+        const bool vec = !IN_SMEM && (reinterpret_cast<uintptr_t>(grow) & 15) == 0;
+        const int n4 = vec ? T / 4 : 0;
+        const float4 *g4 = reinterpret_cast<const float4 *>(grow);
         if (nk > 0) {
-            if (!IN_SMEM)
-                for (int t = threadIdx.x; t < T; t += NT) see(srow[t]);
+            if (!IN_SMEM) {
+                for (int i = threadIdx.x; i < n4; i += NT * kUnroll) {
+                    float4 v[kUnroll];
+#pragma unroll
+                    for (int k = 0; k < kUnroll; ++k)
+                        if (i + k * NT < n4) v[k] = g4[i + k * NT];
+#pragma unroll
+                    for (int k = 0; k < kUnroll; ++k)
+                        if (i + k * NT < n4) {
+                            see(v[k].x);
+                            see(v[k].y);
+                            see(v[k].z);
+                            see(v[k].w);
+                        }
+                }
+                for (int t = 4 * n4 + threadIdx.x; t < T; t += NT) see(srow[t]);
+            }
 #pragma unroll
             for (int o = 16; o; o >>= 1) {
                 kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
@@ -225,6 +245,32 @@ select_item(int64_t item, const float *__restrict__ S, const int32_t *__restrict
                             const uint32_t u = s_cand[i];
                             if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (uint32_t)(nb - 1)], 1u);
                         }
+                    } else if (!IN_SMEM) {
+                        auto visit = [&](float x) {
+                            const uint32_t u = score_key(x);
+                            if ((u & pmask) == prefix) {
+                                atomicAdd(&hist[(u >> shift) & (uint32_t)(nb - 1)], 1u);
+                                if (build) {
+                                    const uint32_t c = atomicAdd(&s_ncand, 1u);
+                                    if (c < (uint32_t)kSelectCandidates) s_cand[c] = u;
+                                }
+                            }
+                        };
+                        for (int i = threadIdx.x; i < n4; i += NT * kUnroll) {
+                            float4 v[kUnroll];
+#pragma unroll
+                            for (int k = 0; k < kUnroll; ++k)
+                                if (i + k * NT < n4) v[k] = g4[i + k * NT];
+#pragma unroll
+                            for (int k = 0; k < kUnroll; ++k)
+                                if (i + k * NT < n4) {
+                                    visit(v[k].x);
+                                    visit(v[k].y);
+                                    visit(v[k].z);
+                                    visit(v[k].w);
+                                }
+                        }
+                        for (int t = 4 * n4 + threadIdx.x; t < T; t += NT) visit(srow[t]);
                     } else {
                         for (int base = 0; base < T; base += NT * kUnroll) {
                             uint32_t u[kUnroll];
