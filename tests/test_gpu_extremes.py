@@ -78,3 +78,18 @@ def test_many_tiny_heads():
     heads = sorted(set(rng.integers(0, rows * H, size=600).tolist()) | {0, rows * H - 1})
     for mode, window, ratio in (("l2", 0, 0.5), ("cosine", 2, 0.2)):
         _compress_and_check(f"tiny-{mode}-w{window}", K, V, lens, ratio, mode, window, heads=heads)
+
+
+@pytest.mark.parametrize("mode,window,ratio", [("l2", 0, 0.5), ("cosine", 7001, 0.3)])
+def test_long_heads_with_unaligned_score_rows(mode, window, ratio):
+    # t_max = 45001 (above the 40960 scores a select keeps in shared memory):
+    # the select's passes and the compaction read the scores from L2, as
+    # 16-byte vectors where a head's row of scores starts on a 16-byte
+    # boundary (head 0, 4, ...) and one score at a time elsewhere; the
+    # lengths leave tails of 1, 0 and 3 scores past the last full vector
+    w = synthkv.WORKLOADS["phi4-kv-t128k"].scaled("odd", layers=1, batch=3, heads=2, t_max=45001)
+    K, V, _ = synthkv.make_kv(w, seed=53, device=DEV)
+    lens = torch.tensor([45001, 45000, 41003], dtype=torch.int32, device=DEV)
+    _compress_and_check(f"odd-{mode}-w{window}", K, V, lens, ratio, mode, window)
+    del K, V
+    torch.cuda.empty_cache()
