@@ -460,6 +460,9 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms,
+        # value counts token rows (layer x KV head x position); the same per
+        # sequence position, every layer and KV head of it compressed
+        "sequence_tokens_per_s": value / (w.layers * w.heads),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
