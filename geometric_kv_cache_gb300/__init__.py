@@ -49,7 +49,7 @@ EXPORTED = (
     "mkv_inject_stalled_windows", "mkv_window_means", "mkv_num_keep_quota", "mkv_select_quota",
     "mkv_compress_quota", "mkv_oja_workspace_size", "mkv_oja_score", "mkv_compress_oja", "mkv_oja_score_profiled",
     "mkv_compress_inplace", "mkv_set_head_groups", "mkv_set_fused", "mkv_centroid_score",
-    "mkv_inject_stalled_fused", "mkv_set_head_group_ring", "mkv_head_group_plan",
+    "mkv_inject_stalled_fused", "mkv_set_head_group_ring", "mkv_head_group_plan", "mkv_set_oja_pair",
 )
 
 
@@ -105,6 +105,7 @@ def load(build_if_missing: bool = True):
             "mkv_set_head_group_ring": (i32, [i32]),
             "mkv_head_group_plan": (i32, [MkvShape, i32, i32, ctypes.POINTER(i32)]),
             "mkv_set_fused": (i32, [i32, i32]),
+            "mkv_set_oja_pair": (i32, [i32]),
             "mkv_centroid_score": (i32, [vp, MkvShape, i32, i32, vp, vp, vp, sz, vp]),
             "mkv_layer_budgets": (i32, [vp, i32, f64, f64, ctypes.c_int64, vp, vp]),
             "mkv_inject_stalled_windows": (i32, [vp, vp, MkvShape, f64, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
@@ -226,6 +227,13 @@ def mkv_head_group_plan(shape, window: int, mode) -> Optional[dict]:
     if load().mkv_head_group_plan(shape, int(window), _MODES[mode], out) != 0:
         return None
     return {"groups": out[0], "gsize": out[1], "windows_per_unit": out[2], "ring": bool(out[3])}
+
+
+def mkv_set_oja_pair(enable: bool) -> bool:
+    """Run the OjaKV contraction (n_query <= 128) on pairs of CTAs (tcgen05
+    cta_group::2, 256 tokens per MMA) or on one CTA per SM; returns the
+    previous setting."""
+    return bool(load().mkv_set_oja_pair(1 if enable else 0))
 
 
 def mkv_set_fused(scorer_ctas: int, select_ctas: int = 0) -> int:

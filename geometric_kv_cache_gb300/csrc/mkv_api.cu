@@ -725,6 +725,11 @@ int32_t mkv_head_group_plan(mkv_shape shape, int32_t window, mkv_mode mode, int3
     return hp.groups > 0 ? 0 : -1;
 }
 
+int32_t mkv_set_oja_pair(int32_t enable)
+{
+    return oja_set_pair(enable);
+}
+
 int32_t mkv_set_head_groups(int32_t enable)
 {
     return g_head_groups_enabled.exchange(enable ? 1 : 0);

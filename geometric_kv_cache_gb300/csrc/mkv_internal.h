@@ -150,6 +150,9 @@ cudaError_t launch_gather_inplace(const Geometry &g, const int32_t *idx, int32_t
 // contraction writing S[head * t_max + t] for t < T_head.
 size_t oja_operand_bytes(int64_t n_heads, int32_t n_query);
 int oja_stages(int32_t n_query);
+// the CTA-pair contraction: the setting (returns the previous one) and whether it runs for n_query
+int oja_set_pair(int enable);
+bool oja_uses_pair(int32_t n_query);
 cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, const float *U, const int32_t *seq_lens,
                               int32_t n_query, int32_t rank, void *qhl, float *S, uint32_t *status, cudaStream_t st,
                               void *const *events = nullptr);

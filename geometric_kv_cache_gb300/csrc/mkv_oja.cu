@@ -53,6 +53,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "mkv_device.cuh"
@@ -569,6 +570,322 @@ k_oja_scores(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     }
 }
 
+// ------------------------------- 2b: the contraction on pairs of CTAs --
+//
+// k_oja_scores_pair: the same contraction with tcgen05.mma.cta_group::2 on a
+// cluster of two CTAs, one per SM. One MMA covers 256 tokens: the CTA of
+// cluster rank r holds tokens [128 r, 128 r + 128) of the tile (operand A)
+// and operand split r (r = 0 the hi rows, r = 1 the lo rows: operand B, N =
+// 2M) in its shared memory, and receives its 128 tokens x 2M accumulator
+// columns in its own TMEM -- the one-CTA kernel's layout, so the epilogue
+// is the same. Rank 0's MMA thread issues every MMA of the pair: for the
+// same work each SM issues half as many MMAs, and each reads only its half
+// of the operand rows.
+//  * Each CTA's producer loads its own halves with TMA onto its own
+//    barriers. In rank 1 a relay thread waits for each of those copies in
+//    order and arrives on rank 0's peer_full / peer_qfull, so the MMA thread
+//    sees both halves land, and each CTA can still wait out its own copies.
+//  * The MMA thread commits a stage's, an operand's and an accumulator's
+//    completion to the barriers of both CTAs at once (multicast commit).
+//  * Both CTAs' epilogue warps release an accumulator buffer on rank 0's
+//    tempty (rank 1's with remote arrives).
+//  * Both CTAs allocate and free the TMEM together (cta_group::2); the pair
+//    checks that both received the same address before any MMA.
+// Every wait is bounded as in the one-CTA kernel; the pair meets at a
+// cluster barrier after the setup and again before the TMEM is freed.
+__device__ __forceinline__ uint32_t pair_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pair_map(const void *p, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void pair_arrive_remote(uint32_t caddr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pair_ld_u32(uint32_t caddr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void pair_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+// Completion of the MMAs issued so far arrives on the barrier at the same
+// offset in both CTAs of the pair.
+__device__ __forceinline__ void mma_commit_pair(uint64_t *b)
+{
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            saddr(b)),
+        "h"(mask)
+        : "memory");
+}
+
+// ... on this CTA's barrier only.
+__device__ __forceinline__ void mma_commit_pair_local(uint64_t *b)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(b))
+                 : "memory");
+}
+
+// Instruction descriptor of kind::f16 for the pair: M = 256 (128 tokens per
+// CTA), N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16_pair(int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
+constexpr int kPairTok = 2 * kTok;  // tokens of one pair MMA
+
+__global__ void __launch_bounds__(kOjaThreads, 1)
+k_oja_scores_pair(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                  const int32_t *__restrict__ seq_lens, int heads, int t_max, int64_t n_heads, int n_query, int stages,
+                  uint32_t tmem_cols, float scale, float *__restrict__ S, uint32_t *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *kring = smem;                               // stages x 32 KB: this CTA's 128 tokens of each tile
+    uint8_t *qbuf = smem + (size_t)stages * kTileBytes;  // [dims 0-63, 64-127][n_query rows x 128 B]: this CTA's split (room for both)
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], peer_full[kMaxStages], qfull, qempty,
+        peer_qfull, tfull[2], tempty[2], pready[2], drain;
+    __shared__ float part[2][kTok];
+    __shared__ uint32_t tmem_base_sh, s_ok;
+    __shared__ volatile uint32_t abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = pair_rank();
+    const uint32_t q_block = (uint32_t)n_query * 128u;  // bytes of one dims half of this CTA's operand rows
+    const int acc_cols = 2 * n_query;                    // hi then lo columns
+    const int groups = n_query % 64 == 0 ? 2 : 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            bar_init(&full[s], 1);
+            bar_init(&empty[s], 1);
+            bar_init(&peer_full[s], 1);
+        }
+        bar_init(&qfull, 1);
+        bar_init(&qempty, 1);
+        bar_init(&peer_qfull, 1);
+        for (int b = 0; b < 2; ++b) {
+            bar_init(&tfull[b], 1);
+            bar_init(&tempty[b], 2 * 4 * groups);
+            bar_init(&pready[b], 4);
+        }
+        bar_init(&drain, 1);
+        abort_flag = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base_sh)),
+                     "r"(tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    pair_sync();  // both CTAs' barriers and TMEM are set up
+    fence_after();
+    if (threadIdx.x == 0) {
+        // the MMAs write both CTAs' accumulators at rank 0's address
+        const uint32_t other = pair_ld_u32(pair_map(&tmem_base_sh, rank ^ 1u));
+        s_ok = other == tmem_base_sh ? 1u : 0u;
+        if (!s_ok && rank == 0) atomicOr(status, MKV_DEV_INTERNAL);
+    }
+    __syncthreads();
+    const bool ok = s_ok != 0u;  // the same in both CTAs (a symmetric comparison)
+    const uint32_t tmem = tmem_base_sh;
+    // the pair's tiles of 256 tokens
+    const int tph = (t_max + kPairTok - 1) / kPairTok;
+    const int64_t total = n_heads * tph;
+    const int64_t npairs = gridDim.x / 2, pair = blockIdx.x / 2;
+    const int64_t first = total * pair / npairs, last = total * (pair + 1) / npairs;
+
+    if (ok && warp == 0) {
+        if (lane == 0) {
+            // ------------------------------ TMA producer (this CTA's halves) --
+            uint32_t seq = 0, qseq = 0;
+            uint32_t last_parity[kMaxStages];
+            int64_t cur = -1;
+            for (int64_t tile = first; tile < last; ++tile) {
+                const int64_t head = tile / tph;
+                const int t0 = (int)(tile - head * tph) * kPairTok;
+                if (t0 >= head_len(seq_lens, head, heads, t_max, status, false)) continue;
+                if (head != cur) {
+                    if (qseq > 0 && !bar_wait(&qempty, (qseq - 1) & 1u, status, &abort_flag, true)) break;
+                    bar_expect(&qfull, 2u * q_block);
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_2d(qbuf + half * q_block, &tmap_q, half * 64, (int)((head * 2 + rank) * n_query),
+                                    &qfull);
+                    ++qseq;
+                    cur = head;
+                }
+                const int s = (int)(seq % (uint32_t)stages);
+                if (seq >= (uint32_t)stages &&
+                    !bar_wait(&empty[s], ((seq / stages) - 1) & 1u, status, &abort_flag, true))
+                    break;
+                bar_expect(&full[s], (uint32_t)kTileBytes);
+                const int row = (int)(head * t_max + t0 + (int)rank * kTok);
+                tma_load_2d(kring + (size_t)s * kTileBytes, &tmap_k, 0, row, &full[s]);
+                tma_load_2d(kring + (size_t)s * kTileBytes + kHalfBytes, &tmap_k, 64, row, &full[s]);
+                last_parity[s] = (seq / stages) & 1u;
+                ++seq;
+            }
+            // every copy issued lands before the CTA may exit
+            const uint32_t issued = seq < (uint32_t)stages ? seq : (uint32_t)stages;
+            for (uint32_t s = 0; s < issued; ++s) bar_wait(&full[s], last_parity[s], status, &abort_flag, false);
+            if (qseq > 0) bar_wait(&qfull, (qseq - 1) & 1u, status, &abort_flag, false);
+        }
+    } else if (ok && warp == 1) {
+        if (lane == 0 && rank == 1) {
+            // ----------------------------------- relay (rank 1): copies landed --
+            const uint32_t pf0 = pair_map(&peer_full[0], 0), pq = pair_map(&peer_qfull, 0);
+            uint32_t seq = 0, qseq = 0;
+            int64_t cur = -1;
+            for (int64_t tile = first; tile < last; ++tile) {
+                const int64_t head = tile / tph;
+                const int t0 = (int)(tile - head * tph) * kPairTok;
+                if (t0 >= head_len(seq_lens, head, heads, t_max, status, false)) continue;
+                if (head != cur) {
+                    if (!bar_wait(&qfull, qseq & 1u, status, &abort_flag, true)) break;
+                    pair_arrive_remote(pq);
+                    ++qseq;
+                    cur = head;
+                }
+                const int s = (int)(seq % (uint32_t)stages);
+                if (!bar_wait(&full[s], (seq / stages) & 1u, status, &abort_flag, true)) break;
+                pair_arrive_remote(pf0 + (uint32_t)(s * sizeof(uint64_t)));
+                ++seq;
+            }
+        } else if (lane == 0 && rank == 0) {
+            // ---------------------------------------------- MMA issuer (pair) --
+            const uint32_t idesc = idesc_bf16_pair(2 * n_query);
+            const uint64_t a_desc0 = sdesc(saddr(kring)), b_desc0 = sdesc(saddr(qbuf));
+            uint64_t a_step[8], b_step[8];
+#pragma unroll
+            for (int step = 0; step < 8; ++step) {
+                const int half = step >> 2, kk = step & 3;
+                a_step[step] = (uint64_t)((half * kHalfBytes + kk * 32) >> 4);
+                b_step[step] = (uint64_t)((half * q_block + kk * 32) >> 4);
+            }
+            uint32_t seq = 0, tcount = 0, qseq = 0;
+            int64_t cur = -1;
+            for (int64_t tile = first; tile < last; ++tile) {
+                const int64_t head = tile / tph;
+                const int t0 = (int)(tile - head * tph) * kPairTok;
+                if (t0 >= head_len(seq_lens, head, heads, t_max, status, false)) continue;
+                const uint32_t b = tcount & 1u, use = tcount >> 1;
+                if (use > 0 && !bar_wait(&tempty[b], (use - 1) & 1u, status, &abort_flag, true)) break;
+                fence_after();
+                if (head != cur) {
+                    if (qseq > 0) mma_commit_pair(&qempty);  // the previous head's operand rows are free in both CTAs
+                    if (!bar_wait(&qfull, qseq & 1u, status, &abort_flag, true) ||
+                        !bar_wait(&peer_qfull, qseq & 1u, status, &abort_flag, true))
+                        break;
+                    ++qseq;
+                    cur = head;
+                }
+                const int s = (int)(seq % (uint32_t)stages);
+                if (!bar_wait(&full[s], (seq / stages) & 1u, status, &abort_flag, true) ||
+                    !bar_wait(&peer_full[s], (seq / stages) & 1u, status, &abort_flag, true))
+                    break;
+                fence_after();
+                const uint32_t d_tmem = tmem + b * (uint32_t)acc_cols;
+                const uint64_t a0 = a_desc0 + (uint64_t)((s * kTileBytes) >> 4);
+#pragma unroll
+                for (int step = 0; step < 8; ++step)
+                    mma_bf16_pair(d_tmem, a0 + a_step[step], b_desc0 + b_step[step], idesc, step ? 1u : 0u);
+                mma_commit_pair(&empty[s]);
+                mma_commit_pair(&tfull[b]);
+                ++seq;
+                ++tcount;
+            }
+            // every MMA issued completes before the TMEM is freed
+            mma_commit_pair_local(&drain);
+            bar_wait(&drain, 0, status, &abort_flag, false);
+        }
+    } else if (ok) {
+        // ----------------------------------------------------- epilogue --
+        // as in the one-CTA kernel; rank 1's warps release a buffer on rank
+        // 0's tempty
+        const int grp = (warp - 2) >> 2;
+        const uint32_t wq = (uint32_t)(warp & 3);  // TMEM lanes 32*wq .. 32*wq+31
+        const int cw = n_query / groups;
+        const uint32_t te0 = pair_map(&tempty[0], 0);
+        auto release = [&](uint32_t b) {
+            if (rank == 0)
+                bar_arrive(&tempty[b]);
+            else
+                pair_arrive_remote(te0 + b * (uint32_t)sizeof(uint64_t));
+        };
+        uint32_t tcount = 0;
+        if (grp < groups) {
+            for (int64_t tile = first; tile < last; ++tile) {
+                const int64_t head = tile / tph;
+                const int t0 = (int)(tile - head * tph) * kPairTok;
+                const int T = head_len(seq_lens, head, heads, t_max, status, false);
+                if (t0 >= T) continue;
+                const uint32_t b = tcount & 1u, use = tcount >> 1;
+                if (!bar_wait(&tfull[b], use & 1u, status, &abort_flag, true)) break;
+                fence_after();
+                const uint32_t taddr = tmem + ((wq * 32u) << 16) + b * (uint32_t)acc_cols;
+                float acc = tmem_abs_sum(taddr, (uint32_t)n_query, true, grp * cw, cw);
+                const int row = (int)wq * 32 + lane;
+                if (grp == 1) {
+                    part[b][row] = acc;
+                    fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        bar_arrive(&pready[b]);
+                        release(b);
+                    }
+                } else {
+                    if (groups == 2) {
+                        if (!bar_wait(&pready[b], use & 1u, status, &abort_flag, true)) break;
+                        acc += part[b][row];
+                    }
+                    fence_before();
+                    __syncwarp();
+                    if (lane == 0) release(b);
+                    const int t = t0 + (int)rank * kTok + row;
+                    if (t < T) S[(size_t)head * t_max + t] = acc * scale;
+                }
+                ++tcount;
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    pair_sync();  // every MMA and every TMEM read of both CTAs is done
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
+    }
+}
+
 // --------------------------------------------------------------- host side --
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -616,6 +933,25 @@ size_t oja_operand_bytes(int64_t n_heads, int32_t n_query)
     return (size_t)n_heads * 2 * (size_t)n_query * kRowBytes;
 }
 
+// The CTA-pair contraction (k_oja_scores_pair) for n_query <= 128 (hi and
+// lo stacked in one MMA): 0 never, 1 wherever it applies.
+std::atomic<int> g_oja_pair{0};
+
+int oja_set_pair(int enable) { return g_oja_pair.exchange(enable ? 1 : 0); }
+
+bool oja_uses_pair(int32_t n_query) { return g_oja_pair.load(std::memory_order_relaxed) != 0 && 2 * n_query <= 256; }
+
+// stages of the pair kernel: each CTA loads one split (hi or lo) of the
+// operand rows; the operand buffer keeps the one-CTA kernel's size (both
+// splits), so the MMA's operand reads stay inside the CTA's shared memory
+// whatever rows it addresses
+int oja_pair_stages(int32_t n_query)
+{
+    const int left = kSmemBudget - 1024 - 2048 - 4 * n_query * 128;
+    const int s = left / kTileBytes;
+    return s > kMaxStages ? kMaxStages : s;
+}
+
 int oja_stages(int32_t n_query)
 {
     // alignment slack, up to 2 KB of static shared memory, the operand rows
@@ -651,6 +987,45 @@ cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, c
     if (!make_map(&mk, K, (uint64_t)g.n_heads * g.t_max, kTok) ||
         !make_map(&mq, qhl, (uint64_t)g.n_heads * 2 * n_query, (uint32_t)n_query))
         return cudaErrorInvalidValue;
+    const float scale = (float)(1.0 / ((double)n_query * 11.313708498984760390));  // 1 / (M sqrt(128))
+    const int sms = sms_of_current_device();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    if (oja_uses_pair(n_query)) {
+        // pairs of CTAs (a cluster of two, one CTA per SM), 256 tokens per MMA
+        const int pstages = oja_pair_stages(n_query);
+        if (pstages < 2) return cudaErrorInvalidValue;
+        const size_t psmem2 = 1024 + (size_t)pstages * kTileBytes + 4 * (size_t)n_query * 128;
+        const void *fn = reinterpret_cast<const void *>(k_oja_scores_pair);
+        if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem2)) != cudaSuccess)
+            return e;
+        uint32_t pcols = 32;
+        while (pcols < (uint32_t)(2 * 2 * n_query)) pcols *= 2;  // two accumulator buffers of 2M columns
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kOjaThreads);
+        cfg.dynamicSmemBytes = psmem2;
+        cfg.stream = st;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2);
+        int max_pairs = 0;
+        if ((e = cudaOccupancyMaxActiveClusters(&max_pairs, fn, &cfg)) != cudaSuccess) return e;
+        if (max_pairs < 1) return cudaErrorInvalidConfiguration;
+        const int64_t ptiles = g.n_heads * ((g.t_max + 2 * kTok - 1) / (2 * kTok));
+        const int pairs = (int)(ptiles < max_pairs ? ptiles : max_pairs);
+        cfg.gridDim = dim3((unsigned)(2 * pairs));
+        const int32_t *sl = seq_lens;
+        int heads = g.heads, t_max = g.t_max, nq = n_query, stg = pstages;
+        int64_t nh = g.n_heads;
+        void *args[] = {&mk, &mq, &sl, &heads, &t_max, &nh, &nq, &stg, &pcols, const_cast<float *>(&scale), &S,
+                        &status};
+        if ((e = cudaLaunchKernelExC(&cfg, fn, args)) != cudaSuccess) return e;
+        return mark(2);
+    }
     const int stages = oja_stages(n_query);
     if (stages < 2) return cudaErrorInvalidValue;
     const size_t smem = 1024 + (size_t)stages * kTileBytes + 4 * (size_t)n_query * 128;
@@ -664,10 +1039,7 @@ cudaError_t launch_oja_scores(const Geometry &g, const void *K, const void *Q, c
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * acc_cols)) cols *= 2;
     const int64_t tiles = g.n_heads * ((g.t_max + kTok - 1) / kTok);
-    const int sms = sms_of_current_device();
-    if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = (int)(tiles < sms ? tiles : sms);
-    const float scale = (float)(1.0 / ((double)n_query * 11.313708498984760390));  // 1 / (M sqrt(128))
     k_oja_scores<<<grid, kOjaThreads, smem, st>>>(mk, mq, seq_lens, g.heads, g.t_max, g.n_heads, n_query, stages, cols,
                                                   scale, S, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -261,6 +261,15 @@ size_t mkv_oja_workspace_size(mkv_shape shape, int32_t n_query);
 mkv_status mkv_oja_score(const void *K, const void *Q, const float *U, mkv_shape shape, int32_t n_query,
                          int32_t rank, float *S, void *workspace, size_t workspace_bytes, mkv_stream_t stream);
 
+/* Choose, process-wide, how the OjaKV contraction runs for n_query <= 128;
+ * returns the previous setting. 0 (the default): one CTA per SM, 128 tokens
+ * per tensor-core MMA. 1: pairs of CTAs on two SMs (a thread-block cluster
+ * of two, tcgen05.mma with cta_group::2), 256 tokens per MMA, each SM
+ * holding half of the projected query rows (the hi split on one, the lo
+ * split on the other). Same scores either way; larger n_query always runs on
+ * one CTA per SM. */
+int32_t mkv_set_oja_pair(int32_t enable);
+
 /* mkv_oja_score recording caller-created CUDA events (cudaEvent_t as void*)
  * on `stream`: events[0] before the query projection kernel, events[1]
  * between it and the tensor-core contraction, events[2] after; n_events >= 3.

@@ -202,3 +202,51 @@ def test_oja_full_size_llama():
     assert torch.all(torch.isfinite(S)) and torch.all(S >= 0)
     del K, V, Q, U, S, idx, kept
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n_query", [16, 48, 64, 128])
+def test_pair_kernel_gives_the_one_cta_kernels_bits(n_query):
+    """The contraction on pairs of CTAs (tcgen05 cta_group::2, 256 tokens per
+    MMA, the hi and lo operand rows split over the two SMs) writes exactly the
+    scores of the one-CTA kernel: ragged heads, a head shorter than one pair
+    tile, rank 0 and a non-orthonormal-sized rank."""
+    for rows, heads, t_max, t_min, rank, seed in ((1, 1, 200, None, 64, 61), (3, 2, 3001, 1, 64, 62),
+                                                  (2, 3, 5000, 600, 0, 63)):
+        K, V, lens, Q, U = _case(rows=rows, heads=heads, t_max=t_max, n_query=n_query, rank=rank, seed=seed,
+                                 t_min=t_min)
+        B, H, T, D = K.shape
+        ws = mkv.oja_workspace_for(K, n_query, lens)
+        out = []
+        for pair in (False, True):
+            prev = mkv.mkv_set_oja_pair(pair)
+            try:
+                S = torch.full((B, H, T), float("nan"), device=DEV)
+                mkv.mkv_oja_score(K, Q, U, S, ws, lens)
+                assert mkv.mkv_device_status(ws) == 0
+            finally:
+                mkv.mkv_set_oja_pair(prev)
+            out.append(S)
+        assert torch.equal(out[0].nan_to_num(-1.0), out[1].nan_to_num(-1.0))
+        lens_c = lens.cpu().numpy()
+        for r in range(B):  # every score below T_b written, none past it
+            assert not torch.isnan(out[1][r, :, :int(lens_c[r])]).any()
+            assert torch.isnan(out[1][r, :, int(lens_c[r]):]).all()
+
+
+def test_pair_setting_keeps_large_windows_on_one_cta():
+    """n_query above 128 (hi and lo in separate MMAs) always runs the
+    one-CTA kernel; the pair setting changes nothing there."""
+    K, V, lens, Q, U = _case(rows=2, heads=2, t_max=1500, n_query=192, rank=32, seed=64)
+    B, H, T, D = K.shape
+    ws = mkv.oja_workspace_for(K, 192, lens)
+    out = []
+    for pair in (False, True):
+        prev = mkv.mkv_set_oja_pair(pair)
+        try:
+            S = torch.zeros((B, H, T), device=DEV)
+            mkv.mkv_oja_score(K, Q, U, S, ws, lens)
+            assert mkv.mkv_device_status(ws) == 0
+        finally:
+            mkv.mkv_set_oja_pair(prev)
+        out.append(S)
+    assert torch.equal(out[0], out[1])
