@@ -48,9 +48,10 @@ std::atomic<int> g_fused_selectors{32};
 
 // Scorer and selector budgets of the fused kernel for this shape; scorers 0
 // when it is not to run. Automatic: bf16 caches, head dim 128, global
-// centroids and 12288 < t_max (<= 20480, the kernel's own limit), where it
-// was measured faster than the separate kernels on GB300 (256 heads x 16K:
-// 0.620 against 0.649 ms; 64 x 16K: 0.187 against 0.204) -- not at 8K tokens
+// centroids, 12288 < t_max (<= 20480, the kernel's own limit) and at least
+// 64 heads, where it was measured faster than the separate kernels on GB300
+// (256 heads x 16K: 0.620 against 0.649 ms; 64 x 16K: 0.187 against 0.204)
+// -- not with fewer heads (32 x 16K: 0.119 against 0.113), at 8K tokens
 // (512 x 8K: 0.687 against 0.648) nor for E4M3 caches (256 x 16K: 0.558
 // against 0.42), whose scoring is decode-bound. There it uses 3/4 of the
 // resident grid for scoring and max(16, heads / 16) selector CTAs (fewer
@@ -65,7 +66,7 @@ FusedBudget fused_budget(const Geometry &g)
     if (sc > 0) {
         b.scorers = sc;
         b.selectors = g_fused_selectors.load(std::memory_order_relaxed);
-    } else if (sc < 0 && g.es == 2 && g.d == kHeadDim && g.pg.nwin_max == 1 && g.t_max > 12288) {
+    } else if (sc < 0 && g.es == 2 && g.d == kHeadDim && g.pg.nwin_max == 1 && g.t_max > 12288 && g.n_heads >= 64) {
         b.scorers = -1;  // 3/4 of the resident grid (fused_plan)
         b.selectors = (int)std::max<int64_t>(16, (g.n_heads + 15) / 16);
     }

@@ -345,9 +345,10 @@ int32_t mkv_set_head_group_ring(int32_t enable);
 
 /* Choose, process-wide, when mkv_compress runs the fused whole-path kernel;
  * returns the previous scorer setting. scorer_ctas < 0 (the default): on its
- * own rule -- bf16 caches, head dim 128, global centroids and 12288 < t_max
- * <= 20480, the shapes where it was measured faster than the separate
- * kernels on GB300 -- with 3/4 of the resident grid scoring and max(16,
+ * own rule -- bf16 caches, head dim 128, global centroids, 12288 < t_max
+ * <= 20480 and at least 64 heads (batch * heads), the shapes where it was
+ * measured faster than the separate kernels on GB300 -- with 3/4 of the
+ * resident grid scoring and max(16,
  * heads / 16) selector CTAs. scorer_ctas > 0: wherever it applies, with that
  * scorer budget and select_ctas selector CTAs (select_ctas <= 0 keeps the
  * current value, 32 at start). scorer_ctas == 0: never. It applies to global

@@ -1,7 +1,8 @@
 """GPU parity of the fused whole-path kernel: one cooperative launch whose
 scorer head groups, selector CTAs and gatherer warps hand work over through
 bounded waits. mkv_compress takes it by default under its own shape rule
-(bf16, head dim 128, global centroids, 12288 < t_max <= 20480);
+(bf16, head dim 128, global centroids, 12288 < t_max <= 20480, at least 64
+heads);
 mkv_set_fused forces scorer/selector budgets wherever it applies, or turns
 it off (this module turns it off and forces it per test, then restores the
 previous setting). Its outputs must be the separate kernels' bits
@@ -155,7 +156,8 @@ def test_fused_small_case_against_the_oracle():
 
 def test_fused_kernel_own_rule():
     """The default setting runs the fused kernel where it was measured faster:
-    bf16, head dim 128, global centroids, 12288 < t_max <= 20480."""
+    bf16, head dim 128, global centroids, 12288 < t_max <= 20480, at least 64
+    heads."""
     prev = mkv.mkv_set_fused(-1)
     try:
         q = mkv.mkv_compress_single_pass
@@ -168,9 +170,11 @@ def test_fused_kernel_own_rule():
         assert q(mkv.MkvShape(8, 8, 20481, 128, 0, None), 0, "l2") != 3          # above the kernel's limit
         assert q(mkv.MkvShape(8, 8, 16384, 64, 0, None), 0, "l2") != 3           # other head dims
         assert q(mkv.MkvShape(32, 8, 16384, 128, 1, None), 0, "l2") != 3         # E4M3 caches
+        assert q(mkv.MkvShape(4, 8, 16384, 128, 0, None), 0, "l2") != 3          # 32 heads
+        assert q(mkv.MkvShape(8, 8, 16384, 128, 0, None), 0, "l2") == 3          # 64 heads
     finally:
         mkv.mkv_set_fused(prev)
-    K, V, lens = _cache("fused-rule", 7, layers=2)
+    K, V, lens = _cache("fused-rule", 7, layers=8)
     prev = mkv.mkv_set_fused(-1)
     try:
         assert mkv.mkv_compress_single_pass(mkv.shape_of(K), 0, "l2") == 3
