@@ -88,16 +88,47 @@ k_chunk_offsets(const float *__restrict__ S, const mkv_cut *__restrict__ cuts,
 // ------------------------------------------------------- a4: compaction --
 
 // Item = (head, chunk of 4096 tokens). Each thread classifies 16 consecutive
-// tokens against the cut; two CTA scans give each kept token its tie rank
-// and its output slot; each thread then writes its kept token ids, in
-// ascending order, to idx[head * idx_stride + slot].
+// tokens against the cut; a CTA scan gives each kept token its output slot
+// (a first scan its tie rank, in the chunks that hold tokens equal to the
+// cut); the kept token ids go, in ascending order, to shared memory and from
+// there, coalesced, to idx[head * idx_stride + slot]. The next item's scores
+// are loaded while the current item's scans and stores run.
 __global__ void __launch_bounds__(kStreamThreads)
 k_compact(const float *__restrict__ S, const mkv_cut *__restrict__ cuts, const int2 *__restrict__ chunk_info,
           const int32_t *__restrict__ seq_lens, int heads, int t_max, int nch_max, int keep_stride, int64_t n_items,
           int32_t *__restrict__ idx, int idx_stride, uint32_t *status)
 {
     __shared__ uint32_t s_warp[kStreamThreads / 32];
+    __shared__ int32_t s_idx[kCompactChunk];
+    // the thread's 16 scores of `item` (tokens past the head's end: not read)
+    auto load16 = [&](int64_t item, float v[16]) {
+        const int64_t head = item / nch_max;
+        const int c = (int)(item - head * nch_max);
+        const int T = head_len(seq_lens, head, heads, t_max, status, false);
+        const float *srow = S + (size_t)head * t_max;
+        const int t0 = c * kCompactChunk + threadIdx.x * 16;
+        if (t0 + 16 <= T && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
+            const float4 *s4 = reinterpret_cast<const float4 *>(srow + t0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 x = s4[i];
+                v[4 * i] = x.x;
+                v[4 * i + 1] = x.y;
+                v[4 * i + 2] = x.z;
+                v[4 * i + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = t0 + j < T ? srow[t0 + j] : 0.f;
+        }
+    };
+    float nxt[16];
+    if ((int64_t)blockIdx.x < n_items) load16(blockIdx.x, nxt);
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = nxt[j];
+        if (item + gridDim.x < n_items) load16(item + gridDim.x, nxt);
         const int64_t head = item / nch_max;
         const int c = (int)(item - head * nch_max);
         const int T = head_len(seq_lens, head, heads, t_max, status, false);
@@ -112,48 +143,35 @@ k_compact(const float *__restrict__ S, const mkv_cut *__restrict__ cuts, const i
             if (threadIdx.x == 0 && info.x != -1) atomicOr(status, MKV_DEV_INTERNAL);
             continue;
         }
-        const float *srow = S + (size_t)head * t_max;
         const int t0 = a + threadIdx.x * 16;
         uint32_t gtm = 0, eqm = 0;
-        auto classify = [&](float v, int j) {
-            const uint32_t u = score_key(v);
-            gtm |= (uint32_t)(u > cut.key) << j;
-            eqm |= (uint32_t)(u == cut.key) << j;
-        };
-        if (t0 + 16 <= T && (reinterpret_cast<uintptr_t>(srow + t0) & 15) == 0) {
-            // the thread's 16 scores as four 16-byte loads
-            const float4 *s4 = reinterpret_cast<const float4 *>(srow + t0);
-            float4 v[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = s4[i];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                classify(v[i].x, 4 * i);
-                classify(v[i].y, 4 * i + 1);
-                classify(v[i].z, 4 * i + 2);
-                classify(v[i].w, 4 * i + 3);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = t0 + j;
-                if (t < T) classify(srow[t], j);
+        for (int j = 0; j < 16; ++j) {
+            if (t0 + j < T) {
+                const uint32_t u = score_key(v[j]);
+                gtm |= (uint32_t)(u > cut.key) << j;
+                eqm |= (uint32_t)(u == cut.key) << j;
             }
         }
-        uint32_t rank = (uint32_t)info.y + block_exclusive_scan<kStreamThreads>(__popc(eqm), s_warp, nullptr);
         uint32_t keepm = gtm;
-        for (uint32_t m = eqm; m; m &= m - 1) {
-            if (rank < (uint32_t)cut.ties) keepm |= m & (~m + 1);
-            ++rank;
+        if (__syncthreads_or(eqm != 0u)) {
+            uint32_t rank = (uint32_t)info.y + block_exclusive_scan<kStreamThreads>(__popc(eqm), s_warp, nullptr);
+            for (uint32_t m = eqm; m; m &= m - 1) {
+                if (rank < (uint32_t)cut.ties) keepm |= m & (~m + 1);
+                ++rank;
+            }
         }
-        const uint32_t kb = block_exclusive_scan<kStreamThreads>(__popc(keepm), s_warp, nullptr);
+        uint32_t nk = 0;
+        uint32_t r = block_exclusive_scan<kStreamThreads>(__popc(keepm), s_warp, &nk);
+        for (uint32_t m = keepm; m; m &= m - 1, ++r) s_idx[r] = t0 + __ffs(m) - 1;
+        __syncthreads();
         int32_t *idx_head = idx + head * idx_stride;
-        uint32_t r = kb;
-        for (uint32_t m = keepm; m; m &= m - 1, ++r) {
-            const int64_t slot = (int64_t)info.x + r;
-            if (slot >= 0 && slot < keep_stride) idx_head[slot] = t0 + __ffs(m) - 1;
+        for (uint32_t i = threadIdx.x; i < nk; i += kStreamThreads) {
+            const int64_t slot = (int64_t)info.x + i;
+            if (slot < keep_stride) idx_head[slot] = s_idx[i];
             else atomicOr(status, MKV_DEV_INTERNAL);
         }
+        __syncthreads();  // s_idx is rewritten by the next item
     }
 }
 
