@@ -238,6 +238,47 @@ def test_selection_alone_on_tied_scores_matches_the_oracle():
                 assert np.array_equal(idx.cpu().numpy().reshape(6, -1)[h, :ks], want), (levels, tie, ratio, h)
 
 
+def test_all_tied_long_heads_keep_the_lowest_indices():
+    # 45000 tokens: the select passes over the scores in L2 (above 40960) and
+    # the compaction's every chunk holds only tokens equal to the cut
+    K = torch.ones(1, 2, 45000, 128, dtype=torch.bfloat16, device=DEV)
+    K[0, 1] = 0
+    V = torch.randn(1, 2, 45000, 128, device=DEV).to(torch.bfloat16)
+    for mode in ("l2", "cosine"):
+        for ratio in (0.3, 0.5):
+            Ko, Vo, idx, kept, st = _run_fused(K, V, ratio, mode, 0)
+            n = mkv.mkv_num_keep(45000, ratio)
+            assert st == 0
+            assert torch.all(kept == n)
+            assert torch.equal(idx[..., :n].cpu(), torch.arange(n, dtype=torch.int32).expand(1, 2, n))
+            assert torch.equal(Vo[..., :n, :], V[..., :n, :])
+
+
+def test_selection_on_tied_scores_of_long_heads_matches_the_oracle():
+    # heads above 40960 tokens (the select's passes read L2; the step-wise
+    # compaction counts the chunks itself) with heavy ties at the cut
+    T = 45003  # not a multiple of 4: unaligned score rows after the first head
+    for levels, tie in ((1, 0.0), (7, 0.0), (0, 0.3)):
+        S = synthkv.random_scores(4, T, seed=levels + 30, tie_fraction=tie, levels=levels, device=DEV)
+        S = S.reshape(2, 2, T).contiguous()
+        K = torch.empty(2, 2, T, 128, dtype=torch.bfloat16, device="meta")
+        shape = mkv.shape_of(K)
+        Sc = S.cpu().numpy().reshape(4, T)
+        for ratio in (0.13, 0.5, 0.77):
+            ks = mkv.mkv_num_keep(T, ratio)
+            cut = torch.zeros(4, 2, dtype=torch.int32, device=DEV)
+            idx = torch.full((2, 2, ks), -7, dtype=torch.int32, device=DEV)
+            kept = torch.zeros(2, 2, dtype=torch.int32, device=DEV)
+            ws = torch.zeros(mkv.mkv_workspace_size(shape, 0), dtype=torch.uint8, device=DEV)
+            mkv.mkv_select_topk(S, shape, ratio, cut, ws)
+            mkv.mkv_compact(S, cut, None, None, shape, ratio, ks, idx, kept, None, None, ws)
+            assert mkv.mkv_device_status(ws) == 0
+            for h in range(4):
+                want = oracle.select(Sc[h].astype(np.float64), ks)
+                assert int(kept.reshape(-1)[h]) == ks
+                assert np.array_equal(idx.cpu().numpy().reshape(4, -1)[h, :ks], want), (levels, tie, ratio, h)
+
+
 def test_per_head_keep_counts_and_wider_stride():
     g = torch.Generator(device=DEV).manual_seed(14)
     K = torch.randn(2, 3, 3000, 128, generator=g, device=DEV).to(torch.bfloat16)
