@@ -40,6 +40,8 @@ def test_committed_record_matches_the_gather_sources():
     rec = os.path.join(ROOT, "profiles", "traffic.json")
     got = bench.load_traffic(rec, "llama3.1-8b-kv-t16k", 0, "bf16", ("l2", 0, 0.5))
     assert got is not None and got.get("gather", 0) > 0
+    # the Llama workload's default step is the fused kernel: its record must match its sources too
+    assert got.get("fused_path", 0) > 0
     # the default bench line (the Phi-4 workload's windowed run) has a record too
     import synthkv
     w, mode, window, ratio = bench.workload_run(synthkv.BENCH_WORKLOAD)
